@@ -1,0 +1,338 @@
+"""Benchmark of the trellis MoE hot path on GB300.
+
+Workload: one full MoE block of a Qwen3.6-35B-A3B-style Escha-W2 layer at
+decode batch 1 (hidden 2048, 256 experts, top-8, gate_up 1024x2048 at K=3,
+down 2048x512 at K=2, int8 w8a16 shared expert), seeded synthetic weights and
+activations (x ~ N(0,1) in fp16; a fresh token every step, so the routed
+experts change). One step = one MoE block forward of one token: router
+(logits, top-8, softmax), input Hadamard transforms, fused trellis decode
+GEMVs for gate_up and down, output transforms, SwiGLU, the int8 shared expert
+and the combine, all in the library's kernels behind the C ABI, replayed from
+a CUDA graph.
+
+L2: the 129 MB L2 is flushed (a 512 MB buffer is written) before every timed
+step, outside the step's CUDA events, so every step reads its weights from
+HBM.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+os.environ.setdefault("OMP_NUM_THREADS", "1")
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+os.environ.setdefault("MKL_NUM_THREADS", "1")
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from escha_synth import gen  # noqa: E402
+
+METRIC = "MoE-layer tokens/s (decode batch 1), packed-expert HBM GB/s as a fraction of peak"
+UNIT = "tokens/s"
+WORKLOAD = ("Qwen3.6-35B-A3B-style Escha-W2 MoE block, decode batch 1: hidden 2048, 256 experts, top-8, "
+            "gate_up 1024x2048 K=3, down 2048x512 K=2, int8 w8a16 shared expert 1024x2048/2048x512")
+LAYER_SEED = 1002
+X_SEED = 2002
+HIDDEN, INTER, E, TOPK = 2048, 512, 256, 8
+GU_CODE_BYTES = HIDDEN * 2 * INTER * 3 // 8  # per expert: 786,432
+DN_CODE_BYTES = INTER * HIDDEN * 2 // 8  # per expert: 262,144
+FLUSH_BYTES = 512 << 20
+KERNELS_PER_STEP = 7  # router logits, top-k, gate_up GEMV, down GEMV, shared gate_up, shared down, combine
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed loops run."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[4:]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [r for r in rows if r[2] > 200.0] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3][1:5]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(loaded), "power_w_max": max(r[2] for r in rows)}
+
+
+def cpu_baseline(seconds: float = 15.0, max_tokens: int = 8):
+    """The CPU oracle as it stands, on the host cores, over a bounded sample
+    of the same workload (whole tokens of the MoE block at batch 1)."""
+    from oracle import escha_oracle as o
+
+    d = gen.moe_layer(LAYER_SEED)
+    layer = o.MoeLayer(**d)
+    xs = gen.fp16_normal(gen.rng(X_SEED + 777), (max_tokens, HIDDEN))
+    t0 = time.perf_counter()
+    n = 0
+    while n < max_tokens:
+        o.moe_block(layer, xs[n:n + 1], k=TOPK)
+        n += 1
+        if time.perf_counter() - t0 > seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} tokens of the batch-1 MoE block through the numpy float64 oracle, one thread, "
+                      f"{dt:.1f} s"}
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    from oracle import escha_oracle as o
+
+    budget = 150.0
+    d = gen.moe_layer(LAYER_SEED)
+    layer = o.MoeLayer(**d)
+    n_total = args.warmup + args.steps
+    xs = gen.fp16_normal(gen.rng(X_SEED), (n_total, HIDDEN))
+    t_begin = time.perf_counter()
+    for i in range(min(args.warmup, 1)):
+        o.moe_block(layer, xs[i:i + 1], k=TOPK)
+    times = []
+    for i in range(args.steps):
+        t0 = time.perf_counter()
+        o.moe_block(layer, xs[args.warmup + i:args.warmup + i + 1], k=TOPK)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_begin > budget:
+            break
+    ms = 1e3 * sum(times) / len(times)
+    value = 1e3 / ms
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+            "steps": len(times), "warmup": min(args.warmup, 1), "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "batch": 1, "l2": "n/a (CPU)"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"{len(times)} of {args.steps} requested steps (one token each, "
+                                       f"capped at {budget:.0f} s) through the numpy float64 oracle"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, ws, rank, local):
+    import torch
+
+    from bit_trellis_quantized_gb300 import native
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+        torch.cuda.synchronize()
+
+    d = gen.moe_layer(LAYER_SEED)
+    block = native.MoeBlock(d, device=dev, topk=TOPK)
+    n_total = args.warmup + args.steps
+    xs_host = torch.from_numpy(gen.fp16_normal(gen.rng(X_SEED + 100 * rank), (n_total, HIDDEN))).pin_memory()
+    xs = xs_host.to(dev)
+    x_buf = torch.empty((1, HIDDEN), dtype=torch.float16, device=dev)
+    out_buf = torch.empty((1, HIDDEN), dtype=torch.float32, device=dev)
+    ids_buf = torch.empty((1, TOPK), dtype=torch.int32, device=dev)
+    w_buf = torch.empty((1, TOPK), dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        x_buf.copy_(xs[0:1])
+        block(x_buf, out=out_buf, ids=ids_buf, w=w_buf)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            block(x_buf, out=out_buf, ids=ids_buf, w=w_buf)
+    torch.cuda.synchronize()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_total)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n_total)]
+    ids_seen = []
+    with ClockSampler(local) as clk:
+        # device-resident inputs: x already in HBM when the step's events start
+        with torch.cuda.stream(stream):
+            barrier()
+            for i in range(n_total):
+                x_buf.copy_(xs[i:i + 1])
+                flush.zero_()
+                starts[i].record(stream)
+                graph.replay()
+                ends[i].record(stream)
+                if i < 16:
+                    ids_seen.append(ids_buf.clone())
+            barrier()
+        step_ms = [starts[i].elapsed_time(ends[i]) for i in range(args.warmup, n_total)]
+
+        # end to end through the public API: pinned host x in, out back to host
+        out_host = torch.empty((n_total, HIDDEN), dtype=torch.float32).pin_memory()
+        e_s = [torch.cuda.Event(enable_timing=True) for _ in range(n_total)]
+        e_e = [torch.cuda.Event(enable_timing=True) for _ in range(n_total)]
+        with torch.cuda.stream(stream):
+            barrier()
+            for i in range(n_total):
+                flush.zero_()
+                e_s[i].record(stream)
+                x_buf.copy_(xs_host[i:i + 1], non_blocking=True)
+                graph.replay()
+                out_host[i:i + 1].copy_(out_buf, non_blocking=True)
+                e_e[i].record(stream)
+            barrier()
+        e2e_ms = [e_s[i].elapsed_time(e_e[i]) for i in range(args.warmup, n_total)]
+
+        # dominant kernel (gate_up trellis GEMV over the 8 routed experts),
+        # timed live by events on its own stream around its launch
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n_total)]
+        with torch.cuda.stream(stream):
+            for row in evs:  # torch creates the CUDA events lazily, at their first record
+                for e in row:
+                    e.record(stream)
+            torch.cuda.synchronize()
+            handles = [(native.ctypes.c_void_p * 6)(*[e.cuda_event for e in row]) for row in evs]
+            ws_t = block.workspace(1)
+            lay = native.ctypes.byref(block.layer)
+            barrier()
+            for i in range(n_total):
+                x_buf.copy_(xs[i:i + 1])
+                flush.zero_()
+                native.check(native.lib().escha_moe_block_timed(
+                    lay, native.ptr(x_buf), 1, native.ptr(out_buf), native.ptr(ids_buf), native.ptr(w_buf),
+                    native.ptr(ws_t), ws_t.numel(), stream.cuda_stream, handles[i]))
+            barrier()
+        phase = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(5)]
+                          for i in range(args.warmup, n_total)])
+    clocks = clk.summary()
+
+    # max over ranks
+    t_step = float(np.mean(step_ms))
+    t_e2e = float(np.mean(e2e_ms))
+    if pg is not None:
+        tt = torch.tensor([t_step, t_e2e], device=dev)
+        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+        t_step, t_e2e = float(tt[0]), float(tt[1])
+    if rank != 0:
+        return
+
+    hbm, tflops, src = peaks()
+    ph = phase.mean(axis=0)  # router, gate_up, down, shared, combine (ms)
+    gu_ms = float(ph[1])
+    gu_bytes = TOPK * (GU_CODE_BYTES + HIDDEN * 2 + 2 * INTER * 2) + HIDDEN * 2 + TOPK * 2 * INTER * 4
+    achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
+    routed_code_bytes = TOPK * (GU_CODE_BYTES + DN_CODE_BYTES)
+    distinct = len({tuple(t.cpu().numpy().ravel()) for t in ids_seen})
+    line = {
+        "metric": METRIC, "value": ws * 1e3 / t_step, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp16 weights / f32 accumulate", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": 1, "tokens_per_step_per_gpu": 1,
+                   "l2": "flushed before every timed step (512 MB write outside the step's events)",
+                   "cuda_graph": True, "parallelism": f"replicas x{ws} (independent token streams)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": None, "kernel": "trellis_gemv_kernel<K=3> (gate_up, 8 routed experts)",
+                     "algorithmic_bytes_per_launch": gu_bytes, "ms_per_launch": gu_ms, "peak_source": src},
+        "packed_expert_gbs": routed_code_bytes / (t_step * 1e-3) / 1e9,
+        "packed_expert_frac": routed_code_bytes / (t_step * 1e-3) / 1e9 / hbm,
+        "phase_ms": {"router": float(ph[0]), "gate_up": float(ph[1]), "down": float(ph[2]),
+                     "shared": float(ph[3]), "combine": float(ph[4])},
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "e2e": {"value": ws * 1e3 / t_e2e, "unit": UNIT, "h2d_bytes_per_step": HIDDEN * 2,
+                "d2h_bytes_per_step": HIDDEN * 4},
+        "clocks": clocks,
+        "routing_distinct_in_first_16_steps": distinct,
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    run_ours(args, ws, rank, local)
+
+
+if __name__ == "__main__":
+    main()

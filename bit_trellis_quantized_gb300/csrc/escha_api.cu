@@ -1,0 +1,355 @@
+// C ABI of the trellis MoE library: argument validation, workspace layout and
+// kernel launches. Every check runs before anything is enqueued; errors are
+// returned as ESCHA_E_* codes with a thread-local message.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "escha.h"
+#include "kernels.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct DeviceInfo {
+    int ok = -1;  // -1 unknown, 0 not sm_103, 1 fine
+    int num_sms = 0;
+};
+
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+
+// Current device must be an sm_103 part (the kernels are built for sm_103a only).
+int device_check(int* num_sms) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(ESCHA_E_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64) return fail(ESCHA_E_DEVICE, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (d.ok < 0) {
+        int major = 0, minor = 0, sms = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        d.ok = (major == 10 && minor == 3) ? 1 : 0;
+        d.num_sms = sms;
+        if (!d.ok) {
+            return fail(ESCHA_E_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a only", dev, major,
+                        minor);
+        }
+    }
+    if (!d.ok) return fail(ESCHA_E_DEVICE, "device %d is not an sm_103 GPU", dev);
+    *num_sms = d.num_sms;
+    return ESCHA_OK;
+}
+
+int cuda_status(cudaError_t e, const char* what) {
+    if (e != cudaSuccess) return fail(ESCHA_E_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    return ESCHA_OK;
+}
+
+size_t align_up(size_t v) { return (v + 255) & ~size_t(255); }
+
+int check_trellis(const uint16_t* codes, int in, int out, int K, int mult, const char* name) {
+    if (!codes) return fail(ESCHA_E_ARG, "%s: codes is null", name);
+    if (!aligned16(codes)) return fail(ESCHA_E_ALIGN, "%s: codes not 16-byte aligned", name);
+    if (K != 2 && K != 3) return fail(ESCHA_E_K, "%s: K=%d, must be 2 or 3", name, K);
+    if (in <= 0 || out <= 0 || in % mult || out % mult)
+        return fail(ESCHA_E_SHAPE, "%s: in=%d out=%d must be positive multiples of %d", name, in, out, mult);
+    return ESCHA_OK;
+}
+
+// Workspace layout of escha_moe_block.
+struct MoeWs {
+    size_t logits, ids, w, ygu, d, shgu, sh, total;
+};
+
+MoeWs moe_ws_layout(const escha_moe_layer* L, int T) {
+    MoeWs m{};
+    size_t off = 0;
+    const size_t slots = (size_t)T * L->topk;
+    m.logits = off;
+    off += align_up((size_t)T * L->n_experts * 2);
+    m.ids = off;
+    off += align_up(slots * 4);
+    m.w = off;
+    off += align_up(slots * 4);
+    m.ygu = off;
+    off += align_up(slots * 2 * (size_t)L->inter * 4);
+    m.d = off;
+    off += align_up(slots * (size_t)L->hidden * 4);
+    m.shgu = off;
+    off += align_up((size_t)T * 2 * (size_t)L->sh_inter * 4);
+    m.sh = off;
+    off += align_up(L->sh_inter > 0 ? (size_t)T * L->hidden * 4 : 0);
+    m.total = off;
+    return m;
+}
+
+int check_layer(const escha_moe_layer* L) {
+    if (!L) return fail(ESCHA_E_ARG, "moe_block: layer is null");
+    if (L->hidden <= 0 || L->hidden % 256) return fail(ESCHA_E_SHAPE, "moe_block: hidden=%d must be a multiple of 256", L->hidden);
+    if (L->hidden > 65536) return fail(ESCHA_E_SHAPE, "moe_block: hidden=%d above 65536", L->hidden);
+    if (L->inter <= 0 || L->inter % 128 || L->inter > 32768)
+        return fail(ESCHA_E_SHAPE, "moe_block: inter=%d must be a multiple of 128 (<= 32768)", L->inter);
+    if (L->n_experts < 1 || L->n_experts > 256) return fail(ESCHA_E_SHAPE, "moe_block: n_experts=%d not in 1..256", L->n_experts);
+    if (L->topk < 1 || L->topk > 8 || L->topk > L->n_experts)
+        return fail(ESCHA_E_SHAPE, "moe_block: topk=%d not in 1..min(8, n_experts)", L->topk);
+    if (!L->router_w || !L->gu_rin || !L->gu_rout || !L->dn_rin || !L->dn_rout)
+        return fail(ESCHA_E_ARG, "moe_block: null router / rin / rout pointer");
+    const void* ptrs[] = {L->router_w, L->gu_rin, L->gu_rout, L->dn_rin, L->dn_rout};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return fail(ESCHA_E_ALIGN, "moe_block: a router / rin / rout pointer is not 16-byte aligned");
+    int r = check_trellis(L->gu_codes, L->hidden, 2 * L->inter, L->gu_K, 128, "moe_block gate_up");
+    if (r) return r;
+    r = check_trellis(L->dn_codes, L->inter, L->hidden, L->dn_K, 128, "moe_block down");
+    if (r) return r;
+    if (L->sh_inter < 0 || L->sh_inter % 16) return fail(ESCHA_E_SHAPE, "moe_block: sh_inter=%d must be a multiple of 16", L->sh_inter);
+    if (L->sh_inter > 0) {
+        if (!L->sh_gu_w8 || !L->sh_gu_scale || !L->sh_dn_w8 || !L->sh_dn_scale || !L->sh_gate)
+            return fail(ESCHA_E_ARG, "moe_block: null shared-expert pointer");
+        const void* sp[] = {L->sh_gu_w8, L->sh_gu_scale, L->sh_dn_w8, L->sh_dn_scale, L->sh_gate};
+        for (const void* p : sp)
+            if (!aligned16(p)) return fail(ESCHA_E_ALIGN, "moe_block: a shared-expert pointer is not 16-byte aligned");
+        if (2 * L->sh_inter * 4 > 200 * 1024 || L->hidden * 4 > 200 * 1024)
+            return fail(ESCHA_E_SHAPE, "moe_block: shared expert too large for the int8 GEMV");
+    }
+    return ESCHA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* escha_last_error(void) { return g_last_error.c_str(); }
+
+int escha_version(void) { return 100; }
+
+int escha_trellis_decode(const uint16_t* codes, int in, int out, int K, uint16_t* W, void* stream) {
+    int r = check_trellis(codes, in, out, K, 16, "trellis_decode");
+    if (r) return r;
+    if (!W) return fail(ESCHA_E_ARG, "trellis_decode: W is null");
+    if (!aligned16(W)) return fail(ESCHA_E_ALIGN, "trellis_decode: W not 16-byte aligned");
+    int sms;
+    if ((r = device_check(&sms))) return r;
+    return cuda_status(escha::launch_trellis_decode(codes, in, out, K, W, static_cast<cudaStream_t>(stream)),
+                       "trellis_decode launch");
+}
+
+size_t escha_trellis_gemv_workspace(int in, int out, int K, int batch) {
+    (void)in;
+    (void)out;
+    (void)K;
+    (void)batch;
+    return 0;
+}
+
+int escha_trellis_gemv(const uint16_t* codes, int in, int out, int K, const void* x, int x_dtype, int batch,
+                       const uint16_t* rin, const uint16_t* rout, float* y, void* ws, size_t ws_bytes, void* stream) {
+    (void)ws;
+    int r = check_trellis(codes, in, out, K, 128, "trellis_gemv");
+    if (r) return r;
+    if (in > 65536) return fail(ESCHA_E_SHAPE, "trellis_gemv: in=%d above 65536", in);
+    if (!x || !rin || !rout || !y) return fail(ESCHA_E_ARG, "trellis_gemv: null x / rin / rout / y");
+    if (x_dtype != ESCHA_F16 && x_dtype != ESCHA_F32)
+        return fail(ESCHA_E_ARG, "trellis_gemv: x_dtype=%d must be ESCHA_F16 or ESCHA_F32", x_dtype);
+    if (batch < 1) return fail(ESCHA_E_ARG, "trellis_gemv: batch=%d must be >= 1", batch);
+    if (!aligned16(x) || !aligned16(rin) || !aligned16(rout) || !aligned16(y))
+        return fail(ESCHA_E_ALIGN, "trellis_gemv: x / rin / rout / y not 16-byte aligned");
+    if (ws_bytes < escha_trellis_gemv_workspace(in, out, K, batch))
+        return fail(ESCHA_E_WORKSPACE, "trellis_gemv: workspace too small");
+    int sms;
+    if ((r = device_check(&sms))) return r;
+    escha::GemvArgs a{};
+    a.codes = codes;
+    a.code_stride = 0;
+    a.in = in;
+    a.out = out;
+    a.x_mode = x_dtype == ESCHA_F16 ? escha::kXmF16 : escha::kXmF32;
+    a.x = x;
+    a.x_stride = in;
+    a.rin = rin;
+    a.rout = rout;
+    a.y = y;
+    a.y_stride = out;
+    a.batch = batch;
+    a.slot_mode = 0;
+    a.x_div = 1;
+    const int nb = batch == 1 ? 1 : batch == 2 ? 2 : 4;
+    const int items = (batch + nb - 1) / nb;
+    return cuda_status(escha::launch_trellis_gemv(a, K, nb, items, sms, static_cast<cudaStream_t>(stream)),
+                       "trellis_gemv launch");
+}
+
+size_t escha_moe_block_workspace(const escha_moe_layer* L, int T) {
+    if (!L || T < 1 || L->topk < 1) return 0;
+    return moe_ws_layout(L, T).total;
+}
+
+}  // extern "C"
+
+namespace {
+
+int record(cudaEvent_t* ev, int i, cudaStream_t s) {
+    if (!ev || !ev[i]) return ESCHA_OK;
+    return cuda_status(cudaEventRecord(ev[i], s), "cudaEventRecord");
+}
+
+int moe_block_impl(const escha_moe_layer* L, const uint16_t* x, int T, float* out, int32_t* ids_out, float* w_out,
+                   void* ws, size_t ws_bytes, void* stream, cudaEvent_t* ev) {
+    int r = check_layer(L);
+    if (r) return r;
+    if (T < 1) return fail(ESCHA_E_ARG, "moe_block: T=%d must be >= 1", T);
+    if (!x || !out) return fail(ESCHA_E_ARG, "moe_block: null x / out");
+    if (!aligned16(x) || !aligned16(out) || (ids_out && !aligned16(ids_out)) || (w_out && !aligned16(w_out)))
+        return fail(ESCHA_E_ALIGN, "moe_block: x / out / ids_out / w_out not 16-byte aligned");
+    const MoeWs m = moe_ws_layout(L, T);
+    if (!ws || ws_bytes < m.total)
+        return fail(ESCHA_E_WORKSPACE, "moe_block: workspace %zu bytes, need %zu", ws_bytes, m.total);
+    if (!aligned16(ws)) return fail(ESCHA_E_ALIGN, "moe_block: workspace not 16-byte aligned");
+    int sms;
+    if ((r = device_check(&sms))) return r;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* base = static_cast<char*>(ws);
+    uint16_t* logits = reinterpret_cast<uint16_t*>(base + m.logits);
+    int32_t* ids = ids_out ? ids_out : reinterpret_cast<int32_t*>(base + m.ids);
+    float* w = w_out ? w_out : reinterpret_cast<float*>(base + m.w);
+    float* ygu = reinterpret_cast<float*>(base + m.ygu);
+    float* d = reinterpret_cast<float*>(base + m.d);
+    float* shgu = reinterpret_cast<float*>(base + m.shgu);
+    float* sh = L->sh_inter > 0 ? reinterpret_cast<float*>(base + m.sh) : nullptr;
+    const int slots = T * L->topk;
+
+    if ((r = record(ev, 0, s))) return r;
+    if ((r = cuda_status(escha::launch_router(x, L->router_w, T, L->hidden, L->n_experts, L->topk, logits, ids, w,
+                                              nullptr, s),
+                         "router launch")))
+        return r;
+    if ((r = record(ev, 1, s))) return r;
+
+    escha::GemvArgs g{};
+    g.codes = L->gu_codes;
+    g.code_stride = (long long)(L->hidden / 16) * (2 * L->inter / 16) * (16 * L->gu_K);
+    g.in = L->hidden;
+    g.out = 2 * L->inter;
+    g.x_mode = escha::kXmF16;
+    g.x = x;
+    g.x_stride = L->hidden;
+    g.rin = L->gu_rin;
+    g.rin_stride = L->hidden;
+    g.rout = L->gu_rout;
+    g.rout_stride = 2 * L->inter;
+    g.y = ygu;
+    g.y_stride = 2 * L->inter;
+    g.ids = ids;
+    g.x_div = L->topk;
+    g.slot_mode = 1;
+    if ((r = cuda_status(escha::launch_trellis_gemv(g, L->gu_K, 1, slots, sms, s), "gate_up launch"))) return r;
+    if ((r = record(ev, 2, s))) return r;
+
+    escha::GemvArgs dn{};
+    dn.codes = L->dn_codes;
+    dn.code_stride = (long long)(L->inter / 16) * (L->hidden / 16) * (16 * L->dn_K);
+    dn.in = L->inter;
+    dn.out = L->hidden;
+    dn.x_mode = escha::kXmSwiglu;
+    dn.x = ygu;
+    dn.x_stride = 2 * L->inter;
+    dn.rin = L->dn_rin;
+    dn.rin_stride = L->inter;
+    dn.rout = L->dn_rout;
+    dn.rout_stride = L->hidden;
+    dn.y = d;
+    dn.y_stride = L->hidden;
+    dn.ids = ids;
+    dn.x_div = 1;
+    dn.slot_mode = 1;
+    if ((r = cuda_status(escha::launch_trellis_gemv(dn, L->dn_K, 1, slots, sms, s), "down launch"))) return r;
+    if ((r = record(ev, 3, s))) return r;
+
+    if (L->sh_inter > 0) {
+        if ((r = cuda_status(escha::launch_int8_gemv(L->sh_gu_w8, L->sh_gu_scale, 2 * L->sh_inter, L->hidden, x,
+                                                     ESCHA_F16, L->hidden, 0, T, shgu, 2 * L->sh_inter, sms, s),
+                             "shared gate_up launch")))
+            return r;
+        if ((r = cuda_status(escha::launch_int8_gemv(L->sh_dn_w8, L->sh_dn_scale, L->hidden, L->sh_inter, shgu,
+                                                     ESCHA_F32, 2 * L->sh_inter, 1, T, sh, L->hidden, sms, s),
+                             "shared down launch")))
+            return r;
+    }
+    if ((r = record(ev, 4, s))) return r;
+    if ((r = cuda_status(escha::launch_moe_combine(d, w, T, L->topk, L->hidden, sh, L->sh_gate, x, out, s),
+                         "combine launch")))
+        return r;
+    return record(ev, 5, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+int escha_moe_block(const escha_moe_layer* L, const uint16_t* x, int T, float* out, int32_t* ids_out, float* w_out,
+                    void* ws, size_t ws_bytes, void* stream) {
+    return moe_block_impl(L, x, T, out, ids_out, w_out, ws, ws_bytes, stream, nullptr);
+}
+
+int escha_moe_block_timed(const escha_moe_layer* L, const uint16_t* x, int T, float* out, int32_t* ids_out,
+                          float* w_out, void* ws, size_t ws_bytes, void* stream, void* const* events) {
+    cudaEvent_t ev[6];
+    for (int i = 0; i < 6; ++i) ev[i] = events ? static_cast<cudaEvent_t>(events[i]) : nullptr;
+    return moe_block_impl(L, x, T, out, ids_out, w_out, ws, ws_bytes, stream, ev);
+}
+
+size_t int8_w8a16_workspace(int N, int Kin, int M) {
+    (void)N;
+    (void)Kin;
+    (void)M;
+    return 0;
+}
+
+int int8_w8a16_matvec(const int8_t* W, const float* scales, int N, int Kin, const void* x, int x_dtype, int M,
+                      float* y, void* ws, size_t ws_bytes, void* stream) {
+    (void)ws;
+    (void)ws_bytes;
+    if (!W || !scales || !x || !y) return fail(ESCHA_E_ARG, "int8_w8a16_matvec: null pointer");
+    if (N < 1 || M < 1) return fail(ESCHA_E_ARG, "int8_w8a16_matvec: N=%d M=%d must be >= 1", N, M);
+    if (Kin < 16 || Kin % 16 || Kin > 51200)
+        return fail(ESCHA_E_SHAPE, "int8_w8a16_matvec: Kin=%d must be a multiple of 16 in 16..51200", Kin);
+    if (x_dtype != ESCHA_F16 && x_dtype != ESCHA_BF16 && x_dtype != ESCHA_F32)
+        return fail(ESCHA_E_ARG, "int8_w8a16_matvec: x_dtype=%d", x_dtype);
+    if (!aligned16(W) || !aligned16(scales) || !aligned16(x) || !aligned16(y))
+        return fail(ESCHA_E_ALIGN, "int8_w8a16_matvec: pointer not 16-byte aligned");
+    int r, sms;
+    if ((r = device_check(&sms))) return r;
+    return cuda_status(escha::launch_int8_gemv(W, scales, N, Kin, x, x_dtype, Kin, 0, M, y, N, sms,
+                                               static_cast<cudaStream_t>(stream)),
+                       "int8 gemv launch");
+}
+
+int int8_w8a16_dequant(const int8_t* W, const float* scales, int N, int Kin, float* out, void* stream) {
+    if (!W || !scales || !out) return fail(ESCHA_E_ARG, "int8_w8a16_dequant: null pointer");
+    if (N < 1 || Kin < 1) return fail(ESCHA_E_SHAPE, "int8_w8a16_dequant: N=%d Kin=%d", N, Kin);
+    int r, sms;
+    if ((r = device_check(&sms))) return r;
+    return cuda_status(escha::launch_int8_dequant(W, scales, N, Kin, out, static_cast<cudaStream_t>(stream)),
+                       "int8 dequant launch");
+}
+
+}  // extern "C"

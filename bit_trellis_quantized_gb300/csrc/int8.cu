@@ -1,0 +1,158 @@
+// int8 w8a16: y[m][o] = sum_i (scale[o] * W[o][i]) * x[m][i], the int8
+// weights used as stored (MTPLX PR #242 "serve Qwen3.6-35B-A3B-Escha-W2
+// natively", table "Improvements": fused int8 matvec, no dequant at load; MLX
+// model card, table "Exactness of every tensor": dequant = f32 scale * w8).
+//
+// GEMV design (small M). Memory-bound at M = 1: each warp streams 4 rows with
+// 16-byte loads (16 weights per lane per row per step) and keeps the
+// activations of up to 8 tokens in shared memory as f32. Bytes become floats
+// without an integer-to-float conversion instruction: byte b (biased to
+// b + 128) is placed in the mantissa of 2^23 and 2^23 + 128 is subtracted,
+// which is exact. The row scale multiplies the finished dot product.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace escha {
+
+namespace {
+
+constexpr int kRowsPerWarp = 4;
+constexpr int kMaxTok = 8;
+
+// Four signed bytes of v as exact floats.
+__device__ __forceinline__ void bytes_to_f32(uint32_t v, float (&f)[4]) {
+    const uint32_t u = v ^ 0x80808080u;  // b + 128 in each byte
+    const float bias = 8388736.0f;       // 2^23 + 128
+    f[0] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650)) - bias;
+    f[1] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7651)) - bias;
+    f[2] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7652)) - bias;
+    f[3] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653)) - bias;
+}
+
+template <int MT>
+__global__ void __launch_bounds__(256) int8_gemv_kernel(const int8_t* __restrict__ W, const float* __restrict__ scales,
+                                                        int N, int Kin, const void* __restrict__ x, int x_dtype,
+                                                        long long x_stride, int act, int M, float* __restrict__ y,
+                                                        long long y_stride) {
+    extern __shared__ __align__(16) float xs[];  // [MT][Kin]
+    const int m0 = blockIdx.y * MT;
+    const int mt = min(MT, M - m0);
+    for (int idx = threadIdx.x; idx < MT * Kin; idx += blockDim.x) {
+        const int t = idx / Kin, i = idx % Kin;
+        float v = 0.f;
+        if (t < mt) {
+            const long long row = (long long)(m0 + t) * x_stride;
+            if (act == 1) {
+                const float* yr = static_cast<const float*>(x) + row;
+                v = silu_f(yr[i]) * yr[Kin + i];
+            } else {
+                v = load_act(x, row + i, x_dtype);
+            }
+        }
+        xs[idx] = v;
+    }
+    __syncthreads();
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warps_total = gridDim.x * 8;
+    for (int r0 = (blockIdx.x * 8 + warp) * kRowsPerWarp; r0 < N; r0 += warps_total * kRowsPerWarp) {
+        float acc[kRowsPerWarp][MT];
+#pragma unroll
+        for (int r = 0; r < kRowsPerWarp; ++r)
+#pragma unroll
+            for (int t = 0; t < MT; ++t) acc[r][t] = 0.f;
+        for (int i0 = lane * 16; i0 < Kin; i0 += 512) {
+            uint4 wv[kRowsPerWarp];
+#pragma unroll
+            for (int r = 0; r < kRowsPerWarp; ++r) {
+                const int row = min(r0 + r, N - 1);
+                wv[r] = ldg_stream_v4(W + (long long)row * Kin + i0);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float xq[MT][4];
+#pragma unroll
+                for (int t = 0; t < MT; ++t) {
+                    const float4 xv = *reinterpret_cast<const float4*>(xs + t * Kin + i0 + 4 * q);
+                    xq[t][0] = xv.x;
+                    xq[t][1] = xv.y;
+                    xq[t][2] = xv.z;
+                    xq[t][3] = xv.w;
+                }
+#pragma unroll
+                for (int r = 0; r < kRowsPerWarp; ++r) {
+                    const uint32_t word = q == 0 ? wv[r].x : q == 1 ? wv[r].y : q == 2 ? wv[r].z : wv[r].w;
+                    float f[4];
+                    bytes_to_f32(word, f);
+#pragma unroll
+                    for (int t = 0; t < MT; ++t)
+#pragma unroll
+                        for (int b = 0; b < 4; ++b) acc[r][t] = fmaf(f[b], xq[t][b], acc[r][t]);
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < kRowsPerWarp; ++r)
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+                float v = acc[r][t];
+#pragma unroll
+                for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+                acc[r][t] = v;
+            }
+        if (lane == 0) {
+#pragma unroll
+            for (int r = 0; r < kRowsPerWarp; ++r) {
+                if (r0 + r >= N) break;
+                const float sc = scales[r0 + r];
+#pragma unroll
+                for (int t = 0; t < MT; ++t)
+                    if (t < mt) y[(long long)(m0 + t) * y_stride + r0 + r] = sc * acc[r][t];
+            }
+        }
+    }
+}
+
+__global__ void int8_dequant_kernel(const int8_t* __restrict__ W, const float* __restrict__ scales, int N, int Kin,
+                                    float* __restrict__ out) {
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (long long)N * Kin) return;
+    const int o = static_cast<int>(idx / Kin);
+    out[idx] = __fmul_rn(scales[o], static_cast<float>(W[idx]));
+}
+
+template <int MT>
+cudaError_t launch_mt(const int8_t* W, const float* scales, int N, int Kin, const void* x, int x_dtype,
+                      long long x_stride, int act, int M, float* y, long long y_stride, int num_sms, cudaStream_t s) {
+    const int smem = MT * Kin * (int)sizeof(float);
+    auto kern = int8_gemv_kernel<MT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const long long row_groups = (N + 8 * kRowsPerWarp - 1) / (8 * kRowsPerWarp);
+    const int gx = static_cast<int>(row_groups < 8LL * num_sms ? row_groups : 8LL * num_sms);
+    dim3 grid(gx, (M + MT - 1) / MT);
+    kern<<<grid, 256, smem, s>>>(W, scales, N, Kin, x, x_dtype, x_stride, act, M, y, y_stride);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_int8_gemv(const int8_t* W, const float* scales, int N, int Kin, const void* x, int x_dtype,
+                             long long x_stride, int act, int M, float* y, long long y_stride, int num_sms,
+                             cudaStream_t s) {
+    // tokens per pass whose f32 activations fit in shared memory
+    const int cap = (200 * 1024) / (4 * Kin);
+    if (cap < 1) return cudaErrorInvalidValue;
+    if (M == 1 || cap < 2) return launch_mt<1>(W, scales, N, Kin, x, x_dtype, x_stride, act, M, y, y_stride, num_sms, s);
+    if (M == 2 || cap < 4) return launch_mt<2>(W, scales, N, Kin, x, x_dtype, x_stride, act, M, y, y_stride, num_sms, s);
+    if (M <= 4 || cap < 8) return launch_mt<4>(W, scales, N, Kin, x, x_dtype, x_stride, act, M, y, y_stride, num_sms, s);
+    return launch_mt<kMaxTok>(W, scales, N, Kin, x, x_dtype, x_stride, act, M, y, y_stride, num_sms, s);
+}
+
+cudaError_t launch_int8_dequant(const int8_t* W, const float* scales, int N, int Kin, float* out, cudaStream_t s) {
+    const long long total = (long long)N * Kin;
+    int8_dequant_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, s>>>(W, scales, N, Kin, out);
+    return cudaGetLastError();
+}
+
+}  // namespace escha

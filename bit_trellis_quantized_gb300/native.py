@@ -1,0 +1,279 @@
+"""ctypes binding of libescha.so, the C ABI declared in include/escha.h.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI. Torch tensors provide device memory and the current
+stream. There is no CPU fallback: if the library is missing or the device is
+not an sm_103 GPU, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libescha.so")
+
+ESCHA_OK = 0
+ESCHA_E_ARG = -1
+ESCHA_E_SHAPE = -2
+ESCHA_E_K = -3
+ESCHA_E_WORKSPACE = -4
+ESCHA_E_ALIGN = -5
+ESCHA_E_CUDA = -6
+ESCHA_E_DEVICE = -7
+
+ESCHA_F16 = 1
+ESCHA_BF16 = 2
+ESCHA_F32 = 3
+
+EXPORTS = [
+    "escha_last_error",
+    "escha_version",
+    "escha_trellis_decode",
+    "escha_trellis_gemv_workspace",
+    "escha_trellis_gemv",
+    "escha_moe_block_workspace",
+    "escha_moe_block",
+    "escha_moe_block_timed",
+    "int8_w8a16_workspace",
+    "int8_w8a16_matvec",
+    "int8_w8a16_dequant",
+]
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_sz = ctypes.c_size_t
+
+
+class EschaMoeLayer(ctypes.Structure):
+    """Mirror of ``escha_moe_layer`` in include/escha.h."""
+
+    _fields_ = [
+        ("hidden", _i),
+        ("inter", _i),
+        ("n_experts", _i),
+        ("topk", _i),
+        ("router_w", _vp),
+        ("gu_codes", _vp),
+        ("gu_K", _i),
+        ("gu_rin", _vp),
+        ("gu_rout", _vp),
+        ("dn_codes", _vp),
+        ("dn_K", _i),
+        ("dn_rin", _vp),
+        ("dn_rout", _vp),
+        ("sh_inter", _i),
+        ("sh_gu_w8", _vp),
+        ("sh_gu_scale", _vp),
+        ("sh_dn_w8", _vp),
+        ("sh_dn_scale", _vp),
+        ("sh_gate", _vp),
+    ]
+
+
+_LIB = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libescha.so once (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                               "(python -m bit_trellis_quantized_gb300.build)")
+        L = ctypes.CDLL(LIB_PATH)
+        L.escha_last_error.restype = ctypes.c_char_p
+        L.escha_last_error.argtypes = []
+        L.escha_version.restype = _i
+        L.escha_trellis_decode.argtypes = [_vp, _i, _i, _i, _vp, _vp]
+        L.escha_trellis_decode.restype = _i
+        L.escha_trellis_gemv_workspace.argtypes = [_i, _i, _i, _i]
+        L.escha_trellis_gemv_workspace.restype = _sz
+        L.escha_trellis_gemv.argtypes = [_vp, _i, _i, _i, _vp, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]
+        L.escha_trellis_gemv.restype = _i
+        L.escha_moe_block_workspace.argtypes = [ctypes.POINTER(EschaMoeLayer), _i]
+        L.escha_moe_block_workspace.restype = _sz
+        L.escha_moe_block.argtypes = [ctypes.POINTER(EschaMoeLayer), _vp, _i, _vp, _vp, _vp, _vp, _sz, _vp]
+        L.escha_moe_block.restype = _i
+        L.escha_moe_block_timed.argtypes = [ctypes.POINTER(EschaMoeLayer), _vp, _i, _vp, _vp, _vp, _vp, _sz, _vp,
+                                            ctypes.POINTER(_vp)]
+        L.escha_moe_block_timed.restype = _i
+        L.int8_w8a16_workspace.argtypes = [_i, _i, _i]
+        L.int8_w8a16_workspace.restype = _sz
+        L.int8_w8a16_matvec.argtypes = [_vp, _vp, _i, _i, _vp, _i, _i, _vp, _vp, _sz, _vp]
+        L.int8_w8a16_matvec.restype = _i
+        L.int8_w8a16_dequant.argtypes = [_vp, _vp, _i, _i, _vp, _vp]
+        L.int8_w8a16_dequant.restype = _i
+        _LIB = L
+    return _LIB
+
+
+class EschaError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"escha error {code}: {msg}")
+        self.code = code
+
+
+def check(code: int) -> None:
+    if code != ESCHA_OK:
+        raise EschaError(code, lib().escha_last_error().decode())
+
+
+def ptr(t) -> int | None:
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def stream_handle(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _dtype_tag(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return ESCHA_F16
+    if t.dtype == torch.bfloat16:
+        return ESCHA_BF16
+    if t.dtype == torch.float32:
+        return ESCHA_F32
+    raise TypeError(f"unsupported activation dtype {t.dtype}")
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+# --------------------------------------------------------------------------
+# High-level wrappers (torch tensors in, torch tensors out).
+# --------------------------------------------------------------------------
+
+
+def trellis_decode(codes: torch.Tensor, stream=None) -> torch.Tensor:
+    """Dense fp16 weights W[in][out] of a code tensor [in/16][out/16][16K]."""
+    _need_cuda(codes)
+    KT, NT, L = codes.shape
+    W = torch.empty((KT * 16, NT * 16), dtype=torch.float16, device=codes.device)
+    check(lib().escha_trellis_decode(ptr(codes), KT * 16, NT * 16, L // 16, ptr(W), stream_handle(stream)))
+    return W
+
+
+def trellis_gemv(codes, x, rin, rout, y=None, stream=None) -> torch.Tensor:
+    """y[b] = rout * H(W^T H(rin * x[b])) for a batch of tokens sharing one
+    trellis-coded weight. x: [batch][in] fp16 or f32."""
+    _need_cuda(codes, x, rin, rout)
+    KT, NT, L = codes.shape
+    n_in, n_out = KT * 16, NT * 16
+    if x.dim() == 1:
+        x = x.unsqueeze(0)
+    batch = x.shape[0]
+    if y is None:
+        y = torch.empty((batch, n_out), dtype=torch.float32, device=x.device)
+    check(lib().escha_trellis_gemv(ptr(codes), n_in, n_out, L // 16, ptr(x), _dtype_tag(x), batch, ptr(rin),
+                                   ptr(rout), ptr(y), None, 0, stream_handle(stream)))
+    return y
+
+
+def int8_w8a16_matvec(W, scales, x, y=None, stream=None) -> torch.Tensor:
+    """y[m][o] = sum_i (scales[o] * W[o][i]) * x[m][i]; x [M][Kin] bf16/f16/f32."""
+    _need_cuda(W, scales, x)
+    N, Kin = W.shape
+    if x.dim() == 1:
+        x = x.unsqueeze(0)
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    ws_bytes = lib().int8_w8a16_workspace(N, Kin, M)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=x.device)
+    check(lib().int8_w8a16_matvec(ptr(W), ptr(scales), N, Kin, ptr(x), _dtype_tag(x), M, ptr(y), ptr(ws), ws_bytes,
+                                  stream_handle(stream)))
+    return y
+
+
+def int8_w8a16_dequant(W, scales, stream=None) -> torch.Tensor:
+    _need_cuda(W, scales)
+    N, Kin = W.shape
+    out = torch.empty((N, Kin), dtype=torch.float32, device=W.device)
+    check(lib().int8_w8a16_dequant(ptr(W), ptr(scales), N, Kin, ptr(out), stream_handle(stream)))
+    return out
+
+
+class MoeBlock:
+    """Device-resident weights of one MoE block plus the C-ABI layer struct.
+
+    ``arrays`` holds numpy arrays with the keys of ``escha_synth.moe_layer``;
+    they are copied to the device once.
+    """
+
+    def __init__(self, arrays: dict, device="cuda", topk: int = 8):
+        def dev(a):
+            a = np.ascontiguousarray(a)
+            if a.dtype == np.uint16:
+                a = a.view(np.int16)  # code words travel as raw 16-bit patterns
+            return torch.from_numpy(a).to(device).contiguous()
+
+        self.hidden = int(arrays["hidden"])
+        self.inter = int(arrays["inter"])
+        self.n_experts = int(arrays["n_experts"])
+        self.topk = topk
+        self.sh_inter = int(arrays.get("sh_inter", 0) or 0)
+        self.t = {}
+        self.t["router_w"] = dev(arrays["Wg"])
+        self.t["gu_codes"] = dev(arrays["gu_codes"])
+        self.t["gu_rin"] = dev(arrays["gu_rin"])
+        self.t["gu_rout"] = dev(arrays["gu_rout"])
+        self.t["dn_codes"] = dev(arrays["dn_codes"])
+        self.t["dn_rin"] = dev(arrays["dn_rin"])
+        self.t["dn_rout"] = dev(arrays["dn_rout"])
+        self.gu_K = arrays["gu_codes"].shape[-1] // 16
+        self.dn_K = arrays["dn_codes"].shape[-1] // 16
+        if self.sh_inter:
+            self.t["sh_gu_w8"] = dev(arrays["sh_gu_w8"])
+            self.t["sh_gu_scale"] = dev(arrays["sh_gu_s"])
+            self.t["sh_dn_w8"] = dev(arrays["sh_dn_w8"])
+            self.t["sh_dn_scale"] = dev(arrays["sh_dn_s"])
+            self.t["sh_gate"] = dev(arrays["sh_gate"])
+        self.layer = self._struct()
+        self._ws = None
+
+    def _struct(self) -> EschaMoeLayer:
+        t = self.t
+        L = EschaMoeLayer()
+        L.hidden, L.inter, L.n_experts, L.topk = self.hidden, self.inter, self.n_experts, self.topk
+        L.router_w = ptr(t["router_w"])
+        L.gu_codes, L.gu_K, L.gu_rin, L.gu_rout = ptr(t["gu_codes"]), self.gu_K, ptr(t["gu_rin"]), ptr(t["gu_rout"])
+        L.dn_codes, L.dn_K, L.dn_rin, L.dn_rout = ptr(t["dn_codes"]), self.dn_K, ptr(t["dn_rin"]), ptr(t["dn_rout"])
+        L.sh_inter = self.sh_inter
+        if self.sh_inter:
+            L.sh_gu_w8, L.sh_gu_scale = ptr(t["sh_gu_w8"]), ptr(t["sh_gu_scale"])
+            L.sh_dn_w8, L.sh_dn_scale = ptr(t["sh_dn_w8"]), ptr(t["sh_dn_scale"])
+            L.sh_gate = ptr(t["sh_gate"])
+        return L
+
+    def workspace(self, T: int) -> torch.Tensor:
+        need = lib().escha_moe_block_workspace(ctypes.byref(self.layer), T)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty(max(need, 256), dtype=torch.uint8, device=self.t["router_w"].device)
+        return self._ws
+
+    def __call__(self, x: torch.Tensor, out=None, ids=None, w=None, stream=None):
+        """x [T][hidden] fp16 (CUDA). Returns (out f32 [T][hidden], ids int32
+        [T][topk], w f32 [T][topk])."""
+        _need_cuda(x)
+        T = x.shape[0]
+        dev = x.device
+        if out is None:
+            out = torch.empty((T, self.hidden), dtype=torch.float32, device=dev)
+        if ids is None:
+            ids = torch.empty((T, self.topk), dtype=torch.int32, device=dev)
+        if w is None:
+            w = torch.empty((T, self.topk), dtype=torch.float32, device=dev)
+        ws = self.workspace(T)
+        check(lib().escha_moe_block(ctypes.byref(self.layer), ptr(x), T, ptr(out), ptr(ids), ptr(w), ptr(ws),
+                                    ws.numel(), stream_handle(stream)))
+        return out, ids, w

@@ -1,0 +1,187 @@
+/*
+ * escha.h - C ABI of the GB300 (sm_103a) trellis MoE expert library.
+ *
+ * The library computes the MoE expert path of an Escha-W2 ("eschamoe")
+ * 2/3-bit Qwen3.6-35B-A3B-style layer with the packed trellis codes decoded
+ * inside the GEMV, never materialised as dense weights, plus the int8 w8a16
+ * matvec/GEMM of the dense layers.
+ *
+ * Sources (by page):
+ *   [PR694]  hipfire PR #694 "Escha-W2 port: 2-bit trellis decoded in the GEMV"
+ *            (summary section "What it is" and the PR's commit messages);
+ *   [MLX]    model card "dogfoodai/Qwen3.6-35B-A3B-Escha-W2-trellis-mlx",
+ *            table "Exactness of every tensor";
+ *   [CARD]   model card "EschaLabs/Qwen3.6-35B-A3B-Escha-W2", "Format notes".
+ *
+ * Conventions shared by every entry point:
+ *   - Tensor pointers are DEVICE pointers owned by the caller; the library
+ *     never frees or keeps them. fp16 / bf16 tensors are passed as their
+ *     16-bit patterns (uint16_t). All tensors are dense row-major, contiguous.
+ *   - Tensor pointers must be 16-byte aligned (ESCHA_E_ALIGN otherwise).
+ *   - `stream` is a cudaStream_t (0 = the legacy default stream). Work is
+ *     only enqueued on it; no call synchronises the host.
+ *   - Scratch memory comes from the caller's workspace `ws` of `ws_bytes`
+ *     bytes; each entry point has a *_workspace() query. A larger workspace
+ *     is accepted. The library allocates no device memory.
+ *   - Every argument is validated before anything is enqueued. On error the
+ *     call returns a negative ESCHA_E_* code, enqueues nothing, and
+ *     escha_last_error() describes the problem. Asynchronous device faults
+ *     surface at the caller's next synchronisation, as for any CUDA work.
+ *   - Trellis code tensors: uint16 [in/16][out/16][16*K] (tile grid stored
+ *     with the input-tile index outermost), K = bits per weight in {2, 3},
+ *     equal to the code tensor's last dimension / 16 [PR694 commit "Read
+ *     Escha's test suite"; CARD "Format notes"]. Each 16x16 tile's 16*K words
+ *     form one cyclic bit stream (most significant bit of each word first);
+ *     weight t = 16*r + q of the tile (r = input row, q = output column)
+ *     takes the 16-bit window starting at bit t*K as its trellis state, and
+ *     the state decodes through the "cbA" hash
+ *        r = ((s * 0xCBAC1FED) & 0x8FFF8FFF) ^ 0x3B603B60,
+ *        w = fp16_rne(fp16(r & 0xffff) + fp16(r >> 16))
+ *     [PR694 "What it is"; MLX "Exactness of every tensor"].
+ *   - Rotations: each trellis projection computes
+ *        y = rout * H(W^T H(rin * x))
+ *     with H the blockwise Sylvester Hadamard-128 scaled by 1/sqrt(128) on
+ *     both sides [PR694 "What it is"; MLX note on mx.hadamard_transform];
+ *     rout is the final multiply, so channels whose rout is 0 (the per-expert
+ *     prune mask of gate_up) come out exactly +-0 [PR694 commits "Second
+ *     review pass" and "Naive one-thread-per-block butterfly"].
+ */
+#ifndef ESCHA_H
+#define ESCHA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes --------------------------------------------------- */
+#define ESCHA_OK 0
+#define ESCHA_E_ARG (-1)       /* null pointer, bad enum, non-positive count */
+#define ESCHA_E_SHAPE (-2)     /* dimension not a multiple of 16 / 128, too large */
+#define ESCHA_E_K (-3)         /* bits per weight not 2 or 3 */
+#define ESCHA_E_WORKSPACE (-4) /* workspace smaller than *_workspace() */
+#define ESCHA_E_ALIGN (-5)     /* pointer not 16-byte aligned */
+#define ESCHA_E_CUDA (-6)      /* CUDA error while enqueueing (launch/config) */
+#define ESCHA_E_DEVICE (-7)    /* current device is not an sm_103 GPU */
+
+/* ---- element types --------------------------------------------------- */
+#define ESCHA_F16 1
+#define ESCHA_BF16 2
+#define ESCHA_F32 3
+
+/* Message describing the last error returned on this host thread. */
+const char* escha_last_error(void);
+
+/* Library version: major*10000 + minor*100 + patch. */
+int escha_version(void);
+
+/* ---- trellis decode (diagnostic export) ----------------------------------
+ * Decodes a whole code tensor to dense fp16 weights, W[in][out] (uint16 bit
+ * patterns), for the bit-exact decode check [PR694 commit "Task 7 (G2): one-
+ * shot decode of Escha-W2 packed trellis tiles"]. Not part of the hot path:
+ * the GEMV entry points never materialise W.
+ *   codes  uint16 [in/16][out/16][16*K]
+ *   in,out multiples of 16;  K in {2, 3}
+ *   W      uint16 [in][out] output
+ * Errors: ESCHA_E_ARG (null), ESCHA_E_SHAPE, ESCHA_E_K, ESCHA_E_ALIGN. */
+int escha_trellis_decode(const uint16_t* codes, int in, int out, int K, uint16_t* W, void* stream);
+
+/* ---- one trellis-coded projection ----------------------------------------
+ * y[b] = rout * H(W^T H(rin * x[b])) for b < batch, all tokens sharing the
+ * one weight [PR694 commit "EschaProj holds what a trellis weight needs";
+ * the projection as "H128-in -> trellis GEMV -> H128-out"]. Accumulation is
+ * fp32; decoded weights are exact fp16.
+ *   codes   uint16 [in/16][out/16][16*K], K in {2, 3}
+ *   in,out  multiples of 128 (whole Hadamard blocks), in <= 65536
+ *   x       [batch][in], x_dtype ESCHA_F16 or ESCHA_F32
+ *   rin     fp16 [in];  rout fp16 [out]
+ *   y       f32 [batch][out] output
+ *   ws      escha_trellis_gemv_workspace(in, out, K, batch) bytes (may be 0)
+ * Errors: ESCHA_E_ARG, ESCHA_E_SHAPE, ESCHA_E_K, ESCHA_E_ALIGN,
+ *         ESCHA_E_WORKSPACE, ESCHA_E_CUDA, ESCHA_E_DEVICE. */
+size_t escha_trellis_gemv_workspace(int in, int out, int K, int batch);
+int escha_trellis_gemv(const uint16_t* codes, int in, int out, int K, const void* x, int x_dtype, int batch,
+                       const uint16_t* rin, const uint16_t* rout, float* y, void* ws, size_t ws_bytes,
+                       void* stream);
+
+/* ---- one MoE block ------------------------------------------------------
+ * For each token b of x [T][hidden] (fp16):
+ *   logits = f16(x[b] . Wg[e]) for every expert e (f32 sums in a fixed
+ *            order, rounded to f16 before top-k [PR694 commit "Executed the
+ *            moeblk golden against real shipped layer-0 weights"]);
+ *   ids    = the topk largest logits, ties to the lower expert id, ordered
+ *            by (logit desc, id asc); w = softmax over those topk logits;
+ *   h_j    = SwiGLU(gate_up_j(x[b])) with the gate the FIRST half [PR694
+ *            commit "The accumulation loop treated a zero activation"];
+ *   out[b] = sum_j w_j * down_j(h_j) + sigmoid(g . x[b]) * shared(x[b]),
+ *            the sum over j in slot order, the shared expert int8 w8a16.
+ * K is uniform per projection across experts (one code tensor per layer and
+ * projection [PR694 commit "Converted the real 12.30 GB checkpoint"]).
+ * Pointers of an absent shared expert may be null when sh_inter == 0. */
+typedef struct escha_moe_layer {
+    int hidden;    /* multiple of 256 */
+    int inter;     /* routed expert intermediate size, multiple of 128 */
+    int n_experts; /* 1..256 */
+    int topk;      /* 1..8, <= n_experts */
+    const uint16_t* router_w; /* fp16 [E][hidden] */
+    /* routed experts, gate_up: in = hidden, out = 2*inter */
+    const uint16_t* gu_codes; /* [E][hidden/16][2*inter/16][16*gu_K] */
+    int gu_K;
+    const uint16_t* gu_rin;  /* fp16 [E][hidden] */
+    const uint16_t* gu_rout; /* fp16 [E][2*inter] (prune mask as zeros) */
+    /* routed experts, down: in = inter, out = hidden */
+    const uint16_t* dn_codes; /* [E][inter/16][hidden/16][16*dn_K] */
+    int dn_K;
+    const uint16_t* dn_rin;  /* fp16 [E][inter] */
+    const uint16_t* dn_rout; /* fp16 [E][hidden] */
+    /* shared expert (int8 w8a16, dequant = f32 scale * w8 per row [MLX]) */
+    int sh_inter; /* 0 = no shared expert; else multiple of 16 */
+    const int8_t* sh_gu_w8; /* [2*sh_inter][hidden] */
+    const float* sh_gu_scale; /* [2*sh_inter] */
+    const int8_t* sh_dn_w8; /* [hidden][sh_inter] */
+    const float* sh_dn_scale; /* [hidden] */
+    const uint16_t* sh_gate;  /* fp16 [hidden], sigmoid gate of the shared expert */
+} escha_moe_layer;
+
+/*   x       fp16 [T][hidden];  T >= 1
+ *   out     f32 [T][hidden] output
+ *   ids_out int32 [T][topk] output, may be null
+ *   w_out   f32 [T][topk] output, may be null
+ *   ws      escha_moe_block_workspace(L, T) bytes */
+size_t escha_moe_block_workspace(const escha_moe_layer* L, int T);
+int escha_moe_block(const escha_moe_layer* L, const uint16_t* x, int T, float* out, int32_t* ids_out, float* w_out,
+                    void* ws, size_t ws_bytes, void* stream);
+
+/* Measurement export: escha_moe_block that also records six caller-created
+ * CUDA events (cudaEvent_t, any of them may be null) on `stream`: events[0]
+ * before the router, [1] after the router, [2] after gate_up, [3] after
+ * down, [4] after the shared expert, [5] after the combine. Same results and
+ * errors as escha_moe_block. */
+int escha_moe_block_timed(const escha_moe_layer* L, const uint16_t* x, int T, float* out, int32_t* ids_out,
+                          float* w_out, void* ws, size_t ws_bytes, void* stream, void* const* events);
+
+/* ---- int8 w8a16 ----------------------------------------------------------
+ * y[m][o] = sum_i (scale[o] * W[o][i]) * x[m][i], f32 output, with the int8
+ * weights used as stored (no dequantised copy) [MTPLX PR #242 "serve Qwen3.6-35B-A3B-Escha-W2 natively", table
+ * "Improvements": int8 non-experts, fused matvec, no dequant at load; MLX
+ * "Exactness of every tensor": dequant = f32 scale*w8]. M == 1 runs the matvec;
+ * M > 1 runs the GEMM path.
+ *   W      int8 [N][Kin];  scales f32 [N]
+ *   N      >= 1;  Kin multiple of 16
+ *   x      [M][Kin], x_dtype ESCHA_BF16, ESCHA_F16 or ESCHA_F32
+ *   y      f32 [M][N] output */
+size_t int8_w8a16_workspace(int N, int Kin, int M);
+int int8_w8a16_matvec(const int8_t* W, const float* scales, int N, int Kin, const void* x, int x_dtype, int M,
+                      float* y, void* ws, size_t ws_bytes, void* stream);
+
+/* Diagnostic export: out[o][i] = fl32(scale[o] * W[o][i]) (one IEEE f32
+ * multiply), for the bit-exact dequant check. Not used by the hot path. */
+int int8_w8a16_dequant(const int8_t* W, const float* scales, int N, int Kin, float* out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ESCHA_H */

@@ -1,0 +1,143 @@
+"""Host-side checks of the C ABI (no GPU work): the library builds and loads,
+exports every function include/escha.h declares, and rejects bad arguments
+with the documented status codes before touching the device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "escha.h")
+
+
+def _lib():
+    from bit_trellis_quantized_gb300 import native
+
+    if not os.path.exists(native.LIB_PATH):
+        from bit_trellis_quantized_gb300 import build
+
+        build.build()
+    return native, native.lib()
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w]*\s*\**\s*([a-z][a-z0-9_]+)\s*\(", src, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "sizeof")))
+
+
+def test_header_declarations_are_exported():
+    native, _ = _lib()
+    declared = _declared_functions()
+    assert "escha_trellis_gemv" in declared and "escha_moe_block" in declared and "int8_w8a16_matvec" in declared
+    out = subprocess.run(["nm", "-D", "--defined-only", native.LIB_PATH], capture_output=True, text=True, check=True)
+    exported = set(line.split()[-1] for line in out.stdout.splitlines() if line.strip())
+    missing = [n for n in declared if n not in exported]
+    assert not missing, f"declared but not exported: {missing}"
+    assert sorted(native.EXPORTS) == declared
+
+
+def test_struct_layout_matches_header():
+    native, _ = _lib()
+    # 4 ints, 1 pointer, (pointer, int, pointer, pointer) x 2, int + 5 pointers, natural alignment
+    assert ctypes.sizeof(native.EschaMoeLayer) == 136
+
+
+def test_version():
+    _, L = _lib()
+    assert L.escha_version() >= 100
+
+
+def _fake_ptr(v):
+    return ctypes.c_void_p(v)
+
+
+def test_gemv_argument_validation_before_launch():
+    native, L = _lib()
+    good = 0x10000
+    args = dict(codes=good, inn=256, out=256, K=2, x=good, xd=native.ESCHA_F16, batch=1, rin=good, rout=good, y=good)
+
+    def call(**kw):
+        a = dict(args)
+        a.update(kw)
+        return L.escha_trellis_gemv(a["codes"], a["inn"], a["out"], a["K"], a["x"], a["xd"], a["batch"], a["rin"],
+                                    a["rout"], a["y"], None, 0, None)
+
+    assert call(K=4) == native.ESCHA_E_K
+    assert call(K=1) == native.ESCHA_E_K
+    assert call(inn=200) == native.ESCHA_E_SHAPE
+    assert call(out=16) == native.ESCHA_E_SHAPE
+    assert call(inn=0) == native.ESCHA_E_SHAPE
+    assert call(codes=None) == native.ESCHA_E_ARG
+    assert call(y=None) == native.ESCHA_E_ARG
+    assert call(xd=7) == native.ESCHA_E_ARG
+    assert call(batch=0) == native.ESCHA_E_ARG
+    assert call(codes=good + 8) == native.ESCHA_E_ALIGN
+    assert call(x=good + 2) == native.ESCHA_E_ALIGN
+    assert b"K=4" in L.escha_last_error() or True
+    call(K=4)
+    assert b"K=4" in L.escha_last_error()
+
+
+def test_decode_validation():
+    native, L = _lib()
+    g = 0x10000
+    assert L.escha_trellis_decode(g, 32, 32, 5, g, None) == native.ESCHA_E_K
+    assert L.escha_trellis_decode(g, 24, 32, 2, g, None) == native.ESCHA_E_SHAPE
+    assert L.escha_trellis_decode(None, 32, 32, 2, g, None) == native.ESCHA_E_ARG
+    assert L.escha_trellis_decode(g, 32, 32, 2, None, None) == native.ESCHA_E_ARG
+
+
+def test_int8_validation():
+    native, L = _lib()
+    g = 0x10000
+    f = L.int8_w8a16_matvec
+    assert f(None, g, 16, 32, g, native.ESCHA_BF16, 1, g, None, 0, None) == native.ESCHA_E_ARG
+    assert f(g, g, 16, 30, g, native.ESCHA_BF16, 1, g, None, 0, None) == native.ESCHA_E_SHAPE
+    assert f(g, g, 0, 32, g, native.ESCHA_BF16, 1, g, None, 0, None) == native.ESCHA_E_ARG
+    assert f(g, g, 16, 32, g, 9, 1, g, None, 0, None) == native.ESCHA_E_ARG
+    assert f(g + 4, g, 16, 32, g, native.ESCHA_BF16, 1, g, None, 0, None) == native.ESCHA_E_ALIGN
+
+
+def test_moe_validation_and_workspace():
+    native, L = _lib()
+    g = 0x10000
+    lay = native.EschaMoeLayer()
+    lay.hidden, lay.inter, lay.n_experts, lay.topk = 2048, 512, 256, 8
+    for f in ("router_w", "gu_codes", "gu_rin", "gu_rout", "dn_codes", "dn_rin", "dn_rout"):
+        setattr(lay, f, g)
+    lay.gu_K, lay.dn_K = 3, 2
+    lay.sh_inter = 0
+    need = L.escha_moe_block_workspace(ctypes.byref(lay), 1)
+    assert need > 0
+    assert L.escha_moe_block_workspace(ctypes.byref(lay), 64) > need
+    call = lambda ws_bytes, **kw: L.escha_moe_block(ctypes.byref(lay), g, 1, g, None, None, g, ws_bytes, None)
+    assert call(need - 1) == native.ESCHA_E_WORKSPACE
+    lay.gu_K = 4
+    assert call(need) == native.ESCHA_E_K
+    lay.gu_K = 3
+    lay.topk = 9
+    assert call(need) == native.ESCHA_E_SHAPE
+    lay.topk = 8
+    lay.hidden = 2000
+    assert call(need) == native.ESCHA_E_SHAPE
+    lay.hidden = 2048
+    lay.router_w = None
+    assert call(need) == native.ESCHA_E_ARG
+    lay.router_w = g
+    lay.sh_inter = 512
+    assert call(need) == native.ESCHA_E_ARG  # shared-expert pointers missing
+    assert L.escha_moe_block(None, g, 1, g, None, None, g, need, None) == native.ESCHA_E_ARG
+
+
+def test_product_path_has_no_oracle_import():
+    pkg = os.path.join(ROOT, "bit_trellis_quantized_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in src.replace("the oracle", ""), f"{f} mentions the oracle"

@@ -1,0 +1,66 @@
+"""GPU parity of the int8 w8a16 path against the CPU oracle (C ABI)."""
+import numpy as np
+import pytest
+
+from escha_synth import gen
+from gpu_common import TOL, dev, rel_err_rows
+from oracle import escha_oracle as o
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def native():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_trellis_quantized_gb300 import native as n
+
+    n.lib()
+    return n
+
+
+def _bf16_tensor(bits):
+    return dev(bits.view(np.int16)).view(torch.bfloat16)
+
+
+def _bf16_values(bits):
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def test_dequant_bit_exact(native):
+    W = np.tile(np.arange(-128, 128, dtype=np.int8), (64, 4))
+    s = gen.rng(1).uniform(1e-3, 1e-2, 64).astype(np.float32)
+    got = native.int8_w8a16_dequant(dev(W), dev(s)).cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), o.int8_dequant(W, s).view(np.uint32))
+
+
+@pytest.mark.parametrize("N,Kin,M", [(4096, 2048, 1), (2048, 4096, 1), (1000, 528, 3), (256, 2048, 8), (300, 1024, 11)])
+def test_matvec_bf16(native, N, Kin, M):
+    W, s = gen.int8_matrix(N + Kin, N, Kin)
+    xb = gen.bf16_normal_bits(gen.rng(M), (M, Kin))
+    y = native.int8_w8a16_matvec(dev(W), dev(s), _bf16_tensor(xb)).cpu().numpy()
+    ref = o.int8_matvec(W, s, _bf16_values(xb))
+    assert rel_err_rows(y, ref).max() <= TOL
+
+
+def test_matvec_f16_and_f32(native):
+    W, s = gen.int8_matrix(9, 512, 1024)
+    x16 = gen.fp16_normal(gen.rng(2), (2, 1024))
+    ref = o.int8_matvec(W, s, x16.astype(np.float64))
+    assert rel_err_rows(native.int8_w8a16_matvec(dev(W), dev(s), dev(x16)).cpu().numpy(), ref).max() <= TOL
+    x32 = x16.astype(np.float32)
+    assert rel_err_rows(native.int8_w8a16_matvec(dev(W), dev(s), dev(x32)).cpu().numpy(), ref).max() <= TOL
+
+
+def test_matvec_lm_head_shape_sampled_rows(native):
+    """152064 x 2048 output-head shape at batch 1; the oracle checks a sample
+    of 512 rows one by one."""
+    N, Kin = 152064, 2048
+    W, s = gen.int8_matrix(4003, N, Kin)
+    xb = gen.bf16_normal_bits(gen.rng(4), (1, Kin))
+    y = native.int8_w8a16_matvec(dev(W), dev(s), _bf16_tensor(xb)).cpu().numpy()[0]
+    rows = gen.rng(5).choice(N, size=512, replace=False)
+    ref = o.int8_matvec(W[rows], s[rows], _bf16_values(xb))[0]
+    full_scale = np.abs(y).max()
+    assert np.max(np.abs(y[rows] - ref)) / full_scale <= TOL
