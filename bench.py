@@ -10,9 +10,10 @@ GEMVs for gate_up and down, output transforms, SwiGLU, the int8 shared expert
 and the combine, all in the library's kernels behind the C ABI, replayed from
 a CUDA graph.
 
-L2: the 129 MB L2 is flushed (a 512 MB buffer is written) before every timed
-step, outside the step's CUDA events, so every step reads its weights from
-HBM.
+L2: inputs larger than L2. The benchmark cycles through 24 distinct layers of
+this shape (about 6.5 GB of weights), one layer per step, so a step's weights
+were last touched 23 steps (hundreds of MB of other traffic) earlier and come
+from HBM, while the kernels' code stays cached as it would in a model.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Prints one JSON line (rank 0).
@@ -47,8 +48,8 @@ X_SEED = 2002
 HIDDEN, INTER, E, TOPK = 2048, 512, 256, 8
 GU_CODE_BYTES = HIDDEN * 2 * INTER * 3 // 8  # per expert: 786,432
 DN_CODE_BYTES = INTER * HIDDEN * 2 // 8  # per expert: 262,144
-FLUSH_BYTES = 512 << 20
-KERNELS_PER_STEP = 7  # router logits, top-k, gate_up GEMV, down GEMV, shared gate_up, shared down, combine
+N_LAYERS = 24
+KERNELS_PER_STEP = 3  # router (+shared gate_up), gate_up (+top-k, shared down), down (+top-k, combine)
 
 
 def peaks():
@@ -178,6 +179,7 @@ def run_ours(args, ws, rank, local):
     import torch
 
     from bit_trellis_quantized_gb300 import native
+    from escha_synth.gen_torch import moe_layer_device
 
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU")
@@ -195,120 +197,125 @@ def run_ours(args, ws, rank, local):
             pg.barrier()
         torch.cuda.synchronize()
 
-    d = gen.moe_layer(LAYER_SEED)
-    block = native.MoeBlock(d, device=dev, topk=TOPK)
+    # NL distinct layers (~272 MB each): a step's weights were last touched
+    # NL-1 steps earlier, far more than L2 holds, so they come from HBM.
+    blocks = [native.MoeBlock(moe_layer_device(LAYER_SEED + 1000 * rank + l, dev), device=dev, topk=TOPK)
+              for l in range(N_LAYERS)]
     n_total = args.warmup + args.steps
     xs_host = torch.from_numpy(gen.fp16_normal(gen.rng(X_SEED + 100 * rank), (n_total, HIDDEN))).pin_memory()
     xs = xs_host.to(dev)
-    x_buf = torch.empty((1, HIDDEN), dtype=torch.float16, device=dev)
-    out_buf = torch.empty((1, HIDDEN), dtype=torch.float32, device=dev)
-    ids_buf = torch.empty((1, TOPK), dtype=torch.int32, device=dev)
-    w_buf = torch.empty((1, TOPK), dtype=torch.float32, device=dev)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    outs = torch.empty((n_total, HIDDEN), dtype=torch.float32, device=dev)
+    ids_all = torch.empty((n_total, TOPK), dtype=torch.int32, device=dev)
+    w_all = torch.empty((n_total, TOPK), dtype=torch.float32, device=dev)
+    layer_of = [i % N_LAYERS for i in range(n_total)]
 
     stream = torch.cuda.Stream(device=dev)
+    graphs = []
     with torch.cuda.stream(stream):
-        x_buf.copy_(xs[0:1])
-        block(x_buf, out=out_buf, ids=ids_buf, w=w_buf)
+        for blk in blocks:  # workspaces sized and kernels loaded before capture
+            blk(xs[0:1], out=outs[0:1], ids=ids_all[0:1], w=w_all[0:1])
         torch.cuda.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            block(x_buf, out=out_buf, ids=ids_buf, w=w_buf)
+        for i in range(n_total):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                blocks[layer_of[i]](xs[i:i + 1], out=outs[i:i + 1], ids=ids_all[i:i + 1], w=w_all[i:i + 1])
+            graphs.append(g)
     torch.cuda.synchronize()
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_total)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n_total)]
-    ids_seen = []
     with ClockSampler(local) as clk:
-        # device-resident inputs: x already in HBM when the step's events start
+        # device-resident inputs: x already in HBM when the timed region starts
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
+            for i in range(args.warmup):
+                graphs[i].replay()
             barrier()
-            for i in range(n_total):
-                x_buf.copy_(xs[i:i + 1])
-                flush.zero_()
-                starts[i].record(stream)
-                graph.replay()
-                ends[i].record(stream)
-                if i < 16:
-                    ids_seen.append(ids_buf.clone())
+            t0.record(stream)
+            for i in range(args.warmup, n_total):
+                graphs[i].replay()
+            t1.record(stream)
             barrier()
-        step_ms = [starts[i].elapsed_time(ends[i]) for i in range(args.warmup, n_total)]
+        step_ms = t0.elapsed_time(t1) / args.steps
 
         # end to end through the public API: pinned host x in, out back to host
         out_host = torch.empty((n_total, HIDDEN), dtype=torch.float32).pin_memory()
-        e_s = [torch.cuda.Event(enable_timing=True) for _ in range(n_total)]
-        e_e = [torch.cuda.Event(enable_timing=True) for _ in range(n_total)]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
+            for i in range(args.warmup):
+                graphs[i].replay()
             barrier()
-            for i in range(n_total):
-                flush.zero_()
-                e_s[i].record(stream)
-                x_buf.copy_(xs_host[i:i + 1], non_blocking=True)
-                graph.replay()
-                out_host[i:i + 1].copy_(out_buf, non_blocking=True)
-                e_e[i].record(stream)
+            e0.record(stream)
+            for i in range(args.warmup, n_total):
+                xs[i:i + 1].copy_(xs_host[i:i + 1], non_blocking=True)
+                graphs[i].replay()
+                out_host[i:i + 1].copy_(outs[i:i + 1], non_blocking=True)
+            e1.record(stream)
             barrier()
-        e2e_ms = [e_s[i].elapsed_time(e_e[i]) for i in range(args.warmup, n_total)]
+        e2e_ms = e0.elapsed_time(e1) / args.steps
 
-        # dominant kernel (gate_up trellis GEMV over the 8 routed experts),
-        # timed live by events on its own stream around its launch
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n_total)]
+        # per-kernel durations, timed live by events on the launch stream
+        # around each kernel (the events serialise the three kernels)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_total)]
         with torch.cuda.stream(stream):
             for row in evs:  # torch creates the CUDA events lazily, at their first record
                 for e in row:
                     e.record(stream)
             torch.cuda.synchronize()
-            handles = [(native.ctypes.c_void_p * 6)(*[e.cuda_event for e in row]) for row in evs]
-            ws_t = block.workspace(1)
-            lay = native.ctypes.byref(block.layer)
+            handles = [(native.ctypes.c_void_p * 4)(*[e.cuda_event for e in row]) for row in evs]
             barrier()
             for i in range(n_total):
-                x_buf.copy_(xs[i:i + 1])
-                flush.zero_()
+                blk = blocks[layer_of[i]]
+                ws_t = blk.workspace(1)
                 native.check(native.lib().escha_moe_block_timed(
-                    lay, native.ptr(x_buf), 1, native.ptr(out_buf), native.ptr(ids_buf), native.ptr(w_buf),
-                    native.ptr(ws_t), ws_t.numel(), stream.cuda_stream, handles[i]))
+                    native.ctypes.byref(blk.layer), native.ptr(xs[i:i + 1]), 1, native.ptr(outs[i:i + 1]),
+                    native.ptr(ids_all[i:i + 1]), native.ptr(w_all[i:i + 1]), native.ptr(ws_t), ws_t.numel(),
+                    stream.cuda_stream, handles[i]))
             barrier()
-        phase = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(5)]
+        phase = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(3)]
                           for i in range(args.warmup, n_total)])
     clocks = clk.summary()
 
     # max over ranks
-    t_step = float(np.mean(step_ms))
-    t_e2e = float(np.mean(e2e_ms))
+    t_step, t_e2e = float(step_ms), float(e2e_ms)
     if pg is not None:
         tt = torch.tensor([t_step, t_e2e], device=dev)
         pg.all_reduce(tt, op=pg.ReduceOp.MAX)
         t_step, t_e2e = float(tt[0]), float(tt[1])
     if rank != 0:
+        if pg is not None:
+            pg.destroy_process_group()
         return
 
     hbm, tflops, src = peaks()
-    ph = phase.mean(axis=0)  # router, gate_up, down, shared, combine (ms)
+    ph = phase.mean(axis=0)  # router (+shared gate_up), gate_up (+shared down), down (+combine) (ms)
     gu_ms = float(ph[1])
-    gu_bytes = TOPK * (GU_CODE_BYTES + HIDDEN * 2 + 2 * INTER * 2) + HIDDEN * 2 + TOPK * 2 * INTER * 4
+    # gate_up kernel. Routed: codes + rin + rout per expert, x once, the
+    # token's logits, gate_up outputs. Shared expert down rows: int8 weights +
+    # scales, its gate_up input and gate, its output.
+    gu_bytes = (TOPK * (GU_CODE_BYTES + HIDDEN * 2 + 2 * INTER * 2) + HIDDEN * 2 + E * 2 + TOPK * 2 * INTER * 4
+                + HIDDEN * INTER + HIDDEN * 4 + 2 * INTER * 4 + 4 + HIDDEN * 4)
     achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
     routed_code_bytes = TOPK * (GU_CODE_BYTES + DN_CODE_BYTES)
-    distinct = len({tuple(t.cpu().numpy().ravel()) for t in ids_seen})
+    distinct = len({tuple(r) for r in ids_all[args.warmup:args.warmup + 16].cpu().numpy().tolist()})
     line = {
         "metric": METRIC, "value": ws * 1e3 / t_step, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp16 weights / f32 accumulate", "data": "synthetic",
         "config": {"workload": WORKLOAD, "batch": 1, "tokens_per_step_per_gpu": 1,
-                   "l2": "flushed before every timed step (512 MB write outside the step's events)",
+                   "l2": f"inputs larger than L2: {N_LAYERS} distinct MoE layers "
+                         f"({N_LAYERS * 272} MB) cycled, one per step, no flush",
                    "cuda_graph": True, "parallelism": f"replicas x{ws} (independent token streams)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": None, "kernel": "trellis_gemv_kernel<K=3> (gate_up, 8 routed experts)",
+                     "traffic": None, "kernel": "moe_gate_up_kernel<K=3> (8 routed experts + int8 shared-expert down rows)",
                      "algorithmic_bytes_per_launch": gu_bytes, "ms_per_launch": gu_ms, "peak_source": src},
         "packed_expert_gbs": routed_code_bytes / (t_step * 1e-3) / 1e9,
         "packed_expert_frac": routed_code_bytes / (t_step * 1e-3) / 1e9 / hbm,
-        "phase_ms": {"router": float(ph[0]), "gate_up": float(ph[1]), "down": float(ph[2]),
-                     "shared": float(ph[3]), "combine": float(ph[4])},
+        "phase_ms": {"router+shared_gate_up": float(ph[0]), "gate_up+shared_down": float(ph[1]),
+                     "down+combine": float(ph[2])},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "e2e": {"value": ws * 1e3 / t_e2e, "unit": UNIT, "h2d_bytes_per_step": HIDDEN * 2,
                 "d2h_bytes_per_step": HIDDEN * 4},
         "clocks": clocks,
-        "routing_distinct_in_first_16_steps": distinct,
+        "routing_distinct_in_16_steps": distinct,
     }
     if ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
@@ -320,7 +327,7 @@ def run_ours(args, ws, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")

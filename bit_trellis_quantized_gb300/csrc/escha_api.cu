@@ -76,15 +76,17 @@ int check_trellis(const uint16_t* codes, int in, int out, int K, int mult, const
     return ESCHA_OK;
 }
 
-// Workspace layout of escha_moe_block.
+// Workspace layout of escha_moe_block (256-byte aligned regions).
 struct MoeWs {
-    size_t logits, ids, w, ygu, d, shgu, sh, total;
+    size_t err, logits, ids, w, ygu, shgu, shgate, sh, total;
 };
 
 MoeWs moe_ws_layout(const escha_moe_layer* L, int T) {
     MoeWs m{};
     size_t off = 0;
     const size_t slots = (size_t)T * L->topk;
+    m.err = off;
+    off += 256;
     m.logits = off;
     off += align_up((size_t)T * L->n_experts * 2);
     m.ids = off;
@@ -93,10 +95,10 @@ MoeWs moe_ws_layout(const escha_moe_layer* L, int T) {
     off += align_up(slots * 4);
     m.ygu = off;
     off += align_up(slots * 2 * (size_t)L->inter * 4);
-    m.d = off;
-    off += align_up(slots * (size_t)L->hidden * 4);
     m.shgu = off;
     off += align_up((size_t)T * 2 * (size_t)L->sh_inter * 4);
+    m.shgate = off;
+    off += align_up((size_t)T * 4);
     m.sh = off;
     off += align_up(L->sh_inter > 0 ? (size_t)T * L->hidden * 4 : 0);
     m.total = off;
@@ -106,9 +108,9 @@ MoeWs moe_ws_layout(const escha_moe_layer* L, int T) {
 int check_layer(const escha_moe_layer* L) {
     if (!L) return fail(ESCHA_E_ARG, "moe_block: layer is null");
     if (L->hidden <= 0 || L->hidden % 256) return fail(ESCHA_E_SHAPE, "moe_block: hidden=%d must be a multiple of 256", L->hidden);
-    if (L->hidden > 65536) return fail(ESCHA_E_SHAPE, "moe_block: hidden=%d above 65536", L->hidden);
-    if (L->inter <= 0 || L->inter % 128 || L->inter > 32768)
-        return fail(ESCHA_E_SHAPE, "moe_block: inter=%d must be a multiple of 128 (<= 32768)", L->inter);
+    if (L->hidden > 8192) return fail(ESCHA_E_SHAPE, "moe_block: hidden=%d above 8192", L->hidden);
+    if (L->inter <= 0 || L->inter % 128 || L->inter > 8192)
+        return fail(ESCHA_E_SHAPE, "moe_block: inter=%d must be a multiple of 128 (<= 8192)", L->inter);
     if (L->n_experts < 1 || L->n_experts > 256) return fail(ESCHA_E_SHAPE, "moe_block: n_experts=%d not in 1..256", L->n_experts);
     if (L->topk < 1 || L->topk > 8 || L->topk > L->n_experts)
         return fail(ESCHA_E_SHAPE, "moe_block: topk=%d not in 1..min(8, n_experts)", L->topk);
@@ -128,8 +130,7 @@ int check_layer(const escha_moe_layer* L) {
         const void* sp[] = {L->sh_gu_w8, L->sh_gu_scale, L->sh_dn_w8, L->sh_dn_scale, L->sh_gate};
         for (const void* p : sp)
             if (!aligned16(p)) return fail(ESCHA_E_ALIGN, "moe_block: a shared-expert pointer is not 16-byte aligned");
-        if (2 * L->sh_inter * 4 > 200 * 1024 || L->hidden * 4 > 200 * 1024)
-            return fail(ESCHA_E_SHAPE, "moe_block: shared expert too large for the int8 GEMV");
+        if (L->sh_inter > 8192) return fail(ESCHA_E_SHAPE, "moe_block: sh_inter=%d above 8192", L->sh_inter);
     }
     return ESCHA_OK;
 }
@@ -179,7 +180,6 @@ int escha_trellis_gemv(const uint16_t* codes, int in, int out, int K, const void
     if ((r = device_check(&sms))) return r;
     escha::GemvArgs a{};
     a.codes = codes;
-    a.code_stride = 0;
     a.in = in;
     a.out = out;
     a.x_mode = x_dtype == ESCHA_F16 ? escha::kXmF16 : escha::kXmF32;
@@ -190,8 +190,6 @@ int escha_trellis_gemv(const uint16_t* codes, int in, int out, int K, const void
     a.y = y;
     a.y_stride = out;
     a.batch = batch;
-    a.slot_mode = 0;
-    a.x_div = 1;
     const int nb = batch == 1 ? 1 : batch == 2 ? 2 : 4;
     const int items = (batch + nb - 1) / nb;
     return cuda_status(escha::launch_trellis_gemv(a, K, nb, items, sms, static_cast<cudaStream_t>(stream)),
@@ -228,77 +226,45 @@ int moe_block_impl(const escha_moe_layer* L, const uint16_t* x, int T, float* ou
     if ((r = device_check(&sms))) return r;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char* base = static_cast<char*>(ws);
-    uint16_t* logits = reinterpret_cast<uint16_t*>(base + m.logits);
-    int32_t* ids = ids_out ? ids_out : reinterpret_cast<int32_t*>(base + m.ids);
-    float* w = w_out ? w_out : reinterpret_cast<float*>(base + m.w);
-    float* ygu = reinterpret_cast<float*>(base + m.ygu);
-    float* d = reinterpret_cast<float*>(base + m.d);
-    float* shgu = reinterpret_cast<float*>(base + m.shgu);
-    float* sh = L->sh_inter > 0 ? reinterpret_cast<float*>(base + m.sh) : nullptr;
-    const int slots = T * L->topk;
+    escha::MoeArgs a{};
+    a.T = T;
+    a.hidden = L->hidden;
+    a.inter = L->inter;
+    a.E = L->n_experts;
+    a.topk = L->topk;
+    a.sh_inter = L->sh_inter;
+    a.x = x;
+    a.router_w = L->router_w;
+    a.gu_codes = L->gu_codes;
+    a.gu_K = L->gu_K;
+    a.gu_rin = L->gu_rin;
+    a.gu_rout = L->gu_rout;
+    a.dn_codes = L->dn_codes;
+    a.dn_K = L->dn_K;
+    a.dn_rin = L->dn_rin;
+    a.dn_rout = L->dn_rout;
+    a.sh_gu_w8 = L->sh_gu_w8;
+    a.sh_gu_scale = L->sh_gu_scale;
+    a.sh_dn_w8 = L->sh_dn_w8;
+    a.sh_dn_scale = L->sh_dn_scale;
+    a.sh_gate = L->sh_gate;
+    a.out = out;
+    a.ids = ids_out ? ids_out : reinterpret_cast<int32_t*>(base + m.ids);
+    a.w = w_out ? w_out : reinterpret_cast<float*>(base + m.w);
+    a.logits = reinterpret_cast<uint16_t*>(base + m.logits);
+    a.ygu = reinterpret_cast<float*>(base + m.ygu);
+    a.shgu = reinterpret_cast<float*>(base + m.shgu);
+    a.shgate = reinterpret_cast<float*>(base + m.shgate);
+    a.sh = reinterpret_cast<float*>(base + m.sh);
+    a.err = reinterpret_cast<int*>(base + m.err);
 
     if ((r = record(ev, 0, s))) return r;
-    if ((r = cuda_status(escha::launch_router(x, L->router_w, T, L->hidden, L->n_experts, L->topk, logits, ids, w,
-                                              nullptr, s),
-                         "router launch")))
-        return r;
+    if ((r = cuda_status(escha::launch_moe_router(a, s), "router launch"))) return r;
     if ((r = record(ev, 1, s))) return r;
-
-    escha::GemvArgs g{};
-    g.codes = L->gu_codes;
-    g.code_stride = (long long)(L->hidden / 16) * (2 * L->inter / 16) * (16 * L->gu_K);
-    g.in = L->hidden;
-    g.out = 2 * L->inter;
-    g.x_mode = escha::kXmF16;
-    g.x = x;
-    g.x_stride = L->hidden;
-    g.rin = L->gu_rin;
-    g.rin_stride = L->hidden;
-    g.rout = L->gu_rout;
-    g.rout_stride = 2 * L->inter;
-    g.y = ygu;
-    g.y_stride = 2 * L->inter;
-    g.ids = ids;
-    g.x_div = L->topk;
-    g.slot_mode = 1;
-    if ((r = cuda_status(escha::launch_trellis_gemv(g, L->gu_K, 1, slots, sms, s), "gate_up launch"))) return r;
+    if ((r = cuda_status(escha::launch_moe_gate_up(a, sms, s), "gate_up launch"))) return r;
     if ((r = record(ev, 2, s))) return r;
-
-    escha::GemvArgs dn{};
-    dn.codes = L->dn_codes;
-    dn.code_stride = (long long)(L->inter / 16) * (L->hidden / 16) * (16 * L->dn_K);
-    dn.in = L->inter;
-    dn.out = L->hidden;
-    dn.x_mode = escha::kXmSwiglu;
-    dn.x = ygu;
-    dn.x_stride = 2 * L->inter;
-    dn.rin = L->dn_rin;
-    dn.rin_stride = L->inter;
-    dn.rout = L->dn_rout;
-    dn.rout_stride = L->hidden;
-    dn.y = d;
-    dn.y_stride = L->hidden;
-    dn.ids = ids;
-    dn.x_div = 1;
-    dn.slot_mode = 1;
-    if ((r = cuda_status(escha::launch_trellis_gemv(dn, L->dn_K, 1, slots, sms, s), "down launch"))) return r;
-    if ((r = record(ev, 3, s))) return r;
-
-    if (L->sh_inter > 0) {
-        if ((r = cuda_status(escha::launch_int8_gemv(L->sh_gu_w8, L->sh_gu_scale, 2 * L->sh_inter, L->hidden, x,
-                                                     ESCHA_F16, L->hidden, 0, T, shgu, 2 * L->sh_inter, sms, s),
-                             "shared gate_up launch")))
-            return r;
-        if ((r = cuda_status(escha::launch_int8_gemv(L->sh_dn_w8, L->sh_dn_scale, L->hidden, L->sh_inter, shgu,
-                                                     ESCHA_F32, 2 * L->sh_inter, 1, T, sh, L->hidden, sms, s),
-                             "shared down launch")))
-            return r;
-    }
-    if ((r = record(ev, 4, s))) return r;
-    if ((r = cuda_status(escha::launch_moe_combine(d, w, T, L->topk, L->hidden, sh, L->sh_gate, x, out, s),
-                         "combine launch")))
-        return r;
-    return record(ev, 5, s);
+    if ((r = cuda_status(escha::launch_moe_down(a, s), "down/combine launch"))) return r;
+    return record(ev, 3, s);
 }
 
 }  // namespace
@@ -312,8 +278,8 @@ int escha_moe_block(const escha_moe_layer* L, const uint16_t* x, int T, float* o
 
 int escha_moe_block_timed(const escha_moe_layer* L, const uint16_t* x, int T, float* out, int32_t* ids_out,
                           float* w_out, void* ws, size_t ws_bytes, void* stream, void* const* events) {
-    cudaEvent_t ev[6];
-    for (int i = 0; i < 6; ++i) ev[i] = events ? static_cast<cudaEvent_t>(events[i]) : nullptr;
+    cudaEvent_t ev[4];
+    for (int i = 0; i < 4; ++i) ev[i] = events ? static_cast<cudaEvent_t>(events[i]) : nullptr;
     return moe_block_impl(L, x, T, out, ids_out, w_out, ws, ws_bytes, stream, ev);
 }
 

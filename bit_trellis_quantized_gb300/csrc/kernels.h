@@ -8,55 +8,74 @@
 namespace escha {
 
 // Input modes of the trellis GEMV prologue.
-constexpr int kXmF16 = 0;     // x is fp16 [rows][in]
-constexpr int kXmF32 = 1;     // x is f32 [rows][in]
-constexpr int kXmSwiglu = 2;  // x is a gate_up output f32 [rows][2*in]; input = silu(gate) * up
+constexpr int kXmF16 = 0;  // x is fp16 [rows][in]
+constexpr int kXmF32 = 1;  // x is f32 [rows][in]
 
 struct GemvArgs {
-    const uint16_t* codes;  // expert 0's code tensor [in/16][out/16][16K]
-    long long code_stride;  // words between consecutive experts' code tensors
+    const uint16_t* codes;  // code tensor [in/16][out/16][16K]
     int in, out;
     int kt_per_cta;  // filled by the launcher
-    int x_mode;
+    int x_mode;      // kXmF16 or kXmF32
     const void* x;
     long long x_stride;  // elements between x rows
     const uint16_t* rin;
-    long long rin_stride;  // elements between experts
     const uint16_t* rout;
-    long long rout_stride;
     float* y;
     long long y_stride;
-    // items: slot mode (one token per item, expert ids[item], x row item/x_div)
-    // or plain mode (tokens item*NB .. item*NB+NB-1 of `batch`, expert 0)
-    const int32_t* ids;
-    int x_div;
     int batch;
-    int slot_mode;
 };
 
-// Trellis GEMV. nb = tokens per item in plain mode (1, 2 or 4); items = grid z.
+// Trellis GEMV of one projection for `batch` tokens, nb tokens per CTA
+// (1, 2 or 4); items = ceil(batch / nb).
 cudaError_t launch_trellis_gemv(const GemvArgs& a, int K, int nb, int items, int num_sms, cudaStream_t s);
+
+// Input-row split of a trellis GEMV: CTAs per cluster and rows per CTA.
+void gemv_plan(int in, int blocks_per_split, int num_sms, int ctas_per_sm, int* kt_per_cta, int* csize);
 
 // Dense decode of a code tensor to fp16 bit patterns W[in][out].
 cudaError_t launch_trellis_decode(const uint16_t* codes, int in, int out, int K, uint16_t* W, cudaStream_t s);
 
-// Router: logits (f16 bits) [T][E], then top-k + softmax. `counter` is a
-// zeroed int in device memory used to elect the CTA that runs the top-k.
-cudaError_t launch_router(const uint16_t* x, const uint16_t* Wg, int T, int hidden, int E, int topk,
-                          uint16_t* logits, int32_t* ids, float* w, unsigned int* counter, cudaStream_t s);
-
-// int8 w8a16 matvec / small-M GEMV: y[m][o] = sum_i (scale[o]*W[o][i]) * x[m][i].
-// x_dtype: 1 = f16, 2 = bf16, 3 = f32; act = 0 plain, 1 SwiGLU of a
-// [M][2*Kin] f32 input (gate first).
+// int8 w8a16 GEMV: y[m][o] = sum_i (scale[o]*W[o][i]) * x[m][i]; x_dtype
+// 1 = f16, 2 = bf16, 3 = f32.
 cudaError_t launch_int8_gemv(const int8_t* W, const float* scales, int N, int Kin, const void* x, int x_dtype,
                              long long x_stride, int act, int M, float* y, long long y_stride, int num_sms,
                              cudaStream_t s);
 
 cudaError_t launch_int8_dequant(const int8_t* W, const float* scales, int N, int Kin, float* out, cudaStream_t s);
 
-// MoE combine: out[t][i] = sum_j w[t][j] * d[t*topk + j][i] + sigmoid(g . x[t]) * sh[t][i]
-// (sh may be null: no shared expert).
-cudaError_t launch_moe_combine(const float* d, const float* w, int T, int topk, int hidden, const float* sh,
-                               const uint16_t* sh_gate, const uint16_t* x, float* out, cudaStream_t s);
+// Everything the three MoE-block kernels read and write.
+struct MoeArgs {
+    int T, hidden, inter, E, topk, sh_inter;
+    const uint16_t* x;         // fp16 [T][hidden]
+    const uint16_t* router_w;  // fp16 [E][hidden]
+    const uint16_t* gu_codes;
+    int gu_K;
+    const uint16_t* gu_rin;
+    const uint16_t* gu_rout;
+    const uint16_t* dn_codes;
+    int dn_K;
+    const uint16_t* dn_rin;
+    const uint16_t* dn_rout;
+    const int8_t* sh_gu_w8;
+    const float* sh_gu_scale;
+    const int8_t* sh_dn_w8;
+    const float* sh_dn_scale;
+    const uint16_t* sh_gate;
+    uint16_t* logits;  // f16 [T][E]
+    float* out;      // [T][hidden]
+    int32_t* ids;    // [T][topk]
+    float* w;        // [T][topk]
+    float* ygu;      // [T*topk][2*inter]
+    float* shgu;     // [T][2*sh_inter]
+    float* shgate;   // [T]
+    float* sh;       // [T][hidden] gated shared-expert output
+    int* err;        // set non-zero if a bounded wait gave up (zeroed by the router kernel)
+    int gu_kt_per_cta;  // filled by the gate_up launcher
+    int dn_ksplit;      // filled by the down launcher
+};
+
+cudaError_t launch_moe_router(const MoeArgs& a, cudaStream_t s);
+cudaError_t launch_moe_gate_up(const MoeArgs& a, int num_sms, cudaStream_t s);
+cudaError_t launch_moe_down(const MoeArgs& a, cudaStream_t s);
 
 }  // namespace escha

@@ -1,0 +1,517 @@
+// One MoE block of an Escha-W2 Qwen3.6-35B-A3B-style layer in three kernels
+// chained by programmatic dependent launch:
+//
+//  1. router + shared gate_up: f16-rounded router logits in a fixed
+//     summation order (hipfire PR #694, commit "Executed the moeblk golden
+//     against real shipped layer-0 weights": logits are rounded to f16
+//     before top-k), one warp per expert spread over many SMs so the 1 MB
+//     router matrix streams in one memory round trip; in the same grid, the
+//     int8 shared expert's gate_up rows and its sigmoid gate, which need no
+//     routing.
+//  2. gate_up: each routed CTA selects its token's top-k (ties to the lower
+//     expert id) and softmax weights with one warp, then runs the expert's
+//     gate_up projection (fused trellis decode GEMV with the input/output
+//     Hadamard transforms and rout); a cluster splits the input rows and
+//     pushes its partial sums into rank 0. Extra CTAs compute the shared
+//     expert's down rows (SwiGLU of its gate_up, times the sigmoid gate).
+//  3. down + combine: one cluster per (token, 128-wide output block), rank
+//     j*ks + h = routed expert j, input split h. Ranks push partials into
+//     rank 0, which finishes each expert (output transform, routing weight),
+//     sums the experts in slot order and adds the shared expert (SwiGLU with
+//     gate = first half: hipfire PR #694, commit "The accumulation loop
+//     treated a zero activation as a no-op").
+#include "kernels.h"
+#include "trellis_core.cuh"
+
+namespace escha {
+
+namespace {
+
+constexpr int kK0Threads = 128;
+constexpr int kK0Warps = kK0Threads / 32;
+constexpr int kLgTG = 8;            // tokens per logits CTA
+constexpr int kShMT = 4;            // tokens per pass of the shared-expert rows
+constexpr int kShRowsPerWarp = 2;   // shared-expert rows per warp
+constexpr int kGuThreads = 256;
+constexpr int kGuWarps = kGuThreads / 32;
+constexpr int kDnThreads = 256;
+constexpr int kDnWarps = kDnThreads / 32;
+constexpr int kMaxCluster = 16;
+
+// ---------------------------------------------------------------------------
+// 1. Router logits + shared expert gate_up.
+// Summation order of a logit (its f16 rounding depends on it): lane l of the
+// expert's warp adds, one at a time in ascending index order, the exact f32
+// products x[i] * Wg[e][i] whose index has floor(i/8) mod 32 == l; the 32
+// partials are combined by the xor butterfly (offsets 16, 8, 4, 2, 1) and
+// rounded to f16 (RNE).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void dot8_f16(const uint4& xv, const uint4& wv, float& acc) {
+    const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
+    const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        acc = fmaf(h2f_bits(static_cast<uint16_t>(xs[k] & 0xFFFFu)), h2f_bits(static_cast<uint16_t>(ws[k] & 0xFFFFu)), acc);
+        acc = fmaf(h2f_bits(static_cast<uint16_t>(xs[k] >> 16)), h2f_bits(static_cast<uint16_t>(ws[k] >> 16)), acc);
+    }
+}
+
+__device__ void router_logits(const MoeArgs& a, int warp, int lane) {
+    const int e = blockIdx.x * kK0Warps + warp;
+    const int t0 = blockIdx.y * kLgTG;
+    const int nt = min(kLgTG, a.T - t0);
+    if (e >= a.E) return;
+    const uint16_t* wrow = a.router_w + (long long)e * a.hidden;
+    const int passes = a.hidden >> 8;
+    float acc[kLgTG];
+#pragma unroll
+    for (int t = 0; t < kLgTG; ++t) acc[t] = 0.f;
+    for (int pg = 0; pg < passes; pg += 8) {
+        uint4 wv[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            if (pg + q < passes) wv[q] = ldg_stream_v4(wrow + (pg + q) * 256 + lane * 8);
+#pragma unroll
+        for (int t = 0; t < kLgTG; ++t) {
+            if (t < nt) {
+                const uint16_t* xrow = a.x + (long long)(t0 + t) * a.hidden;
+                uint4 xv[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (pg + q < passes) xv[q] = __ldg(reinterpret_cast<const uint4*>(xrow + (pg + q) * 256 + lane * 8));
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (pg + q < passes) dot8_f16(xv[q], wv[q], acc[t]);
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < kLgTG; ++t) {
+        if (t < nt) {
+            float v = acc[t];
+#pragma unroll
+            for (int m = 16; m >= 1; m >>= 1) v = v + __shfl_xor_sync(0xffffffffu, v, m);
+            if (lane == 0) a.logits[(long long)(t0 + t) * a.E + e] = __half_as_ushort(__float2half_rn(v));
+        }
+    }
+}
+
+// Shared expert gate_up rows (kShRowsPerWarp per warp) for every token, and
+// in CTA 0 the sigmoid gate (an f32 dot product of the fp16 gate vector with
+// x, not rounded).
+__device__ void shared_gate_up(const MoeArgs& a, int cta, float* xs, int warp, int lane) {
+    const int rows = 2 * a.sh_inter;
+    const int r0 = (cta * kK0Warps + warp) * kShRowsPerWarp;
+    for (int tb = 0; tb < a.T; tb += kShMT) {
+        const int mt = min(kShMT, a.T - tb);
+        __syncthreads();
+        for (int i = threadIdx.x * 8; i < kShMT * a.hidden; i += kK0Threads * 8) {
+            const int t = i / a.hidden, c = i % a.hidden;
+            float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
+            if (t < mt) {
+                const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x + (long long)(tb + t) * a.hidden + c));
+                lo = make_float4(h2f_bits(v.x & 0xFFFFu), h2f_bits(v.x >> 16), h2f_bits(v.y & 0xFFFFu), h2f_bits(v.y >> 16));
+                hi = make_float4(h2f_bits(v.z & 0xFFFFu), h2f_bits(v.z >> 16), h2f_bits(v.w & 0xFFFFu), h2f_bits(v.w >> 16));
+            }
+            *reinterpret_cast<float4*>(xs + i) = lo;
+            *reinterpret_cast<float4*>(xs + i + 4) = hi;
+        }
+        __syncthreads();
+        if (r0 < rows) {
+            float dots[kShRowsPerWarp][kShMT];
+            int8_rows_dot<kShRowsPerWarp, kShMT>(a.sh_gu_w8 + (long long)r0 * a.hidden, a.hidden, rows - r0, a.hidden,
+                                                 xs, a.hidden, lane, dots);
+            if (lane == 0) {
+#pragma unroll
+                for (int r = 0; r < kShRowsPerWarp; ++r) {
+                    if (r0 + r >= rows) break;
+                    const float sc = a.sh_gu_scale[r0 + r];
+                    for (int t = 0; t < mt; ++t) a.shgu[(long long)(tb + t) * rows + r0 + r] = sc * dots[r][t];
+                }
+            }
+        }
+        if (cta == 0 && warp == kK0Warps - 1) {
+            float acc[kShMT] = {};
+#pragma unroll 8
+            for (int i0 = lane * 8; i0 < a.hidden; i0 += 256) {
+                const uint4 gv = __ldg(reinterpret_cast<const uint4*>(a.sh_gate + i0));
+                const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+                for (int t = 0; t < kShMT; ++t) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        acc[t] = fmaf(h2f_bits(static_cast<uint16_t>(gw[k] & 0xFFFFu)), xs[t * a.hidden + i0 + 2 * k], acc[t]);
+                        acc[t] = fmaf(h2f_bits(static_cast<uint16_t>(gw[k] >> 16)), xs[t * a.hidden + i0 + 2 * k + 1], acc[t]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < kShMT; ++t) {
+                float v = acc[t];
+#pragma unroll
+                for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+                if (lane == 0 && t < mt) a.shgate[tb + t] = sigmoid_f(v);
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kK0Threads) moe_router_kernel(const MoeArgs a) {
+    // The gate_up kernel can be scheduled at once; its CTAs wait for this
+    // grid before reading anything it writes.
+    pdl_trigger();
+    extern __shared__ __align__(16) float smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *a.err = 0;  // the whole previous call has finished
+    const int n_lg = (a.E + kK0Warps - 1) / kK0Warps;
+    if (static_cast<int>(blockIdx.x) < n_lg) {
+        router_logits(a, warp, lane);
+    } else if (blockIdx.y == 0) {
+        shared_gate_up(a, blockIdx.x - n_lg, smem, warp, lane);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// 2. gate_up (routed) + shared expert down rows.
+// ---------------------------------------------------------------------------
+template <int K>
+__device__ void gate_up_routed(const MoeArgs& a, float* smem) {
+    const int crank = static_cast<int>(cg::this_cluster().block_rank());
+    const int csize = static_cast<int>(cg::this_cluster().num_blocks());
+    const int ob = blockIdx.y;
+    const int slot = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_out = 2 * a.inter;
+    const int KT = a.hidden >> 4, NT = n_out >> 4;
+    const int kt0 = crank * a.gu_kt_per_cta;
+    const int kt1 = min(KT, kt0 + a.gu_kt_per_cta);
+    const int nk = (kt1 - kt0) * 16;
+    float* slots = smem;                     // [csize][128] partials, on rank 0
+    float* xt = slots + kMaxCluster * 128;   // [gu_kt_per_cta * 16]
+    float* red = xt + a.gu_kt_per_cta * 16;  // [kGuWarps][128] (+128: partial of ranks != 0)
+    __shared__ __align__(8) unsigned long long bar;
+    __shared__ int e_s[8];
+    __shared__ float w_s[8];
+
+    if (crank == 0 && threadIdx.x == 0 && csize > 1) mbar_init(smem_u32(&bar), 32 * (csize - 1));
+    cluster_arrive();  // rank 0's barrier is initialised before anyone arrives on it
+
+    const int t = slot / a.topk;
+    const int j = slot % a.topk;
+    pdl_wait();     // router logits and shared gate_up
+    pdl_trigger();  // logits complete: the down kernel may read them early
+    if (warp == 0) {
+        int e_l;
+        float w_l;
+        topk_softmax_warp(a.logits + (long long)t * a.E, a.E, a.topk, lane, &e_l, &w_l);
+        if (lane < a.topk) {
+            e_s[lane] = e_l;
+            w_s[lane] = w_l;
+            if (crank == 0 && ob == 0 && j == 0) {  // one CTA per token publishes the routing
+                a.ids[(long long)t * a.topk + lane] = e_l;
+                a.w[(long long)t * a.topk + lane] = w_l;
+            }
+        }
+    }
+    __syncthreads();
+    const int e = e_s[j];
+    const uint16_t* codes = a.gu_codes + (long long)e * KT * NT * (16 * K);
+    LaneCodes<K> cur;
+    if (kt0 + warp < kt1) load_lane_codes<K>(cur, codes + ((long long)(kt0 + warp) * NT + ob * 8) * (16 * K), lane);
+
+    // xt = H128(rin_e * x[t]) over this CTA's inputs
+    const uint16_t* rin = a.gu_rin + (long long)e * a.hidden;
+    const uint16_t* xrow = a.x + (long long)t * a.hidden;
+    for (int blk = warp; blk < nk / 128; blk += kGuWarps) {
+        const int ib = kt0 * 16 + blk * 128 + 4 * lane;
+        const uint2 rb = *reinterpret_cast<const uint2*>(rin + ib);
+        const uint2 xb = *reinterpret_cast<const uint2*>(xrow + ib);
+        float v[4];
+        v[0] = h2f_bits(static_cast<uint16_t>(rb.x & 0xFFFFu)) * h2f_bits(static_cast<uint16_t>(xb.x & 0xFFFFu));
+        v[1] = h2f_bits(static_cast<uint16_t>(rb.x >> 16)) * h2f_bits(static_cast<uint16_t>(xb.x >> 16));
+        v[2] = h2f_bits(static_cast<uint16_t>(rb.y & 0xFFFFu)) * h2f_bits(static_cast<uint16_t>(xb.y & 0xFFFFu));
+        v[3] = h2f_bits(static_cast<uint16_t>(rb.y >> 16)) * h2f_bits(static_cast<uint16_t>(xb.y >> 16));
+        h128_warp(v, lane);
+        *reinterpret_cast<float4*>(xt + blk * 128 + 4 * lane) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+    __syncthreads();
+    float* zp = crank == 0 ? slots : red + kGuWarps * 128;  // rank 0 keeps its partial in slot 0
+    cta_gemv_partial<K, 1, kGuWarps>(codes, NT, ob, kt0, kt1, xt, nk, cur, red, zp);
+
+    cluster_wait();
+    if (crank != 0) {
+        if (warp == 0) {
+            const uint32_t dst = cluster_map(smem_u32(slots + crank * 128 + 4 * lane), 0);
+            st_cluster_v4(dst, *reinterpret_cast<const float4*>(zp + 4 * lane));
+            mbar_arrive_cluster(cluster_map(smem_u32(&bar), 0));
+        }
+        return;
+    }
+    if (warp == 0) {
+        if (csize > 1) mbar_wait_bounded(smem_u32(&bar), a.err, 1);
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int r = 0; r < csize; ++r) {
+            const float4 z4 = *reinterpret_cast<const float4*>(slots + r * 128 + 4 * lane);
+            v[0] += z4.x;
+            v[1] += z4.y;
+            v[2] += z4.z;
+            v[3] += z4.w;
+        }
+        output_transform_warp(v, a.gu_rout + (long long)e * n_out + ob * 128, lane);
+        *reinterpret_cast<float4*>(a.ygu + (long long)slot * n_out + ob * 128 + 4 * lane) =
+            make_float4(v[0], v[1], v[2], v[3]);
+    }
+}
+
+// Shared expert down rows: sh[t][row] = sigmoid gate * scale[row] *
+// (w8[row] . SwiGLU(shgu[t])), kShRowsPerWarp rows per warp.
+__device__ void down_shared(const MoeArgs& a, float* smem) {
+    pdl_wait();  // shared gate_up rows and gate
+    pdl_trigger();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int slots = a.T * a.topk;
+    const int cta = ((blockIdx.z - slots) * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+    const int n = a.sh_inter;
+    const int r0 = (cta * kGuWarps + warp) * kShRowsPerWarp;
+    float* hs = smem;  // [kShMT][sh_inter]
+    for (int tb = 0; tb < a.T; tb += kShMT) {
+        const int mt = min(kShMT, a.T - tb);
+        __syncthreads();
+        for (int i = threadIdx.x; i < kShMT * n; i += kGuThreads) {
+            const int t = i / n, c = i % n;
+            float v = 0.f;
+            if (t < mt) {
+                const float* gu = a.shgu + (long long)(tb + t) * 2 * n;
+                v = silu_f(gu[c]) * gu[n + c];
+            }
+            hs[i] = v;
+        }
+        __syncthreads();
+        if (r0 < a.hidden) {
+            float dots[kShRowsPerWarp][kShMT];
+            int8_rows_dot<kShRowsPerWarp, kShMT, 1>(a.sh_dn_w8 + (long long)r0 * n, n, a.hidden - r0, n, hs, n, lane,
+                                                    dots);
+            if (lane == 0) {
+#pragma unroll
+                for (int r = 0; r < kShRowsPerWarp; ++r) {
+                    if (r0 + r >= a.hidden) break;
+                    const float sc = a.sh_dn_scale[r0 + r];
+                    for (int t = 0; t < mt; ++t)
+                        a.sh[(long long)(tb + t) * a.hidden + r0 + r] = a.shgate[tb + t] * (sc * dots[r][t]);
+                }
+            }
+        }
+    }
+}
+
+template <int K>
+__global__ void __launch_bounds__(kGuThreads, 3) moe_gate_up_kernel(const MoeArgs a) {
+    extern __shared__ __align__(16) float smem[];
+    if (static_cast<int>(blockIdx.z) < a.T * a.topk) {
+        gate_up_routed<K>(a, smem);
+    } else {
+        down_shared(a, smem);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// 3. down + combine.
+// ---------------------------------------------------------------------------
+template <int K>
+__global__ void __launch_bounds__(kDnThreads, 3) moe_down_kernel(const MoeArgs a) {
+    const int rank = static_cast<int>(cg::this_cluster().block_rank());
+    const int csz = static_cast<int>(cg::this_cluster().num_blocks());
+    const int ks = a.dn_ksplit;
+    const int j = rank / ks, h = rank % ks;
+    const int ob = blockIdx.y;
+    const int t = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    extern __shared__ __align__(16) float smem[];
+    float* slots = smem;                      // [csz][128] partials, on rank 0
+    float* dres = slots + kMaxCluster * 128;  // [topk][128] finished experts, on rank 0
+    float* red = dres + 8 * 128;              // [kDnWarps][128] (+128: partial of ranks != 0)
+    float* xt = red + (kDnWarps + 1) * 128;   // [inter / ks]
+    __shared__ __align__(8) unsigned long long bar;
+    __shared__ int e_s[8];
+    __shared__ float w_s[8];
+
+    if (rank == 0 && threadIdx.x == 0 && csz > 1) mbar_init(smem_u32(&bar), 32 * (csz - 1));
+    cluster_arrive();
+
+    const int slot = t * a.topk + j;
+    // The logits kernel finished before this grid was scheduled (every
+    // gate_up CTA waited for it before triggering this launch).
+    if (warp == 0) {
+        int e_l;
+        float w_l;
+        topk_softmax_warp(a.logits + (long long)t * a.E, a.E, a.topk, lane, &e_l, &w_l);
+        if (lane < a.topk) {
+            e_s[lane] = e_l;
+            w_s[lane] = w_l;
+        }
+    }
+    __syncthreads();
+    const int e = e_s[j];
+    const int KT = a.inter >> 4, NT = a.hidden >> 4;
+    const int rows_h = KT / ks;  // whole Hadamard blocks per input split
+    const int kt0 = h * rows_h, kt1 = kt0 + rows_h;
+    const uint16_t* codes = a.dn_codes + (long long)e * KT * NT * (16 * K);
+    LaneCodes<K> cur;
+    if (kt0 + warp < kt1) load_lane_codes<K>(cur, codes + ((long long)(kt0 + warp) * NT + ob * 8) * (16 * K), lane);
+    pdl_wait();  // gate_up outputs and the shared expert's down rows
+
+    // xt = H128(rin_e * SwiGLU(ygu[slot])) over this rank's inputs
+    const float* yr = a.ygu + (long long)slot * 2 * a.inter;
+    const uint16_t* rin = a.dn_rin + (long long)e * a.inter;
+    const int nk = rows_h * 16;
+    for (int blk = warp; blk < nk / 128; blk += kDnWarps) {
+        const int ib = kt0 * 16 + blk * 128 + 4 * lane;
+        const float4 g = *reinterpret_cast<const float4*>(yr + ib);
+        const float4 u = *reinterpret_cast<const float4*>(yr + a.inter + ib);
+        const uint2 rb = *reinterpret_cast<const uint2*>(rin + ib);
+        float v[4];
+        v[0] = h2f_bits(static_cast<uint16_t>(rb.x & 0xFFFFu)) * (silu_f(g.x) * u.x);
+        v[1] = h2f_bits(static_cast<uint16_t>(rb.x >> 16)) * (silu_f(g.y) * u.y);
+        v[2] = h2f_bits(static_cast<uint16_t>(rb.y & 0xFFFFu)) * (silu_f(g.z) * u.z);
+        v[3] = h2f_bits(static_cast<uint16_t>(rb.y >> 16)) * (silu_f(g.w) * u.w);
+        h128_warp(v, lane);
+        *reinterpret_cast<float4*>(xt + blk * 128 + 4 * lane) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+    __syncthreads();
+    float* zp = rank == 0 ? slots : red + kDnWarps * 128;
+    cta_gemv_partial<K, 1, kDnWarps>(codes, NT, ob, kt0, kt1, xt, nk, cur, red, zp);
+
+    cluster_wait();
+    if (rank != 0) {
+        if (warp == 0) {
+            const uint32_t dst = cluster_map(smem_u32(slots + rank * 128 + 4 * lane), 0);
+            st_cluster_v4(dst, *reinterpret_cast<const float4*>(zp + 4 * lane));
+            mbar_arrive_cluster(cluster_map(smem_u32(&bar), 0));
+        }
+        return;
+    }
+    if (csz > 1) {
+        if (warp == 0) mbar_wait_bounded(smem_u32(&bar), a.err, 2);
+        __syncthreads();
+    }
+    if (warp < a.topk) {  // warp q finishes expert q: its splits in order, output transform, routing weight
+        const int q = warp;
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int s = 0; s < ks; ++s) {
+            const float4 z4 = *reinterpret_cast<const float4*>(slots + (q * ks + s) * 128 + 4 * lane);
+            v[0] += z4.x;
+            v[1] += z4.y;
+            v[2] += z4.z;
+            v[3] += z4.w;
+        }
+        output_transform_warp(v, a.dn_rout + (long long)e_s[q] * a.hidden + ob * 128, lane);
+        const float wq = w_s[q];
+        *reinterpret_cast<float4*>(dres + q * 128 + 4 * lane) = make_float4(wq * v[0], wq * v[1], wq * v[2], wq * v[3]);
+    }
+    __syncthreads();
+    if (threadIdx.x < 128) {
+        const int i = threadIdx.x;
+        float s = 0.f;
+        for (int q = 0; q < a.topk; ++q) s += dres[q * 128 + i];
+        if (a.sh_inter > 0) s += a.sh[(long long)t * a.hidden + ob * 128 + i];
+        a.out[(long long)t * a.hidden + ob * 128 + i] = s;
+    }
+}
+
+cudaError_t launch_ex(const void* func, dim3 grid, dim3 block, int smem, int cluster_x, bool pdl, cudaStream_t s,
+                      const MoeArgs& a) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (cluster_x > 0) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster_x;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    void* args[] = {const_cast<MoeArgs*>(&a)};
+    return cudaLaunchKernelExC(&cfg, func, args);
+}
+
+template <int K>
+cudaError_t launch_gate_up(MoeArgs a, int num_sms, cudaStream_t s) {
+    const int oblks = 2 * a.inter / 128;
+    const int slots = a.T * a.topk;
+    const int kblks = a.hidden / 128;
+    // Largest input split (CTAs per cluster, <= 8) for which the routed CTAs
+    // plus the shared-down CTAs fit in one wave of 3 CTAs per SM.
+    const int rows_per_cta = kGuWarps * kShRowsPerWarp;
+    auto shared_z = [&](int per_z) {
+        return a.sh_inter > 0 ? (a.hidden + per_z * rows_per_cta - 1) / (per_z * rows_per_cta) : 0;
+    };
+    int csize = 1;
+    for (int c = 1; c <= 8 && c <= kblks; ++c) {
+        const int per = (kblks + c - 1) / c;
+        const int cs = (kblks + per - 1) / per;
+        const int per_z = cs * oblks;
+        if ((long long)per_z * (slots + shared_z(per_z)) <= 3LL * num_sms) csize = cs;
+    }
+    const int per = (kblks + csize - 1) / csize;
+    csize = (kblks + per - 1) / per;
+    a.gu_kt_per_cta = per * 8;
+    const int sh_z = shared_z(csize * oblks);
+    const int smem_routed = (kMaxCluster * 128 + a.gu_kt_per_cta * 16 + (kGuWarps + 1) * 128) * 4;
+    const int smem_shared = a.sh_inter > 0 ? kShMT * a.sh_inter * 4 : 0;
+    const int smem = smem_routed > smem_shared ? smem_routed : smem_shared;
+    const void* f = reinterpret_cast<const void*>(moe_gate_up_kernel<K>);
+    cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    return launch_ex(f, dim3(csize, oblks, slots + sh_z), dim3(kGuThreads), smem, csize, true, s, a);
+}
+
+template <int K>
+cudaError_t launch_down(MoeArgs a, cudaStream_t s) {
+    // Split each expert's input in two when it spans an even number (>= 2)
+    // of Hadamard blocks and the cluster stays within 16 CTAs.
+    a.dn_ksplit = ((a.inter / 128) % 2 == 0 && 2 * a.topk <= kMaxCluster) ? 2 : 1;
+    const int csz = a.topk * a.dn_ksplit;
+    const int smem = (kMaxCluster * 128 + 8 * 128 + (kDnWarps + 1) * 128 + a.inter / a.dn_ksplit) * 4;
+    const void* f = reinterpret_cast<const void*>(moe_down_kernel<K>);
+    cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    if (csz > 8) {
+        e = cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    return launch_ex(f, dim3(csz, a.hidden / 128, a.T), dim3(kDnThreads), smem, csz, true, s, a);
+}
+
+}  // namespace
+
+cudaError_t launch_moe_router(const MoeArgs& a, cudaStream_t s) {
+    const int n_lg = (a.E + kK0Warps - 1) / kK0Warps;
+    const int rows_per_cta = kK0Warps * kShRowsPerWarp;
+    const int n_sh = a.sh_inter > 0 ? (2 * a.sh_inter + rows_per_cta - 1) / rows_per_cta : 0;
+    const int smem = a.sh_inter > 0 ? kShMT * a.hidden * 4 : 0;
+    const void* f = reinterpret_cast<const void*>(moe_router_kernel);
+    cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    return launch_ex(f, dim3(n_lg + n_sh, (a.T + kLgTG - 1) / kLgTG), dim3(kK0Threads), smem, 0, false, s, a);
+}
+
+cudaError_t launch_moe_gate_up(const MoeArgs& a, int num_sms, cudaStream_t s) {
+    return a.gu_K == 2 ? launch_gate_up<2>(a, num_sms, s) : launch_gate_up<3>(a, num_sms, s);
+}
+
+cudaError_t launch_moe_down(const MoeArgs& a, cudaStream_t s) {
+    return a.dn_K == 2 ? launch_down<2>(a, s) : launch_down<3>(a, s);
+}
+
+}  // namespace escha

@@ -212,6 +212,8 @@ class MoeBlock:
 
     def __init__(self, arrays: dict, device="cuda", topk: int = 8):
         def dev(a):
+            if isinstance(a, torch.Tensor):
+                return a.to(device).contiguous()
             a = np.ascontiguousarray(a)
             if a.dtype == np.uint16:
                 a = a.view(np.int16)  # code words travel as raw 16-bit patterns
@@ -230,8 +232,8 @@ class MoeBlock:
         self.t["dn_codes"] = dev(arrays["dn_codes"])
         self.t["dn_rin"] = dev(arrays["dn_rin"])
         self.t["dn_rout"] = dev(arrays["dn_rout"])
-        self.gu_K = arrays["gu_codes"].shape[-1] // 16
-        self.dn_K = arrays["dn_codes"].shape[-1] // 16
+        self.gu_K = int(arrays["gu_codes"].shape[-1]) // 16
+        self.dn_K = int(arrays["dn_codes"].shape[-1]) // 16
         if self.sh_inter:
             self.t["sh_gu_w8"] = dev(arrays["sh_gu_w8"])
             self.t["sh_gu_scale"] = dev(arrays["sh_gu_s"])

@@ -121,8 +121,8 @@ int escha_trellis_gemv(const uint16_t* codes, int in, int out, int K, const void
  * projection [PR694 commit "Converted the real 12.30 GB checkpoint"]).
  * Pointers of an absent shared expert may be null when sh_inter == 0. */
 typedef struct escha_moe_layer {
-    int hidden;    /* multiple of 256 */
-    int inter;     /* routed expert intermediate size, multiple of 128 */
+    int hidden;    /* multiple of 256, <= 8192 */
+    int inter;     /* routed expert intermediate size, multiple of 128, <= 8192 */
     int n_experts; /* 1..256 */
     int topk;      /* 1..8, <= n_experts */
     const uint16_t* router_w; /* fp16 [E][hidden] */
@@ -137,7 +137,7 @@ typedef struct escha_moe_layer {
     const uint16_t* dn_rin;  /* fp16 [E][inter] */
     const uint16_t* dn_rout; /* fp16 [E][hidden] */
     /* shared expert (int8 w8a16, dequant = f32 scale * w8 per row [MLX]) */
-    int sh_inter; /* 0 = no shared expert; else multiple of 16 */
+    int sh_inter; /* 0 = no shared expert; else multiple of 16, <= 8192 */
     const int8_t* sh_gu_w8; /* [2*sh_inter][hidden] */
     const float* sh_gu_scale; /* [2*sh_inter] */
     const int8_t* sh_dn_w8; /* [hidden][sh_inter] */
@@ -145,7 +145,11 @@ typedef struct escha_moe_layer {
     const uint16_t* sh_gate;  /* fp16 [hidden], sigmoid gate of the shared expert */
 } escha_moe_layer;
 
-/*   x       fp16 [T][hidden];  T >= 1
+/* The first 4 bytes of the workspace hold a status word that the call sets
+ * to 0 when its first kernel starts and to a non-zero value if a kernel had
+ * to give up waiting on a cluster peer (it then returns instead of hanging;
+ * the outputs of that call are invalid). Read it after synchronising.
+ *   x       fp16 [T][hidden];  T >= 1
  *   out     f32 [T][hidden] output
  *   ids_out int32 [T][topk] output, may be null
  *   w_out   f32 [T][topk] output, may be null
@@ -154,11 +158,13 @@ size_t escha_moe_block_workspace(const escha_moe_layer* L, int T);
 int escha_moe_block(const escha_moe_layer* L, const uint16_t* x, int T, float* out, int32_t* ids_out, float* w_out,
                     void* ws, size_t ws_bytes, void* stream);
 
-/* Measurement export: escha_moe_block that also records six caller-created
+/* Measurement export: escha_moe_block that also records four caller-created
  * CUDA events (cudaEvent_t, any of them may be null) on `stream`: events[0]
- * before the router, [1] after the router, [2] after gate_up, [3] after
- * down, [4] after the shared expert, [5] after the combine. Same results and
- * errors as escha_moe_block. */
+ * before the router kernel, [1] after it, [2] after the gate_up kernel (routed
+ * gate_up plus the shared expert's gate_up), [3] after the down/combine
+ * kernel. Recording events between the kernels serialises them (no
+ * programmatic overlap), so each interval is one kernel's duration. Same
+ * results and errors as escha_moe_block. */
 int escha_moe_block_timed(const escha_moe_layer* L, const uint16_t* x, int T, float* out, int32_t* ids_out,
                           float* w_out, void* ws, size_t ws_bytes, void* stream, void* const* events);
 
