@@ -9,8 +9,8 @@
 // without an integer-to-float conversion instruction: byte b (biased to
 // b + 128) is placed in the mantissa of 2^23 and 2^23 + 128 is subtracted,
 // which is exact. The row scale multiplies the finished dot product.
-#include "common.cuh"
 #include "kernels.h"
+#include "trellis_core.cuh"
 
 namespace escha {
 
@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(256) int8_gemv_kernel(const int8_t* __restrict
                 v = load_act(x, row + i, x_dtype);
             }
         }
-        xs[idx] = v;
+        xs[xs_swz(idx)] = v;
     }
     __syncthreads();
 
@@ -73,7 +73,7 @@ __global__ void __launch_bounds__(256) int8_gemv_kernel(const int8_t* __restrict
                 float xq[MT][4];
 #pragma unroll
                 for (int t = 0; t < MT; ++t) {
-                    const float4 xv = *reinterpret_cast<const float4*>(xs + t * Kin + i0 + 4 * q);
+                    const float4 xv = *reinterpret_cast<const float4*>(xs + xs_swz(t * Kin + i0 + 4 * q));
                     xq[t][0] = xv.x;
                     xq[t][1] = xv.y;
                     xq[t][2] = xv.z;
@@ -124,7 +124,7 @@ __global__ void int8_dequant_kernel(const int8_t* __restrict__ W, const float* _
 template <int MT>
 cudaError_t launch_mt(const int8_t* W, const float* scales, int N, int Kin, const void* x, int x_dtype,
                       long long x_stride, int act, int M, float* y, long long y_stride, int num_sms, cudaStream_t s) {
-    const int smem = MT * Kin * (int)sizeof(float);
+    const int smem = ((MT * Kin + 31) / 32 * 32) * (int)sizeof(float);  // swizzle groups of 32 floats
     auto kern = int8_gemv_kernel<MT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -141,7 +141,7 @@ cudaError_t launch_int8_gemv(const int8_t* W, const float* scales, int N, int Ki
                              long long x_stride, int act, int M, float* y, long long y_stride, int num_sms,
                              cudaStream_t s) {
     // tokens per pass whose f32 activations fit in shared memory
-    const int cap = (200 * 1024) / (4 * Kin);
+    const int cap = (200 * 1024 - 128) / (4 * Kin);
     if (cap < 1) return cudaErrorInvalidValue;
     if (M == 1 || cap < 2) return launch_mt<1>(W, scales, N, Kin, x, x_dtype, x_stride, act, M, y, y_stride, num_sms, s);
     if (M == 2 || cap < 4) return launch_mt<2>(W, scales, N, Kin, x, x_dtype, x_stride, act, M, y, y_stride, num_sms, s);

@@ -1,25 +1,25 @@
 // One MoE block of an Escha-W2 Qwen3.6-35B-A3B-style layer in three kernels
 // chained by programmatic dependent launch:
 //
-//  1. router + shared gate_up: f16-rounded router logits in a fixed
-//     summation order (hipfire PR #694, commit "Executed the moeblk golden
-//     against real shipped layer-0 weights": logits are rounded to f16
-//     before top-k), one warp per expert spread over many SMs so the 1 MB
-//     router matrix streams in one memory round trip; in the same grid, the
-//     int8 shared expert's gate_up rows and its sigmoid gate, which need no
-//     routing.
+//  1. router logits: f16-rounded logits in a fixed summation order (hipfire
+//     PR #694, commit "Executed the moeblk golden against real shipped
+//     layer-0 weights": logits are rounded to f16 before top-k), one warp per
+//     expert spread over many SMs so the 1 MB router matrix streams in one
+//     memory round trip.
 //  2. gate_up: each routed CTA selects its token's top-k (ties to the lower
 //     expert id) and softmax weights with one warp, then runs the expert's
 //     gate_up projection (fused trellis decode GEMV with the input/output
 //     Hadamard transforms and rout); a cluster splits the input rows and
-//     pushes its partial sums into rank 0. Extra CTAs compute the shared
-//     expert's down rows (SwiGLU of its gate_up, times the sigmoid gate).
+//     pushes its partial sums into rank 0. Extra CTAs, which do not wait for
+//     the router, compute the int8 shared expert's gate_up rows and its
+//     sigmoid gate.
 //  3. down + combine: one cluster per (token, 128-wide output block), rank
-//     j*ks + h = routed expert j, input split h. Ranks push partials into
-//     rank 0, which finishes each expert (output transform, routing weight),
-//     sums the experts in slot order and adds the shared expert (SwiGLU with
-//     gate = first half: hipfire PR #694, commit "The accumulation loop
-//     treated a zero activation as a no-op").
+//     j*ks + h = routed expert j, input split h; every rank also computes an
+//     equal share of the shared expert's down rows of the block. Ranks push
+//     partials into rank 0, which finishes each expert (output transform,
+//     routing weight), sums the experts in slot order and adds the shared
+//     expert (SwiGLU with gate = first half: hipfire PR #694, commit "The
+//     accumulation loop treated a zero activation as a no-op").
 #include "kernels.h"
 #include "trellis_core.cuh"
 
@@ -101,11 +101,11 @@ __device__ void router_logits(const MoeArgs& a, int warp, int lane) {
 // x, not rounded).
 __device__ void shared_gate_up(const MoeArgs& a, int cta, float* xs, int warp, int lane) {
     const int rows = 2 * a.sh_inter;
-    const int r0 = (cta * kK0Warps + warp) * kShRowsPerWarp;
+    const int r0 = (cta * kGuWarps + warp) * kShRowsPerWarp;
     for (int tb = 0; tb < a.T; tb += kShMT) {
         const int mt = min(kShMT, a.T - tb);
         __syncthreads();
-        for (int i = threadIdx.x * 8; i < kShMT * a.hidden; i += kK0Threads * 8) {
+        for (int i = threadIdx.x * 8; i < kShMT * a.hidden; i += kGuThreads * 8) {
             const int t = i / a.hidden, c = i % a.hidden;
             float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
             if (t < mt) {
@@ -113,8 +113,8 @@ __device__ void shared_gate_up(const MoeArgs& a, int cta, float* xs, int warp, i
                 lo = make_float4(h2f_bits(v.x & 0xFFFFu), h2f_bits(v.x >> 16), h2f_bits(v.y & 0xFFFFu), h2f_bits(v.y >> 16));
                 hi = make_float4(h2f_bits(v.z & 0xFFFFu), h2f_bits(v.z >> 16), h2f_bits(v.w & 0xFFFFu), h2f_bits(v.w >> 16));
             }
-            *reinterpret_cast<float4*>(xs + i) = lo;
-            *reinterpret_cast<float4*>(xs + i + 4) = hi;
+            *reinterpret_cast<float4*>(xs + xs_swz(i)) = lo;
+            *reinterpret_cast<float4*>(xs + xs_swz(i + 4)) = hi;
         }
         __syncthreads();
         if (r0 < rows) {
@@ -130,7 +130,7 @@ __device__ void shared_gate_up(const MoeArgs& a, int cta, float* xs, int warp, i
                 }
             }
         }
-        if (cta == 0 && warp == kK0Warps - 1) {
+        if (cta == 0 && warp == kGuWarps - 1) {
             float acc[kShMT] = {};
 #pragma unroll 8
             for (int i0 = lane * 8; i0 < a.hidden; i0 += 256) {
@@ -140,8 +140,10 @@ __device__ void shared_gate_up(const MoeArgs& a, int cta, float* xs, int warp, i
                 for (int t = 0; t < kShMT; ++t) {
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        acc[t] = fmaf(h2f_bits(static_cast<uint16_t>(gw[k] & 0xFFFFu)), xs[t * a.hidden + i0 + 2 * k], acc[t]);
-                        acc[t] = fmaf(h2f_bits(static_cast<uint16_t>(gw[k] >> 16)), xs[t * a.hidden + i0 + 2 * k + 1], acc[t]);
+                        acc[t] = fmaf(h2f_bits(static_cast<uint16_t>(gw[k] & 0xFFFFu)), xs[xs_swz(t * a.hidden + i0 + 2 * k)],
+                                      acc[t]);
+                        acc[t] = fmaf(h2f_bits(static_cast<uint16_t>(gw[k] >> 16)), xs[xs_swz(t * a.hidden + i0 + 2 * k + 1)],
+                                      acc[t]);
                     }
                 }
             }
@@ -157,18 +159,12 @@ __device__ void shared_gate_up(const MoeArgs& a, int cta, float* xs, int warp, i
 }
 
 __global__ void __launch_bounds__(kK0Threads) moe_router_kernel(const MoeArgs a) {
-    // The gate_up kernel can be scheduled at once; its CTAs wait for this
-    // grid before reading anything it writes.
+    // The gate_up kernel can be scheduled at once; its routed CTAs wait for
+    // this grid before reading the logits.
     pdl_trigger();
-    extern __shared__ __align__(16) float smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *a.err = 0;  // the whole previous call has finished
-    const int n_lg = (a.E + kK0Warps - 1) / kK0Warps;
-    if (static_cast<int>(blockIdx.x) < n_lg) {
-        router_logits(a, warp, lane);
-    } else if (blockIdx.y == 0) {
-        shared_gate_up(a, blockIdx.x - n_lg, smem, warp, lane);
-    }
+    router_logits(a, warp, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -198,7 +194,7 @@ __device__ void gate_up_routed(const MoeArgs& a, float* smem) {
 
     const int t = slot / a.topk;
     const int j = slot % a.topk;
-    pdl_wait();     // router logits and shared gate_up
+    pdl_wait();     // router logits
     pdl_trigger();  // logits complete: the down kernel may read them early
     if (warp == 0) {
         int e_l;
@@ -235,6 +231,9 @@ __device__ void gate_up_routed(const MoeArgs& a, float* smem) {
         *reinterpret_cast<float4*>(xt + blk * 128 + 4 * lane) = make_float4(v[0], v[1], v[2], v[3]);
     }
     __syncthreads();
+    uint2 rout_pre = make_uint2(0u, 0u);  // rank 0's output scales, fetched while the loop runs
+    if (crank == 0 && warp == 0)
+        rout_pre = *reinterpret_cast<const uint2*>(a.gu_rout + (long long)e * n_out + ob * 128 + 4 * lane);
     float* zp = crank == 0 ? slots : red + kGuWarps * 128;  // rank 0 keeps its partial in slot 0
     cta_gemv_partial<K, 1, kGuWarps>(codes, NT, ob, kt0, kt1, xt, nk, cur, red, zp);
 
@@ -257,50 +256,9 @@ __device__ void gate_up_routed(const MoeArgs& a, float* smem) {
             v[2] += z4.z;
             v[3] += z4.w;
         }
-        output_transform_warp(v, a.gu_rout + (long long)e * n_out + ob * 128, lane);
+        output_transform_regs(v, rout_pre, lane);
         *reinterpret_cast<float4*>(a.ygu + (long long)slot * n_out + ob * 128 + 4 * lane) =
             make_float4(v[0], v[1], v[2], v[3]);
-    }
-}
-
-// Shared expert down rows: sh[t][row] = sigmoid gate * scale[row] *
-// (w8[row] . SwiGLU(shgu[t])), kShRowsPerWarp rows per warp.
-__device__ void down_shared(const MoeArgs& a, float* smem) {
-    pdl_wait();  // shared gate_up rows and gate
-    pdl_trigger();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int slots = a.T * a.topk;
-    const int cta = ((blockIdx.z - slots) * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
-    const int n = a.sh_inter;
-    const int r0 = (cta * kGuWarps + warp) * kShRowsPerWarp;
-    float* hs = smem;  // [kShMT][sh_inter]
-    for (int tb = 0; tb < a.T; tb += kShMT) {
-        const int mt = min(kShMT, a.T - tb);
-        __syncthreads();
-        for (int i = threadIdx.x; i < kShMT * n; i += kGuThreads) {
-            const int t = i / n, c = i % n;
-            float v = 0.f;
-            if (t < mt) {
-                const float* gu = a.shgu + (long long)(tb + t) * 2 * n;
-                v = silu_f(gu[c]) * gu[n + c];
-            }
-            hs[i] = v;
-        }
-        __syncthreads();
-        if (r0 < a.hidden) {
-            float dots[kShRowsPerWarp][kShMT];
-            int8_rows_dot<kShRowsPerWarp, kShMT, 1>(a.sh_dn_w8 + (long long)r0 * n, n, a.hidden - r0, n, hs, n, lane,
-                                                    dots);
-            if (lane == 0) {
-#pragma unroll
-                for (int r = 0; r < kShRowsPerWarp; ++r) {
-                    if (r0 + r >= a.hidden) break;
-                    const float sc = a.sh_dn_scale[r0 + r];
-                    for (int t = 0; t < mt; ++t)
-                        a.sh[(long long)(tb + t) * a.hidden + r0 + r] = a.shgate[tb + t] * (sc * dots[r][t]);
-                }
-            }
-        }
     }
 }
 
@@ -310,7 +268,9 @@ __global__ void __launch_bounds__(kGuThreads, 3) moe_gate_up_kernel(const MoeArg
     if (static_cast<int>(blockIdx.z) < a.T * a.topk) {
         gate_up_routed<K>(a, smem);
     } else {
-        down_shared(a, smem);
+        pdl_trigger();  // needs nothing from the router
+        const int cta = ((blockIdx.z - a.T * a.topk) * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+        shared_gate_up(a, cta, smem, threadIdx.x >> 5, threadIdx.x & 31);
     }
 }
 
@@ -328,15 +288,29 @@ __global__ void __launch_bounds__(kDnThreads, 3) moe_down_kernel(const MoeArgs a
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     extern __shared__ __align__(16) float smem[];
     float* slots = smem;                      // [csz][128] partials, on rank 0
-    float* dres = slots + kMaxCluster * 128;  // [topk][128] finished experts, on rank 0
+    float* shres = slots + kMaxCluster * 128; // [128] shared-expert rows of the block, on rank 0
+    float* dres = shres + 128;                // [topk][128] finished experts, on rank 0
     float* red = dres + 8 * 128;              // [kDnWarps][128] (+128: partial of ranks != 0)
-    float* xt = red + (kDnWarps + 1) * 128;   // [inter / ks]
+    float* xt = red + (kDnWarps + 1) * 128;   // [max(inter / ks, sh_inter)]
     __shared__ __align__(8) unsigned long long bar;
     __shared__ int e_s[8];
     __shared__ float w_s[8];
 
     if (rank == 0 && threadIdx.x == 0 && csz > 1) mbar_init(smem_u32(&bar), 32 * (csz - 1));
     cluster_arrive();
+
+    // This rank's share of the shared expert's 128 down rows of the block:
+    // rows rank*sh_per + warp + 8*i; with sh_inter <= 512 a warp's first two
+    // rows are prefetched now.
+    const int sh_per = (128 + csz - 1) / csz;
+    const int n_sh = a.sh_inter;
+    uint4 shw[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int rr = warp + kDnWarps * i, row = rank * sh_per + rr;
+        if (n_sh > 0 && n_sh <= 512 && rr < sh_per && row < 128 && lane * 16 < n_sh)
+            shw[i] = ldg_stream_v4(a.sh_dn_w8 + (long long)(ob * 128 + row) * n_sh + lane * 16);
+    }
 
     const int slot = t * a.topk + j;
     // The logits kernel finished before this grid was scheduled (every
@@ -355,20 +329,22 @@ __global__ void __launch_bounds__(kDnThreads, 3) moe_down_kernel(const MoeArgs a
     const int KT = a.inter >> 4, NT = a.hidden >> 4;
     const int rows_h = KT / ks;  // whole Hadamard blocks per input split
     const int kt0 = h * rows_h, kt1 = kt0 + rows_h;
+    const int nk = rows_h * 16;
     const uint16_t* codes = a.dn_codes + (long long)e * KT * NT * (16 * K);
     LaneCodes<K> cur;
     if (kt0 + warp < kt1) load_lane_codes<K>(cur, codes + ((long long)(kt0 + warp) * NT + ob * 8) * (16 * K), lane);
-    pdl_wait();  // gate_up outputs and the shared expert's down rows
+    const uint16_t* rin = a.dn_rin + (long long)e * a.inter;
+    uint2 rin_pre = make_uint2(0u, 0u);
+    if (warp < nk / 128) rin_pre = *reinterpret_cast<const uint2*>(rin + kt0 * 16 + warp * 128 + 4 * lane);
+    pdl_wait();  // gate_up outputs and the shared expert's gate_up
 
     // xt = H128(rin_e * SwiGLU(ygu[slot])) over this rank's inputs
     const float* yr = a.ygu + (long long)slot * 2 * a.inter;
-    const uint16_t* rin = a.dn_rin + (long long)e * a.inter;
-    const int nk = rows_h * 16;
     for (int blk = warp; blk < nk / 128; blk += kDnWarps) {
         const int ib = kt0 * 16 + blk * 128 + 4 * lane;
         const float4 g = *reinterpret_cast<const float4*>(yr + ib);
         const float4 u = *reinterpret_cast<const float4*>(yr + a.inter + ib);
-        const uint2 rb = *reinterpret_cast<const uint2*>(rin + ib);
+        const uint2 rb = blk == warp ? rin_pre : *reinterpret_cast<const uint2*>(rin + ib);
         float v[4];
         v[0] = h2f_bits(static_cast<uint16_t>(rb.x & 0xFFFFu)) * (silu_f(g.x) * u.x);
         v[1] = h2f_bits(static_cast<uint16_t>(rb.x >> 16)) * (silu_f(g.y) * u.y);
@@ -378,12 +354,67 @@ __global__ void __launch_bounds__(kDnThreads, 3) moe_down_kernel(const MoeArgs a
         *reinterpret_cast<float4*>(xt + blk * 128 + 4 * lane) = make_float4(v[0], v[1], v[2], v[3]);
     }
     __syncthreads();
+    uint2 rout_pre = make_uint2(0u, 0u);  // rank 0: every expert's output scales, fetched while the loop runs
+    if (rank == 0 && warp < a.topk)
+        rout_pre = *reinterpret_cast<const uint2*>(a.dn_rout + (long long)e_s[warp] * a.hidden + ob * 128 + 4 * lane);
     float* zp = rank == 0 ? slots : red + kDnWarps * 128;
     cta_gemv_partial<K, 1, kDnWarps>(codes, NT, ob, kt0, kt1, xt, nk, cur, red, zp);
 
-    cluster_wait();
+    // shared expert rows: xt <- SwiGLU(shgu[t]); the values go to rank 0's
+    // shres (directly on rank 0, through distributed shared memory elsewhere)
+    if (a.sh_inter > 0) {
+        const float* gu = a.shgu + (long long)t * 2 * n_sh;
+        for (int i = threadIdx.x; i < n_sh; i += kDnThreads) xt[xs_swz(i)] = silu_f(gu[i]) * gu[n_sh + i];
+        __syncthreads();
+        cluster_wait();  // rank 0's shared memory may be written from here on
+        const float gate = a.shgate[t];
+        for (int rr = warp, i = 0; rr < sh_per; rr += kDnWarps, ++i) {
+            const int sh_row = rank * sh_per + rr;
+            if (sh_row >= 128) break;
+            float dot;
+            if (n_sh <= 512 && i < 2) {
+                float acc = 0.f;
+                if (lane * 16 < n_sh) {
+                    const uint4 wv = i == 0 ? shw[0] : shw[1];
+                    const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        float f[4];
+                        i8x4_to_f32(words[q], f);
+                        const float4 xv = *reinterpret_cast<const float4*>(xt + xs_swz(lane * 16 + 4 * q));
+                        acc = fmaf(f[0], xv.x, acc);
+                        acc = fmaf(f[1], xv.y, acc);
+                        acc = fmaf(f[2], xv.z, acc);
+                        acc = fmaf(f[3], xv.w, acc);
+                    }
+                }
+#pragma unroll
+                for (int m = 16; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+                dot = acc;
+            } else {
+                float d1[1][1];
+                int8_rows_dot<1, 1, 4>(a.sh_dn_w8 + (long long)(ob * 128 + sh_row) * n_sh, n_sh, 1, n_sh, xt, n_sh, lane,
+                                       d1);
+                dot = d1[0][0];
+            }
+            const float sh_val = gate * (a.sh_dn_scale[ob * 128 + sh_row] * dot);
+            if (lane == 0) {
+                if (rank == 0) {
+                    shres[sh_row] = sh_val;
+                } else {
+                    const uint32_t dst = cluster_map(smem_u32(shres + sh_row), 0);
+                    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst), "f"(sh_val) : "memory");
+                }
+            }
+        }
+    } else {
+        cluster_wait();
+    }
+
     if (rank != 0) {
+        __syncthreads();
         if (warp == 0) {
+            asm volatile("fence.acq_rel.cluster;" ::: "memory");
             const uint32_t dst = cluster_map(smem_u32(slots + rank * 128 + 4 * lane), 0);
             st_cluster_v4(dst, *reinterpret_cast<const float4*>(zp + 4 * lane));
             mbar_arrive_cluster(cluster_map(smem_u32(&bar), 0));
@@ -392,29 +423,29 @@ __global__ void __launch_bounds__(kDnThreads, 3) moe_down_kernel(const MoeArgs a
     }
     if (csz > 1) {
         if (warp == 0) mbar_wait_bounded(smem_u32(&bar), a.err, 2);
-        __syncthreads();
     }
+    __syncthreads();
     if (warp < a.topk) {  // warp q finishes expert q: its splits in order, output transform, routing weight
         const int q = warp;
         float v[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int s = 0; s < ks; ++s) {
-            const float4 z4 = *reinterpret_cast<const float4*>(slots + (q * ks + s) * 128 + 4 * lane);
+        for (int sp = 0; sp < ks; ++sp) {
+            const float4 z4 = *reinterpret_cast<const float4*>(slots + (q * ks + sp) * 128 + 4 * lane);
             v[0] += z4.x;
             v[1] += z4.y;
             v[2] += z4.z;
             v[3] += z4.w;
         }
-        output_transform_warp(v, a.dn_rout + (long long)e_s[q] * a.hidden + ob * 128, lane);
+        output_transform_regs(v, rout_pre, lane);
         const float wq = w_s[q];
         *reinterpret_cast<float4*>(dres + q * 128 + 4 * lane) = make_float4(wq * v[0], wq * v[1], wq * v[2], wq * v[3]);
     }
     __syncthreads();
     if (threadIdx.x < 128) {
         const int i = threadIdx.x;
-        float s = 0.f;
-        for (int q = 0; q < a.topk; ++q) s += dres[q * 128 + i];
-        if (a.sh_inter > 0) s += a.sh[(long long)t * a.hidden + ob * 128 + i];
-        a.out[(long long)t * a.hidden + ob * 128 + i] = s;
+        float sum = 0.f;
+        for (int q = 0; q < a.topk; ++q) sum += dres[q * 128 + i];
+        if (a.sh_inter > 0) sum += shres[i];
+        a.out[(long long)t * a.hidden + ob * 128 + i] = sum;
     }
 }
 
@@ -451,10 +482,10 @@ cudaError_t launch_gate_up(MoeArgs a, int num_sms, cudaStream_t s) {
     const int slots = a.T * a.topk;
     const int kblks = a.hidden / 128;
     // Largest input split (CTAs per cluster, <= 8) for which the routed CTAs
-    // plus the shared-down CTAs fit in one wave of 3 CTAs per SM.
+    // plus the shared gate_up CTAs fit in one wave of 3 CTAs per SM.
     const int rows_per_cta = kGuWarps * kShRowsPerWarp;
     auto shared_z = [&](int per_z) {
-        return a.sh_inter > 0 ? (a.hidden + per_z * rows_per_cta - 1) / (per_z * rows_per_cta) : 0;
+        return a.sh_inter > 0 ? (2 * a.sh_inter + per_z * rows_per_cta - 1) / (per_z * rows_per_cta) : 0;
     };
     int csize = 1;
     for (int c = 1; c <= 8 && c <= kblks; ++c) {
@@ -468,7 +499,7 @@ cudaError_t launch_gate_up(MoeArgs a, int num_sms, cudaStream_t s) {
     a.gu_kt_per_cta = per * 8;
     const int sh_z = shared_z(csize * oblks);
     const int smem_routed = (kMaxCluster * 128 + a.gu_kt_per_cta * 16 + (kGuWarps + 1) * 128) * 4;
-    const int smem_shared = a.sh_inter > 0 ? kShMT * a.sh_inter * 4 : 0;
+    const int smem_shared = a.sh_inter > 0 ? kShMT * a.hidden * 4 : 0;
     const int smem = smem_routed > smem_shared ? smem_routed : smem_shared;
     const void* f = reinterpret_cast<const void*>(moe_gate_up_kernel<K>);
     cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -482,7 +513,9 @@ cudaError_t launch_down(MoeArgs a, cudaStream_t s) {
     // of Hadamard blocks and the cluster stays within 16 CTAs.
     a.dn_ksplit = ((a.inter / 128) % 2 == 0 && 2 * a.topk <= kMaxCluster) ? 2 : 1;
     const int csz = a.topk * a.dn_ksplit;
-    const int smem = (kMaxCluster * 128 + 8 * 128 + (kDnWarps + 1) * 128 + a.inter / a.dn_ksplit) * 4;
+    int nx = a.inter / a.dn_ksplit > a.sh_inter ? a.inter / a.dn_ksplit : a.sh_inter;
+    nx = (nx + 31) / 32 * 32;  // the shared rows' swizzled staging works on groups of 32 floats
+    const int smem = (kMaxCluster * 128 + 128 + 8 * 128 + (kDnWarps + 1) * 128 + nx) * 4;
     const void* f = reinterpret_cast<const void*>(moe_down_kernel<K>);
     cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -497,13 +530,8 @@ cudaError_t launch_down(MoeArgs a, cudaStream_t s) {
 
 cudaError_t launch_moe_router(const MoeArgs& a, cudaStream_t s) {
     const int n_lg = (a.E + kK0Warps - 1) / kK0Warps;
-    const int rows_per_cta = kK0Warps * kShRowsPerWarp;
-    const int n_sh = a.sh_inter > 0 ? (2 * a.sh_inter + rows_per_cta - 1) / rows_per_cta : 0;
-    const int smem = a.sh_inter > 0 ? kShMT * a.hidden * 4 : 0;
-    const void* f = reinterpret_cast<const void*>(moe_router_kernel);
-    cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    return launch_ex(f, dim3(n_lg + n_sh, (a.T + kLgTG - 1) / kLgTG), dim3(kK0Threads), smem, 0, false, s, a);
+    return launch_ex(reinterpret_cast<const void*>(moe_router_kernel), dim3(n_lg, (a.T + kLgTG - 1) / kLgTG),
+                     dim3(kK0Threads), 0, 0, false, s, a);
 }
 
 cudaError_t launch_moe_gate_up(const MoeArgs& a, int num_sms, cudaStream_t s) {

@@ -147,13 +147,17 @@ __device__ __forceinline__ void cta_gemv_partial(const uint16_t* codes, int NT, 
 // values per lane (element 4*lane + j); returns rout * (2^-7 * H128(v)) in v.
 // (Both Hadamards run unscaled; their two 1/sqrt(128) factors make the exact
 // 2^-7, applied before rout so that rout stays the final multiply.)
-__device__ __forceinline__ void output_transform_warp(float (&v)[4], const uint16_t* rout_blk, int lane) {
+// rb: the lane's 4 rout values (fp16 bits), already loaded.
+__device__ __forceinline__ void output_transform_regs(float (&v)[4], uint2 rb, int lane) {
     h128_warp(v, lane);
-    const uint2 rb = *reinterpret_cast<const uint2*>(rout_blk + 4 * lane);
     v[0] = h2f_bits(static_cast<uint16_t>(rb.x & 0xFFFFu)) * (v[0] * 0.0078125f);
     v[1] = h2f_bits(static_cast<uint16_t>(rb.x >> 16)) * (v[1] * 0.0078125f);
     v[2] = h2f_bits(static_cast<uint16_t>(rb.y & 0xFFFFu)) * (v[2] * 0.0078125f);
     v[3] = h2f_bits(static_cast<uint16_t>(rb.y >> 16)) * (v[3] * 0.0078125f);
+}
+
+__device__ __forceinline__ void output_transform_warp(float (&v)[4], const uint16_t* rout_blk, int lane) {
+    output_transform_regs(v, *reinterpret_cast<const uint2*>(rout_blk + 4 * lane), lane);
 }
 
 // int8 weights -> exact floats without a conversion instruction: each byte,
@@ -168,8 +172,19 @@ __device__ __forceinline__ void i8x4_to_f32(uint32_t v, float (&f)[4]) {
     f[3] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653)) - bias;
 }
 
+// Position of activation element i in a staged activation buffer. Lane l of
+// an int8 row dot reads the float4s 4l + q (q = 0..3) of each 512-column
+// chunk; unswizzled, the 8 lanes of a shared-memory wavefront would hit only
+// 2 of the 8 16-byte bank groups. XOR-ing the float4 index with bits 3..5 of
+// itself spreads them over all 8.
+__device__ __forceinline__ int xs_swz(int i) {
+    const int f = i >> 2;
+    return ((f ^ ((f >> 3) & 7)) << 2) | (i & 3);
+}
+
 // One warp: dot products of R int8 rows (row r at w + r*ld, n columns,
-// n % 16 == 0) with MT f32 vectors in shared memory (xs + t*xstride). All
+// n % 16 == 0) with MT f32 vectors in shared memory, element i of vector t
+// at xs[xs_swz(t*xstride + i)] (xstride % 32 == 0). All
 // 16-byte loads of a group of NCH chunks of 512 columns are issued before any
 // arithmetic, so a warp waits for memory once per group, not once per row.
 // Rows r >= nrows are skipped. Lane 0 holds the sums.
@@ -199,7 +214,7 @@ __device__ __forceinline__ void int8_rows_dot(const int8_t* w, long long ld, int
                 float xq[MT][4];
 #pragma unroll
                 for (int t = 0; t < MT; ++t) {
-                    const float4 xv = *reinterpret_cast<const float4*>(xs + t * xstride + i0 + 4 * q);
+                    const float4 xv = *reinterpret_cast<const float4*>(xs + xs_swz(t * xstride + i0 + 4 * q));
                     xq[t][0] = xv.x;
                     xq[t][1] = xv.y;
                     xq[t][2] = xv.z;
