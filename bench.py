@@ -50,7 +50,33 @@ GU_CODE_BYTES = HIDDEN * 2 * INTER * 3 // 8  # per expert: 786,432
 DN_CODE_BYTES = INTER * HIDDEN * 2 // 8  # per expert: 262,144
 N_LAYERS = 24
 STEPS_PER_GRAPH = 8
-KERNELS_PER_STEP = 3  # router (+shared gate_up), gate_up (+top-k, shared down), down (+top-k, combine)
+KERNELS_PER_STEP = 3  # router, gate_up (+top-k, shared gate_up), down (+top-k, shared down, combine)
+
+
+# Algorithmic bytes of one launch of the gate_up kernel at batch 1. Routed:
+# 8 experts' codes, rin and rout, x once, the token's 256 f16 logits, the
+# 8 x 1024 f32 outputs. Shared expert: int8 gate_up rows and scales, the fp16
+# gate vector, its 1024 f32 outputs and the gate value.
+GATE_UP_KERNEL_BYTES = (TOPK * (GU_CODE_BYTES + HIDDEN * 2 + 2 * INTER * 2) + HIDDEN * 2 + E * 2
+                        + TOPK * 2 * INTER * 4 + 2 * INTER * HIDDEN + 2 * INTER * 4 + HIDDEN * 2
+                        + 2 * INTER * 4 + 4)
+
+
+def measured_traffic():
+    """DRAM bytes per launch of the gate_up kernel from the committed ncu
+    capture, or None when the kernel sources changed since the capture."""
+    import hashlib
+
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f)
+    h = hashlib.sha256()
+    for name in rec["sources"]:
+        with open(os.path.join(ROOT, "bit_trellis_quantized_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return rec["dram_bytes_per_launch"] if h.hexdigest() == rec["sources_sha256"] else None
 
 
 def peaks():
@@ -200,15 +226,16 @@ def run_ours(args, ws, rank, local):
 
     # NL distinct layers (~272 MB each): a step's weights were last touched
     # NL-1 steps earlier, far more than L2 holds, so they come from HBM.
+    n_layers = args.layers
     blocks = [native.MoeBlock(moe_layer_device(LAYER_SEED + 1000 * rank + l, dev), device=dev, topk=TOPK)
-              for l in range(N_LAYERS)]
+              for l in range(n_layers)]
     n_total = args.warmup + args.steps
     xs_host = torch.from_numpy(gen.fp16_normal(gen.rng(X_SEED + 100 * rank), (n_total, HIDDEN))).pin_memory()
     xs = xs_host.to(dev)
     outs = torch.empty((n_total, HIDDEN), dtype=torch.float32, device=dev)
     ids_all = torch.empty((n_total, TOPK), dtype=torch.int32, device=dev)
     w_all = torch.empty((n_total, TOPK), dtype=torch.float32, device=dev)
-    layer_of = [i % N_LAYERS for i in range(n_total)]
+    layer_of = [i % n_layers for i in range(n_total)]
 
     # One CUDA graph holds STEPS_PER_GRAPH consecutive steps (as a model's
     # decode graph holds its layers). Every step still runs after the
@@ -220,7 +247,7 @@ def run_ours(args, ws, rank, local):
         for blk in blocks:  # workspaces sized and kernels loaded before capture
             blk(xs[0:1], out=outs[0:1], ids=ids_all[0:1], w=w_all[0:1])
         torch.cuda.synchronize()
-        for i0 in range(0, n_total, STEPS_PER_GRAPH):
+        for i0 in range(0, n_total if not args.no_graph else 0, STEPS_PER_GRAPH):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 for i in range(i0, i0 + STEPS_PER_GRAPH):
@@ -233,28 +260,46 @@ def run_ours(args, ws, rank, local):
         # device-resident inputs: x already in HBM when the timed region starts
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
-            for g in graphs[:n_warm_graphs]:
-                g.replay()
-            barrier()
-            t0.record(stream)
-            for g in graphs[n_warm_graphs:]:
-                g.replay()
-            t1.record(stream)
-            barrier()
+            if args.no_graph:  # direct launches (for profilers)
+                for i in range(args.warmup):
+                    blocks[layer_of[i]](xs[i:i + 1], out=outs[i:i + 1], ids=ids_all[i:i + 1], w=w_all[i:i + 1])
+                barrier()
+                t0.record(stream)
+                for i in range(args.warmup, n_total):
+                    blocks[layer_of[i]](xs[i:i + 1], out=outs[i:i + 1], ids=ids_all[i:i + 1], w=w_all[i:i + 1])
+                t1.record(stream)
+                barrier()
+            else:
+                for g in graphs[:n_warm_graphs]:
+                    g.replay()
+                barrier()
+                t0.record(stream)
+                for g in graphs[n_warm_graphs:]:
+                    g.replay()
+                t1.record(stream)
+                barrier()
         step_ms = t0.elapsed_time(t1) / args.steps
 
         # end to end through the public API: pinned host x in, out back to host
         out_host = torch.empty((n_total, HIDDEN), dtype=torch.float32).pin_memory()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        def run_group(gi):
+            if args.no_graph:
+                for i in range(gi * STEPS_PER_GRAPH, (gi + 1) * STEPS_PER_GRAPH):
+                    blocks[layer_of[i]](xs[i:i + 1], out=outs[i:i + 1], ids=ids_all[i:i + 1], w=w_all[i:i + 1])
+            else:
+                graphs[gi].replay()
+
+        n_groups = n_total // STEPS_PER_GRAPH
         with torch.cuda.stream(stream):
-            for g in graphs[:n_warm_graphs]:
-                g.replay()
+            for gi in range(n_warm_graphs):
+                run_group(gi)
             barrier()
             e0.record(stream)
-            for gi in range(n_warm_graphs, len(graphs)):
+            for gi in range(n_warm_graphs, n_groups):
                 i0 = gi * STEPS_PER_GRAPH
                 xs[i0:i0 + STEPS_PER_GRAPH].copy_(xs_host[i0:i0 + STEPS_PER_GRAPH], non_blocking=True)
-                graphs[gi].replay()
+                run_group(gi)
                 out_host[i0:i0 + STEPS_PER_GRAPH].copy_(outs[i0:i0 + STEPS_PER_GRAPH], non_blocking=True)
             e1.record(stream)
             barrier()
@@ -294,13 +339,9 @@ def run_ours(args, ws, rank, local):
         return
 
     hbm, tflops, src = peaks()
-    ph = phase.mean(axis=0)  # router (+shared gate_up), gate_up (+shared down), down (+combine) (ms)
+    ph = phase.mean(axis=0)  # router, gate_up (+shared gate_up), down (+shared down, combine) (ms)
     gu_ms = float(ph[1])
-    # gate_up kernel. Routed: codes + rin + rout per expert, x once, the
-    # token's logits, gate_up outputs. Shared expert down rows: int8 weights +
-    # scales, its gate_up input and gate, its output.
-    gu_bytes = (TOPK * (GU_CODE_BYTES + HIDDEN * 2 + 2 * INTER * 2) + HIDDEN * 2 + E * 2 + TOPK * 2 * INTER * 4
-                + HIDDEN * INTER + HIDDEN * 4 + 2 * INTER * 4 + 4 + HIDDEN * 4)
+    gu_bytes = GATE_UP_KERNEL_BYTES
     achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
     routed_code_bytes = TOPK * (GU_CODE_BYTES + DN_CODE_BYTES)
     distinct = len({tuple(r) for r in ids_all[args.warmup:args.warmup + 16].cpu().numpy().tolist()})
@@ -309,17 +350,18 @@ def run_ours(args, ws, rank, local):
         "warmup": args.warmup, "ms_per_step": t_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp16 weights / f32 accumulate", "data": "synthetic",
         "config": {"workload": WORKLOAD, "batch": 1, "tokens_per_step_per_gpu": 1,
-                   "l2": f"inputs larger than L2: {N_LAYERS} distinct MoE layers "
-                         f"({N_LAYERS * 272} MB) cycled, one per step, no flush",
-                   "cuda_graph": f"{STEPS_PER_GRAPH} serialized steps per graph",
+                   "l2": f"inputs larger than L2: {n_layers} distinct MoE layers "
+                         f"({n_layers * 272} MB) cycled, one per step, no flush",
+                   "cuda_graph": "none (direct launches)" if args.no_graph else
+                                 f"{STEPS_PER_GRAPH} serialized steps per graph",
                    "parallelism": f"replicas x{ws} (independent token streams)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": None, "kernel": "moe_gate_up_kernel<K=3> (8 routed experts + int8 shared-expert down rows)",
+                     "traffic": measured_traffic(), "kernel": "moe_gate_up_kernel<K=3> (8 routed experts + int8 shared gate_up)",
                      "algorithmic_bytes_per_launch": gu_bytes, "ms_per_launch": gu_ms, "peak_source": src},
         "packed_expert_gbs": routed_code_bytes / (t_step * 1e-3) / 1e9,
         "packed_expert_frac": routed_code_bytes / (t_step * 1e-3) / 1e9 / hbm,
-        "phase_ms": {"router+shared_gate_up": float(ph[0]), "gate_up+shared_down": float(ph[1]),
-                     "down+combine": float(ph[2])},
+        "phase_ms": {"router": float(ph[0]), "gate_up+shared_gate_up": float(ph[1]),
+                     "down+shared_down+combine": float(ph[2])},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "e2e": {"value": ws * 1e3 / t_e2e, "unit": UNIT, "h2d_bytes_per_step": HIDDEN * 2,
                 "d2h_bytes_per_step": HIDDEN * 4,
@@ -341,6 +383,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch the steps directly (for profilers)")
+    ap.add_argument("--layers", type=int, default=N_LAYERS, help="distinct layers cycled through")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
