@@ -319,3 +319,65 @@ int int8_w8a16_dequant(const int8_t* W, const float* scales, int N, int Kin, flo
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// MoE block without any allocation by the caller.
+//
+// Some callers cannot allocate device memory when they run the block: an
+// operator plugin inside a framework that owns every device allocation, code
+// issuing work while a stream is being captured into a CUDA graph in a mode
+// that forbids cudaMalloc, or a process whose memory must be fixed at
+// start-up. For them the scratch lives in the buffer below, compiled into the
+// library: every GPU that loads the library holds these bytes until the
+// process exits. Host code cannot use the buffer's name as a device address,
+// so its address is looked up once per device and kept.
+// ---------------------------------------------------------------------------
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[ESCHA_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64];
+
+// Device address of g_noalloc_scratch on the current device (looked up on the
+// first call for that device).
+int noalloc_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(ESCHA_E_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64) return fail(ESCHA_E_DEVICE, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p)
+            return fail(ESCHA_E_CUDA, "cudaGetSymbolAddress(built-in scratch): %s", cudaGetErrorString(e));
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return ESCHA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int escha_moe_block_noalloc(const escha_moe_layer* L, const uint16_t* x, int T, float* out, int32_t* ids_out,
+                            float* w_out, void* stream) {
+    int r = check_layer(L);
+    if (r) return r;
+    if (T < 1) return fail(ESCHA_E_ARG, "moe_block_noalloc: T=%d must be >= 1", T);
+    const size_t need = moe_ws_layout(L, T).total;
+    if (need > (size_t)ESCHA_NOALLOC_SCRATCH_BYTES)
+        return fail(ESCHA_E_WORKSPACE,
+                    "moe_block_noalloc: this layer at T=%d needs %zu bytes of scratch, more than the %zu-byte "
+                    "built-in buffer; call escha_moe_block with a workspace instead",
+                    T, need, (size_t)ESCHA_NOALLOC_SCRATCH_BYTES);
+    void* ws = nullptr;
+    if ((r = noalloc_scratch(&ws))) return r;
+    // Nothing in the scratch has to start at zero: the status word is reset
+    // by the router kernel and every other region is written before it is read.
+    return moe_block_impl(L, x, T, out, ids_out, w_out, ws, (size_t)ESCHA_NOALLOC_SCRATCH_BYTES, stream, nullptr);
+}
+
+}  // extern "C"

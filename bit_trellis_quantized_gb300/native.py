@@ -38,6 +38,7 @@ EXPORTS = [
     "escha_moe_block_workspace",
     "escha_moe_block",
     "escha_moe_block_timed",
+    "escha_moe_block_noalloc",
     "int8_w8a16_workspace",
     "int8_w8a16_matvec",
     "int8_w8a16_dequant",
@@ -101,6 +102,8 @@ def lib() -> ctypes.CDLL:
         L.escha_moe_block_timed.argtypes = [ctypes.POINTER(EschaMoeLayer), _vp, _i, _vp, _vp, _vp, _vp, _sz, _vp,
                                             ctypes.POINTER(_vp)]
         L.escha_moe_block_timed.restype = _i
+        L.escha_moe_block_noalloc.argtypes = [ctypes.POINTER(EschaMoeLayer), _vp, _i, _vp, _vp, _vp, _vp]
+        L.escha_moe_block_noalloc.restype = _i
         L.int8_w8a16_workspace.argtypes = [_i, _i, _i]
         L.int8_w8a16_workspace.restype = _sz
         L.int8_w8a16_matvec.argtypes = [_vp, _vp, _i, _i, _vp, _i, _i, _vp, _vp, _sz, _vp]

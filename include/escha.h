@@ -168,6 +168,29 @@ int escha_moe_block(const escha_moe_layer* L, const uint16_t* x, int T, float* o
 int escha_moe_block_timed(const escha_moe_layer* L, const uint16_t* x, int T, float* out, int32_t* ids_out,
                           float* w_out, void* ws, size_t ws_bytes, void* stream, void* const* events);
 
+/* ---- MoE block with built-in scratch (no allocation by the caller) -------
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot allocate device memory when they run the block (an operator
+ * plugin in a framework that owns all device allocations, work issued while a
+ * stream is captured into a CUDA graph in a mode that forbids cudaMalloc, a
+ * process whose memory is fixed at start-up). Same computation, arguments,
+ * outputs and errors as escha_moe_block, minus the workspace: the scratch is a
+ * device buffer of ESCHA_NOALLOC_SCRATCH_BYTES built into the library, which
+ * every GPU that loads the library holds until the process exits.
+ *   - Calls whose escha_moe_block_workspace(L, T) exceeds the buffer are
+ *     rejected with ESCHA_E_WORKSPACE before anything is enqueued (about
+ *     T <= 8 tokens for a hidden-2048, inter-512, 256-expert, top-8 layer).
+ *   - The first call on a device looks the buffer's device address up
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - All calls on a device share the one buffer, which keeps the last call's
+ *     contents: calls that can overlap on the GPU (different streams without
+ *     ordering between them) race and corrupt each other's results. Nothing
+ *     in the buffer needs to be zero beforehand.
+ *   - The library allocates nothing for this call. */
+#define ESCHA_NOALLOC_SCRATCH_BYTES (2u << 20)
+int escha_moe_block_noalloc(const escha_moe_layer* L, const uint16_t* x, int T, float* out, int32_t* ids_out,
+                            float* w_out, void* stream);
+
 /* ---- int8 w8a16 ----------------------------------------------------------
  * y[m][o] = sum_i (scale[o] * W[o][i]) * x[m][i], f32 output, with the int8
  * weights used as stored (no dequantised copy) [MTPLX PR #242 "serve Qwen3.6-35B-A3B-Escha-W2 natively", table
