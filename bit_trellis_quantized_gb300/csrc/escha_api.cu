@@ -78,7 +78,7 @@ int check_trellis(const uint16_t* codes, int in, int out, int K, int mult, const
 
 // Workspace layout of escha_moe_block (256-byte aligned regions).
 struct MoeWs {
-    size_t err, logits, ids, w, ygu, shgu, shgate, sh, total;
+    size_t err, logits, ids, w, ygu, shgu, shgate, sh, d, grp, total;
 };
 
 MoeWs moe_ws_layout(const escha_moe_layer* L, int T) {
@@ -101,6 +101,11 @@ MoeWs moe_ws_layout(const escha_moe_layer* L, int T) {
     off += align_up((size_t)T * 4);
     m.sh = off;
     off += align_up(L->sh_inter > 0 ? (size_t)T * L->hidden * 4 : 0);
+    const bool grouped = T > escha::kSlotModeMaxT;
+    m.d = off;
+    off += align_up(grouped ? slots * (size_t)L->hidden * 4 : 0);
+    m.grp = off;
+    off += align_up(grouped ? escha::grouped_extra_bytes(T, L->topk, L->n_experts) : 0);
     m.total = off;
     return m;
 }
@@ -215,6 +220,7 @@ int moe_block_impl(const escha_moe_layer* L, const uint16_t* x, int T, float* ou
     int r = check_layer(L);
     if (r) return r;
     if (T < 1) return fail(ESCHA_E_ARG, "moe_block: T=%d must be >= 1", T);
+    if (T > 8192) return fail(ESCHA_E_SHAPE, "moe_block: T=%d above 8192 tokens per call", T);
     if (!x || !out) return fail(ESCHA_E_ARG, "moe_block: null x / out");
     if (!aligned16(x) || !aligned16(out) || (ids_out && !aligned16(ids_out)) || (w_out && !aligned16(w_out)))
         return fail(ESCHA_E_ALIGN, "moe_block: x / out / ids_out / w_out not 16-byte aligned");
@@ -257,6 +263,32 @@ int moe_block_impl(const escha_moe_layer* L, const uint16_t* x, int T, float* ou
     a.shgate = reinterpret_cast<float*>(base + m.shgate);
     a.sh = reinterpret_cast<float*>(base + m.sh);
     a.err = reinterpret_cast<int*>(base + m.err);
+    if (T > escha::kSlotModeMaxT) {
+        int* g = reinterpret_cast<int*>(base + m.grp);
+        a.grp_counts = g;
+        a.grp_offsets = a.grp_counts + L->n_experts;
+        a.grp_items = a.grp_offsets + L->n_experts + 1;
+        a.grp_nitems = a.grp_items + (T * L->topk) / escha::kGrpTok + L->n_experts;
+        a.grp_perm = a.grp_nitems + 1;
+        float* d = reinterpret_cast<float*>(base + m.d);
+        if ((r = record(ev, 0, s))) return r;
+        if ((r = cuda_status(escha::launch_moe_router(a, s), "router launch"))) return r;
+        if ((r = record(ev, 1, s))) return r;
+        if ((r = cuda_status(escha::launch_moe_grouped(a, d, sms, s), "grouped expert launch"))) return r;
+        if ((r = record(ev, 2, s))) return r;
+        if (L->sh_inter > 0) {
+            if ((r = cuda_status(escha::launch_int8_gemv(L->sh_gu_w8, L->sh_gu_scale, 2 * L->sh_inter, L->hidden, x,
+                                                         ESCHA_F16, L->hidden, 0, T, a.shgu, 2 * L->sh_inter, sms, s),
+                                 "shared gate_up launch")))
+                return r;
+            if ((r = cuda_status(escha::launch_int8_gemv(L->sh_dn_w8, L->sh_dn_scale, L->hidden, L->sh_inter, a.shgu,
+                                                         ESCHA_F32, 2 * L->sh_inter, 1, T, a.sh, L->hidden, sms, s),
+                                 "shared down launch")))
+                return r;
+        }
+        if ((r = cuda_status(escha::launch_moe_combine(a, d, s), "combine launch"))) return r;
+        return record(ev, 3, s);
+    }
 
     if ((r = record(ev, 0, s))) return r;
     if ((r = cuda_status(escha::launch_moe_router(a, s), "router launch"))) return r;

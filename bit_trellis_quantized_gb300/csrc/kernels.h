@@ -72,7 +72,24 @@ struct MoeArgs {
     int* err;        // set non-zero if a bounded wait gave up (zeroed by the router kernel)
     int gu_kt_per_cta;  // filled by the gate_up launcher
     int dn_ksplit;      // filled by the down launcher
+    // grouped path (T > kSlotModeMaxT): token grouping by expert
+    int* grp_counts;   // [E]
+    int* grp_offsets;  // [E+1]
+    int* grp_items;    // [T*topk/kGrpTok + E]: (expert << 16) | first position in its group
+    int* grp_nitems;   // [1]
+    int* grp_perm;     // [T*topk]: slots t*topk + j sorted stably by expert
 };
+
+// Tokens per work item of the grouped (tensor-core) path and the largest
+// batch that runs the per-slot GEMV path instead.
+constexpr int kGrpTok = 64;
+constexpr int kSlotModeMaxT = 4;
+
+size_t grouped_extra_bytes(int T, int topk, int E);
+// top-k, grouping, grouped gate_up and down GEMMs (down output d [T*topk][hidden]).
+cudaError_t launch_moe_grouped(const MoeArgs& a, float* d, int num_sms, cudaStream_t s);
+// out = sum_j w * d + sigmoid(gate) * sh
+cudaError_t launch_moe_combine(const MoeArgs& a, const float* d, cudaStream_t s);
 
 cudaError_t launch_moe_router(const MoeArgs& a, cudaStream_t s);
 cudaError_t launch_moe_gate_up(const MoeArgs& a, int num_sms, cudaStream_t s);

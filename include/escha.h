@@ -149,7 +149,10 @@ typedef struct escha_moe_layer {
  * to 0 when its first kernel starts and to a non-zero value if a kernel had
  * to give up waiting on a cluster peer (it then returns instead of hanging;
  * the outputs of that call are invalid). Read it after synchronising.
- *   x       fp16 [T][hidden];  T >= 1
+ * Batches of up to 4 tokens run fused decode GEMVs per (token, expert);
+ * larger batches group the tokens by expert and decode each expert's codes
+ * once per group of up to 64 tokens, feeding tcgen05 tensor-core MMAs.
+ *   x       fp16 [T][hidden];  1 <= T <= 8192
  *   out     f32 [T][hidden] output
  *   ids_out int32 [T][topk] output, may be null
  *   w_out   f32 [T][topk] output, may be null

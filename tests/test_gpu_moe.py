@@ -33,6 +33,8 @@ def _check_block(native, d, x, topk, tokens=None):
     assert np.allclose(w, ref_w, rtol=1e-5, atol=1e-6)
     rows = slice(None) if tokens is None else list(tokens)
     err = rel_err_rows(out[rows], ref)
+    status = int(block.workspace(x.shape[0])[:4].view(torch.int32).item())
+    assert status == 0, "a bounded wait gave up"
     assert err.max() <= TOL, err
     return out, ids, w
 
@@ -124,3 +126,48 @@ def test_moe_pruned_gate_up_channels_stay_zero(native):
     assert pruned[:256].sum() == pruned[256:].sum() > 0
     assert np.array_equal(pruned[:256], pruned[256:])
     assert np.all(y[0, pruned] == 0)
+
+
+# --------------------------------------------------------------- grouped path
+# More than 4 tokens per call run the grouped path: tokens sorted by expert,
+# each expert decoded once per group of up to 64 tokens into tcgen05 MMAs.
+
+
+def test_moe_grouped_small_groups(native):
+    d = gen.moe_layer(23, hidden=512, inter=256, n_experts=16, k_gu=3, k_dn=2)
+    x = gen.fp16_normal(gen.rng(24), (40, 512))
+    _check_block(native, d, x, topk=4)
+
+
+def test_moe_grouped_multiple_items_per_expert(native):
+    """300 tokens over 8 experts, top-2: about 75 slots per expert, so each
+    expert spans two 64-token work items."""
+    d = gen.moe_layer(25, hidden=256, inter=128, n_experts=8, k_gu=2, k_dn=3)
+    x = gen.fp16_normal(gen.rng(26), (300, 256))
+    _check_block(native, d, x, topk=2, tokens=range(0, 300, 7))
+
+
+def test_moe_grouped_full_size_batch64_sampled(native):
+    """The full Qwen3.6-35B-A3B-shaped block at batch 64; the oracle checks a
+    sample of tokens one by one (routing for all 64)."""
+    d = gen.moe_layer(1003)
+    x = gen.fp16_normal(gen.rng(2004), (64, 2048))
+    _check_block(native, d, x, topk=8, tokens=[0, 17, 38, 63])
+
+
+def test_moe_grouped_deterministic(native):
+    d = gen.moe_layer(27, hidden=512, inter=256, n_experts=16)
+    x = dev(gen.fp16_normal(gen.rng(28), (33, 512)))
+    block = native.MoeBlock(d, topk=4)
+    a = block(x)[0].cpu().numpy()
+    b = block(x)[0].cpu().numpy()
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_moe_grouped_status_word_clear(native):
+    d = gen.moe_layer(29, hidden=512, inter=256, n_experts=16)
+    x = dev(gen.fp16_normal(gen.rng(30), (20, 512)))
+    block = native.MoeBlock(d, topk=4)
+    block(x)
+    torch.cuda.synchronize()
+    assert int(block.workspace(20)[:4].view(torch.int32).item()) == 0
