@@ -77,8 +77,20 @@ int check_trellis(const uint16_t* codes, int in, int out, int K, int mult, const
 }
 
 // Workspace layout of escha_moe_block (256-byte aligned regions).
+// int8 w8a16 product of M tokens: the tensor-core GEMM from kInt8GemmMinM
+// tokens on (when Kin allows it and an image buffer is given), else the GEMV.
+cudaError_t int8_matmul(const int8_t* W, const float* scales, int N, int Kin, const void* x, int x_dtype,
+                        long long x_stride, int act, int M, float* y, long long y_stride, void* img, int sms,
+                        cudaStream_t s) {
+    if (M >= escha::kInt8GemmMinM && Kin % 128 == 0 && img)
+        return escha::launch_int8_gemm(W, scales, N, Kin, x, x_dtype, x_stride, act, M, y, y_stride, img, s);
+    return escha::launch_int8_gemv(W, scales, N, Kin, x, x_dtype, x_stride, act, M, y, y_stride, sms, s);
+}
+
+bool int8_uses_gemm(int Kin, int M) { return M >= escha::kInt8GemmMinM && Kin % 128 == 0; }
+
 struct MoeWs {
-    size_t err, logits, ids, w, ygu, shgu, shgate, sh, d, grp, total;
+    size_t err, logits, ids, w, ygu, shgu, shgate, sh, d, grp, img, total;
 };
 
 MoeWs moe_ws_layout(const escha_moe_layer* L, int T) {
@@ -104,8 +116,11 @@ MoeWs moe_ws_layout(const escha_moe_layer* L, int T) {
     const bool grouped = T > escha::kSlotModeMaxT;
     m.d = off;
     off += align_up(grouped ? slots * (size_t)L->hidden * 4 : 0);
+    const escha::GroupPlan g = escha::group_plan(T, L->topk, L->n_experts, L->hidden, L->inter, L->sh_inter);
     m.grp = off;
-    off += align_up(grouped ? escha::grouped_extra_bytes(T, L->topk, L->n_experts) : 0);
+    off += align_up(grouped ? g.int_bytes : 0);
+    m.img = off;
+    off += align_up(grouped ? g.img_bytes : 0);
     m.total = off;
     return m;
 }
@@ -264,12 +279,20 @@ int moe_block_impl(const escha_moe_layer* L, const uint16_t* x, int T, float* ou
     a.sh = reinterpret_cast<float*>(base + m.sh);
     a.err = reinterpret_cast<int*>(base + m.err);
     if (T > escha::kSlotModeMaxT) {
+        const escha::GroupPlan gp = escha::group_plan(T, L->topk, L->n_experts, L->hidden, L->inter, L->sh_inter);
+        const int E = L->n_experts, S = T * L->topk;
         int* g = reinterpret_cast<int*>(base + m.grp);
+        a.grp_cap = gp.cap;
+        a.grp_max_items = gp.max_items;
         a.grp_counts = g;
-        a.grp_offsets = a.grp_counts + L->n_experts;
-        a.grp_items = a.grp_offsets + L->n_experts + 1;
-        a.grp_nitems = a.grp_items + (T * L->topk) / escha::kGrpTok + L->n_experts;
+        a.grp_offsets = a.grp_counts + E;
+        a.grp_poff = a.grp_offsets + E + 1;
+        a.grp_items = a.grp_poff + E;
+        a.grp_nitems = a.grp_items + gp.max_items;
         a.grp_perm = a.grp_nitems + 1;
+        a.grp_ppos = a.grp_perm + S;
+        a.grp_img = reinterpret_cast<uint8_t*>(base + m.img);
+        a.grp_img_rows = 2 * gp.pos_cap;
         float* d = reinterpret_cast<float*>(base + m.d);
         if ((r = record(ev, 0, s))) return r;
         if ((r = cuda_status(escha::launch_moe_router(a, s), "router launch"))) return r;
@@ -277,12 +300,12 @@ int moe_block_impl(const escha_moe_layer* L, const uint16_t* x, int T, float* ou
         if ((r = cuda_status(escha::launch_moe_grouped(a, d, sms, s), "grouped expert launch"))) return r;
         if ((r = record(ev, 2, s))) return r;
         if (L->sh_inter > 0) {
-            if ((r = cuda_status(escha::launch_int8_gemv(L->sh_gu_w8, L->sh_gu_scale, 2 * L->sh_inter, L->hidden, x,
-                                                         ESCHA_F16, L->hidden, 0, T, a.shgu, 2 * L->sh_inter, sms, s),
+            if ((r = cuda_status(int8_matmul(L->sh_gu_w8, L->sh_gu_scale, 2 * L->sh_inter, L->hidden, x, ESCHA_F16,
+                                             L->hidden, 0, T, a.shgu, 2 * L->sh_inter, a.grp_img, sms, s),
                                  "shared gate_up launch")))
                 return r;
-            if ((r = cuda_status(escha::launch_int8_gemv(L->sh_dn_w8, L->sh_dn_scale, L->hidden, L->sh_inter, a.shgu,
-                                                         ESCHA_F32, 2 * L->sh_inter, 1, T, a.sh, L->hidden, sms, s),
+            if ((r = cuda_status(int8_matmul(L->sh_dn_w8, L->sh_dn_scale, L->hidden, L->sh_inter, a.shgu, ESCHA_F32,
+                                             2 * L->sh_inter, 1, T, a.sh, L->hidden, a.grp_img, sms, s),
                                  "shared down launch")))
                 return r;
         }
@@ -317,15 +340,12 @@ int escha_moe_block_timed(const escha_moe_layer* L, const uint16_t* x, int T, fl
 
 size_t int8_w8a16_workspace(int N, int Kin, int M) {
     (void)N;
-    (void)Kin;
-    (void)M;
-    return 0;
+    if (M < 1 || Kin < 16) return 0;
+    return int8_uses_gemm(Kin, M) ? escha::int8_gemm_image_bytes(Kin, M) : 0;
 }
 
 int int8_w8a16_matvec(const int8_t* W, const float* scales, int N, int Kin, const void* x, int x_dtype, int M,
                       float* y, void* ws, size_t ws_bytes, void* stream) {
-    (void)ws;
-    (void)ws_bytes;
     if (!W || !scales || !x || !y) return fail(ESCHA_E_ARG, "int8_w8a16_matvec: null pointer");
     if (N < 1 || M < 1) return fail(ESCHA_E_ARG, "int8_w8a16_matvec: N=%d M=%d must be >= 1", N, M);
     if (Kin < 16 || Kin % 16 || Kin > 51200)
@@ -334,11 +354,18 @@ int int8_w8a16_matvec(const int8_t* W, const float* scales, int N, int Kin, cons
         return fail(ESCHA_E_ARG, "int8_w8a16_matvec: x_dtype=%d", x_dtype);
     if (!aligned16(W) || !aligned16(scales) || !aligned16(x) || !aligned16(y))
         return fail(ESCHA_E_ALIGN, "int8_w8a16_matvec: pointer not 16-byte aligned");
+    const bool gemm = int8_uses_gemm(Kin, M);
+    if (gemm) {
+        const size_t need = escha::int8_gemm_image_bytes(Kin, M);
+        if (!ws || ws_bytes < need)
+            return fail(ESCHA_E_WORKSPACE, "int8_w8a16_matvec: workspace of %zu bytes, %zu needed", ws_bytes, need);
+        if (!aligned16(ws)) return fail(ESCHA_E_ALIGN, "int8_w8a16_matvec: workspace not 16-byte aligned");
+    }
     int r, sms;
     if ((r = device_check(&sms))) return r;
-    return cuda_status(escha::launch_int8_gemv(W, scales, N, Kin, x, x_dtype, Kin, 0, M, y, N, sms,
-                                               static_cast<cudaStream_t>(stream)),
-                       "int8 gemv launch");
+    return cuda_status(int8_matmul(W, scales, N, Kin, x, x_dtype, Kin, 0, M, y, N, gemm ? ws : nullptr, sms,
+                                   static_cast<cudaStream_t>(stream)),
+                       "int8 matmul launch");
 }
 
 int int8_w8a16_dequant(const int8_t* W, const float* scales, int N, int Kin, float* out, void* stream) {

@@ -1,0 +1,231 @@
+// int8 w8a16 GEMM on the 5th-generation tensor cores, for many tokens:
+// y[m][o] = scale[o] * sum_i W[o][i] * x[m][i] (MTPLX PR #242, table
+// "Improvements": int8 non-experts used as stored, no dequant at load; MLX
+// model card, table "Exactness of every tensor": dequant = f32 scale * w8).
+//
+// Operands. An int8 weight is an integer in [-128, 127], exact in fp16 and in
+// bf16, so A (128 weight rows per CTA) is the int8 block converted exactly to
+// the activation's 16-bit type: fp16 x and bf16 x are then used as they are
+// (exact products, f32 accumulation). f32 activations (and SwiGLU of an f32
+// gate/up pair, act == 1) are split into bf16 hi + lo (16 significant bits,
+// relative error <= 2^-17, full f32 range) and both rows enter the MMA; the
+// epilogue adds the two columns. The row scale multiplies the finished sum.
+//
+// Kernels: a prep kernel writes the activations as the MMA's B image (K-major,
+// 128-byte swizzled, every 64-value chunk holding all rows), then one CTA per
+// (128 outputs, 256 image rows) runs the shared tensor-core main loop: the
+// 256 threads convert the next int8 block while the MMAs of the current one
+// run; B blocks arrive by bulk copy.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "tc_mainloop.cuh"
+#include "trellis_core.cuh"
+
+namespace escha {
+
+namespace {
+
+constexpr int kDtF16 = 1, kDtBf16 = 2, kDtF32 = 3;
+constexpr int kRowsPerCta = 256;  // image rows (B rows) per CTA = MMA N at most
+
+__host__ __device__ __forceinline__ int img_rows_for(int parts, int M) { return (parts * M + 7) & ~7; }
+
+// One warp per (token m, 128-value block).
+__global__ void __launch_bounds__(256) int8_prep_kernel(const void* __restrict__ x, int x_dtype, long long x_stride,
+                                                        int act, int M, int Kin, uint8_t* __restrict__ img,
+                                                        int img_rows) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_wait();
+    pdl_trigger();
+    const int nblk = Kin >> 7;
+    const long long task = (long long)blockIdx.x * 8 + warp;
+    if (task >= (long long)M * nblk) return;
+    const int m = static_cast<int>(task / nblk), b = static_cast<int>(task % nblk);
+    const int k = b * 128 + 4 * lane;
+    uint8_t* base = img + (long long)(2 * b + (lane >> 4)) * img_rows * 128;
+    const uint32_t k_in = static_cast<uint32_t>((4 * lane) & 63);
+    if (act == 0 && x_dtype != kDtF32) {  // 16-bit x: copied as is
+        const uint2 v = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(x) + m * x_stride + k);
+        *reinterpret_cast<uint2*>(base + tc::kmajor_off(static_cast<uint32_t>(m), k_in)) = v;
+        return;
+    }
+    float v[4];
+    const float* xr = static_cast<const float*>(x) + m * x_stride;
+    if (act == 1) {
+        const float4 g = *reinterpret_cast<const float4*>(xr + k);
+        const float4 u = *reinterpret_cast<const float4*>(xr + Kin + k);
+        v[0] = silu_f(g.x) * u.x;
+        v[1] = silu_f(g.y) * u.y;
+        v[2] = silu_f(g.z) * u.z;
+        v[3] = silu_f(g.w) * u.w;
+    } else {
+        const float4 g = *reinterpret_cast<const float4*>(xr + k);
+        v[0] = g.x;
+        v[1] = g.y;
+        v[2] = g.z;
+        v[3] = g.w;
+    }
+    uint32_t hv[2], lv[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * q]), h1 = __float2bfloat16_rn(v[2 * q + 1]);
+        const __nv_bfloat16 l0 = __float2bfloat16_rn(v[2 * q] - __bfloat162float(h0));
+        const __nv_bfloat16 l1 = __float2bfloat16_rn(v[2 * q + 1] - __bfloat162float(h1));
+        hv[q] = static_cast<uint32_t>(__bfloat16_as_ushort(h0)) | (static_cast<uint32_t>(__bfloat16_as_ushort(h1)) << 16);
+        lv[q] = static_cast<uint32_t>(__bfloat16_as_ushort(l0)) | (static_cast<uint32_t>(__bfloat16_as_ushort(l1)) << 16);
+    }
+    *reinterpret_cast<uint2*>(base + tc::kmajor_off(2u * m, k_in)) = make_uint2(hv[0], hv[1]);
+    *reinterpret_cast<uint2*>(base + tc::kmajor_off(2u * m + 1u, k_in)) = make_uint2(lv[0], lv[1]);
+}
+
+// Four int8 values (one 32-bit word) as two packed 16-bit pairs, exactly.
+template <bool BF16>
+__device__ __forceinline__ uint2 i8x4_to_16(uint32_t w) {
+    if constexpr (BF16) {
+        float f[4];
+        i8x4_to_f32(w, f);
+        const __nv_bfloat162 a = __floats2bfloat162_rn(f[0], f[1]);
+        const __nv_bfloat162 b = __floats2bfloat162_rn(f[2], f[3]);
+        return make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+    } else {
+        // byte b biased to u = b + 128 under the fp16 exponent of 1024 (ulp 1):
+        // 1024 + u, minus 1152, is b exactly
+        const uint32_t u = w ^ 0x80808080u;
+        const uint32_t p01 = __byte_perm(u, 0x64646464u, 0x4140);
+        const uint32_t p23 = __byte_perm(u, 0x64646464u, 0x4342);
+        const __half2 off = __half2half2(__ushort_as_half(0x6480));  // 1152
+        const __half2 a = __hsub2(*reinterpret_cast<const __half2*>(&p01), off);
+        const __half2 b = __hsub2(*reinterpret_cast<const __half2*>(&p23), off);
+        return make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+    }
+}
+
+template <bool BF16, int PARTS>
+__global__ void __launch_bounds__(tc::kMlThreads, 1)
+    int8_gemm_kernel(const int8_t* __restrict__ W, const float* __restrict__ scales, int N, int Kin,
+                     const uint8_t* __restrict__ img, int img_rows, int M, float* __restrict__ y, long long y_stride) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    constexpr uint32_t kBChunk = kRowsPerCta * 128;
+    uint8_t* Abuf = smem;                         // [2][32 KB]: two 64-value K-major chunks of 128 rows
+    uint8_t* Bbuf = smem + 2 * tc::kABlockBytes;  // [2][2 chunks][256 rows x 128 B]
+    __shared__ tc::MmaBars bars;
+    __shared__ uint32_t tmem_base;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n0 = blockIdx.x * 128;
+    const int R0 = blockIdx.y * kRowsPerCta;
+
+    pdl_wait();  // the B image is complete
+    pdl_trigger();
+    const int nrows = min(kRowsPerCta, img_rows - R0);  // a multiple of 8
+    const int npad = (nrows + 15) & ~15;
+    if (tid == 0) tc::mma_bars_init(bars);
+    if (warp == 0) {
+        tc::tmem_alloc(&tmem_base, 256);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = tmem_base;
+    const uint32_t idesc = tc::idesc_f16(128, npad, false, false, BF16);
+
+    // thread t converts row t/2, values 64*(t%2) .. +63 of every 128-value block
+    const int r = tid >> 1, h = tid & 1;
+    const int8_t* wrow = W + (long long)min(n0 + r, N - 1) * Kin + 64 * h;
+    const int nblk = Kin >> 7;
+    uint4 cur[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) cur[j] = __ldg(reinterpret_cast<const uint4*>(wrow) + j);
+
+    const bool ok = tc::mma_mainloop<false>(
+        Abuf, Bbuf, kBChunk, img + (long long)R0 * 128, (long long)img_rows * 128, static_cast<uint32_t>(nrows) * 128u,
+        nblk, tmem, idesc, bars, [&](int b, uint8_t* A) {
+            uint4 nxt[4];
+            const bool more = b + 1 < nblk;
+            if (more) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) nxt[j] = __ldg(reinterpret_cast<const uint4*>(wrow + (b + 1) * 128) + j);
+            }
+            uint8_t* dst = A + h * 16384;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint2 x0 = i8x4_to_16<BF16>(cur[j].x), x1 = i8x4_to_16<BF16>(cur[j].y);
+                const uint2 x2 = i8x4_to_16<BF16>(cur[j].z), x3 = i8x4_to_16<BF16>(cur[j].w);
+                *reinterpret_cast<uint4*>(dst + tc::kmajor_off(static_cast<uint32_t>(r), 16u * j)) =
+                    make_uint4(x0.x, x0.y, x1.x, x1.y);
+                *reinterpret_cast<uint4*>(dst + tc::kmajor_off(static_cast<uint32_t>(r), 16u * j + 8u)) =
+                    make_uint4(x2.x, x2.y, x3.x, x3.y);
+            }
+            if (more) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) cur[j] = nxt[j];
+            }
+        });
+
+    // epilogue: TMEM lane = output row, column = image row; warps w and w + 4
+    // share lane quarter w % 4 and split the columns. A bounded wait that gave
+    // up leaves NaN in the CTA's outputs.
+    {
+        const int q = warp & 3;
+        const int n = n0 + 32 * q + lane;
+        const float sc = !ok ? __int_as_float(0x7fc00000) : (n < N ? scales[n] : 0.f);
+        for (int c0 = 16 * (warp >> 2); c0 < npad; c0 += 32) {
+            float v[16];
+            tc::tmem_ld16(tmem + (static_cast<uint32_t>(32 * q) << 16) + c0, v);
+            tc::tmem_ld_wait();
+            if (n >= N) continue;
+            if constexpr (PARTS == 1) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int m = R0 + c0 + i;
+                    if (m < M) y[m * y_stride + n] = sc * v[i];
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int m = (R0 + c0) / 2 + i;
+                    if (m < M) y[m * y_stride + n] = sc * (v[2 * i] + v[2 * i + 1]);
+                }
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, 256);
+}
+
+template <bool BF16, int PARTS>
+cudaError_t launch_gemm(const int8_t* W, const float* scales, int N, int Kin, const uint8_t* img, int img_rows, int M,
+                        float* y, long long y_stride, cudaStream_t s) {
+    const int smem = 2 * tc::kABlockBytes + 2 * 2 * kRowsPerCta * 128 + 1024;
+    const void* f = reinterpret_cast<const void*>(int8_gemm_kernel<BF16, PARTS>);
+    cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    void* args[] = {&W, &scales, &N, &Kin, &img, &img_rows, &M, &y, &y_stride};
+    return launch_kernel(f, dim3((N + 127) / 128, (img_rows + kRowsPerCta - 1) / kRowsPerCta), dim3(tc::kMlThreads),
+                         smem, true, s, args);
+}
+
+}  // namespace
+
+size_t int8_gemm_image_bytes(int Kin, int M) { return (size_t)Kin * img_rows_for(2, M) * 2; }
+
+cudaError_t launch_int8_gemm(const int8_t* W, const float* scales, int N, int Kin, const void* x, int x_dtype,
+                             long long x_stride, int act, int M, float* y, long long y_stride, void* img_v,
+                             cudaStream_t s) {
+    const int parts = (act == 1 || x_dtype == kDtF32) ? 2 : 1;
+    int img_rows = img_rows_for(parts, M);
+    uint8_t* img = static_cast<uint8_t*>(img_v);
+    const long long tasks = (long long)M * (Kin / 128);
+    void* pargs[] = {&x, &x_dtype, &x_stride, &act, &M, &Kin, &img, &img_rows};
+    cudaError_t e = launch_kernel(reinterpret_cast<const void*>(int8_prep_kernel),
+                                  dim3(static_cast<unsigned>((tasks + 7) / 8)), dim3(256), 0, true, s, pargs);
+    if (e != cudaSuccess) return e;
+    if (parts == 2) return launch_gemm<true, 2>(W, scales, N, Kin, img, img_rows, M, y, y_stride, s);
+    if (x_dtype == kDtBf16) return launch_gemm<true, 1>(W, scales, N, Kin, img, img_rows, M, y, y_stride, s);
+    return launch_gemm<false, 1>(W, scales, N, Kin, img, img_rows, M, y, y_stride, s);
+}
+
+}  // namespace escha

@@ -43,6 +43,20 @@ cudaError_t launch_int8_gemv(const int8_t* W, const float* scales, int N, int Ki
 
 cudaError_t launch_int8_dequant(const int8_t* W, const float* scales, int N, int Kin, float* out, cudaStream_t s);
 
+// int8 w8a16 GEMM on the tensor cores (same result as the GEMV, for many
+// tokens): a prep kernel writes x (or SwiGLU of x when act == 1) as the MMA's
+// B image into `img` (int8_gemm_image_bytes(Kin, M) bytes), then one CTA per
+// 128 outputs x 256 image rows runs the MMAs. Needs Kin % 128 == 0.
+size_t int8_gemm_image_bytes(int Kin, int M);
+constexpr int kInt8GemmMinM = 16;  // smallest M that takes the GEMM
+cudaError_t launch_int8_gemm(const int8_t* W, const float* scales, int N, int Kin, const void* x, int x_dtype,
+                             long long x_stride, int act, int M, float* y, long long y_stride, void* img,
+                             cudaStream_t s);
+
+// Launch with cudaLaunchKernelExC; pdl = programmatic dependent launch (the
+// kernel waits for its predecessor with griddepcontrol.wait).
+cudaError_t launch_kernel(const void* f, dim3 grid, dim3 block, int smem, bool pdl, cudaStream_t s, void** args);
+
 // Everything the three MoE-block kernels read and write.
 struct MoeArgs {
     int T, hidden, inter, E, topk, sh_inter;
@@ -73,19 +87,31 @@ struct MoeArgs {
     int gu_kt_per_cta;  // filled by the gate_up launcher
     int dn_ksplit;      // filled by the down launcher
     // grouped path (T > kSlotModeMaxT): token grouping by expert
-    int* grp_counts;   // [E]
-    int* grp_offsets;  // [E+1]
-    int* grp_items;    // [T*topk/kGrpTok + E]: (expert << 16) | first position in its group
-    int* grp_nitems;   // [1]
-    int* grp_perm;     // [T*topk]: slots t*topk + j sorted stably by expert
+    int grp_cap;        // tokens per work item (16, 32, 64 or 128)
+    int grp_max_items;  // T*topk/grp_cap + E
+    int* grp_counts;    // [E]
+    int* grp_offsets;   // [E+1]
+    int* grp_poff;      // [E]: first padded position of each expert (runs padded to 4 tokens)
+    int* grp_items;     // [grp_max_items]: (expert << 16) | first position in its run
+    int* grp_nitems;    // [1]
+    int* grp_perm;      // [T*topk]: slots t*topk + j sorted stably by expert
+    int* grp_ppos;      // [T*topk]: padded position of each slot
+    uint8_t* grp_img;   // B image: [in/64 chunks][grp_img_rows][128 B]
+    int grp_img_rows;   // 2 * padded positions
 };
 
-// Tokens per work item of the grouped (tensor-core) path and the largest
-// batch that runs the per-slot GEMV path instead.
-constexpr int kGrpTok = 64;
+// Largest token count of a grouped work item, and the largest batch that
+// runs the per-slot GEMV path instead.
+constexpr int kGrpCapMax = 128;
 constexpr int kSlotModeMaxT = 4;
 
-size_t grouped_extra_bytes(int T, int topk, int E);
+// Scratch of the grouped path for T tokens.
+struct GroupPlan {
+    int cap, max_items, pos_cap;
+    size_t int_bytes;  // counts, offsets, poff, items, nitems, perm, ppos
+    size_t img_bytes;  // B image (shared by both projections and the shared expert)
+};
+GroupPlan group_plan(int T, int topk, int E, int hidden, int inter, int sh_inter);
 // top-k, grouping, grouped gate_up and down GEMMs (down output d [T*topk][hidden]).
 cudaError_t launch_moe_grouped(const MoeArgs& a, float* d, int num_sms, cudaStream_t s);
 // out = sum_j w * d + sigmoid(gate) * sh

@@ -1,43 +1,39 @@
 // Batched / prefill MoE block: tokens grouped by expert, each expert's packed
-// trellis codes decoded once per group of up to kGrpTok tokens and fed to the
-// 5th-generation tensor cores (tcgen05) as a dense contraction (hipfire PR
-// #694, commits on the grouped prefill GEMM: decode each expert's weights once
-// and share them across its tokens instead of re-reading them per slot).
+// trellis codes decoded once per work item (up to `cap` of its tokens) and fed
+// to the 5th-generation tensor cores (tcgen05) as a dense contraction (hipfire
+// PR #694, commits on the grouped prefill GEMM: decode each expert's weights
+// once and share them across its tokens instead of re-reading them per slot).
 //
 // Kernels, after the router-logits kernel shared with the batch-1 path:
 //  1. top-k: one warp per token (ids ordered by (logit desc, id asc), softmax
 //     over the k selected logits).
-//  2. grouping: one CTA; stable counting sort of the (token, slot) pairs by
-//     expert -> counts, offsets, perm, and a list of work items
-//     (expert, first group position) of at most kGrpTok tokens each.
-//  3. grouped GEMM (gate_up, then down): one CTA per (work item, 128-wide
-//     output block). Per 128-input block: the 8 warps decode one tile row
-//     each into an MN-major A operand in shared memory; the input transform
-//     H128(rin * input) of the item's tokens, prescaled by 2^-8 and split into
-//     fp16 hi + lo parts, fills the K-major B operand (rows 2i and 2i+1 for
-//     token i); one thread issues the tcgen05 MMAs (M = 128 outputs, N = 2 x
-//     tokens, K = 16 per instruction) into a TMEM accumulator, double-buffered
-//     against the next block's decode. The epilogue adds the hi and lo
-//     columns, applies the output Hadamard, 2^-7 * 2^8 and rout.
-//  4. combine: out[t] = sum_j w[t][j] * down(slot t*k + j) + sigmoid(g . x[t])
-//     * shared(x[t]) in slot order; the shared expert runs on the int8 GEMV.
+//  2. grouping: one CTA; stable counting sort of the slots t*k + j by expert
+//     -> counts, offsets, perm (grouped position -> slot), each slot's padded
+//     position (every expert's run padded to a multiple of 4 tokens) and the
+//     work items (expert, first position) of at most `cap` tokens.
+//  3. prep (gate_up, later down): one warp per (slot, 128-input block) writes
+//     x~ = H128(rin_e * input) * 2^-8, split into fp16 hi and lo, as rows 2P
+//     and 2P+1 (P = padded position) of the B image, in the layout the MMA
+//     reads. The input is x[token] for gate_up, SwiGLU(gate_up output) for
+//     down.
+//  4. grouped GEMM: one CTA per (work item, 128-wide output block). The 8
+//     warps decode one tile row each per 128-input block into an MN-major A
+//     operand; the item's B rows arrive by bulk copy; one thread issues the
+//     MMAs (M = 128 outputs, N = 2 x tokens) into TMEM. The epilogue adds the
+//     hi and lo columns and applies 2^8, the output Hadamard, 2^-7 and rout.
+//  5. combine: out[t] = sum_j w[t][j] * down(slot t*k + j) + sigmoid(g . x[t])
+//     * shared(x[t]) in slot order (the shared expert runs on the int8 GEMM).
 #include "kernels.h"
-#include "tcgen05.cuh"
+#include "tc_mainloop.cuh"
 #include "trellis_core.cuh"
 
 namespace escha {
 
 namespace {
 
-constexpr int kGrpThreads = 256;
+constexpr int kGrpThreads = tc::kMlThreads;
 constexpr int kGrpWarps = kGrpThreads / 32;
-constexpr int kARowBytes = 4096;                  // one tile row: M = 128 outputs x K = 16 inputs, fp16
-constexpr int kABufBytes = 8 * kARowBytes;        // one 128-input block
-constexpr int kBRows = 2 * kGrpTok;               // hi and lo row per token
-constexpr int kBChunkBytes = kBRows * 128;        // 64 inputs of every B row
-constexpr int kBBufBytes = 2 * kBChunkBytes;      // one 128-input block
-constexpr int kSmemOperands = 2 * kABufBytes + 2 * kBBufBytes;
-constexpr float kPrescale = 0.00390625f;          // 2^-8: B operand range guard, undone in the epilogue
+constexpr float kPrescale = 0.00390625f;  // 2^-8: keeps x~ inside the fp16 range, undone in the epilogue
 
 // ---------------------------------------------------------------------------
 // 1. top-k
@@ -46,6 +42,7 @@ __global__ void __launch_bounds__(256) moe_topk_kernel(const MoeArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + warp;
     pdl_wait();
+    pdl_trigger();
     if (t >= a.T) return;
     int e;
     float w;
@@ -57,64 +54,117 @@ __global__ void __launch_bounds__(256) moe_topk_kernel(const MoeArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// 2. grouping (one CTA of 1024 threads)
+// 2. grouping (one CTA of 32 warps). Warp w owns the slots of segment w (in
+// slot order) and walks them 32 at a time; lanes holding the same expert
+// find each other with match_any, so ranks inside a round follow lane order
+// and the sort is stable without atomics.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024, 1) moe_group_kernel(const MoeArgs a) {
-    __shared__ int cnt[256];
-    __shared__ int base[256];
-    __shared__ int wcnt[32][256];  // per-warp counts of one 1024-slot chunk, then per-warp bases
+    __shared__ int hist[32][256];  // per-warp counts, then per-warp running starts within each expert
+    __shared__ int off_s[257], poff_s[257], ibase_s[257];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int S = a.T * a.topk;
+    const int S = a.T * a.topk, E = a.E, cap = a.grp_cap;
+    const int seg = (S + 31) / 32;
+    const int s_begin = warp * seg, s_end = min(S, s_begin + seg);
+    const unsigned lt = (1u << lane) - 1u;
     pdl_wait();
-    for (int e = tid; e < 256; e += 1024) cnt[e] = 0;
+    pdl_trigger();
+    for (int i = tid; i < 32 * 256; i += 1024) (&hist[0][0])[i] = 0;
     __syncthreads();
-    for (int s = tid; s < S; s += 1024) atomicAdd(&cnt[a.ids[s]], 1);
-    __syncthreads();
-    if (tid == 0) {  // exclusive scan, work items
-        int off = 0, items = 0;
-        for (int e = 0; e < a.E; ++e) {
-            a.grp_counts[e] = cnt[e];
-            a.grp_offsets[e] = off;
-            base[e] = off;
-            for (int g0 = 0; g0 < cnt[e]; g0 += kGrpTok) {
-                a.grp_items[items] = (e << 16) | g0;
-                ++items;
-            }
-            off += cnt[e];
-        }
-        a.grp_offsets[a.E] = off;
-        *a.grp_nitems = items;
+    // pass 1: per-warp counts
+    for (int s0 = s_begin; s0 < s_end; s0 += 32) {
+        const int s = s0 + lane;
+        const bool valid = s < s_end;
+        const int e = valid ? a.ids[s] : 256 + lane;
+        const unsigned m = __match_any_sync(0xffffffffu, e);
+        if (valid && (m & lt) == 0) hist[warp][e] += __popc(m);
+        __syncwarp();
     }
     __syncthreads();
-    // stable scatter, 1024 slots at a time in slot order
-    const unsigned lt = (1u << lane) - 1u;
-    for (int s0 = 0; s0 < S; s0 += 1024) {
-        const int s = s0 + tid;
-        const bool valid = s < S;
-        const int e = valid ? a.ids[s] : 256 + lane;  // invalid lanes never match a real expert
-        const unsigned m = __match_any_sync(0xffffffffu, e);
-        const int rank = __popc(m & lt);
-        for (int i = tid; i < 32 * 256; i += 1024) (&wcnt[0][0])[i] = 0;
-        __syncthreads();
-        if (valid && rank == 0) wcnt[warp][e] = __popc(m);
-        __syncthreads();
-        for (int ee = tid; ee < 256; ee += 1024) {  // per-warp exclusive bases for expert ee
-            int run = base[ee];
-            for (int w = 0; w < 32; ++w) {
-                const int c = wcnt[w][ee];
-                wcnt[w][ee] = run;
-                run += c;
-            }
-            base[ee] = run;
+    int cnt = 0;
+    if (tid < E) {  // per-expert: each warp's start inside the expert's run
+        for (int w = 0; w < 32; ++w) {
+            const int c = hist[w][tid];
+            hist[w][tid] = cnt;
+            cnt += c;
         }
-        __syncthreads();
-        if (valid) a.grp_perm[wcnt[warp][e] + rank] = s;
-        __syncthreads();
+        a.grp_counts[tid] = cnt;
+    }
+    // exclusive scans over experts (warps 0..7 hold experts 32*warp + lane)
+    __shared__ int wsum[3][8];
+    int c4 = 0, ni = 0;
+    if (tid < 256) {
+        c4 = tid < E ? (cnt + 3) & ~3 : 0;
+        ni = tid < E ? (cnt + cap - 1) / cap : 0;
+        if (tid >= E) cnt = 0;
+        int v0 = cnt, v1 = c4, v2 = ni;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int u0 = __shfl_up_sync(0xffffffffu, v0, d);
+            const int u1 = __shfl_up_sync(0xffffffffu, v1, d);
+            const int u2 = __shfl_up_sync(0xffffffffu, v2, d);
+            if (lane >= d) {
+                v0 += u0;
+                v1 += u1;
+                v2 += u2;
+            }
+        }
+        if (lane == 31) {
+            wsum[0][warp] = v0;
+            wsum[1][warp] = v1;
+            wsum[2][warp] = v2;
+        }
+        off_s[tid] = v0 - cnt;  // warp-local exclusive, completed below
+        poff_s[tid] = v1 - c4;
+        ibase_s[tid] = v2 - ni;
+    }
+    __syncthreads();
+    if (tid < 256) {
+        int b0 = 0, b1 = 0, b2 = 0;
+        for (int w = 0; w < warp; ++w) {
+            b0 += wsum[0][w];
+            b1 += wsum[1][w];
+            b2 += wsum[2][w];
+        }
+        off_s[tid] += b0;
+        poff_s[tid] += b1;
+        ibase_s[tid] += b2;
+        if (tid == 255) {
+            off_s[256] = off_s[255] + cnt;
+            poff_s[256] = poff_s[255] + c4;
+            ibase_s[256] = ibase_s[255] + ni;
+        }
+    }
+    __syncthreads();
+    if (tid < E) {
+        a.grp_offsets[tid] = off_s[tid];
+        a.grp_poff[tid] = poff_s[tid];
+        for (int j = 0; j < ni; ++j) a.grp_items[ibase_s[tid] + j] = (tid << 16) | (j * cap);
+    }
+    if (tid == 0) {
+        a.grp_offsets[E] = off_s[256];
+        *a.grp_nitems = ibase_s[256];
+    }
+    // pass 2: stable scatter
+    for (int s0 = s_begin; s0 < s_end; s0 += 32) {
+        const int s = s0 + lane;
+        const bool valid = s < s_end;
+        const int e = valid ? a.ids[s] : 256 + lane;
+        const unsigned m = __match_any_sync(0xffffffffu, e);
+        const int start = valid ? hist[warp][e] : 0;
+        __syncwarp();
+        if (valid) {
+            const int r = start + __popc(m & lt);
+            a.grp_perm[off_s[e] + r] = s;
+            a.grp_ppos[s] = poff_s[e] + r;
+            if ((m & lt) == 0) hist[warp][e] = start + __popc(m);
+        }
+        __syncwarp();
     }
 }
 
 // ---------------------------------------------------------------------------
-// 3. grouped GEMM
+// 3. prep: the B image of one projection
 // ---------------------------------------------------------------------------
 struct GroupedProj {
     const uint16_t* codes;  // [E][in/16][out/16][16K]
@@ -125,6 +175,58 @@ struct GroupedProj {
     float* y;               // [slots][out]
 };
 
+__global__ void __launch_bounds__(256) moe_prep_kernel(const MoeArgs a, const GroupedProj p) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_wait();
+    pdl_trigger();
+    const int nblk = p.in >> 7;
+    const long long task = (long long)blockIdx.x * 8 + warp;
+    if (task >= (long long)a.T * a.topk * nblk) return;
+    const int s = static_cast<int>(task / nblk), b = static_cast<int>(task % nblk);
+    const int e = a.ids[s];
+    const int P = a.grp_ppos[s];
+    const int ib = b * 128 + 4 * lane;
+    float v[4];
+    if (p.mode == 0) {
+        const uint2 xb = *reinterpret_cast<const uint2*>(a.x + (long long)(s / a.topk) * a.hidden + ib);
+        v[0] = h2f_bits(static_cast<uint16_t>(xb.x & 0xFFFFu));
+        v[1] = h2f_bits(static_cast<uint16_t>(xb.x >> 16));
+        v[2] = h2f_bits(static_cast<uint16_t>(xb.y & 0xFFFFu));
+        v[3] = h2f_bits(static_cast<uint16_t>(xb.y >> 16));
+    } else {
+        const float* yr = a.ygu + (long long)s * 2 * a.inter;
+        const float4 g = *reinterpret_cast<const float4*>(yr + ib);
+        const float4 u = *reinterpret_cast<const float4*>(yr + a.inter + ib);
+        v[0] = silu_f(g.x) * u.x;
+        v[1] = silu_f(g.y) * u.y;
+        v[2] = silu_f(g.z) * u.z;
+        v[3] = silu_f(g.w) * u.w;
+    }
+    const uint2 rb = *reinterpret_cast<const uint2*>(p.rin + (long long)e * p.in + ib);
+    v[0] *= h2f_bits(static_cast<uint16_t>(rb.x & 0xFFFFu));
+    v[1] *= h2f_bits(static_cast<uint16_t>(rb.x >> 16));
+    v[2] *= h2f_bits(static_cast<uint16_t>(rb.y & 0xFFFFu));
+    v[3] *= h2f_bits(static_cast<uint16_t>(rb.y >> 16));
+    h128_warp(v, lane);
+    uint32_t hv[2], lv[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const float s0 = v[2 * q] * kPrescale, s1 = v[2 * q + 1] * kPrescale;
+        const __half h0 = __float2half_rn(s0), h1 = __float2half_rn(s1);
+        const __half l0 = __float2half_rn(s0 - __half2float(h0)), l1 = __float2half_rn(s1 - __half2float(h1));
+        hv[q] = static_cast<uint32_t>(__half_as_ushort(h0)) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
+        lv[q] = static_cast<uint32_t>(__half_as_ushort(l0)) | (static_cast<uint32_t>(__half_as_ushort(l1)) << 16);
+    }
+    const int chunk = 2 * b + (lane >> 4);
+    const uint32_t k_in = static_cast<uint32_t>((4 * lane) & 63);
+    uint8_t* base = a.grp_img + (long long)chunk * a.grp_img_rows * 128;
+    *reinterpret_cast<uint2*>(base + tc::kmajor_off(2u * P, k_in)) = make_uint2(hv[0], hv[1]);
+    *reinterpret_cast<uint2*>(base + tc::kmajor_off(2u * P + 1u, k_in)) = make_uint2(lv[0], lv[1]);
+}
+
+// ---------------------------------------------------------------------------
+// 4. grouped GEMM
+// ---------------------------------------------------------------------------
 // The lane's 64 decoded weights of one tile row (tile lane/4, input rows
 // 4c..4c+3, 16 output columns each) written into the MN-major A slice of that
 // row: element (m = 16*(lane/4) + q, k = r) at mnmajor_off(m, k, 2048, 1024).
@@ -155,35 +257,31 @@ template <int K>
 __global__ void __launch_bounds__(kGrpThreads, 1) moe_grouped_gemm_kernel(const MoeArgs a, const GroupedProj p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* Abuf = smem;                       // [2][8 rows][4 KB]
-    uint8_t* Bbuf = smem + 2 * kABufBytes;      // [2][2 chunks][kBRows x 128 B]
-    float* zs = reinterpret_cast<float*>(smem); // epilogue: [kGrpTok][128] f32, reuses the A buffers
-    __shared__ __align__(8) unsigned long long mma_done[2];
+    const int cap = a.grp_cap;
+    const uint32_t b_chunk = 256u * static_cast<uint32_t>(cap);  // 2*cap rows x 128 B
+    uint8_t* Abuf = smem;                                         // [2][32 KB]
+    uint8_t* Bbuf = smem + 2 * tc::kABlockBytes;                  // [2][2 chunks][b_chunk]
+    float* zs = reinterpret_cast<float*>(smem);                   // epilogue: [cap][128] f32 over the A buffers
+    __shared__ tc::MmaBars bars;
     __shared__ uint32_t tmem_base;
-    __shared__ int slot_s[kGrpTok];
-    __shared__ int row_s[kGrpTok];  // x row (token) for mode 0, slot for mode 1
+    __shared__ int slot_s[kGrpCapMax];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int ob = blockIdx.x;
     const int item = blockIdx.y;
 
-    pdl_wait();  // grouping (and for down, the gate_up outputs) complete
+    pdl_wait();  // the B image (and the grouping) are complete
     pdl_trigger();
     if (item >= *a.grp_nitems) return;
     const int packed = a.grp_items[item];
     const int e = packed >> 16, g0 = packed & 0xFFFF;
-    const int nt = min(kGrpTok, a.grp_counts[e] - g0);
+    const int nt = min(cap, a.grp_counts[e] - g0);
     const int npad = (2 * nt + 15) & ~15;  // MMA N: hi/lo rows of nt tokens, multiple of 16
-    for (int i = tid; i < kGrpTok; i += kGrpThreads) {
-        const int s = i < nt ? a.grp_perm[a.grp_offsets[e] + g0 + i] : 0;
-        slot_s[i] = s;
-        row_s[i] = p.mode == 0 ? s / a.topk : s;
-    }
-    if (tid == 0) {
-        tc::mbar_init_cta(tc::smem_addr(&mma_done[0]), 1);
-        tc::mbar_init_cta(tc::smem_addr(&mma_done[1]), 1);
-    }
+    const int nt4 = (nt + 3) & ~3;          // rows copied: whole 8-row atoms
+    for (int i = tid; i < nt; i += kGrpThreads) slot_s[i] = a.grp_perm[a.grp_offsets[e] + g0 + i];
+    const uint32_t tcols = 2u * static_cast<uint32_t>(cap) < 32u ? 32u : 2u * static_cast<uint32_t>(cap);
+    if (tid == 0) tc::mma_bars_init(bars);
     if (warp == 0) {
-        tc::tmem_alloc(&tmem_base, 128);
+        tc::tmem_alloc(&tmem_base, tcols);
         tc::tmem_relinquish();
     }
     tc::fence_before_sync();
@@ -194,115 +292,43 @@ __global__ void __launch_bounds__(kGrpThreads, 1) moe_grouped_gemm_kernel(const 
 
     const int KT = p.in >> 4, NT = p.out >> 4;
     const uint16_t* codes = p.codes + (long long)e * KT * NT * (16 * K);
-    const uint16_t* rin = p.rin + (long long)e * p.in;
-    const int nblk = p.in / 128;
-    bool ok = true;
+    const int nblk = p.in >> 7;
     LaneCodes<K> cur;
     load_lane_codes<K>(cur, codes + ((long long)warp * NT + ob * 8) * (16 * K), lane);
     const int nbr = (lane & ~3) | ((lane + 1) & 3);
+    const uint8_t* img = a.grp_img + (long long)2 * (a.grp_poff[e] + g0) * 128;
 
-    for (int b = 0; b < nblk; ++b) {
-        const int buf = b & 1;
-        uint8_t* A = Abuf + buf * kABufBytes;
-        uint8_t* B = Bbuf + buf * kBBufBytes;
-        if (b >= 2) {  // the MMAs of block b-2 have finished reading this buffer
-            if (!tc::mbar_wait_parity_bounded(tc::smem_addr(&mma_done[buf]), ((b >> 1) - 1) & 1)) ok = false;
-        }
-        // prefetch the next block's row while this one is decoded
-        LaneCodes<K> nxt;
-        const bool more = b + 1 < nblk;
-        if (more) load_lane_codes<K>(nxt, codes + ((long long)(8 * (b + 1) + warp) * NT + ob * 8) * (16 * K), lane);
-        // B: x~ for every token of the item, hi/lo, this block's 128 inputs
-        for (int i = warp; i < nt; i += kGrpWarps) {
-            const int ib = b * 128 + 4 * lane;
-            float v[4];
-            const uint2 rb = *reinterpret_cast<const uint2*>(rin + ib);
-            if (p.mode == 0) {
-                const uint2 xb = *reinterpret_cast<const uint2*>(a.x + (long long)row_s[i] * a.hidden + ib);
-                v[0] = h2f_bits(static_cast<uint16_t>(xb.x & 0xFFFFu));
-                v[1] = h2f_bits(static_cast<uint16_t>(xb.x >> 16));
-                v[2] = h2f_bits(static_cast<uint16_t>(xb.y & 0xFFFFu));
-                v[3] = h2f_bits(static_cast<uint16_t>(xb.y >> 16));
-            } else {
-                const float* yr = a.ygu + (long long)row_s[i] * 2 * a.inter;
-                const float4 g = *reinterpret_cast<const float4*>(yr + ib);
-                const float4 u = *reinterpret_cast<const float4*>(yr + a.inter + ib);
-                v[0] = silu_f(g.x) * u.x;
-                v[1] = silu_f(g.y) * u.y;
-                v[2] = silu_f(g.z) * u.z;
-                v[3] = silu_f(g.w) * u.w;
-            }
-            v[0] *= h2f_bits(static_cast<uint16_t>(rb.x & 0xFFFFu));
-            v[1] *= h2f_bits(static_cast<uint16_t>(rb.x >> 16));
-            v[2] *= h2f_bits(static_cast<uint16_t>(rb.y & 0xFFFFu));
-            v[3] *= h2f_bits(static_cast<uint16_t>(rb.y >> 16));
-            h128_warp(v, lane);
-            __half hi[4], lo[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float sv = v[q] * kPrescale;
-                hi[q] = __float2half_rn(sv);
-                lo[q] = __float2half_rn(sv - __half2float(hi[q]));
-            }
-            // K index inside the block: 4*lane .. 4*lane + 3 -> chunk (4*lane)/64
-            const int kk = 4 * lane;
-            uint8_t* chunk = B + (kk >> 6) * kBChunkBytes;
-            const uint32_t k_in = static_cast<uint32_t>(kk & 63);
-            const uint2 hv = make_uint2(static_cast<uint32_t>(__half_as_ushort(hi[0])) | (static_cast<uint32_t>(__half_as_ushort(hi[1])) << 16),
-                                        static_cast<uint32_t>(__half_as_ushort(hi[2])) | (static_cast<uint32_t>(__half_as_ushort(hi[3])) << 16));
-            const uint2 lv = make_uint2(static_cast<uint32_t>(__half_as_ushort(lo[0])) | (static_cast<uint32_t>(__half_as_ushort(lo[1])) << 16),
-                                        static_cast<uint32_t>(__half_as_ushort(lo[2])) | (static_cast<uint32_t>(__half_as_ushort(lo[3])) << 16));
-            *reinterpret_cast<uint2*>(chunk + tc::kmajor_off(2u * i, k_in)) = hv;
-            *reinterpret_cast<uint2*>(chunk + tc::kmajor_off(2u * i + 1u, k_in)) = lv;
-        }
-        // A: warp w decodes tile row 8b + w of output block ob
-        cur.p[2 * K] = __shfl_sync(0xffffffffu, cur.p[0], nbr) & 0xFFFFu;
-        decode_row_to_smem<K>(cur, A + warp * kARowBytes, lane);
-        if (more) cur = nxt;
-        tc::fence_proxy_async_smem();
-        tc::fence_before_sync();
-        __syncthreads();
-        if (tid == 0) {
-            tc::fence_after_sync();
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t ad =
-                    tc::smem_desc(tc::smem_addr(A + kk * kARowBytes), 2048u, 1024u, tc::kSwizzle128B);
-                const uint64_t bd = tc::smem_desc(tc::smem_addr(B + (kk >> 2) * kBChunkBytes) + (kk & 3) * 32u, 16u,
-                                                  1024u, tc::kSwizzle128B);
-                tc::mma_f16(tmem, ad, bd, idesc, b > 0 || kk > 0);
-            }
-            tc::commit(tc::smem_addr(&mma_done[buf]));
-        }
-    }
-    // the last commit covers every MMA issued before it
-    const int last = nblk - 1;
-    if (!tc::mbar_wait_parity_bounded(tc::smem_addr(&mma_done[last & 1]), (last >> 1) & 1)) ok = false;
-    if (nblk >= 2) {  // and the other buffer's final phase has completed as well
-        const int prev = nblk - 2;
-        if (!tc::mbar_wait_parity_bounded(tc::smem_addr(&mma_done[prev & 1]), (prev >> 1) & 1)) ok = false;
-    }
-    tc::fence_after_sync();
+    const bool ok = tc::mma_mainloop<true>(
+        Abuf, Bbuf, b_chunk, img, (long long)a.grp_img_rows * 128, 256u * static_cast<uint32_t>(nt4), nblk, tmem,
+        idesc, bars, [&](int b, uint8_t* A) {
+            // warp w decodes tile row 8b + w of output block ob, prefetching the next
+            LaneCodes<K> nxt;
+            const bool more = b + 1 < nblk;
+            if (more) load_lane_codes<K>(nxt, codes + ((long long)(8 * (b + 1) + warp) * NT + ob * 8) * (16 * K), lane);
+            cur.p[2 * K] = __shfl_sync(0xffffffffu, cur.p[0], nbr) & 0xFFFFu;
+            decode_row_to_smem<K>(cur, A + warp * 4096, lane);
+            if (more) cur = nxt;
+        });
     if (!ok && tid == 0) atomicExch(a.err, 3);
 
-    // epilogue: TMEM lane m holds columns 2i (hi) and 2i + 1 (lo) of token i
-    __syncthreads();  // every warp is done with the A buffers before zs overwrites them
-    if (warp < 4 && ok) {
-        const int m = 32 * warp + lane;
-        for (int c0 = 0; c0 < npad; c0 += 16) {
+    // epilogue: TMEM lane m holds columns 2i (hi) and 2i + 1 (lo) of token i;
+    // warps w and w + 4 share lane quarter w % 4 and split the columns
+    if (ok) {
+        const int q = warp & 3, m = 32 * q + lane;
+        for (int c0 = 16 * (warp >> 2); c0 < npad; c0 += 32) {
             float v[16];
-            tc::tmem_ld16(tmem + (static_cast<uint32_t>(32 * warp) << 16) + c0, v);
+            tc::tmem_ld16(tmem + (static_cast<uint32_t>(32 * q) << 16) + c0, v);
             tc::tmem_ld_wait();
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const int i = c0 / 2 + q;
-                if (i < nt) zs[i * 128 + m] = v[2 * q] + v[2 * q + 1];
+            for (int qq = 0; qq < 8; ++qq) {
+                const int i = c0 / 2 + qq;
+                if (i < nt) zs[i * 128 + m] = v[2 * qq] + v[2 * qq + 1];
             }
         }
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tmem, 128);
+    if (warp == 0) tc::tmem_dealloc(tmem, tcols);
     if (!ok) return;
     const uint16_t* rout = p.rout + (long long)e * p.out + ob * 128;
     const uint2 rb = *reinterpret_cast<const uint2*>(rout + 4 * lane);
@@ -316,7 +342,7 @@ __global__ void __launch_bounds__(kGrpThreads, 1) moe_grouped_gemm_kernel(const 
 }
 
 // ---------------------------------------------------------------------------
-// 4. combine: out[t] = sum_j w[t][j] * d[t*k + j] + sigmoid(g . x[t]) * sh[t]
+// 5. combine: out[t] = sum_j w[t][j] * d[t*k + j] + sigmoid(g . x[t]) * sh[t]
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeArgs a, const float* d) {
     const int t = blockIdx.y;
@@ -349,7 +375,26 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeArgs a, const
     a.out[(long long)t * a.hidden + i] = acc;
 }
 
-cudaError_t launch_plain(const void* f, dim3 grid, dim3 block, int smem, bool pdl, cudaStream_t s, void** args) {
+template <int K>
+cudaError_t launch_grouped(const MoeArgs& a, const GroupedProj& p, cudaStream_t s) {
+    const int smem = 2 * tc::kABlockBytes + 2 * 2 * 256 * a.grp_cap + 1024;
+    const void* f = reinterpret_cast<const void*>(moe_grouped_gemm_kernel<K>);
+    cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    void* args[] = {const_cast<MoeArgs*>(&a), const_cast<GroupedProj*>(&p)};
+    return launch_kernel(f, dim3(p.out / 128, a.grp_max_items), dim3(kGrpThreads), smem, true, s, args);
+}
+
+cudaError_t launch_prep(const MoeArgs& a, const GroupedProj& p, cudaStream_t s) {
+    const long long tasks = (long long)a.T * a.topk * (p.in / 128);
+    void* args[] = {const_cast<MoeArgs*>(&a), const_cast<GroupedProj*>(&p)};
+    return launch_kernel(reinterpret_cast<const void*>(moe_prep_kernel), dim3(static_cast<unsigned>((tasks + 7) / 8)),
+                         dim3(256), 0, true, s, args);
+}
+
+}  // namespace
+
+cudaError_t launch_kernel(const void* f, dim3 grid, dim3 block, int smem, bool pdl, cudaStream_t s, void** args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
@@ -363,45 +408,43 @@ cudaError_t launch_plain(const void* f, dim3 grid, dim3 block, int smem, bool pd
     return cudaLaunchKernelExC(&cfg, f, args);
 }
 
-template <int K>
-cudaError_t launch_grouped(const MoeArgs& a, const GroupedProj& p, cudaStream_t s) {
-    const int smem = kSmemOperands + 1024;
-    const void* f = reinterpret_cast<const void*>(moe_grouped_gemm_kernel<K>);
-    cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    // at most one partial chunk per expert on top of the full ones
-    const int max_items = (a.T * a.topk) / kGrpTok + a.E;
-    void* args[] = {const_cast<MoeArgs*>(&a), const_cast<GroupedProj*>(&p)};
-    return launch_plain(f, dim3(p.out / 128, max_items), dim3(kGrpThreads), smem, true, s, args);
-}
-
-}  // namespace
-
-size_t grouped_extra_bytes(int T, int topk, int E) {
-    // counts[E], offsets[E+1], items[T*topk/kGrpTok + E], nitems, perm[T*topk]
-    return (size_t)(E + (E + 1) + (T * topk) / kGrpTok + E + 1 + T * topk) * 4;
+GroupPlan group_plan(int T, int topk, int E, int hidden, int inter, int sh_inter) {
+    GroupPlan g{};
+    const long long S = (long long)T * topk;
+    const long long want = 2 * S / E + 8;  // twice the mean run per expert, plus slack
+    g.cap = 16;
+    while (g.cap < kGrpCapMax && g.cap < want) g.cap *= 2;
+    g.max_items = static_cast<int>(S / g.cap) + E;  // full items plus at most one partial per expert
+    g.pos_cap = static_cast<int>((S + 3 * E + 3) & ~3ll);
+    // counts[E], offsets[E+1], poff[E], items[max_items], nitems, perm[S], ppos[S]
+    g.int_bytes = (size_t)(E + (E + 1) + E + g.max_items + 1 + 2 * S) * 4;
+    const size_t trellis_img = (size_t)(hidden > inter ? hidden : inter) * 2 * g.pos_cap * 2;
+    const size_t shared_img = sh_inter > 0 ? int8_gemm_image_bytes(hidden > sh_inter ? hidden : sh_inter, T) : 0;
+    g.img_bytes = trellis_img > shared_img ? trellis_img : shared_img;
+    return g;
 }
 
 cudaError_t launch_moe_grouped(const MoeArgs& a, float* d, int num_sms, cudaStream_t s) {
     (void)num_sms;
     void* args[] = {const_cast<MoeArgs*>(&a)};
-    cudaError_t e = launch_plain(reinterpret_cast<const void*>(moe_topk_kernel), dim3((a.T + 7) / 8), dim3(256), 0,
-                                 true, s, args);
+    cudaError_t e = launch_kernel(reinterpret_cast<const void*>(moe_topk_kernel), dim3((a.T + 7) / 8), dim3(256), 0,
+                                  true, s, args);
     if (e != cudaSuccess) return e;
-    e = launch_plain(reinterpret_cast<const void*>(moe_group_kernel), dim3(1), dim3(1024), 0, true, s, args);
+    e = launch_kernel(reinterpret_cast<const void*>(moe_group_kernel), dim3(1), dim3(1024), 0, true, s, args);
     if (e != cudaSuccess) return e;
-    GroupedProj gu{a.gu_codes, a.gu_rin, a.gu_rout, a.hidden, 2 * a.inter, 0, a.ygu};
+    const GroupedProj gu{a.gu_codes, a.gu_rin, a.gu_rout, a.hidden, 2 * a.inter, 0, a.ygu};
+    if ((e = launch_prep(a, gu, s)) != cudaSuccess) return e;
     e = a.gu_K == 2 ? launch_grouped<2>(a, gu, s) : launch_grouped<3>(a, gu, s);
     if (e != cudaSuccess) return e;
-    GroupedProj dn{a.dn_codes, a.dn_rin, a.dn_rout, a.inter, a.hidden, 1, d};
-    e = a.dn_K == 2 ? launch_grouped<2>(a, dn, s) : launch_grouped<3>(a, dn, s);
-    return e;
+    const GroupedProj dn{a.dn_codes, a.dn_rin, a.dn_rout, a.inter, a.hidden, 1, d};
+    if ((e = launch_prep(a, dn, s)) != cudaSuccess) return e;
+    return a.dn_K == 2 ? launch_grouped<2>(a, dn, s) : launch_grouped<3>(a, dn, s);
 }
 
 cudaError_t launch_moe_combine(const MoeArgs& a, const float* d, cudaStream_t s) {
     void* args[] = {const_cast<MoeArgs*>(&a), const_cast<float**>(&d)};
-    return launch_plain(reinterpret_cast<const void*>(moe_combine_kernel), dim3((a.hidden + 255) / 256, a.T),
-                        dim3(256), 0, false, s, args);
+    return launch_kernel(reinterpret_cast<const void*>(moe_combine_kernel), dim3((a.hidden + 255) / 256, a.T),
+                         dim3(256), 0, true, s, args);
 }
 
 }  // namespace escha

@@ -1,0 +1,103 @@
+// Main loop shared by the tensor-core GEMMs whose A operand is made by the
+// CTA's own threads (trellis decode, int8 -> 16-bit conversion) and whose B
+// operand is a prepared image in global memory.
+//
+//   D[128][N] (TMEM, f32) = sum over K blocks of 128:  A_blk[128][128] * B_blk[N][128]^T
+//
+// Per K block, 256 threads produce A into one of two 32 KB shared buffers
+// while the MMAs of the previous block run; one thread issues the eight
+// K = 16 MMAs of the block and the bulk copy of the next block's B (two
+// 64-value chunks of N rows x 128 B each, K-major 128-byte swizzled, copied
+// as they lie in the image) into one of two B buffers.
+//
+// The B image holds, for every 64-value K chunk, all rows one after the
+// other (row r at r * 128 B, 16-byte pieces swizzled by r % 8), so a CTA's
+// rows are one contiguous range per chunk; a range starting at a multiple of
+// 8 rows lands in shared memory with the swizzle phase the MMA expects.
+#pragma once
+
+#include "tcgen05.cuh"
+
+namespace escha {
+namespace tc {
+
+constexpr int kMlThreads = 256;
+constexpr int kABlockBytes = 32768;  // 128 x 128 16-bit values
+
+struct MmaBars {
+    unsigned long long full[2];  // B block landed
+    unsigned long long done[2];  // MMAs of the block finished reading A and B
+};
+
+__device__ __forceinline__ void mma_bars_init(MmaBars& bars) {
+    mbar_init_cta(smem_addr(&bars.full[0]), 1);
+    mbar_init_cta(smem_addr(&bars.full[1]), 1);
+    mbar_init_cta(smem_addr(&bars.done[0]), 1);
+    mbar_init_cta(smem_addr(&bars.done[1]), 1);
+    fence_proxy_async_smem();
+}
+
+// A_MN: A is MN-major (eight 4 KB slices, one per K = 16 step, atoms of 64 m
+// 2048 B apart and of 8 k 1024 B apart) or K-major (two 16 KB chunks of 128
+// rows x 64 values). `produce(b, A)` writes block b's A into A and is called
+// by every thread. `img` points at the CTA's first row in chunk 0;
+// consecutive chunks are `img_chunk_bytes` apart. Returns false in every
+// thread when a bounded wait gave up.
+template <bool A_MN, class ProduceA>
+__device__ __forceinline__ bool mma_mainloop(uint8_t* Abuf, uint8_t* Bbuf, uint32_t b_chunk_bytes, const uint8_t* img,
+                                             long long img_chunk_bytes, uint32_t copy_bytes, int nblk, uint32_t tmem,
+                                             uint32_t idesc, MmaBars& bars, ProduceA&& produce) {
+    const int tid = threadIdx.x;
+    bool ok = true;
+    auto issue_b = [&](int b) {
+        const int buf = b & 1;
+        const uint32_t bar = smem_addr(&bars.full[buf]);
+        mbar_arrive_expect_tx(bar, 2u * copy_bytes);
+        uint8_t* dst = Bbuf + buf * 2 * b_chunk_bytes;
+        bulk_g2s(smem_addr(dst), img + (2ll * b) * img_chunk_bytes, copy_bytes, bar);
+        bulk_g2s(smem_addr(dst + b_chunk_bytes), img + (2ll * b + 1) * img_chunk_bytes, copy_bytes, bar);
+    };
+    if (tid == 0) issue_b(0);
+    for (int b = 0; b < nblk; ++b) {
+        const int buf = b & 1;
+        // the MMAs of block b-2 have finished with this A buffer
+        if (b >= 2 && !mbar_wait_parity_bounded(smem_addr(&bars.done[buf]), ((b >> 1) - 1) & 1)) ok = false;
+        uint8_t* A = Abuf + buf * kABlockBytes;
+        produce(b, A);
+        fence_proxy_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            fence_after_sync();
+            if (!mbar_wait_parity_bounded(smem_addr(&bars.full[buf]), (b >> 1) & 1)) ok = false;
+            const uint8_t* B = Bbuf + buf * 2 * b_chunk_bytes;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t ad =
+                    A_MN ? smem_desc(smem_addr(A + kk * 4096), 2048u, 1024u, kSwizzle128B)
+                         : smem_desc(smem_addr(A + (kk >> 2) * 16384) + (kk & 3) * 32u, 16u, 1024u, kSwizzle128B);
+                const uint64_t bd =
+                    smem_desc(smem_addr(B + (kk >> 2) * b_chunk_bytes) + (kk & 3) * 32u, 16u, 1024u, kSwizzle128B);
+                mma_f16(tmem, ad, bd, idesc, b > 0 || kk > 0);
+            }
+            commit(smem_addr(&bars.done[buf]));
+            if (b + 1 < nblk) {
+                // the next B block goes into the buffer the MMAs of block b-1 read
+                if (b >= 1 && !mbar_wait_parity_bounded(smem_addr(&bars.done[(b + 1) & 1]), ((b - 1) >> 1) & 1))
+                    ok = false;
+                issue_b(b + 1);
+            }
+        }
+    }
+    // the last commit covers every MMA issued before it; wait for the other
+    // buffer's final phase too so that no arrival is pending at exit
+    const int last = nblk - 1;
+    if (!mbar_wait_parity_bounded(smem_addr(&bars.done[last & 1]), (last >> 1) & 1)) ok = false;
+    if (nblk >= 2 && !mbar_wait_parity_bounded(smem_addr(&bars.done[(last - 1) & 1]), ((last - 1) >> 1) & 1))
+        ok = false;
+    fence_after_sync();
+    return !__syncthreads_or(!ok);
+}
+
+}  // namespace tc
+}  // namespace escha

@@ -143,6 +143,20 @@ __device__ __forceinline__ bool mbar_wait_parity_bounded(uint32_t bar, uint32_t 
         if (mbar_test_parity(bar, parity)) return true;
     return false;
 }
+// One arrival that also announces `bytes` of bulk-copy data to come.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// ---- bulk copy global -> shared (the TMA's untiled form) -----------------
+// Both addresses 16-byte aligned, bytes a multiple of 16; completion is
+// signalled to the mbarrier as transaction bytes.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst_saddr, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst_saddr),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
 
 }  // namespace tc
 }  // namespace escha

@@ -64,3 +64,55 @@ def test_matvec_lm_head_shape_sampled_rows(native):
     ref = o.int8_matvec(W[rows], s[rows], _bf16_values(xb))[0]
     full_scale = np.abs(y).max()
     assert np.max(np.abs(y[rows] - ref)) / full_scale <= TOL
+
+
+# ------------------------------------------------------- tensor-core GEMM route
+# From 16 tokens on (Kin a multiple of 128) the product runs as a tcgen05 GEMM:
+# int8 rows converted exactly to the activation's 16-bit type, f32 activations
+# split into bf16 hi + lo.
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("N,Kin,M", [(1000, 1024, 16), (256, 2048, 300), (4096, 2048, 64), (384, 512, 517)])
+def test_gemm_route(native, dtype, N, Kin, M):
+    W, s = gen.int8_matrix(N * 7 + M, N, Kin)
+    if dtype == "bf16":
+        xb = gen.bf16_normal_bits(gen.rng(M + 1), (M, Kin))
+        x, xv = _bf16_tensor(xb), _bf16_values(xb)
+    else:
+        x16 = gen.fp16_normal(gen.rng(M + 2), (M, Kin))
+        xv = x16.astype(np.float64)
+        x = dev(x16) if dtype == "f16" else dev(x16.astype(np.float32))
+        if dtype == "f32":  # values that need more than 16 bits
+            x32 = (x16.astype(np.float32) * np.float32(1.0009765625)).astype(np.float32)
+            xv = x32.astype(np.float64)
+            x = dev(x32)
+    y = native.int8_w8a16_matvec(dev(W), dev(s), x).cpu().numpy()
+    ref = o.int8_matvec(W, s, xv)
+    assert np.all(np.isfinite(y))
+    assert rel_err_rows(y, ref).max() <= TOL
+
+
+def test_gemm_route_matches_gemv_route(native):
+    """The same rows through the GEMM (M = 16) and the GEMV (M = 8, twice)."""
+    W, s = gen.int8_matrix(77, 640, 1024)
+    x16 = gen.fp16_normal(gen.rng(78), (16, 1024))
+    y_gemm = native.int8_w8a16_matvec(dev(W), dev(s), dev(x16)).cpu().numpy()
+    y_a = native.int8_w8a16_matvec(dev(W), dev(s), dev(x16[:8])).cpu().numpy()
+    y_b = native.int8_w8a16_matvec(dev(W), dev(s), dev(x16[8:])).cpu().numpy()
+    ref = o.int8_matvec(W, s, x16.astype(np.float64))
+    assert rel_err_rows(y_gemm, ref).max() <= 1e-5
+    assert rel_err_rows(np.concatenate([y_a, y_b]), ref).max() <= 1e-5
+
+
+def test_gemm_route_lm_head_prefill_sampled(native):
+    """152064 x 2048 output head at 2048 tokens (bf16): sampled rows and tokens."""
+    N, Kin, M = 152064, 2048, 2048
+    W, s = gen.int8_matrix(4005, N, Kin)
+    xb = gen.bf16_normal_bits(gen.rng(6), (M, Kin))
+    y = native.int8_w8a16_matvec(dev(W), dev(s), _bf16_tensor(xb))
+    rows = gen.rng(7).choice(N, size=256, replace=False)
+    toks = gen.rng(8).choice(M, size=16, replace=False)
+    got = y[torch.as_tensor(toks, device=y.device)][:, torch.as_tensor(rows, device=y.device)].cpu().numpy()
+    ref = o.int8_matvec(W[rows], s[rows], _bf16_values(xb[toks]))
+    assert rel_err_rows(got, ref).max() <= TOL

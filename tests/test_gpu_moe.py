@@ -155,6 +155,37 @@ def test_moe_grouped_full_size_batch64_sampled(native):
     _check_block(native, d, x, topk=8, tokens=[0, 17, 38, 63])
 
 
+@pytest.mark.parametrize("T,E,topk,tokens", [
+    (8, 64, 8, None),                     # item capacity 16, runs of 1-2 tokens
+    (96, 32, 4, range(0, 96, 5)),         # capacity 32
+    (700, 4, 1, range(0, 700, 23)),       # capacity 128, two and more items per expert
+    (130, 16, 8, range(0, 130, 9)),       # capacity 128, ragged runs
+])
+def test_moe_grouped_capacities(native, T, E, topk, tokens):
+    d = gen.moe_layer(40 + T, hidden=512, inter=256, n_experts=E, k_gu=3, k_dn=2)
+    x = gen.fp16_normal(gen.rng(41 + T), (T, 512))
+    _check_block(native, d, x, topk=topk, tokens=tokens)
+
+
+def test_moe_grouped_prefill_2048_sampled(native):
+    """2048-token prefill chunk through the full-size block (capacity 128):
+    routing checked for every token (the oracle routes 64 tokens at a time),
+    outputs for a sample of tokens."""
+    d = gen.moe_layer(1004)
+    x = gen.fp16_normal(gen.rng(2005), (2048, 2048))
+    block = native.MoeBlock(d, topk=8)
+    out, ids, w = block(dev(x))
+    out, ids, w = out.cpu().numpy(), ids.cpu().numpy(), w.cpu().numpy()
+    assert int(block.workspace(2048)[:4].view(torch.int32).item()) == 0
+    for c in range(0, 2048, 64):
+        ref_ids, ref_w, _ = o.route(x[c:c + 64], d["Wg"], 8)
+        assert np.array_equal(ids[c:c + 64], ref_ids), c
+        assert np.allclose(w[c:c + 64], ref_w, rtol=1e-5, atol=1e-6)
+    sample = [0, 511, 1024, 2047]
+    ref, _, _, _ = o.moe_block(o.MoeLayer(**d), x[sample], k=8)
+    assert rel_err_rows(out[sample], ref).max() <= TOL
+
+
 def test_moe_grouped_deterministic(native):
     d = gen.moe_layer(27, hidden=512, inter=256, n_experts=16)
     x = dev(gen.fp16_normal(gen.rng(28), (33, 512)))
