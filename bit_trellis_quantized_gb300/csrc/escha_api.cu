@@ -93,7 +93,7 @@ struct MoeWs {
     size_t err, logits, ids, w, ygu, shgu, shgate, sh, d, grp, img, total;
 };
 
-MoeWs moe_ws_layout(const escha_moe_layer* L, int T) {
+MoeWs moe_ws_layout(const escha_moe_layer* L, int T, bool force_grouped = false) {
     MoeWs m{};
     size_t off = 0;
     const size_t slots = (size_t)T * L->topk;
@@ -113,7 +113,7 @@ MoeWs moe_ws_layout(const escha_moe_layer* L, int T) {
     off += align_up((size_t)T * 4);
     m.sh = off;
     off += align_up(L->sh_inter > 0 ? (size_t)T * L->hidden * 4 : 0);
-    const bool grouped = T > escha::kSlotModeMaxT;
+    const bool grouped = force_grouped || T > escha::kSlotModeMaxT;
     m.d = off;
     off += align_up(grouped ? slots * (size_t)L->hidden * 4 : 0);
     const escha::GroupPlan g = escha::group_plan(T, L->topk, L->n_experts, L->hidden, L->inter, L->sh_inter);
@@ -230,23 +230,10 @@ int record(cudaEvent_t* ev, int i, cudaStream_t s) {
     return cuda_status(cudaEventRecord(ev[i], s), "cudaEventRecord");
 }
 
-int moe_block_impl(const escha_moe_layer* L, const uint16_t* x, int T, float* out, int32_t* ids_out, float* w_out,
-                   void* ws, size_t ws_bytes, void* stream, cudaEvent_t* ev) {
-    int r = check_layer(L);
-    if (r) return r;
-    if (T < 1) return fail(ESCHA_E_ARG, "moe_block: T=%d must be >= 1", T);
-    if (T > 8192) return fail(ESCHA_E_SHAPE, "moe_block: T=%d above 8192 tokens per call", T);
-    if (!x || !out) return fail(ESCHA_E_ARG, "moe_block: null x / out");
-    if (!aligned16(x) || !aligned16(out) || (ids_out && !aligned16(ids_out)) || (w_out && !aligned16(w_out)))
-        return fail(ESCHA_E_ALIGN, "moe_block: x / out / ids_out / w_out not 16-byte aligned");
-    const MoeWs m = moe_ws_layout(L, T);
-    if (!ws || ws_bytes < m.total)
-        return fail(ESCHA_E_WORKSPACE, "moe_block: workspace %zu bytes, need %zu", ws_bytes, m.total);
-    if (!aligned16(ws)) return fail(ESCHA_E_ALIGN, "moe_block: workspace not 16-byte aligned");
-    int sms;
-    if ((r = device_check(&sms))) return r;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    char* base = static_cast<char*>(ws);
+// Kernel arguments of a MoE-block call over the workspace layout m (the
+// grouping fields are filled for every T; only the grouped path uses them).
+escha::MoeArgs moe_args(const escha_moe_layer* L, const uint16_t* x, int T, float* out, int32_t* ids_out, float* w_out,
+                        char* base, const MoeWs& m) {
     escha::MoeArgs a{};
     a.T = T;
     a.hidden = L->hidden;
@@ -278,7 +265,7 @@ int moe_block_impl(const escha_moe_layer* L, const uint16_t* x, int T, float* ou
     a.shgate = reinterpret_cast<float*>(base + m.shgate);
     a.sh = reinterpret_cast<float*>(base + m.sh);
     a.err = reinterpret_cast<int*>(base + m.err);
-    if (T > escha::kSlotModeMaxT) {
+    {
         const escha::GroupPlan gp = escha::group_plan(T, L->topk, L->n_experts, L->hidden, L->inter, L->sh_inter);
         const int E = L->n_experts, S = T * L->topk;
         int* g = reinterpret_cast<int*>(base + m.grp);
@@ -293,6 +280,29 @@ int moe_block_impl(const escha_moe_layer* L, const uint16_t* x, int T, float* ou
         a.grp_ppos = a.grp_perm + S;
         a.grp_img = reinterpret_cast<uint8_t*>(base + m.img);
         a.grp_img_rows = 2 * gp.pos_cap;
+    }
+    return a;
+}
+
+int moe_block_impl(const escha_moe_layer* L, const uint16_t* x, int T, float* out, int32_t* ids_out, float* w_out,
+                   void* ws, size_t ws_bytes, void* stream, cudaEvent_t* ev) {
+    int r = check_layer(L);
+    if (r) return r;
+    if (T < 1) return fail(ESCHA_E_ARG, "moe_block: T=%d must be >= 1", T);
+    if (T > 8192) return fail(ESCHA_E_SHAPE, "moe_block: T=%d above 8192 tokens per call", T);
+    if (!x || !out) return fail(ESCHA_E_ARG, "moe_block: null x / out");
+    if (!aligned16(x) || !aligned16(out) || (ids_out && !aligned16(ids_out)) || (w_out && !aligned16(w_out)))
+        return fail(ESCHA_E_ALIGN, "moe_block: x / out / ids_out / w_out not 16-byte aligned");
+    const MoeWs m = moe_ws_layout(L, T);
+    if (!ws || ws_bytes < m.total)
+        return fail(ESCHA_E_WORKSPACE, "moe_block: workspace %zu bytes, need %zu", ws_bytes, m.total);
+    if (!aligned16(ws)) return fail(ESCHA_E_ALIGN, "moe_block: workspace not 16-byte aligned");
+    int sms;
+    if ((r = device_check(&sms))) return r;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* base = static_cast<char*>(ws);
+    escha::MoeArgs a = moe_args(L, x, T, out, ids_out, w_out, base, m);
+    if (T > escha::kSlotModeMaxT) {
         float* d = reinterpret_cast<float*>(base + m.d);
         if ((r = record(ev, 0, s))) return r;
         if ((r = cuda_status(escha::launch_moe_router(a, s), "router launch"))) return r;
@@ -338,10 +348,53 @@ int escha_moe_block_timed(const escha_moe_layer* L, const uint16_t* x, int T, fl
     return moe_block_impl(L, x, T, out, ids_out, w_out, ws, ws_bytes, stream, ev);
 }
 
+size_t escha_moe_route_workspace(const escha_moe_layer* L, int T) {
+    if (!L || T < 1 || L->topk < 1) return 0;
+    return moe_ws_layout(L, T, true).total;
+}
+
+int escha_moe_route(const escha_moe_layer* L, const uint16_t* x, int T, uint16_t* logits_out, int32_t* ids_out,
+                    float* w_out, int32_t* counts_out, int32_t* offsets_out, int32_t* perm_out, void* ws,
+                    size_t ws_bytes, void* stream) {
+    int r = check_layer(L);
+    if (r) return r;
+    if (T < 1 || T > 8192) return fail(ESCHA_E_SHAPE, "moe_route: T=%d not in 1..8192", T);
+    if (!x || !ids_out || !w_out) return fail(ESCHA_E_ARG, "moe_route: null x / ids_out / w_out");
+    if (!aligned16(x) || (reinterpret_cast<uintptr_t>(ids_out) & 3) || (reinterpret_cast<uintptr_t>(w_out) & 3))
+        return fail(ESCHA_E_ALIGN, "moe_route: x not 16-byte aligned or ids_out / w_out not 4-byte aligned");
+    const MoeWs m = moe_ws_layout(L, T, true);
+    if (!ws || ws_bytes < m.total)
+        return fail(ESCHA_E_WORKSPACE, "moe_route: workspace %zu bytes, need %zu", ws_bytes, m.total);
+    if (!aligned16(ws)) return fail(ESCHA_E_ALIGN, "moe_route: workspace not 16-byte aligned");
+    int sms;
+    if ((r = device_check(&sms))) return r;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* base = static_cast<char*>(ws);
+    const escha::MoeArgs a = moe_args(L, x, T, nullptr, ids_out, w_out, base, m);
+    if ((r = cuda_status(escha::launch_moe_router(a, s), "router launch"))) return r;
+    if ((r = cuda_status(escha::launch_moe_topk_group(a, s), "top-k / grouping launch"))) return r;
+    const int E = L->n_experts;
+    const size_t S = (size_t)T * L->topk;
+    struct {
+        void* dst;
+        const void* src;
+        size_t bytes;
+    } copies[] = {{logits_out, a.logits, (size_t)T * E * 2},
+                  {counts_out, a.grp_counts, (size_t)E * 4},
+                  {offsets_out, a.grp_offsets, (size_t)(E + 1) * 4},
+                  {perm_out, a.grp_perm, S * 4}};
+    for (const auto& c : copies) {
+        if (!c.dst) continue;
+        if ((r = cuda_status(cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyDeviceToDevice, s), "route copy")))
+            return r;
+    }
+    return ESCHA_OK;
+}
+
 size_t int8_w8a16_workspace(int N, int Kin, int M) {
     (void)N;
     if (M < 1 || Kin < 16) return 0;
-    return int8_uses_gemm(Kin, M) ? escha::int8_gemm_image_bytes(Kin, M) : 0;
+    return int8_uses_gemm(Kin, M) ? escha::int8_gemm_ws_bytes(N, Kin, M) : 0;
 }
 
 int int8_w8a16_matvec(const int8_t* W, const float* scales, int N, int Kin, const void* x, int x_dtype, int M,
@@ -356,7 +409,7 @@ int int8_w8a16_matvec(const int8_t* W, const float* scales, int N, int Kin, cons
         return fail(ESCHA_E_ALIGN, "int8_w8a16_matvec: pointer not 16-byte aligned");
     const bool gemm = int8_uses_gemm(Kin, M);
     if (gemm) {
-        const size_t need = escha::int8_gemm_image_bytes(Kin, M);
+        const size_t need = escha::int8_gemm_ws_bytes(N, Kin, M);
         if (!ws || ws_bytes < need)
             return fail(ESCHA_E_WORKSPACE, "int8_w8a16_matvec: workspace of %zu bytes, %zu needed", ws_bytes, need);
         if (!aligned16(ws)) return fail(ESCHA_E_ALIGN, "int8_w8a16_matvec: workspace not 16-byte aligned");

@@ -37,19 +37,56 @@ __global__ void __launch_bounds__(256) int8_gemv_kernel(const int8_t* __restrict
     extern __shared__ __align__(16) float xs[];  // [MT][Kin]
     const int m0 = blockIdx.y * MT;
     const int mt = min(MT, M - m0);
-    for (int idx = threadIdx.x; idx < MT * Kin; idx += blockDim.x) {
-        const int t = idx / Kin, i = idx % Kin;
-        float v = 0.f;
+    // 8 consecutive activations per thread and step, 16-byte loads, several
+    // steps' loads in flight
+#pragma unroll 4
+    for (int c = threadIdx.x; c < MT * Kin / 8; c += blockDim.x) {
+        const int idx = c * 8;
+        const int t = idx / Kin, i = idx - t * Kin;
+        float v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = 0.f;
         if (t < mt) {
             const long long row = (long long)(m0 + t) * x_stride;
             if (act == 1) {
                 const float* yr = static_cast<const float*>(x) + row;
-                v = silu_f(yr[i]) * yr[Kin + i];
+                const float4 g0 = *reinterpret_cast<const float4*>(yr + i);
+                const float4 g1 = *reinterpret_cast<const float4*>(yr + i + 4);
+                const float4 u0 = *reinterpret_cast<const float4*>(yr + Kin + i);
+                const float4 u1 = *reinterpret_cast<const float4*>(yr + Kin + i + 4);
+                v[0] = silu_f(g0.x) * u0.x;
+                v[1] = silu_f(g0.y) * u0.y;
+                v[2] = silu_f(g0.z) * u0.z;
+                v[3] = silu_f(g0.w) * u0.w;
+                v[4] = silu_f(g1.x) * u1.x;
+                v[5] = silu_f(g1.y) * u1.y;
+                v[6] = silu_f(g1.z) * u1.z;
+                v[7] = silu_f(g1.w) * u1.w;
+            } else if (x_dtype == 3) {
+                const float* xr = static_cast<const float*>(x) + row + i;
+                const float4 a0 = *reinterpret_cast<const float4*>(xr);
+                const float4 a1 = *reinterpret_cast<const float4*>(xr + 4);
+                v[0] = a0.x;
+                v[1] = a0.y;
+                v[2] = a0.z;
+                v[3] = a0.w;
+                v[4] = a1.x;
+                v[5] = a1.y;
+                v[6] = a1.z;
+                v[7] = a1.w;
             } else {
-                v = load_act(x, row + i, x_dtype);
+                const uint4 hv = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + row + i);
+                const uint32_t w[4] = {hv.x, hv.y, hv.z, hv.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint16_t lo = static_cast<uint16_t>(w[q] & 0xFFFFu), hi = static_cast<uint16_t>(w[q] >> 16);
+                    v[2 * q] = x_dtype == 1 ? h2f_bits(lo) : bf2f_bits(lo);
+                    v[2 * q + 1] = x_dtype == 1 ? h2f_bits(hi) : bf2f_bits(hi);
+                }
             }
         }
-        xs[xs_swz(idx)] = v;
+        *reinterpret_cast<float4*>(xs + xs_swz(idx)) = make_float4(v[0], v[1], v[2], v[3]);
+        *reinterpret_cast<float4*>(xs + xs_swz(idx + 4)) = make_float4(v[4], v[5], v[6], v[7]);
     }
     __syncthreads();
 

@@ -104,7 +104,8 @@ __device__ __forceinline__ uint2 i8x4_to_16(uint32_t w) {
 template <bool BF16, int PARTS>
 __global__ void __launch_bounds__(tc::kMlThreads, 1)
     int8_gemm_kernel(const int8_t* __restrict__ W, const float* __restrict__ scales, int N, int Kin,
-                     const uint8_t* __restrict__ img, int img_rows, int M, float* __restrict__ y, long long y_stride) {
+                     const uint8_t* __restrict__ img, int img_rows, int M, float* __restrict__ y, long long y_stride,
+                     int bps) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     constexpr uint32_t kBChunk = kRowsPerCta * 128;
@@ -131,16 +132,24 @@ __global__ void __launch_bounds__(tc::kMlThreads, 1)
     const uint32_t tmem = tmem_base;
     const uint32_t idesc = tc::idesc_f16(128, npad, false, false, BF16);
 
+    // K split z (blockIdx.z) covers blocks [z * bps, z * bps + nblk); with more
+    // than one split, y points at split z's partial sums ([M][N] each)
+    const int b_first = blockIdx.z * bps;
+    const int nblk = min(Kin / 128 - b_first, bps);
+    if (gridDim.z > 1) {
+        y += (long long)blockIdx.z * M * N;
+        y_stride = N;
+    }
     // thread t converts row t/2, values 64*(t%2) .. +63 of every 128-value block
     const int r = tid >> 1, h = tid & 1;
-    const int8_t* wrow = W + (long long)min(n0 + r, N - 1) * Kin + 64 * h;
-    const int nblk = Kin >> 7;
+    const int8_t* wrow = W + (long long)min(n0 + r, N - 1) * Kin + 64 * h + b_first * 128;
     uint4 cur[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) cur[j] = __ldg(reinterpret_cast<const uint4*>(wrow) + j);
 
     const bool ok = tc::mma_mainloop<false>(
-        Abuf, Bbuf, kBChunk, img + (long long)R0 * 128, (long long)img_rows * 128, static_cast<uint32_t>(nrows) * 128u,
+        Abuf, Bbuf, kBChunk, img + (long long)R0 * 128 + 2ll * b_first * img_rows * 128, (long long)img_rows * 128,
+        static_cast<uint32_t>(nrows) * 128u,
         nblk, tmem, idesc, bars, [&](int b, uint8_t* A) {
             uint4 nxt[4];
             const bool more = b + 1 < nblk;
@@ -196,21 +205,78 @@ __global__ void __launch_bounds__(tc::kMlThreads, 1)
     if (warp == 0) tc::tmem_dealloc(tmem, 256);
 }
 
+// y[m][n] = sum over the splits z (in order) of part[z][m][n]; four
+// consecutive n per thread when N % 4 == 0 (y_stride too), else one.
+__global__ void __launch_bounds__(256) int8_split_reduce_kernel(const float* __restrict__ part, int ks, int M, int N,
+                                                                float* __restrict__ y, long long y_stride) {
+    pdl_wait();
+    pdl_trigger();
+    const long long MN = (long long)M * N;
+    if ((N & 3) == 0 && (y_stride & 3) == 0) {
+        const long long i = 4 * ((long long)blockIdx.x * 256 + threadIdx.x);
+        if (i >= MN) return;
+        float4 acc = *reinterpret_cast<const float4*>(part + i);
+        for (int z = 1; z < ks; ++z) {
+            const float4 v = *reinterpret_cast<const float4*>(part + z * MN + i);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        *reinterpret_cast<float4*>(y + (i / N) * y_stride + i % N) = acc;
+        return;
+    }
+    const long long i = (long long)blockIdx.x * 256 + threadIdx.x;
+    if (i >= MN) return;
+    float acc = part[i];
+    for (int z = 1; z < ks; ++z) acc += part[z * MN + i];
+    y[(i / N) * y_stride + i % N] = acc;
+}
+
 template <bool BF16, int PARTS>
 cudaError_t launch_gemm(const int8_t* W, const float* scales, int N, int Kin, const uint8_t* img, int img_rows, int M,
-                        float* y, long long y_stride, cudaStream_t s) {
+                        float* y, long long y_stride, float* part, cudaStream_t s) {
     const int smem = 2 * tc::kABlockBytes + 2 * 2 * kRowsPerCta * 128 + 1024;
     const void* f = reinterpret_cast<const void*>(int8_gemm_kernel<BF16, PARTS>);
     cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    void* args[] = {&W, &scales, &N, &Kin, &img, &img_rows, &M, &y, &y_stride};
-    return launch_kernel(f, dim3((N + 127) / 128, (img_rows + kRowsPerCta - 1) / kRowsPerCta), dim3(tc::kMlThreads),
-                         smem, true, s, args);
+    const int nblk = Kin / 128;
+    int bps = (nblk + int8_gemm_ksplit(N, Kin, M, PARTS) - 1) / int8_gemm_ksplit(N, Kin, M, PARTS);
+    const int ks = (nblk + bps - 1) / bps;  // every split starts inside K
+    float* out = ks > 1 ? part : y;
+    void* args[] = {&W, &scales, &N, &Kin, &img, &img_rows, &M, &out, &y_stride, &bps};
+    e = launch_kernel(f, dim3((N + 127) / 128, (img_rows + kRowsPerCta - 1) / kRowsPerCta, ks), dim3(tc::kMlThreads),
+                      smem, true, s, args);
+    if (e != cudaSuccess || ks == 1) return e;
+    int ks_ = ks;
+    void* rargs[] = {&part, &ks_, &M, &N, &y, &y_stride};
+    const long long per_thread = ((N & 3) == 0 && (y_stride & 3) == 0) ? 4 : 1;
+    const long long threads = ((long long)M * N + per_thread - 1) / per_thread;
+    return launch_kernel(reinterpret_cast<const void*>(int8_split_reduce_kernel),
+                         dim3(static_cast<unsigned>((threads + 255) / 256)), dim3(256), 0, true, s, rargs);
 }
 
 }  // namespace
 
+// K splits of the GEMM: enough CTAs for about one wave of 152 SMs, at least
+// two 128-value blocks per split, at most 8 splits. A fixed function of the
+// shape, so results do not depend on the device.
+int int8_gemm_ksplit(int N, int Kin, int M, int parts) {
+    const long long tiles = (long long)((N + 127) / 128) * ((img_rows_for(parts, M) + kRowsPerCta - 1) / kRowsPerCta);
+    const int nblk = Kin / 128;
+    if (tiles >= 48) return 1;  // most SMs busy already; a split would cost more in partial traffic
+    int ks = static_cast<int>((152 + tiles - 1) / tiles);
+    ks = min(ks, max(1, nblk / 2));
+    return min(ks, 8);
+}
+
 size_t int8_gemm_image_bytes(int Kin, int M) { return (size_t)Kin * img_rows_for(2, M) * 2; }
+
+size_t int8_gemm_ws_bytes(int N, int Kin, int M) {
+    const int ks = max(int8_gemm_ksplit(N, Kin, M, 1), int8_gemm_ksplit(N, Kin, M, 2));
+    const size_t img = (int8_gemm_image_bytes(Kin, M) + 255) & ~size_t(255);
+    return img + (ks > 1 ? (size_t)ks * M * N * 4 : 0);
+}
 
 cudaError_t launch_int8_gemm(const int8_t* W, const float* scales, int N, int Kin, const void* x, int x_dtype,
                              long long x_stride, int act, int M, float* y, long long y_stride, void* img_v,
@@ -218,14 +284,15 @@ cudaError_t launch_int8_gemm(const int8_t* W, const float* scales, int N, int Ki
     const int parts = (act == 1 || x_dtype == kDtF32) ? 2 : 1;
     int img_rows = img_rows_for(parts, M);
     uint8_t* img = static_cast<uint8_t*>(img_v);
+    float* part = reinterpret_cast<float*>(img + ((int8_gemm_image_bytes(Kin, M) + 255) & ~size_t(255)));
     const long long tasks = (long long)M * (Kin / 128);
     void* pargs[] = {&x, &x_dtype, &x_stride, &act, &M, &Kin, &img, &img_rows};
     cudaError_t e = launch_kernel(reinterpret_cast<const void*>(int8_prep_kernel),
                                   dim3(static_cast<unsigned>((tasks + 7) / 8)), dim3(256), 0, true, s, pargs);
     if (e != cudaSuccess) return e;
-    if (parts == 2) return launch_gemm<true, 2>(W, scales, N, Kin, img, img_rows, M, y, y_stride, s);
-    if (x_dtype == kDtBf16) return launch_gemm<true, 1>(W, scales, N, Kin, img, img_rows, M, y, y_stride, s);
-    return launch_gemm<false, 1>(W, scales, N, Kin, img, img_rows, M, y, y_stride, s);
+    if (parts == 2) return launch_gemm<true, 2>(W, scales, N, Kin, img, img_rows, M, y, y_stride, part, s);
+    if (x_dtype == kDtBf16) return launch_gemm<true, 1>(W, scales, N, Kin, img, img_rows, M, y, y_stride, part, s);
+    return launch_gemm<false, 1>(W, scales, N, Kin, img, img_rows, M, y, y_stride, part, s);
 }
 
 }  // namespace escha

@@ -45,9 +45,13 @@ cudaError_t launch_int8_dequant(const int8_t* W, const float* scales, int N, int
 
 // int8 w8a16 GEMM on the tensor cores (same result as the GEMV, for many
 // tokens): a prep kernel writes x (or SwiGLU of x when act == 1) as the MMA's
-// B image into `img` (int8_gemm_image_bytes(Kin, M) bytes), then one CTA per
-// 128 outputs x 256 image rows runs the MMAs. Needs Kin % 128 == 0.
+// B image into the scratch `img` (int8_gemm_ws_bytes(N, Kin, M) bytes: the
+// image, then the partial sums of the K splits), then one CTA per 128 outputs
+// x 256 image rows x K split runs the MMAs; with several splits a last kernel
+// adds the partials in split order. Needs Kin % 128 == 0.
 size_t int8_gemm_image_bytes(int Kin, int M);
+size_t int8_gemm_ws_bytes(int N, int Kin, int M);
+int int8_gemm_ksplit(int N, int Kin, int M, int parts);
 constexpr int kInt8GemmMinM = 16;  // smallest M that takes the GEMM
 cudaError_t launch_int8_gemm(const int8_t* W, const float* scales, int N, int Kin, const void* x, int x_dtype,
                              long long x_stride, int act, int M, float* y, long long y_stride, void* img,
@@ -112,6 +116,8 @@ struct GroupPlan {
     size_t img_bytes;  // B image (shared by both projections and the shared expert)
 };
 GroupPlan group_plan(int T, int topk, int E, int hidden, int inter, int sh_inter);
+// top-k (ids, w) and the grouping by expert.
+cudaError_t launch_moe_topk_group(const MoeArgs& a, cudaStream_t s);
 // top-k, grouping, grouped gate_up and down GEMMs (down output d [T*topk][hidden]).
 cudaError_t launch_moe_grouped(const MoeArgs& a, float* d, int num_sms, cudaStream_t s);
 // out = sum_j w * d + sigmoid(gate) * sh

@@ -46,14 +46,24 @@ constexpr int kMaxCluster = 16;
 // partials are combined by the xor butterfly (offsets 16, 8, 4, 2, 1) and
 // rounded to f16 (RNE).
 // ---------------------------------------------------------------------------
+// acc += x.lo * w.lo, then acc += x.hi * w.hi: fp16 operands, f32 accumulator,
+// one rounding per step (the product of two fp16 values is exact in f32, so
+// this equals an f32 fma of the converted operands).
+__device__ __forceinline__ void fma2_f16(uint32_t x2, uint32_t w2, float& acc) {
+    asm("{\n\t.reg .f16 xl, xh, wl, wh;\n\t"
+        "mov.b32 {xl, xh}, %1;\n\t"
+        "mov.b32 {wl, wh}, %2;\n\t"
+        "fma.rn.f32.f16 %0, xl, wl, %0;\n\t"
+        "fma.rn.f32.f16 %0, xh, wh, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(x2), "r"(w2));
+}
+
 __device__ __forceinline__ void dot8_f16(const uint4& xv, const uint4& wv, float& acc) {
-    const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
-    const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        acc = fmaf(h2f_bits(static_cast<uint16_t>(xs[k] & 0xFFFFu)), h2f_bits(static_cast<uint16_t>(ws[k] & 0xFFFFu)), acc);
-        acc = fmaf(h2f_bits(static_cast<uint16_t>(xs[k] >> 16)), h2f_bits(static_cast<uint16_t>(ws[k] >> 16)), acc);
-    }
+    fma2_f16(xv.x, wv.x, acc);
+    fma2_f16(xv.y, wv.y, acc);
+    fma2_f16(xv.z, wv.z, acc);
+    fma2_f16(xv.w, wv.w, acc);
 }
 
 __device__ void router_logits(const MoeArgs& a, int warp, int lane) {
@@ -165,6 +175,66 @@ __global__ void __launch_bounds__(kK0Threads) moe_router_kernel(const MoeArgs a)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *a.err = 0;  // the whole previous call has finished
     router_logits(a, warp, lane);
+}
+
+// Router logits for many tokens: a CTA stages 16 tokens of x in shared memory
+// (1024 columns at a time) and each of its 8 warps computes 2 experts x 16
+// tokens, so x is read from L2 once per 16 experts instead of once per
+// expert. Each logit keeps the summation order stated above.
+constexpr int kRtTok = 16, kRtExpW = 2, kRtExp = 8 * kRtExpW, kRtCols = 1024;
+
+__global__ void __launch_bounds__(256) moe_router_tiled_kernel(const MoeArgs a) {
+    __shared__ __align__(16) uint16_t xs[kRtTok][kRtCols];
+    pdl_trigger();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) *a.err = 0;  // the whole previous call has finished
+    const int e0 = blockIdx.x * kRtExp + warp * kRtExpW;
+    const int t0 = blockIdx.y * kRtTok;
+    const int nt = min(kRtTok, a.T - t0);
+    float acc[kRtExpW][kRtTok];
+#pragma unroll
+    for (int j = 0; j < kRtExpW; ++j)
+#pragma unroll
+        for (int t = 0; t < kRtTok; ++t) acc[j][t] = 0.f;
+    for (int c0 = 0; c0 < a.hidden; c0 += kRtCols) {
+        const int ncols = min(kRtCols, a.hidden - c0);  // a multiple of 256
+        __syncthreads();
+        for (int i = tid; i < kRtTok * (kRtCols / 8); i += 256) {
+            const int t = i / (kRtCols / 8), c = (i % (kRtCols / 8)) * 8;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (t < nt && c < ncols) v = __ldg(reinterpret_cast<const uint4*>(a.x + (long long)(t0 + t) * a.hidden + c0 + c));
+            *reinterpret_cast<uint4*>(&xs[t][c]) = v;
+        }
+        __syncthreads();
+        uint4 wv[kRtExpW][kRtCols / 256];
+#pragma unroll
+        for (int j = 0; j < kRtExpW; ++j)
+#pragma unroll
+            for (int p = 0; p < kRtCols / 256; ++p)
+                wv[j][p] = (e0 + j < a.E && p * 256 < ncols)
+                               ? ldg_stream_v4(a.router_w + (long long)(e0 + j) * a.hidden + c0 + p * 256 + lane * 8)
+                               : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int p = 0; p < kRtCols / 256; ++p) {
+            if (p * 256 >= ncols) break;
+#pragma unroll
+            for (int t = 0; t < kRtTok; ++t) {
+                const uint4 xv = *reinterpret_cast<const uint4*>(&xs[t][p * 256 + lane * 8]);
+#pragma unroll
+                for (int j = 0; j < kRtExpW; ++j) dot8_f16(xv, wv[j][p], acc[j][t]);
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < kRtExpW; ++j)
+#pragma unroll
+        for (int t = 0; t < kRtTok; ++t) {
+            float v = acc[j][t];
+#pragma unroll
+            for (int m = 16; m >= 1; m >>= 1) v = v + __shfl_xor_sync(0xffffffffu, v, m);
+            if (lane == 0 && t < nt && e0 + j < a.E)
+                a.logits[(long long)(t0 + t) * a.E + e0 + j] = __half_as_ushort(__float2half_rn(v));
+        }
 }
 
 // ---------------------------------------------------------------------------
@@ -529,6 +599,12 @@ cudaError_t launch_down(MoeArgs a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_moe_router(const MoeArgs& a, cudaStream_t s) {
+    if (a.T >= kRtTok) {
+        void* args[] = {const_cast<MoeArgs*>(&a)};
+        return launch_kernel(reinterpret_cast<const void*>(moe_router_tiled_kernel),
+                             dim3((a.E + kRtExp - 1) / kRtExp, (a.T + kRtTok - 1) / kRtTok), dim3(256), 0, false, s,
+                             args);
+    }
     const int n_lg = (a.E + kK0Warps - 1) / kK0Warps;
     return launch_ex(reinterpret_cast<const void*>(moe_router_kernel), dim3(n_lg, (a.T + kLgTG - 1) / kLgTG),
                      dim3(kK0Threads), 0, 0, false, s, a);

@@ -31,8 +31,6 @@ namespace escha {
 
 namespace {
 
-constexpr int kGrpThreads = tc::kMlThreads;
-constexpr int kGrpWarps = kGrpThreads / 32;
 constexpr float kPrescale = 0.00390625f;  // 2^-8: keeps x~ inside the fp16 range, undone in the epilogue
 
 // ---------------------------------------------------------------------------
@@ -53,11 +51,24 @@ __global__ void __launch_bounds__(256) moe_topk_kernel(const MoeArgs a) {
     }
 }
 
+// Lanes whose 9-bit value v equals this lane's (the mask match_any would give),
+// from one ballot per bit.
+__device__ __forceinline__ unsigned match_any_9bit(int v) {
+    unsigned m = 0xffffffffu;
+#pragma unroll
+    for (int b = 0; b < 9; ++b) {
+        const bool bit = (v >> b) & 1;
+        const unsigned bal = __ballot_sync(0xffffffffu, bit);
+        m &= bit ? bal : ~bal;
+    }
+    return m;
+}
+
 // ---------------------------------------------------------------------------
 // 2. grouping (one CTA of 32 warps). Warp w owns the slots of segment w (in
 // slot order) and walks them 32 at a time; lanes holding the same expert
-// find each other with match_any, so ranks inside a round follow lane order
-// and the sort is stable without atomics.
+// find each other with ballots, so ranks inside a round follow lane order and
+// the sort is stable without atomics.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024, 1) moe_group_kernel(const MoeArgs a) {
     __shared__ int hist[32][256];  // per-warp counts, then per-warp running starts within each expert
@@ -71,14 +82,22 @@ __global__ void __launch_bounds__(1024, 1) moe_group_kernel(const MoeArgs a) {
     pdl_trigger();
     for (int i = tid; i < 32 * 256; i += 1024) (&hist[0][0])[i] = 0;
     __syncthreads();
-    // pass 1: per-warp counts
-    for (int s0 = s_begin; s0 < s_end; s0 += 32) {
-        const int s = s0 + lane;
-        const bool valid = s < s_end;
-        const int e = valid ? a.ids[s] : 256 + lane;
-        const unsigned m = __match_any_sync(0xffffffffu, e);
-        if (valid && (m & lt) == 0) hist[warp][e] += __popc(m);
-        __syncwarp();
+    // pass 1: per-warp counts (the ids of 8 rounds are loaded before any is used)
+    for (int s0 = s_begin; s0 < s_end; s0 += 256) {
+        int ev[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            const int s = s0 + 32 * r + lane;
+            ev[r] = s < s_end ? a.ids[s] : 256 + lane;
+        }
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            if (s0 + 32 * r >= s_end) break;  // warp-uniform
+            const bool valid = s0 + 32 * r + lane < s_end;
+            const unsigned m = match_any_9bit(ev[r]);
+            if (valid && (m & lt) == 0) hist[warp][ev[r]] += __popc(m);
+            __syncwarp();
+        }
     }
     __syncthreads();
     int cnt = 0;
@@ -146,20 +165,30 @@ __global__ void __launch_bounds__(1024, 1) moe_group_kernel(const MoeArgs a) {
         *a.grp_nitems = ibase_s[256];
     }
     // pass 2: stable scatter
-    for (int s0 = s_begin; s0 < s_end; s0 += 32) {
-        const int s = s0 + lane;
-        const bool valid = s < s_end;
-        const int e = valid ? a.ids[s] : 256 + lane;
-        const unsigned m = __match_any_sync(0xffffffffu, e);
-        const int start = valid ? hist[warp][e] : 0;
-        __syncwarp();
-        if (valid) {
-            const int r = start + __popc(m & lt);
-            a.grp_perm[off_s[e] + r] = s;
-            a.grp_ppos[s] = poff_s[e] + r;
-            if ((m & lt) == 0) hist[warp][e] = start + __popc(m);
+    for (int s0 = s_begin; s0 < s_end; s0 += 256) {
+        int ev[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            const int s = s0 + 32 * r + lane;
+            ev[r] = s < s_end ? a.ids[s] : 256 + lane;
         }
-        __syncwarp();
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            if (s0 + 32 * r >= s_end) break;  // warp-uniform
+            const int s = s0 + 32 * r + lane;
+            const bool valid = s < s_end;
+            const int e = ev[r];
+            const unsigned m = match_any_9bit(e);
+            const int start = valid ? hist[warp][e] : 0;
+            __syncwarp();
+            if (valid) {
+                const int rk = start + __popc(m & lt);
+                a.grp_perm[off_s[e] + rk] = s;
+                a.grp_ppos[s] = poff_s[e] + rk;
+                if ((m & lt) == 0) hist[warp][e] = start + __popc(m);
+            }
+            __syncwarp();
+        }
     }
 }
 
@@ -175,53 +204,66 @@ struct GroupedProj {
     float* y;               // [slots][out]
 };
 
+// BPW 128-input blocks per warp, their loads issued together (4 when there
+// are enough tasks to fill the GPU anyway, else 1 for more warps).
+template <int kPrepBlk>
 __global__ void __launch_bounds__(256) moe_prep_kernel(const MoeArgs a, const GroupedProj p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_wait();
     pdl_trigger();
     const int nblk = p.in >> 7;
+    const int ngrp = (nblk + kPrepBlk - 1) / kPrepBlk;
     const long long task = (long long)blockIdx.x * 8 + warp;
-    if (task >= (long long)a.T * a.topk * nblk) return;
-    const int s = static_cast<int>(task / nblk), b = static_cast<int>(task % nblk);
+    if (task >= (long long)a.T * a.topk * ngrp) return;
+    const int s = static_cast<int>(task / ngrp), b0 = static_cast<int>(task % ngrp) * kPrepBlk;
     const int e = a.ids[s];
     const int P = a.grp_ppos[s];
-    const int ib = b * 128 + 4 * lane;
-    float v[4];
-    if (p.mode == 0) {
-        const uint2 xb = *reinterpret_cast<const uint2*>(a.x + (long long)(s / a.topk) * a.hidden + ib);
-        v[0] = h2f_bits(static_cast<uint16_t>(xb.x & 0xFFFFu));
-        v[1] = h2f_bits(static_cast<uint16_t>(xb.x >> 16));
-        v[2] = h2f_bits(static_cast<uint16_t>(xb.y & 0xFFFFu));
-        v[3] = h2f_bits(static_cast<uint16_t>(xb.y >> 16));
-    } else {
-        const float* yr = a.ygu + (long long)s * 2 * a.inter;
-        const float4 g = *reinterpret_cast<const float4*>(yr + ib);
-        const float4 u = *reinterpret_cast<const float4*>(yr + a.inter + ib);
-        v[0] = silu_f(g.x) * u.x;
-        v[1] = silu_f(g.y) * u.y;
-        v[2] = silu_f(g.z) * u.z;
-        v[3] = silu_f(g.w) * u.w;
-    }
-    const uint2 rb = *reinterpret_cast<const uint2*>(p.rin + (long long)e * p.in + ib);
-    v[0] *= h2f_bits(static_cast<uint16_t>(rb.x & 0xFFFFu));
-    v[1] *= h2f_bits(static_cast<uint16_t>(rb.x >> 16));
-    v[2] *= h2f_bits(static_cast<uint16_t>(rb.y & 0xFFFFu));
-    v[3] *= h2f_bits(static_cast<uint16_t>(rb.y >> 16));
-    h128_warp(v, lane);
-    uint32_t hv[2], lv[2];
+    float v[kPrepBlk][4];
+    uint2 rb[kPrepBlk];
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-        const float s0 = v[2 * q] * kPrescale, s1 = v[2 * q + 1] * kPrescale;
-        const __half h0 = __float2half_rn(s0), h1 = __float2half_rn(s1);
-        const __half l0 = __float2half_rn(s0 - __half2float(h0)), l1 = __float2half_rn(s1 - __half2float(h1));
-        hv[q] = static_cast<uint32_t>(__half_as_ushort(h0)) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
-        lv[q] = static_cast<uint32_t>(__half_as_ushort(l0)) | (static_cast<uint32_t>(__half_as_ushort(l1)) << 16);
+    for (int q = 0; q < kPrepBlk; ++q) {
+        if (b0 + q >= nblk) break;
+        const int ib = (b0 + q) * 128 + 4 * lane;
+        rb[q] = *reinterpret_cast<const uint2*>(p.rin + (long long)e * p.in + ib);
+        if (p.mode == 0) {
+            const uint2 xb = *reinterpret_cast<const uint2*>(a.x + (long long)(s / a.topk) * a.hidden + ib);
+            v[q][0] = h2f_bits(static_cast<uint16_t>(xb.x & 0xFFFFu));
+            v[q][1] = h2f_bits(static_cast<uint16_t>(xb.x >> 16));
+            v[q][2] = h2f_bits(static_cast<uint16_t>(xb.y & 0xFFFFu));
+            v[q][3] = h2f_bits(static_cast<uint16_t>(xb.y >> 16));
+        } else {
+            const float* yr = a.ygu + (long long)s * 2 * a.inter;
+            const float4 g = *reinterpret_cast<const float4*>(yr + ib);
+            const float4 u = *reinterpret_cast<const float4*>(yr + a.inter + ib);
+            v[q][0] = silu_f(g.x) * u.x;
+            v[q][1] = silu_f(g.y) * u.y;
+            v[q][2] = silu_f(g.z) * u.z;
+            v[q][3] = silu_f(g.w) * u.w;
+        }
     }
-    const int chunk = 2 * b + (lane >> 4);
-    const uint32_t k_in = static_cast<uint32_t>((4 * lane) & 63);
-    uint8_t* base = a.grp_img + (long long)chunk * a.grp_img_rows * 128;
-    *reinterpret_cast<uint2*>(base + tc::kmajor_off(2u * P, k_in)) = make_uint2(hv[0], hv[1]);
-    *reinterpret_cast<uint2*>(base + tc::kmajor_off(2u * P + 1u, k_in)) = make_uint2(lv[0], lv[1]);
+#pragma unroll
+    for (int q = 0; q < kPrepBlk; ++q) {
+        if (b0 + q >= nblk) break;
+        float w[4] = {v[q][0] * h2f_bits(static_cast<uint16_t>(rb[q].x & 0xFFFFu)),
+                      v[q][1] * h2f_bits(static_cast<uint16_t>(rb[q].x >> 16)),
+                      v[q][2] * h2f_bits(static_cast<uint16_t>(rb[q].y & 0xFFFFu)),
+                      v[q][3] * h2f_bits(static_cast<uint16_t>(rb[q].y >> 16))};
+        h128_warp(w, lane);
+        uint32_t hv[2], lv[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const float s0 = w[2 * r] * kPrescale, s1 = w[2 * r + 1] * kPrescale;
+            const __half h0 = __float2half_rn(s0), h1 = __float2half_rn(s1);
+            const __half l0 = __float2half_rn(s0 - __half2float(h0)), l1 = __float2half_rn(s1 - __half2float(h1));
+            hv[r] = static_cast<uint32_t>(__half_as_ushort(h0)) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
+            lv[r] = static_cast<uint32_t>(__half_as_ushort(l0)) | (static_cast<uint32_t>(__half_as_ushort(l1)) << 16);
+        }
+        const int chunk = 2 * (b0 + q) + (lane >> 4);
+        const uint32_t k_in = static_cast<uint32_t>((4 * lane) & 63);
+        uint8_t* base = a.grp_img + (long long)chunk * a.grp_img_rows * 128;
+        *reinterpret_cast<uint2*>(base + tc::kmajor_off(2u * P, k_in)) = make_uint2(hv[0], hv[1]);
+        *reinterpret_cast<uint2*>(base + tc::kmajor_off(2u * P + 1u, k_in)) = make_uint2(lv[0], lv[1]);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -253,8 +295,15 @@ __device__ __forceinline__ void decode_row_to_smem(const LaneCodes<K>& lc, uint8
     });
 }
 
-template <int K>
-__global__ void __launch_bounds__(kGrpThreads, 1) moe_grouped_gemm_kernel(const MoeArgs a, const GroupedProj p) {
+// GROUPS = 2: 512 threads in two producer groups taking alternate blocks
+// (one CTA per SM; for items of 64 or 128 tokens, whose B buffers fill the
+// shared memory anyway). GROUPS = 1: 256 threads, double-buffered A, two CTAs
+// per SM (items of up to 32 tokens), so one CTA's prologue and epilogue
+// overlap the other's decode.
+template <int K, int GROUPS>
+__global__ void __launch_bounds__(GROUPS * tc::kMlThreads, 3 - GROUPS)
+    moe_grouped_gemm_kernel(const MoeArgs a, const GroupedProj p) {
+    constexpr int kThreads = GROUPS * tc::kMlThreads, kWarps = kThreads / 32;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int cap = a.grp_cap;
@@ -277,8 +326,9 @@ __global__ void __launch_bounds__(kGrpThreads, 1) moe_grouped_gemm_kernel(const 
     const int nt = min(cap, a.grp_counts[e] - g0);
     const int npad = (2 * nt + 15) & ~15;  // MMA N: hi/lo rows of nt tokens, multiple of 16
     const int nt4 = (nt + 3) & ~3;          // rows copied: whole 8-row atoms
-    for (int i = tid; i < nt; i += kGrpThreads) slot_s[i] = a.grp_perm[a.grp_offsets[e] + g0 + i];
-    const uint32_t tcols = 2u * static_cast<uint32_t>(cap) < 32u ? 32u : 2u * static_cast<uint32_t>(cap);
+    for (int i = tid; i < nt; i += kThreads) slot_s[i] = a.grp_perm[a.grp_offsets[e] + g0 + i];
+    const uint32_t acc_cols = 2u * static_cast<uint32_t>(cap) < 32u ? 32u : 2u * static_cast<uint32_t>(cap);
+    const uint32_t tcols = GROUPS * acc_cols;  // one accumulator per producer group
     if (tid == 0) tc::mma_bars_init(bars);
     if (warp == 0) {
         tc::tmem_alloc(&tmem_base, tcols);
@@ -293,36 +343,62 @@ __global__ void __launch_bounds__(kGrpThreads, 1) moe_grouped_gemm_kernel(const 
     const int KT = p.in >> 4, NT = p.out >> 4;
     const uint16_t* codes = p.codes + (long long)e * KT * NT * (16 * K);
     const int nblk = p.in >> 7;
-    LaneCodes<K> cur;
-    load_lane_codes<K>(cur, codes + ((long long)warp * NT + ob * 8) * (16 * K), lane);
+    const int gw = warp & 7;  // tile row of the block inside the warp's group
+    // two register sets of lane codes used in turn: the set for the next block
+    // is loaded while the other is decoded, and never copied (a copy would
+    // wait for the load)
+    LaneCodes<K> c0, c1;
+    const int first = GROUPS == 2 ? (warp >> 3) : 0;
+    if (first < nblk) load_lane_codes<K>(c0, codes + ((long long)(8 * first + gw) * NT + ob * 8) * (16 * K), lane);
     const int nbr = (lane & ~3) | ((lane + 1) & 3);
     const uint8_t* img = a.grp_img + (long long)2 * (a.grp_poff[e] + g0) * 128;
-
-    const bool ok = tc::mma_mainloop<true>(
-        Abuf, Bbuf, b_chunk, img, (long long)a.grp_img_rows * 128, 256u * static_cast<uint32_t>(nt4), nblk, tmem,
-        idesc, bars, [&](int b, uint8_t* A) {
-            // warp w decodes tile row 8b + w of output block ob, prefetching the next
-            LaneCodes<K> nxt;
-            const bool more = b + 1 < nblk;
-            if (more) load_lane_codes<K>(nxt, codes + ((long long)(8 * (b + 1) + warp) * NT + ob * 8) * (16 * K), lane);
-            cur.p[2 * K] = __shfl_sync(0xffffffffu, cur.p[0], nbr) & 0xFFFFu;
-            decode_row_to_smem<K>(cur, A + warp * 4096, lane);
-            if (more) cur = nxt;
-        });
+    int parity = 0;
+    // warp gw decodes tile row 8b + gw of output block ob and loads its row of
+    // block b_next
+    auto produce = [&](int b, int b_next, uint8_t* A) {
+        (void)b;
+        const bool more = b_next < nblk;
+        const uint16_t* nrow = codes + ((long long)(8 * b_next + gw) * NT + ob * 8) * (16 * K);
+        if (parity == 0) {
+            if (more) load_lane_codes<K>(c1, nrow, lane);
+            c0.p[2 * K] = __shfl_sync(0xffffffffu, c0.p[0], nbr) & 0xFFFFu;
+            decode_row_to_smem<K>(c0, A + gw * 4096, lane);
+        } else {
+            if (more) load_lane_codes<K>(c0, nrow, lane);
+            c1.p[2 * K] = __shfl_sync(0xffffffffu, c1.p[0], nbr) & 0xFFFFu;
+            decode_row_to_smem<K>(c1, A + gw * 4096, lane);
+        }
+        parity ^= 1;
+    };
+    const long long img_chunk = (long long)a.grp_img_rows * 128;
+    const uint32_t copy_bytes = 256u * static_cast<uint32_t>(nt4);
+    bool ok;
+    if constexpr (GROUPS == 2)
+        ok = tc::mma_mainloop_2grp<true>(Abuf, Bbuf, b_chunk, img, img_chunk, copy_bytes, nblk, tmem, acc_cols, idesc,
+                                         bars, produce);
+    else
+        ok = tc::mma_mainloop<true>(Abuf, Bbuf, b_chunk, img, img_chunk, copy_bytes, nblk, tmem, idesc, bars,
+                                    [&](int b, uint8_t* A) { produce(b, b + 1, A); });
     if (!ok && tid == 0) atomicExch(a.err, 3);
 
-    // epilogue: TMEM lane m holds columns 2i (hi) and 2i + 1 (lo) of token i;
-    // warps w and w + 4 share lane quarter w % 4 and split the columns
+    // epilogue: TMEM lane m of accumulator g holds columns 2i (hi) and 2i + 1
+    // (lo) of token i; warps w, w + 4, w + 8, w + 12 share lane quarter w % 4
+    // and split the columns
     if (ok) {
         const int q = warp & 3, m = 32 * q + lane;
-        for (int c0 = 16 * (warp >> 2); c0 < npad; c0 += 32) {
-            float v[16];
-            tc::tmem_ld16(tmem + (static_cast<uint32_t>(32 * q) << 16) + c0, v);
+        const bool two = GROUPS == 2 && nblk >= 2;
+        for (int c0 = 16 * (warp >> 2); c0 < npad; c0 += 16 * (kWarps / 4)) {
+            float v0[16], v1[16];
+            const uint32_t ta = tmem + (static_cast<uint32_t>(32 * q) << 16) + c0;
+            tc::tmem_ld16(ta, v0);
+            if (two) tc::tmem_ld16(ta + acc_cols, v1);
             tc::tmem_ld_wait();
 #pragma unroll
             for (int qq = 0; qq < 8; ++qq) {
                 const int i = c0 / 2 + qq;
-                if (i < nt) zs[i * 128 + m] = v[2 * qq] + v[2 * qq + 1];
+                float z = v0[2 * qq] + v0[2 * qq + 1];
+                if (two) z += v1[2 * qq] + v1[2 * qq + 1];
+                if (i < nt) zs[i * 128 + m] = z;
             }
         }
     }
@@ -332,7 +408,7 @@ __global__ void __launch_bounds__(kGrpThreads, 1) moe_grouped_gemm_kernel(const 
     if (!ok) return;
     const uint16_t* rout = p.rout + (long long)e * p.out + ob * 128;
     const uint2 rb = *reinterpret_cast<const uint2*>(rout + 4 * lane);
-    for (int i = warp; i < nt; i += kGrpWarps) {
+    for (int i = warp; i < nt; i += kWarps) {
         const float4 z4 = *reinterpret_cast<const float4*>(zs + i * 128 + 4 * lane);
         float v[4] = {z4.x * 256.f, z4.y * 256.f, z4.z * 256.f, z4.w * 256.f};  // undo the 2^-8 prescale (exact)
         output_transform_regs(v, rb, lane);
@@ -345,7 +421,7 @@ __global__ void __launch_bounds__(kGrpThreads, 1) moe_grouped_gemm_kernel(const 
 // 5. combine: out[t] = sum_j w[t][j] * d[t*k + j] + sigmoid(g . x[t]) * sh[t]
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeArgs a, const float* d) {
-    const int t = blockIdx.y;
+    const int t = blockIdx.x;
     __shared__ float red[8];
     __shared__ float gate_s;
     pdl_wait();
@@ -366,29 +442,49 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeArgs a, const
         __syncthreads();
         gate = gate_s;
     }
-    const int i = blockIdx.x * 256 + threadIdx.x;
-    if (i >= a.hidden) return;
-    float acc = 0.f;
-    for (int j = 0; j < a.topk; ++j)
-        acc = fmaf(a.w[(long long)t * a.topk + j], d[((long long)t * a.topk + j) * a.hidden + i], acc);
-    if (a.sh_inter > 0) acc = fmaf(gate, a.sh[(long long)t * a.hidden + i], acc);
-    a.out[(long long)t * a.hidden + i] = acc;
+    const float* wt = a.w + (long long)t * a.topk;
+    for (int i = 4 * threadIdx.x; i < a.hidden; i += 4 * 256) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < a.topk; ++j) {
+            const float wj = wt[j];
+            const float4 v = *reinterpret_cast<const float4*>(d + ((long long)t * a.topk + j) * a.hidden + i);
+            acc.x = fmaf(wj, v.x, acc.x);
+            acc.y = fmaf(wj, v.y, acc.y);
+            acc.z = fmaf(wj, v.z, acc.z);
+            acc.w = fmaf(wj, v.w, acc.w);
+        }
+        if (a.sh_inter > 0) {
+            const float4 v = *reinterpret_cast<const float4*>(a.sh + (long long)t * a.hidden + i);
+            acc.x = fmaf(gate, v.x, acc.x);
+            acc.y = fmaf(gate, v.y, acc.y);
+            acc.z = fmaf(gate, v.z, acc.z);
+            acc.w = fmaf(gate, v.w, acc.w);
+        }
+        *reinterpret_cast<float4*>(a.out + (long long)t * a.hidden + i) = acc;
+    }
 }
 
 template <int K>
 cudaError_t launch_grouped(const MoeArgs& a, const GroupedProj& p, cudaStream_t s) {
     const int smem = 2 * tc::kABlockBytes + 2 * 2 * 256 * a.grp_cap + 1024;
-    const void* f = reinterpret_cast<const void*>(moe_grouped_gemm_kernel<K>);
+    const int groups = a.grp_cap >= 64 ? 2 : 1;
+    const void* f = groups == 2 ? reinterpret_cast<const void*>(moe_grouped_gemm_kernel<K, 2>)
+                                : reinterpret_cast<const void*>(moe_grouped_gemm_kernel<K, 1>);
     cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     void* args[] = {const_cast<MoeArgs*>(&a), const_cast<GroupedProj*>(&p)};
-    return launch_kernel(f, dim3(p.out / 128, a.grp_max_items), dim3(kGrpThreads), smem, true, s, args);
+    return launch_kernel(f, dim3(p.out / 128, a.grp_max_items), dim3(groups * tc::kMlThreads), smem, true, s, args);
 }
 
 cudaError_t launch_prep(const MoeArgs& a, const GroupedProj& p, cudaStream_t s) {
-    const long long tasks = (long long)a.T * a.topk * (p.in / 128);
+    const long long blocks = (long long)a.T * a.topk * (p.in / 128);
     void* args[] = {const_cast<MoeArgs*>(&a), const_cast<GroupedProj*>(&p)};
-    return launch_kernel(reinterpret_cast<const void*>(moe_prep_kernel), dim3(static_cast<unsigned>((tasks + 7) / 8)),
+    if (blocks >= 4ll * 152 * 64) {  // four blocks per warp still leave 64 warps per SM
+        const long long tasks = (long long)a.T * a.topk * ((p.in / 128 + 3) / 4);
+        return launch_kernel(reinterpret_cast<const void*>(moe_prep_kernel<4>),
+                             dim3(static_cast<unsigned>((tasks + 7) / 8)), dim3(256), 0, true, s, args);
+    }
+    return launch_kernel(reinterpret_cast<const void*>(moe_prep_kernel<1>), dim3(static_cast<unsigned>((blocks + 7) / 8)),
                          dim3(256), 0, true, s, args);
 }
 
@@ -419,18 +515,26 @@ GroupPlan group_plan(int T, int topk, int E, int hidden, int inter, int sh_inter
     // counts[E], offsets[E+1], poff[E], items[max_items], nitems, perm[S], ppos[S]
     g.int_bytes = (size_t)(E + (E + 1) + E + g.max_items + 1 + 2 * S) * 4;
     const size_t trellis_img = (size_t)(hidden > inter ? hidden : inter) * 2 * g.pos_cap * 2;
-    const size_t shared_img = sh_inter > 0 ? int8_gemm_image_bytes(hidden > sh_inter ? hidden : sh_inter, T) : 0;
+    size_t shared_img = 0;
+    if (sh_inter > 0) {
+        const size_t gu = int8_gemm_ws_bytes(2 * sh_inter, hidden, T), dn = int8_gemm_ws_bytes(hidden, sh_inter, T);
+        shared_img = gu > dn ? gu : dn;
+    }
     g.img_bytes = trellis_img > shared_img ? trellis_img : shared_img;
     return g;
 }
 
-cudaError_t launch_moe_grouped(const MoeArgs& a, float* d, int num_sms, cudaStream_t s) {
-    (void)num_sms;
+cudaError_t launch_moe_topk_group(const MoeArgs& a, cudaStream_t s) {
     void* args[] = {const_cast<MoeArgs*>(&a)};
     cudaError_t e = launch_kernel(reinterpret_cast<const void*>(moe_topk_kernel), dim3((a.T + 7) / 8), dim3(256), 0,
                                   true, s, args);
     if (e != cudaSuccess) return e;
-    e = launch_kernel(reinterpret_cast<const void*>(moe_group_kernel), dim3(1), dim3(1024), 0, true, s, args);
+    return launch_kernel(reinterpret_cast<const void*>(moe_group_kernel), dim3(1), dim3(1024), 0, true, s, args);
+}
+
+cudaError_t launch_moe_grouped(const MoeArgs& a, float* d, int num_sms, cudaStream_t s) {
+    (void)num_sms;
+    cudaError_t e = launch_moe_topk_group(a, s);
     if (e != cudaSuccess) return e;
     const GroupedProj gu{a.gu_codes, a.gu_rin, a.gu_rout, a.hidden, 2 * a.inter, 0, a.ygu};
     if ((e = launch_prep(a, gu, s)) != cudaSuccess) return e;
@@ -443,7 +547,7 @@ cudaError_t launch_moe_grouped(const MoeArgs& a, float* d, int num_sms, cudaStre
 
 cudaError_t launch_moe_combine(const MoeArgs& a, const float* d, cudaStream_t s) {
     void* args[] = {const_cast<MoeArgs*>(&a), const_cast<float**>(&d)};
-    return launch_kernel(reinterpret_cast<const void*>(moe_combine_kernel), dim3((a.hidden + 255) / 256, a.T),
+    return launch_kernel(reinterpret_cast<const void*>(moe_combine_kernel), dim3(a.T),
                          dim3(256), 0, true, s, args);
 }
 

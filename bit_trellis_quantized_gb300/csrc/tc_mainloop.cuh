@@ -101,3 +101,65 @@ __device__ __forceinline__ bool mma_mainloop(uint8_t* Abuf, uint8_t* Bbuf, uint3
 
 }  // namespace tc
 }  // namespace escha
+
+namespace escha {
+namespace tc {
+
+__device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Two producer groups of 256 threads (warps 0-7 and 8-15) take alternate K
+// blocks (group g: blocks g, g+2, ...). Each group has its own A buffer, B
+// buffer, barrier pair and TMEM accumulator (columns g*acc_cols ..), so one
+// group decodes while the other's MMAs run; the caller adds the two
+// accumulators (group 1 holds nothing when nblk == 1). `produce(b, b_next, A)`
+// writes block b's A and may prefetch block b_next (>= nblk: none); it is
+// called by the group's 256 threads.
+template <bool A_MN, class ProduceA>
+__device__ __forceinline__ bool mma_mainloop_2grp(uint8_t* Abuf, uint8_t* Bbuf, uint32_t b_chunk_bytes,
+                                                  const uint8_t* img, long long img_chunk_bytes, uint32_t copy_bytes,
+                                                  int nblk, uint32_t tmem, uint32_t acc_cols, uint32_t idesc,
+                                                  MmaBars& bars, ProduceA&& produce) {
+    const int g = threadIdx.x >> 8;
+    const bool leader = (threadIdx.x & 255) == 0;
+    uint8_t* A = Abuf + g * kABlockBytes;
+    uint8_t* B = Bbuf + g * 2 * b_chunk_bytes;
+    const uint32_t full = smem_addr(&bars.full[g]), done = smem_addr(&bars.done[g]);
+    const uint32_t acc = tmem + static_cast<uint32_t>(g) * acc_cols;
+    bool ok = true;
+    int k = 0;
+    for (int b = g; b < nblk; b += 2, ++k) {
+        // the group's previous MMAs have finished with its A and B buffers
+        if (k >= 1 && !mbar_wait_parity_bounded(done, (k - 1) & 1)) ok = false;
+        if (leader) {
+            mbar_arrive_expect_tx(full, 2u * copy_bytes);
+            bulk_g2s(smem_addr(B), img + (2ll * b) * img_chunk_bytes, copy_bytes, full);
+            bulk_g2s(smem_addr(B + b_chunk_bytes), img + (2ll * b + 1) * img_chunk_bytes, copy_bytes, full);
+        }
+        produce(b, b + 2, A);
+        fence_proxy_async_smem();
+        fence_before_sync();
+        named_barrier_sync(1 + g, 256);
+        if (leader) {
+            fence_after_sync();
+            if (!mbar_wait_parity_bounded(full, k & 1)) ok = false;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t ad =
+                    A_MN ? smem_desc(smem_addr(A + kk * 4096), 2048u, 1024u, kSwizzle128B)
+                         : smem_desc(smem_addr(A + (kk >> 2) * 16384) + (kk & 3) * 32u, 16u, 1024u, kSwizzle128B);
+                const uint64_t bd =
+                    smem_desc(smem_addr(B + (kk >> 2) * b_chunk_bytes) + (kk & 3) * 32u, 16u, 1024u, kSwizzle128B);
+                mma_f16(acc, ad, bd, idesc, k > 0 || kk > 0);
+            }
+            commit(done);
+        }
+    }
+    if (k >= 1 && !mbar_wait_parity_bounded(done, (k - 1) & 1)) ok = false;
+    fence_after_sync();
+    return !__syncthreads_or(!ok);
+}
+
+}  // namespace tc
+}  // namespace escha

@@ -92,11 +92,8 @@ __device__ __forceinline__ void cta_gemv_partial(const uint16_t* codes, int NT, 
 #pragma unroll
         for (int q = 0; q < 16; ++q) acc[t][q] = 0.f;
 
-    for (int kt = kt0 + warp; kt < kt1; kt += NW) {
-        LaneCodes<K> nxt;
-        const bool more = kt + NW < kt1;
-        if (more) load_lane_codes<K>(nxt, codes + ((long long)(kt + NW) * NT + ob * 8) * (16 * K), lane);
-        cur.p[2 * K] = __shfl_sync(0xffffffffu, cur.p[0], nbr) & 0xFFFFu;
+    auto step = [&](LaneCodes<K>& lc, int kt) {
+        lc.p[2 * K] = __shfl_sync(0xffffffffu, lc.p[0], nbr) & 0xFFFFu;
         float xr[NB][4];
 #pragma unroll
         for (int t = 0; t < NB; ++t) {
@@ -106,8 +103,19 @@ __device__ __forceinline__ void cta_gemv_partial(const uint16_t* codes, int NT, 
             xr[t][2] = xv.z;
             xr[t][3] = xv.w;
         }
-        decode_fma<K, NB>(cur, xr, acc);
-        if (more) cur = nxt;
+        decode_fma<K, NB>(lc, xr, acc);
+    };
+    // rows kt0 + warp + i*NW, two per iteration: `cur` and `nxt` take turns, so
+    // the codes of the next row load while a row is decoded and are never
+    // copied (a register copy would wait for the load)
+    LaneCodes<K> nxt;
+    for (int kt = kt0 + warp; kt < kt1; kt += 2 * NW) {
+        const bool more1 = kt + NW < kt1;
+        if (more1) load_lane_codes<K>(nxt, codes + ((long long)(kt + NW) * NT + ob * 8) * (16 * K), lane);
+        step(cur, kt);
+        if (!more1) break;
+        if (kt + 2 * NW < kt1) load_lane_codes<K>(cur, codes + ((long long)(kt + 2 * NW) * NT + ob * 8) * (16 * K), lane);
+        step(nxt, kt + NW);
     }
 
     // Reduce-scatter over the 4 lanes of a tile: lane c keeps output columns

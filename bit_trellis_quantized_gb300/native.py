@@ -39,6 +39,8 @@ EXPORTS = [
     "escha_moe_block",
     "escha_moe_block_timed",
     "escha_moe_block_noalloc",
+    "escha_moe_route_workspace",
+    "escha_moe_route",
     "int8_w8a16_workspace",
     "int8_w8a16_matvec",
     "int8_w8a16_dequant",
@@ -104,6 +106,11 @@ def lib() -> ctypes.CDLL:
         L.escha_moe_block_timed.restype = _i
         L.escha_moe_block_noalloc.argtypes = [ctypes.POINTER(EschaMoeLayer), _vp, _i, _vp, _vp, _vp, _vp]
         L.escha_moe_block_noalloc.restype = _i
+        L.escha_moe_route_workspace.argtypes = [ctypes.POINTER(EschaMoeLayer), _i]
+        L.escha_moe_route_workspace.restype = _sz
+        L.escha_moe_route.argtypes = [ctypes.POINTER(EschaMoeLayer), _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
+                                      _vp]
+        L.escha_moe_route.restype = _i
         L.int8_w8a16_workspace.argtypes = [_i, _i, _i]
         L.int8_w8a16_workspace.restype = _sz
         L.int8_w8a16_matvec.argtypes = [_vp, _vp, _i, _i, _vp, _i, _i, _vp, _vp, _sz, _vp]
@@ -282,3 +289,24 @@ class MoeBlock:
         check(lib().escha_moe_block(ctypes.byref(self.layer), ptr(x), T, ptr(out), ptr(ids), ptr(w), ptr(ws),
                                     ws.numel(), stream_handle(stream)))
         return out, ids, w
+
+    def route(self, x: torch.Tensor, stream=None) -> dict:
+        """Diagnostic: router logits (fp16 bits), ids, w and the grouping by
+        expert (counts, offsets, perm) for x [T][hidden] fp16."""
+        _need_cuda(x)
+        T, E, k = x.shape[0], self.n_experts, self.topk
+        dev = x.device
+        r = {
+            "logits": torch.empty((T, E), dtype=torch.int16, device=dev),
+            "ids": torch.empty((T, k), dtype=torch.int32, device=dev),
+            "w": torch.empty((T, k), dtype=torch.float32, device=dev),
+            "counts": torch.empty(E, dtype=torch.int32, device=dev),
+            "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+            "perm": torch.empty(T * k, dtype=torch.int32, device=dev),
+        }
+        need = lib().escha_moe_route_workspace(ctypes.byref(self.layer), T)
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        check(lib().escha_moe_route(ctypes.byref(self.layer), ptr(x), T, ptr(r["logits"]), ptr(r["ids"]), ptr(r["w"]),
+                                    ptr(r["counts"]), ptr(r["offsets"]), ptr(r["perm"]), ptr(ws), ws.numel(),
+                                    stream_handle(stream)))
+        return r

@@ -194,12 +194,35 @@ int escha_moe_block_timed(const escha_moe_layer* L, const uint16_t* x, int T, fl
 int escha_moe_block_noalloc(const escha_moe_layer* L, const uint16_t* x, int T, float* out, int32_t* ids_out,
                             float* w_out, void* stream);
 
+/* ---- routing diagnostic -------------------------------------------------
+ * Diagnostic export, not used by the hot path: the router, top-k and
+ * grouping steps of escha_moe_block (the grouped path's kernels, run for any
+ * T) with their intermediate results copied out, for bit-exact checks.
+ *   logits_out  fp16 bits [T][E]: f16_rne of the router dot products, summed in
+ *               the order stated for escha_moe_block (nullable)
+ *   ids_out     int32 [T][topk], w_out f32 [T][topk] (required, 4-byte aligned)
+ *   counts_out  int32 [E]: slots per expert (nullable)
+ *   offsets_out int32 [E+1]: exclusive prefix sum of counts (nullable)
+ *   perm_out    int32 [T*topk]: the slots t*topk + j in expert order, stable in
+ *               slot order within an expert (nullable)
+ * Workspace from escha_moe_route_workspace(L, T); layer checks and errors as
+ * escha_moe_block. Grouping as in [PR694], commits on the grouped prefill GEMM
+ * (per-expert offsets and a slot permutation feeding one GEMM per expert). */
+size_t escha_moe_route_workspace(const escha_moe_layer* L, int T);
+int escha_moe_route(const escha_moe_layer* L, const uint16_t* x, int T, uint16_t* logits_out, int32_t* ids_out,
+                    float* w_out, int32_t* counts_out, int32_t* offsets_out, int32_t* perm_out, void* ws,
+                    size_t ws_bytes, void* stream);
+
 /* ---- int8 w8a16 ----------------------------------------------------------
  * y[m][o] = sum_i (scale[o] * W[o][i]) * x[m][i], f32 output, with the int8
  * weights used as stored (no dequantised copy) [MTPLX PR #242 "serve Qwen3.6-35B-A3B-Escha-W2 natively", table
  * "Improvements": int8 non-experts, fused matvec, no dequant at load; MLX
- * "Exactness of every tensor": dequant = f32 scale*w8]. M == 1 runs the matvec;
- * M > 1 runs the GEMM path.
+ * "Exactness of every tensor": dequant = f32 scale*w8]. M < 16 (or Kin not a
+ * multiple of 128) runs the CUDA-core matvec; M >= 16 with Kin % 128 == 0 runs
+ * the tensor-core GEMM (int8 converted exactly to the activation's 16-bit type;
+ * f32 activations split into bf16 hi + lo), whose scratch (B image and K-split
+ * partial sums) comes from the workspace: ws_bytes >= int8_w8a16_workspace(N,
+ * Kin, M), else ESCHA_E_WORKSPACE.
  *   W      int8 [N][Kin];  scales f32 [N]
  *   N      >= 1;  Kin multiple of 16
  *   x      [M][Kin], x_dtype ESCHA_BF16, ESCHA_F16 or ESCHA_F32

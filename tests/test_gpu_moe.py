@@ -202,3 +202,48 @@ def test_moe_grouped_status_word_clear(native):
     block(x)
     torch.cuda.synchronize()
     assert int(block.workspace(20)[:4].view(torch.int32).item()) == 0
+
+
+# ---------------------------------------------------------- routing diagnostic
+# escha_moe_route copies out the router logits and the grouping, so the router
+# sum order, the top-k selection and the stable counting sort are checked bit
+# for bit against the oracle.
+
+
+def _check_route(native, d, x, topk):
+    block = native.MoeBlock(d, topk=topk)
+    r = {k: v.cpu().numpy() for k, v in block.route(dev(x)).items()}
+    ref_ids, ref_w, ref_logits = o.route(x, d["Wg"], topk)
+    assert np.array_equal(r["logits"].view(np.uint16), ref_logits), "router logits must match bit for bit"
+    assert np.array_equal(r["ids"], ref_ids)
+    assert np.allclose(r["w"], ref_w, rtol=1e-5, atol=1e-6)
+    counts, offsets, perm = o.group_by_expert(ref_ids, d["Wg"].shape[0])
+    assert np.array_equal(r["counts"], counts)
+    assert np.array_equal(r["offsets"], offsets)
+    assert np.array_equal(r["perm"], perm)
+
+
+@pytest.mark.parametrize("T", [1, 3, 16, 64, 257])
+def test_route_bit_exact(native, T):
+    """Both router kernels (T < 16 one expert per warp, T >= 16 tiled) and the
+    grouping; 257 tokens span several 256-slot rounds and a ragged tail."""
+    d = gen.moe_layer(50 + T, hidden=2048, inter=128, n_experts=256)
+    x = gen.fp16_normal(gen.rng(60 + T), (T, 2048))
+    _check_route(native, d, x, topk=8)
+
+
+def test_route_hidden_not_multiple_of_1024(native):
+    """hidden 768: the tiled router's last column chunk is partial."""
+    d = gen.moe_layer(70, hidden=768, inter=128, n_experts=40)
+    x = gen.fp16_normal(gen.rng(71), (37, 768))
+    _check_route(native, d, x, topk=6)
+
+
+def test_route_skewed_load(native):
+    """Most tokens prefer the same few experts (inputs along one direction):
+    long runs per expert, several grouping rounds per warp segment."""
+    d = gen.moe_layer(72, hidden=512, inter=128, n_experts=16)
+    g = gen.rng(73)
+    base = g.standard_normal(512)
+    x = (base[None, :] + 0.1 * g.standard_normal((600, 512))).astype(np.float16)
+    _check_route(native, d, x, topk=2)
