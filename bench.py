@@ -369,11 +369,121 @@ def run_ours(args, ws, rank, local):
         "clocks": clocks,
         "routing_distinct_in_16_steps": distinct,
     }
+    if ws == 1 and not args.no_extended:
+        line["configs"] = extended(dev, blocks, hbm, tflops)
     if ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
+
+
+def _time_graph(torch, stream, fn, reps: int, warm: int = 3) -> float:
+    """ms per call of fn (captured once into a CUDA graph holding `reps`
+    calls; fn(i) issues call i), after warm-up replays; CUDA events on the
+    launching stream."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn(0)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(reps):
+                fn(i)
+        for _ in range(warm):
+            g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def extended(dev, blocks, hbm, tflops):
+    """The other workloads of the benchmark's configuration list, each with
+    inputs larger than L2 (distinct weights cycled) unless stated:
+    single projection at batch 1, the MoE block at batch 64 / 256 and a
+    2048-token prefill chunk, the int8 w8a16 shapes at M = 1 and 2048, and
+    the 40-block stack at batch 1 / 8 / 128 and a 2048-token chunk."""
+    import torch
+
+    from bit_trellis_quantized_gb300 import native
+    from escha_synth.gen_torch import moe_layer_device, projections_device
+
+    stream = torch.cuda.Stream(device=dev)
+    res = {}
+
+    # single projection 1024x2048, K=2, batch 1: 1024 distinct projections (512 MB)
+    P = 1024
+    pj = projections_device(7001, dev, P)
+    y = torch.empty((P, 1024), dtype=torch.float32, device=dev)
+    ms = _time_graph(torch, stream, lambda i: native.trellis_gemv(pj["codes"][i % P], pj["x"][i % P:i % P + 1],
+                                                                  pj["rin"][i % P], pj["rout"][i % P],
+                                                                  y=y[i % P:i % P + 1]), reps=P)
+    b = 2048 * 1024 * 2 // 8
+    res["single_projection_1024x2048_k2_b1"] = {"us": ms * 1e3, "packed_gbs": b / (ms * 1e-3) / 1e9,
+                                               "frac_of_hbm": b / (ms * 1e-3) / 1e9 / hbm,
+                                               "l2": f"{P} distinct projections ({P * b >> 20} MB) cycled"}
+    del pj, y
+
+    # MoE block at batch 64 / 256 / 2048 over the headline's layers, fresh x per call
+    nl = len(blocks)
+    mb = {}
+    for T in (64, 256, 2048):
+        ws = torch.empty(max(native.lib().escha_moe_block_workspace(native.ctypes.byref(blocks[0].layer), T), 256),
+                         dtype=torch.uint8, device=dev)
+        reps = nl if T <= 256 else 8
+        xs = torch.randn((reps, T, HIDDEN), device=dev).to(torch.float16)
+        out = torch.empty((T, HIDDEN), dtype=torch.float32, device=dev)
+        ms = _time_graph(torch, stream, lambda i: blocks[i % nl](xs[i], out=out, ws=ws), reps=reps)
+        mb[f"b{T}" if T < 2048 else "prefill_2048"] = {"tokens_per_s": T / (ms * 1e-3), "us_per_block": ms * 1e3}
+        del ws, xs
+    res["moe_block"] = mb
+
+    # int8 w8a16: M = 1 (HBM) and M = 2048 (tensor cores), bf16 x
+    i8 = {}
+    for N, Kin in ((4096, 2048), (2048, 4096), (152064, 2048)):
+        copies = max(1, (256 << 20) // (N * Kin))  # >= 256 MB of distinct weights at M = 1
+        W = torch.randint(-127, 128, (copies, N, Kin), dtype=torch.int8, device=dev)
+        s = torch.rand((copies, N), device=dev) * 9e-3 + 1e-3
+        x1 = torch.randn((copies, 1, Kin), device=dev).to(torch.bfloat16)
+        y1 = torch.empty((copies, 1, N), dtype=torch.float32, device=dev)
+        ms1 = _time_graph(torch, stream, lambda i: native.int8_w8a16_matvec(W[i % copies], s[i % copies],
+                                                                            x1[i % copies], y=y1[i % copies]),
+                          reps=max(copies, 8))
+        M = 2048
+        xm = torch.randn((M, Kin), device=dev).to(torch.bfloat16)
+        ym = torch.empty((M, N), dtype=torch.float32, device=dev)
+        ms2 = _time_graph(torch, stream, lambda i: native.int8_w8a16_matvec(W[i % copies], s[i % copies], xm, y=ym),
+                          reps=4)
+        gbs = N * Kin / (ms1 * 1e-3) / 1e9
+        tf = 2.0 * M * N * Kin / (ms2 * 1e-3) / 1e12
+        i8[f"{N}x{Kin}"] = {"m1_us": ms1 * 1e3, "m1_gbs": gbs, "m1_frac_of_hbm": gbs / hbm,
+                            "m2048_us": ms2 * 1e3, "m2048_tflops": tf, "m2048_frac_of_bf16": tf / tflops}
+        del W, s, x1, y1, xm, ym
+    res["int8_w8a16"] = i8
+    torch.cuda.empty_cache()
+
+    # 40-block stack (K per projection from seed 5000 + block), ~10.6 GB
+    sblocks = []
+    for l in range(40):
+        kg, kd = gen.stack_k(l)
+        sblocks.append(native.MoeBlock(moe_layer_device(5000 + l, dev, k_gu=kg, k_dn=kd), device=dev))
+    stack = native.MoeStack(sblocks)
+    st = {}
+    for T in (1, 8, 128, 2048):
+        x0 = torch.randn((T, HIDDEN), device=dev)
+        h = x0.clone()
+        xb = torch.empty((T, HIDDEN), dtype=torch.float16, device=dev)
+        ob = torch.empty((T, HIDDEN), dtype=torch.float32, device=dev)
+        stack.workspace(T)
+        ms = _time_graph(torch, stream, lambda i: stack(h, xb, ob), reps=2 if T == 2048 else 4)
+        st[f"b{T}" if T < 2048 else "prefill_2048"] = {"tokens_per_s": T / (ms * 1e-3), "ms_per_pass": ms}
+    res["stack_40_blocks"] = st
+    del stack, sblocks
+    torch.cuda.empty_cache()
+    return res
 
 
 def main():
@@ -383,6 +493,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extended", action="store_true", help="skip the other configurations (batched, prefill, "
+                                                               "single projection, int8 shapes, 40-block stack)")
     ap.add_argument("--no-graph", action="store_true", help="launch the steps directly (for profilers)")
     ap.add_argument("--layers", type=int, default=N_LAYERS, help="distinct layers cycled through")
     args = ap.parse_args()

@@ -391,6 +391,18 @@ int escha_moe_route(const escha_moe_layer* L, const uint16_t* x, int T, uint16_t
     return ESCHA_OK;
 }
 
+int escha_residual_rmsnorm(float* h, const float* add, int T, int hidden, float eps, uint16_t* x_out, void* stream) {
+    if (!h) return fail(ESCHA_E_ARG, "residual_rmsnorm: null h");
+    if (T < 1 || hidden < 1 || hidden > 8192) return fail(ESCHA_E_SHAPE, "residual_rmsnorm: T=%d hidden=%d", T, hidden);
+    if (!(eps >= 0.f)) return fail(ESCHA_E_ARG, "residual_rmsnorm: eps must be >= 0");
+    if (!aligned16(h) || (add && !aligned16(add)) || (x_out && !aligned16(x_out)))
+        return fail(ESCHA_E_ALIGN, "residual_rmsnorm: pointer not 16-byte aligned");
+    int r, sms;
+    if ((r = device_check(&sms))) return r;
+    return cuda_status(escha::launch_residual_rmsnorm(h, add, T, hidden, eps, x_out, static_cast<cudaStream_t>(stream)),
+                       "residual_rmsnorm launch");
+}
+
 size_t int8_w8a16_workspace(int N, int Kin, int M) {
     (void)N;
     if (M < 1 || Kin < 16) return 0;

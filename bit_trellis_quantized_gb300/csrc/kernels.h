@@ -123,6 +123,11 @@ cudaError_t launch_moe_grouped(const MoeArgs& a, float* d, int num_sms, cudaStre
 // out = sum_j w * d + sigmoid(gate) * sh
 cudaError_t launch_moe_combine(const MoeArgs& a, const float* d, cudaStream_t s);
 
+// h[t] += add[t] (add nullable); then, when x is not null, x[t] = fp16 of the
+// weightless RMSNorm of h[t] (summation order fixed in stack.cu).
+cudaError_t launch_residual_rmsnorm(float* h, const float* add, int T, int hidden, float eps, uint16_t* x,
+                                    cudaStream_t s);
+
 cudaError_t launch_moe_router(const MoeArgs& a, cudaStream_t s);
 cudaError_t launch_moe_gate_up(const MoeArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_moe_down(const MoeArgs& a, cudaStream_t s);

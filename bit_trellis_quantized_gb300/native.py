@@ -41,6 +41,7 @@ EXPORTS = [
     "escha_moe_block_noalloc",
     "escha_moe_route_workspace",
     "escha_moe_route",
+    "escha_residual_rmsnorm",
     "int8_w8a16_workspace",
     "int8_w8a16_matvec",
     "int8_w8a16_dequant",
@@ -111,6 +112,8 @@ def lib() -> ctypes.CDLL:
         L.escha_moe_route.argtypes = [ctypes.POINTER(EschaMoeLayer), _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
                                       _vp]
         L.escha_moe_route.restype = _i
+        L.escha_residual_rmsnorm.argtypes = [_vp, _vp, _i, _i, ctypes.c_float, _vp, _vp]
+        L.escha_residual_rmsnorm.restype = _i
         L.int8_w8a16_workspace.argtypes = [_i, _i, _i]
         L.int8_w8a16_workspace.restype = _sz
         L.int8_w8a16_matvec.argtypes = [_vp, _vp, _i, _i, _vp, _i, _i, _vp, _vp, _sz, _vp]
@@ -205,6 +208,25 @@ def int8_w8a16_matvec(W, scales, x, y=None, stream=None) -> torch.Tensor:
     return y
 
 
+def residual_rmsnorm(h, add=None, x_out=None, eps: float = 1e-6, stream=None):
+    """h f32 [T][hidden] += add (optional); then x_out (fp16 [T][hidden], made
+    if None) = fp16 of the weightless RMSNorm of h. Returns x_out."""
+    _need_cuda(h)
+    T, H = h.shape
+    if x_out is None:
+        x_out = torch.empty((T, H), dtype=torch.float16, device=h.device)
+    check(lib().escha_residual_rmsnorm(ptr(h), ptr(add) if add is not None else None, T, H, float(eps), ptr(x_out),
+                                       stream_handle(stream)))
+    return x_out
+
+
+def residual_add(h, add, stream=None) -> None:
+    """h += add (f32, in place) through the same kernel, without the norm."""
+    _need_cuda(h, add)
+    T, H = h.shape
+    check(lib().escha_residual_rmsnorm(ptr(h), ptr(add), T, H, 0.0, None, stream_handle(stream)))
+
+
 def int8_w8a16_dequant(W, scales, stream=None) -> torch.Tensor:
     _need_cuda(W, scales)
     N, Kin = W.shape
@@ -273,9 +295,10 @@ class MoeBlock:
             self._ws = torch.empty(max(need, 256), dtype=torch.uint8, device=self.t["router_w"].device)
         return self._ws
 
-    def __call__(self, x: torch.Tensor, out=None, ids=None, w=None, stream=None):
+    def __call__(self, x: torch.Tensor, out=None, ids=None, w=None, stream=None, ws=None):
         """x [T][hidden] fp16 (CUDA). Returns (out f32 [T][hidden], ids int32
-        [T][topk], w f32 [T][topk])."""
+        [T][topk], w f32 [T][topk]). ``ws`` optionally replaces the block's own
+        workspace (e.g. one shared by the blocks of a stack)."""
         _need_cuda(x)
         T = x.shape[0]
         dev = x.device
@@ -285,7 +308,8 @@ class MoeBlock:
             ids = torch.empty((T, self.topk), dtype=torch.int32, device=dev)
         if w is None:
             w = torch.empty((T, self.topk), dtype=torch.float32, device=dev)
-        ws = self.workspace(T)
+        if ws is None:
+            ws = self.workspace(T)
         check(lib().escha_moe_block(ctypes.byref(self.layer), ptr(x), T, ptr(out), ptr(ids), ptr(w), ptr(ws),
                                     ws.numel(), stream_handle(stream)))
         return out, ids, w
@@ -310,3 +334,42 @@ class MoeBlock:
                                     ptr(r["counts"]), ptr(r["offsets"]), ptr(r["perm"]), ptr(ws), ws.numel(),
                                     stream_handle(stream)))
         return r
+
+
+class MoeStack:
+    """MoE blocks on an f32 residual stream h: for each block, x =
+    fp16(RMSNorm(h)) (weightless), h += block(x); the add is fused into the
+    next block's norm. One workspace serves all blocks (same shapes)."""
+
+    def __init__(self, blocks, eps: float = 1e-6):
+        self.blocks = list(blocks)
+        self.eps = eps
+        self._ws = None
+
+    def workspace(self, T: int) -> torch.Tensor:
+        need = max(lib().escha_moe_block_workspace(ctypes.byref(b.layer), T) for b in self.blocks)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty(max(need, 256), dtype=torch.uint8, device=self.blocks[0].t["router_w"].device)
+        return self._ws
+
+    def __call__(self, h: torch.Tensor, x_buf=None, out_buf=None, stream=None, trace=None):
+        """Runs the stack on h (f32 [T][hidden], updated in place). With a list
+        ``trace``, appends (h before the block, x, block output) per block as
+        host copies (testing only: it synchronises)."""
+        _need_cuda(h)
+        T, H = h.shape
+        x = x_buf if x_buf is not None else torch.empty((T, H), dtype=torch.float16, device=h.device)
+        out = out_buf if out_buf is not None else torch.empty((T, H), dtype=torch.float32, device=h.device)
+        ws = self.workspace(T)
+        for i, b in enumerate(self.blocks):
+            h_before = h.clone() if trace is not None and i == 0 else None
+            residual_rmsnorm(h, out if i > 0 else None, x, self.eps, stream)
+            if trace is not None:
+                if i > 0:
+                    h_before = h.clone()
+                trace.append([h_before.cpu(), x.cpu()])
+            b(x, out=out, stream=stream, ws=ws)
+            if trace is not None:
+                trace[-1].append(out.cpu())
+        residual_add(h, out, stream)
+        return h

@@ -131,3 +131,10 @@ def bf16_normal_bits(g: np.random.Generator, shape) -> np.ndarray:
     u = f.view(np.uint32).astype(np.uint64)
     rounding = ((u >> 16) & 1) + 0x7FFF
     return ((u + rounding) >> 16).astype(np.uint16)
+
+
+def stack_k(layer: int):
+    """Bits per weight (2 or 3) of gate_up and down in block `layer` of the
+    synthetic 40-block stack, drawn from seed 5000 + layer."""
+    k = rng(5000 + layer).integers(2, 4, size=2)
+    return int(k[0]), int(k[1])

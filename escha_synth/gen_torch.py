@@ -55,3 +55,28 @@ def moe_layer_device(seed: int, device, hidden: int = 2048, inter: int = 512, n_
     d["hidden"], d["inter"], d["n_experts"], d["sh_inter"] = hidden, inter, E, sh_inter
     d["k_gu"], d["k_dn"] = k_gu, k_dn
     return d
+
+
+def projections_device(seed: int, device, P: int, n_in: int = 2048, n_out: int = 1024, K: int = 2,
+                       prune_rate: float = 0.55):
+    """P independent single projections (the gate_up shape by default):
+    codes [P][n_in/16][n_out/16][16K], rin +-1 [P][n_in], rout = U(0.5,1.5)*+-1
+    [P][n_out] with round(rate * n_out/2) channels zeroed by a mask shared by
+    the gate half and the up half, x ~ N(0,1) fp16 [P][n_in]."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    kw = dict(device=device, generator=g)
+    d = {"codes": torch.randint(-32768, 32768, (P, n_in // 16, n_out // 16, 16 * K), dtype=torch.int16, **kw),
+         "rin": ((torch.randint(0, 2, (P, n_in), **kw) * 2 - 1).to(torch.float16))}
+    r = torch.rand((P, n_out), **kw) + 0.5
+    r = r * (torch.randint(0, 2, (P, n_out), **kw) * 2 - 1)
+    half = n_out // 2
+    prune = int(round(prune_rate * half))
+    order = torch.rand((P, half), **kw).argsort(dim=1)
+    mask = torch.zeros((P, half), dtype=torch.bool, device=device)
+    mask.scatter_(1, order[:, :prune], True)
+    r[:, :half][mask] = 0
+    r[:, half:][mask] = 0
+    d["rout"] = r.to(torch.float16)
+    d["x"] = torch.randn((P, n_in), **kw).to(torch.float16)
+    return d

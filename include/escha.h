@@ -194,6 +194,22 @@ int escha_moe_block_timed(const escha_moe_layer* L, const uint16_t* x, int T, fl
 int escha_moe_block_noalloc(const escha_moe_layer* L, const uint16_t* x, int T, float* out, int32_t* ids_out,
                             float* w_out, void* stream);
 
+/* ---- residual stream between MoE blocks ----------------------------------
+ * h[t][i] += add[t][i] (add nullable), then, when x_out is not null,
+ * x_out[t][i] = f16_rne(h[t][i] * inv_t) with inv_t = 1 / sqrt(mean_i(h^2) +
+ * eps): a weightless RMSNorm, the input of the next block. In the pages'
+ * model every escha projection takes a plain RMS-normed input ([PR694],
+ * commit on escha_run_proj / escha_run_resid); random weights without a norm
+ * drive block outputs out of the fp16 range, so a stack of synthetic blocks
+ * needs one. The fp16 rounding feeds the router, so
+ * the arithmetic is fixed: f32 multiply then add of h^2 per thread t of 256
+ * over i = t, t+256, ... ascending; xor butterfly 16..1 within each warp, the
+ * 8 warp sums in order; mean = sum / hidden, IEEE sqrt and division.
+ *   h      f32 [T][hidden], updated in place;  add f32 [T][hidden] or NULL
+ *   x_out  fp16 bits [T][hidden] or NULL (then only the add is done)
+ *   hidden 1..8192, eps >= 0 */
+int escha_residual_rmsnorm(float* h, const float* add, int T, int hidden, float eps, uint16_t* x_out, void* stream);
+
 /* ---- routing diagnostic -------------------------------------------------
  * Diagnostic export, not used by the hot path: the router, top-k and
  * grouping steps of escha_moe_block (the grouped path's kernels, run for any

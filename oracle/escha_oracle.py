@@ -33,6 +33,9 @@ reason, in the design notes of the repository):
   (see ``router_logits``), then rounded to f16; top-k ties go to the lower
   expert id.
 * R-GATE  the shared-expert gate logit is an unrounded dot product.
+* R-NORM  a stack of blocks keeps an f32 residual h and feeds each block
+  fp16(h / sqrt(mean(h^2) + eps)), a weightless RMSNorm, with the sum of
+  squares in a fixed f32 order (see ``residual_rmsnorm``).
 """
 from __future__ import annotations
 
@@ -430,3 +433,45 @@ def moe_block(layer: MoeLayer, x, k: int = 8, tokens=None):
             acc += w[b, j] * moe_expert(layer, ids[b, j], xv[b])
         out[n] = acc + sh[n]
     return out, ids, w, logits
+
+
+# ----------------------------------------------------------------------------
+# Residual stream of a stack of blocks (reading R-NORM). Every escha
+# projection of the pages' model takes a plain RMS-normed input (hipfire PR
+# #694, commit on escha_run_proj / escha_run_resid). With random weights the
+# block outputs grow by ~1e4 per block without a norm, so a synthetic stack
+# normalises the f32 residual (no learned weight) and rounds to fp16. Since
+# that rounding feeds the router, the arithmetic is fixed: f32 multiply then
+# f32 add of h^2 per partial sum p = 0..255 over i = p, p+256, ... ascending;
+# the partials of each group of 32 combined by the xor butterfly (offsets 16,
+# 8, 4, 2, 1), the 8 group sums added in order; mean = sum / hidden; IEEE f32
+# sqrt and division; x = f16_rne(h * (1 / sqrt(mean + eps))).
+# ----------------------------------------------------------------------------
+
+
+def residual_rmsnorm(h, add=None, eps: float = 1e-6):
+    """Returns (h + add as f32 [T][H], x fp16 bit patterns [T][H])."""
+    h = np.array(h, dtype=np.float32, ndmin=2)
+    if add is not None:
+        h = (h + np.asarray(add, dtype=np.float32)).astype(np.float32)
+    T, H = h.shape
+    n = -(-H // 256)
+    hp = np.zeros((T, n * 256), dtype=np.float32)
+    hp[:, :H] = h
+    hp = hp.reshape(T, n, 256)
+    s = np.zeros((T, 256), dtype=np.float32)
+    for j in range(n):
+        present = (j * 256 + np.arange(256)) < H
+        sq = (hp[:, j, :] * hp[:, j, :]).astype(np.float32)
+        s = np.where(present, (sq + s).astype(np.float32), s)
+    s = s.reshape(T, 8, 32)
+    lanes = np.arange(32)
+    for m in (16, 8, 4, 2, 1):
+        s = (s + s[:, :, lanes ^ m]).astype(np.float32)
+    tot = s[:, 0, 0].copy()
+    for w in range(1, 8):
+        tot = (tot + s[:, w, 0]).astype(np.float32)
+    mean = (tot / np.float32(H)).astype(np.float32)
+    inv = (np.float32(1.0) / np.sqrt((mean + np.float32(eps)).astype(np.float32))).astype(np.float32)
+    x = f64_to_f16((h * inv[:, None]).astype(np.float32).astype(np.float64))
+    return h, x

@@ -398,3 +398,43 @@ def test_moe_routes_selected_experts_only():
         want = sum(w[b, j] * o.moe_expert(layer, ids[b, j], xv[b]) for j in range(2)) + sh[b]
         assert np.allclose(out[b], want, rtol=1e-12)
         assert len(set(ids[b])) == 2
+
+
+# ------------------------------------------------------------ R-NORM (stack)
+
+
+def test_rmsnorm_constant_row_closed_form():
+    """h = c everywhere: sum = H c^2 exactly, mean = c^2, x = c / |c| = +-1."""
+    for H in (512, 768, 100):
+        for c in (2.0, -0.5, 8.0):
+            h = np.full((3, H), c, dtype=np.float32)
+            h2, x = o.residual_rmsnorm(h, eps=0.0)
+            assert np.array_equal(h2, h)
+            assert np.all(x == (0x3C00 if c > 0 else 0xBC00))
+
+
+def test_rmsnorm_within_one_ulp_of_float64():
+    """Against an float64 RMSNorm computed directly (numpy's own sum):
+    the fixed-order f32 version lands on the same or an adjacent fp16."""
+    g = np.random.default_rng(5)
+    for H in (2048, 256, 300):
+        h = (g.standard_normal((16, H)) * g.uniform(0.1, 1e3, (16, 1))).astype(np.float32)
+        _, x = o.residual_rmsnorm(h, eps=1e-6)
+        hv = h.astype(np.float64)
+        ref = hv / np.sqrt(np.mean(hv * hv, axis=1, keepdims=True) + 1e-6)
+        xv = o.f16_to_f64(x)
+        ulp = np.abs(ref) * 2.0 ** -10 + 2.0 ** -24
+        assert np.all(np.abs(xv - ref) <= ulp)
+        # normalised rows have mean square 1 up to the fp16 rounding
+        assert np.allclose(np.mean(xv * xv, axis=1), 1.0, atol=2e-3)
+
+
+def test_rmsnorm_residual_add_and_scale_invariance():
+    g = np.random.default_rng(6)
+    h = g.standard_normal((4, 512)).astype(np.float32)
+    add = g.standard_normal((4, 512)).astype(np.float32)
+    h2, x = o.residual_rmsnorm(h, add, eps=0.0)
+    assert np.array_equal(h2, (h + add).astype(np.float32))
+    # multiplying a row by a power of two changes nothing (exact in f32)
+    _, x4 = o.residual_rmsnorm(h2 * np.float32(4.0), eps=0.0)
+    assert np.array_equal(x, x4)
