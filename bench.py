@@ -486,6 +486,44 @@ def extended(dev, blocks, hbm, tflops):
     return res
 
 
+PROFILE_CASES = ("block_b1", "block_b8", "block_b64", "block_b256", "prefill_2048", "projection_b1",
+                 "int8_m1", "int8_m2048")
+
+
+def profile_case(name: str, reps: int):
+    """One workload launched directly (no CUDA graph) `reps` times, for a
+    profiler's launch list or a capture of one kernel; prints nothing timed."""
+    import torch
+
+    from bit_trellis_quantized_gb300 import native
+    from escha_synth.gen_torch import moe_layer_device, projections_device
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if name.startswith("block_") or name == "prefill_2048":
+        T = 2048 if name == "prefill_2048" else int(name.split("_b")[1])
+        blk = native.MoeBlock(moe_layer_device(LAYER_SEED, dev), device=dev, topk=TOPK)
+        xs = torch.randn((reps, T, HIDDEN), device=dev).to(torch.float16)
+        out = torch.empty((T, HIDDEN), dtype=torch.float32, device=dev)
+        for i in range(reps):
+            blk(xs[i], out=out)
+    elif name == "projection_b1":
+        pj = projections_device(7001, dev, 64)
+        y = torch.empty((64, 1024), dtype=torch.float32, device=dev)
+        for i in range(reps):
+            native.trellis_gemv(pj["codes"][i % 64], pj["x"][i % 64:i % 64 + 1], pj["rin"][i % 64],
+                                pj["rout"][i % 64], y=y[i % 64:i % 64 + 1])
+    else:
+        M = 1 if name == "int8_m1" else 2048
+        W = torch.randint(-127, 128, (4096, 2048), dtype=torch.int8, device=dev)
+        s = torch.rand(4096, device=dev) * 9e-3 + 1e-3
+        x = torch.randn((M, 2048), device=dev).to(torch.bfloat16)
+        y = torch.empty((M, 4096), dtype=torch.float32, device=dev)
+        for i in range(reps):
+            native.int8_w8a16_matvec(W, s, x, y=y)
+    torch.cuda.synchronize()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -497,7 +535,13 @@ def main():
                                                                "single projection, int8 shapes, 40-block stack)")
     ap.add_argument("--no-graph", action="store_true", help="launch the steps directly (for profilers)")
     ap.add_argument("--layers", type=int, default=N_LAYERS, help="distinct layers cycled through")
+    ap.add_argument("--profile-case", choices=PROFILE_CASES, help="run one workload with direct launches "
+                                                                  "(for profilers) and exit")
+    ap.add_argument("--reps", type=int, default=3, help="launches of --profile-case")
     args = ap.parse_args()
+    if args.profile_case:
+        profile_case(args.profile_case, args.reps)
+        return
     if args.warmup < 3:
         args.warmup = 3
     # whole graphs of STEPS_PER_GRAPH steps

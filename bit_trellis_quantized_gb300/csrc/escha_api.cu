@@ -420,6 +420,8 @@ int int8_w8a16_matvec(const int8_t* W, const float* scales, int N, int Kin, cons
     if (!aligned16(W) || !aligned16(scales) || !aligned16(x) || !aligned16(y))
         return fail(ESCHA_E_ALIGN, "int8_w8a16_matvec: pointer not 16-byte aligned");
     const bool gemm = int8_uses_gemm(Kin, M);
+    if (!gemm && M > 1 && Kin > 51168)
+        return fail(ESCHA_E_SHAPE, "int8_w8a16_matvec: Kin=%d above 51168 for 2..15 tokens or Kin %% 128 != 0", Kin);
     if (gemm) {
         const size_t need = escha::int8_gemm_ws_bytes(N, Kin, M);
         if (!ws || ws_bytes < need)

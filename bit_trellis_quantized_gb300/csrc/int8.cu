@@ -158,6 +158,127 @@ __global__ void int8_dequant_kernel(const int8_t* __restrict__ W, const float* _
     out[idx] = __fmul_rn(scales[o], static_cast<float>(W[idx]));
 }
 
+// M = 1, enough loads in flight to stream the matrix at HBM rate. A tile is
+// G row groups of 4 rows x all nch 512-column chunks of those rows. Warp w of
+// a CTA always takes row group w / (8/G) and CPW chunks (w % (8/G) + j*(8/G)),
+// so its activations (16 per lane and chunk) are loaded once; per iteration a
+// CTA takes 4/CPW consecutive tiles and each warp issues all of its 4 x 4
+// row loads (16 bytes per lane) before any arithmetic. CTAs walk the tiles
+// grid-stride. Warp sums go to shared memory and are added per row in chunk
+// order.
+template <int CPW>
+__global__ void __launch_bounds__(256) int8_gemv_m1_kernel(const int8_t* __restrict__ W,
+                                                           const float* __restrict__ scales, int N, int Kin,
+                                                           const void* __restrict__ x, int x_dtype,
+                                                           float* __restrict__ y, int G, int nch) {
+    constexpr int TPI = 4 / CPW;     // tiles per iteration
+    extern __shared__ float part[];  // [TPI][G][4][nch]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wpg = 8 / G;           // warps per row group
+    const int g = warp / wpg, cw = warp % wpg;
+    const int rows_per_tile = G * kRowsPerWarp;
+    const int ntiles = (N + rows_per_tile - 1) / rows_per_tile;
+    float xv[CPW][16];
+#pragma unroll
+    for (int q = 0; q < CPW; ++q) {
+        const int c = cw + q * wpg;
+        const int i0 = c * 512 + lane * 16;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) xv[q][k] = 0.f;
+        if (c >= nch || i0 >= Kin) continue;
+        if (x_dtype == 3) {
+            const float4* xp = reinterpret_cast<const float4*>(static_cast<const float*>(x) + i0);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float4 v = __ldg(xp + u);
+                xv[q][4 * u] = v.x;
+                xv[q][4 * u + 1] = v.y;
+                xv[q][4 * u + 2] = v.z;
+                xv[q][4 * u + 3] = v.w;
+            }
+        } else {
+            const uint4* xp = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + i0);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const uint4 v = __ldg(xp + u);
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint16_t lo = static_cast<uint16_t>(w[k] & 0xFFFFu), hi = static_cast<uint16_t>(w[k] >> 16);
+                    xv[q][8 * u + 2 * k] = x_dtype == 1 ? h2f_bits(lo) : bf2f_bits(lo);
+                    xv[q][8 * u + 2 * k + 1] = x_dtype == 1 ? h2f_bits(hi) : bf2f_bits(hi);
+                }
+            }
+        }
+    }
+    for (int t0 = blockIdx.x * TPI; t0 < ntiles; t0 += gridDim.x * TPI) {
+        uint4 wv[TPI][CPW][kRowsPerWarp];
+#pragma unroll
+        for (int tt = 0; tt < TPI; ++tt) {
+            const int r0 = ((t0 + tt) * G + g) * kRowsPerWarp;
+#pragma unroll
+            for (int q = 0; q < CPW; ++q) {
+                const int i0 = (cw + q * wpg) * 512 + lane * 16;
+                if (cw + q * wpg >= nch || i0 >= Kin || t0 + tt >= ntiles) continue;
+#pragma unroll
+                for (int r = 0; r < kRowsPerWarp; ++r)
+                    wv[tt][q][r] = ldg_stream_v4(W + (long long)min(r0 + r, N - 1) * Kin + i0);
+            }
+        }
+#pragma unroll
+        for (int tt = 0; tt < TPI; ++tt) {
+#pragma unroll
+            for (int q = 0; q < CPW; ++q) {
+                const int c = cw + q * wpg;
+                if (c >= nch) break;
+                float acc[kRowsPerWarp] = {0.f, 0.f, 0.f, 0.f};
+                // Kin % 16 == 0: a lane's 16 columns are all in or all out
+                if (c * 512 + lane * 16 < Kin && t0 + tt < ntiles) {
+#pragma unroll
+                    for (int r = 0; r < kRowsPerWarp; ++r) {
+                        const uint32_t words[4] = {wv[tt][q][r].x, wv[tt][q][r].y, wv[tt][q][r].z, wv[tt][q][r].w};
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            float f[4];
+                            bytes_to_f32(words[u], f);
+#pragma unroll
+                            for (int b = 0; b < 4; ++b) acc[r] = fmaf(f[b], xv[q][4 * u + b], acc[r]);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < kRowsPerWarp; ++r) {
+                    float v = acc[r];
+#pragma unroll
+                    for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+                    if (lane == 0) part[((tt * G + g) * kRowsPerWarp + r) * nch + c] = v;
+                }
+            }
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < TPI * rows_per_tile; i += blockDim.x) {
+            const int row = t0 * rows_per_tile + i;
+            if (row < N) {
+                float s = 0.f;
+                for (int c = 0; c < nch; ++c) s += part[i * nch + c];
+                y[row] = scales[row] * s;
+            }
+        }
+        __syncthreads();
+    }
+}
+
+template <int CPW>
+cudaError_t launch_m1(const int8_t* W, const float* scales, int N, int Kin, const void* x, int x_dtype, float* y,
+                      int G, int nch, int num_sms, cudaStream_t s) {
+    const int rows_per_it = (4 / CPW) * G * kRowsPerWarp;
+    const int smem = rows_per_it * nch * (int)sizeof(float);
+    const long long its = (N + rows_per_it - 1) / rows_per_it;
+    const int grid = static_cast<int>(its < 4LL * num_sms ? its : 4LL * num_sms);
+    int8_gemv_m1_kernel<CPW><<<grid, 256, smem, s>>>(W, scales, N, Kin, x, x_dtype, y, G, nch);
+    return cudaGetLastError();
+}
+
 template <int MT>
 cudaError_t launch_mt(const int8_t* W, const float* scales, int N, int Kin, const void* x, int x_dtype,
                       long long x_stride, int act, int M, float* y, long long y_stride, int num_sms, cudaStream_t s) {
@@ -177,6 +298,19 @@ cudaError_t launch_mt(const int8_t* W, const float* scales, int N, int Kin, cons
 cudaError_t launch_int8_gemv(const int8_t* W, const float* scales, int N, int Kin, const void* x, int x_dtype,
                              long long x_stride, int act, int M, float* y, long long y_stride, int num_sms,
                              cudaStream_t s) {
+    const int nch = (Kin + 511) / 512;
+    // Batch 1 with few rows: rows x chunks spread over the CTAs. With many
+    // rows (four or more row groups of 32 per SM) the whole-row kernel below
+    // already has enough loads in flight and needs no shared-memory reduction.
+    if (M == 1 && act == 0 && nch <= 32 && N < 32 * 4 * num_sms) {
+        // warps per row group = chunks rounded up to a power of two (at most 8)
+        const int wpg = nch > 4 ? 8 : nch > 2 ? 4 : nch;
+        const int G = 8 / wpg;
+        const int cpw = (nch + wpg - 1) / wpg;  // chunks per warp: 1, 2 or 4 (up to 3 rounds up to 4)
+        if (cpw == 1) return launch_m1<1>(W, scales, N, Kin, x, x_dtype, y, G, nch, num_sms, s);
+        if (cpw == 2) return launch_m1<2>(W, scales, N, Kin, x, x_dtype, y, G, nch, num_sms, s);
+        return launch_m1<4>(W, scales, N, Kin, x, x_dtype, y, G, nch, num_sms, s);
+    }
     // tokens per pass whose f32 activations fit in shared memory
     const int cap = (200 * 1024 - 128) / (4 * Kin);
     if (cap < 1) return cudaErrorInvalidValue;

@@ -143,33 +143,42 @@ __global__ void __launch_bounds__(tc::kMlThreads, 1)
     // thread t converts row t/2, values 64*(t%2) .. +63 of every 128-value block
     const int r = tid >> 1, h = tid & 1;
     const int8_t* wrow = W + (long long)min(n0 + r, N - 1) * Kin + 64 * h + b_first * 128;
-    uint4 cur[4];
+    // two register sets for the int8 rows, used in turn: the next block loads
+    // into one while the other is converted (never copied: a copy would wait
+    // for the load)
+    uint4 wa[4], wb[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) cur[j] = __ldg(reinterpret_cast<const uint4*>(wrow) + j);
+    for (int j = 0; j < 4; ++j) wa[j] = __ldg(reinterpret_cast<const uint4*>(wrow) + j);
+    auto convert = [&](const uint4 (&w)[4], uint8_t* A) {
+        uint8_t* dst = A + h * 16384;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint2 x0 = i8x4_to_16<BF16>(w[j].x), x1 = i8x4_to_16<BF16>(w[j].y);
+            const uint2 x2 = i8x4_to_16<BF16>(w[j].z), x3 = i8x4_to_16<BF16>(w[j].w);
+            *reinterpret_cast<uint4*>(dst + tc::kmajor_off(static_cast<uint32_t>(r), 16u * j)) =
+                make_uint4(x0.x, x0.y, x1.x, x1.y);
+            *reinterpret_cast<uint4*>(dst + tc::kmajor_off(static_cast<uint32_t>(r), 16u * j + 8u)) =
+                make_uint4(x2.x, x2.y, x3.x, x3.y);
+        }
+    };
 
     const bool ok = tc::mma_mainloop<false>(
         Abuf, Bbuf, kBChunk, img + (long long)R0 * 128 + 2ll * b_first * img_rows * 128, (long long)img_rows * 128,
-        static_cast<uint32_t>(nrows) * 128u,
-        nblk, tmem, idesc, bars, [&](int b, uint8_t* A) {
-            uint4 nxt[4];
+        static_cast<uint32_t>(nrows) * 128u, nblk, tmem, idesc, bars, [&](int b, uint8_t* A) {
             const bool more = b + 1 < nblk;
-            if (more) {
+            const uint4* next = reinterpret_cast<const uint4*>(wrow + (b + 1) * 128);
+            if ((b & 1) == 0) {
+                if (more) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) nxt[j] = __ldg(reinterpret_cast<const uint4*>(wrow + (b + 1) * 128) + j);
-            }
-            uint8_t* dst = A + h * 16384;
+                    for (int j = 0; j < 4; ++j) wb[j] = __ldg(next + j);
+                }
+                convert(wa, A);
+            } else {
+                if (more) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint2 x0 = i8x4_to_16<BF16>(cur[j].x), x1 = i8x4_to_16<BF16>(cur[j].y);
-                const uint2 x2 = i8x4_to_16<BF16>(cur[j].z), x3 = i8x4_to_16<BF16>(cur[j].w);
-                *reinterpret_cast<uint4*>(dst + tc::kmajor_off(static_cast<uint32_t>(r), 16u * j)) =
-                    make_uint4(x0.x, x0.y, x1.x, x1.y);
-                *reinterpret_cast<uint4*>(dst + tc::kmajor_off(static_cast<uint32_t>(r), 16u * j + 8u)) =
-                    make_uint4(x2.x, x2.y, x3.x, x3.y);
-            }
-            if (more) {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) cur[j] = nxt[j];
+                    for (int j = 0; j < 4; ++j) wa[j] = __ldg(next + j);
+                }
+                convert(wb, A);
             }
         });
 

@@ -78,9 +78,13 @@ __global__ void __launch_bounds__(kThreads, 2) trellis_gemv_kernel(const GemvArg
 
     LaneCodes<K> cur;
     if (kt0 + warp < kt1) load_lane_codes<K>(cur, a.codes + ((long long)(kt0 + warp) * NT + ob * 8) * (16 * K), lane);
+    pdl_wait();  // x may be the previous launch's output
     gemv_input_transform<NB, XM>(a, row0, ntok, kt0 * 16, nk, xt, warp, lane);
     __syncthreads();
     cta_gemv_partial<K, NB, kWarps>(a.codes, NT, ob, kt0, kt1, xt, nk, cur, red, zp);
+    // The next launch on the stream may start now; it prefetches its own codes
+    // and waits for this grid before it reads activations or writes outputs.
+    pdl_trigger();
 
     cluster.sync();
     if (crank == 0 && warp < ntok) {
@@ -111,13 +115,15 @@ cudaError_t launch_t(const GemvArgs& a, int csize, int items, cudaStream_t s) {
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = csize;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 

@@ -240,7 +240,8 @@ int escha_moe_route(const escha_moe_layer* L, const uint16_t* x, int T, uint16_t
  * partial sums) comes from the workspace: ws_bytes >= int8_w8a16_workspace(N,
  * Kin, M), else ESCHA_E_WORKSPACE.
  *   W      int8 [N][Kin];  scales f32 [N]
- *   N      >= 1;  Kin multiple of 16
+ *   N      >= 1;  Kin multiple of 16, <= 51200 (<= 51168 on the matvec path
+ *          with M >= 2)
  *   x      [M][Kin], x_dtype ESCHA_BF16, ESCHA_F16 or ESCHA_F32
  *   y      f32 [M][N] output */
 size_t int8_w8a16_workspace(int N, int Kin, int M);

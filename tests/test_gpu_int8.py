@@ -116,3 +116,21 @@ def test_gemm_route_lm_head_prefill_sampled(native):
     got = y[torch.as_tensor(toks, device=y.device)][:, torch.as_tensor(rows, device=y.device)].cpu().numpy()
     ref = o.int8_matvec(W[rows], s[rows], _bf16_values(xb[toks]))
     assert rel_err_rows(got, ref).max() <= TOL
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("N,Kin", [(777, 528), (130, 8192), (64, 12288), (1000, 1536), (33, 16)])
+def test_matvec_m1_chunk_layouts(native, dtype, N, Kin):
+    """Batch 1: row groups x 512-column chunks per CTA (1, 2, 3->4 chunks per
+    warp), ragged last chunk, rows not a multiple of the tile."""
+    W, s = gen.int8_matrix(N + 3 * Kin, N, Kin)
+    g = gen.rng(Kin)
+    if dtype == "bf16":
+        xb = gen.bf16_normal_bits(g, (1, Kin))
+        x, xv = _bf16_tensor(xb), _bf16_values(xb)
+    else:
+        x16 = gen.fp16_normal(g, (1, Kin))
+        xv = x16.astype(np.float64)
+        x = dev(x16) if dtype == "f16" else dev(x16.astype(np.float32))
+    y = native.int8_w8a16_matvec(dev(W), dev(s), x).cpu().numpy()
+    assert rel_err_rows(y, o.int8_matvec(W, s, xv)).max() <= TOL
