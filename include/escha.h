@@ -181,8 +181,10 @@ int escha_moe_block_timed(const escha_moe_layer* L, const uint16_t* x, int T, fl
  * device buffer of ESCHA_NOALLOC_SCRATCH_BYTES built into the library, which
  * every GPU that loads the library holds until the process exits.
  *   - Calls whose escha_moe_block_workspace(L, T) exceeds the buffer are
- *     rejected with ESCHA_E_WORKSPACE before anything is enqueued (about
- *     T <= 8 tokens for a hidden-2048, inter-512, 256-expert, top-8 layer).
+ *     rejected with ESCHA_E_WORKSPACE before anything is enqueued: for a
+ *     hidden-2048, inter-512, 256-expert, top-8 layer, T <= 4 fits (the
+ *     per-slot path, 183 KB at T = 4); the grouped path of T >= 5 needs
+ *     several MB (its B image) and is rejected.
  *   - The first call on a device looks the buffer's device address up
  *     (cudaGetSymbolAddress); make that first call before any stream capture.
  *   - All calls on a device share the one buffer, which keeps the last call's
