@@ -268,14 +268,14 @@ escha::MoeArgs moe_args(const escha_moe_layer* L, const uint16_t* x, int T, floa
     {
         const escha::GroupPlan gp = escha::group_plan(T, L->topk, L->n_experts, L->hidden, L->inter, L->sh_inter);
         const int E = L->n_experts, S = T * L->topk;
-        int* g = reinterpret_cast<int*>(base + m.grp);
         a.grp_cap = gp.cap;
         a.grp_max_items = gp.max_items;
+        a.grp_items = reinterpret_cast<int4*>(base + m.grp);  // 256-byte aligned region
+        int* g = reinterpret_cast<int*>(a.grp_items + gp.max_items);
         a.grp_counts = g;
         a.grp_offsets = a.grp_counts + E;
         a.grp_poff = a.grp_offsets + E + 1;
-        a.grp_items = a.grp_poff + E;
-        a.grp_nitems = a.grp_items + gp.max_items;
+        a.grp_nitems = a.grp_poff + E;
         a.grp_perm = a.grp_nitems + 1;
         a.grp_ppos = a.grp_perm + S;
         a.grp_img = reinterpret_cast<uint8_t*>(base + m.img);

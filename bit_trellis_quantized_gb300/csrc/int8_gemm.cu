@@ -13,9 +13,9 @@
 //
 // Kernels: a prep kernel writes the activations as the MMA's B image (K-major,
 // 128-byte swizzled, every 64-value chunk holding all rows), then one CTA per
-// (128 outputs, 256 image rows) runs the shared tensor-core main loop: the
-// 256 threads convert the next int8 block while the MMAs of the current one
-// run; B blocks arrive by bulk copy.
+// (128 outputs, 256 image rows) runs the warp-specialised tensor-core loop:
+// 8 warps convert int8 chunks into 4 shared-memory stages, a ninth issues the
+// B bulk copies three chunks ahead and the MMAs.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -102,16 +102,16 @@ __device__ __forceinline__ uint2 i8x4_to_16(uint32_t w) {
 }
 
 template <bool BF16, int PARTS>
-__global__ void __launch_bounds__(tc::kMlThreads, 1)
+__global__ void __launch_bounds__(tc::kMlThreads + 32, 1)
     int8_gemm_kernel(const int8_t* __restrict__ W, const float* __restrict__ scales, int N, int Kin,
                      const uint8_t* __restrict__ img, int img_rows, int M, float* __restrict__ y, long long y_stride,
                      int bps) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    constexpr uint32_t kBChunk = kRowsPerCta * 128;
-    uint8_t* Abuf = smem;                         // [2][32 KB]: two 64-value K-major chunks of 128 rows
-    uint8_t* Bbuf = smem + 2 * tc::kABlockBytes;  // [2][2 chunks][256 rows x 128 B]
-    __shared__ tc::MmaBars bars;
+    constexpr uint32_t kBStage = kRowsPerCta * 128;
+    uint8_t* Abuf = smem;                                     // [4][16 KB]: 128 rows x 64 values, K-major
+    uint8_t* Bbuf = smem + tc::kWsStages * tc::kWsAStageBytes;  // [4][256 rows x 128 B]
+    __shared__ tc::WsBars bars;
     __shared__ uint32_t tmem_base;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n0 = blockIdx.x * 128;
@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(tc::kMlThreads, 1)
     pdl_trigger();
     const int nrows = min(kRowsPerCta, img_rows - R0);  // a multiple of 8
     const int npad = (nrows + 15) & ~15;
-    if (tid == 0) tc::mma_bars_init(bars);
+    if (tid == 0) tc::ws_bars_init(bars);
     if (warp == 0) {
         tc::tmem_alloc(&tmem_base, 256);
         tc::tmem_relinquish();
@@ -132,51 +132,54 @@ __global__ void __launch_bounds__(tc::kMlThreads, 1)
     const uint32_t tmem = tmem_base;
     const uint32_t idesc = tc::idesc_f16(128, npad, false, false, BF16);
 
-    // K split z (blockIdx.z) covers blocks [z * bps, z * bps + nblk); with more
-    // than one split, y points at split z's partial sums ([M][N] each)
+    // K split z (blockIdx.z) covers blocks [z * bps, z * bps + nblk) of 128
+    // values = chunks of 64 from 2 * z * bps; with more than one split, y
+    // points at split z's partial sums ([M][N] each)
     const int b_first = blockIdx.z * bps;
     const int nblk = min(Kin / 128 - b_first, bps);
     if (gridDim.z > 1) {
         y += (long long)blockIdx.z * M * N;
         y_stride = N;
     }
-    // thread t converts row t/2, values 64*(t%2) .. +63 of every 128-value block
-    const int r = tid >> 1, h = tid & 1;
-    const int8_t* wrow = W + (long long)min(n0 + r, N - 1) * Kin + 64 * h + b_first * 128;
-    // two register sets for the int8 rows, used in turn: the next block loads
-    // into one while the other is converted (never copied: a copy would wait
-    // for the load)
-    uint4 wa[4], wb[4];
+    // producer thread t converts row t/2, values 32*(t%2) .. +31 of every
+    // 64-value chunk; the next chunk's int8 loads into one of two register
+    // sets used in turn (a copy would wait for the load)
+    const int r = (tid & 255) >> 1, h = tid & 1;
+    const int8_t* wrow = W + (long long)min(n0 + r, N - 1) * Kin + 32 * h + b_first * 128;
+    const int nch = 2 * nblk;
+    uint4 wa[2], wb[2];
+    if (tid < tc::kMlThreads) {
+        wa[0] = __ldg(reinterpret_cast<const uint4*>(wrow));
+        wa[1] = __ldg(reinterpret_cast<const uint4*>(wrow) + 1);
+    }
+    auto convert = [&](const uint4 (&w)[2], uint8_t* A) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) wa[j] = __ldg(reinterpret_cast<const uint4*>(wrow) + j);
-    auto convert = [&](const uint4 (&w)[4], uint8_t* A) {
-        uint8_t* dst = A + h * 16384;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 2; ++j) {
             const uint2 x0 = i8x4_to_16<BF16>(w[j].x), x1 = i8x4_to_16<BF16>(w[j].y);
             const uint2 x2 = i8x4_to_16<BF16>(w[j].z), x3 = i8x4_to_16<BF16>(w[j].w);
-            *reinterpret_cast<uint4*>(dst + tc::kmajor_off(static_cast<uint32_t>(r), 16u * j)) =
+            const uint32_t k = 32u * h + 16u * j;
+            *reinterpret_cast<uint4*>(A + tc::kmajor_off(static_cast<uint32_t>(r), k)) =
                 make_uint4(x0.x, x0.y, x1.x, x1.y);
-            *reinterpret_cast<uint4*>(dst + tc::kmajor_off(static_cast<uint32_t>(r), 16u * j + 8u)) =
+            *reinterpret_cast<uint4*>(A + tc::kmajor_off(static_cast<uint32_t>(r), k + 8u)) =
                 make_uint4(x2.x, x2.y, x3.x, x3.y);
         }
     };
 
-    const bool ok = tc::mma_mainloop<false>(
-        Abuf, Bbuf, kBChunk, img + (long long)R0 * 128 + 2ll * b_first * img_rows * 128, (long long)img_rows * 128,
-        static_cast<uint32_t>(nrows) * 128u, nblk, tmem, idesc, bars, [&](int b, uint8_t* A) {
-            const bool more = b + 1 < nblk;
-            const uint4* next = reinterpret_cast<const uint4*>(wrow + (b + 1) * 128);
-            if ((b & 1) == 0) {
+    const bool ok = tc::mma_mainloop_ws4(
+        Abuf, Bbuf, kBStage, img + (long long)R0 * 128 + 2ll * b_first * img_rows * 128, (long long)img_rows * 128,
+        static_cast<uint32_t>(nrows) * 128u, nch, tmem, idesc, bars, [&](int c, uint8_t* A) {
+            const bool more = c + 1 < nch;
+            const uint4* next = reinterpret_cast<const uint4*>(wrow + (c + 1) * 64);
+            if ((c & 1) == 0) {
                 if (more) {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) wb[j] = __ldg(next + j);
+                    wb[0] = __ldg(next);
+                    wb[1] = __ldg(next + 1);
                 }
                 convert(wa, A);
             } else {
                 if (more) {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) wa[j] = __ldg(next + j);
+                    wa[0] = __ldg(next);
+                    wa[1] = __ldg(next + 1);
                 }
                 convert(wb, A);
             }
@@ -185,7 +188,7 @@ __global__ void __launch_bounds__(tc::kMlThreads, 1)
     // epilogue: TMEM lane = output row, column = image row; warps w and w + 4
     // share lane quarter w % 4 and split the columns. A bounded wait that gave
     // up leaves NaN in the CTA's outputs.
-    {
+    if (warp < 8) {
         const int q = warp & 3;
         const int n = n0 + 32 * q + lane;
         const float sc = !ok ? __int_as_float(0x7fc00000) : (n < N ? scales[n] : 0.f);
@@ -245,7 +248,7 @@ __global__ void __launch_bounds__(256) int8_split_reduce_kernel(const float* __r
 template <bool BF16, int PARTS>
 cudaError_t launch_gemm(const int8_t* W, const float* scales, int N, int Kin, const uint8_t* img, int img_rows, int M,
                         float* y, long long y_stride, float* part, cudaStream_t s) {
-    const int smem = 2 * tc::kABlockBytes + 2 * 2 * kRowsPerCta * 128 + 1024;
+    const int smem = tc::kWsStages * (tc::kWsAStageBytes + kRowsPerCta * 128) + 1024;
     const void* f = reinterpret_cast<const void*>(int8_gemm_kernel<BF16, PARTS>);
     cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -254,8 +257,8 @@ cudaError_t launch_gemm(const int8_t* W, const float* scales, int N, int Kin, co
     const int ks = (nblk + bps - 1) / bps;  // every split starts inside K
     float* out = ks > 1 ? part : y;
     void* args[] = {&W, &scales, &N, &Kin, &img, &img_rows, &M, &out, &y_stride, &bps};
-    e = launch_kernel(f, dim3((N + 127) / 128, (img_rows + kRowsPerCta - 1) / kRowsPerCta, ks), dim3(tc::kMlThreads),
-                      smem, true, s, args);
+    e = launch_kernel(f, dim3((N + 127) / 128, (img_rows + kRowsPerCta - 1) / kRowsPerCta, ks),
+                      dim3(tc::kMlThreads + 32), smem, true, s, args);
     if (e != cudaSuccess || ks == 1) return e;
     int ks_ = ks;
     void* rargs[] = {&part, &ks_, &M, &N, &y, &y_stride};

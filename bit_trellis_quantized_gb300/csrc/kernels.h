@@ -96,7 +96,7 @@ struct MoeArgs {
     int* grp_counts;    // [E]
     int* grp_offsets;   // [E+1]
     int* grp_poff;      // [E]: first padded position of each expert (runs padded to 4 tokens)
-    int* grp_items;     // [grp_max_items]: (expert << 16) | first position in its run
+    int4* grp_items;    // [grp_max_items]: {expert, tokens, first B-image row, first index into perm}
     int* grp_nitems;    // [1]
     int* grp_perm;      // [T*topk]: slots t*topk + j sorted stably by expert
     int* grp_ppos;      // [T*topk]: padded position of each slot
@@ -112,7 +112,7 @@ constexpr int kSlotModeMaxT = 4;
 // Scratch of the grouped path for T tokens.
 struct GroupPlan {
     int cap, max_items, pos_cap;
-    size_t int_bytes;  // counts, offsets, poff, items, nitems, perm, ppos
+    size_t int_bytes;  // items (16 B each, first), counts, offsets, poff, nitems, perm, ppos
     size_t img_bytes;  // B image (shared by both projections and the shared expert)
 };
 GroupPlan group_plan(int T, int topk, int E, int hidden, int inter, int sh_inter);

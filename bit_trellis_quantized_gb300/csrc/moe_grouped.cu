@@ -158,7 +158,9 @@ __global__ void __launch_bounds__(1024, 1) moe_group_kernel(const MoeArgs a) {
     if (tid < E) {
         a.grp_offsets[tid] = off_s[tid];
         a.grp_poff[tid] = poff_s[tid];
-        for (int j = 0; j < ni; ++j) a.grp_items[ibase_s[tid] + j] = (tid << 16) | (j * cap);
+        for (int j = 0; j < ni; ++j)
+            a.grp_items[ibase_s[tid] + j] =
+                make_int4(tid, min(cap, cnt - j * cap), 2 * (poff_s[tid] + j * cap), off_s[tid] + j * cap);
     }
     if (tid == 0) {
         a.grp_offsets[E] = off_s[256];
@@ -320,13 +322,17 @@ __global__ void __launch_bounds__(GROUPS * tc::kMlThreads, 3 - GROUPS)
 
     pdl_wait();  // the B image (and the grouping) are complete
     pdl_trigger();
-    if (item >= *a.grp_nitems) return;
-    const int packed = a.grp_items[item];
-    const int e = packed >> 16, g0 = packed & 0xFFFF;
-    const int nt = min(cap, a.grp_counts[e] - g0);
+    // the item's descriptor is loaded together with the item count (entries
+    // past the count are never used), so one round trip gives everything the
+    // CTA needs to start its other loads
+    const int nitems = *a.grp_nitems;
+    const int4 desc = a.grp_items[item];
+    if (item >= nitems) return;
+    const int e = desc.x, nt = desc.y;
+    const uint2 rb = *reinterpret_cast<const uint2*>(p.rout + (long long)e * p.out + ob * 128 + 4 * lane);
     const int npad = (2 * nt + 15) & ~15;  // MMA N: hi/lo rows of nt tokens, multiple of 16
     const int nt4 = (nt + 3) & ~3;          // rows copied: whole 8-row atoms
-    for (int i = tid; i < nt; i += kThreads) slot_s[i] = a.grp_perm[a.grp_offsets[e] + g0 + i];
+    for (int i = tid; i < nt; i += kThreads) slot_s[i] = a.grp_perm[desc.w + i];
     const uint32_t acc_cols = 2u * static_cast<uint32_t>(cap) < 32u ? 32u : 2u * static_cast<uint32_t>(cap);
     const uint32_t tcols = GROUPS * acc_cols;  // one accumulator per producer group
     if (tid == 0) tc::mma_bars_init(bars);
@@ -351,7 +357,7 @@ __global__ void __launch_bounds__(GROUPS * tc::kMlThreads, 3 - GROUPS)
     const int first = GROUPS == 2 ? (warp >> 3) : 0;
     if (first < nblk) load_lane_codes<K>(c0, codes + ((long long)(8 * first + gw) * NT + ob * 8) * (16 * K), lane);
     const int nbr = (lane & ~3) | ((lane + 1) & 3);
-    const uint8_t* img = a.grp_img + (long long)2 * (a.grp_poff[e] + g0) * 128;
+    const uint8_t* img = a.grp_img + (long long)desc.z * 128;
     int parity = 0;
     // warp gw decodes tile row 8b + gw of output block ob and loads its row of
     // block b_next
@@ -406,8 +412,6 @@ __global__ void __launch_bounds__(GROUPS * tc::kMlThreads, 3 - GROUPS)
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, tcols);
     if (!ok) return;
-    const uint16_t* rout = p.rout + (long long)e * p.out + ob * 128;
-    const uint2 rb = *reinterpret_cast<const uint2*>(rout + 4 * lane);
     for (int i = warp; i < nt; i += kWarps) {
         const float4 z4 = *reinterpret_cast<const float4*>(zs + i * 128 + 4 * lane);
         float v[4] = {z4.x * 256.f, z4.y * 256.f, z4.z * 256.f, z4.w * 256.f};  // undo the 2^-8 prescale (exact)
@@ -512,8 +516,8 @@ GroupPlan group_plan(int T, int topk, int E, int hidden, int inter, int sh_inter
     while (g.cap < kGrpCapMax && g.cap < want) g.cap *= 2;
     g.max_items = static_cast<int>(S / g.cap) + E;  // full items plus at most one partial per expert
     g.pos_cap = static_cast<int>((S + 3 * E + 3) & ~3ll);
-    // counts[E], offsets[E+1], poff[E], items[max_items], nitems, perm[S], ppos[S]
-    g.int_bytes = (size_t)(E + (E + 1) + E + g.max_items + 1 + 2 * S) * 4;
+    // items[max_items] (16 B each), counts[E], offsets[E+1], poff[E], nitems, perm[S], ppos[S]
+    g.int_bytes = (size_t)g.max_items * 16 + (size_t)(E + (E + 1) + E + 1 + 2 * S) * 4;
     const size_t trellis_img = (size_t)(hidden > inter ? hidden : inter) * 2 * g.pos_cap * 2;
     size_t shared_img = 0;
     if (sh_inter > 0) {
