@@ -142,15 +142,24 @@ __global__ void __launch_bounds__(tc::kMlThreads + 32, 1)
         y_stride = N;
     }
     // producer thread t converts row t/2, values 32*(t%2) .. +31 of every
-    // 64-value chunk; the next chunk's int8 loads into one of two register
-    // sets used in turn (a copy would wait for the load)
+    // 64-value chunk. Three register sets rotate: chunk c + 2 loads into one
+    // while chunk c is converted from another, so a load has two chunks of
+    // MMA time to arrive, and no set is ever copied (a copy would wait for
+    // the load).
     const int r = (tid & 255) >> 1, h = tid & 1;
     const int8_t* wrow = W + (long long)min(n0 + r, N - 1) * Kin + 32 * h + b_first * 128;
     const int nch = 2 * nblk;
-    uint4 wa[2], wb[2];
+    uint4 w0[2], w1[2], w2[2];
+    auto load = [&](uint4 (&w)[2], int c) {
+        if (c < nch) {
+            const uint4* src = reinterpret_cast<const uint4*>(wrow + c * 64);
+            w[0] = __ldg(src);
+            w[1] = __ldg(src + 1);
+        }
+    };
     if (tid < tc::kMlThreads) {
-        wa[0] = __ldg(reinterpret_cast<const uint4*>(wrow));
-        wa[1] = __ldg(reinterpret_cast<const uint4*>(wrow) + 1);
+        load(w0, 0);
+        load(w1, 1);
     }
     auto convert = [&](const uint4 (&w)[2], uint8_t* A) {
 #pragma unroll
@@ -165,24 +174,21 @@ __global__ void __launch_bounds__(tc::kMlThreads + 32, 1)
         }
     };
 
+    int rot = 0;  // c % 3
     const bool ok = tc::mma_mainloop_ws4(
         Abuf, Bbuf, kBStage, img + (long long)R0 * 128 + 2ll * b_first * img_rows * 128, (long long)img_rows * 128,
         static_cast<uint32_t>(nrows) * 128u, nch, tmem, idesc, bars, [&](int c, uint8_t* A) {
-            const bool more = c + 1 < nch;
-            const uint4* next = reinterpret_cast<const uint4*>(wrow + (c + 1) * 64);
-            if ((c & 1) == 0) {
-                if (more) {
-                    wb[0] = __ldg(next);
-                    wb[1] = __ldg(next + 1);
-                }
-                convert(wa, A);
+            if (rot == 0) {
+                load(w2, c + 2);
+                convert(w0, A);
+            } else if (rot == 1) {
+                load(w0, c + 2);
+                convert(w1, A);
             } else {
-                if (more) {
-                    wa[0] = __ldg(next);
-                    wa[1] = __ldg(next + 1);
-                }
-                convert(wb, A);
+                load(w1, c + 2);
+                convert(w2, A);
             }
+            rot = rot == 2 ? 0 : rot + 1;
         });
 
     // epilogue: TMEM lane = output row, column = image row; warps w and w + 4

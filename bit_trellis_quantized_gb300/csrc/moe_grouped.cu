@@ -271,14 +271,41 @@ __global__ void __launch_bounds__(256) moe_prep_kernel(const MoeArgs a, const Gr
 // ---------------------------------------------------------------------------
 // 4. grouped GEMM
 // ---------------------------------------------------------------------------
-// The lane's 64 decoded weights of one tile row (tile lane/4, input rows
-// 4c..4c+3, 16 output columns each) written into the MN-major A slice of that
-// row: element (m = 16*(lane/4) + q, k = r) at mnmajor_off(m, k, 2048, 1024).
+// Half tile rows. A warp decodes 4 of the 8 tiles of one tile row of the
+// output block (16 inputs x 64 outputs): lane = 8 * tile + c, c = 0..7, owns
+// input rows 2c and 2c+1 of its tile, i.e. bits [32 K c, 32 K (c+1)) of the
+// tile's stream = K 32-bit words, plus the first 16-bit word of the next lane
+// of the tile (tail-biting: lane 0 after lane 7) for the windows that cross
+// the end.
 template <int K>
-__device__ __forceinline__ void decode_row_to_smem(const LaneCodes<K>& lc, uint8_t* slice, int lane) {
-    const int tile = lane >> 2, c = lane & 3;
-    const uint32_t m0 = 16u * tile;
-    static_for<8>([&](auto J) {  // half-row j: input row 4c + j/2, columns 8*(j%2)..+7
+struct HalfRowCodes {
+    uint32_t p[K + 1];
+};
+
+// base4: the first 16-bit word of the warp's 4 tiles (K * 16 words each).
+template <int K>
+__device__ __forceinline__ void load_half_row(HalfRowCodes<K>& lc, const uint16_t* base4, int lane) {
+    const uint16_t* b = base4 + (lane >> 3) * (16 * K) + (lane & 7) * (2 * K);
+    if constexpr (K == 2) {
+        const uint2 v = ldg_stream_v2(b);  // 8-byte aligned: 64 B per tile, 8 B per lane
+        lc.p[0] = v.x;
+        lc.p[1] = v.y;
+    } else {
+        lc.p[0] = ldg_stream_u32(b);  // 4-byte aligned: 96 B per tile, 12 B per lane
+        lc.p[1] = ldg_stream_u32(b + 2);
+        lc.p[2] = ldg_stream_u32(b + 4);
+    }
+}
+
+// The lane's 32 weights (input rows 2c, 2c+1; 16 output columns of tile
+// tile0 + lane/8) into the MN-major A slice of the tile row: element (m, k) at
+// mnmajor_off(m, k, 2048, 1024). Needs lc.p[K] = the next lane's first word.
+template <int K>
+__device__ __forceinline__ void decode_half_row_to_smem(const HalfRowCodes<K>& lc, uint8_t* slice, int lane,
+                                                        int tile0) {
+    const int c = lane & 7;
+    const uint32_t m0 = 16u * static_cast<uint32_t>(tile0 + (lane >> 3));
+    static_for<4>([&](auto J) {  // quarter j: input row 2c + j/2, columns 8*(j%2)..+7
         constexpr int j = decltype(J)::value;
         uint32_t packed[4];
         static_for<4>([&](auto P) {
@@ -290,29 +317,30 @@ __device__ __forceinline__ void decode_row_to_smem(const LaneCodes<K>& lc, uint8
             const __half2 w2 = cb_decode_h2(s0, s1);
             packed[p] = *reinterpret_cast<const uint32_t*>(&w2);
         });
-        const uint32_t k = 4u * c + (j >> 1);
+        const uint32_t k = 2u * c + (j >> 1);
         const uint32_t m = m0 + 8u * (j & 1);
         *reinterpret_cast<uint4*>(slice + tc::mnmajor_off(m, k, 2048u, 1024u)) =
             make_uint4(packed[0], packed[1], packed[2], packed[3]);
     });
 }
 
-// GROUPS = 2: 512 threads in two producer groups taking alternate blocks
-// (one CTA per SM; for items of 64 or 128 tokens, whose B buffers fill the
-// shared memory anyway). GROUPS = 1: 256 threads, double-buffered A, two CTAs
-// per SM (items of up to 32 tokens), so one CTA's prologue and epilogue
-// overlap the other's decode.
-template <int K, int GROUPS>
-__global__ void __launch_bounds__(GROUPS * tc::kMlThreads, 3 - GROUPS)
-    moe_grouped_gemm_kernel(const MoeArgs a, const GroupedProj p) {
-    constexpr int kThreads = GROUPS * tc::kMlThreads, kWarps = kThreads / 32;
+// One CTA per (work item, 128-wide output block), 256 threads, K blocks of 64
+// inputs: per block warp w decodes half tile row w%2 of tile row 4b + w/2
+// into the double-buffered A (16 KB), while the MMAs of the previous block
+// run; the item's B rows of the block arrive by bulk copy. Shared memory
+// (2 x 16 KB A + 2 x 2 cap x 128 B B) stays under 100 KB for every item
+// size, so two CTAs share an SM and one's prologue and epilogue overlap the
+// other's decode.
+template <int K>
+__global__ void __launch_bounds__(tc::kMlThreads, 2) moe_grouped_gemm_kernel(const MoeArgs a, const GroupedProj p) {
+    constexpr int kThreads = tc::kMlThreads, kWarps = kThreads / 32;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int cap = a.grp_cap;
     const uint32_t b_chunk = 256u * static_cast<uint32_t>(cap);  // 2*cap rows x 128 B
-    uint8_t* Abuf = smem;                                         // [2][32 KB]
-    uint8_t* Bbuf = smem + 2 * tc::kABlockBytes;                  // [2][2 chunks][b_chunk]
-    float* zs = reinterpret_cast<float*>(smem);                   // epilogue: [cap][128] f32 over the A buffers
+    uint8_t* Abuf = smem;                                         // [2][16 KB]
+    uint8_t* Bbuf = smem + 2 * 16384;                             // [2][b_chunk]
+    float* zs = reinterpret_cast<float*>(smem);                   // epilogue: [cap][128] f32 over A and B
     __shared__ tc::MmaBars bars;
     __shared__ uint32_t tmem_base;
     __shared__ int slot_s[kGrpCapMax];
@@ -333,8 +361,7 @@ __global__ void __launch_bounds__(GROUPS * tc::kMlThreads, 3 - GROUPS)
     const int npad = (2 * nt + 15) & ~15;  // MMA N: hi/lo rows of nt tokens, multiple of 16
     const int nt4 = (nt + 3) & ~3;          // rows copied: whole 8-row atoms
     for (int i = tid; i < nt; i += kThreads) slot_s[i] = a.grp_perm[desc.w + i];
-    const uint32_t acc_cols = 2u * static_cast<uint32_t>(cap) < 32u ? 32u : 2u * static_cast<uint32_t>(cap);
-    const uint32_t tcols = GROUPS * acc_cols;  // one accumulator per producer group
+    const uint32_t tcols = 2u * static_cast<uint32_t>(cap) < 32u ? 32u : 2u * static_cast<uint32_t>(cap);
     if (tid == 0) tc::mma_bars_init(bars);
     if (warp == 0) {
         tc::tmem_alloc(&tmem_base, tcols);
@@ -348,63 +375,46 @@ __global__ void __launch_bounds__(GROUPS * tc::kMlThreads, 3 - GROUPS)
 
     const int KT = p.in >> 4, NT = p.out >> 4;
     const uint16_t* codes = p.codes + (long long)e * KT * NT * (16 * K);
-    const int nblk = p.in >> 7;
-    const int gw = warp & 7;  // tile row of the block inside the warp's group
-    // two register sets of lane codes used in turn: the set for the next block
-    // is loaded while the other is decoded, and never copied (a copy would
-    // wait for the load)
-    LaneCodes<K> c0, c1;
-    const int first = GROUPS == 2 ? (warp >> 3) : 0;
-    if (first < nblk) load_lane_codes<K>(c0, codes + ((long long)(8 * first + gw) * NT + ob * 8) * (16 * K), lane);
-    const int nbr = (lane & ~3) | ((lane + 1) & 3);
+    const int nblk = p.in >> 6;  // blocks of 64 inputs = 4 tile rows
+    const int hr = warp >> 1, half = warp & 1;
+    // the warp's 4 tiles of tile row 4b + hr
+    auto row4 = [&](int b) { return codes + ((long long)(4 * b + hr) * NT + ob * 8 + 4 * half) * (16 * K); };
+    // two register sets used in turn: the next block's codes load into one
+    // while the other is decoded (never copied: a copy would wait for the load)
+    HalfRowCodes<K> c0, c1;
+    load_half_row<K>(c0, row4(0), lane);
+    const int nbr = (lane & ~7) | ((lane + 1) & 7);
     const uint8_t* img = a.grp_img + (long long)desc.z * 128;
-    int parity = 0;
-    // warp gw decodes tile row 8b + gw of output block ob and loads its row of
-    // block b_next
-    auto produce = [&](int b, int b_next, uint8_t* A) {
-        (void)b;
-        const bool more = b_next < nblk;
-        const uint16_t* nrow = codes + ((long long)(8 * b_next + gw) * NT + ob * 8) * (16 * K);
-        if (parity == 0) {
-            if (more) load_lane_codes<K>(c1, nrow, lane);
-            c0.p[2 * K] = __shfl_sync(0xffffffffu, c0.p[0], nbr) & 0xFFFFu;
-            decode_row_to_smem<K>(c0, A + gw * 4096, lane);
-        } else {
-            if (more) load_lane_codes<K>(c0, nrow, lane);
-            c1.p[2 * K] = __shfl_sync(0xffffffffu, c1.p[0], nbr) & 0xFFFFu;
-            decode_row_to_smem<K>(c1, A + gw * 4096, lane);
-        }
-        parity ^= 1;
-    };
-    const long long img_chunk = (long long)a.grp_img_rows * 128;
-    const uint32_t copy_bytes = 256u * static_cast<uint32_t>(nt4);
-    bool ok;
-    if constexpr (GROUPS == 2)
-        ok = tc::mma_mainloop_2grp<true>(Abuf, Bbuf, b_chunk, img, img_chunk, copy_bytes, nblk, tmem, acc_cols, idesc,
-                                         bars, produce);
-    else
-        ok = tc::mma_mainloop<true>(Abuf, Bbuf, b_chunk, img, img_chunk, copy_bytes, nblk, tmem, idesc, bars,
-                                    [&](int b, uint8_t* A) { produce(b, b + 1, A); });
+
+    const bool ok = tc::mma_mainloop<true, 4>(
+        Abuf, Bbuf, b_chunk, img, (long long)a.grp_img_rows * 128, 256u * static_cast<uint32_t>(nt4), nblk, tmem,
+        idesc, bars, [&](int b, uint8_t* A) {
+            const bool more = b + 1 < nblk;
+            uint8_t* slice = A + hr * 4096;
+            if ((b & 1) == 0) {
+                if (more) load_half_row<K>(c1, row4(b + 1), lane);
+                c0.p[K] = __shfl_sync(0xffffffffu, c0.p[0], nbr) & 0xFFFFu;
+                decode_half_row_to_smem<K>(c0, slice, lane, 4 * half);
+            } else {
+                if (more) load_half_row<K>(c0, row4(b + 1), lane);
+                c1.p[K] = __shfl_sync(0xffffffffu, c1.p[0], nbr) & 0xFFFFu;
+                decode_half_row_to_smem<K>(c1, slice, lane, 4 * half);
+            }
+        });
     if (!ok && tid == 0) atomicExch(a.err, 3);
 
-    // epilogue: TMEM lane m of accumulator g holds columns 2i (hi) and 2i + 1
-    // (lo) of token i; warps w, w + 4, w + 8, w + 12 share lane quarter w % 4
-    // and split the columns
+    // epilogue: TMEM lane m holds columns 2i (hi) and 2i + 1 (lo) of token i;
+    // warps w and w + 4 share lane quarter w % 4 and split the columns
     if (ok) {
         const int q = warp & 3, m = 32 * q + lane;
-        const bool two = GROUPS == 2 && nblk >= 2;
-        for (int c0 = 16 * (warp >> 2); c0 < npad; c0 += 16 * (kWarps / 4)) {
-            float v0[16], v1[16];
-            const uint32_t ta = tmem + (static_cast<uint32_t>(32 * q) << 16) + c0;
-            tc::tmem_ld16(ta, v0);
-            if (two) tc::tmem_ld16(ta + acc_cols, v1);
+        for (int c0c = 16 * (warp >> 2); c0c < npad; c0c += 32) {
+            float v[16];
+            tc::tmem_ld16(tmem + (static_cast<uint32_t>(32 * q) << 16) + c0c, v);
             tc::tmem_ld_wait();
 #pragma unroll
             for (int qq = 0; qq < 8; ++qq) {
-                const int i = c0 / 2 + qq;
-                float z = v0[2 * qq] + v0[2 * qq + 1];
-                if (two) z += v1[2 * qq] + v1[2 * qq + 1];
-                if (i < nt) zs[i * 128 + m] = z;
+                const int i = c0c / 2 + qq;
+                if (i < nt) zs[i * 128 + m] = v[2 * qq] + v[2 * qq + 1];
             }
         }
     }
@@ -470,14 +480,12 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeArgs a, const
 
 template <int K>
 cudaError_t launch_grouped(const MoeArgs& a, const GroupedProj& p, cudaStream_t s) {
-    const int smem = 2 * tc::kABlockBytes + 2 * 2 * 256 * a.grp_cap + 1024;
-    const int groups = a.grp_cap >= 64 ? 2 : 1;
-    const void* f = groups == 2 ? reinterpret_cast<const void*>(moe_grouped_gemm_kernel<K, 2>)
-                                : reinterpret_cast<const void*>(moe_grouped_gemm_kernel<K, 1>);
+    const int smem = 2 * 16384 + 2 * 256 * a.grp_cap + 1024;
+    const void* f = reinterpret_cast<const void*>(moe_grouped_gemm_kernel<K>);
     cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     void* args[] = {const_cast<MoeArgs*>(&a), const_cast<GroupedProj*>(&p)};
-    return launch_kernel(f, dim3(p.out / 128, a.grp_max_items), dim3(groups * tc::kMlThreads), smem, true, s, args);
+    return launch_kernel(f, dim3(p.out / 128, a.grp_max_items), dim3(tc::kMlThreads), smem, true, s, args);
 }
 
 cudaError_t launch_prep(const MoeArgs& a, const GroupedProj& p, cudaStream_t s) {

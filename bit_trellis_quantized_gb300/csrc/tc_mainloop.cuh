@@ -43,26 +43,35 @@ __device__ __forceinline__ void mma_bars_init(MmaBars& bars) {
 // by every thread. `img` points at the CTA's first row in chunk 0;
 // consecutive chunks are `img_chunk_bytes` apart. Returns false in every
 // thread when a bounded wait gave up.
-template <bool A_MN, class ProduceA>
+//
+// KSTEPS = 8: blocks of 128 values (A 32 KB, B two 64-value chunks);
+// KSTEPS = 4: blocks of 64 values (A 16 KB, B one chunk); A_MN slices are
+// 4 KB per K = 16 step either way.
+template <bool A_MN, int KSTEPS = 8, class ProduceA>
 __device__ __forceinline__ bool mma_mainloop(uint8_t* Abuf, uint8_t* Bbuf, uint32_t b_chunk_bytes, const uint8_t* img,
                                              long long img_chunk_bytes, uint32_t copy_bytes, int nblk, uint32_t tmem,
                                              uint32_t idesc, MmaBars& bars, ProduceA&& produce) {
+    static_assert(KSTEPS == 4 || KSTEPS == 8, "blocks of 64 or 128 values");
+    constexpr int kChunks = KSTEPS / 4;
+    constexpr int kABytes = KSTEPS * 4096;
     const int tid = threadIdx.x;
     bool ok = true;
     auto issue_b = [&](int b) {
         const int buf = b & 1;
         const uint32_t bar = smem_addr(&bars.full[buf]);
-        mbar_arrive_expect_tx(bar, 2u * copy_bytes);
-        uint8_t* dst = Bbuf + buf * 2 * b_chunk_bytes;
-        bulk_g2s(smem_addr(dst), img + (2ll * b) * img_chunk_bytes, copy_bytes, bar);
-        bulk_g2s(smem_addr(dst + b_chunk_bytes), img + (2ll * b + 1) * img_chunk_bytes, copy_bytes, bar);
+        mbar_arrive_expect_tx(bar, kChunks * copy_bytes);
+        uint8_t* dst = Bbuf + buf * kChunks * b_chunk_bytes;
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c)
+            bulk_g2s(smem_addr(dst + c * b_chunk_bytes), img + ((long long)kChunks * b + c) * img_chunk_bytes,
+                     copy_bytes, bar);
     };
     if (tid == 0) issue_b(0);
     for (int b = 0; b < nblk; ++b) {
         const int buf = b & 1;
         // the MMAs of block b-2 have finished with this A buffer
         if (b >= 2 && !mbar_wait_parity_bounded(smem_addr(&bars.done[buf]), ((b >> 1) - 1) & 1)) ok = false;
-        uint8_t* A = Abuf + buf * kABlockBytes;
+        uint8_t* A = Abuf + buf * kABytes;
         produce(b, A);
         fence_proxy_async_smem();
         fence_before_sync();
@@ -70,9 +79,9 @@ __device__ __forceinline__ bool mma_mainloop(uint8_t* Abuf, uint8_t* Bbuf, uint3
         if (tid == 0) {
             fence_after_sync();
             if (!mbar_wait_parity_bounded(smem_addr(&bars.full[buf]), (b >> 1) & 1)) ok = false;
-            const uint8_t* B = Bbuf + buf * 2 * b_chunk_bytes;
+            const uint8_t* B = Bbuf + buf * kChunks * b_chunk_bytes;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
+            for (int kk = 0; kk < KSTEPS; ++kk) {
                 const uint64_t ad =
                     A_MN ? smem_desc(smem_addr(A + kk * 4096), 2048u, 1024u, kSwizzle128B)
                          : smem_desc(smem_addr(A + (kk >> 2) * 16384) + (kk & 3) * 32u, 16u, 1024u, kSwizzle128B);
