@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(tc::kMlThreads + 32, 1)
     };
 
     int rot = 0;  // c % 3
-    const bool ok = tc::mma_mainloop_ws4(
+    const bool ok = tc::mma_mainloop_ws<4, false>(
         Abuf, Bbuf, kBStage, img + (long long)R0 * 128 + 2ll * b_first * img_rows * 128, (long long)img_rows * 128,
         static_cast<uint32_t>(nrows) * 128u, nch, tmem, idesc, bars, [&](int c, uint8_t* A) {
             if (rot == 0) {

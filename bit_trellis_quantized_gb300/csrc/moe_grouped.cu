@@ -324,16 +324,18 @@ __device__ __forceinline__ void decode_half_row_to_smem(const HalfRowCodes<K>& l
     });
 }
 
-// One CTA per (work item, 128-wide output block), 256 threads, K blocks of 64
-// inputs: per block warp w decodes half tile row w%2 of tile row 4b + w/2
-// into the double-buffered A (16 KB), while the MMAs of the previous block
-// run; the item's B rows of the block arrive by bulk copy. Shared memory
-// (2 x 16 KB A + 2 x 2 cap x 128 B B) stays under 100 KB for every item
-// size, so two CTAs share an SM and one's prologue and epilogue overlap the
-// other's decode.
+// One CTA per (work item, 128-wide output block), K blocks of 64 inputs, 8
+// decode warps + 1 issuer warp: per block decode warp w writes half tile row
+// w%2 of tile row 4b + w/2 into one of two A stages (16 KB) and arrives on an
+// mbarrier, without waiting for the other warps; the issuer waits for the
+// stage and the item's bulk-copied B rows, issues the MMAs and copies the
+// next block's B. Shared memory (2 x 16 KB A + 2 x 2 cap x 128 B B) stays
+// under 100 KB for every item size, so two CTAs share an SM and one's
+// prologue and epilogue overlap the other's decode.
 template <int K>
-__global__ void __launch_bounds__(tc::kMlThreads, 2) moe_grouped_gemm_kernel(const MoeArgs a, const GroupedProj p) {
-    constexpr int kThreads = tc::kMlThreads, kWarps = kThreads / 32;
+__global__ void __launch_bounds__(tc::kMlThreads + 32, 2)
+    moe_grouped_gemm_kernel(const MoeArgs a, const GroupedProj p) {
+    constexpr int kThreads = tc::kMlThreads + 32, kDecodeWarps = tc::kMlThreads / 32;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int cap = a.grp_cap;
@@ -341,7 +343,7 @@ __global__ void __launch_bounds__(tc::kMlThreads, 2) moe_grouped_gemm_kernel(con
     uint8_t* Abuf = smem;                                         // [2][16 KB]
     uint8_t* Bbuf = smem + 2 * 16384;                             // [2][b_chunk]
     float* zs = reinterpret_cast<float*>(smem);                   // epilogue: [cap][128] f32 over A and B
-    __shared__ tc::MmaBars bars;
+    __shared__ tc::WsBars bars;
     __shared__ uint32_t tmem_base;
     __shared__ int slot_s[kGrpCapMax];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -362,7 +364,7 @@ __global__ void __launch_bounds__(tc::kMlThreads, 2) moe_grouped_gemm_kernel(con
     const int nt4 = (nt + 3) & ~3;          // rows copied: whole 8-row atoms
     for (int i = tid; i < nt; i += kThreads) slot_s[i] = a.grp_perm[desc.w + i];
     const uint32_t tcols = 2u * static_cast<uint32_t>(cap) < 32u ? 32u : 2u * static_cast<uint32_t>(cap);
-    if (tid == 0) tc::mma_bars_init(bars);
+    if (tid == 0) tc::ws_bars_init(bars);
     if (warp == 0) {
         tc::tmem_alloc(&tmem_base, tcols);
         tc::tmem_relinquish();
@@ -382,11 +384,11 @@ __global__ void __launch_bounds__(tc::kMlThreads, 2) moe_grouped_gemm_kernel(con
     // two register sets used in turn: the next block's codes load into one
     // while the other is decoded (never copied: a copy would wait for the load)
     HalfRowCodes<K> c0, c1;
-    load_half_row<K>(c0, row4(0), lane);
+    if (warp < kDecodeWarps) load_half_row<K>(c0, row4(0), lane);
     const int nbr = (lane & ~7) | ((lane + 1) & 7);
     const uint8_t* img = a.grp_img + (long long)desc.z * 128;
 
-    const bool ok = tc::mma_mainloop<true, 4>(
+    const bool ok = tc::mma_mainloop_ws<2, true>(
         Abuf, Bbuf, b_chunk, img, (long long)a.grp_img_rows * 128, 256u * static_cast<uint32_t>(nt4), nblk, tmem,
         idesc, bars, [&](int b, uint8_t* A) {
             const bool more = b + 1 < nblk;
@@ -405,7 +407,7 @@ __global__ void __launch_bounds__(tc::kMlThreads, 2) moe_grouped_gemm_kernel(con
 
     // epilogue: TMEM lane m holds columns 2i (hi) and 2i + 1 (lo) of token i;
     // warps w and w + 4 share lane quarter w % 4 and split the columns
-    if (ok) {
+    if (ok && warp < kDecodeWarps) {
         const int q = warp & 3, m = 32 * q + lane;
         for (int c0c = 16 * (warp >> 2); c0c < npad; c0c += 32) {
             float v[16];
@@ -422,7 +424,7 @@ __global__ void __launch_bounds__(tc::kMlThreads, 2) moe_grouped_gemm_kernel(con
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, tcols);
     if (!ok) return;
-    for (int i = warp; i < nt; i += kWarps) {
+    for (int i = warp; i < nt; i += kThreads / 32) {
         const float4 z4 = *reinterpret_cast<const float4*>(zs + i * 128 + 4 * lane);
         float v[4] = {z4.x * 256.f, z4.y * 256.f, z4.z * 256.f, z4.w * 256.f};  // undo the 2^-8 prescale (exact)
         output_transform_regs(v, rb, lane);
@@ -485,7 +487,7 @@ cudaError_t launch_grouped(const MoeArgs& a, const GroupedProj& p, cudaStream_t 
     cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     void* args[] = {const_cast<MoeArgs*>(&a), const_cast<GroupedProj*>(&p)};
-    return launch_kernel(f, dim3(p.out / 128, a.grp_max_items), dim3(tc::kMlThreads), smem, true, s, args);
+    return launch_kernel(f, dim3(p.out / 128, a.grp_max_items), dim3(tc::kMlThreads + 32), smem, true, s, args);
 }
 
 cudaError_t launch_prep(const MoeArgs& a, const GroupedProj& p, cudaStream_t s) {

@@ -176,14 +176,17 @@ __device__ __forceinline__ bool mma_mainloop_2grp(uint8_t* Abuf, uint8_t* Bbuf, 
 namespace escha {
 namespace tc {
 
-// Warp-specialised main loop over 64-value K chunks in 4 stages (A 16 KB:
-// 128 rows x 64 values K-major; B: up to 256 rows x 128 B), for kernels of
-// 256 producer threads (warps 0-7) + one issuer warp (warp 8):
-//  * producers: for chunk c, wait until the MMAs of chunk c-4 released stage
-//    c % 4, write A (`produce(c, A_stage)`), fence, arrive on a_full;
-//  * issuer (one thread): B copies run 3 chunks ahead; per chunk wait a_full
-//    and b_full, issue four K = 16 MMAs, commit to done; then wait for the
-//    MMAs of chunk c-1 and copy chunk c+3's B into the stage they released.
+// Warp-specialised main loop over 64-value K chunks in STAGES stages (A:
+// 16 KB per chunk, K-major 128 rows x 64 values or MN-major four 4 KB slices;
+// B: up to 256 rows x 128 B), for kernels of 256 producer threads (warps
+// 0-7) + one issuer warp (warp 8):
+//  * producers: for chunk c, wait until the MMAs of chunk c - STAGES released
+//    stage c % STAGES, write A (`produce(c, A_stage)`), fence, arrive on
+//    a_full;
+//  * issuer (one thread): B copies run STAGES - 1 chunks ahead; per chunk wait
+//    a_full and b_full, issue four K = 16 MMAs, commit to done; then wait for
+//    the MMAs of chunk c - 1 and copy chunk c + STAGES - 1's B into the stage
+//    they released.
 // No CTA-wide barrier inside the loop. Returns false in every thread when a
 // bounded wait gave up.
 constexpr int kWsStages = 4;
@@ -204,51 +207,57 @@ __device__ __forceinline__ void ws_bars_init(WsBars& bars) {
     fence_proxy_async_smem();
 }
 
-template <class ProduceChunk>
-__device__ __forceinline__ bool mma_mainloop_ws4(uint8_t* Abuf, uint8_t* Bbuf, uint32_t b_stage_bytes,
-                                                 const uint8_t* img, long long img_chunk_bytes, uint32_t copy_bytes,
-                                                 int nch, uint32_t tmem, uint32_t idesc, WsBars& bars,
-                                                 ProduceChunk&& produce) {
+template <int STAGES, bool A_MN, class ProduceChunk>
+__device__ __forceinline__ bool mma_mainloop_ws(uint8_t* Abuf, uint8_t* Bbuf, uint32_t b_stage_bytes,
+                                                const uint8_t* img, long long img_chunk_bytes, uint32_t copy_bytes,
+                                                int nch, uint32_t tmem, uint32_t idesc, WsBars& bars,
+                                                ProduceChunk&& produce) {
+    static_assert(STAGES == 2 || STAGES == 4, "2 or 4 stages");
     const int tid = threadIdx.x;
     bool ok = true;
     if (tid < kMlThreads) {
         for (int c = 0; c < nch; ++c) {
-            const int s = c & 3;
-            if (c >= kWsStages && !mbar_wait_parity_bounded(smem_addr(&bars.done[s]), ((c >> 2) - 1) & 1)) ok = false;
+            const int s = c % STAGES;
+            if (c >= STAGES && !mbar_wait_parity_bounded(smem_addr(&bars.done[s]), ((c / STAGES) - 1) & 1))
+                ok = false;
             produce(c, Abuf + s * kWsAStageBytes);
             fence_proxy_async_smem();
             mbar_arrive_cta(smem_addr(&bars.a_full[s]));
         }
     } else if (tid == kMlThreads) {
         auto issue_b = [&](int c) {
-            const uint32_t bar = smem_addr(&bars.b_full[c & 3]);
+            const uint32_t bar = smem_addr(&bars.b_full[c % STAGES]);
             mbar_arrive_expect_tx(bar, copy_bytes);
-            bulk_g2s(smem_addr(Bbuf + (c & 3) * b_stage_bytes), img + (long long)c * img_chunk_bytes, copy_bytes, bar);
+            bulk_g2s(smem_addr(Bbuf + (c % STAGES) * b_stage_bytes), img + (long long)c * img_chunk_bytes, copy_bytes,
+                     bar);
         };
-        for (int c = 0; c < nch && c < kWsStages - 1; ++c) issue_b(c);
+        for (int c = 0; c < nch && c < STAGES - 1; ++c) issue_b(c);
         for (int c = 0; c < nch; ++c) {
-            const int s = c & 3;
-            const uint32_t ph = (c >> 2) & 1;
+            const int s = c % STAGES;
+            const uint32_t ph = (c / STAGES) & 1;
             if (!mbar_wait_parity_bounded(smem_addr(&bars.a_full[s]), ph)) ok = false;
             if (!mbar_wait_parity_bounded(smem_addr(&bars.b_full[s]), ph)) ok = false;
             fence_after_sync();
             const uint32_t a0 = smem_addr(Abuf + s * kWsAStageBytes), b0 = smem_addr(Bbuf + s * b_stage_bytes);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_f16(tmem, smem_desc(a0 + kk * 32u, 16u, 1024u, kSwizzle128B),
-                        smem_desc(b0 + kk * 32u, 16u, 1024u, kSwizzle128B), idesc, c > 0 || kk > 0);
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t ad = A_MN ? smem_desc(a0 + kk * 4096u, 2048u, 1024u, kSwizzle128B)
+                                         : smem_desc(a0 + kk * 32u, 16u, 1024u, kSwizzle128B);
+                mma_f16(tmem, ad, smem_desc(b0 + kk * 32u, 16u, 1024u, kSwizzle128B), idesc, c > 0 || kk > 0);
+            }
             commit(smem_addr(&bars.done[s]));
-            if (c + kWsStages - 1 < nch) {
-                // stage (c + 3) % 4 was last read by the MMAs of chunk c - 1
-                if (c >= 1 && !mbar_wait_parity_bounded(smem_addr(&bars.done[(c - 1) & 3]), ((c - 1) >> 2) & 1))
+            if (c + STAGES - 1 < nch) {
+                // stage (c + STAGES - 1) % STAGES was last read by the MMAs of chunk c - 1
+                if (c >= 1 && !mbar_wait_parity_bounded(smem_addr(&bars.done[(c - 1) % STAGES]),
+                                                        ((c - 1) / STAGES) & 1))
                     ok = false;
-                issue_b(c + kWsStages - 1);
+                issue_b(c + STAGES - 1);
             }
         }
         // the final phase of every stage used: all MMAs complete, no arrival pending
-        for (int s = 0; s < kWsStages && s < nch; ++s) {
-            const int last = s + ((nch - 1 - s) / kWsStages) * kWsStages;
-            if (!mbar_wait_parity_bounded(smem_addr(&bars.done[s]), (last >> 2) & 1)) ok = false;
+        for (int s = 0; s < STAGES && s < nch; ++s) {
+            const int last = s + ((nch - 1 - s) / STAGES) * STAGES;
+            if (!mbar_wait_parity_bounded(smem_addr(&bars.done[s]), (last / STAGES) & 1)) ok = false;
         }
     }
     fence_before_sync();
