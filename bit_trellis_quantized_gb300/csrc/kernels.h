@@ -90,6 +90,7 @@ struct MoeArgs {
     int* err;        // set non-zero if a bounded wait gave up (zeroed by the router kernel)
     int gu_kt_per_cta;  // filled by the gate_up launcher
     int dn_ksplit;      // filled by the down launcher
+    int dn_xt_floats;   // filled by the down launcher: routed input floats of one down rank (multiple of 32)
     // grouped path (T > kSlotModeMaxT): token grouping by expert
     int grp_cap;        // tokens per work item (16, 32, 64 or 128)
     int grp_max_items;  // T*topk/grp_cap + E

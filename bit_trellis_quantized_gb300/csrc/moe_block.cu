@@ -264,6 +264,11 @@ __device__ void gate_up_routed(const MoeArgs& a, float* smem) {
 
     const int t = slot / a.topk;
     const int j = slot % a.topk;
+    // x is this call's input: its loads for the input transform go out before
+    // the wait for the router (only rin depends on the routing)
+    const uint16_t* xrow = a.x + (long long)t * a.hidden;
+    uint2 x_pre = make_uint2(0u, 0u);
+    if (warp < nk / 128) x_pre = *reinterpret_cast<const uint2*>(xrow + kt0 * 16 + warp * 128 + 4 * lane);
     pdl_wait();     // router logits
     pdl_trigger();  // logits complete: the down kernel may read them early
     if (warp == 0) {
@@ -287,11 +292,10 @@ __device__ void gate_up_routed(const MoeArgs& a, float* smem) {
 
     // xt = H128(rin_e * x[t]) over this CTA's inputs
     const uint16_t* rin = a.gu_rin + (long long)e * a.hidden;
-    const uint16_t* xrow = a.x + (long long)t * a.hidden;
     for (int blk = warp; blk < nk / 128; blk += kGuWarps) {
         const int ib = kt0 * 16 + blk * 128 + 4 * lane;
         const uint2 rb = *reinterpret_cast<const uint2*>(rin + ib);
-        const uint2 xb = *reinterpret_cast<const uint2*>(xrow + ib);
+        const uint2 xb = blk == warp ? x_pre : *reinterpret_cast<const uint2*>(xrow + ib);
         float v[4];
         v[0] = h2f_bits(static_cast<uint16_t>(rb.x & 0xFFFFu)) * h2f_bits(static_cast<uint16_t>(xb.x & 0xFFFFu));
         v[1] = h2f_bits(static_cast<uint16_t>(rb.x >> 16)) * h2f_bits(static_cast<uint16_t>(xb.x >> 16));
@@ -361,7 +365,8 @@ __global__ void __launch_bounds__(kDnThreads, 3) moe_down_kernel(const MoeArgs a
     float* shres = slots + kMaxCluster * 128; // [128] shared-expert rows of the block, on rank 0
     float* dres = shres + 128;                // [topk][128] finished experts, on rank 0
     float* red = dres + 8 * 128;              // [kDnWarps][128] (+128: partial of ranks != 0)
-    float* xt = red + (kDnWarps + 1) * 128;   // [max(inter / ks, sh_inter)]
+    float* xt = red + (kDnWarps + 1) * 128;   // [inter / ks] (rounded up to 32)
+    float* xsh = xt + a.dn_xt_floats;          // [sh_inter] (rounded up to 32): SwiGLU(shgu[t]), swizzled
     __shared__ __align__(8) unsigned long long bar;
     __shared__ int e_s[8];
     __shared__ float w_s[8];
@@ -373,13 +378,12 @@ __global__ void __launch_bounds__(kDnThreads, 3) moe_down_kernel(const MoeArgs a
     // rows rank*sh_per + warp + 8*i; with sh_inter <= 512 a warp's first two
     // rows are prefetched now.
     const int sh_per = (128 + csz - 1) / csz;
-    const int n_sh = a.sh_inter;
     uint4 shw[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
         const int rr = warp + kDnWarps * i, row = rank * sh_per + rr;
-        if (n_sh > 0 && n_sh <= 512 && rr < sh_per && row < 128 && lane * 16 < n_sh)
-            shw[i] = ldg_stream_v4(a.sh_dn_w8 + (long long)(ob * 128 + row) * n_sh + lane * 16);
+        if (a.sh_inter > 0 && a.sh_inter <= 512 && rr < sh_per && row < 128 && lane * 16 < a.sh_inter)
+            shw[i] = ldg_stream_v4(a.sh_dn_w8 + (long long)(ob * 128 + row) * a.sh_inter + lane * 16);
     }
 
     const int slot = t * a.topk + j;
@@ -408,6 +412,24 @@ __global__ void __launch_bounds__(kDnThreads, 3) moe_down_kernel(const MoeArgs a
     if (warp < nk / 128) rin_pre = *reinterpret_cast<const uint2*>(rin + kt0 * 16 + warp * 128 + 4 * lane);
     pdl_wait();  // gate_up outputs and the shared expert's gate_up
 
+    // the shared expert's down input, SwiGLU(shgu[t]): its loads (two per
+    // thread for sh_inter <= 512) go out together with the routed input
+    // transform's, and the shared rows after the main loop then only need
+    // their dot products
+    const int n_sh = a.sh_inter;
+    const float* gu = a.shgu + (long long)t * 2 * n_sh;
+    float shg[2] = {0.f, 0.f}, shu[2] = {0.f, 0.f};
+    if (n_sh > 0 && n_sh <= 2 * kDnThreads) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int i = threadIdx.x + q * kDnThreads;
+            if (i < n_sh) {
+                shg[q] = gu[i];
+                shu[q] = gu[n_sh + i];
+            }
+        }
+    }
+
     // xt = H128(rin_e * SwiGLU(ygu[slot])) over this rank's inputs
     const float* yr = a.ygu + (long long)slot * 2 * a.inter;
     for (int blk = warp; blk < nk / 128; blk += kDnWarps) {
@@ -423,6 +445,15 @@ __global__ void __launch_bounds__(kDnThreads, 3) moe_down_kernel(const MoeArgs a
         h128_warp(v, lane);
         *reinterpret_cast<float4*>(xt + blk * 128 + 4 * lane) = make_float4(v[0], v[1], v[2], v[3]);
     }
+    if (n_sh > 0 && n_sh <= 2 * kDnThreads) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int i = threadIdx.x + q * kDnThreads;
+            if (i < n_sh) xsh[xs_swz(i)] = silu_f(shg[q]) * shu[q];
+        }
+    } else {
+        for (int i = threadIdx.x; i < n_sh; i += kDnThreads) xsh[xs_swz(i)] = silu_f(gu[i]) * gu[n_sh + i];
+    }
     __syncthreads();
     uint2 rout_pre = make_uint2(0u, 0u);  // rank 0: every expert's output scales, fetched while the loop runs
     if (rank == 0 && warp < a.topk)
@@ -433,10 +464,8 @@ __global__ void __launch_bounds__(kDnThreads, 3) moe_down_kernel(const MoeArgs a
     // shared expert rows: xt <- SwiGLU(shgu[t]); the values go to rank 0's
     // shres (directly on rank 0, through distributed shared memory elsewhere)
     if (a.sh_inter > 0) {
-        const float* gu = a.shgu + (long long)t * 2 * n_sh;
-        for (int i = threadIdx.x; i < n_sh; i += kDnThreads) xt[xs_swz(i)] = silu_f(gu[i]) * gu[n_sh + i];
-        __syncthreads();
-        cluster_wait();  // rank 0's shared memory may be written from here on
+        cluster_wait();  // rank 0's shared memory may be written from here on (xsh is complete: the main
+                         // loop ended with a CTA barrier)
         const float gate = a.shgate[t];
         for (int rr = warp, i = 0; rr < sh_per; rr += kDnWarps, ++i) {
             const int sh_row = rank * sh_per + rr;
@@ -451,7 +480,7 @@ __global__ void __launch_bounds__(kDnThreads, 3) moe_down_kernel(const MoeArgs a
                     for (int q = 0; q < 4; ++q) {
                         float f[4];
                         i8x4_to_f32(words[q], f);
-                        const float4 xv = *reinterpret_cast<const float4*>(xt + xs_swz(lane * 16 + 4 * q));
+                        const float4 xv = *reinterpret_cast<const float4*>(xsh + xs_swz(lane * 16 + 4 * q));
                         acc = fmaf(f[0], xv.x, acc);
                         acc = fmaf(f[1], xv.y, acc);
                         acc = fmaf(f[2], xv.z, acc);
@@ -463,7 +492,7 @@ __global__ void __launch_bounds__(kDnThreads, 3) moe_down_kernel(const MoeArgs a
                 dot = acc;
             } else {
                 float d1[1][1];
-                int8_rows_dot<1, 1, 4>(a.sh_dn_w8 + (long long)(ob * 128 + sh_row) * n_sh, n_sh, 1, n_sh, xt, n_sh, lane,
+                int8_rows_dot<1, 1, 4>(a.sh_dn_w8 + (long long)(ob * 128 + sh_row) * n_sh, n_sh, 1, n_sh, xsh, n_sh, lane,
                                        d1);
                 dot = d1[0][0];
             }
@@ -583,9 +612,11 @@ cudaError_t launch_down(MoeArgs a, cudaStream_t s) {
     // of Hadamard blocks and the cluster stays within 16 CTAs.
     a.dn_ksplit = ((a.inter / 128) % 2 == 0 && 2 * a.topk <= kMaxCluster) ? 2 : 1;
     const int csz = a.topk * a.dn_ksplit;
-    int nx = a.inter / a.dn_ksplit > a.sh_inter ? a.inter / a.dn_ksplit : a.sh_inter;
-    nx = (nx + 31) / 32 * 32;  // the shared rows' swizzled staging works on groups of 32 floats
-    const int smem = (kMaxCluster * 128 + 128 + 8 * 128 + (kDnWarps + 1) * 128 + nx) * 4;
+    a.dn_xt_floats = (a.inter / a.dn_ksplit + 31) / 32 * 32;
+    // routed inputs of one rank, then the shared expert's inputs (swizzled
+    // staging works on groups of 32 floats)
+    const int nsh = (a.sh_inter + 31) / 32 * 32;
+    const int smem = (kMaxCluster * 128 + 128 + 8 * 128 + (kDnWarps + 1) * 128 + a.dn_xt_floats + nsh) * 4;
     const void* f = reinterpret_cast<const void*>(moe_down_kernel<K>);
     cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
