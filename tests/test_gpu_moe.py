@@ -247,3 +247,42 @@ def test_route_skewed_load(native):
     base = g.standard_normal(512)
     x = (base[None, :] + 0.1 * g.standard_normal((600, 512))).astype(np.float16)
     _check_route(native, d, x, topk=2)
+
+
+# ------------------------------------------------------------- edge cases
+
+
+@pytest.mark.parametrize("T", [3, 20])
+def test_moe_single_expert_top1(native, T):
+    """One expert, top-1: every slot goes to expert 0 with weight exactly 1
+    (per-slot path at T = 3, one grouped item at T = 20)."""
+    d = gen.moe_layer(95 + T, hidden=256, inter=128, n_experts=1)
+    x = gen.fp16_normal(gen.rng(96 + T), (T, 256))
+    out, ids, w = _check_block(native, d, x, topk=1)
+    assert np.all(ids == 0) and np.all(w == 1.0)
+
+
+def test_moe_max_tokens_per_call(native):
+    """T = 8192, the largest batch of one call, on a small layer: 16,384 slots
+    over 8 experts (items of 128 tokens, ~16 per expert); routing of every
+    token is checked, outputs on a sample."""
+    d = gen.moe_layer(97, hidden=256, inter=128, n_experts=8)
+    x = gen.fp16_normal(gen.rng(98), (8192, 256))
+    block = native.MoeBlock(d, topk=2)
+    out, ids, w = block(dev(x))
+    ref_ids, ref_w, _ = o.route(x, d["Wg"], 2)
+    assert np.array_equal(ids.cpu().numpy(), ref_ids)
+    assert int(block.workspace(8192)[:4].view(torch.int32).item()) == 0
+    sample = [0, 1, 4095, 4096, 8190, 8191]
+    ref, _, _, _ = o.moe_block(o.MoeLayer(**d), x[sample], k=2)
+    assert rel_err_rows(out.cpu().numpy()[sample], ref).max() <= TOL
+
+
+@pytest.mark.parametrize("T", [2, 24])
+def test_moe_max_hidden(native, T):
+    """hidden = 8192, the largest the boundary accepts: the router's column
+    chunks, 64 input blocks of gate_up, an 8192-row down projection and an
+    int8 shared expert with 8192 inputs."""
+    d = gen.moe_layer(99, hidden=8192, inter=128, n_experts=4, sh_inter=64)
+    x = gen.fp16_normal(gen.rng(100), (T, 8192))
+    _check_block(native, d, x, topk=2, tokens=[0, T - 1])
