@@ -108,7 +108,7 @@ struct MoeArgs {
 // Largest token count of a grouped work item, and the largest batch that
 // runs the per-slot GEMV path instead.
 constexpr int kGrpCapMax = 128;
-constexpr int kSlotModeMaxT = 4;
+constexpr int kSlotModeMaxT = 12;
 
 // Scratch of the grouped path for T tokens.
 struct GroupPlan {

@@ -149,9 +149,10 @@ typedef struct escha_moe_layer {
  * to 0 when its first kernel starts and to a non-zero value if a kernel had
  * to give up waiting on a cluster peer (it then returns instead of hanging;
  * the outputs of that call are invalid). Read it after synchronising.
- * Batches of up to 4 tokens run fused decode GEMVs per (token, expert);
+ * Batches of up to 12 tokens run fused decode GEMVs per (token, expert);
  * larger batches group the tokens by expert and decode each expert's codes
- * once per group of up to 64 tokens, feeding tcgen05 tensor-core MMAs.
+ * once per work item of up to 128 of its tokens, feeding tcgen05
+ * tensor-core MMAs.
  *   x       fp16 [T][hidden];  1 <= T <= 8192
  *   out     f32 [T][hidden] output
  *   ids_out int32 [T][topk] output, may be null
@@ -182,8 +183,8 @@ int escha_moe_block_timed(const escha_moe_layer* L, const uint16_t* x, int T, fl
  * every GPU that loads the library holds until the process exits.
  *   - Calls whose escha_moe_block_workspace(L, T) exceeds the buffer are
  *     rejected with ESCHA_E_WORKSPACE before anything is enqueued: for a
- *     hidden-2048, inter-512, 256-expert, top-8 layer, T <= 4 fits (the
- *     per-slot path, 183 KB at T = 4); the grouped path of T >= 5 needs
+ *     hidden-2048, inter-512, 256-expert, top-8 layer, T <= 12 fits (the
+ *     per-slot path, 548 KB at T = 12); the grouped path of T >= 13 needs
  *     several MB (its B image) and is rejected.
  *   - The first call on a device looks the buffer's device address up
  *     (cudaGetSymbolAddress); make that first call before any stream capture.

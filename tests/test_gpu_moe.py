@@ -77,6 +77,14 @@ def test_moe_block_full_size_batch1(native):
     assert len(set(ids[0])) == 8
 
 
+def test_moe_block_per_slot_path_at_its_largest_batch(native):
+    """12 tokens, the largest batch of the per-slot path, full-size block:
+    96 slots, the fused shared expert in three passes of 4 tokens."""
+    d = gen.moe_layer(1005)
+    x = gen.fp16_normal(gen.rng(2006), (12, 2048))
+    _check_block(native, d, x, topk=8, tokens=[0, 5, 11])
+
+
 def test_router_ids_bit_exact_many_tokens(native):
     d = gen.moe_layer(1003, hidden=2048, inter=128, n_experts=256)
     x = gen.fp16_normal(gen.rng(2003), (64, 2048))
@@ -129,8 +137,9 @@ def test_moe_pruned_gate_up_channels_stay_zero(native):
 
 
 # --------------------------------------------------------------- grouped path
-# More than 4 tokens per call run the grouped path: tokens sorted by expert,
-# each expert decoded once per group of up to 64 tokens into tcgen05 MMAs.
+# More than 12 tokens per call run the grouped path: tokens sorted by expert,
+# each expert decoded once per work item of up to 128 tokens into tcgen05
+# MMAs.
 
 
 def test_moe_grouped_small_groups(native):
@@ -156,7 +165,7 @@ def test_moe_grouped_full_size_batch64_sampled(native):
 
 
 @pytest.mark.parametrize("T,E,topk,tokens", [
-    (8, 64, 8, None),                     # item capacity 16, runs of 1-2 tokens
+    (16, 64, 8, None),                    # item capacity 16, runs of 1-4 tokens
     (96, 32, 4, range(0, 96, 5)),         # capacity 32
     (700, 4, 1, range(0, 700, 23)),       # capacity 128, two and more items per expert
     (130, 16, 8, range(0, 130, 9)),       # capacity 128, ragged runs
