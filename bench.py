@@ -62,6 +62,13 @@ GATE_UP_KERNEL_BYTES = (TOPK * (GU_CODE_BYTES + HIDDEN * 2 + 2 * INTER * 2) + HI
                         + 2 * INTER * 4 + 4)
 
 
+# Routed weights decoded by one launch of the gate_up kernel at batch 1 and the
+# issue peak of the GPU (warp-instructions per second).
+GU_WEIGHTS = TOPK * HIDDEN * 2 * INTER
+ALU_OPS_PER_WEIGHT = 6
+ALU_PEAK_WARP_INSTR = 152 * 4 * 2.07e9
+
+
 def measured_traffic():
     """DRAM bytes per launch of the gate_up kernel from the committed ncu
     capture, or None when the kernel sources changed since the capture."""
@@ -373,6 +380,18 @@ def run_ours(args, ws, rank, local):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "traffic": measured_traffic(), "kernel": "moe_gate_up_kernel<K=3> (8 routed experts + int8 shared gate_up)",
                      "algorithmic_bytes_per_launch": gu_bytes, "ms_per_launch": gu_ms, "peak_source": src},
+        # The decode is bound by instruction issue, not HBM: the same kernel
+        # against the issue peak (152 SMs x 4 schedulers x 1 warp-instruction
+        # per clock at the maximum SM clock), counting the algorithm's 6
+        # operations per decoded weight and token (16-bit window, hash
+        # multiply, and-xor, fp16 add, conversion, f32 fma).
+        "roofline_alu": {"bound": "alu", "achieved": GU_WEIGHTS * ALU_OPS_PER_WEIGHT / 32 / (gu_ms * 1e-3) / 1e12,
+                         "peak": ALU_PEAK_WARP_INSTR / 1e12,
+                         "unit": "T warp-instructions/s",
+                         "frac": GU_WEIGHTS * ALU_OPS_PER_WEIGHT / 32 / (gu_ms * 1e-3) / ALU_PEAK_WARP_INSTR,
+                         "kernel": "moe_gate_up_kernel<K=3>, routed decode only",
+                         "algorithmic_ops_per_launch": GU_WEIGHTS * ALU_OPS_PER_WEIGHT,
+                         "peak_source": "derived: 152 SMs x 4 x 2.07e9 /s"},
         "packed_expert_gbs": routed_code_bytes / (t_step * 1e-3) / 1e9,
         "packed_expert_frac": routed_code_bytes / (t_step * 1e-3) / 1e9 / hbm,
         "phase_ms": {"router": float(ph[0]), "gate_up+shared_gate_up": float(ph[1]),

@@ -11,7 +11,7 @@
 //     -> counts, offsets, perm (grouped position -> slot), each slot's padded
 //     position (every expert's run padded to a multiple of 4 tokens) and the
 //     work items (expert, first position) of at most `cap` tokens.
-//  3. prep (gate_up, later down): one warp per (slot, 128-input block) writes
+//  3. prep (gate_up, later down): for every (slot, 128-input block) writes
 //     x~ = H128(rin_e * input) * 2^-8, split into fp16 hi and lo, as rows 2P
 //     and 2P+1 (P = padded position) of the B image, in the layout the MMA
 //     reads. The input is x[token] for gate_up, SwiGLU(gate_up output) for
@@ -206,66 +206,102 @@ struct GroupedProj {
     float* y;               // [slots][out]
 };
 
-// BPW 128-input blocks per warp, their loads issued together (4 when there
-// are enough tasks to fill the GPU anyway, else 1 for more warps).
-template <int kPrepBlk>
+// One warp per (slot, 4 consecutive 128-input blocks): 8 lanes per block, 16
+// consecutive values per lane, so the blockwise Hadamard runs its first four
+// butterfly stages in registers and only the last three across lanes
+// (shuffles within the 8 lanes). Loads and image stores are 16-byte vectors.
 __global__ void __launch_bounds__(256) moe_prep_kernel(const MoeArgs a, const GroupedProj p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_wait();
     pdl_trigger();
     const int nblk = p.in >> 7;
-    const int ngrp = (nblk + kPrepBlk - 1) / kPrepBlk;
+    const int ngrp = (nblk + 3) / 4;
     const long long task = (long long)blockIdx.x * 8 + warp;
-    if (task >= (long long)a.T * a.topk * ngrp) return;
-    const int s = static_cast<int>(task / ngrp), b0 = static_cast<int>(task % ngrp) * kPrepBlk;
+    if (task >= (long long)a.T * a.topk * ngrp) return;  // warp-uniform
+    const int s = static_cast<int>(task / ngrp);
+    const int b = static_cast<int>(task % ngrp) * 4 + (lane >> 3);
+    const int l8 = lane & 7;
+    const bool live = b < nblk;  // lanes of a block past the input still join the shuffles
     const int e = a.ids[s];
     const int P = a.grp_ppos[s];
-    float v[kPrepBlk][4];
-    uint2 rb[kPrepBlk];
-#pragma unroll
-    for (int q = 0; q < kPrepBlk; ++q) {
-        if (b0 + q >= nblk) break;
-        const int ib = (b0 + q) * 128 + 4 * lane;
-        rb[q] = *reinterpret_cast<const uint2*>(p.rin + (long long)e * p.in + ib);
+    const int ib = b * 128 + 16 * l8;
+    float v[16];
+    if (live) {
+        const uint4* rp = reinterpret_cast<const uint4*>(p.rin + (long long)e * p.in + ib);
+        const uint4 r0 = rp[0], r1 = rp[1];
+        const uint32_t rw[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
         if (p.mode == 0) {
-            const uint2 xb = *reinterpret_cast<const uint2*>(a.x + (long long)(s / a.topk) * a.hidden + ib);
-            v[q][0] = h2f_bits(static_cast<uint16_t>(xb.x & 0xFFFFu));
-            v[q][1] = h2f_bits(static_cast<uint16_t>(xb.x >> 16));
-            v[q][2] = h2f_bits(static_cast<uint16_t>(xb.y & 0xFFFFu));
-            v[q][3] = h2f_bits(static_cast<uint16_t>(xb.y >> 16));
+            const uint4* xp = reinterpret_cast<const uint4*>(a.x + (long long)(s / a.topk) * a.hidden + ib);
+            const uint4 x0 = xp[0], x1 = xp[1];
+            const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                v[2 * q] = h2f_bits(static_cast<uint16_t>(xw[q] & 0xFFFFu));
+                v[2 * q + 1] = h2f_bits(static_cast<uint16_t>(xw[q] >> 16));
+            }
         } else {
-            const float* yr = a.ygu + (long long)s * 2 * a.inter;
-            const float4 g = *reinterpret_cast<const float4*>(yr + ib);
-            const float4 u = *reinterpret_cast<const float4*>(yr + a.inter + ib);
-            v[q][0] = silu_f(g.x) * u.x;
-            v[q][1] = silu_f(g.y) * u.y;
-            v[q][2] = silu_f(g.z) * u.z;
-            v[q][3] = silu_f(g.w) * u.w;
+            const float4* gp = reinterpret_cast<const float4*>(a.ygu + (long long)s * 2 * a.inter + ib);
+            const float4* up = reinterpret_cast<const float4*>(a.ygu + (long long)s * 2 * a.inter + a.inter + ib);
+            float4 g4[4], u4[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                g4[q] = gp[q];
+                u4[q] = up[q];
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                v[4 * q] = silu_f(g4[q].x) * u4[q].x;
+                v[4 * q + 1] = silu_f(g4[q].y) * u4[q].y;
+                v[4 * q + 2] = silu_f(g4[q].z) * u4[q].z;
+                v[4 * q + 3] = silu_f(g4[q].w) * u4[q].w;
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            v[2 * q] *= h2f_bits(static_cast<uint16_t>(rw[q] & 0xFFFFu));
+            v[2 * q + 1] *= h2f_bits(static_cast<uint16_t>(rw[q] >> 16));
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < 16; ++q) v[q] = 0.f;
+    }
+    // unscaled Sylvester butterflies: index bits 0-3 in registers, 4-6 across lanes
+#pragma unroll
+    for (int m = 1; m < 16; m <<= 1) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            if (j & m) continue;
+            const float x0 = v[j], x1 = v[j | m];
+            v[j] = x0 + x1;
+            v[j | m] = x0 - x1;
         }
     }
 #pragma unroll
-    for (int q = 0; q < kPrepBlk; ++q) {
-        if (b0 + q >= nblk) break;
-        float w[4] = {v[q][0] * h2f_bits(static_cast<uint16_t>(rb[q].x & 0xFFFFu)),
-                      v[q][1] * h2f_bits(static_cast<uint16_t>(rb[q].x >> 16)),
-                      v[q][2] * h2f_bits(static_cast<uint16_t>(rb[q].y & 0xFFFFu)),
-                      v[q][3] * h2f_bits(static_cast<uint16_t>(rb[q].y >> 16))};
-        h128_warp(w, lane);
-        uint32_t hv[2], lv[2];
+    for (int m = 1; m < 8; m <<= 1) {
+        const float sgn = (l8 & m) ? -1.f : 1.f;  // upper element: partner - own; lower: own + partner
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const float s0 = w[2 * r] * kPrescale, s1 = w[2 * r + 1] * kPrescale;
-            const __half h0 = __float2half_rn(s0), h1 = __float2half_rn(s1);
-            const __half l0 = __float2half_rn(s0 - __half2float(h0)), l1 = __float2half_rn(s1 - __half2float(h1));
-            hv[r] = static_cast<uint32_t>(__half_as_ushort(h0)) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
-            lv[r] = static_cast<uint32_t>(__half_as_ushort(l0)) | (static_cast<uint32_t>(__half_as_ushort(l1)) << 16);
+        for (int j = 0; j < 16; ++j) {
+            const float pv = __shfl_xor_sync(0xffffffffu, v[j], m);
+            v[j] = fmaf(sgn, v[j], pv);
         }
-        const int chunk = 2 * (b0 + q) + (lane >> 4);
-        const uint32_t k_in = static_cast<uint32_t>((4 * lane) & 63);
-        uint8_t* base = a.grp_img + (long long)chunk * a.grp_img_rows * 128;
-        *reinterpret_cast<uint2*>(base + tc::kmajor_off(2u * P, k_in)) = make_uint2(hv[0], hv[1]);
-        *reinterpret_cast<uint2*>(base + tc::kmajor_off(2u * P + 1u, k_in)) = make_uint2(lv[0], lv[1]);
     }
+    if (!live) return;
+    uint32_t hv[8], lv[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float s0 = v[2 * q] * kPrescale, s1 = v[2 * q + 1] * kPrescale;
+        const __half h0 = __float2half_rn(s0), h1 = __float2half_rn(s1);
+        const __half q0 = __float2half_rn(s0 - __half2float(h0)), q1 = __float2half_rn(s1 - __half2float(h1));
+        hv[q] = static_cast<uint32_t>(__half_as_ushort(h0)) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
+        lv[q] = static_cast<uint32_t>(__half_as_ushort(q0)) | (static_cast<uint32_t>(__half_as_ushort(q1)) << 16);
+    }
+    const int chunk = 2 * b + (l8 >> 2);
+    const uint32_t k_in = static_cast<uint32_t>((16 * l8) & 63);
+    uint8_t* base = a.grp_img + (long long)chunk * a.grp_img_rows * 128;
+    *reinterpret_cast<uint4*>(base + tc::kmajor_off(2u * P, k_in)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+    *reinterpret_cast<uint4*>(base + tc::kmajor_off(2u * P, k_in + 8u)) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+    *reinterpret_cast<uint4*>(base + tc::kmajor_off(2u * P + 1u, k_in)) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+    *reinterpret_cast<uint4*>(base + tc::kmajor_off(2u * P + 1u, k_in + 8u)) = make_uint4(lv[4], lv[5], lv[6], lv[7]);
 }
 
 // ---------------------------------------------------------------------------
@@ -436,14 +472,38 @@ __global__ void __launch_bounds__(tc::kMlThreads + 32, 2)
 // ---------------------------------------------------------------------------
 // 5. combine: out[t] = sum_j w[t][j] * d[t*k + j] + sigmoid(g . x[t]) * sh[t]
 // ---------------------------------------------------------------------------
+// One CTA per token. For hidden <= 2048 every load of a thread (its two
+// float4 columns of the k down outputs and of the shared output, and its
+// part of the gate's dot product) is issued before any arithmetic, so the
+// CTA waits for memory once; larger hidden sizes loop.
+constexpr int kCombineMaxK = 8;
+
 __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeArgs a, const float* d) {
     const int t = blockIdx.x;
     __shared__ float red[8];
     __shared__ float gate_s;
     pdl_wait();
+    const float* wt = a.w + (long long)t * a.topk;
+    const uint16_t* xr = a.x + (long long)t * a.hidden;
+    const bool two = a.hidden <= 2 * 4 * 256 && a.topk <= kCombineMaxK;
+    float4 dv[2][kCombineMaxK], sv[2];
+    float wj[kCombineMaxK];
+    if (two) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int i = 4 * threadIdx.x + q * 4 * 256;
+            if (i >= a.hidden) continue;
+#pragma unroll
+            for (int j = 0; j < kCombineMaxK; ++j)
+                if (j < a.topk) dv[q][j] = *reinterpret_cast<const float4*>(d + ((long long)t * a.topk + j) * a.hidden + i);
+            if (a.sh_inter > 0) sv[q] = *reinterpret_cast<const float4*>(a.sh + (long long)t * a.hidden + i);
+        }
+#pragma unroll
+        for (int j = 0; j < kCombineMaxK; ++j)
+            if (j < a.topk) wj[j] = wt[j];
+    }
     float gate = 0.f;
     if (a.sh_inter > 0) {
-        const uint16_t* xr = a.x + (long long)t * a.hidden;
         float acc = 0.f;
         for (int i = threadIdx.x; i < a.hidden; i += 256) acc = fmaf(h2f_bits(a.sh_gate[i]), h2f_bits(xr[i]), acc);
 #pragma unroll
@@ -458,16 +518,39 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeArgs a, const
         __syncthreads();
         gate = gate_s;
     }
-    const float* wt = a.w + (long long)t * a.topk;
+    if (two) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int i = 4 * threadIdx.x + q * 4 * 256;
+            if (i >= a.hidden) continue;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < kCombineMaxK; ++j) {
+                if (j >= a.topk) break;
+                acc.x = fmaf(wj[j], dv[q][j].x, acc.x);
+                acc.y = fmaf(wj[j], dv[q][j].y, acc.y);
+                acc.z = fmaf(wj[j], dv[q][j].z, acc.z);
+                acc.w = fmaf(wj[j], dv[q][j].w, acc.w);
+            }
+            if (a.sh_inter > 0) {
+                acc.x = fmaf(gate, sv[q].x, acc.x);
+                acc.y = fmaf(gate, sv[q].y, acc.y);
+                acc.z = fmaf(gate, sv[q].z, acc.z);
+                acc.w = fmaf(gate, sv[q].w, acc.w);
+            }
+            *reinterpret_cast<float4*>(a.out + (long long)t * a.hidden + i) = acc;
+        }
+        return;
+    }
     for (int i = 4 * threadIdx.x; i < a.hidden; i += 4 * 256) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int j = 0; j < a.topk; ++j) {
-            const float wj = wt[j];
+            const float w = wt[j];
             const float4 v = *reinterpret_cast<const float4*>(d + ((long long)t * a.topk + j) * a.hidden + i);
-            acc.x = fmaf(wj, v.x, acc.x);
-            acc.y = fmaf(wj, v.y, acc.y);
-            acc.z = fmaf(wj, v.z, acc.z);
-            acc.w = fmaf(wj, v.w, acc.w);
+            acc.x = fmaf(w, v.x, acc.x);
+            acc.y = fmaf(w, v.y, acc.y);
+            acc.z = fmaf(w, v.z, acc.z);
+            acc.w = fmaf(w, v.w, acc.w);
         }
         if (a.sh_inter > 0) {
             const float4 v = *reinterpret_cast<const float4*>(a.sh + (long long)t * a.hidden + i);
@@ -491,14 +574,9 @@ cudaError_t launch_grouped(const MoeArgs& a, const GroupedProj& p, cudaStream_t 
 }
 
 cudaError_t launch_prep(const MoeArgs& a, const GroupedProj& p, cudaStream_t s) {
-    const long long blocks = (long long)a.T * a.topk * (p.in / 128);
+    const long long tasks = (long long)a.T * a.topk * ((p.in / 128 + 3) / 4);
     void* args[] = {const_cast<MoeArgs*>(&a), const_cast<GroupedProj*>(&p)};
-    if (blocks >= 4ll * 152 * 64) {  // four blocks per warp still leave 64 warps per SM
-        const long long tasks = (long long)a.T * a.topk * ((p.in / 128 + 3) / 4);
-        return launch_kernel(reinterpret_cast<const void*>(moe_prep_kernel<4>),
-                             dim3(static_cast<unsigned>((tasks + 7) / 8)), dim3(256), 0, true, s, args);
-    }
-    return launch_kernel(reinterpret_cast<const void*>(moe_prep_kernel<1>), dim3(static_cast<unsigned>((blocks + 7) / 8)),
+    return launch_kernel(reinterpret_cast<const void*>(moe_prep_kernel), dim3(static_cast<unsigned>((tasks + 7) / 8)),
                          dim3(256), 0, true, s, args);
 }
 
