@@ -417,27 +417,38 @@ __global__ void __launch_bounds__(tc::kMlThreads + 32, 2)
     const int hr = warp >> 1, half = warp & 1;
     // the warp's 4 tiles of tile row 4b + hr
     auto row4 = [&](int b) { return codes + ((long long)(4 * b + hr) * NT + ob * 8 + 4 * half) * (16 * K); };
-    // two register sets used in turn: the next block's codes load into one
-    // while the other is decoded (never copied: a copy would wait for the load)
-    HalfRowCodes<K> c0, c1;
-    if (warp < kDecodeWarps) load_half_row<K>(c0, row4(0), lane);
+    // three register sets used in turn: block b + 2's codes load into one
+    // while block b is decoded from another, so a load has two blocks of
+    // decode time to arrive; no set is ever copied (a copy would wait for the
+    // load)
+    HalfRowCodes<K> c0, c1, c2;
+    if (warp < kDecodeWarps) {
+        load_half_row<K>(c0, row4(0), lane);
+        if (nblk > 1) load_half_row<K>(c1, row4(1), lane);
+    }
+    int rot = 0;  // b % 3
     const int nbr = (lane & ~7) | ((lane + 1) & 7);
     const uint8_t* img = a.grp_img + (long long)desc.z * 128;
 
     const bool ok = tc::mma_mainloop_ws<2, true>(
         Abuf, Bbuf, b_chunk, img, (long long)a.grp_img_rows * 128, 256u * static_cast<uint32_t>(nt4), nblk, tmem,
         idesc, bars, [&](int b, uint8_t* A) {
-            const bool more = b + 1 < nblk;
+            const bool more = b + 2 < nblk;
             uint8_t* slice = A + hr * 4096;
-            if ((b & 1) == 0) {
-                if (more) load_half_row<K>(c1, row4(b + 1), lane);
+            if (rot == 0) {
+                if (more) load_half_row<K>(c2, row4(b + 2), lane);
                 c0.p[K] = __shfl_sync(0xffffffffu, c0.p[0], nbr) & 0xFFFFu;
                 decode_half_row_to_smem<K>(c0, slice, lane, 4 * half);
-            } else {
-                if (more) load_half_row<K>(c0, row4(b + 1), lane);
+            } else if (rot == 1) {
+                if (more) load_half_row<K>(c0, row4(b + 2), lane);
                 c1.p[K] = __shfl_sync(0xffffffffu, c1.p[0], nbr) & 0xFFFFu;
                 decode_half_row_to_smem<K>(c1, slice, lane, 4 * half);
+            } else {
+                if (more) load_half_row<K>(c1, row4(b + 2), lane);
+                c2.p[K] = __shfl_sync(0xffffffffu, c2.p[0], nbr) & 0xFFFFu;
+                decode_half_row_to_smem<K>(c2, slice, lane, 4 * half);
             }
+            rot = rot == 2 ? 0 : rot + 1;
         });
     if (!ok && tid == 0) atomicExch(a.err, 3);
 
