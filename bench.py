@@ -95,6 +95,29 @@ def peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+def replica_seeds(rank: int):
+    """Seeds of one replica's layers and token stream: every rank runs its own
+    independent stream (replicas, weak scaling)."""
+    return LAYER_SEED + 1000 * rank, X_SEED + 100 * rank
+
+
+def max_over_ranks(values, dist_mod=None, device=None):
+    """Element-wise maximum of per-rank timings over all ranks (the slowest
+    rank defines the job's time); identity on one process."""
+    if dist_mod is None:
+        return [float(v) for v in values]
+    import torch
+
+    tt = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist_mod.all_reduce(tt, op=dist_mod.ReduceOp.MAX)
+    return [float(v) for v in tt.tolist()]
+
+
+def aggregate_tokens_per_s(world_size: int, ms_per_step: float, tokens_per_step: int = 1) -> float:
+    """Whole-job throughput: every rank processes tokens_per_step per step."""
+    return world_size * tokens_per_step * 1e3 / ms_per_step
+
+
 def dist_setup():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -238,10 +261,11 @@ def run_ours(args, ws, rank, local):
     # NL distinct layers (~272 MB each): a step's weights were last touched
     # NL-1 steps earlier, far more than L2 holds, so they come from HBM.
     n_layers = args.layers
-    blocks = [native.MoeBlock(moe_layer_device(LAYER_SEED + 1000 * rank + l, dev), device=dev, topk=TOPK)
+    layer_seed, x_seed = replica_seeds(rank)
+    blocks = [native.MoeBlock(moe_layer_device(layer_seed + l, dev), device=dev, topk=TOPK)
               for l in range(n_layers)]
     n_total = args.warmup + args.steps
-    xs_host = torch.from_numpy(gen.fp16_normal(gen.rng(X_SEED + 100 * rank), (n_total, HIDDEN))).pin_memory()
+    xs_host = torch.from_numpy(gen.fp16_normal(gen.rng(x_seed), (n_total, HIDDEN))).pin_memory()
     xs = xs_host.to(dev)
     outs = torch.empty((n_total, HIDDEN), dtype=torch.float32, device=dev)
     ids_all = torch.empty((n_total, TOPK), dtype=torch.int32, device=dev)
@@ -350,11 +374,7 @@ def run_ours(args, ws, rank, local):
     clocks = clk.summary()
 
     # max over ranks
-    t_step, t_e2e = float(step_ms), float(e2e_ms)
-    if pg is not None:
-        tt = torch.tensor([t_step, t_e2e], device=dev)
-        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-        t_step, t_e2e = float(tt[0]), float(tt[1])
+    t_step, t_e2e = max_over_ranks([step_ms, e2e_ms], pg, dev)
     if rank != 0:
         if pg is not None:
             pg.destroy_process_group()
@@ -368,7 +388,7 @@ def run_ours(args, ws, rank, local):
     routed_code_bytes = TOPK * (GU_CODE_BYTES + DN_CODE_BYTES)
     distinct = len({tuple(r) for r in ids_all[args.warmup:args.warmup + 16].cpu().numpy().tolist()})
     line = {
-        "metric": METRIC, "value": ws * 1e3 / t_step, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "metric": METRIC, "value": aggregate_tokens_per_s(ws, t_step), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp16 weights / f32 accumulate", "data": "synthetic",
         "config": {"workload": WORKLOAD, "batch": 1, "tokens_per_step_per_gpu": 1,
@@ -397,7 +417,7 @@ def run_ours(args, ws, rank, local):
         "phase_ms": {"router": float(ph[0]), "gate_up+shared_gate_up": float(ph[1]),
                      "down+shared_down+combine": float(ph[2])},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
-        "e2e": {"value": ws * 1e3 / t_e2e, "unit": UNIT, "h2d_bytes_per_step": HIDDEN * 2,
+        "e2e": {"value": aggregate_tokens_per_s(ws, t_e2e), "unit": UNIT, "h2d_bytes_per_step": HIDDEN * 2,
                 "d2h_bytes_per_step": HIDDEN * 4,
                 "note": f"per group of {STEPS_PER_GRAPH} steps, one graph: pinned-host x in, the steps, "
                         f"outputs back to pinned host; all inside the timed region"},
