@@ -13,9 +13,10 @@
 //
 // Kernels: a prep kernel writes the activations as the MMA's B image (K-major,
 // 128-byte swizzled, every 64-value chunk holding all rows), then one CTA per
-// (128 outputs, 256 image rows) runs the warp-specialised tensor-core loop:
-// 8 warps convert int8 chunks into 4 shared-memory stages, a ninth issues the
-// B bulk copies three chunks ahead and the MMAs.
+// (256 outputs, 256 image rows) runs the warp-specialised tensor-core loop:
+// 8 warps convert int8 chunks into 3 shared-memory stages, a ninth issues the
+// B bulk copies two chunks ahead and two M = 128 MMAs per K step that share
+// the B chunk (so B, the re-read operand, comes from L2 once per 256 outputs).
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -28,6 +29,8 @@ namespace {
 
 constexpr int kDtF16 = 1, kDtBf16 = 2, kDtF32 = 3;
 constexpr int kRowsPerCta = 256;  // image rows (B rows) per CTA = MMA N at most
+constexpr int kOutPerCta = 256;   // output rows per CTA: two M = 128 tiles sharing each B chunk
+constexpr int kStages = 3;
 
 __host__ __device__ __forceinline__ int img_rows_for(int parts, int M) { return (parts * M + 7) & ~7; }
 
@@ -109,12 +112,13 @@ __global__ void __launch_bounds__(tc::kMlThreads + 32, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     constexpr uint32_t kBStage = kRowsPerCta * 128;
-    uint8_t* Abuf = smem;                                     // [4][16 KB]: 128 rows x 64 values, K-major
-    uint8_t* Bbuf = smem + tc::kWsStages * tc::kWsAStageBytes;  // [4][256 rows x 128 B]
+    constexpr int kAStage = 2 * tc::kWsAStageBytes;
+    uint8_t* Abuf = smem;                         // [3][2 tiles][16 KB]: 128 rows x 64 values, K-major
+    uint8_t* Bbuf = smem + kStages * kAStage;     // [3][256 rows x 128 B]
     __shared__ tc::WsBars bars;
     __shared__ uint32_t tmem_base;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n0 = blockIdx.x * 128;
+    const int n0 = blockIdx.x * kOutPerCta;
     const int R0 = blockIdx.y * kRowsPerCta;
 
     pdl_wait();  // the B image is complete
@@ -123,7 +127,7 @@ __global__ void __launch_bounds__(tc::kMlThreads + 32, 1)
     const int npad = (nrows + 15) & ~15;
     if (tid == 0) tc::ws_bars_init(bars);
     if (warp == 0) {
-        tc::tmem_alloc(&tmem_base, 256);
+        tc::tmem_alloc(&tmem_base, 512);  // two accumulators of 256 columns
         tc::tmem_relinquish();
     }
     tc::fence_before_sync();
@@ -141,43 +145,43 @@ __global__ void __launch_bounds__(tc::kMlThreads + 32, 1)
         y += (long long)blockIdx.z * M * N;
         y_stride = N;
     }
-    // producer thread t converts row t/2, values 32*(t%2) .. +31 of every
-    // 64-value chunk. Three register sets rotate: chunk c + 2 loads into one
-    // while chunk c is converted from another, so a load has two chunks of
-    // MMA time to arrive, and no set is ever copied (a copy would wait for
-    // the load).
-    const int r = (tid & 255) >> 1, h = tid & 1;
-    const int8_t* wrow = W + (long long)min(n0 + r, N - 1) * Kin + 32 * h + b_first * 128;
+    // producer thread t converts output row t of the CTA (M tile t / 128), all
+    // 64 values of every chunk. Three register sets rotate: chunk c + 2 loads
+    // into one while chunk c is converted from another, so a load has two
+    // chunks of MMA time to arrive, and no set is ever copied (a copy would
+    // wait for the load).
+    const int r = tid & 255;
+    const int8_t* wrow = W + (long long)min(n0 + r, N - 1) * Kin + b_first * 128;
     const int nch = 2 * nblk;
-    uint4 w0[2], w1[2], w2[2];
-    auto load = [&](uint4 (&w)[2], int c) {
+    uint4 w0[4], w1[4], w2[4];
+    auto load = [&](uint4 (&w)[4], int c) {
         if (c < nch) {
             const uint4* src = reinterpret_cast<const uint4*>(wrow + c * 64);
-            w[0] = __ldg(src);
-            w[1] = __ldg(src + 1);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) w[j] = __ldg(src + j);
         }
     };
     if (tid < tc::kMlThreads) {
         load(w0, 0);
         load(w1, 1);
     }
-    auto convert = [&](const uint4 (&w)[2], uint8_t* A) {
+    auto convert = [&](const uint4 (&w)[4], uint8_t* A) {
+        uint8_t* dst = A + (r >> 7) * tc::kWsAStageBytes;
+        const uint32_t rr = static_cast<uint32_t>(r & 127);
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
+        for (int j = 0; j < 4; ++j) {
             const uint2 x0 = i8x4_to_16<BF16>(w[j].x), x1 = i8x4_to_16<BF16>(w[j].y);
             const uint2 x2 = i8x4_to_16<BF16>(w[j].z), x3 = i8x4_to_16<BF16>(w[j].w);
-            const uint32_t k = 32u * h + 16u * j;
-            *reinterpret_cast<uint4*>(A + tc::kmajor_off(static_cast<uint32_t>(r), k)) =
-                make_uint4(x0.x, x0.y, x1.x, x1.y);
-            *reinterpret_cast<uint4*>(A + tc::kmajor_off(static_cast<uint32_t>(r), k + 8u)) =
-                make_uint4(x2.x, x2.y, x3.x, x3.y);
+            *reinterpret_cast<uint4*>(dst + tc::kmajor_off(rr, 16u * j)) = make_uint4(x0.x, x0.y, x1.x, x1.y);
+            *reinterpret_cast<uint4*>(dst + tc::kmajor_off(rr, 16u * j + 8u)) = make_uint4(x2.x, x2.y, x3.x, x3.y);
         }
     };
 
     int rot = 0;  // c % 3
-    const bool ok = tc::mma_mainloop_ws<4, false>(
+    const bool ok = tc::mma_mainloop_ws<kStages, false, 2>(
         Abuf, Bbuf, kBStage, img + (long long)R0 * 128 + 2ll * b_first * img_rows * 128, (long long)img_rows * 128,
-        static_cast<uint32_t>(nrows) * 128u, nch, tmem, idesc, bars, [&](int c, uint8_t* A) {
+        static_cast<uint32_t>(nrows) * 128u, nch, tmem, idesc, bars,
+        [&](int c, uint8_t* A) {
             if (rot == 0) {
                 load(w2, c + 2);
                 convert(w0, A);
@@ -189,18 +193,20 @@ __global__ void __launch_bounds__(tc::kMlThreads + 32, 1)
                 convert(w2, A);
             }
             rot = rot == 2 ? 0 : rot + 1;
-        });
+        },
+        256u);
 
-    // epilogue: TMEM lane = output row, column = image row; warps w and w + 4
-    // share lane quarter w % 4 and split the columns. A bounded wait that gave
-    // up leaves NaN in the CTA's outputs.
+    // epilogue: TMEM lane = output row of an M tile, column = image row;
+    // warps w (tile 0, columns 0..255) and w + 4 (tile 1, columns 256..511)
+    // share lane quarter w % 4. A bounded wait that gave up leaves NaN in the
+    // CTA's outputs.
     if (warp < 8) {
-        const int q = warp & 3;
-        const int n = n0 + 32 * q + lane;
+        const int q = warp & 3, mt = warp >> 2;
+        const int n = n0 + 128 * mt + 32 * q + lane;
         const float sc = !ok ? __int_as_float(0x7fc00000) : (n < N ? scales[n] : 0.f);
-        for (int c0 = 16 * (warp >> 2); c0 < npad; c0 += 32) {
+        for (int c0 = 0; c0 < npad; c0 += 16) {
             float v[16];
-            tc::tmem_ld16(tmem + (static_cast<uint32_t>(32 * q) << 16) + c0, v);
+            tc::tmem_ld16(tmem + (static_cast<uint32_t>(32 * q) << 16) + 256u * mt + c0, v);
             tc::tmem_ld_wait();
             if (n >= N) continue;
             if constexpr (PARTS == 1) {
@@ -220,7 +226,7 @@ __global__ void __launch_bounds__(tc::kMlThreads + 32, 1)
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tmem, 256);
+    if (warp == 0) tc::tmem_dealloc(tmem, 512);
 }
 
 // y[m][n] = sum over the splits z (in order) of part[z][m][n]; four
@@ -254,7 +260,7 @@ __global__ void __launch_bounds__(256) int8_split_reduce_kernel(const float* __r
 template <bool BF16, int PARTS>
 cudaError_t launch_gemm(const int8_t* W, const float* scales, int N, int Kin, const uint8_t* img, int img_rows, int M,
                         float* y, long long y_stride, float* part, cudaStream_t s) {
-    const int smem = tc::kWsStages * (tc::kWsAStageBytes + kRowsPerCta * 128) + 1024;
+    const int smem = kStages * (2 * tc::kWsAStageBytes + kRowsPerCta * 128) + 1024;
     const void* f = reinterpret_cast<const void*>(int8_gemm_kernel<BF16, PARTS>);
     cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -263,7 +269,7 @@ cudaError_t launch_gemm(const int8_t* W, const float* scales, int N, int Kin, co
     const int ks = (nblk + bps - 1) / bps;  // every split starts inside K
     float* out = ks > 1 ? part : y;
     void* args[] = {&W, &scales, &N, &Kin, &img, &img_rows, &M, &out, &y_stride, &bps};
-    e = launch_kernel(f, dim3((N + 127) / 128, (img_rows + kRowsPerCta - 1) / kRowsPerCta, ks),
+    e = launch_kernel(f, dim3((N + kOutPerCta - 1) / kOutPerCta, (img_rows + kRowsPerCta - 1) / kRowsPerCta, ks),
                       dim3(tc::kMlThreads + 32), smem, true, s, args);
     if (e != cudaSuccess || ks == 1) return e;
     int ks_ = ks;
@@ -280,7 +286,8 @@ cudaError_t launch_gemm(const int8_t* W, const float* scales, int N, int Kin, co
 // two 128-value blocks per split, at most 8 splits. A fixed function of the
 // shape, so results do not depend on the device.
 int int8_gemm_ksplit(int N, int Kin, int M, int parts) {
-    const long long tiles = (long long)((N + 127) / 128) * ((img_rows_for(parts, M) + kRowsPerCta - 1) / kRowsPerCta);
+    const long long tiles =
+        (long long)((N + kOutPerCta - 1) / kOutPerCta) * ((img_rows_for(parts, M) + kRowsPerCta - 1) / kRowsPerCta);
     const int nblk = Kin / 128;
     if (tiles >= 48) return 1;  // most SMs busy already; a split would cost more in partial traffic
     int ks = static_cast<int>((152 + tiles - 1) / tiles);

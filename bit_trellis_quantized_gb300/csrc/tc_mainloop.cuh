@@ -207,12 +207,18 @@ __device__ __forceinline__ void ws_bars_init(WsBars& bars) {
     fence_proxy_async_smem();
 }
 
-template <int STAGES, bool A_MN, class ProduceChunk>
+//
+// MT = 2: two 128-row M tiles share each B chunk (A stage 2 x 16 KB, tile t at
+// +16 KB), accumulating into TMEM columns [t * acc_cols, ...): the B operand is
+// read from L2 once per 256 rows of A instead of once per 128.
+template <int STAGES, bool A_MN, int MT = 1, class ProduceChunk>
 __device__ __forceinline__ bool mma_mainloop_ws(uint8_t* Abuf, uint8_t* Bbuf, uint32_t b_stage_bytes,
                                                 const uint8_t* img, long long img_chunk_bytes, uint32_t copy_bytes,
                                                 int nch, uint32_t tmem, uint32_t idesc, WsBars& bars,
-                                                ProduceChunk&& produce) {
-    static_assert(STAGES == 2 || STAGES == 4, "2 or 4 stages");
+                                                ProduceChunk&& produce, uint32_t acc_cols = 0) {
+    static_assert(STAGES >= 2 && STAGES <= kWsStages, "2 to 4 stages");
+    static_assert(MT == 1 || MT == 2, "one or two M tiles");
+    constexpr int kAStage = MT * kWsAStageBytes;
     const int tid = threadIdx.x;
     bool ok = true;
     if (tid < kMlThreads) {
@@ -220,7 +226,7 @@ __device__ __forceinline__ bool mma_mainloop_ws(uint8_t* Abuf, uint8_t* Bbuf, ui
             const int s = c % STAGES;
             if (c >= STAGES && !mbar_wait_parity_bounded(smem_addr(&bars.done[s]), ((c / STAGES) - 1) & 1))
                 ok = false;
-            produce(c, Abuf + s * kWsAStageBytes);
+            produce(c, Abuf + s * kAStage);
             fence_proxy_async_smem();
             mbar_arrive_cta(smem_addr(&bars.a_full[s]));
         }
@@ -238,12 +244,17 @@ __device__ __forceinline__ bool mma_mainloop_ws(uint8_t* Abuf, uint8_t* Bbuf, ui
             if (!mbar_wait_parity_bounded(smem_addr(&bars.a_full[s]), ph)) ok = false;
             if (!mbar_wait_parity_bounded(smem_addr(&bars.b_full[s]), ph)) ok = false;
             fence_after_sync();
-            const uint32_t a0 = smem_addr(Abuf + s * kWsAStageBytes), b0 = smem_addr(Bbuf + s * b_stage_bytes);
+            const uint32_t a0 = smem_addr(Abuf + s * kAStage), b0 = smem_addr(Bbuf + s * b_stage_bytes);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t ad = A_MN ? smem_desc(a0 + kk * 4096u, 2048u, 1024u, kSwizzle128B)
-                                         : smem_desc(a0 + kk * 32u, 16u, 1024u, kSwizzle128B);
-                mma_f16(tmem, ad, smem_desc(b0 + kk * 32u, 16u, 1024u, kSwizzle128B), idesc, c > 0 || kk > 0);
+                const uint64_t bd = smem_desc(b0 + kk * 32u, 16u, 1024u, kSwizzle128B);
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    const uint32_t at = a0 + mt * kWsAStageBytes;
+                    const uint64_t ad = A_MN ? smem_desc(at + kk * 4096u, 2048u, 1024u, kSwizzle128B)
+                                             : smem_desc(at + kk * 32u, 16u, 1024u, kSwizzle128B);
+                    mma_f16(tmem + mt * acc_cols, ad, bd, idesc, c > 0 || kk > 0);
+                }
             }
             commit(smem_addr(&bars.done[s]));
             if (c + STAGES - 1 < nch) {
