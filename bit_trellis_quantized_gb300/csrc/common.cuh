@@ -33,12 +33,15 @@ __device__ __forceinline__ __half cb_decode_h(uint32_t s) {
 __device__ __forceinline__ float cb_decode_f(uint32_t s) { return __half2float(cb_decode_h(s)); }
 
 // Two decodes packed as one half2 (a in .x, b in .y).
+// Each state's two halves are added by their own fp16 add (round to nearest
+// even, like the pairwise form) and the sums packed: measured faster on GB300
+// than gathering the low and the high halves first (fewer byte permutes on
+// the integer pipe, which the decode saturates).
 __device__ __forceinline__ __half2 cb_decode_h2(uint32_t sa, uint32_t sb) {
     const uint32_t ra = ((sa * kCbMul) & kCbMask) ^ kCbXor;
     const uint32_t rb = ((sb * kCbMul) & kCbMask) ^ kCbXor;
-    const uint32_t lo = __byte_perm(ra, rb, 0x5410);  // (ra.lo, rb.lo)
-    const uint32_t hi = __byte_perm(ra, rb, 0x7632);  // (ra.hi, rb.hi)
-    return __hadd2(*reinterpret_cast<const __half2*>(&lo), *reinterpret_cast<const __half2*>(&hi));
+    const __half2 a2 = *reinterpret_cast<const __half2*>(&ra), b2 = *reinterpret_cast<const __half2*>(&rb);
+    return __halves2half2(__hadd(__low2half(a2), __high2half(a2)), __hadd(__low2half(b2), __high2half(b2)));
 }
 
 // ---------------------------------------------------------------------------

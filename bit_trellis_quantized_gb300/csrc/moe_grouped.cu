@@ -368,7 +368,7 @@ __device__ __forceinline__ void decode_half_row_to_smem(const HalfRowCodes<K>& l
 // next block's B. Shared memory (2 x 16 KB A + 2 x 2 cap x 128 B B) stays
 // under 100 KB for every item size, so two CTAs share an SM and one's
 // prologue and epilogue overlap the other's decode.
-template <int K>
+template <int K, int STAGES>
 __global__ void __launch_bounds__(tc::kMlThreads + 32, 2)
     moe_grouped_gemm_kernel(const MoeArgs a, const GroupedProj p) {
     constexpr int kThreads = tc::kMlThreads + 32, kDecodeWarps = tc::kMlThreads / 32;
@@ -376,8 +376,8 @@ __global__ void __launch_bounds__(tc::kMlThreads + 32, 2)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int cap = a.grp_cap;
     const uint32_t b_chunk = 256u * static_cast<uint32_t>(cap);  // 2*cap rows x 128 B
-    uint8_t* Abuf = smem;                                         // [2][16 KB]
-    uint8_t* Bbuf = smem + 2 * 16384;                             // [2][b_chunk]
+    uint8_t* Abuf = smem;                                         // [STAGES][16 KB]
+    uint8_t* Bbuf = smem + STAGES * 16384;                        // [STAGES][b_chunk]
     float* zs = reinterpret_cast<float*>(smem);                   // epilogue: [cap][128] f32 over A and B
     __shared__ tc::WsBars bars;
     __shared__ uint32_t tmem_base;
@@ -430,7 +430,7 @@ __global__ void __launch_bounds__(tc::kMlThreads + 32, 2)
     const int nbr = (lane & ~7) | ((lane + 1) & 7);
     const uint8_t* img = a.grp_img + (long long)desc.z * 128;
 
-    const bool ok = tc::mma_mainloop_ws<2, true>(
+    const bool ok = tc::mma_mainloop_ws<STAGES, true>(
         Abuf, Bbuf, b_chunk, img, (long long)a.grp_img_rows * 128, 256u * static_cast<uint32_t>(nt4), nblk, tmem,
         idesc, bars, [&](int b, uint8_t* A) {
             const bool more = b + 2 < nblk;
@@ -576,8 +576,12 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeArgs a, const
 
 template <int K>
 cudaError_t launch_grouped(const MoeArgs& a, const GroupedProj& p, cudaStream_t s) {
-    const int smem = 2 * 16384 + 2 * 256 * a.grp_cap + 1024;
-    const void* f = reinterpret_cast<const void*>(moe_grouped_gemm_kernel<K>);
+    // three stages where shared memory keeps the same CTAs per SM (items of up
+    // to 64 tokens), two for 128-token items
+    const int stages = a.grp_cap <= 64 ? 3 : 2;
+    const int smem = stages * (16384 + 256 * a.grp_cap) + 1024;
+    const void* f = stages == 3 ? reinterpret_cast<const void*>(moe_grouped_gemm_kernel<K, 3>)
+                                : reinterpret_cast<const void*>(moe_grouped_gemm_kernel<K, 2>);
     cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     void* args[] = {const_cast<MoeArgs*>(&a), const_cast<GroupedProj*>(&p)};
