@@ -59,16 +59,23 @@ __device__ __forceinline__ void load_lane_codes(LaneCodes<K>& lc, const uint16_t
 // over its 4 input rows. Half-row j (input row j/2, output columns
 // 8*(j%2)..+7) starts at bit 8*K*j of the lane's words and its weight m at
 // bit 8*K*j + K*m; all offsets are compile-time constants.
+// Weights are decoded in pairs (m, m+1): measured faster on GB300 than one at
+// a time (fewer integer-pipe instructions); every accumulator still receives
+// its weights in the same order, so the sums are unchanged.
 template <int K, int NB>
 __device__ __forceinline__ void decode_fma(const LaneCodes<K>& lc, const float (&xr)[NB][4], float (&acc)[NB][16]) {
-    static_for<64>([&](auto I) {
-        constexpr int j = decltype(I)::value / 8;
-        constexpr int m = decltype(I)::value % 8;
-        constexpr int b = 8 * K * j + K * m;
-        const uint32_t s = window_state<(b & 15)>(stream_window<(b >> 4)>(lc.p));
-        const float wv = cb_decode_f(s);
+    static_for<32>([&](auto I) {
+        constexpr int j = (2 * decltype(I)::value) / 8;
+        constexpr int m = (2 * decltype(I)::value) % 8;
+        constexpr int b0 = 8 * K * j + K * m, b1 = b0 + K;
+        const uint32_t s0 = window_state<(b0 & 15)>(stream_window<(b0 >> 4)>(lc.p));
+        const uint32_t s1 = window_state<(b1 & 15)>(stream_window<(b1 >> 4)>(lc.p));
+        const float2 w = __half22float2(cb_decode_h2(s0, s1));
 #pragma unroll
-        for (int t = 0; t < NB; ++t) acc[t][8 * (j & 1) + m] = fmaf(wv, xr[t][j >> 1], acc[t][8 * (j & 1) + m]);
+        for (int t = 0; t < NB; ++t) {
+            acc[t][8 * (j & 1) + m] = fmaf(w.x, xr[t][j >> 1], acc[t][8 * (j & 1) + m]);
+            acc[t][8 * (j & 1) + m + 1] = fmaf(w.y, xr[t][j >> 1], acc[t][8 * (j & 1) + m + 1]);
+        }
     });
 }
 
