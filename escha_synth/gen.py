@@ -16,7 +16,10 @@ Recipes:
   gate half and the up half;
 * router weights: N(0, 0.02) in fp16; shared-expert gate: N(0, 0.02) fp16;
 * int8 weights: uniform integers in [-127, 127]; per-row f32 scales
-  U(1e-3, 1e-2); bf16 activations N(0, 1).
+  U(1e-3, 1e-2); bf16 activations N(0, 1);
+* dense projections: the trellis recipe above for one weight, plus an f32
+  output bias N(0, 8^2) (large enough to be seen next to outputs of
+  magnitude ~sqrt(in)).
 """
 from __future__ import annotations
 
@@ -29,6 +32,7 @@ __all__ = [
     "rout_vector",
     "fp16_normal",
     "projection",
+    "dense_projection",
     "moe_layer",
     "int8_matrix",
     "bf16_normal_bits",
@@ -86,6 +90,20 @@ def projection(seed: int, n_in: int, n_out: int, K: int, prune_rate: float = 0.5
     prune = prune_count(prune_rate, n_out // 2 if glu else n_out) if prune_rate else 0
     rout = rout_vector(g, n_out, prune=prune, glu=glu)
     return {"codes": codes, "x": x, "rin": rin, "rout": rout, "K": K}
+
+
+def dense_projection(seed: int, n_in: int, n_out: int, K: int, M: int, prune_rate: float = 0.0,
+                     bias: bool = True):
+    """One dense projection for M tokens: codes (kt-major), x [M][n_in] fp16,
+    rin, rout (``prune_rate`` of the output channels zeroed), and an f32
+    output bias [n_out] (None without ``bias``)."""
+    g = rng(seed)
+    codes = trellis_codes(g, n_in, n_out, K)
+    x = fp16_normal(g, (M, n_in))
+    rin = signs(g, n_in)
+    rout = rout_vector(g, n_out, prune=prune_count(prune_rate, n_out), glu=False)
+    b = (g.standard_normal(size=n_out) * 8.0).astype(np.float32) if bias else None
+    return {"codes": codes, "x": x, "rin": rin, "rout": rout, "bias": b, "K": K}
 
 
 def moe_layer(seed: int, hidden: int = 2048, inter: int = 512, n_experts: int = 256, k_gu: int = 3,

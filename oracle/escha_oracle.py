@@ -246,6 +246,55 @@ def trellis_gemv(codes, x, rin, rout, W=None) -> np.ndarray:
 
 
 # ----------------------------------------------------------------------------
+# Dense linear. hipfire PR #694: a dense projection is the one-expert case of
+# the expert GEMV (commit "EschaProj holds what a trellis weight needs"); the
+# dense export adds a per-projection output bias at the point where each
+# projection's result is complete, before SwiGLU for gate/up (commit adding
+# the escha dense export's biases in decode and prefill); the checkpoint's
+# kt-major tile grid may be moved at load to nt-major, whole tiles, contents
+# untouched (commit on the nt-major tile grid).
+# ----------------------------------------------------------------------------
+
+
+def codes_to_nt_major(codes) -> np.ndarray:
+    """[in/16][out/16][16K] -> [out/16][in/16][16K]: tile (kt, nt) moves to
+    position (nt, kt); its words are not changed."""
+    c = np.asarray(codes)
+    KT, NT, L = c.shape
+    out = np.empty((NT, KT, L), dtype=c.dtype)
+    for kt in range(KT):
+        for nt in range(NT):
+            out[nt, kt] = c[kt, nt]
+    return out
+
+
+def codes_from_nt_major(codes_nt) -> np.ndarray:
+    """Inverse of ``codes_to_nt_major``."""
+    c = np.asarray(codes_nt)
+    NT, KT, L = c.shape
+    out = np.empty((KT, NT, L), dtype=c.dtype)
+    for nt in range(NT):
+        for kt in range(KT):
+            out[kt, nt] = c[nt, kt]
+    return out
+
+
+def dense_linear(codes, x, rin, rout, bias=None, nt_major: bool = False, W=None) -> np.ndarray:
+    """y[m] = rout * H(W^T H(rin * x[m])) + bias for each token m.
+
+    ``codes`` is kt-major, or nt-major with ``nt_major`` (then the grid is
+    moved back before decoding). ``bias`` (length out) is added after the
+    output transform, i.e. after rout, so a pruned channel (rout = 0) yields
+    exactly its bias."""
+    if W is None:
+        W = decode_weights(codes_from_nt_major(codes) if nt_major else codes)
+    y = trellis_gemv(None, x, rin, rout, W=W)
+    if bias is not None:
+        y = y + np.asarray(bias, dtype=np.float64)
+    return y
+
+
+# ----------------------------------------------------------------------------
 # Router. Logits are rounded to f16 before top-k (hipfire PR #694, commit
 # "Executed the moeblk golden against real shipped layer-0 weights"), which is
 # what makes exact ties possible. Softmax over all experts renormalised over

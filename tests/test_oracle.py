@@ -290,6 +290,74 @@ def test_nan_weight_behind_zero_activation_propagates():
     assert np.all(np.isnan(y))
 
 
+# ------------------------------------------------------------ dense linear ---
+
+
+@pytest.mark.parametrize("K", [2, 3])
+def test_nt_major_makes_consecutive_kt_adjacent(K):
+    """In the nt-major grid the tiles of one output tile column are stored
+    one after another: flat tile index nt * KT + kt holds tile (kt, nt)."""
+    KT, NT = 5, 3
+    codes = np.zeros((KT, NT, 16 * K), dtype=np.uint16)
+    for kt in range(KT):
+        for nt in range(NT):
+            codes[kt, nt, :] = 1000 * kt + 10 * nt + np.arange(16 * K)
+    t = o.codes_to_nt_major(codes)
+    flat = t.reshape(-1, 16 * K)
+    for kt in range(KT):
+        for nt in range(NT):
+            assert np.array_equal(flat[nt * KT + kt], codes[kt, nt])
+    assert np.array_equal(o.codes_from_nt_major(t), codes)
+
+
+@pytest.mark.parametrize("K", [2, 3])
+def test_nt_major_decodes_to_identical_weights(K):
+    """Whole tiles move, so the decoded weights of both grids are identical."""
+    codes = gen.trellis_codes(gen.rng(40 + K), 128, 256, K)
+    nt = o.codes_to_nt_major(codes)
+    x = gen.rng(41).standard_normal((2, 128))
+    rin = np.ones(128)
+    rout = np.ones(256)
+    assert np.array_equal(o.dense_linear(nt, x, rin, rout, nt_major=True), o.dense_linear(codes, x, rin, rout))
+
+
+def test_dense_bias_lands_after_the_output_transform():
+    """x = 0 gives exactly the bias, and a pruned channel (rout = 0) gives
+    exactly its bias for any x; a bias added before the output Hadamard or
+    before the rout multiply would spread over or vanish from those channels."""
+    g = gen.rng(42)
+    codes = gen.trellis_codes(g, 256, 384, 2)
+    rin = np.where(g.integers(0, 2, 256) == 1, 1.0, -1.0)
+    rout = g.uniform(0.5, 1.5, 384)
+    rout[[0, 17, 300]] = 0.0
+    bias = g.standard_normal(384) * 8
+    y0 = o.dense_linear(codes, np.zeros((1, 256)), rin, rout, bias=bias)
+    assert np.array_equal(y0[0], bias)
+    x = g.standard_normal((3, 256))
+    y = o.dense_linear(codes, x, rin, rout, bias=bias)
+    assert np.all(y[:, [0, 17, 300]] == bias[[0, 17, 300]])
+    live = rout != 0
+    assert np.all(np.abs(y[:, live] - bias[live]) > 0)
+
+
+def test_dense_closed_form_constant_weights_with_bias():
+    """Constant weights c: y = rout * sqrt(128) * c * sqrt(128) * sum_b v[128 b]
+    at the first channel of each output block, 0 elsewhere, plus the bias."""
+    K, n_in, n_out = 3, 256, 256
+    codes = np.full((n_in // 16, n_out // 16, 16 * K), 0xFFFF, dtype=np.uint16)
+    c = float(o.f16_to_f64(o.codebook_f16(np.array([0xFFFF])))[0])
+    g = gen.rng(43)
+    x = g.standard_normal(n_in)
+    rin = np.where(g.integers(0, 2, n_in) == 1, 1.0, -1.0)
+    rout = g.uniform(0.5, 1.5, n_out)
+    bias = g.standard_normal(n_out)
+    v = rin * x
+    want = bias.copy()
+    want[::128] += rout[::128] * 128.0 * c * v[::128].sum()
+    got = o.dense_linear(o.codes_to_nt_major(codes), x, rin, rout, bias=bias, nt_major=True)
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-9)
+
+
 def test_swiglu_gate_is_first_half():
     y = np.array([2.0, 3.0])
     assert o.swiglu(y)[0] == pytest.approx(2.0 / (1 + math.exp(-2.0)) * 3.0)
