@@ -458,7 +458,8 @@ def _time_graph(torch, stream, fn, reps: int, warm: int = 3) -> float:
 def extended(dev, blocks, hbm, tflops):
     """The other workloads of the benchmark's configuration list, each with
     inputs larger than L2 (distinct weights cycled) unless stated:
-    single projection at batch 1, the MoE block at batch 64 / 256 and a
+    single projection at batch 1, the dense 5120 x 17408 linear at M = 1..2048,
+    the MoE block at batch 64 / 256 and a
     2048-token prefill chunk, the int8 w8a16 shapes at M = 1 and 2048, and
     the 40-block stack at batch 1 / 8 / 128 and a 2048-token chunk."""
     import torch
@@ -481,6 +482,34 @@ def extended(dev, blocks, hbm, tflops):
                                                "frac_of_hbm": b / (ms * 1e-3) / 1e9 / hbm,
                                                "l2": f"{P} distinct projections ({P * b >> 20} MB) cycled"}
     del pj, y
+
+    # dense trellis linear 5120 -> 17408, K = 2 (a 27B-class gate_proj) with an
+    # output bias: 8 distinct weights (178 MB packed) cycled; kt-major and
+    # nt-major grids at M = 1, nt-major at M = 8, 64 and 2048
+    n_in, n_out, nw = 5120, 17408, 8
+    g = torch.Generator(device=dev).manual_seed(7101)
+    codes = torch.randint(-32768, 32768, (nw, n_in // 16, n_out // 16, 32), dtype=torch.int16, device=dev,
+                          generator=g)
+    rin = (torch.randint(0, 2, (n_in,), device=dev, generator=g) * 2 - 1).to(torch.float16)
+    rout = ((torch.rand(n_out, device=dev, generator=g) + 0.5)
+            * (torch.randint(0, 2, (n_out,), device=dev, generator=g) * 2 - 1)).to(torch.float16)
+    bias = torch.randn(n_out, device=dev, generator=g) * 8
+    dn = {}
+    packed = n_in * n_out * 2 // 8
+    for nt_major, Ms in ((False, (1,)), (True, (1, 8, 64, 2048))):
+        lins = [native.DenseLinear(codes[i], rin, rout, bias=bias, nt_major=nt_major) for i in range(nw)]
+        for M in Ms:
+            x = torch.randn((M, n_in), device=dev).to(torch.float16)
+            y = torch.empty((M, n_out), dtype=torch.float32, device=dev)
+            ws = torch.empty(lins[0].workspace_bytes(M), dtype=torch.uint8, device=dev)
+            ms = _time_graph(torch, stream, lambda i: lins[i % nw](x, y=y, ws=ws), reps=nw)
+            dn[f"{'nt' if nt_major else 'kt'}_major_m{M}"] = {
+                "us": ms * 1e3, "tokens_per_s": M / (ms * 1e-3), "packed_gbs": packed / (ms * 1e-3) / 1e9,
+                "weight_fmas_per_s": float(M) * n_in * n_out / (ms * 1e-3)}
+        del lins
+    res["dense_linear_5120x17408_k2_bias"] = dn
+    del codes
+    torch.cuda.empty_cache()
 
     # MoE block at batch 64 / 256 / 2048 over the headline's layers, fresh x per call
     nl = len(blocks)
@@ -542,7 +571,7 @@ def extended(dev, blocks, hbm, tflops):
 
 
 PROFILE_CASES = ("block_b1", "block_b8", "block_b64", "block_b256", "prefill_2048", "projection_b1",
-                 "int8_m1", "int8_m2048")
+                 "int8_m1", "int8_m2048", "dense_m1", "dense_m2048")
 
 
 def profile_case(name: str, reps: int):
@@ -568,6 +597,17 @@ def profile_case(name: str, reps: int):
         for i in range(reps):
             native.trellis_gemv(pj["codes"][i % 64], pj["x"][i % 64:i % 64 + 1], pj["rin"][i % 64],
                                 pj["rout"][i % 64], y=y[i % 64:i % 64 + 1])
+    elif name.startswith("dense_"):
+        M = 1 if name == "dense_m1" else 2048
+        n_in, n_out = 5120, 17408
+        codes = torch.randint(-32768, 32768, (n_in // 16, n_out // 16, 32), dtype=torch.int16, device=dev)
+        rin = (torch.randint(0, 2, (n_in,), device=dev) * 2 - 1).to(torch.float16)
+        rout = (torch.rand(n_out, device=dev) + 0.5).to(torch.float16)
+        lin = native.DenseLinear(codes, rin, rout, bias=torch.randn(n_out, device=dev), nt_major=True)
+        x = torch.randn((M, n_in), device=dev).to(torch.float16)
+        y = torch.empty((M, n_out), dtype=torch.float32, device=dev)
+        for i in range(reps):
+            lin(x, y=y)
     else:
         M = 1 if name == "int8_m1" else 2048
         W = torch.randint(-127, 128, (4096, 2048), dtype=torch.int8, device=dev)

@@ -45,7 +45,32 @@ __global__ void trellis_decode_kernel(const uint16_t* __restrict__ codes, int KT
     *reinterpret_cast<uint4*>(dst) = v;
 }
 
+// Load-time move of whole tiles from the kt-major grid [in/16][out/16] to the
+// nt-major grid [out/16][in/16], so that the tiles one output tile column
+// walks through are adjacent (hipfire PR #694, commit on the nt-major tile
+// grid). Tile contents are untouched. One thread per 16-byte piece of a
+// destination tile (2K pieces of 16 bytes per tile), in destination order.
+__global__ void codes_to_nt_major_kernel(const uint4* __restrict__ src, int KT, int NT, int pieces, uint4* __restrict__ dst) {
+    const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long total = (long long)KT * NT * pieces;
+    if (gid >= total) return;
+    const long long tile_d = gid / pieces;
+    const int c = static_cast<int>(gid % pieces);
+    const long long nt = tile_d / KT, kt = tile_d % KT;
+    dst[gid] = src[(kt * NT + nt) * pieces + c];
+}
+
 }  // namespace
+
+cudaError_t launch_codes_to_nt_major(const uint16_t* src, int in, int out, int K, uint16_t* dst, cudaStream_t s) {
+    const int KT = in / 16, NT = out / 16, pieces = 2 * K;
+    const long long total = (long long)KT * NT * pieces;
+    if (total == 0) return cudaSuccess;
+    const int threads = 256;
+    codes_to_nt_major_kernel<<<static_cast<unsigned>((total + threads - 1) / threads), threads, 0, s>>>(
+        reinterpret_cast<const uint4*>(src), KT, NT, pieces, reinterpret_cast<uint4*>(dst));
+    return cudaGetLastError();
+}
 
 cudaError_t launch_trellis_decode(const uint16_t* codes, int in, int out, int K, uint16_t* W, cudaStream_t s) {
     const int KT = in / 16, NT = out / 16;

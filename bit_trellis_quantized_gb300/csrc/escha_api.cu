@@ -76,6 +76,34 @@ int check_trellis(const uint16_t* codes, int in, int out, int K, int mult, const
     return ESCHA_OK;
 }
 
+// Dense linear: up to kDenseGemvMaxM tokens run the per-token fused GEMV
+// (weights decoded once per 1, 2 or 4 tokens); more tokens run the grouped
+// tensor-core GEMM with all tokens in one group, in items of dense_cap(M).
+constexpr int kDenseGemvMaxM = 12;
+constexpr int kDenseMaxM = 65536;
+
+int dense_cap(int M) {
+    int cap = 16;
+    while (cap < escha::kGrpCapMax && cap < M) cap *= 2;
+    return cap;
+}
+
+struct DenseWs {
+    size_t err, img, total;
+    int img_rows;
+};
+
+// Status word, then (grouped GEMM only) the B image: in/64 chunks of
+// 2 * round_up(M, 4) rows of 128 bytes.
+DenseWs dense_ws_layout(int in, int M) {
+    DenseWs w{};
+    w.err = 0;
+    w.img = 256;
+    w.img_rows = M > kDenseGemvMaxM ? 2 * ((M + 3) & ~3) : 0;
+    w.total = w.img + align_up((size_t)(in / 64) * w.img_rows * 128);
+    return w;
+}
+
 // Workspace layout of escha_moe_block (256-byte aligned regions).
 // int8 w8a16 product of M tokens: the tensor-core GEMM from kInt8GemmMinM
 // tokens on (when Kin allows it and an image buffer is given), else the GEMV.
@@ -214,6 +242,88 @@ int escha_trellis_gemv(const uint16_t* codes, int in, int out, int K, const void
     const int items = (batch + nb - 1) / nb;
     return cuda_status(escha::launch_trellis_gemv(a, K, nb, items, sms, static_cast<cudaStream_t>(stream)),
                        "trellis_gemv launch");
+}
+
+int escha_codes_to_nt_major(const uint16_t* codes, int in, int out, int K, uint16_t* dst, void* stream) {
+    int r = check_trellis(codes, in, out, K, 16, "codes_to_nt_major");
+    if (r) return r;
+    if (!dst) return fail(ESCHA_E_ARG, "codes_to_nt_major: dst is null");
+    if (!aligned16(dst)) return fail(ESCHA_E_ALIGN, "codes_to_nt_major: dst not 16-byte aligned");
+    const size_t bytes = (size_t)in * out * K * 2 / 16;  // 16 K words per 256 weights
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(codes), b0 = reinterpret_cast<uintptr_t>(dst);
+    if (a0 < b0 + bytes && b0 < a0 + bytes) return fail(ESCHA_E_ARG, "codes_to_nt_major: dst overlaps codes");
+    int sms;
+    if ((r = device_check(&sms))) return r;
+    return cuda_status(escha::launch_codes_to_nt_major(codes, in, out, K, dst, static_cast<cudaStream_t>(stream)),
+                       "codes_to_nt_major launch");
+}
+
+size_t escha_dense_linear_workspace(int in, int out, int K, int M) {
+    (void)out;
+    (void)K;
+    if (in <= 0 || M <= 0) return 0;
+    const DenseWs w = dense_ws_layout(in, M);
+    return w.total;
+}
+
+int escha_dense_linear(const uint16_t* codes, int in, int out, int K, int nt_major, const void* x, int x_dtype, int M,
+                       const uint16_t* rin, const uint16_t* rout, const float* bias, float* y, void* ws,
+                       size_t ws_bytes, void* stream) {
+    int r = check_trellis(codes, in, out, K, 128, "dense_linear");
+    if (r) return r;
+    if (in > 65536) return fail(ESCHA_E_SHAPE, "dense_linear: in=%d above 65536", in);
+    if (nt_major != 0 && nt_major != 1) return fail(ESCHA_E_ARG, "dense_linear: nt_major=%d must be 0 or 1", nt_major);
+    if (!x || !rin || !rout || !y || !ws) return fail(ESCHA_E_ARG, "dense_linear: null x / rin / rout / y / ws");
+    if (x_dtype != ESCHA_F16 && x_dtype != ESCHA_F32)
+        return fail(ESCHA_E_ARG, "dense_linear: x_dtype=%d must be ESCHA_F16 or ESCHA_F32", x_dtype);
+    if (M < 1 || M > kDenseMaxM) return fail(ESCHA_E_ARG, "dense_linear: M=%d outside [1, %d]", M, kDenseMaxM);
+    if (!aligned16(x) || !aligned16(rin) || !aligned16(rout) || !aligned16(y) || !aligned16(ws) ||
+        (bias && !aligned16(bias)))
+        return fail(ESCHA_E_ALIGN, "dense_linear: x / rin / rout / bias / y / ws not 16-byte aligned");
+    const DenseWs w = dense_ws_layout(in, M);
+    if (ws_bytes < w.total) return fail(ESCHA_E_WORKSPACE, "dense_linear: workspace too small");
+    int sms;
+    if ((r = device_check(&sms))) return r;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* base = static_cast<char*>(ws);
+    int* err = reinterpret_cast<int*>(base + w.err);
+    if ((r = cuda_status(cudaMemsetAsync(err, 0, sizeof(int), s), "dense_linear status reset"))) return r;
+    if (M <= kDenseGemvMaxM) {
+        escha::GemvArgs a{};
+        a.codes = codes;
+        a.in = in;
+        a.out = out;
+        a.x_mode = x_dtype == ESCHA_F16 ? escha::kXmF16 : escha::kXmF32;
+        a.x = x;
+        a.x_stride = in;
+        a.rin = rin;
+        a.rout = rout;
+        a.y = y;
+        a.y_stride = out;
+        a.batch = M;
+        a.nt_major = nt_major;
+        a.bias = bias;
+        const int nb = M == 1 ? 1 : M == 2 ? 2 : 4;
+        return cuda_status(escha::launch_trellis_gemv(a, K, nb, (M + nb - 1) / nb, sms, s), "dense_linear gemv launch");
+    }
+    escha::DenseArgs d{};
+    d.codes = codes;
+    d.in = in;
+    d.out = out;
+    d.K = K;
+    d.nt_major = nt_major;
+    d.x = x;
+    d.x_f32 = x_dtype == ESCHA_F32;
+    d.M = M;
+    d.cap = dense_cap(M);
+    d.rin = rin;
+    d.rout = rout;
+    d.bias = bias;
+    d.y = y;
+    d.img = reinterpret_cast<uint8_t*>(base + w.img);
+    d.img_rows = w.img_rows;
+    d.err = err;
+    return cuda_status(escha::launch_dense_grouped(d, s), "dense_linear grouped launch");
 }
 
 size_t escha_moe_block_workspace(const escha_moe_layer* L, int T) {

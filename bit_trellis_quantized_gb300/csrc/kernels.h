@@ -23,6 +23,8 @@ struct GemvArgs {
     float* y;
     long long y_stride;
     int batch;
+    int nt_major;        // code tiles stored [out/16][in/16] (else [in/16][out/16])
+    const float* bias;   // f32 [out] added after the output transform, or null
 };
 
 // Trellis GEMV of one projection for `batch` tokens, nb tokens per CTA
@@ -121,6 +123,28 @@ GroupPlan group_plan(int T, int topk, int E, int hidden, int inter, int sh_inter
 cudaError_t launch_moe_topk_group(const MoeArgs& a, cudaStream_t s);
 // top-k, grouping, grouped gate_up and down GEMMs (down output d [T*topk][hidden]).
 cudaError_t launch_moe_grouped(const MoeArgs& a, float* d, int num_sms, cudaStream_t s);
+// Dense trellis linear on the grouped tensor-core GEMM: one expert, tokens in
+// order, items of `cap` tokens; the B image (img, img_rows rows per 64-input
+// chunk, img_rows >= 2 * round_up(M, 4)) is written by the prep kernel.
+struct DenseArgs {
+    const uint16_t* codes;
+    int in, out, K, nt_major;
+    const void* x;  // [M][in] fp16 or f32
+    int x_f32;
+    int M, cap;
+    const uint16_t* rin;
+    const uint16_t* rout;
+    const float* bias;  // [out] or null
+    float* y;           // [M][out]
+    uint8_t* img;
+    int img_rows;
+    int* err;
+};
+cudaError_t launch_dense_grouped(const DenseArgs& d, cudaStream_t s);
+
+// Whole-tile transpose of a code tensor: [in/16][out/16] tiles -> [out/16][in/16].
+cudaError_t launch_codes_to_nt_major(const uint16_t* src, int in, int out, int K, uint16_t* dst, cudaStream_t s);
+
 // out = sum_j w * d + sigmoid(gate) * sh
 cudaError_t launch_moe_combine(const MoeArgs& a, const float* d, cudaStream_t s);
 

@@ -288,7 +288,8 @@ __device__ void gate_up_routed(const MoeArgs& a, float* smem) {
     const int e = e_s[j];
     const uint16_t* codes = a.gu_codes + (long long)e * KT * NT * (16 * K);
     LaneCodes<K> cur;
-    if (kt0 + warp < kt1) load_lane_codes<K>(cur, codes + ((long long)(kt0 + warp) * NT + ob * 8) * (16 * K), lane);
+    const TileStrides grid{NT, 1};  // experts are stored kt-major
+    if (kt0 + warp < kt1) load_lane_codes<K>(cur, codes, grid, kt0 + warp, ob * 8, lane);
 
     // xt = H128(rin_e * x[t]) over this CTA's inputs
     const uint16_t* rin = a.gu_rin + (long long)e * a.hidden;
@@ -309,7 +310,7 @@ __device__ void gate_up_routed(const MoeArgs& a, float* smem) {
     if (crank == 0 && warp == 0)
         rout_pre = *reinterpret_cast<const uint2*>(a.gu_rout + (long long)e * n_out + ob * 128 + 4 * lane);
     float* zp = crank == 0 ? slots : red + kGuWarps * 128;  // rank 0 keeps its partial in slot 0
-    cta_gemv_partial<K, 1, kGuWarps>(codes, NT, ob, kt0, kt1, xt, nk, cur, red, zp);
+    cta_gemv_partial<K, 1, kGuWarps>(codes, grid, ob, kt0, kt1, xt, nk, cur, red, zp);
 
     cluster_wait();
     if (crank != 0) {
@@ -406,7 +407,8 @@ __global__ void __launch_bounds__(kDnThreads, 3) moe_down_kernel(const MoeArgs a
     const int nk = rows_h * 16;
     const uint16_t* codes = a.dn_codes + (long long)e * KT * NT * (16 * K);
     LaneCodes<K> cur;
-    if (kt0 + warp < kt1) load_lane_codes<K>(cur, codes + ((long long)(kt0 + warp) * NT + ob * 8) * (16 * K), lane);
+    const TileStrides grid{NT, 1};  // experts are stored kt-major
+    if (kt0 + warp < kt1) load_lane_codes<K>(cur, codes, grid, kt0 + warp, ob * 8, lane);
     const uint16_t* rin = a.dn_rin + (long long)e * a.inter;
     uint2 rin_pre = make_uint2(0u, 0u);
     if (warp < nk / 128) rin_pre = *reinterpret_cast<const uint2*>(rin + kt0 * 16 + warp * 128 + 4 * lane);
@@ -459,7 +461,7 @@ __global__ void __launch_bounds__(kDnThreads, 3) moe_down_kernel(const MoeArgs a
     if (rank == 0 && warp < a.topk)
         rout_pre = *reinterpret_cast<const uint2*>(a.dn_rout + (long long)e_s[warp] * a.hidden + ob * 128 + 4 * lane);
     float* zp = rank == 0 ? slots : red + kDnWarps * 128;
-    cta_gemv_partial<K, 1, kDnWarps>(codes, NT, ob, kt0, kt1, xt, nk, cur, red, zp);
+    cta_gemv_partial<K, 1, kDnWarps>(codes, grid, ob, kt0, kt1, xt, nk, cur, red, zp);
 
     // shared expert rows: xt <- SwiGLU(shgu[t]); the values go to rank 0's
     // shres (directly on rank 0, through distributed shared memory elsewhere)

@@ -198,12 +198,15 @@ __global__ void __launch_bounds__(1024, 1) moe_group_kernel(const MoeArgs a) {
 // 3. prep: the B image of one projection
 // ---------------------------------------------------------------------------
 struct GroupedProj {
-    const uint16_t* codes;  // [E][in/16][out/16][16K]
+    const uint16_t* codes;  // [E] x tile grid of [in/16][out/16] (kt-major) or [out/16][in/16] tiles of 16K words
     const uint16_t* rin;    // [E][in]
     const uint16_t* rout;   // [E][out]
     int in, out;
-    int mode;               // 0: input = x[token] (fp16); 1: input = SwiGLU(ygu[slot])
+    int mode;               // 0: input = x[token] (fp16); 1: input = SwiGLU(ygu[slot]); 2: input = xf[token] (f32)
     float* y;               // [slots][out]
+    TileStrides grid;       // tile grid of one expert's codes
+    const float* bias;      // f32 [out] added after the output transform, or null
+    const float* xf;        // mode 2: f32 input [T][in]
 };
 
 // One warp per (slot, 4 consecutive 128-input blocks): 8 lanes per block, 16
@@ -222,15 +225,26 @@ __global__ void __launch_bounds__(256) moe_prep_kernel(const MoeArgs a, const Gr
     const int b = static_cast<int>(task % ngrp) * 4 + (lane >> 3);
     const int l8 = lane & 7;
     const bool live = b < nblk;  // lanes of a block past the input still join the shuffles
-    const int e = a.ids[s];
-    const int P = a.grp_ppos[s];
+    // a dense linear (no ids) is one expert with the tokens in order
+    const int e = a.ids ? a.ids[s] : 0;
+    const int P = a.grp_ppos ? a.grp_ppos[s] : s;
     const int ib = b * 128 + 16 * l8;
     float v[16];
     if (live) {
         const uint4* rp = reinterpret_cast<const uint4*>(p.rin + (long long)e * p.in + ib);
         const uint4 r0 = rp[0], r1 = rp[1];
         const uint32_t rw[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-        if (p.mode == 0) {
+        if (p.mode == 2) {
+            const float4* xp = reinterpret_cast<const float4*>(p.xf + (long long)(s / a.topk) * p.in + ib);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 f = xp[q];
+                v[4 * q] = f.x;
+                v[4 * q + 1] = f.y;
+                v[4 * q + 2] = f.z;
+                v[4 * q + 3] = f.w;
+            }
+        } else if (p.mode == 0) {
             const uint4* xp = reinterpret_cast<const uint4*>(a.x + (long long)(s / a.topk) * a.hidden + ib);
             const uint4 x0 = xp[0], x1 = xp[1];
             const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
@@ -318,10 +332,13 @@ struct HalfRowCodes {
     uint32_t p[K + 1];
 };
 
-// base4: the first 16-bit word of the warp's 4 tiles (K * 16 words each).
+// Tile row kt, tile columns nt0 .. nt0 + 3 of a code tensor with tile grid g;
+// the lane reads tile nt0 + lane/8.
 template <int K>
-__device__ __forceinline__ void load_half_row(HalfRowCodes<K>& lc, const uint16_t* base4, int lane) {
-    const uint16_t* b = base4 + (lane >> 3) * (16 * K) + (lane & 7) * (2 * K);
+__device__ __forceinline__ void load_half_row(HalfRowCodes<K>& lc, const uint16_t* codes, const TileStrides& g, int kt,
+                                              int nt0, int lane) {
+    const uint16_t* b = codes + ((long long)kt * g.s_kt + (long long)(nt0 + (lane >> 3)) * g.s_nt) * (16 * K) +
+                        (lane & 7) * (2 * K);
     if constexpr (K == 2) {
         const uint2 v = ldg_stream_v2(b);  // 8-byte aligned: 64 B per tile, 8 B per lane
         lc.p[0] = v.x;
@@ -391,14 +408,21 @@ __global__ void __launch_bounds__(tc::kMlThreads + 32, 2)
     // the item's descriptor is loaded together with the item count (entries
     // past the count are never used), so one round trip gives everything the
     // CTA needs to start its other loads
-    const int nitems = *a.grp_nitems;
-    const int4 desc = a.grp_items[item];
+    int nitems;
+    int4 desc;
+    if (a.grp_items) {
+        nitems = *a.grp_nitems;
+        desc = a.grp_items[item];
+    } else {  // dense linear: one expert, items of cap tokens in token order
+        nitems = (a.T + cap - 1) / cap;
+        desc = make_int4(0, min(cap, a.T - item * cap), 2 * item * cap, item * cap);
+    }
     if (item >= nitems) return;
     const int e = desc.x, nt = desc.y;
     const uint2 rb = *reinterpret_cast<const uint2*>(p.rout + (long long)e * p.out + ob * 128 + 4 * lane);
     const int npad = (2 * nt + 15) & ~15;  // MMA N: hi/lo rows of nt tokens, multiple of 16
     const int nt4 = (nt + 3) & ~3;          // rows copied: whole 8-row atoms
-    for (int i = tid; i < nt; i += kThreads) slot_s[i] = a.grp_perm[desc.w + i];
+    for (int i = tid; i < nt; i += kThreads) slot_s[i] = a.grp_perm ? a.grp_perm[desc.w + i] : desc.w + i;
     const uint32_t tcols = 2u * static_cast<uint32_t>(cap) < 32u ? 32u : 2u * static_cast<uint32_t>(cap);
     if (tid == 0) tc::ws_bars_init(bars);
     if (warp == 0) {
@@ -415,16 +439,14 @@ __global__ void __launch_bounds__(tc::kMlThreads + 32, 2)
     const uint16_t* codes = p.codes + (long long)e * KT * NT * (16 * K);
     const int nblk = p.in >> 6;  // blocks of 64 inputs = 4 tile rows
     const int hr = warp >> 1, half = warp & 1;
-    // the warp's 4 tiles of tile row 4b + hr
-    auto row4 = [&](int b) { return codes + ((long long)(4 * b + hr) * NT + ob * 8 + 4 * half) * (16 * K); };
     // three register sets used in turn: block b + 2's codes load into one
     // while block b is decoded from another, so a load has two blocks of
     // decode time to arrive; no set is ever copied (a copy would wait for the
     // load)
     HalfRowCodes<K> c0, c1, c2;
     if (warp < kDecodeWarps) {
-        load_half_row<K>(c0, row4(0), lane);
-        if (nblk > 1) load_half_row<K>(c1, row4(1), lane);
+        load_half_row<K>(c0, codes, p.grid, hr, ob * 8 + 4 * half, lane);
+        if (nblk > 1) load_half_row<K>(c1, codes, p.grid, 4 + hr, ob * 8 + 4 * half, lane);
     }
     int rot = 0;  // b % 3
     const int nbr = (lane & ~7) | ((lane + 1) & 7);
@@ -436,15 +458,15 @@ __global__ void __launch_bounds__(tc::kMlThreads + 32, 2)
             const bool more = b + 2 < nblk;
             uint8_t* slice = A + hr * 4096;
             if (rot == 0) {
-                if (more) load_half_row<K>(c2, row4(b + 2), lane);
+                if (more) load_half_row<K>(c2, codes, p.grid, 4 * (b + 2) + hr, ob * 8 + 4 * half, lane);
                 c0.p[K] = __shfl_sync(0xffffffffu, c0.p[0], nbr) & 0xFFFFu;
                 decode_half_row_to_smem<K>(c0, slice, lane, 4 * half);
             } else if (rot == 1) {
-                if (more) load_half_row<K>(c0, row4(b + 2), lane);
+                if (more) load_half_row<K>(c0, codes, p.grid, 4 * (b + 2) + hr, ob * 8 + 4 * half, lane);
                 c1.p[K] = __shfl_sync(0xffffffffu, c1.p[0], nbr) & 0xFFFFu;
                 decode_half_row_to_smem<K>(c1, slice, lane, 4 * half);
             } else {
-                if (more) load_half_row<K>(c1, row4(b + 2), lane);
+                if (more) load_half_row<K>(c1, codes, p.grid, 4 * (b + 2) + hr, ob * 8 + 4 * half, lane);
                 c2.p[K] = __shfl_sync(0xffffffffu, c2.p[0], nbr) & 0xFFFFu;
                 decode_half_row_to_smem<K>(c2, slice, lane, 4 * half);
             }
@@ -475,6 +497,13 @@ __global__ void __launch_bounds__(tc::kMlThreads + 32, 2)
         const float4 z4 = *reinterpret_cast<const float4*>(zs + i * 128 + 4 * lane);
         float v[4] = {z4.x * 256.f, z4.y * 256.f, z4.z * 256.f, z4.w * 256.f};  // undo the 2^-8 prescale (exact)
         output_transform_regs(v, rb, lane);
+        if (p.bias) {  // additive output bias, after the output transform
+            const float4 b4 = *reinterpret_cast<const float4*>(p.bias + ob * 128 + 4 * lane);
+            v[0] += b4.x;
+            v[1] += b4.y;
+            v[2] += b4.z;
+            v[3] += b4.w;
+        }
         *reinterpret_cast<float4*>(p.y + (long long)slot_s[i] * p.out + ob * 128 + 4 * lane) =
             make_float4(v[0], v[1], v[2], v[3]);
     }
@@ -643,13 +672,35 @@ cudaError_t launch_moe_grouped(const MoeArgs& a, float* d, int num_sms, cudaStre
     (void)num_sms;
     cudaError_t e = launch_moe_topk_group(a, s);
     if (e != cudaSuccess) return e;
-    const GroupedProj gu{a.gu_codes, a.gu_rin, a.gu_rout, a.hidden, 2 * a.inter, 0, a.ygu};
+    const GroupedProj gu{a.gu_codes, a.gu_rin, a.gu_rout, a.hidden, 2 * a.inter, 0, a.ygu,
+                         tile_strides(a.hidden, 2 * a.inter, false), nullptr, nullptr};
     if ((e = launch_prep(a, gu, s)) != cudaSuccess) return e;
     e = a.gu_K == 2 ? launch_grouped<2>(a, gu, s) : launch_grouped<3>(a, gu, s);
     if (e != cudaSuccess) return e;
-    const GroupedProj dn{a.dn_codes, a.dn_rin, a.dn_rout, a.inter, a.hidden, 1, d};
+    const GroupedProj dn{a.dn_codes, a.dn_rin, a.dn_rout, a.inter, a.hidden, 1, d,
+                         tile_strides(a.inter, a.hidden, false), nullptr, nullptr};
     if ((e = launch_prep(a, dn, s)) != cudaSuccess) return e;
     return a.dn_K == 2 ? launch_grouped<2>(a, dn, s) : launch_grouped<3>(a, dn, s);
+}
+
+cudaError_t launch_dense_grouped(const DenseArgs& d, cudaStream_t s) {
+    MoeArgs a{};
+    a.T = d.M;
+    a.topk = 1;
+    a.E = 1;
+    a.hidden = d.in;
+    a.x = static_cast<const uint16_t*>(d.x_f32 ? nullptr : d.x);
+    a.grp_cap = d.cap;
+    a.grp_img = d.img;
+    a.grp_img_rows = d.img_rows;
+    a.err = d.err;
+    const GroupedProj p{d.codes, d.rin, d.rout, d.in, d.out, d.x_f32 ? 2 : 0, d.y,
+                        tile_strides(d.in, d.out, d.nt_major != 0), d.bias,
+                        static_cast<const float*>(d.x_f32 ? d.x : nullptr)};
+    cudaError_t e = launch_prep(a, p, s);
+    if (e != cudaSuccess) return e;
+    a.grp_max_items = (d.M + d.cap - 1) / d.cap;
+    return d.K == 2 ? launch_grouped<2>(a, p, s) : launch_grouped<3>(a, p, s);
 }
 
 cudaError_t launch_moe_combine(const MoeArgs& a, const float* d, cudaStream_t s) {

@@ -31,18 +31,32 @@ struct LaneCodes {
     uint32_t p[2 * K + 1];  // word pairs; p[2K] low half receives the neighbour's first word
 };
 
-// The lane's 4K words of one tile row of an output block (row_base points at
-// the block's first tile in that row).
+// Tile grid of a code tensor: tile (kt, nt) starts at codes + (kt * s_kt +
+// nt * s_nt) * 16K words. kt-major (as checkpoints store it, [in/16][out/16]):
+// s_kt = out/16, s_nt = 1. nt-major (the load-time transpose that puts a tile
+// column's tiles next to each other, [out/16][in/16]): s_kt = 1, s_nt = in/16.
+struct TileStrides {
+    long long s_kt, s_nt;
+};
+
+__host__ __device__ inline TileStrides tile_strides(int in, int out, bool nt_major) {
+    return nt_major ? TileStrides{1, in / 16} : TileStrides{out / 16, 1};
+}
+
+// The lane's 4K words of tile row kt of the output block whose first tile
+// column is nt0: tile nt0 + lane/4, input rows 4*(lane%4) .. +3.
 template <int K>
-__device__ __forceinline__ void load_lane_codes(LaneCodes<K>& lc, const uint16_t* row_base, int lane) {
+__device__ __forceinline__ void load_lane_codes(LaneCodes<K>& lc, const uint16_t* codes, const TileStrides& g, int kt,
+                                                int nt0, int lane) {
+    const uint16_t* tile = codes + ((long long)kt * g.s_kt + (long long)(nt0 + (lane >> 2)) * g.s_nt) * (16 * K);
     if constexpr (K == 2) {
-        const uint4 v = ldg_stream_v4(row_base + lane * 8);
+        const uint4 v = ldg_stream_v4(tile + (lane & 3) * 8);
         lc.p[0] = v.x;
         lc.p[1] = v.y;
         lc.p[2] = v.z;
         lc.p[3] = v.w;
     } else {
-        const uint16_t* b = row_base + lane * 12;
+        const uint16_t* b = tile + (lane & 3) * 12;
         const uint2 v0 = ldg_stream_v2(b);
         const uint2 v1 = ldg_stream_v2(b + 4);
         const uint2 v2 = ldg_stream_v2(b + 8);
@@ -79,14 +93,14 @@ __device__ __forceinline__ void decode_fma(const LaneCodes<K>& lc, const float (
     });
 }
 
-// Main loop and in-CTA reduction. `codes` is the expert's code tensor,
-// `NT` its number of output tiles, `ob` the output block, rows kt0..kt1-1,
+// Main loop and in-CTA reduction. `codes` is the expert's code tensor, `g`
+// its tile grid, `ob` the output block, rows kt0..kt1-1,
 // `xt` the transformed inputs [NB][nk] of those rows (smem), `first` the
 // lane's codes of its first row (already loaded). Writes the CTA's partial
 // sums zp[NB][128] (smem). `red` is smem scratch of NW*NB*128 floats.
 // Ends with __syncthreads().
 template <int K, int NB, int NW>
-__device__ __forceinline__ void cta_gemv_partial(const uint16_t* codes, int NT, int ob, int kt0, int kt1,
+__device__ __forceinline__ void cta_gemv_partial(const uint16_t* codes, const TileStrides& g, int ob, int kt0, int kt1,
                                                  const float* xt, int nk, LaneCodes<K>& cur, float* red,
                                                  float* zp) {
     const int warp = threadIdx.x >> 5;
@@ -118,10 +132,10 @@ __device__ __forceinline__ void cta_gemv_partial(const uint16_t* codes, int NT, 
     LaneCodes<K> nxt;
     for (int kt = kt0 + warp; kt < kt1; kt += 2 * NW) {
         const bool more1 = kt + NW < kt1;
-        if (more1) load_lane_codes<K>(nxt, codes + ((long long)(kt + NW) * NT + ob * 8) * (16 * K), lane);
+        if (more1) load_lane_codes<K>(nxt, codes, g, kt + NW, ob * 8, lane);
         step(cur, kt);
         if (!more1) break;
-        if (kt + 2 * NW < kt1) load_lane_codes<K>(cur, codes + ((long long)(kt + 2 * NW) * NT + ob * 8) * (16 * K), lane);
+        if (kt + 2 * NW < kt1) load_lane_codes<K>(cur, codes, g, kt + 2 * NW, ob * 8, lane);
         step(nxt, kt + NW);
     }
 

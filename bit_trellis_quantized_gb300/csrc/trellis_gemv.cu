@@ -66,7 +66,6 @@ __global__ void __launch_bounds__(kThreads, 2) trellis_gemv_kernel(const GemvArg
     const int ntok = min(NB, a.batch - row0);
 
     const int KT = a.in >> 4;
-    const int NT = a.out >> 4;
     const int kt0 = crank * a.kt_per_cta;
     const int kt1 = min(KT, kt0 + a.kt_per_cta);
     const int nk = (kt1 - kt0) * 16;
@@ -76,12 +75,13 @@ __global__ void __launch_bounds__(kThreads, 2) trellis_gemv_kernel(const GemvArg
     float* red = xt + NB * a.kt_per_cta * 16;    // [kWarps][NB][128]
     float* zp = red + kWarps * NB * 128;         // [NB][128]
 
+    const TileStrides grid = tile_strides(a.in, a.out, a.nt_major != 0);
     LaneCodes<K> cur;
-    if (kt0 + warp < kt1) load_lane_codes<K>(cur, a.codes + ((long long)(kt0 + warp) * NT + ob * 8) * (16 * K), lane);
+    if (kt0 + warp < kt1) load_lane_codes<K>(cur, a.codes, grid, kt0 + warp, ob * 8, lane);
     pdl_wait();  // x may be the previous launch's output
     gemv_input_transform<NB, XM>(a, row0, ntok, kt0 * 16, nk, xt, warp, lane);
     __syncthreads();
-    cta_gemv_partial<K, NB, kWarps>(a.codes, NT, ob, kt0, kt1, xt, nk, cur, red, zp);
+    cta_gemv_partial<K, NB, kWarps>(a.codes, grid, ob, kt0, kt1, xt, nk, cur, red, zp);
     // The next launch on the stream may start now; it prefetches its own codes
     // and waits for this grid before it reads activations or writes outputs.
     pdl_trigger();
@@ -98,6 +98,13 @@ __global__ void __launch_bounds__(kThreads, 2) trellis_gemv_kernel(const GemvArg
             v[3] += z4.w;
         }
         output_transform_warp(v, a.rout + ob * 128, lane);
+        if (a.bias) {  // additive output bias, after the output transform
+            const float4 b4 = *reinterpret_cast<const float4*>(a.bias + ob * 128 + 4 * lane);
+            v[0] += b4.x;
+            v[1] += b4.y;
+            v[2] += b4.z;
+            v[3] += b4.w;
+        }
         *reinterpret_cast<float4*>(a.y + (long long)(row0 + t) * a.y_stride + ob * 128 + 4 * lane) =
             make_float4(v[0], v[1], v[2], v[3]);
     }

@@ -35,6 +35,9 @@ EXPORTS = [
     "escha_trellis_decode",
     "escha_trellis_gemv_workspace",
     "escha_trellis_gemv",
+    "escha_codes_to_nt_major",
+    "escha_dense_linear_workspace",
+    "escha_dense_linear",
     "escha_moe_block_workspace",
     "escha_moe_block",
     "escha_moe_block_timed",
@@ -98,6 +101,12 @@ def lib() -> ctypes.CDLL:
         L.escha_trellis_gemv_workspace.restype = _sz
         L.escha_trellis_gemv.argtypes = [_vp, _i, _i, _i, _vp, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]
         L.escha_trellis_gemv.restype = _i
+        L.escha_codes_to_nt_major.argtypes = [_vp, _i, _i, _i, _vp, _vp]
+        L.escha_codes_to_nt_major.restype = _i
+        L.escha_dense_linear_workspace.argtypes = [_i, _i, _i, _i]
+        L.escha_dense_linear_workspace.restype = _sz
+        L.escha_dense_linear.argtypes = [_vp, _i, _i, _i, _i, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+        L.escha_dense_linear.restype = _i
         L.escha_moe_block_workspace.argtypes = [ctypes.POINTER(EschaMoeLayer), _i]
         L.escha_moe_block_workspace.restype = _sz
         L.escha_moe_block.argtypes = [ctypes.POINTER(EschaMoeLayer), _vp, _i, _vp, _vp, _vp, _vp, _sz, _vp]
@@ -190,6 +199,59 @@ def trellis_gemv(codes, x, rin, rout, y=None, stream=None) -> torch.Tensor:
     check(lib().escha_trellis_gemv(ptr(codes), n_in, n_out, L // 16, ptr(x), _dtype_tag(x), batch, ptr(rin),
                                    ptr(rout), ptr(y), None, 0, stream_handle(stream)))
     return y
+
+
+def codes_to_nt_major(codes: torch.Tensor, stream=None) -> torch.Tensor:
+    """Whole-tile transpose of a code tensor [in/16][out/16][16K] to the
+    nt-major grid [out/16][in/16][16K] (a load-time step)."""
+    _need_cuda(codes)
+    KT, NT, L = codes.shape
+    dst = torch.empty((NT, KT, L), dtype=codes.dtype, device=codes.device)
+    check(lib().escha_codes_to_nt_major(ptr(codes), KT * 16, NT * 16, L // 16, ptr(dst), stream_handle(stream)))
+    return dst
+
+
+class DenseLinear:
+    """One trellis-coded dense projection y = rout * H(W^T H(rin * x)) + bias.
+
+    ``codes`` is the stored kt-major tensor [in/16][out/16][16K]; with
+    ``nt_major=True`` it is transposed once here and the kernels walk the
+    nt-major grid. ``bias`` (f32 [out]) is optional."""
+
+    def __init__(self, codes, rin, rout, bias=None, nt_major: bool = True, stream=None):
+        _need_cuda(codes, rin, rout)
+        KT, NT, L = codes.shape
+        self.n_in, self.n_out, self.K = KT * 16, NT * 16, L // 16
+        self.nt_major = bool(nt_major)
+        self.codes = codes_to_nt_major(codes, stream) if self.nt_major else codes
+        self.rin, self.rout = rin, rout
+        self.bias = bias.contiguous() if bias is not None else None
+        self._ws = None
+
+    def workspace_bytes(self, M: int) -> int:
+        return lib().escha_dense_linear_workspace(self.n_in, self.n_out, self.K, M)
+
+    def __call__(self, x, y=None, ws=None, stream=None) -> torch.Tensor:
+        if x.dim() == 1:
+            x = x.unsqueeze(0)
+        _need_cuda(x)
+        M = x.shape[0]
+        if y is None:
+            y = torch.empty((M, self.n_out), dtype=torch.float32, device=x.device)
+        nbytes = self.workspace_bytes(M)
+        if ws is None:
+            if self._ws is None or self._ws.numel() < nbytes:
+                self._ws = torch.empty(nbytes, dtype=torch.uint8, device=x.device)
+            ws = self._ws
+        check(lib().escha_dense_linear(ptr(self.codes), self.n_in, self.n_out, self.K, int(self.nt_major), ptr(x),
+                                       _dtype_tag(x), M, ptr(self.rin), ptr(self.rout),
+                                       ptr(self.bias) if self.bias is not None else None, ptr(y), ptr(ws),
+                                       ws.numel(), stream_handle(stream)))
+        return y
+
+    def status(self) -> int:
+        """The status word of the last call (0: every bounded wait completed)."""
+        return int(self._ws[:4].view(torch.int32).item()) if self._ws is not None else 0
 
 
 def int8_w8a16_matvec(W, scales, x, y=None, stream=None) -> torch.Tensor:

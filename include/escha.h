@@ -106,6 +106,52 @@ int escha_trellis_gemv(const uint16_t* codes, int in, int out, int K, const void
                        const uint16_t* rin, const uint16_t* rout, float* y, void* ws, size_t ws_bytes,
                        void* stream);
 
+/* ---- tile-grid transpose (load time) --------------------------------------
+ * Moves whole tiles of a code tensor from the stored kt-major grid
+ * [in/16][out/16][16*K] to the nt-major grid [out/16][in/16][16*K], so the
+ * tiles that one output tile column walks through sit next to each other
+ * [PR694 commit on the nt-major tile grid: transposed at load, payload kept
+ * verbatim, tile contents untouched, every decoded weight identical].
+ *   codes  uint16 source, dst uint16 destination of the same size; the two
+ *          must not overlap (ESCHA_E_ARG). Both caller-owned, 16-byte aligned.
+ *   in,out multiples of 16;  K in {2, 3}
+ * Errors: ESCHA_E_ARG, ESCHA_E_SHAPE, ESCHA_E_K, ESCHA_E_ALIGN, ESCHA_E_CUDA,
+ *         ESCHA_E_DEVICE. */
+int escha_codes_to_nt_major(const uint16_t* codes, int in, int out, int K, uint16_t* dst, void* stream);
+
+/* ---- dense trellis linear ---------------------------------------------------
+ * y[m] = rout * H(W^T H(rin * x[m])) + bias for m < M: one dense projection
+ * served as the one-expert case of the expert kernels [PR694 commits
+ * "EschaProj holds what a trellis weight needs" (one expert, ids all zero)
+ * and on batched prefill grouping all slots of a dense linear into a single
+ * group, so each weight is read once per batch rather than once per slot].
+ * The bias is the dense export's additive per-projection output bias [PR694
+ * commit adding the escha dense export's biases in decode and prefill]: it is
+ * added after the output transform, so for gate/up it lands before any
+ * activation the caller applies, and for down/o_proj it may equally be added
+ * onto the residual afterwards.
+ * M <= 12 runs the fused per-token decode GEMV (weights decoded once per 1,
+ * 2 or 4 tokens); M >= 13 writes an fp16 hi/lo image of H(rin * x) and runs
+ * the tcgen05 tensor-core GEMM with all tokens in one group (weights decoded
+ * once per 16..128 tokens). Accumulation is fp32 on both routes.
+ *   codes    uint16, kt-major [in/16][out/16][16*K] (nt_major = 0) or
+ *            nt-major [out/16][in/16][16*K] (nt_major = 1, see
+ *            escha_codes_to_nt_major); K in {2, 3}
+ *   in,out   multiples of 128, in <= 65536
+ *   x        [M][in], x_dtype ESCHA_F16 or ESCHA_F32;  1 <= M <= 65536
+ *   rin      fp16 [in];  rout fp16 [out];  bias f32 [out] or NULL
+ *   y        f32 [M][out] output
+ *   ws       escha_dense_linear_workspace(in, out, K, M) bytes, caller-owned;
+ *            its first 4 bytes are a status word, set to 0 by the call and
+ *            non-zero if a kernel gave up a bounded wait (outputs invalid).
+ * All pointers 16-byte aligned. Errors: ESCHA_E_ARG, ESCHA_E_SHAPE,
+ * ESCHA_E_K, ESCHA_E_ALIGN, ESCHA_E_WORKSPACE, ESCHA_E_CUDA, ESCHA_E_DEVICE;
+ * on error nothing is enqueued. */
+size_t escha_dense_linear_workspace(int in, int out, int K, int M);
+int escha_dense_linear(const uint16_t* codes, int in, int out, int K, int nt_major, const void* x, int x_dtype, int M,
+                       const uint16_t* rin, const uint16_t* rout, const float* bias, float* y, void* ws,
+                       size_t ws_bytes, void* stream);
+
 /* ---- one MoE block ------------------------------------------------------
  * For each token b of x [T][hidden] (fp16):
  *   logits = f16(x[b] . Wg[e]) for every expert e (f32 sums in a fixed
