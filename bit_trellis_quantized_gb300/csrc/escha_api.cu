@@ -76,11 +76,18 @@ int check_trellis(const uint16_t* codes, int in, int out, int K, int mult, const
     return ESCHA_OK;
 }
 
-// Dense linear: up to kDenseGemvMaxM tokens run the per-token fused GEMV
-// (weights decoded once per 1, 2 or 4 tokens); more tokens run the grouped
-// tensor-core GEMM with all tokens in one group, in items of dense_cap(M).
+// Dense linear: the per-token fused GEMV decodes the weights once per 1, 2 or
+// 4 tokens; the grouped tensor-core GEMM decodes them once per item of
+// dense_cap(M) tokens but has a fixed cost of its own (the B image, a second
+// launch, TMEM). Measured on GB300 (5120 x 6144 .. 17408 x 5120), the GEMV is
+// faster up to 2 tokens, and up to 12 tokens for weights of at most 2^23
+// values; the GEMM from there on.
 constexpr int kDenseGemvMaxM = 12;
 constexpr int kDenseMaxM = 65536;
+
+bool dense_uses_gemv(int in, int out, int M) {
+    return M <= 2 || (M <= kDenseGemvMaxM && (long long)in * out <= (1ll << 23));
+}
 
 int dense_cap(int M) {
     int cap = 16;
@@ -89,18 +96,21 @@ int dense_cap(int M) {
 }
 
 struct DenseWs {
-    size_t err, img, total;
-    int img_rows;
+    size_t err, img, part, total;
+    int img_rows, splits;
 };
 
-// Status word, then (grouped GEMM only) the B image: in/64 chunks of
-// 2 * round_up(M, 4) rows of 128 bytes.
-DenseWs dense_ws_layout(int in, int M) {
+// Status word, then (grouped GEMM only) the B image, in/64 chunks of
+// 2 * round_up(M, 4) rows of 128 bytes, and the K split partial sums.
+DenseWs dense_ws_layout(int in, int out, int M) {
     DenseWs w{};
     w.err = 0;
     w.img = 256;
-    w.img_rows = M > kDenseGemvMaxM ? 2 * ((M + 3) & ~3) : 0;
-    w.total = w.img + align_up((size_t)(in / 64) * w.img_rows * 128);
+    const bool gemm = !dense_uses_gemv(in, out, M);
+    w.img_rows = gemm ? 2 * ((M + 3) & ~3) : 0;
+    w.splits = gemm ? escha::dense_ksplit(in, out, M, dense_cap(M)) : 1;
+    w.part = w.img + align_up((size_t)(in / 64) * w.img_rows * 128);
+    w.total = w.part + (w.splits > 1 ? align_up((size_t)w.splits * M * out * 4) : 0);
     return w;
 }
 
@@ -259,10 +269,9 @@ int escha_codes_to_nt_major(const uint16_t* codes, int in, int out, int K, uint1
 }
 
 size_t escha_dense_linear_workspace(int in, int out, int K, int M) {
-    (void)out;
     (void)K;
-    if (in <= 0 || M <= 0) return 0;
-    const DenseWs w = dense_ws_layout(in, M);
+    if (in <= 0 || out <= 0 || M <= 0) return 0;
+    const DenseWs w = dense_ws_layout(in, out, M);
     return w.total;
 }
 
@@ -280,7 +289,7 @@ int escha_dense_linear(const uint16_t* codes, int in, int out, int K, int nt_maj
     if (!aligned16(x) || !aligned16(rin) || !aligned16(rout) || !aligned16(y) || !aligned16(ws) ||
         (bias && !aligned16(bias)))
         return fail(ESCHA_E_ALIGN, "dense_linear: x / rin / rout / bias / y / ws not 16-byte aligned");
-    const DenseWs w = dense_ws_layout(in, M);
+    const DenseWs w = dense_ws_layout(in, out, M);
     if (ws_bytes < w.total) return fail(ESCHA_E_WORKSPACE, "dense_linear: workspace too small");
     int sms;
     if ((r = device_check(&sms))) return r;
@@ -288,7 +297,7 @@ int escha_dense_linear(const uint16_t* codes, int in, int out, int K, int nt_maj
     char* base = static_cast<char*>(ws);
     int* err = reinterpret_cast<int*>(base + w.err);
     if ((r = cuda_status(cudaMemsetAsync(err, 0, sizeof(int), s), "dense_linear status reset"))) return r;
-    if (M <= kDenseGemvMaxM) {
+    if (dense_uses_gemv(in, out, M)) {
         escha::GemvArgs a{};
         a.codes = codes;
         a.in = in;
@@ -322,6 +331,8 @@ int escha_dense_linear(const uint16_t* codes, int in, int out, int K, int nt_maj
     d.y = y;
     d.img = reinterpret_cast<uint8_t*>(base + w.img);
     d.img_rows = w.img_rows;
+    d.splits = w.splits;
+    d.part = reinterpret_cast<float*>(base + w.part);
     d.err = err;
     return cuda_status(escha::launch_dense_grouped(d, s), "dense_linear grouped launch");
 }

@@ -283,13 +283,14 @@ cudaError_t launch_gemm(const int8_t* W, const float* scales, int N, int Kin, co
 }  // namespace
 
 // K splits of the GEMM: enough CTAs for about one wave of 152 SMs, at least
-// two 128-value blocks per split, at most 8 splits. A fixed function of the
-// shape, so results do not depend on the device.
+// two 128-value blocks per split, at most 8 splits. From 48 tiles on, a
+// split of two is taken only while the doubled grid still fits one wave.
+// A fixed function of the shape, so results do not depend on the device.
 int int8_gemm_ksplit(int N, int Kin, int M, int parts) {
     const long long tiles =
         (long long)((N + kOutPerCta - 1) / kOutPerCta) * ((img_rows_for(parts, M) + kRowsPerCta - 1) / kRowsPerCta);
     const int nblk = Kin / 128;
-    if (tiles >= 48) return 1;  // most SMs busy already; a split would cost more in partial traffic
+    if (tiles >= 48) return (2 * tiles <= 152 && nblk >= 4) ? 2 : 1;
     int ks = static_cast<int>((152 + tiles - 1) / tiles);
     ks = min(ks, max(1, nblk / 2));
     return min(ks, 8);

@@ -207,6 +207,8 @@ struct GroupedProj {
     TileStrides grid;       // tile grid of one expert's codes
     const float* bias;      // f32 [out] added after the output transform, or null
     const float* xf;        // mode 2: f32 input [T][in]
+    int kblk_per_split;     // 64-input blocks per K split (blockIdx.z); in/64 without a split
+    float* part;            // with K splits: f32 partial sums [splits][slots][out], else null
 };
 
 // One warp per (slot, 4 consecutive 128-input blocks): 8 lanes per block, 16
@@ -437,7 +439,8 @@ __global__ void __launch_bounds__(tc::kMlThreads + 32, 2)
 
     const int KT = p.in >> 4, NT = p.out >> 4;
     const uint16_t* codes = p.codes + (long long)e * KT * NT * (16 * K);
-    const int nblk = p.in >> 6;  // blocks of 64 inputs = 4 tile rows
+    const int kb0 = blockIdx.z * p.kblk_per_split;                // first 64-input block of this K split
+    const int nblk = min((p.in >> 6) - kb0, p.kblk_per_split);  // blocks of 64 inputs = 4 tile rows
     const int hr = warp >> 1, half = warp & 1;
     // three register sets used in turn: block b + 2's codes load into one
     // while block b is decoded from another, so a load has two blocks of
@@ -445,12 +448,12 @@ __global__ void __launch_bounds__(tc::kMlThreads + 32, 2)
     // load)
     HalfRowCodes<K> c0, c1, c2;
     if (warp < kDecodeWarps) {
-        load_half_row<K>(c0, codes, p.grid, hr, ob * 8 + 4 * half, lane);
-        if (nblk > 1) load_half_row<K>(c1, codes, p.grid, 4 + hr, ob * 8 + 4 * half, lane);
+        load_half_row<K>(c0, codes, p.grid, 4 * kb0 + hr, ob * 8 + 4 * half, lane);
+        if (nblk > 1) load_half_row<K>(c1, codes, p.grid, 4 * (kb0 + 1) + hr, ob * 8 + 4 * half, lane);
     }
     int rot = 0;  // b % 3
     const int nbr = (lane & ~7) | ((lane + 1) & 7);
-    const uint8_t* img = a.grp_img + (long long)desc.z * 128;
+    const uint8_t* img = a.grp_img + (long long)desc.z * 128 + (long long)kb0 * a.grp_img_rows * 128;
 
     const bool ok = tc::mma_mainloop_ws<STAGES, true>(
         Abuf, Bbuf, b_chunk, img, (long long)a.grp_img_rows * 128, 256u * static_cast<uint32_t>(nt4), nblk, tmem,
@@ -458,15 +461,15 @@ __global__ void __launch_bounds__(tc::kMlThreads + 32, 2)
             const bool more = b + 2 < nblk;
             uint8_t* slice = A + hr * 4096;
             if (rot == 0) {
-                if (more) load_half_row<K>(c2, codes, p.grid, 4 * (b + 2) + hr, ob * 8 + 4 * half, lane);
+                if (more) load_half_row<K>(c2, codes, p.grid, 4 * (kb0 + b + 2) + hr, ob * 8 + 4 * half, lane);
                 c0.p[K] = __shfl_sync(0xffffffffu, c0.p[0], nbr) & 0xFFFFu;
                 decode_half_row_to_smem<K>(c0, slice, lane, 4 * half);
             } else if (rot == 1) {
-                if (more) load_half_row<K>(c0, codes, p.grid, 4 * (b + 2) + hr, ob * 8 + 4 * half, lane);
+                if (more) load_half_row<K>(c0, codes, p.grid, 4 * (kb0 + b + 2) + hr, ob * 8 + 4 * half, lane);
                 c1.p[K] = __shfl_sync(0xffffffffu, c1.p[0], nbr) & 0xFFFFu;
                 decode_half_row_to_smem<K>(c1, slice, lane, 4 * half);
             } else {
-                if (more) load_half_row<K>(c1, codes, p.grid, 4 * (b + 2) + hr, ob * 8 + 4 * half, lane);
+                if (more) load_half_row<K>(c1, codes, p.grid, 4 * (kb0 + b + 2) + hr, ob * 8 + 4 * half, lane);
                 c2.p[K] = __shfl_sync(0xffffffffu, c2.p[0], nbr) & 0xFFFFu;
                 decode_half_row_to_smem<K>(c2, slice, lane, 4 * half);
             }
@@ -493,6 +496,14 @@ __global__ void __launch_bounds__(tc::kMlThreads + 32, 2)
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, tcols);
     if (!ok) return;
+    if (p.part) {  // K split: the partial sums go out, the reduction applies the output transform
+        float* dst = p.part + ((long long)blockIdx.z * a.T * a.topk) * p.out + ob * 128 + 4 * lane;
+        for (int i = warp; i < nt; i += kThreads / 32) {
+            const float4 z4 = *reinterpret_cast<const float4*>(zs + i * 128 + 4 * lane);
+            *reinterpret_cast<float4*>(dst + (long long)slot_s[i] * p.out) = z4;
+        }
+        return;
+    }
     for (int i = warp; i < nt; i += kThreads / 32) {
         const float4 z4 = *reinterpret_cast<const float4*>(zs + i * 128 + 4 * lane);
         float v[4] = {z4.x * 256.f, z4.y * 256.f, z4.z * 256.f, z4.w * 256.f};  // undo the 2^-8 prescale (exact)
@@ -507,6 +518,39 @@ __global__ void __launch_bounds__(tc::kMlThreads + 32, 2)
         *reinterpret_cast<float4*>(p.y + (long long)slot_s[i] * p.out + ob * 128 + 4 * lane) =
             make_float4(v[0], v[1], v[2], v[3]);
     }
+}
+
+// K-split reduction of a dense projection: one warp per (token, 128-output
+// block) adds the splits' partial sums in split order, undoes the 2^-8
+// prescale, applies the output transform and the bias.
+__global__ void __launch_bounds__(256) dense_split_reduce_kernel(const GroupedProj p, int M, int splits) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_wait();
+    const int nob = p.out >> 7;
+    const long long task = (long long)blockIdx.x * 8 + warp;
+    if (task >= (long long)M * nob) return;
+    const int t = static_cast<int>(task / nob), ob = static_cast<int>(task % nob);
+    const uint2 rb = *reinterpret_cast<const uint2*>(p.rout + ob * 128 + 4 * lane);
+    const float* src = p.part + (long long)t * p.out + ob * 128 + 4 * lane;
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int z = 0; z < splits; ++z) {
+        const float4 z4 = *reinterpret_cast<const float4*>(src + (long long)z * M * p.out);
+        v[0] += z4.x;
+        v[1] += z4.y;
+        v[2] += z4.z;
+        v[3] += z4.w;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) v[q] *= 256.f;
+    output_transform_regs(v, rb, lane);
+    if (p.bias) {
+        const float4 b4 = *reinterpret_cast<const float4*>(p.bias + ob * 128 + 4 * lane);
+        v[0] += b4.x;
+        v[1] += b4.y;
+        v[2] += b4.z;
+        v[3] += b4.w;
+    }
+    *reinterpret_cast<float4*>(p.y + (long long)t * p.out + ob * 128 + 4 * lane) = make_float4(v[0], v[1], v[2], v[3]);
 }
 
 // ---------------------------------------------------------------------------
@@ -614,7 +658,9 @@ cudaError_t launch_grouped(const MoeArgs& a, const GroupedProj& p, cudaStream_t 
     cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     void* args[] = {const_cast<MoeArgs*>(&a), const_cast<GroupedProj*>(&p)};
-    return launch_kernel(f, dim3(p.out / 128, a.grp_max_items), dim3(tc::kMlThreads + 32), smem, true, s, args);
+    const int splits = ((p.in >> 6) + p.kblk_per_split - 1) / p.kblk_per_split;
+    return launch_kernel(f, dim3(p.out / 128, a.grp_max_items, splits), dim3(tc::kMlThreads + 32), smem, true, s,
+                         args);
 }
 
 cudaError_t launch_prep(const MoeArgs& a, const GroupedProj& p, cudaStream_t s) {
@@ -673,12 +719,12 @@ cudaError_t launch_moe_grouped(const MoeArgs& a, float* d, int num_sms, cudaStre
     cudaError_t e = launch_moe_topk_group(a, s);
     if (e != cudaSuccess) return e;
     const GroupedProj gu{a.gu_codes, a.gu_rin, a.gu_rout, a.hidden, 2 * a.inter, 0, a.ygu,
-                         tile_strides(a.hidden, 2 * a.inter, false), nullptr, nullptr};
+                         tile_strides(a.hidden, 2 * a.inter, false), nullptr, nullptr, a.hidden >> 6, nullptr};
     if ((e = launch_prep(a, gu, s)) != cudaSuccess) return e;
     e = a.gu_K == 2 ? launch_grouped<2>(a, gu, s) : launch_grouped<3>(a, gu, s);
     if (e != cudaSuccess) return e;
     const GroupedProj dn{a.dn_codes, a.dn_rin, a.dn_rout, a.inter, a.hidden, 1, d,
-                         tile_strides(a.inter, a.hidden, false), nullptr, nullptr};
+                         tile_strides(a.inter, a.hidden, false), nullptr, nullptr, a.inter >> 6, nullptr};
     if ((e = launch_prep(a, dn, s)) != cudaSuccess) return e;
     return a.dn_K == 2 ? launch_grouped<2>(a, dn, s) : launch_grouped<3>(a, dn, s);
 }
@@ -694,13 +740,31 @@ cudaError_t launch_dense_grouped(const DenseArgs& d, cudaStream_t s) {
     a.grp_img = d.img;
     a.grp_img_rows = d.img_rows;
     a.err = d.err;
+    const int nblk = d.in >> 6;
+    const int bps = (nblk + d.splits - 1) / d.splits;
+    const int splits = (nblk + bps - 1) / bps;  // every split starts inside K
     const GroupedProj p{d.codes, d.rin, d.rout, d.in, d.out, d.x_f32 ? 2 : 0, d.y,
                         tile_strides(d.in, d.out, d.nt_major != 0), d.bias,
-                        static_cast<const float*>(d.x_f32 ? d.x : nullptr)};
+                        static_cast<const float*>(d.x_f32 ? d.x : nullptr), bps, splits > 1 ? d.part : nullptr};
     cudaError_t e = launch_prep(a, p, s);
     if (e != cudaSuccess) return e;
     a.grp_max_items = (d.M + d.cap - 1) / d.cap;
-    return d.K == 2 ? launch_grouped<2>(a, p, s) : launch_grouped<3>(a, p, s);
+    e = d.K == 2 ? launch_grouped<2>(a, p, s) : launch_grouped<3>(a, p, s);
+    if (e != cudaSuccess || splits == 1) return e;
+    int M = d.M, sp = splits;
+    void* rargs[] = {const_cast<GroupedProj*>(&p), &M, &sp};
+    const long long tasks = (long long)d.M * (d.out >> 7);
+    return launch_kernel(reinterpret_cast<const void*>(dense_split_reduce_kernel),
+                         dim3(static_cast<unsigned>((tasks + 7) / 8)), dim3(256), 0, true, s, rargs);
+}
+
+int dense_ksplit(int in, int out, int M, int cap) {
+    const long long base = (long long)(out >> 7) * ((M + cap - 1) / cap);  // CTAs without a split
+    const int nblk = in >> 6;
+    long long ks = (2 * 152 + base - 1) / base;  // about one wave of two CTAs per SM
+    if (ks > nblk / 4) ks = nblk / 4;            // at least 4 blocks of 64 inputs per split
+    if (ks > 16) ks = 16;
+    return ks < 1 ? 1 : static_cast<int>(ks);
 }
 
 cudaError_t launch_moe_combine(const MoeArgs& a, const float* d, cudaStream_t s) {

@@ -130,10 +130,13 @@ int escha_codes_to_nt_major(const uint16_t* codes, int in, int out, int K, uint1
  * added after the output transform, so for gate/up it lands before any
  * activation the caller applies, and for down/o_proj it may equally be added
  * onto the residual afterwards.
- * M <= 12 runs the fused per-token decode GEMV (weights decoded once per 1,
- * 2 or 4 tokens); M >= 13 writes an fp16 hi/lo image of H(rin * x) and runs
- * the tcgen05 tensor-core GEMM with all tokens in one group (weights decoded
- * once per 16..128 tokens). Accumulation is fp32 on both routes.
+ * M <= 2 (M <= 12 when in * out <= 2^23) runs the fused per-token decode
+ * GEMV (weights decoded once per 1, 2 or 4 tokens); larger M writes an fp16
+ * hi/lo image of H(rin * x) and runs the tcgen05 tensor-core GEMM with all
+ * tokens in one group (weights decoded once per 16..128 tokens), its inputs
+ * split over up to 16 CTAs when output blocks x items leave SMs idle (the
+ * partial sums are added in a fixed order). Accumulation is fp32 on both
+ * routes; the route and the split are fixed functions of (in, out, M).
  *   codes    uint16, kt-major [in/16][out/16][16*K] (nt_major = 0) or
  *            nt-major [out/16][in/16][16*K] (nt_major = 1, see
  *            escha_codes_to_nt_major); K in {2, 3}

@@ -51,8 +51,9 @@ def _ref(p, x, use_bias, cols=None):
                           bias=bias.astype(np.float64) if use_bias else None)
 
 
-# M = 1..12 run the fused GEMV, M >= 13 the grouped tensor-core GEMM (items
-# of 16, 32, 64 or 128 tokens); 300 tokens leave a ragged last item of 44.
+# For this 1024 x 768 weight M = 1..12 run the fused GEMV, M >= 13 the
+# grouped tensor-core GEMM (items of 16, 32, 64 or 128 tokens, inputs split
+# over 4 CTAs); 300 tokens leave a ragged last item of 44.
 @pytest.mark.parametrize("M", [1, 3, 12, 13, 64, 300])
 @pytest.mark.parametrize("nt_major", [False, True])
 def test_dense_linear_matches_oracle(native, M, nt_major):
@@ -101,14 +102,17 @@ def test_dense_linear_rows_independent_of_batch(native):
     assert rel_err_rows(y100[:20], y20).max() <= 1e-5
 
 
-@pytest.mark.parametrize("M", [1, 2048])
-def test_dense_linear_full_size_gate_proj_sampled(native, M):
-    """5120 -> 17408, K = 2 (the 27B dense gate_proj shape), nt-major with
-    bias: two 128-output blocks (the first and the last) checked against the
-    oracle on every token for M = 1 and on 24 sampled tokens for M = 2048."""
-    n_in, n_out = 5120, 17408
+@pytest.mark.parametrize("n_in,n_out,K,M", [(5120, 17408, 2, 1), (5120, 17408, 2, 3), (5120, 17408, 2, 2048),
+                                             (17408, 5120, 3, 13), (17408, 5120, 3, 200)])
+def test_dense_linear_full_size_sampled(native, n_in, n_out, K, M):
+    """The 27B-class dense MLP shapes (gate/up 5120 -> 17408, down 17408 ->
+    5120), nt-major with bias: two 128-output blocks (the first and the last)
+    checked against the oracle on every token up to 32 tokens, else on 24
+    sampled tokens. From 3 tokens on these shapes run the GEMM; at 3, 13
+    and 200 tokens its inputs are split over several CTAs (partial sums
+    reduced in order)."""
     g = gen.rng(6000 + M)
-    codes = gen.trellis_codes(g, n_in, n_out, 2)
+    codes = gen.trellis_codes(g, n_in, n_out, K)
     x = gen.fp16_normal(g, (M, n_in))
     rin = gen.signs(g, n_in)
     rout = gen.rout_vector(g, n_out)
