@@ -27,6 +27,12 @@ int fail(int code, const char* fmt, ...) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+}  // namespace
+
+void escha::set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
+
+namespace {
+
 struct DeviceInfo {
     int ok = -1;  // -1 unknown, 0 not sm_103, 1 fine
     int num_sms = 0;

@@ -146,6 +146,9 @@ cudaError_t launch_dense_grouped(const DenseArgs& d, cudaStream_t s);
 // K splits of the dense grouped GEMM: a fixed function of the shape.
 int dense_ksplit(int in, int out, int M, int cap);
 
+// Sets the message escha_last_error() returns on this host thread.
+void set_last_error(const char* msg);
+
 // Whole-tile transpose of a code tensor: [in/16][out/16] tiles -> [out/16][in/16].
 cudaError_t launch_codes_to_nt_major(const uint16_t* src, int in, int out, int K, uint16_t* dst, cudaStream_t s);
 

@@ -24,6 +24,8 @@ ESCHA_E_WORKSPACE = -4
 ESCHA_E_ALIGN = -5
 ESCHA_E_CUDA = -6
 ESCHA_E_DEVICE = -7
+ESCHA_E_CKPT = -8
+ESCHA_E_IO = -9
 
 ESCHA_F16 = 1
 ESCHA_BF16 = 2
@@ -38,6 +40,13 @@ EXPORTS = [
     "escha_codes_to_nt_major",
     "escha_dense_linear_workspace",
     "escha_dense_linear",
+    "escha_ckpt_open",
+    "escha_ckpt_close",
+    "escha_ckpt_num_projections",
+    "escha_ckpt_projection",
+    "escha_ckpt_tensor_info",
+    "escha_ckpt_read",
+    "escha_ckpt_load_projection",
     "escha_moe_block_workspace",
     "escha_moe_block",
     "escha_moe_block_timed",
@@ -81,6 +90,30 @@ class EschaMoeLayer(ctypes.Structure):
     ]
 
 
+class EschaProjInfo(ctypes.Structure):
+    """Mirror of ``escha_proj_info`` in include/escha.h."""
+
+    _fields_ = [
+        ("prefix", ctypes.c_char * 256),
+        ("K", _i),
+        ("n_experts", _i),
+        ("n_in", _i),
+        ("n_out", _i),
+        ("has_bias", _i),
+        ("has_s_in", _i),
+        ("has_s_out", _i),
+        ("has_config", _i),
+        ("scales_all_ones", _i),
+        ("config_k", _i),
+    ]
+
+
+class EschaTensorInfo(ctypes.Structure):
+    """Mirror of ``escha_tensor_info`` in include/escha.h."""
+
+    _fields_ = [("dtype", ctypes.c_char * 8), ("ndim", _i), ("shape", ctypes.c_longlong * 8), ("nbytes", _sz)]
+
+
 _LIB = None
 
 
@@ -107,6 +140,20 @@ def lib() -> ctypes.CDLL:
         L.escha_dense_linear_workspace.restype = _sz
         L.escha_dense_linear.argtypes = [_vp, _i, _i, _i, _i, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
         L.escha_dense_linear.restype = _i
+        L.escha_ckpt_open.argtypes = [ctypes.POINTER(ctypes.c_char_p), _i, ctypes.POINTER(_vp)]
+        L.escha_ckpt_open.restype = _i
+        L.escha_ckpt_close.argtypes = [_vp]
+        L.escha_ckpt_close.restype = None
+        L.escha_ckpt_num_projections.argtypes = [_vp]
+        L.escha_ckpt_num_projections.restype = _i
+        L.escha_ckpt_projection.argtypes = [_vp, _i, ctypes.POINTER(EschaProjInfo)]
+        L.escha_ckpt_projection.restype = _i
+        L.escha_ckpt_tensor_info.argtypes = [_vp, ctypes.c_char_p, ctypes.POINTER(EschaTensorInfo)]
+        L.escha_ckpt_tensor_info.restype = _i
+        L.escha_ckpt_read.argtypes = [_vp, ctypes.c_char_p, _vp, _sz, _i, _vp]
+        L.escha_ckpt_read.restype = _i
+        L.escha_ckpt_load_projection.argtypes = [_vp, _i, _vp, _vp, _vp, _vp, _i, _vp]
+        L.escha_ckpt_load_projection.restype = _i
         L.escha_moe_block_workspace.argtypes = [ctypes.POINTER(EschaMoeLayer), _i]
         L.escha_moe_block_workspace.restype = _sz
         L.escha_moe_block.argtypes = [ctypes.POINTER(EschaMoeLayer), _vp, _i, _vp, _vp, _vp, _vp, _sz, _vp]
@@ -228,6 +275,20 @@ class DenseLinear:
         self.bias = bias.contiguous() if bias is not None else None
         self._ws = None
 
+    @classmethod
+    def from_checkpoint(cls, ckpt: "Checkpoint", i: int, device="cuda", nt_major: bool = True, stream=None):
+        """Dense projection i of an opened checkpoint, its tiles moved to the
+        nt-major grid at load (nt_major) and its bias, if any, widened to f32."""
+        ld = ckpt.load_projection(i, device=device, nt_major=nt_major, stream=stream)
+        p = ld["info"]
+        if p["n_experts"]:
+            raise ValueError(f"{p['prefix']} holds stacked experts, not a dense projection")
+        self = cls.__new__(cls)
+        self.n_in, self.n_out, self.K, self.nt_major = p["in"], p["out"], p["K"], bool(nt_major)
+        self.codes, self.rin, self.rout, self.bias = ld["codes"], ld["rin"], ld["rout"], ld["bias"]
+        self._ws = None
+        return self
+
     def workspace_bytes(self, M: int) -> int:
         return lib().escha_dense_linear_workspace(self.n_in, self.n_out, self.K, M)
 
@@ -252,6 +313,74 @@ class DenseLinear:
     def status(self) -> int:
         """The status word of the last call (0: every bounded wait completed)."""
         return int(self._ws[:4].view(torch.int32).item()) if self._ws is not None else 0
+
+
+_ST_DTYPES = {"F16": np.float16, "BF16": np.uint16, "F32": np.float32, "F64": np.float64, "I8": np.int8,
+              "U8": np.uint8, "I16": np.int16, "U16": np.uint16, "I32": np.int32, "U32": np.uint32,
+              "I64": np.int64, "U64": np.uint64, "BOOL": np.bool_}
+
+
+class Checkpoint:
+    """Safetensors shards of an Escha-W2 export, opened through the native
+    loader, which checks the escha leaf contract on open (EschaError with
+    code ESCHA_E_CKPT / ESCHA_E_IO otherwise)."""
+
+    def __init__(self, paths):
+        if isinstance(paths, (str, os.PathLike)):
+            paths = [paths]
+        enc = [os.fspath(p).encode() for p in paths]
+        arr = (ctypes.c_char_p * len(enc))(*enc)
+        h = _vp()
+        check(lib().escha_ckpt_open(arr, len(enc), ctypes.byref(h)))
+        self._h = h
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().escha_ckpt_close(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # pragma: no cover - interpreter shutdown
+            pass
+
+    def projections(self) -> list:
+        out = []
+        for i in range(lib().escha_ckpt_num_projections(self._h)):
+            info = EschaProjInfo()
+            check(lib().escha_ckpt_projection(self._h, i, ctypes.byref(info)))
+            out.append({"prefix": info.prefix.decode(), "K": info.K, "n_experts": info.n_experts, "in": info.n_in,
+                        "out": info.n_out, "has_bias": bool(info.has_bias), "has_s_in": bool(info.has_s_in),
+                        "has_s_out": bool(info.has_s_out), "has_config": bool(info.has_config),
+                        "scales_all_ones": bool(info.scales_all_ones), "config_k": info.config_k})
+        return out
+
+    def tensor_info(self, name: str):
+        info = EschaTensorInfo()
+        check(lib().escha_ckpt_tensor_info(self._h, name.encode(), ctypes.byref(info)))
+        return info.dtype.decode(), tuple(info.shape[:info.ndim]), int(info.nbytes)
+
+    def read(self, name: str) -> np.ndarray:
+        """The tensor as stored (BF16 as uint16 bit patterns), in host memory."""
+        dt, shape, nbytes = self.tensor_info(name)
+        a = np.empty(shape, dtype=_ST_DTYPES[dt])
+        check(lib().escha_ckpt_read(self._h, name.encode(), a.ctypes.data, nbytes, 0, None))
+        return a
+
+    def load_projection(self, i: int, device="cuda", nt_major: bool = False, stream=None) -> dict:
+        """Projection i's codes / rin / rout (and bias, f32) in device memory."""
+        p = self.projections()[i]
+        KT, NT, L = p["in"] // 16, p["out"] // 16, 16 * p["K"]
+        shape = ((NT, KT, L) if nt_major else (KT, NT, L)) if not p["n_experts"] else (p["n_experts"], KT, NT, L)
+        lead = (p["n_experts"],) if p["n_experts"] else ()
+        codes = torch.empty(shape, dtype=torch.int16, device=device)
+        rin = torch.empty(lead + (p["in"],), dtype=torch.float16, device=device)
+        rout = torch.empty(lead + (p["out"],), dtype=torch.float16, device=device)
+        bias = torch.empty(p["out"], dtype=torch.float32, device=device) if p["has_bias"] else None
+        check(lib().escha_ckpt_load_projection(self._h, i, ptr(codes), ptr(rin), ptr(rout), ptr(bias), int(nt_major),
+                                               stream_handle(stream)))
+        return {"codes": codes, "rin": rin, "rout": rout, "bias": bias, "info": p}
 
 
 def int8_w8a16_matvec(W, scales, x, y=None, stream=None) -> torch.Tensor:

@@ -65,6 +65,8 @@ extern "C" {
 #define ESCHA_E_ALIGN (-5)     /* pointer not 16-byte aligned */
 #define ESCHA_E_CUDA (-6)      /* CUDA error while enqueueing (launch/config) */
 #define ESCHA_E_DEVICE (-7)    /* current device is not an sm_103 GPU */
+#define ESCHA_E_CKPT (-8)      /* checkpoint breaks the escha leaf contract */
+#define ESCHA_E_IO (-9)        /* shard missing, unreadable or not safetensors */
 
 /* ---- element types --------------------------------------------------- */
 #define ESCHA_F16 1
@@ -154,6 +156,69 @@ size_t escha_dense_linear_workspace(int in, int out, int K, int M);
 int escha_dense_linear(const uint16_t* codes, int in, int out, int K, int nt_major, const void* x, int x_dtype, int M,
                        const uint16_t* rin, const uint16_t* rout, const float* bias, float* y, void* ws,
                        size_t ws_bytes, void* stream);
+
+/* ---- checkpoint loader (safetensors shards of an Escha-W2 export) ---------
+ * A shard is an 8-byte little-endian header length N, N bytes of JSON
+ * ({name: {"dtype", "shape", "data_offsets": [begin, end]}}, begin/end
+ * relative to the data after the header) and the data. Opening checks the
+ * escha leaf contract [PR694 commit reading Escha's test suite; model card
+ * "EschaLabs/Qwen3.6-35B-A3B-Escha-W2", section "Format notes"]:
+ *   - a coded projection <prefix> has the required leaves <prefix>.escha_code
+ *     (I16/U16 [in/16][out/16][16*K], or [E][..] for stacked experts),
+ *     .escha_rin (F16 [in] / [E][in]) and .escha_rout (F16 [out] / [E][out]);
+ *     a missing one is ESCHA_E_CKPT naming it;
+ *   - .escha_s_in, .escha_s_out (all ones as shipped: never applied) and
+ *     .escha_config (int32[9], informational) are optional;
+ *   - any other leaf escha_* (e.g. escha_rotation_theta, a rotation variant
+ *     the format anticipates) is ESCHA_E_CKPT naming it;
+ *   - K = (last dimension of escha_code) / 16, K in {2, 3};
+ *   - <prefix>.bias (F32/F16/BF16 [out]) is the dense export's additive
+ *     output bias [PR694 commit on the dense export's biases]; the dense
+ *     coded projections of one layer ("...layers.<n>.") carry biases all
+ *     together or not at all, else ESCHA_E_CKPT.
+ * A tensor name present in two shards, offsets that disagree with the shape
+ * or an unknown dtype are rejected too. The handle owns only host memory. */
+typedef struct escha_ckpt escha_ckpt;
+
+typedef struct escha_proj_info {
+    char prefix[256];    /* tensor names without ".escha_code" etc. */
+    int K;               /* bits per weight, from the code tensor's shape */
+    int n_experts;       /* 0: one dense projection; E: E stacked experts */
+    int in, out;
+    int has_bias;        /* <prefix>.bias present (dense projections only) */
+    int has_s_in, has_s_out, has_config;
+    int scales_all_ones; /* s_in / s_out absent or all ones */
+    int config_k;        /* escha_config[1] when present (reported, not trusted), else -1 */
+} escha_proj_info;
+
+typedef struct escha_tensor_info {
+    char dtype[8];       /* safetensors dtype: "F16", "BF16", "F32", "I16", "U16", "I8", "I32", ... */
+    int ndim;
+    long long shape[8];
+    size_t nbytes;
+} escha_tensor_info;
+
+/* Opens and validates n_paths shards; *out receives a handle to close with
+ * escha_ckpt_close. Errors: ESCHA_E_ARG, ESCHA_E_IO, ESCHA_E_CKPT. */
+int escha_ckpt_open(const char* const* paths, int n_paths, escha_ckpt** out);
+void escha_ckpt_close(escha_ckpt* c);
+/* Coded projections, in name order. */
+int escha_ckpt_num_projections(const escha_ckpt* c);
+int escha_ckpt_projection(const escha_ckpt* c, int i, escha_proj_info* info);
+/* Any tensor by name (router weights, int8 matrices and their scales, ...). */
+int escha_ckpt_tensor_info(const escha_ckpt* c, const char* name, escha_tensor_info* info);
+/* Its bytes, as stored, into dst (dst_device 0: host memory, 1: device
+ * memory through `stream`, synchronised before return). dst_bytes must be at
+ * least info.nbytes. Errors: ESCHA_E_ARG, ESCHA_E_IO, ESCHA_E_CUDA. */
+int escha_ckpt_read(const escha_ckpt* c, const char* name, void* dst, size_t dst_bytes, int dst_device, void* stream);
+/* Projection i's leaves into caller-owned device buffers: codes (the code
+ * tensor's size; nt_major = 1 moves a dense projection's tiles to the
+ * nt-major grid at load, see escha_codes_to_nt_major; experts stay
+ * kt-major), rin / rout fp16, and, when bias is not NULL, the bias widened
+ * to f32 [out] (ESCHA_E_ARG if the projection has none). Synchronises
+ * `stream` before returning. Errors: ESCHA_E_ARG, ESCHA_E_IO, ESCHA_E_CUDA. */
+int escha_ckpt_load_projection(const escha_ckpt* c, int i, uint16_t* codes, uint16_t* rin, uint16_t* rout,
+                               float* bias, int nt_major, void* stream);
 
 /* ---- one MoE block ------------------------------------------------------
  * For each token b of x [T][hidden] (fp16):

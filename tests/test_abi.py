@@ -45,6 +45,9 @@ def test_struct_layout_matches_header():
     native, _ = _lib()
     # 4 ints, 1 pointer, (pointer, int, pointer, pointer) x 2, int + 5 pointers, natural alignment
     assert ctypes.sizeof(native.EschaMoeLayer) == 136
+    # char[256] + 10 ints; char[8], int, (pad 4), long long[8], size_t
+    assert ctypes.sizeof(native.EschaProjInfo) == 296
+    assert ctypes.sizeof(native.EschaTensorInfo) == 88
 
 
 def test_version():

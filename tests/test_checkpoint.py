@@ -96,3 +96,98 @@ def test_scales_are_reported_not_applied(tmp_path):
     t["a.proj.escha_config"][1] = 3  # informational: reported, not trusted
     (p,) = oc.validate([_write(tmp_path, t, name="b.safetensors")])
     assert not p["scales_all_ones"] and p["config_k"] == 3 and p["K"] == 2
+
+
+# ------------------------------------------------- native loader vs oracle ---
+
+
+def _cases(tmp_path):
+    """(name, list of shard paths): valid exports and one file per way of
+    breaking the contract or the format."""
+    out = []
+    exp = ckpt.small_export(7)
+    names = sorted(exp)
+    half = len(names) // 2
+    out.append(("export_one_shard", [_write(tmp_path, exp, name="one.safetensors")]))
+    out.append(("export_two_shards", [_write(tmp_path, {k: exp[k] for k in names[:half]}, name="s1.safetensors"),
+                                      _write(tmp_path, {k: exp[k] for k in names[half:]}, name="s2.safetensors")]))
+    out.append(("duplicate_across_shards", [_write(tmp_path, exp, name="d1.safetensors"),
+                                            _write(tmp_path, {names[0]: exp[names[0]]}, name="d2.safetensors")]))
+    g = gen.rng(3)
+    base = ckpt.coded_projection(g, "model.layers.0.mlp.down_proj", 256, 128, 2, bias=True)
+
+    def variant(tag, edit=None, **kw):
+        t = dict(base)
+        if edit:
+            edit(t)
+        out.append((tag, [_write(tmp_path, t, name=f"{tag}.safetensors", **kw)]))
+
+    variant("dense_biased")
+    for leaf in oc.REQUIRED:
+        variant(f"missing_{leaf}", lambda t, leaf=leaf: t.pop(f"model.layers.0.mlp.down_proj.{leaf}"))
+    variant("rotation_theta", lambda t: t.update({"model.layers.0.mlp.down_proj.escha_rotation_theta":
+                                                  np.zeros(8, np.float32)}))
+    variant("unknown_escha_leaf", lambda t: t.update({"x.escha_zeta": np.zeros(2, np.float16)}))
+    variant("k4_code", lambda t: t.update({"model.layers.0.mlp.down_proj.escha_code":
+                                           np.zeros((16, 8, 64), np.int16)}))
+    variant("f32_code", lambda t: t.update({"model.layers.0.mlp.down_proj.escha_code":
+                                            np.zeros((16, 8, 32), np.float32)}))
+    variant("short_rin", lambda t: t.update({"model.layers.0.mlp.down_proj.escha_rin": np.ones(128, np.float16)}))
+    variant("f32_rout", lambda t: t.update({"model.layers.0.mlp.down_proj.escha_rout": np.ones(128, np.float32)}))
+    variant("bad_bias_len", lambda t: t.update({"model.layers.0.mlp.down_proj.bias": np.ones(64, np.float32)}))
+    variant("half_biased", lambda t: t.update(ckpt.coded_projection(gen.rng(4), "model.layers.0.mlp.up_proj",
+                                                                    128, 256, 3)))
+    variant("other_layer_unbiased", lambda t: t.update(ckpt.coded_projection(gen.rng(4), "model.layers.1.mlp.up_proj",
+                                                                             128, 256, 3)))
+    variant("bf16_bias", lambda t: t.update({"model.layers.0.mlp.down_proj.bias": np.zeros(128, np.uint16)}),
+            dtypes={"model.layers.0.mlp.down_proj.bias": "BF16"})
+    variant("expert_bias", lambda t: t.update(
+        {**ckpt.coded_projection(gen.rng(5), "model.layers.2.mlp.experts.gate_up_proj", 128, 256, 3, experts=4),
+         "model.layers.2.mlp.experts.gate_up_proj.bias": np.zeros(256, np.float32)}))
+    variant("bad_offsets", header_override={"model.layers.0.mlp.down_proj.bias":
+                                            {"dtype": "F32", "shape": [128], "data_offsets": [0, 100]}})
+    variant("unknown_dtype", header_override={"model.layers.0.mlp.down_proj.bias":
+                                              {"dtype": "Q4", "shape": [128], "data_offsets": [0, 512]}})
+    bad = tmp_path / "not_json.safetensors"
+    bad.write_bytes(struct.pack("<Q", 8) + b"{not js}")
+    out.append(("not_json", [str(bad)]))
+    out.append(("missing_file", [str(tmp_path / "absent.safetensors")]))
+    return out
+
+
+def test_loader_matches_oracle_on_every_case(native, tmp_path):
+    expect = {"export_one_shard": "ok", "export_two_shards": "ok", "dense_biased": "ok",
+              "other_layer_unbiased": "ok", "bf16_bias": "ok"}
+    for tag, paths in _cases(tmp_path):
+        if tag == "missing_file":
+            ov = ("io", "")
+        else:
+            ov = _oracle_verdict(paths)
+        nv = _native_verdict(native, paths)
+        assert nv[0] == ov[0], (tag, nv, ov)
+        assert ov[0] == expect.get(tag, ov[0] if ov[0] != "ok" else "error"), (tag, ov)
+        if ov[0] == "ok":
+            assert nv[1] == ov[1], tag
+        elif tag.startswith("missing_escha") or tag in ("rotation_theta",):
+            leaf = "escha_rotation_theta" if tag == "rotation_theta" else tag[len("missing_"):]
+            assert leaf in nv[1] and leaf in ov[1], (tag, nv, ov)
+
+
+def test_export_projections_and_raw_reads(native, tmp_path):
+    exp = ckpt.small_export(11)
+    path = _write(tmp_path, exp)
+    c = native.Checkpoint(path)
+    projs = {p["prefix"]: p for p in c.projections()}
+    gu = projs["model.layers.0.mlp.experts.gate_up_proj"]
+    assert (gu["K"], gu["n_experts"], gu["in"], gu["out"]) == (3, 8, 256, 256)
+    assert gu["has_config"] and gu["config_k"] == 3 and gu["scales_all_ones"]
+    assert projs["model.layers.0.mlp.experts.down_proj"]["K"] == 2
+    dense = [p for k, p in projs.items() if k.startswith("model.layers.1.")]
+    assert len(dense) == 5 and all(p["has_bias"] for p in dense)
+    for name in ("model.layers.0.mlp.gate.weight", "model.layers.0.mlp.shared_expert.gate_up_proj.weight_int8",
+                 "model.layers.1.mlp.up_proj.escha_code", "model.layers.1.mlp.down_proj.bias"):
+        got = c.read(name)
+        assert got.shape == exp[name].shape and got.tobytes() == np.ascontiguousarray(exp[name]).tobytes(), name
+    with pytest.raises(native.EschaError):
+        c.tensor_info("no.such.tensor")
+    c.close()
