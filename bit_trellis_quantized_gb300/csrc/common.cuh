@@ -44,6 +44,35 @@ __device__ __forceinline__ __half2 cb_decode_h2(uint32_t sa, uint32_t sb) {
     return __halves2half2(__hadd(__low2half(a2), __high2half(a2)), __hadd(__low2half(b2), __high2half(b2)));
 }
 
+// K = 2 pair decode. Weights t and t + 8 of a lane's stream (16 bits apart)
+// share one 32-bit window P = s_t << 16 | s_{t+8}: one funnel shift extracts
+// both states, and s_{t+8} * m = P * m - (s_t * m) << 16 (mod 2^32) costs a
+// multiply-add instead of two integer-pipe instructions.
+// Word pair p = w[2i] | w[2i+1] << 16 in stream order: (w[2i] << 16) | w[2i+1].
+__device__ __forceinline__ uint32_t stream_pair(uint32_t p) { return __byte_perm(p, 0u, 0x1032); }
+// 32 stream bits starting at bit O of q0 (q1 follows q0)
+template <int O>
+__device__ __forceinline__ uint32_t bits32(uint32_t q0, uint32_t q1) {
+    if constexpr (O == 0) {
+        return q0;
+    } else {
+        return __funnelshift_l(q1, q0, O);
+    }
+}
+// codebook value from the product u = s * kCbMul
+__device__ __forceinline__ __half cb_finish(uint32_t u) {
+    const uint32_t r = (u & kCbMask) ^ kCbXor;
+    const __half2 h = *reinterpret_cast<const __half2*>(&r);
+    return __hadd(__low2half(h), __high2half(h));
+}
+// the two codebook values of the window P (states P >> 16 and P & 0xFFFF)
+__device__ __forceinline__ void cb_decode_window(uint32_t P, __half& wa, __half& wb) {
+    const uint32_t ua = (P >> 16) * kCbMul;
+    const uint32_t ub = ua * 0xFFFF0000u + P * kCbMul;
+    wa = cb_finish(ua);
+    wb = cb_finish(ub);
+}
+
 // ---------------------------------------------------------------------------
 // Bit-stream windows. A lane holds consecutive 16-bit code words w[0..n) as
 // little-endian pairs p[i] = w[2i] | w[2i+1] << 16 (what a vector load of the

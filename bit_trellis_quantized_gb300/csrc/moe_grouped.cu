@@ -360,6 +360,29 @@ __device__ __forceinline__ void decode_half_row_to_smem(const HalfRowCodes<K>& l
                                                         int tile0) {
     const int c = lane & 7;
     const uint32_t m0 = 16u * static_cast<uint32_t>(tile0 + (lane >> 3));
+    if constexpr (K == 2) {  // weights (row rr, col m) and (row rr, col m + 8) share a window
+        const uint32_t q[3] = {stream_pair(lc.p[0]), stream_pair(lc.p[1]), stream_pair(lc.p[2])};
+        static_for<2>([&](auto R) {
+            constexpr int rr = decltype(R)::value;
+            __half w[16];
+            static_for<8>([&](auto M) {
+                constexpr int m = decltype(M)::value;
+                cb_decode_window(bits32<2 * m>(q[rr], q[rr + 1]), w[m], w[m + 8]);
+            });
+            static_for<2>([&](auto H) {  // columns 8h .. 8h + 7
+                constexpr int h = decltype(H)::value;
+                uint32_t packed[4];
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    const __half2 w2 = __halves2half2(w[8 * h + 2 * p], w[8 * h + 2 * p + 1]);
+                    packed[p] = *reinterpret_cast<const uint32_t*>(&w2);
+                }
+                *reinterpret_cast<uint4*>(slice + tc::mnmajor_off(m0 + 8u * h, 2u * c + rr, 2048u, 1024u)) =
+                    make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            });
+        });
+        return;
+    }
     static_for<4>([&](auto J) {  // quarter j: input row 2c + j/2, columns 8*(j%2)..+7
         constexpr int j = decltype(J)::value;
         uint32_t packed[4];

@@ -73,11 +73,30 @@ __device__ __forceinline__ void load_lane_codes(LaneCodes<K>& lc, const uint16_t
 // over its 4 input rows. Half-row j (input row j/2, output columns
 // 8*(j%2)..+7) starts at bit 8*K*j of the lane's words and its weight m at
 // bit 8*K*j + K*m; all offsets are compile-time constants.
-// Weights are decoded in pairs (m, m+1): measured faster on GB300 than one at
-// a time (fewer integer-pipe instructions); every accumulator still receives
-// its weights in the same order, so the sums are unchanged.
+// K = 3 decodes weights in pairs (m, m+1); K = 2 takes columns m and m + 8 of
+// one input row from a single 32-bit stream window (cb_decode_window). Both
+// were measured faster on GB300 than one weight at a time (fewer
+// integer-pipe instructions); every accumulator still receives its weights
+// in the same order, so the sums are unchanged.
 template <int K, int NB>
 __device__ __forceinline__ void decode_fma(const LaneCodes<K>& lc, const float (&xr)[NB][4], float (&acc)[NB][16]) {
+    if constexpr (K == 2) {  // weights (row r, col m) and (row r, col m + 8) share a window
+        uint32_t q[5];
+#pragma unroll
+        for (int i = 0; i < 5; ++i) q[i] = stream_pair(lc.p[i]);
+        static_for<32>([&](auto I) {
+            constexpr int r = decltype(I)::value / 8, m = decltype(I)::value % 8;
+            __half ha, hb;
+            cb_decode_window(bits32<2 * m>(q[r], q[r + 1]), ha, hb);
+            const float wa = __half2float(ha), wb = __half2float(hb);
+#pragma unroll
+            for (int t = 0; t < NB; ++t) {
+                acc[t][m] = fmaf(wa, xr[t][r], acc[t][m]);
+                acc[t][m + 8] = fmaf(wb, xr[t][r], acc[t][m + 8]);
+            }
+        });
+        return;
+    }
     static_for<32>([&](auto I) {
         constexpr int j = (2 * decltype(I)::value) / 8;
         constexpr int m = (2 * decltype(I)::value) % 8;
