@@ -459,7 +459,7 @@ def extended(dev, blocks, hbm, tflops):
     """The other workloads of the benchmark's configuration list, each with
     inputs larger than L2 (distinct weights cycled) unless stated:
     single projection at batch 1, the dense 5120 x 17408 linear at M = 1..2048,
-    the MoE block at batch 64 / 256 and a
+    the MoE block at batch 8 / 16 / 64 / 256 and a
     2048-token prefill chunk, the int8 w8a16 shapes at M = 1 and 2048, and
     the 40-block stack at batch 1 / 8 / 128 and a 2048-token chunk."""
     import torch
@@ -511,10 +511,11 @@ def extended(dev, blocks, hbm, tflops):
     del codes
     torch.cuda.empty_cache()
 
-    # MoE block at batch 64 / 256 / 2048 over the headline's layers, fresh x per call
+    # MoE block at batch 8 / 16 (per-slot path), 64 / 256 / 2048 (grouped path)
+    # over the headline's layers, fresh x per call
     nl = len(blocks)
     mb = {}
-    for T in (64, 256, 2048):
+    for T in (8, 16, 64, 256, 2048):
         ws = torch.empty(max(native.lib().escha_moe_block_workspace(native.ctypes.byref(blocks[0].layer), T), 256),
                          dtype=torch.uint8, device=dev)
         reps = nl if T <= 256 else 8

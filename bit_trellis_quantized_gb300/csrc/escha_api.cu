@@ -455,7 +455,7 @@ int moe_block_impl(const escha_moe_layer* L, const uint16_t* x, int T, float* ou
     if ((r = record(ev, 1, s))) return r;
     if ((r = cuda_status(escha::launch_moe_gate_up(a, sms, s), "gate_up launch"))) return r;
     if ((r = record(ev, 2, s))) return r;
-    if ((r = cuda_status(escha::launch_moe_down(a, s), "down/combine launch"))) return r;
+    if ((r = cuda_status(escha::launch_moe_down(a, sms, s), "down/combine launch"))) return r;
     return record(ev, 3, s);
 }
 

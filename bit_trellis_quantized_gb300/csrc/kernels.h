@@ -110,7 +110,7 @@ struct MoeArgs {
 // Largest token count of a grouped work item, and the largest batch that
 // runs the per-slot GEMV path instead.
 constexpr int kGrpCapMax = 128;
-constexpr int kSlotModeMaxT = 12;
+constexpr int kSlotModeMaxT = 16;
 
 // Scratch of the grouped path for T tokens.
 struct GroupPlan {
@@ -162,6 +162,6 @@ cudaError_t launch_residual_rmsnorm(float* h, const float* add, int T, int hidde
 
 cudaError_t launch_moe_router(const MoeArgs& a, cudaStream_t s);
 cudaError_t launch_moe_gate_up(const MoeArgs& a, int num_sms, cudaStream_t s);
-cudaError_t launch_moe_down(const MoeArgs& a, cudaStream_t s);
+cudaError_t launch_moe_down(const MoeArgs& a, int num_sms, cudaStream_t s);
 
 }  // namespace escha

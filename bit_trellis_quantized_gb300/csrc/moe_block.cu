@@ -37,6 +37,10 @@ constexpr int kGuWarps = kGuThreads / 32;
 constexpr int kDnThreads = 256;
 constexpr int kDnWarps = kDnThreads / 32;
 constexpr int kMaxCluster = 16;
+// SM count the input splits are sized for (GB300). A constant rather than the
+// device's count, so a split, and with it the order of the partial sums, is a
+// fixed function of the shape.
+constexpr int kWaveSms = 152;
 
 // ---------------------------------------------------------------------------
 // 1. Router logits + shared expert gate_up.
@@ -579,22 +583,27 @@ cudaError_t launch_ex(const void* func, dim3 grid, dim3 block, int smem, int clu
 
 template <int K>
 cudaError_t launch_gate_up(MoeArgs a, int num_sms, cudaStream_t s) {
+    (void)num_sms;  // splits are sized for kWaveSms
     const int oblks = 2 * a.inter / 128;
     const int slots = a.T * a.topk;
     const int kblks = a.hidden / 128;
     // Largest input split (CTAs per cluster, <= 8) for which the routed CTAs
-    // plus the shared gate_up CTAs fit in one wave of 3 CTAs per SM.
+    // plus the shared gate_up CTAs fit in one wave of 3 CTAs per SM; when only
+    // an unsplit grid fits, a split of two is still taken while it needs at
+    // most 1.3 waves (measured on GB300 for the 35B layer: 4 tokens 61 -> 56
+    // us per block; 5 tokens, 1.5 waves, is slower split).
     const int rows_per_cta = kGuWarps * kShRowsPerWarp;
     auto shared_z = [&](int per_z) {
         return a.sh_inter > 0 ? (2 * a.sh_inter + per_z * rows_per_cta - 1) / (per_z * rows_per_cta) : 0;
     };
+    auto ctas = [&](int cs) { return (long long)cs * oblks * (slots + shared_z(cs * oblks)); };
     int csize = 1;
     for (int c = 1; c <= 8 && c <= kblks; ++c) {
         const int per = (kblks + c - 1) / c;
         const int cs = (kblks + per - 1) / per;
-        const int per_z = cs * oblks;
-        if ((long long)per_z * (slots + shared_z(per_z)) <= 3LL * num_sms) csize = cs;
+        if (ctas(cs) <= 3LL * kWaveSms) csize = cs;
     }
+    if (csize == 1 && kblks >= 2 && 10 * ctas(2) <= 13LL * 3 * kWaveSms) csize = 2;
     const int per = (kblks + csize - 1) / csize;
     csize = (kblks + per - 1) / per;
     a.gu_kt_per_cta = per * 8;
@@ -609,10 +618,15 @@ cudaError_t launch_gate_up(MoeArgs a, int num_sms, cudaStream_t s) {
 }
 
 template <int K>
-cudaError_t launch_down(MoeArgs a, cudaStream_t s) {
+cudaError_t launch_down(MoeArgs a, int num_sms, cudaStream_t s) {
+    (void)num_sms;  // splits are sized for kWaveSms
     // Split each expert's input in two when it spans an even number (>= 2)
-    // of Hadamard blocks and the cluster stays within 16 CTAs.
-    a.dn_ksplit = ((a.inter / 128) % 2 == 0 && 2 * a.topk <= kMaxCluster) ? 2 : 1;
+    // of Hadamard blocks, the cluster stays within 16 CTAs and the split grid
+    // still fits one wave of 3 CTAs per SM (one token for the 35B layer;
+    // from 2 tokens on the unsplit grid was measured faster on GB300, e.g. 8
+    // tokens 109 -> 92 us per block).
+    const long long split_ctas = 2LL * a.topk * (a.hidden / 128) * a.T;
+    a.dn_ksplit = ((a.inter / 128) % 2 == 0 && 2 * a.topk <= kMaxCluster && split_ctas <= 3LL * kWaveSms) ? 2 : 1;
     const int csz = a.topk * a.dn_ksplit;
     a.dn_xt_floats = (a.inter / a.dn_ksplit + 31) / 32 * 32;
     // routed inputs of one rank, then the shared expert's inputs (swizzled
@@ -647,8 +661,8 @@ cudaError_t launch_moe_gate_up(const MoeArgs& a, int num_sms, cudaStream_t s) {
     return a.gu_K == 2 ? launch_gate_up<2>(a, num_sms, s) : launch_gate_up<3>(a, num_sms, s);
 }
 
-cudaError_t launch_moe_down(const MoeArgs& a, cudaStream_t s) {
-    return a.dn_K == 2 ? launch_down<2>(a, s) : launch_down<3>(a, s);
+cudaError_t launch_moe_down(const MoeArgs& a, int num_sms, cudaStream_t s) {
+    return a.dn_K == 2 ? launch_down<2>(a, num_sms, s) : launch_down<3>(a, num_sms, s);
 }
 
 }  // namespace escha

@@ -263,7 +263,7 @@ typedef struct escha_moe_layer {
  * to 0 when its first kernel starts and to a non-zero value if a kernel had
  * to give up waiting on a cluster peer (it then returns instead of hanging;
  * the outputs of that call are invalid). Read it after synchronising.
- * Batches of up to 12 tokens run fused decode GEMVs per (token, expert);
+ * Batches of up to 16 tokens run fused decode GEMVs per (token, expert);
  * larger batches group the tokens by expert and decode each expert's codes
  * once per work item of up to 128 of its tokens, feeding tcgen05
  * tensor-core MMAs.
@@ -297,8 +297,8 @@ int escha_moe_block_timed(const escha_moe_layer* L, const uint16_t* x, int T, fl
  * every GPU that loads the library holds until the process exits.
  *   - Calls whose escha_moe_block_workspace(L, T) exceeds the buffer are
  *     rejected with ESCHA_E_WORKSPACE before anything is enqueued: for a
- *     hidden-2048, inter-512, 256-expert, top-8 layer, T <= 12 fits (the
- *     per-slot path, 548 KB at T = 12); the grouped path of T >= 13 needs
+ *     hidden-2048, inter-512, 256-expert, top-8 layer, T <= 16 fits (the
+ *     per-slot path, 731 KB at T = 16); the grouped path of T >= 17 needs
  *     several MB (its B image) and is rejected.
  *   - The first call on a device looks the buffer's device address up
  *     (cudaGetSymbolAddress); make that first call before any stream capture.

@@ -77,12 +77,14 @@ def test_moe_block_full_size_batch1(native):
     assert len(set(ids[0])) == 8
 
 
-def test_moe_block_per_slot_path_at_its_largest_batch(native):
-    """12 tokens, the largest batch of the per-slot path, full-size block:
-    96 slots, the fused shared expert in three passes of 4 tokens."""
+@pytest.mark.parametrize("T", [4, 12, 16])
+def test_moe_block_per_slot_path_full_size(native, T):
+    """Full-size block on the per-slot path: 4 tokens (gate_up inputs split
+    over two CTAs in 1.3 waves), 12, and 16 tokens, the largest batch of the
+    path (128 slots, the fused shared expert in four passes of 4 tokens)."""
     d = gen.moe_layer(1005)
-    x = gen.fp16_normal(gen.rng(2006), (12, 2048))
-    _check_block(native, d, x, topk=8, tokens=[0, 5, 11])
+    x = gen.fp16_normal(gen.rng(2006 + T), (T, 2048))
+    _check_block(native, d, x, topk=8, tokens=[0, T // 2, T - 1])
 
 
 def test_router_ids_bit_exact_many_tokens(native):
@@ -137,7 +139,7 @@ def test_moe_pruned_gate_up_channels_stay_zero(native):
 
 
 # --------------------------------------------------------------- grouped path
-# More than 12 tokens per call run the grouped path: tokens sorted by expert,
+# More than 16 tokens per call run the grouped path: tokens sorted by expert,
 # each expert decoded once per work item of up to 128 tokens into tcgen05
 # MMAs.
 
@@ -165,7 +167,7 @@ def test_moe_grouped_full_size_batch64_sampled(native):
 
 
 @pytest.mark.parametrize("T,E,topk,tokens", [
-    (16, 64, 8, None),                    # item capacity 16, runs of 1-4 tokens
+    (17, 64, 8, None),                    # item capacity 16, runs of 1-4 tokens
     (96, 32, 4, range(0, 96, 5)),         # capacity 32
     (700, 4, 1, range(0, 700, 23)),       # capacity 128, two and more items per expert
     (130, 16, 8, range(0, 130, 9)),       # capacity 128, ragged runs
