@@ -572,7 +572,7 @@ def extended(dev, blocks, hbm, tflops):
 
 
 PROFILE_CASES = ("block_b1", "block_b8", "block_b64", "block_b256", "prefill_2048", "projection_b1",
-                 "int8_m1", "int8_m2048", "dense_m1", "dense_m2048")
+                 "int8_m1", "int8_m2048", "dense_m1", "dense_m2048", "dense_split_m13")
 
 
 def profile_case(name: str, reps: int):
@@ -599,9 +599,10 @@ def profile_case(name: str, reps: int):
             native.trellis_gemv(pj["codes"][i % 64], pj["x"][i % 64:i % 64 + 1], pj["rin"][i % 64],
                                 pj["rout"][i % 64], y=y[i % 64:i % 64 + 1])
     elif name.startswith("dense_"):
-        M = 1 if name == "dense_m1" else 2048
-        n_in, n_out = 5120, 17408
-        codes = torch.randint(-32768, 32768, (n_in // 16, n_out // 16, 32), dtype=torch.int16, device=dev)
+        # 5120 -> 17408 K=2 at 1 or 2048 tokens; 17408 -> 5120 K=3 at 13 tokens (inputs split over CTAs)
+        M = {"dense_m1": 1, "dense_m2048": 2048, "dense_split_m13": 13}[name]
+        n_in, n_out, K = (17408, 5120, 3) if name == "dense_split_m13" else (5120, 17408, 2)
+        codes = torch.randint(-32768, 32768, (n_in // 16, n_out // 16, 16 * K), dtype=torch.int16, device=dev)
         rin = (torch.randint(0, 2, (n_in,), device=dev) * 2 - 1).to(torch.float16)
         rout = (torch.rand(n_out, device=dev) + 0.5).to(torch.float16)
         lin = native.DenseLinear(codes, rin, rout, bias=torch.randn(n_out, device=dev), nt_major=True)

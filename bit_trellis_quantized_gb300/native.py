@@ -466,6 +466,47 @@ class MoeBlock:
         self.layer = self._struct()
         self._ws = None
 
+    @classmethod
+    def from_checkpoint(cls, ckpt: "Checkpoint", prefix: str, topk: int = 8, device="cuda", names: dict | None = None):
+        """The block under ``prefix`` (e.g. "model.layers.0.mlp") of an opened
+        checkpoint: stacked experts ``experts.gate_up_proj`` / ``experts.down_proj``
+        (coded leaves, kt-major), router ``gate.weight``, and, when present,
+        the int8 shared expert ``shared_expert.{gate_up,down}_proj.weight_int8``
+        with ``weight_scale`` and its gate ``shared_expert_gate.weight``.
+        ``names`` overrides any of these relative names."""
+        n = {"gate_up": "experts.gate_up_proj", "down": "experts.down_proj", "router": "gate.weight",
+             "sh_gu_w8": "shared_expert.gate_up_proj.weight_int8",
+             "sh_gu_s": "shared_expert.gate_up_proj.weight_scale",
+             "sh_dn_w8": "shared_expert.down_proj.weight_int8", "sh_dn_s": "shared_expert.down_proj.weight_scale",
+             "sh_gate": "shared_expert_gate.weight"}
+        n.update(names or {})
+        full = {k: f"{prefix}.{v}" for k, v in n.items()}
+        projs = {p["prefix"]: i for i, p in enumerate(ckpt.projections())}
+        for k in ("gate_up", "down"):
+            if full[k] not in projs:
+                raise ValueError(f"checkpoint has no coded projection {full[k]}")
+        gu = ckpt.load_projection(projs[full["gate_up"]], device=device)
+        dn = ckpt.load_projection(projs[full["down"]], device=device)
+        if not gu["info"]["n_experts"] or gu["info"]["n_experts"] != dn["info"]["n_experts"]:
+            raise ValueError(f"{prefix}: expert projections must be stacked with one expert count")
+        arrays = {"hidden": gu["info"]["in"], "inter": dn["info"]["in"], "n_experts": gu["info"]["n_experts"],
+                  "Wg": ckpt.read(full["router"]),
+                  "gu_codes": gu["codes"], "gu_rin": gu["rin"], "gu_rout": gu["rout"],
+                  "dn_codes": dn["codes"], "dn_rin": dn["rin"], "dn_rout": dn["rout"], "sh_inter": 0}
+        try:
+            ckpt.tensor_info(full["sh_gu_w8"])
+            has_shared = True
+        except EschaError:
+            has_shared = False
+        if has_shared:
+            arrays["sh_gu_w8"] = ckpt.read(full["sh_gu_w8"])
+            arrays["sh_inter"] = arrays["sh_gu_w8"].shape[0] // 2
+            arrays["sh_gu_s"] = ckpt.read(full["sh_gu_s"])
+            arrays["sh_dn_w8"] = ckpt.read(full["sh_dn_w8"])
+            arrays["sh_dn_s"] = ckpt.read(full["sh_dn_s"])
+            arrays["sh_gate"] = ckpt.read(full["sh_gate"]).reshape(-1)
+        return cls(arrays, device=device, topk=topk)
+
     def _struct(self) -> EschaMoeLayer:
         t = self.t
         L = EschaMoeLayer()

@@ -86,9 +86,32 @@ def small_export(seed: int, hidden: int = 256, inter: int = 128, n_experts: int 
     t["model.layers.0.mlp.gate.weight"] = gen.fp16_normal(g, (n_experts, hidden), std=0.02)
     W8, s = gen.int8_matrix(seed + 1, 2 * inter, hidden)
     t["model.layers.0.mlp.shared_expert.gate_up_proj.weight_int8"] = W8
-    t["model.layers.0.mlp.shared_expert.gate_up_proj.scales"] = s
+    t["model.layers.0.mlp.shared_expert.gate_up_proj.weight_scale"] = s
     for name, (i, o, K) in {"self_attn.q_proj": (hidden, hidden, 2), "self_attn.o_proj": (hidden, hidden, 2),
                             "mlp.gate_proj": (hidden, dense_inter, 2), "mlp.up_proj": (hidden, dense_inter, 3),
                             "mlp.down_proj": (dense_inter, hidden, 3)}.items():
         t.update(coded_projection(g, f"model.layers.1.{name}", i, o, K, bias=True))
+    return t
+
+
+def moe_layer_export(d: dict, prefix: str = "model.layers.0.mlp") -> dict:
+    """The tensors of one MoE block (a ``gen.moe_layer`` dict) under export
+    names: stacked expert projections as coded leaves, the fp16 router
+    ``gate.weight``, the int8 shared expert (``weight_int8`` with an f32
+    ``weight_scale`` per row) and its fp16 sigmoid gate."""
+    t = {
+        f"{prefix}.experts.gate_up_proj.escha_code": d["gu_codes"].view(np.int16),
+        f"{prefix}.experts.gate_up_proj.escha_rin": d["gu_rin"],
+        f"{prefix}.experts.gate_up_proj.escha_rout": d["gu_rout"],
+        f"{prefix}.experts.down_proj.escha_code": d["dn_codes"].view(np.int16),
+        f"{prefix}.experts.down_proj.escha_rin": d["dn_rin"],
+        f"{prefix}.experts.down_proj.escha_rout": d["dn_rout"],
+        f"{prefix}.gate.weight": d["Wg"],
+    }
+    if d.get("sh_inter"):
+        t[f"{prefix}.shared_expert.gate_up_proj.weight_int8"] = d["sh_gu_w8"]
+        t[f"{prefix}.shared_expert.gate_up_proj.weight_scale"] = d["sh_gu_s"]
+        t[f"{prefix}.shared_expert.down_proj.weight_int8"] = d["sh_dn_w8"]
+        t[f"{prefix}.shared_expert.down_proj.weight_scale"] = d["sh_dn_s"]
+        t[f"{prefix}.shared_expert_gate.weight"] = d["sh_gate"]
     return t

@@ -90,3 +90,23 @@ def test_dense_linear_on_loaded_tensors(native, tmp_path, M):
                          bias=exp[pre + ".bias"].astype(np.float64))
     assert rel_err_rows(y, ref).max() <= TOL
     c.close()
+
+
+@pytest.mark.parametrize("T", [3, 20])
+def test_moe_block_from_checkpoint_matches_arrays(native, tmp_path, T):
+    """A MoE block built from an export (stacked coded experts, fp16 router,
+    int8 shared expert) gives bit for bit the outputs of the same block built
+    from the arrays, on the per-slot (3 tokens) and grouped (20) paths."""
+    d = gen.moe_layer(31, hidden=512, inter=256, n_experts=16, k_gu=3, k_dn=2)
+    path = tmp_path / "moe.safetensors"
+    ckpt.write_safetensors(path, ckpt.moe_layer_export(d))
+    c = native.Checkpoint(str(path))
+    blk_c = native.MoeBlock.from_checkpoint(c, "model.layers.0.mlp", topk=4)
+    blk_a = native.MoeBlock(d, topk=4)
+    assert (blk_c.gu_K, blk_c.dn_K, blk_c.sh_inter) == (3, 2, 256)
+    x = torch.from_numpy(gen.fp16_normal(gen.rng(32), (T, 512))).cuda()
+    out_c, ids_c, w_c = blk_c(x)
+    out_a, ids_a, w_a = blk_a(x)
+    assert torch.equal(ids_c, ids_a) and torch.equal(w_c, w_a)
+    assert torch.equal(out_c, out_a)
+    c.close()
