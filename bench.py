@@ -632,12 +632,17 @@ def main():
                                                                "single projection, int8 shapes, 40-block stack)")
     ap.add_argument("--no-graph", action="store_true", help="launch the steps directly (for profilers)")
     ap.add_argument("--layers", type=int, default=N_LAYERS, help="distinct layers cycled through")
-    ap.add_argument("--profile-case", choices=PROFILE_CASES, help="run one workload with direct launches "
-                                                                  "(for profilers) and exit")
+    ap.add_argument("--profile-case", help="comma-separated workloads (" + ", ".join(PROFILE_CASES) +
+                                           ") run with direct launches (for profilers), then exit")
     ap.add_argument("--reps", type=int, default=3, help="launches of --profile-case")
     args = ap.parse_args()
     if args.profile_case:
-        profile_case(args.profile_case, args.reps)
+        cases = args.profile_case.split(",")
+        bad = [c for c in cases if c not in PROFILE_CASES]
+        if bad:
+            ap.error(f"unknown --profile-case {bad}; choose from {PROFILE_CASES}")
+        for c in cases:
+            profile_case(c, args.reps)
         return
     if args.warmup < 3:
         args.warmup = 3
