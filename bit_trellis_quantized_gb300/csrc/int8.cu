@@ -178,6 +178,27 @@ __global__ void __launch_bounds__(256) int8_gemv_m1_kernel(const int8_t* __restr
     const int g = warp / wpg, cw = warp % wpg;
     const int rows_per_tile = G * kRowsPerWarp;
     const int ntiles = (N + rows_per_tile - 1) / rows_per_tile;
+    // The first tiles' weight loads go out before the wait for the preceding
+    // kernel (weights are never its output); x and y only after it.
+    uint4 wv[TPI][CPW][kRowsPerWarp];
+    auto load_tiles = [&](int t0) {
+#pragma unroll
+        for (int tt = 0; tt < TPI; ++tt) {
+            const int r0 = ((t0 + tt) * G + g) * kRowsPerWarp;
+#pragma unroll
+            for (int q = 0; q < CPW; ++q) {
+                const int i0 = (cw + q * wpg) * 512 + lane * 16;
+                if (cw + q * wpg >= nch || i0 >= Kin || t0 + tt >= ntiles) continue;
+#pragma unroll
+                for (int r = 0; r < kRowsPerWarp; ++r)
+                    wv[tt][q][r] = ldg_stream_v4(W + (long long)min(r0 + r, N - 1) * Kin + i0);
+            }
+        }
+    };
+    const int first = blockIdx.x * TPI;
+    if (first < ntiles) load_tiles(first);
+    pdl_wait();
+    pdl_trigger();
     float xv[CPW][16];
 #pragma unroll
     for (int q = 0; q < CPW; ++q) {
@@ -211,20 +232,8 @@ __global__ void __launch_bounds__(256) int8_gemv_m1_kernel(const int8_t* __restr
             }
         }
     }
-    for (int t0 = blockIdx.x * TPI; t0 < ntiles; t0 += gridDim.x * TPI) {
-        uint4 wv[TPI][CPW][kRowsPerWarp];
-#pragma unroll
-        for (int tt = 0; tt < TPI; ++tt) {
-            const int r0 = ((t0 + tt) * G + g) * kRowsPerWarp;
-#pragma unroll
-            for (int q = 0; q < CPW; ++q) {
-                const int i0 = (cw + q * wpg) * 512 + lane * 16;
-                if (cw + q * wpg >= nch || i0 >= Kin || t0 + tt >= ntiles) continue;
-#pragma unroll
-                for (int r = 0; r < kRowsPerWarp; ++r)
-                    wv[tt][q][r] = ldg_stream_v4(W + (long long)min(r0 + r, N - 1) * Kin + i0);
-            }
-        }
+    for (int t0 = first; t0 < ntiles; t0 += gridDim.x * TPI) {
+        if (t0 != first) load_tiles(t0);
 #pragma unroll
         for (int tt = 0; tt < TPI; ++tt) {
 #pragma unroll
@@ -275,8 +284,10 @@ cudaError_t launch_m1(const int8_t* W, const float* scales, int N, int Kin, cons
     const int smem = rows_per_it * nch * (int)sizeof(float);
     const long long its = (N + rows_per_it - 1) / rows_per_it;
     const int grid = static_cast<int>(its < 4LL * num_sms ? its : 4LL * num_sms);
-    int8_gemv_m1_kernel<CPW><<<grid, 256, smem, s>>>(W, scales, N, Kin, x, x_dtype, y, G, nch);
-    return cudaGetLastError();
+    void* args[] = {const_cast<int8_t**>(&W), const_cast<float**>(&scales), &N, &Kin, const_cast<void**>(&x),
+                    &x_dtype, &y, &G, &nch};
+    return launch_kernel(reinterpret_cast<const void*>(int8_gemv_m1_kernel<CPW>), dim3(grid), dim3(256), smem, true,
+                         s, args);
 }
 
 template <int MT>

@@ -23,6 +23,13 @@
  *   - Scratch memory comes from the caller's workspace `ws` of `ws_bytes`
  *     bytes; each entry point has a *_workspace() query. A larger workspace
  *     is accepted. The library allocates no device memory.
+ *   - Kernels are launched with programmatic dependent launch: a kernel may
+ *     start while the kernel enqueued before it on the stream is finishing,
+ *     and it reads weights (code tensors, rin / rout, int8 matrices, scales,
+ *     router weights) before waiting for that kernel. Activations and
+ *     outputs are only touched after the wait. So weights must not be
+ *     written by the kernel launched just before the call on the same stream
+ *     (a copy, an event or any other kernel in between is enough).
  *   - Every argument is validated before anything is enqueued. On error the
  *     call returns a negative ESCHA_E_* code, enqueues nothing, and
  *     escha_last_error() describes the problem. Asynchronous device faults
