@@ -417,6 +417,7 @@ __global__ void __launch_bounds__(kDnThreads, 3) moe_down_kernel(const MoeArgs a
     uint2 rin_pre = make_uint2(0u, 0u);
     if (warp < nk / 128) rin_pre = *reinterpret_cast<const uint2*>(rin + kt0 * 16 + warp * 128 + 4 * lane);
     pdl_wait();  // gate_up outputs and the shared expert's gate_up
+    pdl_trigger();  // a dependent (the next residual norm) waits for this grid before reading
 
     // the shared expert's down input, SwiGLU(shgu[t]): its loads (two per
     // thread for sh_inter <= 512) go out together with the routed input

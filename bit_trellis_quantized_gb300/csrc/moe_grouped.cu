@@ -590,6 +590,7 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeArgs a, const
     __shared__ float red[8];
     __shared__ float gate_s;
     pdl_wait();
+    pdl_trigger();  // a dependent (the next residual norm) waits for this grid before reading
     const float* wt = a.w + (long long)t * a.topk;
     const uint16_t* xr = a.x + (long long)t * a.hidden;
     const bool two = a.hidden <= 2 * 4 * 256 && a.topk <= kCombineMaxK;

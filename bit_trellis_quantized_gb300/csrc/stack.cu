@@ -72,7 +72,9 @@ __global__ void __launch_bounds__(kNormThreads) residual_rmsnorm_kernel(float* _
 cudaError_t launch_residual_rmsnorm(float* h, const float* add, int T, int hidden, float eps, uint16_t* x,
                                     cudaStream_t s) {
     void* args[] = {&h, const_cast<float**>(&add), &hidden, &eps, &x};
-    return launch_kernel(reinterpret_cast<const void*>(residual_rmsnorm_kernel), dim3(T), dim3(kNormThreads), 0, false,
+    // programmatic launch: the CTAs wait (griddepcontrol.wait) for the block
+    // that wrote `add` instead of waiting to be launched
+    return launch_kernel(reinterpret_cast<const void*>(residual_rmsnorm_kernel), dim3(T), dim3(kNormThreads), 0, true,
                          s, args);
 }
 
