@@ -334,32 +334,39 @@ struct HalfRowCodes {
     uint32_t p[K + 1];
 };
 
-// Tile row kt, tile columns nt0 .. nt0 + 3 of a code tensor with tile grid g;
-// the lane reads tile nt0 + lane/8.
+// The lane's K 32-bit words at b: words (lane % 8) * 2K .. of its tile
+// (64 B per tile at K = 2, 8-byte aligned per lane; 96 B at K = 3, 4-byte
+// aligned).
 template <int K>
-__device__ __forceinline__ void load_half_row(HalfRowCodes<K>& lc, const uint16_t* codes, const TileStrides& g, int kt,
-                                              int nt0, int lane) {
-    const uint16_t* b = codes + ((long long)kt * g.s_kt + (long long)(nt0 + (lane >> 3)) * g.s_nt) * (16 * K) +
-                        (lane & 7) * (2 * K);
+__device__ __forceinline__ void load_half_row_at(HalfRowCodes<K>& lc, const uint16_t* b) {
     if constexpr (K == 2) {
-        const uint2 v = ldg_stream_v2(b);  // 8-byte aligned: 64 B per tile, 8 B per lane
+        const uint2 v = ldg_stream_v2(b);
         lc.p[0] = v.x;
         lc.p[1] = v.y;
     } else {
-        lc.p[0] = ldg_stream_u32(b);  // 4-byte aligned: 96 B per tile, 12 B per lane
+        lc.p[0] = ldg_stream_u32(b);
         lc.p[1] = ldg_stream_u32(b + 2);
         lc.p[2] = ldg_stream_u32(b + 4);
     }
 }
 
-// The lane's 32 weights (input rows 2c, 2c+1; 16 output columns of tile
-// tile0 + lane/8) into the MN-major A slice of the tile row: element (m, k) at
-// mnmajor_off(m, k, 2048, 1024). Needs lc.p[K] = the next lane's first word.
-template <int K>
-__device__ __forceinline__ void decode_half_row_to_smem(const HalfRowCodes<K>& lc, uint8_t* slice, int lane,
-                                                        int tile0) {
-    const int c = lane & 7;
+// Byte offsets, inside a tile row's A slice, of the lane's four 16-byte
+// stores: index 2 * rr + h = input row 2c + rr, columns 8h .. 8h + 7 of the
+// lane's tile (tile0 + lane / 8); element (m, k) sits at
+// mnmajor_off(m, k, 2048, 1024).
+__device__ __forceinline__ void half_row_store_offsets(uint32_t (&off)[4], int lane, int tile0) {
+    const uint32_t c = static_cast<uint32_t>(lane & 7);
     const uint32_t m0 = 16u * static_cast<uint32_t>(tile0 + (lane >> 3));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) off[i] = tc::mnmajor_off(m0 + 8u * (i & 1), 2u * c + (i >> 1), 2048u, 1024u);
+}
+
+// The lane's 32 weights (input rows 2c, 2c+1; 16 output columns of its
+// tile) into the MN-major A slice of the tile row at the offsets above.
+// Needs lc.p[K] = the next lane's first word.
+template <int K>
+__device__ __forceinline__ void decode_half_row_to_smem(const HalfRowCodes<K>& lc, uint8_t* slice,
+                                                        const uint32_t (&off)[4]) {
     if constexpr (K == 2) {  // weights (row rr, col m) and (row rr, col m + 8) share a window
         const uint32_t q[3] = {stream_pair(lc.p[0]), stream_pair(lc.p[1]), stream_pair(lc.p[2])};
         static_for<2>([&](auto R) {
@@ -377,8 +384,7 @@ __device__ __forceinline__ void decode_half_row_to_smem(const HalfRowCodes<K>& l
                     const __half2 w2 = __halves2half2(w[8 * h + 2 * p], w[8 * h + 2 * p + 1]);
                     packed[p] = *reinterpret_cast<const uint32_t*>(&w2);
                 }
-                *reinterpret_cast<uint4*>(slice + tc::mnmajor_off(m0 + 8u * h, 2u * c + rr, 2048u, 1024u)) =
-                    make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                *reinterpret_cast<uint4*>(slice + off[2 * rr + h]) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
             });
         });
         return;
@@ -395,10 +401,7 @@ __device__ __forceinline__ void decode_half_row_to_smem(const HalfRowCodes<K>& l
             const __half2 w2 = cb_decode_h2(s0, s1);
             packed[p] = *reinterpret_cast<const uint32_t*>(&w2);
         });
-        const uint32_t k = 2u * c + (j >> 1);
-        const uint32_t m = m0 + 8u * (j & 1);
-        *reinterpret_cast<uint4*>(slice + tc::mnmajor_off(m, k, 2048u, 1024u)) =
-            make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        *reinterpret_cast<uint4*>(slice + off[j]) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
     });
 }
 
@@ -465,38 +468,36 @@ __global__ void __launch_bounds__(tc::kMlThreads + 32, 2)
     const int kb0 = blockIdx.z * p.kblk_per_split;                // first 64-input block of this K split
     const int nblk = min((p.in >> 6) - kb0, p.kblk_per_split);  // blocks of 64 inputs = 4 tile rows
     const int hr = warp >> 1, half = warp & 1;
-    // three register sets used in turn: block b + 2's codes load into one
-    // while block b is decoded from another, so a load has two blocks of
-    // decode time to arrive; no set is ever copied (a copy would wait for the
-    // load)
-    HalfRowCodes<K> c0, c1, c2;
-    if (warp < kDecodeWarps) {
-        load_half_row<K>(c0, codes, p.grid, 4 * kb0 + hr, ob * 8 + 4 * half, lane);
-        if (nblk > 1) load_half_row<K>(c1, codes, p.grid, 4 * (kb0 + 1) + hr, ob * 8 + 4 * half, lane);
-    }
-    int rot = 0;  // b % 3
+    // two register sets by chunk parity: chunk b + 1's codes load into one
+    // while chunk b is decoded from the other (no set is ever copied: a copy
+    // would wait for the load). The lane's code pointer advances by one
+    // 64-input block (4 tile rows) per chunk.
+    HalfRowCodes<K> c0, c1;
+    const long long blk_step = 4 * p.grid.s_kt * (16 * K);
+    const uint16_t* cp = codes + ((long long)(4 * kb0 + hr) * p.grid.s_kt +
+                                  (long long)(ob * 8 + 4 * half + (lane >> 3)) * p.grid.s_nt) * (16 * K) +
+                         (lane & 7) * (2 * K);
+    uint32_t soff[4];
+    half_row_store_offsets(soff, lane, 4 * half);
+    if (warp < kDecodeWarps) load_half_row_at<K>(c0, cp);
     const int nbr = (lane & ~7) | ((lane + 1) & 7);
     const uint8_t* img = a.grp_img + (long long)desc.z * 128 + (long long)kb0 * a.grp_img_rows * 128;
 
     const bool ok = tc::mma_mainloop_ws<STAGES, true>(
         Abuf, Bbuf, b_chunk, img, (long long)a.grp_img_rows * 128, 256u * static_cast<uint32_t>(nt4), nblk, tmem,
         idesc, bars, [&](int b, uint8_t* A) {
-            const bool more = b + 2 < nblk;
+            const bool more = b + 1 < nblk;
             uint8_t* slice = A + hr * 4096;
-            if (rot == 0) {
-                if (more) load_half_row<K>(c2, codes, p.grid, 4 * (kb0 + b + 2) + hr, ob * 8 + 4 * half, lane);
+            cp += blk_step;
+            if ((b & 1) == 0) {
+                if (more) load_half_row_at<K>(c1, cp);
                 c0.p[K] = __shfl_sync(0xffffffffu, c0.p[0], nbr) & 0xFFFFu;
-                decode_half_row_to_smem<K>(c0, slice, lane, 4 * half);
-            } else if (rot == 1) {
-                if (more) load_half_row<K>(c0, codes, p.grid, 4 * (kb0 + b + 2) + hr, ob * 8 + 4 * half, lane);
-                c1.p[K] = __shfl_sync(0xffffffffu, c1.p[0], nbr) & 0xFFFFu;
-                decode_half_row_to_smem<K>(c1, slice, lane, 4 * half);
+                decode_half_row_to_smem<K>(c0, slice, soff);
             } else {
-                if (more) load_half_row<K>(c1, codes, p.grid, 4 * (kb0 + b + 2) + hr, ob * 8 + 4 * half, lane);
-                c2.p[K] = __shfl_sync(0xffffffffu, c2.p[0], nbr) & 0xFFFFu;
-                decode_half_row_to_smem<K>(c2, slice, lane, 4 * half);
+                if (more) load_half_row_at<K>(c0, cp);
+                c1.p[K] = __shfl_sync(0xffffffffu, c1.p[0], nbr) & 0xFFFFu;
+                decode_half_row_to_smem<K>(c1, slice, soff);
             }
-            rot = rot == 2 ? 0 : rot + 1;
         });
     if (!ok && tid == 0) atomicExch(a.err, 3);
 
