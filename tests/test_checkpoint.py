@@ -191,3 +191,49 @@ def test_export_projections_and_raw_reads(native, tmp_path):
     with pytest.raises(native.EschaError):
         c.tensor_info("no.such.tensor")
     c.close()
+
+
+def test_loader_matches_oracle_on_generated_exports(native, tmp_path):
+    """Random exports (seeded draws of projection shapes, K, expert counts,
+    optional leaves, biases, missing or unknown leaves, shard splits): the
+    native loader and the oracle agree on every verdict and, for valid
+    exports, on every projection's description."""
+    rng = np.random.default_rng(20261202)
+    for case in range(60):
+        g = gen.rng(1000 + case)
+        t = {}
+        n_proj = int(rng.integers(1, 5))
+        for i in range(n_proj):
+            layer = int(rng.integers(0, 3))
+            prefix = f"model.layers.{layer}.p{i}"
+            experts = int(rng.integers(0, 3)) if rng.random() < 0.5 else 0
+            n_in, n_out = 16 * int(rng.integers(1, 5)), 16 * int(rng.integers(1, 5))
+            K = int(rng.integers(2, 4))
+            t.update(ckpt.coded_projection(g, prefix, n_in, n_out, K, experts=experts,
+                                           bias=(not experts) and rng.random() < 0.5,
+                                           optional=rng.random() < 0.3))
+        names = sorted(t)
+        fault = rng.random()
+        if fault < 0.15:
+            victim = names[int(rng.integers(0, len(names)))]
+            if ".escha_" in victim or victim.endswith(".bias"):
+                del t[victim]
+        elif fault < 0.25:
+            t[names[0].rsplit(".", 1)[0] + ".escha_rotation_theta"] = np.zeros(3, np.float32)
+        elif fault < 0.35:
+            code = [n for n in names if n.endswith(".escha_code")][0]
+            sh = list(t[code].shape)
+            sh[-1] = int(rng.choice([16, 40, 64]))
+            t[code] = np.zeros(sh, np.int16)
+        t["model.embed_tokens.weight_int8"] = np.ones((4, 16), np.int8)
+        names = sorted(t)
+        if rng.random() < 0.5:
+            cut = int(rng.integers(1, len(names)))
+            paths = [_write(tmp_path, {k: t[k] for k in names[:cut]}, name=f"g{case}a.safetensors"),
+                     _write(tmp_path, {k: t[k] for k in names[cut:]}, name=f"g{case}b.safetensors")]
+        else:
+            paths = [_write(tmp_path, t, name=f"g{case}.safetensors")]
+        ov, nv = _oracle_verdict(paths), _native_verdict(native, paths)
+        assert nv[0] == ov[0], (case, nv, ov)
+        if ov[0] == "ok":
+            assert nv[1] == ov[1], case
