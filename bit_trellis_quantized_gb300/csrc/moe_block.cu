@@ -74,8 +74,7 @@ __device__ void router_logits(const MoeArgs& a, int warp, int lane) {
     const int e = blockIdx.x * kK0Warps + warp;
     const int t0 = blockIdx.y * kLgTG;
     const int nt = min(kLgTG, a.T - t0);
-    if (e >= a.E) return;
-    const uint16_t* wrow = a.router_w + (long long)e * a.hidden;
+    const uint16_t* wrow = a.router_w + (long long)(e < a.E ? e : 0) * a.hidden;
     const int passes = a.hidden >> 8;
     float acc[kLgTG];
 #pragma unroll
@@ -85,6 +84,13 @@ __device__ void router_logits(const MoeArgs& a, int warp, int lane) {
 #pragma unroll
         for (int q = 0; q < 8; ++q)
             if (pg + q < passes) wv[q] = ldg_stream_v4(wrow + (pg + q) * 256 + lane * 8);
+        if (pg == 0) {
+            // the first weights are in flight; x (and the workspace, which the
+            // previous call's kernels may still read) only after the wait
+            pdl_wait();
+            if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *a.err = 0;  // the previous call has finished
+            if (e >= a.E) return;
+        }
 #pragma unroll
         for (int t = 0; t < kLgTG; ++t) {
             if (t < nt) {
@@ -177,8 +183,7 @@ __global__ void __launch_bounds__(kK0Threads) moe_router_kernel(const MoeArgs a)
     // this grid before reading the logits.
     pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *a.err = 0;  // the whole previous call has finished
-    router_logits(a, warp, lane);
+    router_logits(a, warp, lane);  // waits for the preceding kernel after its first weight loads
 }
 
 // Router logits for many tokens: a CTA stages 16 tokens of x in shared memory
@@ -190,8 +195,9 @@ constexpr int kRtTok = 16, kRtExpW = 2, kRtExp = 8 * kRtExpW, kRtCols = 1024;
 __global__ void __launch_bounds__(256) moe_router_tiled_kernel(const MoeArgs a) {
     __shared__ __align__(16) uint16_t xs[kRtTok][kRtCols];
     pdl_trigger();
+    pdl_wait();  // x and the workspace (the previous call's kernels may still read it)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) *a.err = 0;  // the whole previous call has finished
+    if (blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) *a.err = 0;  // the previous call has finished
     const int e0 = blockIdx.x * kRtExp + warp * kRtExpW;
     const int t0 = blockIdx.y * kRtTok;
     const int nt = min(kRtTok, a.T - t0);
@@ -650,12 +656,12 @@ cudaError_t launch_moe_router(const MoeArgs& a, cudaStream_t s) {
     if (a.T >= kRtTok) {
         void* args[] = {const_cast<MoeArgs*>(&a)};
         return launch_kernel(reinterpret_cast<const void*>(moe_router_tiled_kernel),
-                             dim3((a.E + kRtExp - 1) / kRtExp, (a.T + kRtTok - 1) / kRtTok), dim3(256), 0, false, s,
+                             dim3((a.E + kRtExp - 1) / kRtExp, (a.T + kRtTok - 1) / kRtTok), dim3(256), 0, true, s,
                              args);
     }
     const int n_lg = (a.E + kK0Warps - 1) / kK0Warps;
     return launch_ex(reinterpret_cast<const void*>(moe_router_kernel), dim3(n_lg, (a.T + kLgTG - 1) / kLgTG),
-                     dim3(kK0Threads), 0, 0, false, s, a);
+                     dim3(kK0Threads), 0, 0, true, s, a);
 }
 
 cudaError_t launch_moe_gate_up(const MoeArgs& a, int num_sms, cudaStream_t s) {
