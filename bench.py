@@ -207,34 +207,48 @@ def cpu_baseline(seconds: float = 15.0, max_tokens: int = 8):
 
 
 def run_reference(args, rank):
+    """The oracle on the host cores, as it stands: exactly args.steps timed
+    steps after args.warmup untimed ones. A step is one eighth of a token
+    (one of its 8 routed experts: gate_up, SwiGLU, down, weighted; the
+    token's router runs at its first step, the shared expert and the combine
+    at its last), so 8 steps are one token of the MoE block and the whole run
+    stays within minutes; value = tokens per second = steps / 8 / time."""
     if rank != 0:
         return
     from oracle import escha_oracle as o
 
-    budget = 150.0
     d = gen.moe_layer(LAYER_SEED)
     layer = o.MoeLayer(**d)
-    n_total = args.warmup + args.steps
-    xs = gen.fp16_normal(gen.rng(X_SEED), (n_total, HIDDEN))
-    t_begin = time.perf_counter()
-    for i in range(min(args.warmup, 1)):
-        o.moe_block(layer, xs[i:i + 1], k=TOPK)
-    times = []
-    for i in range(args.steps):
-        t0 = time.perf_counter()
-        o.moe_block(layer, xs[args.warmup + i:args.warmup + i + 1], k=TOPK)
-        times.append(time.perf_counter() - t0)
-        if time.perf_counter() - t_begin > budget:
-            break
-    ms = 1e3 * sum(times) / len(times)
-    value = 1e3 / ms
+    n_tok = -(-(args.warmup + args.steps) // TOPK) + 1
+    xs = gen.fp16_normal(gen.rng(X_SEED), (n_tok, HIDDEN))
+    state = {}
+
+    def step(i):  # slot j of token t
+        t, j = divmod(i, TOPK)
+        if j == 0:
+            ids, w, _ = o.route(xs[t:t + 1], layer.Wg, TOPK)
+            state.update(ids=ids, w=w, acc=np.zeros(HIDDEN))
+        xv = xs[t].astype(np.float64)
+        state["acc"] += state["w"][0, j] * o.moe_expert(layer, state["ids"][0, j], xv)
+        if j == TOPK - 1:
+            state["out"] = state["acc"] + o.shared_expert(layer, xs[t:t + 1])[0]
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.warmup, args.warmup + args.steps):
+        step(i)
+    elapsed = time.perf_counter() - t0
+    ms = 1e3 * elapsed / args.steps
+    value = args.steps / TOPK / elapsed
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
-            "steps": len(times), "warmup": min(args.warmup, 1), "ms_per_step": ms, "higher_is_better": True,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "batch": 1, "l2": "n/a (CPU)"},
+            "config": {"workload": WORKLOAD, "batch": 1, "l2": "n/a (CPU)",
+                       "step": "one routed expert of one token (8 steps = 1 token)"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": f"{len(times)} of {args.steps} requested steps (one token each, "
-                                       f"capped at {budget:.0f} s) through the numpy float64 oracle"},
+                             "sample": f"{args.steps} steps = {args.steps / TOPK:g} tokens of the batch-1 MoE block "
+                                       f"through the numpy float64 oracle, one thread, {elapsed:.1f} s"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -275,20 +289,24 @@ def run_ours(args, ws, rank, local):
     w_all = torch.empty((n_total, TOPK), dtype=torch.float32, device=dev)
     layer_of = [i % n_layers for i in range(n_total)]
 
-    # One CUDA graph holds STEPS_PER_GRAPH consecutive steps (as a model's
-    # decode graph holds its layers). Every step still runs after the
-    # previous one has finished: the first kernel of a step is launched
-    # without programmatic overlap.
+    # One CUDA graph holds up to STEPS_PER_GRAPH consecutive steps (as a
+    # model's decode graph holds its layers): whole graphs of warm-up steps,
+    # then exactly args.steps timed steps (a shorter last graph when needed).
+    # Like every kernel of the library, a step's first kernel is launched
+    # programmatically: it loads router weights while the previous step's
+    # last kernel finishes and waits for it before touching x or outputs.
+    chunks = [(i0, STEPS_PER_GRAPH) for i0 in range(0, args.warmup, STEPS_PER_GRAPH)]
+    chunks += [(i0, min(STEPS_PER_GRAPH, n_total - i0)) for i0 in range(args.warmup, n_total, STEPS_PER_GRAPH)]
     stream = torch.cuda.Stream(device=dev)
     graphs = []
     with torch.cuda.stream(stream):
         for blk in blocks:  # workspaces sized and kernels loaded before capture
             blk(xs[0:1], out=outs[0:1], ids=ids_all[0:1], w=w_all[0:1])
         torch.cuda.synchronize()
-        for i0 in range(0, n_total if not args.no_graph else 0, STEPS_PER_GRAPH):
+        for i0, n in (chunks if not args.no_graph else []):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
-                for i in range(i0, i0 + STEPS_PER_GRAPH):
+                for i in range(i0, i0 + n):
                     blocks[layer_of[i]](xs[i:i + 1], out=outs[i:i + 1], ids=ids_all[i:i + 1], w=w_all[i:i + 1])
             graphs.append(g)
     torch.cuda.synchronize()
@@ -319,19 +337,19 @@ def run_ours(args, ws, rank, local):
         step_ms = t0.elapsed_time(t1) / args.steps
 
         # end to end through the public API: pinned host x in, out back to host.
-        # Each group of STEPS_PER_GRAPH steps is one graph holding the
+        # Each group of steps (the chunks above) is one graph holding the
         # host-to-device copy of its inputs, the steps, and the device-to-host
         # copy of their outputs.
         out_host = torch.empty((n_total, HIDDEN), dtype=torch.float32).pin_memory()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        n_groups = n_total // STEPS_PER_GRAPH
+        n_groups = len(chunks)
 
         def e2e_group(gi):
-            i0 = gi * STEPS_PER_GRAPH
-            xs[i0:i0 + STEPS_PER_GRAPH].copy_(xs_host[i0:i0 + STEPS_PER_GRAPH], non_blocking=True)
-            for i in range(i0, i0 + STEPS_PER_GRAPH):
+            i0, n = chunks[gi]
+            xs[i0:i0 + n].copy_(xs_host[i0:i0 + n], non_blocking=True)
+            for i in range(i0, i0 + n):
                 blocks[layer_of[i]](xs[i:i + 1], out=outs[i:i + 1], ids=ids_all[i:i + 1], w=w_all[i:i + 1])
-            out_host[i0:i0 + STEPS_PER_GRAPH].copy_(outs[i0:i0 + STEPS_PER_GRAPH], non_blocking=True)
+            out_host[i0:i0 + n].copy_(outs[i0:i0 + n], non_blocking=True)
 
         e2e_graphs = []
         if not args.no_graph:
@@ -398,7 +416,7 @@ def run_ours(args, ws, rank, local):
                    "l2": f"inputs larger than L2: {n_layers} distinct MoE layers "
                          f"({n_layers * 272} MB) cycled, one per step, no flush",
                    "cuda_graph": "none (direct launches)" if args.no_graph else
-                                 f"{STEPS_PER_GRAPH} serialized steps per graph",
+                                 f"up to {STEPS_PER_GRAPH} steps per graph (programmatic launches)",
                    "parallelism": f"replicas x{ws} (independent token streams)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "traffic": measured_traffic(), "kernel": "moe_gate_up_kernel<K=3> (8 routed experts + int8 shared gate_up)",
@@ -422,7 +440,7 @@ def run_ours(args, ws, rank, local):
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "e2e": {"value": aggregate_tokens_per_s(ws, t_e2e), "unit": UNIT, "h2d_bytes_per_step": HIDDEN * 2,
                 "d2h_bytes_per_step": HIDDEN * 4,
-                "note": f"per group of {STEPS_PER_GRAPH} steps, one graph: pinned-host x in, the steps, "
+                "note": f"per group of up to {STEPS_PER_GRAPH} steps, one graph: pinned-host x in, the steps, "
                         f"outputs back to pinned host; all inside the timed region"},
         "clocks": clocks,
         "routing_distinct_in_16_steps": distinct,
@@ -649,13 +667,15 @@ def main():
         return
     if args.warmup < 3:
         args.warmup = 3
-    # whole graphs of STEPS_PER_GRAPH steps
-    args.warmup = -(-args.warmup // STEPS_PER_GRAPH) * STEPS_PER_GRAPH
-    args.steps = -(-args.steps // STEPS_PER_GRAPH) * STEPS_PER_GRAPH
+    if args.steps < 1:
+        args.steps = 1
     ws, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, rank)
         return
+    # warm-up in whole graphs of STEPS_PER_GRAPH steps (at least the W asked
+    # for); exactly args.steps timed steps
+    args.warmup = -(-args.warmup // STEPS_PER_GRAPH) * STEPS_PER_GRAPH
     run_ours(args, ws, rank, local)
 
 
