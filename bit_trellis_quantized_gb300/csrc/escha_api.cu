@@ -134,7 +134,7 @@ cudaError_t int8_matmul(const int8_t* W, const float* scales, int N, int Kin, co
 bool int8_uses_gemm(int Kin, int M) { return M >= escha::kInt8GemmMinM && Kin % 128 == 0; }
 
 struct MoeWs {
-    size_t err, logits, ids, w, ygu, shgu, shgate, sh, d, grp, img, total;
+    size_t err, logits, ids, w, ygu, shgu, shgate, sh, d, grp, img, shimg, total;
 };
 
 MoeWs moe_ws_layout(const escha_moe_layer* L, int T, bool force_grouped = false) {
@@ -165,6 +165,8 @@ MoeWs moe_ws_layout(const escha_moe_layer* L, int T, bool force_grouped = false)
     off += align_up(grouped ? g.int_bytes : 0);
     m.img = off;
     off += align_up(grouped ? g.img_bytes : 0);
+    m.shimg = off;  // the shared expert runs beside the routed path, with its own scratch
+    off += align_up(grouped ? g.shared_img_bytes : 0);
     m.total = off;
     return m;
 }
@@ -411,6 +413,36 @@ escha::MoeArgs moe_args(const escha_moe_layer* L, const uint16_t* x, int T, floa
     return a;
 }
 
+// Second stream and fork / join events of this host thread on a device, on
+// which the grouped path runs the shared expert beside the routed chain.
+// Created on first use outside a stream capture (creation is not a stream
+// operation, but it is kept out of captures); until then, or if creation
+// fails, the shared expert runs in line on the caller's stream.
+struct ForkCtx {
+    bool tried = false;
+    cudaStream_t s2 = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+thread_local ForkCtx g_fork[64];
+
+ForkCtx* fork_ctx(cudaStream_t s) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    ForkCtx& f = g_fork[dev];
+    if (!f.tried) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return nullptr;
+        f.tried = true;
+        if (cudaStreamCreateWithFlags(&f.s2, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&f.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&f.join, cudaEventDisableTiming) != cudaSuccess) {
+            cudaGetLastError();  // leave no sticky error behind; run in line from now on
+            f.s2 = nullptr;
+        }
+    }
+    return f.s2 ? &f : nullptr;
+}
+
 int moe_block_impl(const escha_moe_layer* L, const uint16_t* x, int T, float* out, int32_t* ids_out, float* w_out,
                    void* ws, size_t ws_bytes, void* stream, cudaEvent_t* ev) {
     int r = check_layer(L);
@@ -431,21 +463,34 @@ int moe_block_impl(const escha_moe_layer* L, const uint16_t* x, int T, float* ou
     escha::MoeArgs a = moe_args(L, x, T, out, ids_out, w_out, base, m);
     if (T > escha::kSlotModeMaxT) {
         float* d = reinterpret_cast<float*>(base + m.d);
+        uint8_t* shimg = reinterpret_cast<uint8_t*>(base + m.shimg);
+        // the shared expert needs only x: its int8 GEMMs run on a second
+        // stream beside router -> grouping -> grouped GEMMs (except in the
+        // timed variant, whose events bracket the phases on one stream)
+        auto shared = [&](cudaStream_t st) -> int {
+            int rr;
+            if ((rr = cuda_status(int8_matmul(L->sh_gu_w8, L->sh_gu_scale, 2 * L->sh_inter, L->hidden, x, ESCHA_F16,
+                                              L->hidden, 0, T, a.shgu, 2 * L->sh_inter, shimg, sms, st),
+                                  "shared gate_up launch")))
+                return rr;
+            return cuda_status(int8_matmul(L->sh_dn_w8, L->sh_dn_scale, L->hidden, L->sh_inter, a.shgu, ESCHA_F32,
+                                           2 * L->sh_inter, 1, T, a.sh, L->hidden, shimg, sms, st),
+                               "shared down launch");
+        };
+        ForkCtx* fk = (L->sh_inter > 0 && !ev) ? fork_ctx(s) : nullptr;
+        if (fk) {
+            if ((r = cuda_status(cudaEventRecord(fk->fork, s), "fork record"))) return r;
+            if ((r = cuda_status(cudaStreamWaitEvent(fk->s2, fk->fork, 0), "fork wait"))) return r;
+            if ((r = shared(fk->s2))) return r;
+            if ((r = cuda_status(cudaEventRecord(fk->join, fk->s2), "join record"))) return r;
+        }
         if ((r = record(ev, 0, s))) return r;
         if ((r = cuda_status(escha::launch_moe_router(a, s), "router launch"))) return r;
         if ((r = record(ev, 1, s))) return r;
         if ((r = cuda_status(escha::launch_moe_grouped(a, d, sms, s), "grouped expert launch"))) return r;
         if ((r = record(ev, 2, s))) return r;
-        if (L->sh_inter > 0) {
-            if ((r = cuda_status(int8_matmul(L->sh_gu_w8, L->sh_gu_scale, 2 * L->sh_inter, L->hidden, x, ESCHA_F16,
-                                             L->hidden, 0, T, a.shgu, 2 * L->sh_inter, a.grp_img, sms, s),
-                                 "shared gate_up launch")))
-                return r;
-            if ((r = cuda_status(int8_matmul(L->sh_dn_w8, L->sh_dn_scale, L->hidden, L->sh_inter, a.shgu, ESCHA_F32,
-                                             2 * L->sh_inter, 1, T, a.sh, L->hidden, a.grp_img, sms, s),
-                                 "shared down launch")))
-                return r;
-        }
+        if (L->sh_inter > 0 && !fk && (r = shared(s))) return r;
+        if (fk && (r = cuda_status(cudaStreamWaitEvent(s, fk->join, 0), "join wait"))) return r;
         if ((r = cuda_status(escha::launch_moe_combine(a, d, s), "combine launch"))) return r;
         return record(ev, 3, s);
     }

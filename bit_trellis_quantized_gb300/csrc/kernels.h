@@ -116,7 +116,8 @@ constexpr int kSlotModeMaxT = 16;
 struct GroupPlan {
     int cap, max_items, pos_cap;
     size_t int_bytes;  // items (16 B each, first), counts, offsets, poff, nitems, perm, ppos
-    size_t img_bytes;  // B image (shared by both projections and the shared expert)
+    size_t img_bytes;         // B image (shared by the gate_up and down projections)
+    size_t shared_img_bytes;  // scratch of the shared expert's int8 GEMMs (its own region)
 };
 GroupPlan group_plan(int T, int topk, int E, int hidden, int inter, int sh_inter);
 // top-k (ids, w) and the grouping by expert.

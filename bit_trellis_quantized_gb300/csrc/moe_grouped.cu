@@ -727,7 +727,8 @@ GroupPlan group_plan(int T, int topk, int E, int hidden, int inter, int sh_inter
         const size_t gu = int8_gemm_ws_bytes(2 * sh_inter, hidden, T), dn = int8_gemm_ws_bytes(hidden, sh_inter, T);
         shared_img = gu > dn ? gu : dn;
     }
-    g.img_bytes = trellis_img > shared_img ? trellis_img : shared_img;
+    g.img_bytes = trellis_img;
+    g.shared_img_bytes = shared_img;
     return g;
 }
 

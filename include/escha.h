@@ -270,6 +270,12 @@ typedef struct escha_moe_layer {
  * to 0 when its first kernel starts and to a non-zero value if a kernel had
  * to give up waiting on a cluster peer (it then returns instead of hanging;
  * the outputs of that call are invalid). Read it after synchronising.
+ * Larger batches (the grouped path) run the int8 shared expert on a second
+ * stream beside the routed kernels: a non-blocking stream and two events per
+ * host thread and device, created by the first such call made outside a
+ * stream capture and reused after (calls inside a capture fork and join
+ * through them, and are captured as parallel branches); until they exist,
+ * the shared expert runs on `stream` itself. Results are identical either way.
  * Batches of up to 16 tokens run fused decode GEMVs per (token, expert);
  * larger batches group the tokens by expert and decode each expert's codes
  * once per work item of up to 128 of its tokens, feeding tcgen05
