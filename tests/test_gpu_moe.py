@@ -300,3 +300,27 @@ def test_moe_max_hidden(native, T):
     d = gen.moe_layer(99, hidden=8192, inter=128, n_experts=4, sh_inter=64)
     x = gen.fp16_normal(gen.rng(100), (T, 8192))
     _check_block(native, d, x, topk=2, tokens=[0, T - 1])
+
+
+def test_moe_grouped_in_cuda_graph_matches_eager(native):
+    """The grouped path captured in a CUDA graph (the shared expert forks onto
+    the library's second stream and joins back inside the capture) replays to
+    the eager outputs bit for bit."""
+    d = gen.moe_layer(81, hidden=512, inter=256, n_experts=16, k_gu=3, k_dn=2)
+    block = native.MoeBlock(d, topk=4)
+    x = dev(gen.fp16_normal(gen.rng(82), (40, 512)))
+    eager, ids_e, w_e = block(x)  # also creates the second stream outside any capture
+    eager = eager.clone()
+    s = torch.cuda.Stream()
+    out = torch.empty_like(eager)
+    ws = block.workspace(40)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            block(x, out=out, ws=ws)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager)
