@@ -86,6 +86,50 @@ def test_gemv_argument_validation_before_launch():
     assert b"K=4" in L.escha_last_error()
 
 
+def test_dense_linear_validation_before_launch():
+    native, L = _lib()
+    g = 0x10000
+    ws_bytes = L.escha_dense_linear_workspace(256, 256, 2, 4)
+    assert ws_bytes >= 16
+    # the GEMM route needs its B image: more workspace for more tokens
+    assert L.escha_dense_linear_workspace(5120, 17408, 2, 2048) > L.escha_dense_linear_workspace(5120, 17408, 2, 64)
+    args = dict(codes=g, inn=256, out=256, K=2, nt=1, x=g, xd=native.ESCHA_F16, M=4, rin=g, rout=g, bias=None, y=g,
+                ws=g, wsb=ws_bytes)
+
+    def call(**kw):
+        a = dict(args)
+        a.update(kw)
+        return L.escha_dense_linear(a["codes"], a["inn"], a["out"], a["K"], a["nt"], a["x"], a["xd"], a["M"],
+                                    a["rin"], a["rout"], a["bias"], a["y"], a["ws"], a["wsb"], None)
+
+    assert call(K=4) == native.ESCHA_E_K
+    assert call(inn=200) == native.ESCHA_E_SHAPE
+    assert call(out=64) == native.ESCHA_E_SHAPE
+    assert call(inn=65536 + 128) == native.ESCHA_E_SHAPE
+    assert call(nt=2) == native.ESCHA_E_ARG
+    assert call(xd=native.ESCHA_BF16) == native.ESCHA_E_ARG
+    assert call(M=0) == native.ESCHA_E_ARG
+    assert call(M=65537) == native.ESCHA_E_ARG
+    assert call(ws=None) == native.ESCHA_E_ARG
+    assert call(wsb=0) == native.ESCHA_E_WORKSPACE
+    assert call(bias=g + 4) == native.ESCHA_E_ALIGN
+    assert call(y=g + 8) == native.ESCHA_E_ALIGN
+    assert L.escha_codes_to_nt_major(g, 32, 32, 2, g + 16, None) == native.ESCHA_E_ARG  # overlapping buffers
+    assert L.escha_codes_to_nt_major(g, 32, 32, 7, g + 65536, None) == native.ESCHA_E_K
+    assert L.escha_codes_to_nt_major(g, 32, 32, 2, None, None) == native.ESCHA_E_ARG
+
+
+def test_checkpoint_entry_points_reject_null_handles():
+    native, L = _lib()
+    info = native.EschaProjInfo()
+    assert L.escha_ckpt_num_projections(None) == 0
+    assert L.escha_ckpt_projection(None, 0, ctypes.byref(info)) == native.ESCHA_E_ARG
+    assert L.escha_ckpt_read(None, b"x", None, 0, 0, None) == native.ESCHA_E_ARG
+    h = ctypes.c_void_p()
+    assert L.escha_ckpt_open(None, 0, ctypes.byref(h)) == native.ESCHA_E_ARG
+    L.escha_ckpt_close(None)  # a null handle is ignored
+
+
 def test_decode_validation():
     native, L = _lib()
     g = 0x10000
