@@ -51,16 +51,14 @@ GU_CODE_BYTES = HIDDEN * 2 * INTER * 3 // 8  # per expert: 786,432
 DN_CODE_BYTES = INTER * HIDDEN * 2 // 8  # per expert: 262,144
 N_LAYERS = 24
 STEPS_PER_GRAPH = 8
-KERNELS_PER_STEP = 3  # router, gate_up (+top-k, shared gate_up), down (+top-k, shared down, combine)
+KERNELS_PER_STEP = 3  # router (+shared gate_up), gate_up (+top-k), down (+top-k, shared down, combine)
 
 
-# Algorithmic bytes of one launch of the gate_up kernel at batch 1. Routed:
-# 8 experts' codes, rin and rout, x once, the token's 256 f16 logits, the
-# 8 x 1024 f32 outputs. Shared expert: int8 gate_up rows and scales, the fp16
-# gate vector, its 1024 f32 outputs and the gate value.
+# Algorithmic bytes of one launch of the gate_up kernel at batch 1: 8 routed
+# experts' codes, rin and rout, x once, the token's 256 f16 logits, the
+# 8 x 1024 f32 outputs (the shared expert's gate_up runs in the router grid).
 GATE_UP_KERNEL_BYTES = (TOPK * (GU_CODE_BYTES + HIDDEN * 2 + 2 * INTER * 2) + HIDDEN * 2 + E * 2
-                        + TOPK * 2 * INTER * 4 + 2 * INTER * HIDDEN + 2 * INTER * 4 + HIDDEN * 2
-                        + 2 * INTER * 4 + 4)
+                        + TOPK * 2 * INTER * 4)
 
 
 # Routed weights decoded by one launch of the gate_up kernel at batch 1 and the
@@ -402,7 +400,7 @@ def run_ours(args, ws, rank, local):
         return
 
     hbm, tflops, src = peaks()
-    ph = phase.mean(axis=0)  # router, gate_up (+shared gate_up), down (+shared down, combine) (ms)
+    ph = phase.mean(axis=0)  # router (+shared gate_up), gate_up, down (+shared down, combine) (ms)
     gu_ms = float(ph[1])
     gu_bytes = GATE_UP_KERNEL_BYTES
     achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
@@ -428,7 +426,7 @@ def run_ours(args, ws, rank, local):
                      "peak": ALU_PEAK_WARP_INSTR / 1e12, "unit": "T warp-instructions/s",
                      "frac": GU_WEIGHTS * ALU_OPS_PER_WEIGHT / 32 / (gu_ms * 1e-3) / ALU_PEAK_WARP_INSTR,
                      "traffic": measured_traffic(), "algorithmic_bytes_per_launch": gu_bytes,
-                     "kernel": "moe_gate_up_kernel<K=3> (8 routed experts + int8 shared gate_up)",
+                     "kernel": "moe_gate_up_kernel<K=3> (8 routed experts)",
                      "algorithmic_ops_per_launch": GU_WEIGHTS * ALU_OPS_PER_WEIGHT, "ms_per_launch": gu_ms,
                      "peak_source": "derived: 152 SMs x 4 x 2.07e9 /s"},
         # the same launch against the measured HBM copy bandwidth
@@ -437,7 +435,7 @@ def run_ours(args, ws, rank, local):
                          "ms_per_launch": gu_ms, "peak_source": src},
         "packed_expert_gbs": routed_code_bytes / (t_step * 1e-3) / 1e9,
         "packed_expert_frac": routed_code_bytes / (t_step * 1e-3) / 1e9 / hbm,
-        "phase_ms": {"router": float(ph[0]), "gate_up+shared_gate_up": float(ph[1]),
+        "phase_ms": {"router+shared_gate_up": float(ph[0]), "gate_up": float(ph[1]),
                      "down+shared_down+combine": float(ph[2])},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "e2e": {"value": aggregate_tokens_per_s(ws, t_e2e), "unit": UNIT, "h2d_bytes_per_step": HIDDEN * 2,

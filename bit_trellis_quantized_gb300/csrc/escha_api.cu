@@ -485,7 +485,7 @@ int moe_block_impl(const escha_moe_layer* L, const uint16_t* x, int T, float* ou
             if ((r = cuda_status(cudaEventRecord(fk->join, fk->s2), "join record"))) return r;
         }
         if ((r = record(ev, 0, s))) return r;
-        if ((r = cuda_status(escha::launch_moe_router(a, s), "router launch"))) return r;
+        if ((r = cuda_status(escha::launch_moe_router(a, false, s), "router launch"))) return r;
         if ((r = record(ev, 1, s))) return r;
         if ((r = cuda_status(escha::launch_moe_grouped(a, d, sms, s), "grouped expert launch"))) return r;
         if ((r = record(ev, 2, s))) return r;
@@ -496,7 +496,7 @@ int moe_block_impl(const escha_moe_layer* L, const uint16_t* x, int T, float* ou
     }
 
     if ((r = record(ev, 0, s))) return r;
-    if ((r = cuda_status(escha::launch_moe_router(a, s), "router launch"))) return r;
+    if ((r = cuda_status(escha::launch_moe_router(a, true, s), "router launch"))) return r;
     if ((r = record(ev, 1, s))) return r;
     if ((r = cuda_status(escha::launch_moe_gate_up(a, sms, s), "gate_up launch"))) return r;
     if ((r = record(ev, 2, s))) return r;
@@ -543,7 +543,7 @@ int escha_moe_route(const escha_moe_layer* L, const uint16_t* x, int T, uint16_t
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char* base = static_cast<char*>(ws);
     const escha::MoeArgs a = moe_args(L, x, T, nullptr, ids_out, w_out, base, m);
-    if ((r = cuda_status(escha::launch_moe_router(a, s), "router launch"))) return r;
+    if ((r = cuda_status(escha::launch_moe_router(a, false, s), "router launch"))) return r;
     if ((r = cuda_status(escha::launch_moe_topk_group(a, s), "top-k / grouping launch"))) return r;
     const int E = L->n_experts;
     const size_t S = (size_t)T * L->topk;

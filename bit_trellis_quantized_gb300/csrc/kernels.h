@@ -161,7 +161,9 @@ cudaError_t launch_moe_combine(const MoeArgs& a, const float* d, cudaStream_t s)
 cudaError_t launch_residual_rmsnorm(float* h, const float* add, int T, int hidden, float eps, uint16_t* x,
                                     cudaStream_t s);
 
-cudaError_t launch_moe_router(const MoeArgs& a, cudaStream_t s);
+// with_shared (per-slot path): the same grid also computes the shared
+// expert's gate_up rows and gate
+cudaError_t launch_moe_router(const MoeArgs& a, bool with_shared, cudaStream_t s);
 cudaError_t launch_moe_gate_up(const MoeArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_moe_down(const MoeArgs& a, int num_sms, cudaStream_t s);
 

@@ -5,14 +5,13 @@
 //     PR #694, commit "Executed the moeblk golden against real shipped
 //     layer-0 weights": logits are rounded to f16 before top-k), one warp per
 //     expert spread over many SMs so the 1 MB router matrix streams in one
-//     memory round trip.
+//     memory round trip. Extra CTAs of the same grid compute the int8 shared
+//     expert's gate_up rows and its sigmoid gate.
 //  2. gate_up: each routed CTA selects its token's top-k (ties to the lower
 //     expert id) and softmax weights with one warp, then runs the expert's
 //     gate_up projection (fused trellis decode GEMV with the input/output
 //     Hadamard transforms and rout); a cluster splits the input rows and
-//     pushes its partial sums into rank 0. Extra CTAs, which do not wait for
-//     the router, compute the int8 shared expert's gate_up rows and its
-//     sigmoid gate.
+//     pushes its partial sums into rank 0.
 //  3. down + combine: one cluster per (token, 128-wide output block), rank
 //     j*ks + h = routed expert j, input split h; every rank also computes an
 //     equal share of the shared expert's down rows of the block. Ranks push
@@ -116,74 +115,377 @@ __device__ void router_logits(const MoeArgs& a, int warp, int lane) {
     }
 }
 
-// Shared expert gate_up rows (kShRowsPerWarp per warp) for every token, and
-// in CTA 0 the sigmoid gate (an f32 dot product of the fp16 gate vector with
-// x, not rounded).
-__device__ void shared_gate_up(const MoeArgs& a, int cta, float* xs, int warp, int lane) {
-    const int rows = 2 * a.sh_inter;
-    const int r0 = (cta * kGuWarps + warp) * kShRowsPerWarp;
-    for (int tb = 0; tb < a.T; tb += kShMT) {
-        const int mt = min(kShMT, a.T - tb);
-        __syncthreads();
-        for (int i = threadIdx.x * 8; i < kShMT * a.hidden; i += kGuThreads * 8) {
-            const int t = i / a.hidden, c = i % a.hidden;
-            float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
-            if (t < mt) {
-                const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x + (long long)(tb + t) * a.hidden + c));
-                lo = make_float4(h2f_bits(v.x & 0xFFFFu), h2f_bits(v.x >> 16), h2f_bits(v.y & 0xFFFFu), h2f_bits(v.y >> 16));
-                hi = make_float4(h2f_bits(v.z & 0xFFFFu), h2f_bits(v.z >> 16), h2f_bits(v.w & 0xFFFFu), h2f_bits(v.w >> 16));
-            }
-            *reinterpret_cast<float4*>(xs + xs_swz(i)) = lo;
-            *reinterpret_cast<float4*>(xs + xs_swz(i + 4)) = hi;
+// x rows tb .. tb+mt-1 as f32 at xs[xs_swz(t*hidden + i)] (zeros for rows
+// t >= mt up to MT), by the CTA's NW warps; each thread issues its loads in
+// batches of 8 before storing any, so staging costs one L2 round trip per
+// batch instead of one per load.
+template <int NW, int MT>
+__device__ __forceinline__ void stage_x_f32(const MoeArgs& a, int tb, int mt, float* xs) {
+    constexpr int kB = 8, kStride = NW * 32;
+    const int n = MT * a.hidden;
+    for (int u0 = threadIdx.x; u0 * 8 < n; u0 += kB * kStride) {
+        uint4 v[kB];
+#pragma unroll
+        for (int b = 0; b < kB; ++b) {
+            const int i = (u0 + b * kStride) * 8, t = i / a.hidden;
+            v[b] = (i < n && t < mt) ? __ldg(reinterpret_cast<const uint4*>(a.x + (long long)(tb + t) * a.hidden + i % a.hidden))
+                                     : make_uint4(0u, 0u, 0u, 0u);
         }
+#pragma unroll
+        for (int b = 0; b < kB; ++b) {
+            const int i = (u0 + b * kStride) * 8;
+            if (i >= n) break;
+            *reinterpret_cast<float4*>(xs + xs_swz(i)) =
+                make_float4(h2f_bits(v[b].x & 0xFFFFu), h2f_bits(v[b].x >> 16), h2f_bits(v[b].y & 0xFFFFu), h2f_bits(v[b].y >> 16));
+            *reinterpret_cast<float4*>(xs + xs_swz(i + 4)) =
+                make_float4(h2f_bits(v[b].z & 0xFFFFu), h2f_bits(v[b].z >> 16), h2f_bits(v[b].w & 0xFFFFu), h2f_bits(v[b].w >> 16));
+        }
+    }
+}
+
+// Shared expert gate_up rows (kShRowsPerWarp per warp of NW) for every
+// token, MT tokens per pass, and in warp NW-1 of CTA 0 the sigmoid gate (an
+// f32 dot product of the fp16 gate vector with x, not rounded). Every sum
+// runs in one order, whichever variant computes it: lane l adds, per row and
+// token, the products of its 16 columns c*512 + 16l .. +15 for c = 0, 1, ...
+// in column order (int8 rows), or of its 8 columns 256k + 8l .. +7 for k = 0,
+// 1, ... (gate), and the 32 lanes are combined by the xor butterfly.
+//
+// Large hidden sizes: rows and gate vector are fetched into L2 before the wait
+// for the preceding kernel and read with int8_rows_dot.
+template <int NW, int MT>
+__device__ void shared_gate_up_staged(const MoeArgs& a, int cta, float* xs, int warp, int lane) {
+    constexpr int R = kShRowsPerWarp;
+    const int rows = 2 * a.sh_inter;
+    const int r0 = (cta * NW + warp) * R;
+    const int nrows = min(R, rows - r0);  // <= 0: no rows in this warp
+    const bool gate = cta == 0 && warp == NW - 1;
+    const long long nb = nrows > 0 ? (long long)nrows * a.hidden : 0;  // bytes of this warp's rows
+    for (long long off = lane * 128LL; off < nb; off += 32 * 128)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(a.sh_gu_w8 + (long long)r0 * a.hidden + off));
+    if (gate)
+        for (int off = lane * 128; off < 2 * a.hidden; off += 32 * 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(a.sh_gate) + off));
+    pdl_wait();  // x, and the workspace the previous call's kernels may still read
+    for (int tb = 0; tb < a.T; tb += MT) {
+        const int mt = min(MT, a.T - tb);
         __syncthreads();
-        if (r0 < rows) {
-            float dots[kShRowsPerWarp][kShMT];
-            int8_rows_dot<kShRowsPerWarp, kShMT>(a.sh_gu_w8 + (long long)r0 * a.hidden, a.hidden, rows - r0, a.hidden,
-                                                 xs, a.hidden, lane, dots);
+        stage_x_f32<NW, MT>(a, tb, mt, xs);
+        __syncthreads();
+        if (nrows > 0) {
+            float dots[R][MT];
+            int8_rows_dot<R, MT>(a.sh_gu_w8 + (long long)r0 * a.hidden, a.hidden, nrows, a.hidden, xs, a.hidden, lane,
+                                 dots);
             if (lane == 0) {
 #pragma unroll
-                for (int r = 0; r < kShRowsPerWarp; ++r) {
-                    if (r0 + r >= rows) break;
+                for (int r = 0; r < R; ++r) {
+                    if (r >= nrows) break;
                     const float sc = a.sh_gu_scale[r0 + r];
                     for (int t = 0; t < mt; ++t) a.shgu[(long long)(tb + t) * rows + r0 + r] = sc * dots[r][t];
                 }
             }
         }
-        if (cta == 0 && warp == kGuWarps - 1) {
-            float acc[kShMT] = {};
-#pragma unroll 8
-            for (int i0 = lane * 8; i0 < a.hidden; i0 += 256) {
-                const uint4 gv = __ldg(reinterpret_cast<const uint4*>(a.sh_gate + i0));
-                const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-#pragma unroll
-                for (int t = 0; t < kShMT; ++t) {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        acc[t] = fmaf(h2f_bits(static_cast<uint16_t>(gw[k] & 0xFFFFu)), xs[xs_swz(t * a.hidden + i0 + 2 * k)],
-                                      acc[t]);
-                        acc[t] = fmaf(h2f_bits(static_cast<uint16_t>(gw[k] >> 16)), xs[xs_swz(t * a.hidden + i0 + 2 * k + 1)],
-                                      acc[t]);
-                    }
+        if (gate) {
+#pragma unroll 1
+            for (int t = 0; t < mt; ++t) {
+                float acc = 0.f;
+#pragma unroll 1
+                for (int i0 = lane * 8; i0 < a.hidden; i0 += 256) {
+                    const uint4 g4 = __ldg(reinterpret_cast<const uint4*>(a.sh_gate + i0));
+                    const float4 xa = *reinterpret_cast<const float4*>(xs + xs_swz(t * a.hidden + i0));
+                    const float4 xb = *reinterpret_cast<const float4*>(xs + xs_swz(t * a.hidden + i0 + 4));
+                    acc = fmaf(h2f_bits(static_cast<uint16_t>(g4.x & 0xFFFFu)), xa.x, acc);
+                    acc = fmaf(h2f_bits(static_cast<uint16_t>(g4.x >> 16)), xa.y, acc);
+                    acc = fmaf(h2f_bits(static_cast<uint16_t>(g4.y & 0xFFFFu)), xa.z, acc);
+                    acc = fmaf(h2f_bits(static_cast<uint16_t>(g4.y >> 16)), xa.w, acc);
+                    acc = fmaf(h2f_bits(static_cast<uint16_t>(g4.z & 0xFFFFu)), xb.x, acc);
+                    acc = fmaf(h2f_bits(static_cast<uint16_t>(g4.z >> 16)), xb.y, acc);
+                    acc = fmaf(h2f_bits(static_cast<uint16_t>(g4.w & 0xFFFFu)), xb.z, acc);
+                    acc = fmaf(h2f_bits(static_cast<uint16_t>(g4.w >> 16)), xb.w, acc);
                 }
-            }
 #pragma unroll
-            for (int t = 0; t < kShMT; ++t) {
-                float v = acc[t];
-#pragma unroll
-                for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
-                if (lane == 0 && t < mt) a.shgate[tb + t] = sigmoid_f(v);
+                for (int m = 16; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+                if (lane == 0) a.shgate[tb + t] = sigmoid_f(acc);
             }
         }
     }
 }
 
-__global__ void __launch_bounds__(kK0Threads) moe_router_kernel(const MoeArgs a) {
-    // The gate_up kernel can be scheduled at once; its routed CTAs wait for
-    // this grid before reading the logits.
+// hidden <= 2048: a warp's int8 rows and the gate vector are loaded into
+// registers before the wait; after it the rows are converted to f32 once and
+// each token is a short loop over shared-memory x (code executed once per warp
+// is kept small: straight-line code of this size is bound by instruction
+// fetch).
+template <int NW, int MT>
+__device__ void shared_gate_up_regs(const MoeArgs& a, int cta, float* xs, int warp, int lane) {
+    constexpr int R = kShRowsPerWarp;
+    const int rows = 2 * a.sh_inter;
+    const int r0 = (cta * NW + warp) * R;
+    const int nrows = min(R, rows - r0);
+    const bool gate = cta == 0 && warp == NW - 1;
+    uint4 wv[R][4];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            wv[r][c] = (r < nrows && c * 512 + lane * 16 < a.hidden)
+                           ? ldg_stream_v4(a.sh_gu_w8 + (long long)(r0 + r) * a.hidden + c * 512 + lane * 16)
+                           : make_uint4(0u, 0u, 0u, 0u);
+    uint4 gv[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        gv[k] = (gate && lane * 8 + 256 * k < a.hidden)
+                    ? __ldg(reinterpret_cast<const uint4*>(a.sh_gate + lane * 8 + 256 * k))
+                    : make_uint4(0u, 0u, 0u, 0u);
+    float sc[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) sc[r] = r < nrows ? a.sh_gu_scale[r0 + r] : 0.f;
+    pdl_wait();  // x, and the workspace the previous call's kernels may still read
+    float wf[R][64];  // (c, q, k): column c*512 + 16*lane + 4q + k
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float f[4];
+            i8x4_to_f32(wv[r][c].x, f);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) wf[r][16 * c + k] = f[k];
+            i8x4_to_f32(wv[r][c].y, f);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) wf[r][16 * c + 4 + k] = f[k];
+            i8x4_to_f32(wv[r][c].z, f);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) wf[r][16 * c + 8 + k] = f[k];
+            i8x4_to_f32(wv[r][c].w, f);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) wf[r][16 * c + 12 + k] = f[k];
+        }
+    for (int tb = 0; tb < a.T; tb += MT) {
+        const int mt = min(MT, a.T - tb);
+        __syncthreads();
+        stage_x_f32<NW, MT>(a, tb, mt, xs);
+        __syncthreads();
+        if (nrows > 0) {
+            // two tokens at a time (rows t >= mt are staged as zeros), so that
+            // four independent sums hide the fma latency
+#pragma unroll 1
+            for (int t = 0; t < mt; t += 2) {
+                float acc[R][2];
+#pragma unroll
+                for (int r = 0; r < R; ++r) acc[r][0] = acc[r][1] = 0.f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int i0 = c * 512 + lane * 16;
+                    if (i0 >= a.hidden) break;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        float4 xv[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u)
+                            xv[u] = *reinterpret_cast<const float4*>(xs + xs_swz((t + u) * a.hidden + i0 + 4 * q));
+#pragma unroll
+                        for (int r = 0; r < R; ++r)
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                acc[r][u] = fmaf(wf[r][16 * c + 4 * q], xv[u].x, acc[r][u]);
+                                acc[r][u] = fmaf(wf[r][16 * c + 4 * q + 1], xv[u].y, acc[r][u]);
+                                acc[r][u] = fmaf(wf[r][16 * c + 4 * q + 2], xv[u].z, acc[r][u]);
+                                acc[r][u] = fmaf(wf[r][16 * c + 4 * q + 3], xv[u].w, acc[r][u]);
+                            }
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        float v = acc[r][u];
+#pragma unroll
+                        for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+                        if (lane == 0 && r < nrows && t + u < mt) a.shgu[(long long)(tb + t + u) * rows + r0 + r] = sc[r] * v;
+                    }
+            }
+        }
+        if (gate) {
+#pragma unroll 1
+            for (int t = 0; t < mt; t += 2) {
+                float acc[2] = {0.f, 0.f};
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int i0 = lane * 8 + 256 * k;
+                    if (i0 >= a.hidden) break;
+                    const float g[8] = {h2f_bits(static_cast<uint16_t>(gv[k].x & 0xFFFFu)), h2f_bits(static_cast<uint16_t>(gv[k].x >> 16)),
+                                        h2f_bits(static_cast<uint16_t>(gv[k].y & 0xFFFFu)), h2f_bits(static_cast<uint16_t>(gv[k].y >> 16)),
+                                        h2f_bits(static_cast<uint16_t>(gv[k].z & 0xFFFFu)), h2f_bits(static_cast<uint16_t>(gv[k].z >> 16)),
+                                        h2f_bits(static_cast<uint16_t>(gv[k].w & 0xFFFFu)), h2f_bits(static_cast<uint16_t>(gv[k].w >> 16))};
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const float4 xa = *reinterpret_cast<const float4*>(xs + xs_swz((t + u) * a.hidden + i0));
+                        const float4 xb = *reinterpret_cast<const float4*>(xs + xs_swz((t + u) * a.hidden + i0 + 4));
+                        acc[u] = fmaf(g[0], xa.x, acc[u]);
+                        acc[u] = fmaf(g[1], xa.y, acc[u]);
+                        acc[u] = fmaf(g[2], xa.z, acc[u]);
+                        acc[u] = fmaf(g[3], xa.w, acc[u]);
+                        acc[u] = fmaf(g[4], xb.x, acc[u]);
+                        acc[u] = fmaf(g[5], xb.y, acc[u]);
+                        acc[u] = fmaf(g[6], xb.z, acc[u]);
+                        acc[u] = fmaf(g[7], xb.w, acc[u]);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    float v = acc[u];
+#pragma unroll
+                    for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+                    if (lane == 0 && t + u < mt) a.shgate[tb + t + u] = sigmoid_f(v);
+                }
+            }
+        }
+    }
+}
+
+// NT = 1 or 2 tokens, hidden <= 2048: the shared-expert rows of one warp
+// (and, in warp 3 of CTA 0, the gate vector) are loaded into registers before
+// the wait for the preceding kernel; after it only x is read, straight into
+// registers (one L2 round trip, no staging). Sums in the order stated above.
+template <int NT>
+__device__ void shared_gate_up_direct(const MoeArgs& a, int cta, int warp, int lane) {
+    constexpr int R = kShRowsPerWarp;
+    const int rows = 2 * a.sh_inter;
+    const int r0 = (cta * kK0Warps + warp) * R;
+    const int nrows = min(R, rows - r0);
+    const bool gate = cta == 0 && warp == kK0Warps - 1;
+    // chunk c (512 columns) holds this lane's 16 columns when c*512 + 16*lane < hidden
+    uint4 wv[R][4];
+    float sc[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        sc[r] = r < nrows ? a.sh_gu_scale[r0 + r] : 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            wv[r][c] = (r < nrows && c * 512 + lane * 16 < a.hidden)
+                           ? ldg_stream_v4(a.sh_gu_w8 + (long long)(r0 + r) * a.hidden + c * 512 + lane * 16)
+                           : make_uint4(0u, 0u, 0u, 0u);
+    }
+    uint4 gv[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        gv[k] = (gate && lane * 8 + 256 * k < a.hidden)
+                    ? __ldg(reinterpret_cast<const uint4*>(a.sh_gate + lane * 8 + 256 * k))
+                    : make_uint4(0u, 0u, 0u, 0u);
+    pdl_wait();  // x, and the workspace the previous call's kernels may still read
+    if (nrows > 0) {
+        uint4 xv[NT][4][2];
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    xv[t][c][h] = (t < a.T && c * 512 + lane * 16 < a.hidden)
+                                      ? __ldg(reinterpret_cast<const uint4*>(a.x + (long long)t * a.hidden + c * 512 + lane * 16 + 8 * h))
+                                      : make_uint4(0u, 0u, 0u, 0u);
+        float acc[R][NT];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int t = 0; t < NT; ++t) acc[r][t] = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            if (c * 512 + lane * 16 >= a.hidden) break;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float xq[NT][4];
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    const uint32_t x01 = q == 0 ? xv[t][c][0].x : q == 1 ? xv[t][c][0].z : q == 2 ? xv[t][c][1].x : xv[t][c][1].z;
+                    const uint32_t x23 = q == 0 ? xv[t][c][0].y : q == 1 ? xv[t][c][0].w : q == 2 ? xv[t][c][1].y : xv[t][c][1].w;
+                    xq[t][0] = h2f_bits(static_cast<uint16_t>(x01 & 0xFFFFu));
+                    xq[t][1] = h2f_bits(static_cast<uint16_t>(x01 >> 16));
+                    xq[t][2] = h2f_bits(static_cast<uint16_t>(x23 & 0xFFFFu));
+                    xq[t][3] = h2f_bits(static_cast<uint16_t>(x23 >> 16));
+                }
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const uint32_t word = q == 0 ? wv[r][c].x : q == 1 ? wv[r][c].y : q == 2 ? wv[r][c].z : wv[r][c].w;
+                    float f[4];
+                    i8x4_to_f32(word, f);
+#pragma unroll
+                    for (int t = 0; t < NT; ++t) {
+                        acc[r][t] = fmaf(f[0], xq[t][0], acc[r][t]);
+                        acc[r][t] = fmaf(f[1], xq[t][1], acc[r][t]);
+                        acc[r][t] = fmaf(f[2], xq[t][2], acc[r][t]);
+                        acc[r][t] = fmaf(f[3], xq[t][3], acc[r][t]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                float v = acc[r][t];
+#pragma unroll
+                for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+                if (lane == 0 && r < nrows && t < a.T) a.shgu[(long long)t * rows + r0 + r] = sc[r] * v;
+            }
+    }
+    if (gate) {
+        float acc[NT];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) acc[t] = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int i0 = lane * 8 + 256 * k;
+            if (i0 >= a.hidden) break;
+            const uint32_t gw[4] = {gv[k].x, gv[k].y, gv[k].z, gv[k].w};
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                const uint4 xg = t < a.T ? __ldg(reinterpret_cast<const uint4*>(a.x + (long long)t * a.hidden + i0))
+                                         : make_uint4(0u, 0u, 0u, 0u);
+                const uint32_t xw[4] = {xg.x, xg.y, xg.z, xg.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    acc[t] = fmaf(h2f_bits(static_cast<uint16_t>(gw[q] & 0xFFFFu)), h2f_bits(static_cast<uint16_t>(xw[q] & 0xFFFFu)), acc[t]);
+                    acc[t] = fmaf(h2f_bits(static_cast<uint16_t>(gw[q] >> 16)), h2f_bits(static_cast<uint16_t>(xw[q] >> 16)), acc[t]);
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            float v = acc[t];
+#pragma unroll
+            for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+            if (lane == 0 && t < a.T) a.shgate[t] = sigmoid_f(v);
+        }
+    }
+}
+
+// Per-slot path: CTAs x < n_lg compute router logits; with a shared expert,
+// the CTAs after them in row y = 0 compute its gate_up rows and its gate
+// (4 warps each, MT tokens per pass), so that the gate_up kernel is routed
+// experts only and the shared rows run while the logits are computed.
+template <int MT>
+__global__ void __launch_bounds__(kK0Threads) moe_router_kernel(const MoeArgs a, int n_lg) {
+    // The gate_up kernel can be scheduled at once, while the kernel before
+    // this one may still run: every gate_up CTA waits for this grid (and so
+    // for that kernel) before it touches x, the logits or the workspace.
     pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    router_logits(a, warp, lane);  // waits for the preceding kernel after its first weight loads
+    if (static_cast<int>(blockIdx.x) < n_lg) {
+        router_logits(a, warp, lane);  // waits for the preceding kernel after its first weight loads
+        return;
+    }
+    if (blockIdx.y != 0) return;
+    extern __shared__ __align__(16) float xs_sh[];
+    const int cta = static_cast<int>(blockIdx.x) - n_lg;
+    if (a.hidden <= 2048) {
+        if (MT <= 2)
+            shared_gate_up_direct<MT>(a, cta, warp, lane);
+        else
+            shared_gate_up_regs<kK0Warps, MT>(a, cta, xs_sh, warp, lane);
+    } else {
+        shared_gate_up_staged<kK0Warps, MT>(a, cta, xs_sh, warp, lane);
+    }
 }
 
 // Router logits for many tokens: a CTA stages 16 tokens of x in shared memory
@@ -248,7 +550,7 @@ __global__ void __launch_bounds__(256) moe_router_tiled_kernel(const MoeArgs a) 
 }
 
 // ---------------------------------------------------------------------------
-// 2. gate_up (routed) + shared expert down rows.
+// 2. gate_up of the routed experts.
 // ---------------------------------------------------------------------------
 template <int K>
 __device__ void gate_up_routed(const MoeArgs& a, float* smem) {
@@ -274,13 +576,14 @@ __device__ void gate_up_routed(const MoeArgs& a, float* smem) {
 
     const int t = slot / a.topk;
     const int j = slot % a.topk;
-    // x is this call's input: its loads for the input transform go out before
-    // the wait for the router (only rin depends on the routing)
+    // x may still be written by the kernel before the router (this grid can
+    // start while it runs): its loads go out right after the wait, beside
+    // the logits' (only rin depends on the routing)
     const uint16_t* xrow = a.x + (long long)t * a.hidden;
-    uint2 x_pre = make_uint2(0u, 0u);
-    if (warp < nk / 128) x_pre = *reinterpret_cast<const uint2*>(xrow + kt0 * 16 + warp * 128 + 4 * lane);
     pdl_wait();     // router logits
     pdl_trigger();  // logits complete: the down kernel may read them early
+    uint2 x_pre = make_uint2(0u, 0u);
+    if (warp < nk / 128) x_pre = *reinterpret_cast<const uint2*>(xrow + kt0 * 16 + warp * 128 + 4 * lane);
     if (warp == 0) {
         int e_l;
         float w_l;
@@ -348,15 +651,11 @@ __device__ void gate_up_routed(const MoeArgs& a, float* smem) {
 }
 
 template <int K>
-__global__ void __launch_bounds__(kGuThreads, 3) moe_gate_up_kernel(const MoeArgs a) {
+// Four CTAs per SM (64 registers): with the shared expert's rows in the
+// router grid this kernel holds only the routed decode.
+__global__ void __launch_bounds__(kGuThreads, 4) moe_gate_up_kernel(const MoeArgs a) {
     extern __shared__ __align__(16) float smem[];
-    if (static_cast<int>(blockIdx.z) < a.T * a.topk) {
-        gate_up_routed<K>(a, smem);
-    } else {
-        pdl_trigger();  // needs nothing from the router
-        const int cta = ((blockIdx.z - a.T * a.topk) * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
-        shared_gate_up(a, cta, smem, threadIdx.x >> 5, threadIdx.x & 31);
-    }
+    gate_up_routed<K>(a, smem);
 }
 
 // ---------------------------------------------------------------------------
@@ -595,33 +894,28 @@ cudaError_t launch_gate_up(MoeArgs a, int num_sms, cudaStream_t s) {
     const int slots = a.T * a.topk;
     const int kblks = a.hidden / 128;
     // Largest input split (CTAs per cluster, <= 8) for which the routed CTAs
-    // plus the shared gate_up CTAs fit in one wave of 3 CTAs per SM; when only
-    // an unsplit grid fits, a split of two is still taken while it needs at
-    // most 1.3 waves (measured on GB300 for the 35B layer: 4 tokens 61 -> 56
-    // us per block; 5 tokens, 1.5 waves, is slower split).
-    const int rows_per_cta = kGuWarps * kShRowsPerWarp;
-    auto shared_z = [&](int per_z) {
-        return a.sh_inter > 0 ? (2 * a.sh_inter + per_z * rows_per_cta - 1) / (per_z * rows_per_cta) : 0;
-    };
-    auto ctas = [&](int cs) { return (long long)cs * oblks * (slots + shared_z(cs * oblks)); };
+    // fit in one wave of 4 CTAs per SM; when only an unsplit grid fits, a
+    // split of two is still taken while it needs at most 1.3 waves (measured
+    // on GB300 for the 35B layer with 3 CTAs per SM: 4 tokens 61 -> 56 us per
+    // block; 5 tokens, 1.5 waves, is slower split). Four CTAs per SM instead
+    // of three: 1 token 23.7 -> 21.5 us per block, 2 tokens 35.8 -> 31.1 us,
+    // 4 to 16 tokens unchanged.
+    auto ctas = [&](int cs) { return (long long)cs * oblks * slots; };
     int csize = 1;
     for (int c = 1; c <= 8 && c <= kblks; ++c) {
         const int per = (kblks + c - 1) / c;
         const int cs = (kblks + per - 1) / per;
-        if (ctas(cs) <= 3LL * kWaveSms) csize = cs;
+        if (ctas(cs) <= 4LL * kWaveSms) csize = cs;
     }
-    if (csize == 1 && kblks >= 2 && 10 * ctas(2) <= 13LL * 3 * kWaveSms) csize = 2;
+    if (csize == 1 && kblks >= 2 && 10 * ctas(2) <= 13LL * 4 * kWaveSms) csize = 2;
     const int per = (kblks + csize - 1) / csize;
     csize = (kblks + per - 1) / per;
     a.gu_kt_per_cta = per * 8;
-    const int sh_z = shared_z(csize * oblks);
-    const int smem_routed = (kMaxCluster * 128 + a.gu_kt_per_cta * 16 + (kGuWarps + 1) * 128) * 4;
-    const int smem_shared = a.sh_inter > 0 ? kShMT * a.hidden * 4 : 0;
-    const int smem = smem_routed > smem_shared ? smem_routed : smem_shared;
+    const int smem = (kMaxCluster * 128 + a.gu_kt_per_cta * 16 + (kGuWarps + 1) * 128) * 4;
     const void* f = reinterpret_cast<const void*>(moe_gate_up_kernel<K>);
     cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    return launch_ex(f, dim3(csize, oblks, slots + sh_z), dim3(kGuThreads), smem, csize, true, s, a);
+    return launch_ex(f, dim3(csize, oblks, slots), dim3(kGuThreads), smem, csize, true, s, a);
 }
 
 template <int K>
@@ -652,16 +946,37 @@ cudaError_t launch_down(MoeArgs a, int num_sms, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_moe_router(const MoeArgs& a, cudaStream_t s) {
-    if (a.T >= kRtTok) {
+cudaError_t launch_moe_router(const MoeArgs& a, bool with_shared, cudaStream_t s) {
+    if (!with_shared && a.T >= kRtTok) {
         void* args[] = {const_cast<MoeArgs*>(&a)};
         return launch_kernel(reinterpret_cast<const void*>(moe_router_tiled_kernel),
                              dim3((a.E + kRtExp - 1) / kRtExp, (a.T + kRtTok - 1) / kRtTok), dim3(256), 0, true, s,
                              args);
     }
-    const int n_lg = (a.E + kK0Warps - 1) / kK0Warps;
-    return launch_ex(reinterpret_cast<const void*>(moe_router_kernel), dim3(n_lg, (a.T + kLgTG - 1) / kLgTG),
-                     dim3(kK0Threads), 0, 0, true, s, a);
+    int n_lg = (a.E + kK0Warps - 1) / kK0Warps;
+    const int rows_per_cta = kK0Warps * kShRowsPerWarp;
+    const int n_sh = with_shared && a.sh_inter > 0 ? (2 * a.sh_inter + rows_per_cta - 1) / rows_per_cta : 0;
+    // tokens per pass of the shared rows: 1 or 2 read x straight into
+    // registers (hidden <= 2048), otherwise x is staged in shared memory
+    const int mt = a.T <= 2 ? a.T : kShMT;
+    const int smem = n_sh > 0 && !(mt <= 2 && a.hidden <= 2048) ? mt * a.hidden * 4 : 0;
+    const void* f = mt == 1   ? reinterpret_cast<const void*>(moe_router_kernel<1>)
+                    : mt == 2 ? reinterpret_cast<const void*>(moe_router_kernel<2>)
+                              : reinterpret_cast<const void*>(moe_router_kernel<kShMT>);
+    cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(n_lg + n_sh, (a.T + kLgTG - 1) / kLgTG);
+    cfg.blockDim = dim3(kK0Threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void* args[] = {const_cast<MoeArgs*>(&a), &n_lg};
+    return cudaLaunchKernelExC(&cfg, f, args);
 }
 
 cudaError_t launch_moe_gate_up(const MoeArgs& a, int num_sms, cudaStream_t s) {

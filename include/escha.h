@@ -291,9 +291,9 @@ int escha_moe_block(const escha_moe_layer* L, const uint16_t* x, int T, float* o
 
 /* Measurement export: escha_moe_block that also records four caller-created
  * CUDA events (cudaEvent_t, any of them may be null) on `stream`: events[0]
- * before the router kernel, [1] after it, [2] after the gate_up kernel (routed
- * gate_up plus the shared expert's gate_up), [3] after the down/combine
- * kernel. Recording events between the kernels serialises them (no
+ * before the router kernel (on up to 16 tokens it also computes the shared
+ * expert's gate_up rows and gate), [1] after it, [2] after the routed gate_up
+ * kernel, [3] after the down/combine kernel. Recording events between the kernels serialises them (no
  * programmatic overlap), so each interval is one kernel's duration. Same
  * results and errors as escha_moe_block. */
 int escha_moe_block_timed(const escha_moe_layer* L, const uint16_t* x, int T, float* out, int32_t* ids_out,

@@ -292,6 +292,18 @@ def test_moe_max_tokens_per_call(native):
     assert rel_err_rows(out.cpu().numpy()[sample], ref).max() <= TOL
 
 
+@pytest.mark.parametrize("T", [1, 2, 3])
+@pytest.mark.parametrize("hidden", [256, 768, 2048, 8192])
+def test_moe_block_few_token_shared_rows(native, hidden, T):
+    """The router grid's shared-expert CTAs: for 1-2 tokens and hidden <= 2048
+    int8 rows and x in registers (768: a lane's last 512-column chunk is
+    partial), for 3 tokens rows in registers and x staged in shared memory,
+    above 2048 (8192) rows read from L2 and x staged."""
+    d = gen.moe_layer(120 + hidden // 256, hidden=hidden, inter=128, n_experts=8, sh_inter=256)
+    x = gen.fp16_normal(gen.rng(121 + hidden + T), (T, hidden))
+    _check_block(native, d, x, topk=2)
+
+
 @pytest.mark.parametrize("T", [2, 24])
 def test_moe_max_hidden(native, T):
     """hidden = 8192, the largest the boundary accepts: the router's column
