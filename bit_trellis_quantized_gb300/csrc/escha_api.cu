@@ -443,8 +443,16 @@ ForkCtx* fork_ctx(cudaStream_t s) {
     return f.s2 ? &f : nullptr;
 }
 
+// Residual input of escha_moe_block_resid: h += add, x = RMSNorm(h).
+struct ResidIn {
+    float* h;
+    const float* add;
+    float eps;
+    uint16_t* x;
+};
+
 int moe_block_impl(const escha_moe_layer* L, const uint16_t* x, int T, float* out, int32_t* ids_out, float* w_out,
-                   void* ws, size_t ws_bytes, void* stream, cudaEvent_t* ev) {
+                   void* ws, size_t ws_bytes, void* stream, cudaEvent_t* ev, const ResidIn* rs = nullptr) {
     int r = check_layer(L);
     if (r) return r;
     if (T < 1) return fail(ESCHA_E_ARG, "moe_block: T=%d must be >= 1", T);
@@ -461,6 +469,18 @@ int moe_block_impl(const escha_moe_layer* L, const uint16_t* x, int T, float* ou
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char* base = static_cast<char*>(ws);
     escha::MoeArgs a = moe_args(L, x, T, out, ids_out, w_out, base, m);
+    if (rs) {
+        if (T <= escha::kFusedNormMaxT && L->hidden <= 2048) {
+            // the router grid normalises; the gate_up grid stores h += add
+            a.rs_h = rs->h;
+            a.rs_add = rs->add;
+            a.rs_eps = rs->eps;
+            a.x_norm = rs->x;
+        } else if ((r = cuda_status(escha::launch_residual_rmsnorm(rs->h, rs->add, T, L->hidden, rs->eps, rs->x, s),
+                                    "residual_rmsnorm launch"))) {
+            return r;
+        }
+    }
     if (T > escha::kSlotModeMaxT) {
         float* d = reinterpret_cast<float*>(base + m.d);
         uint8_t* shimg = reinterpret_cast<uint8_t*>(base + m.shimg);
@@ -511,6 +531,18 @@ extern "C" {
 int escha_moe_block(const escha_moe_layer* L, const uint16_t* x, int T, float* out, int32_t* ids_out, float* w_out,
                     void* ws, size_t ws_bytes, void* stream) {
     return moe_block_impl(L, x, T, out, ids_out, w_out, ws, ws_bytes, stream, nullptr);
+}
+
+int escha_moe_block_resid(const escha_moe_layer* L, float* h, const float* add, float eps, uint16_t* x, int T,
+                          float* out, int32_t* ids_out, float* w_out, void* ws, size_t ws_bytes, void* stream) {
+    int r = check_layer(L);
+    if (r) return r;
+    if (!h || !x) return fail(ESCHA_E_ARG, "moe_block_resid: null h / x");
+    if (!(eps >= 0.f)) return fail(ESCHA_E_ARG, "moe_block_resid: eps must be >= 0");
+    if (!aligned16(h) || (add && !aligned16(add)))
+        return fail(ESCHA_E_ALIGN, "moe_block_resid: h / add not 16-byte aligned");
+    const ResidIn rs{h, add, eps, x};
+    return moe_block_impl(L, x, T, out, ids_out, w_out, ws, ws_bytes, stream, nullptr, &rs);
 }
 
 int escha_moe_block_timed(const escha_moe_layer* L, const uint16_t* x, int T, float* out, int32_t* ids_out,

@@ -69,7 +69,83 @@ __device__ __forceinline__ void dot8_f16(const uint4& xv, const uint4& wv, float
     fma2_f16(xv.w, wv.w, acc);
 }
 
-__device__ void router_logits(const MoeArgs& a, int warp, int lane) {
+// Residual norm of tokens t0 .. t0+nt-1 (nt <= NT) by one CTA of 128 threads,
+// hidden <= 2048: x = f16_rne(v * inv) with v = h + add, into xh (fp16,
+// [nt][hidden], shared memory), in exactly the arithmetic of
+// residual_rmsnorm_kernel: that kernel's thread u of 256 sums v_i^2 over
+// i = u, u+256, ...; here thread r plays u = 2r and u = 2r+1 (one float2
+// per step), so a warp holds two of the 256-thread kernel's warps (lanes 0-15
+// and 16-31); its xor butterfly over offsets 16, 8, 4, 2, 1 becomes lane
+// offsets 8, 4, 2, 1 and the add of the thread's two sums. Ends with the CTA
+// synchronised.
+template <int NT>
+__device__ void resid_norm_cta(const MoeArgs& a, int t0, int nt, uint16_t* xh) {
+    constexpr int J = 2048 / 256;
+    __shared__ float wsum[NT][8];
+    const int r = threadIdx.x, lane = r & 31, warp = r >> 5;
+    float2 v[NT][J];
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            const int i = 2 * r + 256 * j;
+            v[t][j] = make_float2(0.f, 0.f);
+            if (t < nt && i < a.hidden) {
+                const long long o = (long long)(t0 + t) * a.hidden + i;
+                const float2 hv = __ldg(reinterpret_cast<const float2*>(a.rs_h + o));
+                if (a.rs_add) {
+                    const float2 av = __ldg(reinterpret_cast<const float2*>(a.rs_add + o));
+                    v[t][j] = make_float2(__fadd_rn(hv.x, av.x), __fadd_rn(hv.y, av.y));
+                } else {
+                    v[t][j] = hv;
+                }
+            }
+        }
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            if (2 * r + 256 * j < a.hidden) {
+                s0 = __fadd_rn(__fmul_rn(v[t][j].x, v[t][j].x), s0);
+                s1 = __fadd_rn(__fmul_rn(v[t][j].y, v[t][j].y), s1);
+            }
+        }
+#pragma unroll
+        for (int m = 8; m >= 1; m >>= 1) {
+            s0 = __fadd_rn(s0, __shfl_xor_sync(0xffffffffu, s0, m));
+            s1 = __fadd_rn(s1, __shfl_xor_sync(0xffffffffu, s1, m));
+        }
+        s0 = __fadd_rn(s0, s1);
+        if ((lane & 15) == 0) wsum[t][2 * warp + (lane >> 4)] = s0;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        if (t >= nt) break;
+        float tot = wsum[t][0];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) tot = __fadd_rn(tot, wsum[t][w]);
+        const float mean = __fdiv_rn(tot, static_cast<float>(a.hidden));
+        const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, a.rs_eps)));
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            const int i = 2 * r + 256 * j;
+            if (i < a.hidden) {
+                const uint32_t lo = __half_as_ushort(__float2half_rn(__fmul_rn(v[t][j].x, inv)));
+                const uint32_t hi = __half_as_ushort(__float2half_rn(__fmul_rn(v[t][j].y, inv)));
+                *reinterpret_cast<uint32_t*>(xh + t * a.hidden + i) = lo | (hi << 16);
+            }
+        }
+    }
+    __syncthreads();
+}
+
+// FUSED (residual block, <= kFusedNormMaxT tokens, hidden <= 2048): x is
+// computed by resid_norm_cta into xh (shared memory) after the wait, and CTA
+// x = 0 also stores it as the block's x for the later kernels.
+template <bool FUSED>
+__device__ void router_logits(const MoeArgs& a, int warp, int lane, uint16_t* xh) {
     const int e = blockIdx.x * kK0Warps + warp;
     const int t0 = blockIdx.y * kLgTG;
     const int nt = min(kLgTG, a.T - t0);
@@ -88,16 +164,31 @@ __device__ void router_logits(const MoeArgs& a, int warp, int lane) {
             // previous call's kernels may still read) only after the wait
             pdl_wait();
             if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *a.err = 0;  // the previous call has finished
+            if constexpr (FUSED) {
+                resid_norm_cta<kFusedNormMaxT>(a, t0, nt, xh);
+                if (blockIdx.x == 0) {
+                    const int n16 = nt * a.hidden / 8;
+                    for (int u = threadIdx.x; u < n16; u += kK0Threads)
+                        reinterpret_cast<uint4*>(a.x_norm + (long long)t0 * a.hidden)[u] = reinterpret_cast<const uint4*>(xh)[u];
+                }
+            }
             if (e >= a.E) return;
         }
 #pragma unroll
         for (int t = 0; t < kLgTG; ++t) {
             if (t < nt) {
-                const uint16_t* xrow = a.x + (long long)(t0 + t) * a.hidden;
                 uint4 xv[8];
+                if constexpr (FUSED) {
+                    const uint16_t* xrow = xh + t * a.hidden;
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    if (pg + q < passes) xv[q] = __ldg(reinterpret_cast<const uint4*>(xrow + (pg + q) * 256 + lane * 8));
+                    for (int q = 0; q < 8; ++q)
+                        if (pg + q < passes) xv[q] = *reinterpret_cast<const uint4*>(xrow + (pg + q) * 256 + lane * 8);
+                } else {
+                    const uint16_t* xrow = a.x + (long long)(t0 + t) * a.hidden;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        if (pg + q < passes) xv[q] = __ldg(reinterpret_cast<const uint4*>(xrow + (pg + q) * 256 + lane * 8));
+                }
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
                     if (pg + q < passes) dot8_f16(xv[q], wv[q], acc[t]);
@@ -347,8 +438,10 @@ __device__ void shared_gate_up_regs(const MoeArgs& a, int cta, float* xs, int wa
 // (and, in warp 3 of CTA 0, the gate vector) are loaded into registers before
 // the wait for the preceding kernel; after it only x is read, straight into
 // registers (one L2 round trip, no staging). Sums in the order stated above.
-template <int NT>
-__device__ void shared_gate_up_direct(const MoeArgs& a, int cta, int warp, int lane) {
+// FUSED: x is computed by resid_norm_cta into xh after the wait and read
+// from there.
+template <int NT, bool FUSED>
+__device__ void shared_gate_up_direct(const MoeArgs& a, int cta, int warp, int lane, uint16_t* xh) {
     constexpr int R = kShRowsPerWarp;
     const int rows = 2 * a.sh_inter;
     const int r0 = (cta * kK0Warps + warp) * R;
@@ -373,6 +466,11 @@ __device__ void shared_gate_up_direct(const MoeArgs& a, int cta, int warp, int l
                     ? __ldg(reinterpret_cast<const uint4*>(a.sh_gate + lane * 8 + 256 * k))
                     : make_uint4(0u, 0u, 0u, 0u);
     pdl_wait();  // x, and the workspace the previous call's kernels may still read
+    if constexpr (FUSED) resid_norm_cta<NT>(a, 0, a.T, xh);
+    auto ldx = [&](long long off) -> uint4 {
+        if constexpr (FUSED) return *reinterpret_cast<const uint4*>(xh + off);
+        else return __ldg(reinterpret_cast<const uint4*>(a.x + off));
+    };
     if (nrows > 0) {
         uint4 xv[NT][4][2];
 #pragma unroll
@@ -382,7 +480,7 @@ __device__ void shared_gate_up_direct(const MoeArgs& a, int cta, int warp, int l
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
                     xv[t][c][h] = (t < a.T && c * 512 + lane * 16 < a.hidden)
-                                      ? __ldg(reinterpret_cast<const uint4*>(a.x + (long long)t * a.hidden + c * 512 + lane * 16 + 8 * h))
+                                      ? ldx((long long)t * a.hidden + c * 512 + lane * 16 + 8 * h)
                                       : make_uint4(0u, 0u, 0u, 0u);
         float acc[R][NT];
 #pragma unroll
@@ -440,8 +538,7 @@ __device__ void shared_gate_up_direct(const MoeArgs& a, int cta, int warp, int l
             const uint32_t gw[4] = {gv[k].x, gv[k].y, gv[k].z, gv[k].w};
 #pragma unroll
             for (int t = 0; t < NT; ++t) {
-                const uint4 xg = t < a.T ? __ldg(reinterpret_cast<const uint4*>(a.x + (long long)t * a.hidden + i0))
-                                         : make_uint4(0u, 0u, 0u, 0u);
+                const uint4 xg = t < a.T ? ldx((long long)t * a.hidden + i0) : make_uint4(0u, 0u, 0u, 0u);
                 const uint32_t xw[4] = {xg.x, xg.y, xg.z, xg.w};
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -464,25 +561,28 @@ __device__ void shared_gate_up_direct(const MoeArgs& a, int cta, int warp, int l
 // the CTAs after them in row y = 0 compute its gate_up rows and its gate
 // (4 warps each, MT tokens per pass), so that the gate_up kernel is routed
 // experts only and the shared rows run while the logits are computed.
-template <int MT>
+template <int MT, bool FUSED>
 __global__ void __launch_bounds__(kK0Threads) moe_router_kernel(const MoeArgs a, int n_lg) {
     // The gate_up kernel can be scheduled at once, while the kernel before
     // this one may still run: every gate_up CTA waits for this grid (and so
     // for that kernel) before it touches x, the logits or the workspace.
     pdl_trigger();
+    extern __shared__ __align__(16) float xs_sh[];
+    uint16_t* xh = reinterpret_cast<uint16_t*>(xs_sh);  // residual block: normalised x
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    static_assert(!FUSED || MT <= kFusedNormMaxT, "the residual norm runs in the router grid for few tokens only");
     if (static_cast<int>(blockIdx.x) < n_lg) {
-        router_logits(a, warp, lane);  // waits for the preceding kernel after its first weight loads
+        router_logits<FUSED>(a, warp, lane, xh);  // waits for the preceding kernel after its first weight loads
         return;
     }
     if (blockIdx.y != 0) return;
-    extern __shared__ __align__(16) float xs_sh[];
     const int cta = static_cast<int>(blockIdx.x) - n_lg;
     if (a.hidden <= 2048) {
-        if (MT <= 2)
-            shared_gate_up_direct<MT>(a, cta, warp, lane);
-        else
+        if constexpr (MT <= 2) {
+            shared_gate_up_direct<MT, FUSED>(a, cta, warp, lane, xh);
+        } else {
             shared_gate_up_regs<kK0Warps, MT>(a, cta, xs_sh, warp, lane);
+        }
     } else {
         shared_gate_up_staged<kK0Warps, MT>(a, cta, xs_sh, warp, lane);
     }
@@ -595,6 +695,17 @@ __device__ void gate_up_routed(const MoeArgs& a, float* smem) {
                 a.ids[(long long)t * a.topk + lane] = e_l;
                 a.w[(long long)t * a.topk + lane] = w_l;
             }
+        }
+    } else if (a.rs_h && a.rs_add && crank == 0 && ob == 0 && j == 0) {
+        // residual block: the same CTA stores h += add for its token (the
+        // router grid, which read h, has finished)
+        float* hr = a.rs_h + (long long)t * a.hidden;
+        const float* ar = a.rs_add + (long long)t * a.hidden;
+        for (int i = (threadIdx.x - 32) * 4; i < a.hidden; i += (kGuThreads - 32) * 4) {
+            const float4 hv = *reinterpret_cast<const float4*>(hr + i);
+            const float4 av = *reinterpret_cast<const float4*>(ar + i);
+            *reinterpret_cast<float4*>(hr + i) =
+                make_float4(__fadd_rn(hv.x, av.x), __fadd_rn(hv.y, av.y), __fadd_rn(hv.z, av.z), __fadd_rn(hv.w, av.w));
         }
     }
     __syncthreads();
@@ -959,10 +1070,14 @@ cudaError_t launch_moe_router(const MoeArgs& a, bool with_shared, cudaStream_t s
     // tokens per pass of the shared rows: 1 or 2 read x straight into
     // registers (hidden <= 2048), otherwise x is staged in shared memory
     const int mt = a.T <= 2 ? a.T : kShMT;
-    const int smem = n_sh > 0 && !(mt <= 2 && a.hidden <= 2048) ? mt * a.hidden * 4 : 0;
-    const void* f = mt == 1   ? reinterpret_cast<const void*>(moe_router_kernel<1>)
-                    : mt == 2 ? reinterpret_cast<const void*>(moe_router_kernel<2>)
-                              : reinterpret_cast<const void*>(moe_router_kernel<kShMT>);
+    int smem = n_sh > 0 && !(mt <= 2 && a.hidden <= 2048) ? mt * a.hidden * 4 : 0;
+    if (a.x_norm) smem = max(smem, kFusedNormMaxT * a.hidden * 2);  // residual block: normalised x (fp16)
+    const bool fused = a.x_norm != nullptr;  // set by the caller for <= kFusedNormMaxT tokens only
+    static_assert(kFusedNormMaxT == 1, "fused router instantiations cover one token");
+    const void* f = mt == 1   ? (fused ? reinterpret_cast<const void*>(moe_router_kernel<1, true>)
+                                       : reinterpret_cast<const void*>(moe_router_kernel<1, false>))
+                    : mt == 2 ? reinterpret_cast<const void*>(moe_router_kernel<2, false>)
+                              : reinterpret_cast<const void*>(moe_router_kernel<kShMT, false>);
     cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};

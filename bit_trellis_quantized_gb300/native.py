@@ -50,6 +50,7 @@ EXPORTS = [
     "escha_moe_block_workspace",
     "escha_moe_block",
     "escha_moe_block_timed",
+    "escha_moe_block_resid",
     "escha_moe_block_noalloc",
     "escha_moe_route_workspace",
     "escha_moe_route",
@@ -161,6 +162,9 @@ def lib() -> ctypes.CDLL:
         L.escha_moe_block_timed.argtypes = [ctypes.POINTER(EschaMoeLayer), _vp, _i, _vp, _vp, _vp, _vp, _sz, _vp,
                                             ctypes.POINTER(_vp)]
         L.escha_moe_block_timed.restype = _i
+        L.escha_moe_block_resid.argtypes = [ctypes.POINTER(EschaMoeLayer), _vp, _vp, ctypes.c_float, _vp, _i, _vp, _vp,
+                                            _vp, _vp, _sz, _vp]
+        L.escha_moe_block_resid.restype = _i
         L.escha_moe_block_noalloc.argtypes = [ctypes.POINTER(EschaMoeLayer), _vp, _i, _vp, _vp, _vp, _vp]
         L.escha_moe_block_noalloc.restype = _i
         L.escha_moe_route_workspace.argtypes = [ctypes.POINTER(EschaMoeLayer), _i]
@@ -546,6 +550,27 @@ class MoeBlock:
                                     ws.numel(), stream_handle(stream)))
         return out, ids, w
 
+    def resid(self, h: torch.Tensor, add, x: torch.Tensor, eps: float = 1e-6, out=None, ids=None, w=None,
+              stream=None, ws=None):
+        """Residual block: h (f32 [T][hidden]) += add (or nothing when add is
+        None), x (fp16 [T][hidden], written) = weightless RMSNorm of h, then the
+        block on x. ``out`` may be ``add``. Returns (out, ids, w)."""
+        _need_cuda(h, x)
+        T = h.shape[0]
+        dev = h.device
+        if out is None:
+            out = torch.empty((T, self.hidden), dtype=torch.float32, device=dev)
+        if ids is None:
+            ids = torch.empty((T, self.topk), dtype=torch.int32, device=dev)
+        if w is None:
+            w = torch.empty((T, self.topk), dtype=torch.float32, device=dev)
+        if ws is None:
+            ws = self.workspace(T)
+        check(lib().escha_moe_block_resid(ctypes.byref(self.layer), ptr(h), ptr(add) if add is not None else None,
+                                          float(eps), ptr(x), T, ptr(out), ptr(ids), ptr(w), ptr(ws), ws.numel(),
+                                          stream_handle(stream)))
+        return out, ids, w
+
     def route(self, x: torch.Tensor, stream=None) -> dict:
         """Diagnostic: router logits (fp16 bits), ids, w and the grouping by
         expert (counts, offsets, perm) for x [T][hidden] fp16."""
@@ -570,8 +595,9 @@ class MoeBlock:
 
 class MoeStack:
     """MoE blocks on an f32 residual stream h: for each block, x =
-    fp16(RMSNorm(h)) (weightless), h += block(x); the add is fused into the
-    next block's norm. One workspace serves all blocks (same shapes)."""
+    fp16(RMSNorm(h)) (weightless), h += block(x); the add and the norm are
+    fused into the next block's call (escha_moe_block_resid). One workspace
+    serves all blocks (same shapes)."""
 
     def __init__(self, blocks, eps: float = 1e-6):
         self.blocks = list(blocks)
@@ -594,14 +620,8 @@ class MoeStack:
         out = out_buf if out_buf is not None else torch.empty((T, H), dtype=torch.float32, device=h.device)
         ws = self.workspace(T)
         for i, b in enumerate(self.blocks):
-            h_before = h.clone() if trace is not None and i == 0 else None
-            residual_rmsnorm(h, out if i > 0 else None, x, self.eps, stream)
-            if trace is not None:
-                if i > 0:
-                    h_before = h.clone()
-                trace.append([h_before.cpu(), x.cpu()])
-            b(x, out=out, stream=stream, ws=ws)
-            if trace is not None:
-                trace[-1].append(out.cpu())
+            b.resid(h, out if i > 0 else None, x, self.eps, out=out, stream=stream, ws=ws)
+            if trace is not None:  # h after the add (the h x was normalised from), x, the block output
+                trace.append([h.cpu(), x.cpu(), out.cpu()])
         residual_add(h, out, stream)
         return h

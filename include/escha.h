@@ -289,6 +289,21 @@ size_t escha_moe_block_workspace(const escha_moe_layer* L, int T);
 int escha_moe_block(const escha_moe_layer* L, const uint16_t* x, int T, float* out, int32_t* ids_out, float* w_out,
                     void* ws, size_t ws_bytes, void* stream);
 
+/* Residual MoE block: h += add (add nullable), x = f16_rne(h * inv) with the
+ * weightless RMSNorm of escha_residual_rmsnorm, then escha_moe_block on x:
+ * bit for bit the same h, x, out, ids and weights as those two calls in a
+ * row. On one token with hidden <= 2048 (batch-1 decode of the
+ * Qwen3.6-35B-A3B layer) the norm runs inside the block's router grid: one
+ * kernel boundary fewer per layer of a decode stack; otherwise the norm
+ * kernel runs first.
+ *   h    f32 [T][hidden], updated in place;  add f32 [T][hidden] or NULL
+ *   eps  >= 0;  x fp16 bits [T][hidden], written (the block's input)
+ *   out may be the same buffer as add (the previous block's output); x must
+ *   not overlap h, add or out. Other arguments, workspace and errors as
+ *   escha_moe_block. */
+int escha_moe_block_resid(const escha_moe_layer* L, float* h, const float* add, float eps, uint16_t* x, int T,
+                          float* out, int32_t* ids_out, float* w_out, void* ws, size_t ws_bytes, void* stream);
+
 /* Measurement export: escha_moe_block that also records four caller-created
  * CUDA events (cudaEvent_t, any of them may be null) on `stream`: events[0]
  * before the router kernel (on up to 16 tokens it also computes the shared

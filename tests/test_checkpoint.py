@@ -25,7 +25,7 @@ def _write(tmp_path, tensors, name="model.safetensors", **kw):
     return str(p)
 
 
-def _native_verdict(native, paths):
+def _native_outcome(native, paths):
     try:
         c = native.Checkpoint(paths)
     except native.EschaError as e:
@@ -37,7 +37,7 @@ def _native_verdict(native, paths):
         c.close()
 
 
-def _oracle_verdict(paths):
+def _oracle_outcome(paths):
     try:
         return "ok", oc.validate(paths)
     except oc.ContractError as e:
@@ -162,8 +162,8 @@ def test_loader_matches_oracle_on_every_case(native, tmp_path):
         if tag == "missing_file":
             ov = ("io", "")
         else:
-            ov = _oracle_verdict(paths)
-        nv = _native_verdict(native, paths)
+            ov = _oracle_outcome(paths)
+        nv = _native_outcome(native, paths)
         assert nv[0] == ov[0], (tag, nv, ov)
         assert ov[0] == expect.get(tag, ov[0] if ov[0] != "ok" else "error"), (tag, ov)
         if ov[0] == "ok":
@@ -196,7 +196,7 @@ def test_export_projections_and_raw_reads(native, tmp_path):
 def test_loader_matches_oracle_on_generated_exports(native, tmp_path):
     """Random exports (seeded draws of projection shapes, K, expert counts,
     optional leaves, biases, missing or unknown leaves, shard splits): the
-    native loader and the oracle agree on every verdict and, for valid
+    native loader and the oracle agree on every outcome and, for valid
     exports, on every projection's description."""
     rng = np.random.default_rng(20261202)
     for case in range(60):
@@ -233,7 +233,7 @@ def test_loader_matches_oracle_on_generated_exports(native, tmp_path):
                      _write(tmp_path, {k: t[k] for k in names[cut:]}, name=f"g{case}b.safetensors")]
         else:
             paths = [_write(tmp_path, t, name=f"g{case}.safetensors")]
-        ov, nv = _oracle_verdict(paths), _native_verdict(native, paths)
+        ov, nv = _oracle_outcome(paths), _native_outcome(native, paths)
         assert nv[0] == ov[0], (case, nv, ov)
         if ov[0] == "ok":
             assert nv[1] == ov[1], case

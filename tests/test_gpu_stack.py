@@ -40,14 +40,16 @@ def test_residual_rmsnorm_bit_exact(native, H):
     assert np.array_equal(hd2.cpu().numpy().view(np.uint32), ref_h.view(np.uint32))
 
 
-def test_stack_small_each_block_against_oracle(native):
+@pytest.mark.parametrize("T", [1, 2, 6])
+def test_stack_small_each_block_against_oracle(native, T):
     """Three small blocks with mixed K: at every block, x is the oracle's norm
     of the GPU's h bit for bit, and the block output matches the oracle's
-    block on that x."""
+    block on that x (1 token: the norm inside the router grid; 2 and 6: the
+    norm kernel)."""
     layers = [gen.moe_layer(80 + i, hidden=512, inter=256, n_experts=16, k_gu=k[0], k_dn=k[1])
               for i, k in enumerate([(3, 2), (2, 3), (2, 2)])]
     stack = native.MoeStack([native.MoeBlock(d, topk=4) for d in layers])
-    x0 = gen.fp16_normal(gen.rng(90), (6, 512))
+    x0 = gen.fp16_normal(gen.rng(90 + T), (T, 512))
     h = dev(x0.astype(np.float32))
     trace = []
     stack(h, trace=trace)
@@ -92,3 +94,33 @@ def test_stack_40_blocks_full_size(native, T):
     assert rel_err_rows(out.numpy(), ref).max() <= TOL
     del blocks, stack
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("T,H", [(1, 2048), (2, 2048), (2, 768), (1, 256), (3, 2048), (1, 4096), (20, 512)])
+@pytest.mark.parametrize("with_add", [True, False])
+def test_moe_block_resid_equals_norm_then_block(native, T, H, with_add):
+    """escha_moe_block_resid against escha_residual_rmsnorm followed by
+    escha_moe_block: h, x, outputs, ids and weights bit for bit, whether the
+    norm runs inside the router grid (1 token, hidden <= 2048) or as its own
+    kernel; the output written over the add buffer."""
+    d = gen.moe_layer(300 + T + H, hidden=H, inter=128, n_experts=8, sh_inter=128)
+    block = native.MoeBlock(d, topk=2)
+    g = gen.rng(301 + T * H)
+    h0 = (g.standard_normal((T, H)) * g.uniform(0.1, 10.0, (T, 1))).astype(np.float32)
+    add0 = (g.standard_normal((T, H)) * 3).astype(np.float32)
+    # reference: the two calls
+    h_ref = dev(h0)
+    x_ref = native.residual_rmsnorm(h_ref, dev(add0) if with_add else None, eps=1e-5)
+    out_ref, ids_ref, w_ref = block(x_ref)
+    # fused call, out over the add buffer
+    h = dev(h0)
+    add = dev(add0)
+    x = torch.empty((T, H), dtype=torch.float16, device="cuda")
+    out, ids, w = block.resid(h, add if with_add else None, x, eps=1e-5, out=add)
+    torch.cuda.synchronize()
+    assert torch.equal(h.view(torch.int32), h_ref.view(torch.int32))
+    assert torch.equal(x.view(torch.int16), x_ref.view(torch.int16))
+    assert torch.equal(ids, ids_ref)
+    assert torch.equal(w.view(torch.int32), w_ref.view(torch.int32))
+    assert torch.equal(out.view(torch.int32), out_ref.view(torch.int32))
+    assert int(block.workspace(T)[:4].view(torch.int32).item()) == 0
