@@ -465,6 +465,22 @@ __device__ void shared_gate_up_direct(const MoeArgs& a, int cta, int warp, int l
         gv[k] = (gate && lane * 8 + 256 * k < a.hidden)
                     ? __ldg(reinterpret_cast<const uint4*>(a.sh_gate + lane * 8 + 256 * k))
                     : make_uint4(0u, 0u, 0u, 0u);
+    // the rows in f32 while the preceding kernel finishes: after the wait
+    // only x is converted
+    float wf[R][64];  // (c, q, k): column c*512 + 16*lane + 4q + k
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t words[4] = {wv[r][c].x, wv[r][c].y, wv[r][c].z, wv[r][c].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float f[4];
+                i8x4_to_f32(words[q], f);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) wf[r][16 * c + 4 * q + k] = f[k];
+            }
+        }
     pdl_wait();  // x, and the workspace the previous call's kernels may still read
     if constexpr (FUSED) resid_norm_cta<NT>(a, 0, a.T, xh);
     auto ldx = [&](long long off) -> uint4 {
@@ -504,9 +520,7 @@ __device__ void shared_gate_up_direct(const MoeArgs& a, int cta, int warp, int l
                 }
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    const uint32_t word = q == 0 ? wv[r][c].x : q == 1 ? wv[r][c].y : q == 2 ? wv[r][c].z : wv[r][c].w;
-                    float f[4];
-                    i8x4_to_f32(word, f);
+                    const float* f = &wf[r][16 * c + 4 * q];
 #pragma unroll
                     for (int t = 0; t < NT; ++t) {
                         acc[r][t] = fmaf(f[0], xq[t][0], acc[r][t]);
