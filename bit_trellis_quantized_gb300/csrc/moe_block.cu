@@ -786,8 +786,10 @@ __global__ void __launch_bounds__(kGuThreads, 4) moe_gate_up_kernel(const MoeArg
 // ---------------------------------------------------------------------------
 // 3. down + combine.
 // ---------------------------------------------------------------------------
-template <int K>
-__global__ void __launch_bounds__(kDnThreads, 3) moe_down_kernel(const MoeArgs a) {
+// MINB CTAs per SM: 4 (64 registers) when the grid needs more than one wave
+// of 3, else 3 (80 registers, faster per CTA).
+template <int K, int MINB>
+__global__ void __launch_bounds__(kDnThreads, MINB) moe_down_kernel(const MoeArgs a) {
     const int rank = static_cast<int>(cg::this_cluster().block_rank());
     const int csz = static_cast<int>(cg::this_cluster().num_blocks());
     const int ks = a.dn_ksplit;
@@ -1059,7 +1061,13 @@ cudaError_t launch_down(MoeArgs a, int num_sms, cudaStream_t s) {
     // staging works on groups of 32 floats)
     const int nsh = (a.sh_inter + 31) / 32 * 32;
     const int smem = (kMaxCluster * 128 + 128 + 8 * 128 + (kDnWarps + 1) * 128 + a.dn_xt_floats + nsh) * 4;
-    const void* f = reinterpret_cast<const void*>(moe_down_kernel<K>);
+    // More than one wave of 3 CTAs per SM: the 64-register build, 4 per SM
+    // (measured on GB300 for the 35B layer: 4 tokens 52.3 -> 46.9 us per
+    // block, 8 tokens 88.9 -> 85.0, 16 tokens 155.9 -> 148.2; with one
+    // wave, 1-2 tokens, it was slower: 1 token 21.0 -> 21.6 us).
+    const long long ctas = (long long)csz * (a.hidden / 128) * a.T;
+    const void* f = ctas > 3LL * kWaveSms ? reinterpret_cast<const void*>(moe_down_kernel<K, 4>)
+                                          : reinterpret_cast<const void*>(moe_down_kernel<K, 3>);
     cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (csz > 8) {
