@@ -672,11 +672,10 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeArgs a, const
     }
 }
 
+// stages: 2 or 3 shared-memory stages (A and B). Fewer stages let more
+// CTAs share an SM when items are small.
 template <int K>
-cudaError_t launch_grouped(const MoeArgs& a, const GroupedProj& p, cudaStream_t s) {
-    // three stages where shared memory keeps the same CTAs per SM (items of up
-    // to 64 tokens), two for 128-token items
-    const int stages = a.grp_cap <= 64 ? 3 : 2;
+cudaError_t launch_grouped(const MoeArgs& a, const GroupedProj& p, int stages, cudaStream_t s) {
     const int smem = stages * (16384 + 256 * a.grp_cap) + 1024;
     const void* f = stages == 3 ? reinterpret_cast<const void*>(moe_grouped_gemm_kernel<K, 3>)
                                 : reinterpret_cast<const void*>(moe_grouped_gemm_kernel<K, 2>);
@@ -747,12 +746,16 @@ cudaError_t launch_moe_grouped(const MoeArgs& a, float* d, int num_sms, cudaStre
     const GroupedProj gu{a.gu_codes, a.gu_rin, a.gu_rout, a.hidden, 2 * a.inter, 0, a.ygu,
                          tile_strides(a.hidden, 2 * a.inter, false), nullptr, nullptr, a.hidden >> 6, nullptr};
     if ((e = launch_prep(a, gu, s)) != cudaSuccess) return e;
-    e = a.gu_K == 2 ? launch_grouped<2>(a, gu, s) : launch_grouped<3>(a, gu, s);
+    // MoE items: two stages, so that items of up to 32 tokens run 4 CTAs per
+    // SM (3 with three stages; measured on GB300 for the 35B layer: 17 / 64 /
+    // 256 tokens 165.7 / 290.4 / 346.2 -> 161.6 / 279.1 / 333.3 us per block;
+    // 2048 tokens, items of 128 with two stages already, unchanged)
+    e = a.gu_K == 2 ? launch_grouped<2>(a, gu, 2, s) : launch_grouped<3>(a, gu, 2, s);
     if (e != cudaSuccess) return e;
     const GroupedProj dn{a.dn_codes, a.dn_rin, a.dn_rout, a.inter, a.hidden, 1, d,
                          tile_strides(a.inter, a.hidden, false), nullptr, nullptr, a.inter >> 6, nullptr};
     if ((e = launch_prep(a, dn, s)) != cudaSuccess) return e;
-    return a.dn_K == 2 ? launch_grouped<2>(a, dn, s) : launch_grouped<3>(a, dn, s);
+    return a.dn_K == 2 ? launch_grouped<2>(a, dn, 2, s) : launch_grouped<3>(a, dn, 2, s);
 }
 
 cudaError_t launch_dense_grouped(const DenseArgs& d, cudaStream_t s) {
@@ -775,7 +778,10 @@ cudaError_t launch_dense_grouped(const DenseArgs& d, cudaStream_t s) {
     cudaError_t e = launch_prep(a, p, s);
     if (e != cudaSuccess) return e;
     a.grp_max_items = (d.M + d.cap - 1) / d.cap;
-    e = d.K == 2 ? launch_grouped<2>(a, p, s) : launch_grouped<3>(a, p, s);
+    // dense items: three stages up to 64 tokens (the K split is sized for the
+    // CTAs per SM this gives), two for 128
+    const int stages = d.cap <= 64 ? 3 : 2;
+    e = d.K == 2 ? launch_grouped<2>(a, p, stages, s) : launch_grouped<3>(a, p, stages, s);
     if (e != cudaSuccess || splits == 1) return e;
     int M = d.M, sp = splits;
     void* rargs[] = {const_cast<GroupedProj*>(&p), &M, &sp};
