@@ -778,9 +778,10 @@ cudaError_t launch_dense_grouped(const DenseArgs& d, cudaStream_t s) {
     cudaError_t e = launch_prep(a, p, s);
     if (e != cudaSuccess) return e;
     a.grp_max_items = (d.M + d.cap - 1) / d.cap;
-    // dense items: three stages up to 64 tokens (the K split is sized for the
-    // CTAs per SM this gives), two for 128
-    const int stages = d.cap <= 64 ? 3 : 2;
+    // dense items: three stages up to 32 tokens, two from 64 (measured on
+    // GB300: 64 tokens 5120 -> 17408 57.8 -> 49.6 us, 17408 -> 5120 72.6 ->
+    // 69.8 us; with two stages 8-32 tokens were 1-4% slower)
+    const int stages = d.cap <= 32 ? 3 : 2;
     e = d.K == 2 ? launch_grouped<2>(a, p, stages, s) : launch_grouped<3>(a, p, stages, s);
     if (e != cudaSuccess || splits == 1) return e;
     int M = d.M, sp = splits;
