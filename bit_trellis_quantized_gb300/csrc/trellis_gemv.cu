@@ -54,8 +54,9 @@ __device__ void gemv_input_transform(const GemvArgs& a, int xrow0, int ntok, int
     }
 }
 
+// One token per CTA: 64 registers, 4 CTAs per SM; 2 or 4 tokens: 2 per SM.
 template <int K, int NB, int XM>
-__global__ void __launch_bounds__(kThreads, 2) trellis_gemv_kernel(const GemvArgs a) {
+__global__ void __launch_bounds__(kThreads, NB == 1 ? 4 : 2) trellis_gemv_kernel(const GemvArgs a) {
     cg::cluster_group cluster = cg::this_cluster();
     const int crank = static_cast<int>(cluster.block_rank());
     const int csize = static_cast<int>(cluster.num_blocks());
@@ -186,8 +187,10 @@ cudaError_t launch_trellis_gemv(const GemvArgs& a, int K, int nb, int items, int
     int csize;
     // clusters of up to 16 CTAs for one token per CTA (a short, latency-bound
     // projection: 1024 x 2048 went from 3.88 to 3.73 us); with 2 or 4 tokens
-    // per CTA the larger cluster reduction costs more than it saves
-    gemv_plan_clusters(a.in, items * (a.out / 128), num_sms, 2, nb == 1 ? 16 : 8, &b.kt_per_cta, &csize);
+    // per CTA the larger cluster reduction costs more than it saves. One
+    // token per CTA plans for 4 resident CTAs per SM (5120 -> 6144 at one
+    // token 20.4 -> 16.7 us; other shapes within 1%).
+    gemv_plan_clusters(a.in, items * (a.out / 128), num_sms, nb == 1 ? 4 : 2, nb == 1 ? 16 : 8, &b.kt_per_cta, &csize);
     return K == 2 ? launch_nb<2>(b, nb, csize, items, s) : launch_nb<3>(b, nb, csize, items, s);
 }
 
