@@ -541,6 +541,17 @@ int escha_moe_block_resid(const escha_moe_layer* L, float* h, const float* add, 
     if (!(eps >= 0.f)) return fail(ESCHA_E_ARG, "moe_block_resid: eps must be >= 0");
     if (!aligned16(h) || (add && !aligned16(add)))
         return fail(ESCHA_E_ALIGN, "moe_block_resid: h / add not 16-byte aligned");
+    if (T >= 1 && T <= 8192) {
+        // x is written while h and add are read and before out is written:
+        // it must not share memory with any of them
+        const uintptr_t x0 = reinterpret_cast<uintptr_t>(x), x1 = x0 + (size_t)T * L->hidden * 2;
+        auto overlaps = [&](const void* p) {
+            const uintptr_t p0 = reinterpret_cast<uintptr_t>(p), p1 = p0 + (size_t)T * L->hidden * 4;
+            return p && p0 < x1 && x0 < p1;
+        };
+        if (overlaps(h) || overlaps(add) || overlaps(out))
+            return fail(ESCHA_E_ARG, "moe_block_resid: x overlaps h, add or out");
+    }
     const ResidIn rs{h, add, eps, x};
     return moe_block_impl(L, x, T, out, ids_out, w_out, ws, ws_bytes, stream, nullptr, &rs);
 }

@@ -179,6 +179,20 @@ def test_moe_validation_and_workspace():
     lay.sh_inter = 512
     assert call(need) == native.ESCHA_E_ARG  # shared-expert pointers missing
     assert L.escha_moe_block(None, g, 1, g, None, None, g, need, None) == native.ESCHA_E_ARG
+    # the residual call: its own arguments are checked before the block's
+    lay.sh_inter = 0
+    h, x, out = 0x100000, 0x200000, 0x300000  # [1][2048] f32 / fp16 / f32, apart
+    resid = lambda h_, add_, eps_, x_, out_: L.escha_moe_block_resid(ctypes.byref(lay), h_, add_, eps_, x_, 1, out_,
+                                                                        None, None, g, need, None)
+    assert resid(None, None, 1e-6, x, out) == native.ESCHA_E_ARG
+    assert resid(h, None, 1e-6, None, out) == native.ESCHA_E_ARG
+    assert resid(h, None, -1.0, x, out) == native.ESCHA_E_ARG
+    assert resid(h + 4, None, 1e-6, x, out) == native.ESCHA_E_ALIGN
+    assert resid(h, h + 8192 + 4, 1e-6, x, out) == native.ESCHA_E_ALIGN  # add not 16-byte aligned
+    assert resid(h, None, 1e-6, h + 4096, out) == native.ESCHA_E_ARG  # x inside h
+    assert resid(h, None, 1e-6, x, x - 4096) == native.ESCHA_E_ARG  # out overlaps x
+    assert resid(h, x - 8192 + 16, 1e-6, x, out) == native.ESCHA_E_ARG  # add's tail overlaps x
+    assert L.escha_moe_block_resid(None, h, None, 1e-6, x, 1, out, None, None, g, need, None) == native.ESCHA_E_ARG
 
 
 def test_product_path_has_no_oracle_import():
