@@ -96,7 +96,7 @@ def test_stack_40_blocks_full_size(native, T):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("T,H", [(1, 2048), (2, 2048), (2, 768), (1, 256), (3, 2048), (1, 4096), (20, 512)])
+@pytest.mark.parametrize("T,H", [(1, 2048), (1, 768), (2, 2048), (2, 768), (1, 256), (3, 2048), (1, 4096), (20, 512)])
 @pytest.mark.parametrize("with_add", [True, False])
 def test_moe_block_resid_equals_norm_then_block(native, T, H, with_add):
     """escha_moe_block_resid against escha_residual_rmsnorm followed by
