@@ -63,3 +63,26 @@ def test_aggregate_counts_every_rank():
     assert bench.aggregate_tokens_per_s(1, 0.025) == pytest.approx(40000.0)
     assert bench.aggregate_tokens_per_s(4, 0.025) == pytest.approx(160000.0)
     assert bench.max_over_ranks([1.5, 2.5]) == [1.5, 2.5]
+
+
+def test_reference_arm_json_line():
+    """`bench.py --impl reference` prints one JSON line with the contract's
+    keys, its own metric, the oracle as cpu_baseline and an e2e object."""
+    import json
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    res = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--steps", "1",
+                          "--warmup", "3"], capture_output=True, text=True, timeout=300, cwd=root)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [l for l in res.stdout.splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+              "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["steps"] == 1 and d["warmup"] == 3 and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"]["value"] == d["value"] and d["e2e"]["h2d_bytes_per_step"] == 0
+    assert "workload" in d["config"]
