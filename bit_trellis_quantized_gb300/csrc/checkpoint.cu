@@ -313,7 +313,7 @@ int parse_shard(escha_ckpt* c, int si) {
         return ck_fail(ESCHA_E_IO, "checkpoint: " + path + " has an invalid header length");
     std::string hdr(hlen, '\0');
     if (fread(&hdr[0], 1, hlen, f.get()) != hlen) return ck_fail(ESCHA_E_IO, "checkpoint: cannot read header of " + path);
-    escha_ckpt_impl::Parser ps{hdr.data(), hdr.data() + hdr.size()};
+    escha_ckpt_impl::Parser ps{hdr.data(), hdr.data() + hdr.size(), std::string(), 0};
     Json root;
     if (!ps.value(root)) return ck_fail(ESCHA_E_IO, "checkpoint: header of " + path + " is not JSON (" + ps.err + ")");
     ps.ws();

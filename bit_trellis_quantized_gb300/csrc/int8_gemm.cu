@@ -27,7 +27,7 @@ namespace escha {
 
 namespace {
 
-constexpr int kDtF16 = 1, kDtBf16 = 2, kDtF32 = 3;
+constexpr int kDtBf16 = 2, kDtF32 = 3;  // activation dtypes (ESCHA_BF16, ESCHA_F32); ESCHA_F16 is 1
 constexpr int kRowsPerCta = 256;  // image rows (B rows) per CTA = MMA N at most
 constexpr int kOutPerCta = 256;   // output rows per CTA: two M = 128 tiles sharing each B chunk
 constexpr int kStages = 3;
