@@ -193,6 +193,15 @@ def test_moe_validation_and_workspace():
     assert resid(h, None, 1e-6, x, x - 4096) == native.ESCHA_E_ARG  # out overlaps x
     assert resid(h, x - 8192 + 16, 1e-6, x, out) == native.ESCHA_E_ARG  # add's tail overlaps x
     assert L.escha_moe_block_resid(None, h, None, 1e-6, x, 1, out, None, None, g, need, None) == native.ESCHA_E_ARG
+    # empty and oversized batches are rejected before anything is enqueued
+    assert L.escha_moe_block(ctypes.byref(lay), g, 0, g, None, None, g, need, None) == native.ESCHA_E_ARG
+    assert L.escha_moe_block(ctypes.byref(lay), g, 8193, g, None, None, g, 1 << 40, None) == native.ESCHA_E_SHAPE
+    assert L.escha_moe_block_resid(ctypes.byref(lay), h, None, 1e-6, x, 0, out, None, None, g, need,
+                                   None) == native.ESCHA_E_ARG
+    assert L.escha_moe_block_noalloc(ctypes.byref(lay), g, 0, g, None, None, None) == native.ESCHA_E_ARG
+    assert L.escha_moe_block_workspace(ctypes.byref(lay), 0) == 0
+    assert L.escha_residual_rmsnorm(h, None, 0, 2048, 1e-6, x, None) == native.ESCHA_E_SHAPE
+    assert L.escha_residual_rmsnorm(h, None, 1, 8193, 1e-6, x, None) == native.ESCHA_E_SHAPE
 
 
 def test_product_path_has_no_oracle_import():
