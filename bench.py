@@ -435,7 +435,9 @@ def run_ours(args, ws, rank, local):
     line = {
         "metric": METRIC, "value": aggregate_tokens_per_s(ws, t_step), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "fp16 weights / f32 accumulate", "data": "synthetic",
+        "vs_baseline": None, "dtype": "f32",
+        "dtype_note": "f32 arithmetic on fp16 weights decoded from 2/3-bit trellis codes (int8 shared expert)",
+        "data": "synthetic",
         "config": {"workload": WORKLOAD, "batch": 1, "tokens_per_step_per_gpu": 1,
                    "l2": f"inputs larger than L2: {n_layers} distinct MoE layers "
                          f"({n_layers * 272} MB) cycled, one per step, no flush",
