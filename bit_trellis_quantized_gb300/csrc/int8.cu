@@ -313,7 +313,9 @@ cudaError_t launch_int8_gemv(const int8_t* W, const float* scales, int N, int Ki
     // Batch 1 with few rows: rows x chunks spread over the CTAs. With many
     // rows (four or more row groups of 32 per SM) the whole-row kernel below
     // already has enough loads in flight and needs no shared-memory reduction.
-    if (M == 1 && act == 0 && nch <= 32 && N < 32 * 4 * num_sms) {
+    // route by shape alone (sized for GB300's 152 SMs), so that which kernel,
+    // and which summation order, serves a shape does not depend on the device
+    if (M == 1 && act == 0 && nch <= 32 && N < 32 * 4 * 152) {
         // warps per row group = chunks rounded up to a power of two (at most 8)
         const int wpg = nch > 4 ? 8 : nch > 2 ? 4 : nch;
         const int G = 8 / wpg;

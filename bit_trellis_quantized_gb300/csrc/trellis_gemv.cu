@@ -190,7 +190,11 @@ cudaError_t launch_trellis_gemv(const GemvArgs& a, int K, int nb, int items, int
     // per CTA the larger cluster reduction costs more than it saves. One
     // token per CTA plans for 4 resident CTAs per SM (5120 -> 6144 at one
     // token 20.4 -> 16.7 us; other shapes within 1%).
-    gemv_plan_clusters(a.in, items * (a.out / 128), num_sms, nb == 1 ? 4 : 2, nb == 1 ? 16 : 8, &b.kt_per_cta, &csize);
+    // The split is sized for GB300's 152 SMs whatever the device reports, so
+    // the order of the partial sums (and the result's bits) is a fixed
+    // function of the shape.
+    (void)num_sms;
+    gemv_plan_clusters(a.in, items * (a.out / 128), 152, nb == 1 ? 4 : 2, nb == 1 ? 16 : 8, &b.kt_per_cta, &csize);
     return K == 2 ? launch_nb<2>(b, nb, csize, items, s) : launch_nb<3>(b, nb, csize, items, s);
 }
 
