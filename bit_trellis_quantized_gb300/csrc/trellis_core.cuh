@@ -3,9 +3,9 @@
 // A CTA accumulates, for one 128-wide output block (8 tiles of 16 output
 // columns), the partial sums z[t][o] = sum_i W[i][o] * xt[t][i] over a range
 // of input-tile rows kt, with W decoded from the packed trellis codes in
-// registers and never stored (hipfire PR #694, summary "What it is": the
-// trellis is "decoded in the GEMV"; commit "The 2-bit model now executes with
-// the trellis code resident and decoded inside the GEMV").
+// registers and never stored (hipfire PR #694 "Escha-W2 port: 2-bit trellis
+// decoded in the GEMV", summary "What it is": the packed codes stay resident
+// and each weight is decoded where the matvec consumes it).
 //
 // Inner loop. Warp w walks the tile rows kt0 + w, kt0 + w + NW, ... One warp
 // load covers one tile row of the output block: 8 tiles x 16K words (512 B at
