@@ -61,28 +61,57 @@ GATE_UP_KERNEL_BYTES = (TOPK * (GU_CODE_BYTES + HIDDEN * 2 + 2 * INTER * 2) + HI
                         + TOPK * 2 * INTER * 4)
 
 
-# Routed weights decoded by one launch of the gate_up kernel at batch 1 and the
-# issue peak of the GPU (warp-instructions per second).
+# Routed weights decoded by one launch of the gate_up kernel at batch 1, by a
+# whole block (gate_up and down of 8 experts), and the issue peak of the GPU
+# (warp-instructions per second: 152 SMs x 4 schedulers x 1 per clock).
 GU_WEIGHTS = TOPK * HIDDEN * 2 * INTER
-ALU_OPS_PER_WEIGHT = 6
+BLOCK_WEIGHTS = TOPK * (HIDDEN * 2 * INTER + INTER * HIDDEN)
+ALU_OPS_PER_WEIGHT = 6  # the algorithm's minimum: window, hash multiply, and-xor, fp16 add, conversion, fma
 ALU_PEAK_WARP_INSTR = 152 * 4 * 2.07e9
+# Algorithmic bytes of the cooperative expert kernel of the batch-1 block: 8
+# experts' codes, rin and rout of both projections, the shared expert's int8
+# down rows and their scales, x, the logits, the shared gate_up outputs and
+# the f32 output.
+FUSED_KERNEL_BYTES = (TOPK * (GU_CODE_BYTES + DN_CODE_BYTES + (HIDDEN + 2 * INTER) * 2 + (INTER + HIDDEN) * 2)
+                      + HIDDEN * INTER + HIDDEN * 4 + HIDDEN * 2 + E * 2 + 2 * INTER * 4 + HIDDEN * 4)
+# Algorithmic bytes of one batch-1 block: 8 experts' codes, rin and rout of
+# both projections, the router weights, the int8 shared expert (weights, row
+# scales, gate vector), x in and the f32 output out.
+BLOCK_BYTES = (TOPK * (GU_CODE_BYTES + DN_CODE_BYTES + (HIDDEN + 2 * INTER) * 2 + (INTER + HIDDEN) * 2)
+               + E * HIDDEN * 2 + 3 * HIDDEN * INTER + (2 * INTER + HIDDEN) * 4 + HIDDEN * 2
+               + HIDDEN * 2 + HIDDEN * 4)
 
 
-def measured_traffic():
-    """DRAM bytes per launch of the gate_up kernel from the committed ncu
-    capture, or None when the kernel sources changed since the capture."""
+def _profile_record(name: str):
+    """A committed ncu figure (profiles/<name>.json), or None when the kernel
+    sources it depends on changed since the capture."""
     import hashlib
 
-    p = os.path.join(ROOT, "profiles", "traffic.json")
+    p = os.path.join(ROOT, "profiles", name + ".json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         rec = json.load(f)
     h = hashlib.sha256()
-    for name in rec["sources"]:
-        with open(os.path.join(ROOT, "bit_trellis_quantized_gb300", "csrc", name), "rb") as f:
+    for src in rec["sources"]:
+        with open(os.path.join(ROOT, "bit_trellis_quantized_gb300", "csrc", src), "rb") as f:
             h.update(f.read())
-    return rec["dram_bytes_per_launch"] if h.hexdigest() == rec["sources_sha256"] else None
+    return rec if h.hexdigest() == rec["sources_sha256"] else None
+
+
+def measured_traffic():
+    """DRAM bytes per launch of the batch-1 block's kernel from the committed
+    ncu capture, or None when the kernel sources changed since the capture."""
+    rec = _profile_record("traffic")
+    return rec["dram_bytes_per_launch"] if rec else None
+
+
+def measured_instr_per_weight():
+    """Executed warp-instructions x 32 per decoded weight of the batch-1
+    block's kernel (ncu smsp__inst_executed.sum over the launch, divided by
+    the weights it decodes), or None without a current capture."""
+    rec = _profile_record("traffic")
+    return rec.get("instructions_per_weight") if rec else None
 
 
 def peaks():
@@ -183,9 +212,68 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(loaded), "power_w_max": max(r[2] for r in rows)}
 
 
+def host_info():
+    """Core count and CPU model of the host the oracle runs on."""
+    import platform
+
+    model = platform.processor() or platform.machine()
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k = line.split(":")[0].strip().lower()
+                if k in ("model name", "cpu part", "hardware"):
+                    model = line.split(":", 1)[1].strip() if k == "model name" else f"{platform.machine()} {k} " + \
+                        line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return {"cpu_count": os.cpu_count(), "machine": platform.machine(), "cpu": model}
+
+
+def _oracle_tokens(args):
+    """Worker of the all-core leg: the oracle on a few tokens of the batch-1
+    block (its own process, one thread)."""
+    seed, x_seed, first, n = args
+    from oracle import escha_oracle as o
+
+    layer = o.MoeLayer(**gen.moe_layer(seed))
+    xs = gen.fp16_normal(gen.rng(x_seed), (first + n, HIDDEN))
+    for t in range(first, first + n):
+        o.moe_block(layer, xs[t:t + 1], k=TOPK)
+    return n
+
+
+def r_skip_rates(layer, xs, o):
+    """How often down_proj's 16-input strips are exactly zero on these tokens
+    (oracle values): before its input Hadamard (h = SwiGLU of gate_up, where
+    the gate/up prune mask zeroes channels) and after it (the x~ a tile-exact
+    skip would test)."""
+    pre = post = strips = 0
+    ids, w, _ = o.route(xs, layer.Wg, TOPK)
+    for b in range(xs.shape[0]):
+        xv = o.f16_to_f64(xs[b].view(np.uint16))
+        for j in range(TOPK):
+            e = int(ids[b, j])
+            y = o.trellis_gemv(None, xv, o.f16_to_f64(layer.gu_rin[e].view(np.uint16)),
+                               o.f16_to_f64(layer.gu_rout[e].view(np.uint16)), W=layer.expert_weights("gu", e))
+            h = o.swiglu(y)
+            xt = o.input_transform(h, o.f16_to_f64(layer.dn_rin[e].view(np.uint16)))
+            strips += h.size // 16
+            pre += int(np.sum(np.all(h.reshape(-1, 16) == 0, axis=1)))
+            post += int(np.sum(np.all(xt.reshape(-1, 16) == 0, axis=1)))
+    return {"tokens": int(xs.shape[0]), "strips": strips, "zero_strips_before_hadamard": pre,
+            "zero_strips_after_hadamard": post, "hit_rate": post / max(strips, 1),
+            "note": "16-input strips of down_proj's input whose values are all exactly 0 (oracle, float64): after "
+                    "the input Hadamard (what a tile-exact skip tests) and, for reference, before it"}
+
+
 def cpu_baseline(seconds: float = 15.0, max_tokens: int = 8):
     """The CPU oracle as it stands, on the host cores, over a bounded sample
-    of the same workload (whole tokens of the MoE block at batch 1)."""
+    of the same workload (whole tokens of the MoE block at batch 1): one
+    thread, then every core (one process per core, tokens split over them,
+    the same arithmetic)."""
+    import multiprocessing as mp
+
     from oracle import escha_oracle as o
 
     d = gen.moe_layer(LAYER_SEED)
@@ -199,9 +287,26 @@ def cpu_baseline(seconds: float = 15.0, max_tokens: int = 8):
         if time.perf_counter() - t0 > seconds:
             break
     dt = time.perf_counter() - t0
-    return {"value": n / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+    one = n / dt
+    info = host_info()
+    cores = max(1, int(info["cpu_count"] or 1))
+    # all cores: each process decodes its tokens' experts itself, as the
+    # one-thread leg does; 2 tokens per process
+    per = 2
+    jobs = [(LAYER_SEED, X_SEED + 999, i * per, per) for i in range(cores)]
+    ctx = mp.get_context("spawn")
+    t1 = time.perf_counter()
+    with ctx.Pool(cores) as pool:
+        done = sum(pool.map(_oracle_tokens, jobs))
+    dt_all = time.perf_counter() - t1
+    return {"value": one, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"{n} tokens of the batch-1 MoE block through the numpy float64 oracle, one thread, "
-                      f"{dt:.1f} s"}
+                      f"{dt:.1f} s",
+            "all_cores": {"value": done / dt_all, "unit": UNIT, "cores": cores,
+                          "sample": f"{done} tokens, {per} per process on {cores} processes (spawned, one thread "
+                                    f"each), {dt_all:.1f} s including process start-up"},
+            "host": info,
+            "r_skip": r_skip_rates(layer, xs[:min(n, 4)], o)}
 
 
 def run_reference(args, rank):
@@ -279,6 +384,7 @@ def run_ours(args, ws, rank, local):
     layer_seed, x_seed = replica_seeds(rank)
     blocks = [native.MoeBlock(moe_layer_device(layer_seed + l, dev), device=dev, topk=TOPK)
               for l in range(n_layers)]
+    path = blocks[0].path(1)
     n_total = args.warmup + args.steps
     xs_host = torch.from_numpy(gen.fp16_normal(gen.rng(x_seed), (n_total, HIDDEN))).pin_memory()
     xs = xs_host.to(dev)
@@ -426,10 +532,21 @@ def run_ours(args, ws, rank, local):
         return
 
     hbm, tflops, src = peaks()
-    ph = phase.mean(axis=0)  # router (+shared gate_up), gate_up, down (+shared down, combine) (ms)
-    gu_ms = float(ph[1])
-    gu_bytes = GATE_UP_KERNEL_BYTES
-    achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
+    ph = phase.mean(axis=0)  # per kernel (ms); the fused path records all of it in the first interval
+    fused = path == native.ESCHA_PATH_FUSED
+    if fused:
+        k_ms, k_bytes, k_weights = float(ph[1]), FUSED_KERNEL_BYTES, BLOCK_WEIGHTS
+        k_name = f"moe_fused_kernel<3,2> (top-k, {TOPK} experts' gate_up and down, the shared expert's down rows, " \
+                 f"combine; one cooperative grid)"
+        phase_ms = {"router+shared_gate_up": float(ph[0]), "fused_experts": float(ph[1])}
+    else:
+        k_ms, k_bytes, k_weights = float(ph[1]), GATE_UP_KERNEL_BYTES, GU_WEIGHTS
+        k_name = "moe_gate_up_kernel<K=3> (8 routed experts)"
+        phase_ms = {"router+shared_gate_up": float(ph[0]), "gate_up": float(ph[1]),
+                    "down+shared_down+combine": float(ph[2])}
+    achieved = k_bytes / (k_ms * 1e-3) / 1e9
+    ipw = measured_instr_per_weight() if fused else None
+    ops = ipw if ipw else ALU_OPS_PER_WEIGHT
     routed_code_bytes = TOPK * (GU_CODE_BYTES + DN_CODE_BYTES)
     distinct = len({tuple(r) for r in ids_all[args.warmup:args.warmup + 16].cpu().numpy().tolist()})
     line = {
@@ -444,28 +561,34 @@ def run_ours(args, ws, rank, local):
                    "cuda_graph": "none (direct launches)" if args.no_graph else
                                  f"up to {STEPS_PER_GRAPH} steps per graph (programmatic launches)",
                    "parallelism": f"replicas x{ws} (independent token streams)"},
-        # The dominant kernel (gate_up) is bound by instruction issue for the
-        # decode, not by HBM: its roofline is the issue peak (152 SMs x 4
-        # schedulers x 1 warp-instruction per clock at the maximum SM clock)
-        # against the algorithm's 6 operations per decoded weight and token
-        # (16-bit window, hash multiply, and-xor, fp16 add, conversion, f32
-        # fma). `traffic` is the kernel's measured DRAM bytes per launch.
-        "roofline": {"bound": "alu", "achieved": GU_WEIGHTS * ALU_OPS_PER_WEIGHT / 32 / (gu_ms * 1e-3) / 1e12,
+        # The dominant kernel is bound by instruction issue for the decode,
+        # not by HBM: its roofline is the issue peak (152 SMs x 4 schedulers
+        # x 1 warp-instruction per clock at the maximum SM clock) against the
+        # warp-instructions its decoded weights cost: the instructions per
+        # weight ncu counted on this kernel (smsp__inst_executed.sum over the
+        # launch / weights decoded; profiles/traffic.json), else the
+        # algorithm's 6 operations (16-bit window, hash multiply, and-xor,
+        # fp16 add, conversion, f32 fma). `traffic` is the kernel's measured
+        # DRAM bytes per launch.
+        "roofline": {"bound": "alu", "achieved": k_weights * ops / 32 / (k_ms * 1e-3) / 1e12,
                      "peak": ALU_PEAK_WARP_INSTR / 1e12, "unit": "T warp-instructions/s",
-                     "frac": GU_WEIGHTS * ALU_OPS_PER_WEIGHT / 32 / (gu_ms * 1e-3) / ALU_PEAK_WARP_INSTR,
-                     "traffic": measured_traffic(), "algorithmic_bytes_per_launch": gu_bytes,
-                     "kernel": "moe_gate_up_kernel<K=3> (8 routed experts)",
-                     "algorithmic_ops_per_launch": GU_WEIGHTS * ALU_OPS_PER_WEIGHT, "ms_per_launch": gu_ms,
-                     "peak_source": "derived: 152 SMs x 4 x 2.07e9 /s"},
+                     "frac": k_weights * ops / 32 / (k_ms * 1e-3) / ALU_PEAK_WARP_INSTR,
+                     "traffic": measured_traffic() if fused else None, "algorithmic_bytes_per_launch": k_bytes,
+                     "kernel": k_name, "decoded_weights_per_launch": k_weights,
+                     "instructions_per_weight": ops,
+                     "instructions_per_weight_source": "ncu smsp__inst_executed.sum / weights (profiles/traffic.json)"
+                     if ipw else "assumed: the algorithm's 6 operations per weight",
+                     "ms_per_launch": k_ms, "peak_source": "derived: 152 SMs x 4 x 2.07e9 /s"},
         # the same launch against the measured HBM copy bandwidth
         "roofline_hbm": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                         "traffic": measured_traffic(), "algorithmic_bytes_per_launch": gu_bytes,
-                         "ms_per_launch": gu_ms, "peak_source": src},
+                         "traffic": measured_traffic() if fused else None, "algorithmic_bytes_per_launch": k_bytes,
+                         "ms_per_launch": k_ms, "peak_source": src},
         "packed_expert_gbs": routed_code_bytes / (t_step * 1e-3) / 1e9,
         "packed_expert_frac": routed_code_bytes / (t_step * 1e-3) / 1e9 / hbm,
-        "phase_ms": {"router+shared_gate_up": float(ph[0]), "gate_up": float(ph[1]),
-                     "down+shared_down+combine": float(ph[2])},
-        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "phase_ms": phase_ms,
+        "block_path": {native.ESCHA_PATH_FUSED: "fused (one cooperative kernel)",
+                       native.ESCHA_PATH_SLOT: "per-slot (three kernels)"}.get(path, str(path)),
+        "gpu_launches": (2 if fused else KERNELS_PER_STEP) * args.steps,
         "e2e": {"value": aggregate_tokens_per_s(ws, t_e2e), "unit": UNIT, "h2d_bytes_per_step": HIDDEN * 2,
                 "d2h_bytes_per_step": HIDDEN * 4,
                 "note": f"per group of up to {STEPS_PER_GRAPH} steps, one graph: the steps, and on a copy stream "
@@ -484,10 +607,11 @@ def run_ours(args, ws, rank, local):
         pg.destroy_process_group()
 
 
-def _time_graph(torch, stream, fn, reps: int, warm: int = 3) -> float:
-    """ms per call of fn (captured once into a CUDA graph holding `reps`
-    calls; fn(i) issues call i), after warm-up replays; CUDA events on the
-    launching stream."""
+def _time_graph(torch, stream, fn, reps: int, warm: int = 3, replays: int = 20):
+    """ms per call of fn: the calls are captured once into a CUDA graph
+    holding `reps` calls (fn(i) issues call i), replayed `warm` times, then
+    `replays` times, each replay bracketed by CUDA events on the launching
+    stream. Returns (median, min, max) over the replays, in ms per call."""
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         fn(0)
@@ -498,12 +622,19 @@ def _time_graph(torch, stream, fn, reps: int, warm: int = 3) -> float:
         for _ in range(warm):
             g.replay()
         torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        g.replay()
-        b.record(stream)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(replays)]
+        for a, b in evs:
+            a.record(stream)
+            g.replay()
+            b.record(stream)
         torch.cuda.synchronize()
-    return a.elapsed_time(b) / reps
+    t = sorted(a.elapsed_time(b) / reps for a, b in evs)
+    return statistics.median(t), t[0], t[-1]
+
+
+def _stats(t):
+    """{median, min, max} in microseconds of a (median, min, max) in ms."""
+    return {"us_median": t[0] * 1e3, "us_min": t[1] * 1e3, "us_max": t[2] * 1e3}
 
 
 def extended(dev, blocks, hbm, tflops):
@@ -525,11 +656,12 @@ def extended(dev, blocks, hbm, tflops):
     P = 1024
     pj = projections_device(7001, dev, P)
     y = torch.empty((P, 1024), dtype=torch.float32, device=dev)
-    ms = _time_graph(torch, stream, lambda i: native.trellis_gemv(pj["codes"][i % P], pj["x"][i % P:i % P + 1],
-                                                                  pj["rin"][i % P], pj["rout"][i % P],
-                                                                  y=y[i % P:i % P + 1]), reps=P)
+    t = _time_graph(torch, stream, lambda i: native.trellis_gemv(pj["codes"][i % P], pj["x"][i % P:i % P + 1],
+                                                                 pj["rin"][i % P], pj["rout"][i % P],
+                                                                 y=y[i % P:i % P + 1]), reps=P)
+    ms = t[0]
     b = 2048 * 1024 * 2 // 8
-    res["single_projection_1024x2048_k2_b1"] = {"us": ms * 1e3, "packed_gbs": b / (ms * 1e-3) / 1e9,
+    res["single_projection_1024x2048_k2_b1"] = {"us": ms * 1e3, **_stats(t), "packed_gbs": b / (ms * 1e-3) / 1e9,
                                                "frac_of_hbm": b / (ms * 1e-3) / 1e9 / hbm,
                                                "l2": f"{P} distinct projections ({P * b >> 20} MB) cycled"}
     del pj, y
@@ -553,9 +685,10 @@ def extended(dev, blocks, hbm, tflops):
             x = torch.randn((M, n_in), device=dev).to(torch.float16)
             y = torch.empty((M, n_out), dtype=torch.float32, device=dev)
             ws = torch.empty(lins[0].workspace_bytes(M), dtype=torch.uint8, device=dev)
-            ms = _time_graph(torch, stream, lambda i: lins[i % nw](x, y=y, ws=ws), reps=nw)
+            t = _time_graph(torch, stream, lambda i: lins[i % nw](x, y=y, ws=ws), reps=nw)
+            ms = t[0]
             dn[f"{'nt' if nt_major else 'kt'}_major_m{M}"] = {
-                "us": ms * 1e3, "tokens_per_s": M / (ms * 1e-3), "packed_gbs": packed / (ms * 1e-3) / 1e9,
+                "us": ms * 1e3, **_stats(t), "tokens_per_s": M / (ms * 1e-3), "packed_gbs": packed / (ms * 1e-3) / 1e9,
                 "weight_fmas_per_s": float(M) * n_in * n_out / (ms * 1e-3)}
         del lins
     res["dense_linear_5120x17408_k2_bias"] = dn
@@ -572,8 +705,10 @@ def extended(dev, blocks, hbm, tflops):
         reps = nl if T <= 256 else 8
         xs = torch.randn((reps, T, HIDDEN), device=dev).to(torch.float16)
         out = torch.empty((T, HIDDEN), dtype=torch.float32, device=dev)
-        ms = _time_graph(torch, stream, lambda i: blocks[i % nl](xs[i], out=out, ws=ws), reps=reps)
-        mb[f"b{T}" if T < 2048 else "prefill_2048"] = {"tokens_per_s": T / (ms * 1e-3), "us_per_block": ms * 1e3}
+        t = _time_graph(torch, stream, lambda i: blocks[i % nl](xs[i], out=out, ws=ws), reps=reps)
+        ms = t[0]
+        mb[f"b{T}" if T < 2048 else "prefill_2048"] = {"tokens_per_s": T / (ms * 1e-3), "us_per_block": ms * 1e3,
+                                                       **_stats(t)}
         del ws, xs
     res["moe_block"] = mb
 
@@ -585,18 +720,22 @@ def extended(dev, blocks, hbm, tflops):
         s = torch.rand((copies, N), device=dev) * 9e-3 + 1e-3
         x1 = torch.randn((copies, 1, Kin), device=dev).to(torch.bfloat16)
         y1 = torch.empty((copies, 1, N), dtype=torch.float32, device=dev)
-        ms1 = _time_graph(torch, stream, lambda i: native.int8_w8a16_matvec(W[i % copies], s[i % copies],
-                                                                            x1[i % copies], y=y1[i % copies]),
-                          reps=max(copies, 8))
+        t1 = _time_graph(torch, stream, lambda i: native.int8_w8a16_matvec(W[i % copies], s[i % copies],
+                                                                           x1[i % copies], y=y1[i % copies]),
+                         reps=max(copies, 8))
+        ms1 = t1[0]
         M = 2048
         xm = torch.randn((M, Kin), device=dev).to(torch.bfloat16)
         ym = torch.empty((M, N), dtype=torch.float32, device=dev)
-        ms2 = _time_graph(torch, stream, lambda i: native.int8_w8a16_matvec(W[i % copies], s[i % copies], xm, y=ym),
-                          reps=4)
+        t2 = _time_graph(torch, stream, lambda i: native.int8_w8a16_matvec(W[i % copies], s[i % copies], xm, y=ym),
+                         reps=4)
+        ms2 = t2[0]
         gbs = N * Kin / (ms1 * 1e-3) / 1e9
         tf = 2.0 * M * N * Kin / (ms2 * 1e-3) / 1e12
-        i8[f"{N}x{Kin}"] = {"m1_us": ms1 * 1e3, "m1_gbs": gbs, "m1_frac_of_hbm": gbs / hbm,
-                            "m2048_us": ms2 * 1e3, "m2048_tflops": tf, "m2048_frac_of_bf16": tf / tflops}
+        i8[f"{N}x{Kin}"] = {"m1_us": ms1 * 1e3, "m1_us_min_max": [t1[1] * 1e3, t1[2] * 1e3], "m1_gbs": gbs,
+                            "m1_frac_of_hbm": gbs / hbm, "m2048_us": ms2 * 1e3,
+                            "m2048_us_min_max": [t2[1] * 1e3, t2[2] * 1e3], "m2048_tflops": tf,
+                            "m2048_frac_of_bf16": tf / tflops}
         del W, s, x1, y1, xm, ym
     res["int8_w8a16"] = i8
     torch.cuda.empty_cache()
@@ -614,8 +753,10 @@ def extended(dev, blocks, hbm, tflops):
         xb = torch.empty((T, HIDDEN), dtype=torch.float16, device=dev)
         ob = torch.empty((T, HIDDEN), dtype=torch.float32, device=dev)
         stack.workspace(T)
-        ms = _time_graph(torch, stream, lambda i: stack(h, xb, ob), reps=2 if T == 2048 else 4)
-        st[f"b{T}" if T < 2048 else "prefill_2048"] = {"tokens_per_s": T / (ms * 1e-3), "ms_per_pass": ms}
+        t = _time_graph(torch, stream, lambda i: stack(h, xb, ob), reps=2 if T == 2048 else 4)
+        ms = t[0]
+        st[f"b{T}" if T < 2048 else "prefill_2048"] = {"tokens_per_s": T / (ms * 1e-3), "ms_per_pass": ms,
+                                                       "ms_per_pass_min_max": [t[1], t[2]]}
     res["stack_40_blocks"] = st
     del stack, sblocks
     torch.cuda.empty_cache()

@@ -145,6 +145,27 @@ __device__ __forceinline__ uint2 ldg_stream_v2(const void* p) {
     return r;
 }
 
+// Router dot products: acc += x.lo * w.lo, then acc += x.hi * w.hi, fp16
+// operands and an f32 accumulator, one rounding per step (the product of two
+// fp16 values is exact in f32, so this equals an f32 fma of the converted
+// operands). dot8_f16 takes 8 consecutive columns in order.
+__device__ __forceinline__ void fma2_f16(uint32_t x2, uint32_t w2, float& acc) {
+    asm("{\n\t.reg .f16 xl, xh, wl, wh;\n\t"
+        "mov.b32 {xl, xh}, %1;\n\t"
+        "mov.b32 {wl, wh}, %2;\n\t"
+        "fma.rn.f32.f16 %0, xl, wl, %0;\n\t"
+        "fma.rn.f32.f16 %0, xh, wh, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(x2), "r"(w2));
+}
+
+__device__ __forceinline__ void dot8_f16(const uint4& xv, const uint4& wv, float& acc) {
+    fma2_f16(xv.x, wv.x, acc);
+    fma2_f16(xv.y, wv.y, acc);
+    fma2_f16(xv.z, wv.z, acc);
+    fma2_f16(xv.w, wv.w, acc);
+}
+
 __device__ __forceinline__ float h2f_bits(uint16_t b) { return __half2float(__ushort_as_half(b)); }
 __device__ __forceinline__ float bf2f_bits(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
 

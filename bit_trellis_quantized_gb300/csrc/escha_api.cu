@@ -3,10 +3,13 @@
 // returned as ESCHA_E_* codes with a thread-local message.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <mutex>
 #include <string>
+#include <utility>
+#include <vector>
 
 #include "escha.h"
 #include "kernels.h"
@@ -73,6 +76,14 @@ int cuda_status(cudaError_t e, const char* what) {
 
 size_t align_up(size_t v) { return (v + 255) & ~size_t(255); }
 
+// Diagnostic settings (escha_debug_*): the route of one-token blocks (0 the
+// fused kernel where it applies, 1 always the three per-slot kernels, 2
+// always the fused kernel or an error) and the fused kernel's wait limit and
+// publish hook.
+std::atomic<int> g_moe_route_mode{0};
+std::atomic<long long> g_fz_wait_ns{2000000000ll};
+std::atomic<int> g_fz_skip_publish{0};
+
 int check_trellis(const uint16_t* codes, int in, int out, int K, int mult, const char* name) {
     if (!codes) return fail(ESCHA_E_ARG, "%s: codes is null", name);
     if (!aligned16(codes)) return fail(ESCHA_E_ALIGN, "%s: codes not 16-byte aligned", name);
@@ -134,7 +145,7 @@ cudaError_t int8_matmul(const int8_t* W, const float* scales, int N, int Kin, co
 bool int8_uses_gemm(int Kin, int M) { return M >= escha::kInt8GemmMinM && Kin % 128 == 0; }
 
 struct MoeWs {
-    size_t err, logits, ids, w, ygu, shgu, shgate, sh, d, grp, img, shimg, total;
+    size_t err, logits, ids, w, ygu, shgu, shgate, sh, d, grp, img, shimg, fz, total;
 };
 
 MoeWs moe_ws_layout(const escha_moe_layer* L, int T, bool force_grouped = false) {
@@ -167,6 +178,11 @@ MoeWs moe_ws_layout(const escha_moe_layer* L, int T, bool force_grouped = false)
     off += align_up(grouped ? g.img_bytes : 0);
     m.shimg = off;  // the shared expert runs beside the routed path, with its own scratch
     off += align_up(grouped ? g.shared_img_bytes : 0);
+    m.fz = off;  // one token: counters, split partials and finished experts of the fused kernel
+    if (T == 1 && !grouped) {
+        const escha::FusedPlan p = escha::fused_plan(L->hidden, L->inter, L->n_experts, L->topk, L->sh_inter);
+        off += align_up(p.ctr_bytes) + align_up(p.gu_part_bytes) + align_up(p.dn_part_bytes) + align_up(p.dres_bytes);
+    }
     m.total = off;
     return m;
 }
@@ -410,7 +426,72 @@ escha::MoeArgs moe_args(const escha_moe_layer* L, const uint16_t* x, int T, floa
         a.grp_img = reinterpret_cast<uint8_t*>(base + m.img);
         a.grp_img_rows = 2 * gp.pos_cap;
     }
+    if (T == 1) {
+        const escha::FusedPlan p = escha::fused_plan(L->hidden, L->inter, L->n_experts, L->topk, L->sh_inter);
+        size_t off = m.fz;
+        a.fz_ctr = reinterpret_cast<unsigned*>(base + off);
+        off += align_up(p.ctr_bytes);
+        a.fz_gu_part = reinterpret_cast<float*>(base + off);
+        off += align_up(p.gu_part_bytes);
+        a.fz_dn_part = reinterpret_cast<float*>(base + off);
+        off += align_up(p.dn_part_bytes);
+        a.fz_dres = reinterpret_cast<float*>(base + off);
+    }
+    a.fz_wait_ns = g_fz_wait_ns.load();
+    a.fz_skip_publish = g_fz_skip_publish.load();
     return a;
+}
+
+// Route of a one-token block: the fused single-kernel path when the shape
+// and the device allow it (and no diagnostic override forbids it).
+struct FusedRoute {
+    bool use;
+    escha::FusedPlan plan;
+};
+
+std::mutex g_fz_mu;
+struct FzFitKey {
+    int dev, gu_K, dn_K, grid, smem;
+};
+std::vector<std::pair<FzFitKey, bool>> g_fz_fits;
+
+int fused_route(const escha_moe_layer* L, int T, int sms, FusedRoute* out) {
+    out->use = false;
+    const int mode = g_moe_route_mode.load();
+    if (T != 1 || mode == 1) return ESCHA_OK;
+    const bool shape = escha::fused_shape_ok(L->hidden, L->inter, L->n_experts, L->topk, L->sh_inter);
+    if (!shape) {
+        if (mode == 2) return fail(ESCHA_E_SHAPE, "moe_block: the one-token fused kernel does not cover this layer");
+        return ESCHA_OK;
+    }
+    out->plan = escha::fused_plan(L->hidden, L->inter, L->n_experts, L->topk, L->sh_inter);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(ESCHA_E_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    bool fits = false, known = false;
+    {
+        std::lock_guard<std::mutex> lk(g_fz_mu);
+        for (const auto& kv : g_fz_fits) {
+            const FzFitKey& k = kv.first;
+            if (k.dev == dev && k.gu_K == L->gu_K && k.dn_K == L->dn_K && k.grid == out->plan.grid &&
+                k.smem == out->plan.smem) {
+                fits = kv.second;
+                known = true;
+                break;
+            }
+        }
+    }
+    if (!known) {
+        e = escha::fused_fits(out->plan, L->gu_K, L->dn_K, sms, &fits);
+        if (e != cudaSuccess) return fail(ESCHA_E_CUDA, "fused kernel occupancy: %s", cudaGetErrorString(e));
+        std::lock_guard<std::mutex> lk(g_fz_mu);
+        g_fz_fits.push_back({FzFitKey{dev, L->gu_K, L->dn_K, out->plan.grid, out->plan.smem}, fits});
+    }
+    if (!fits && mode == 2)
+        return fail(ESCHA_E_SHAPE, "moe_block: the one-token fused grid (%d CTAs) cannot be resident at once",
+                    out->plan.grid);
+    out->use = fits;
+    return ESCHA_OK;
 }
 
 // Second stream and fork / join events of this host thread on a device, on
@@ -469,6 +550,24 @@ int moe_block_impl(const escha_moe_layer* L, const uint16_t* x, int T, float* ou
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char* base = static_cast<char*>(ws);
     escha::MoeArgs a = moe_args(L, x, T, out, ids_out, w_out, base, m);
+    FusedRoute fr{};
+    if ((r = fused_route(L, T, sms, &fr))) return r;
+    if (fr.use) {
+        if (rs) {  // the router and shared CTAs normalise; one CTA stores h += add
+            a.rs_h = rs->h;
+            a.rs_add = rs->add;
+            a.rs_eps = rs->eps;
+            a.x_norm = rs->x;
+        }
+        if ((r = record(ev, 0, s))) return r;
+        if ((r = cuda_status(escha::launch_moe_router(a, true, s), "router launch"))) return r;
+        if ((r = record(ev, 1, s))) return r;
+        if ((r = cuda_status(escha::launch_moe_fused(a, fr.plan, s), "fused experts launch"))) return r;
+        for (int i = 2; i < 4; ++i)
+            if ((r = record(ev, i, s))) return r;
+        return ESCHA_OK;
+    }
+    a.fz_ctr = nullptr;  // the per-slot kernels use no counters
     if (rs) {
         if (T <= escha::kFusedNormMaxT && L->hidden <= 2048) {
             // the router grid normalises; the gate_up grid stores h += add
@@ -554,6 +653,34 @@ int escha_moe_block_resid(const escha_moe_layer* L, float* h, const float* add, 
     }
     const ResidIn rs{h, add, eps, x};
     return moe_block_impl(L, x, T, out, ids_out, w_out, ws, ws_bytes, stream, nullptr, &rs);
+}
+
+int escha_moe_block_path(const escha_moe_layer* L, int T) {
+    int r = check_layer(L);
+    if (r) return r;
+    if (T < 1 || T > 8192) return fail(ESCHA_E_SHAPE, "moe_block_path: T=%d not in 1..8192", T);
+    if (T > escha::kSlotModeMaxT) return ESCHA_PATH_GROUPED;
+    int sms;
+    if ((r = device_check(&sms))) return r;
+    FusedRoute fr{};
+    if ((r = fused_route(L, T, sms, &fr))) return r;
+    return fr.use ? ESCHA_PATH_FUSED : ESCHA_PATH_SLOT;
+}
+
+int escha_debug_set_moe_route(int mode) {
+    if (mode < 0 || mode > 2) return fail(ESCHA_E_ARG, "debug_set_moe_route: mode=%d not in 0..2", mode);
+    g_moe_route_mode.store(mode);
+    return ESCHA_OK;
+}
+
+int escha_debug_set_fused_wait(long long wait_ns, int skip_publish) {
+    if (wait_ns < 1000 || wait_ns > 60000000000ll)
+        return fail(ESCHA_E_ARG, "debug_set_fused_wait: wait_ns=%lld not in [1e3, 6e10]", wait_ns);
+    if (skip_publish != 0 && skip_publish != 1)
+        return fail(ESCHA_E_ARG, "debug_set_fused_wait: skip_publish=%d must be 0 or 1", skip_publish);
+    g_fz_wait_ns.store(wait_ns);
+    g_fz_skip_publish.store(skip_publish);
+    return ESCHA_OK;
 }
 
 int escha_moe_block_timed(const escha_moe_layer* L, const uint16_t* x, int T, float* out, int32_t* ids_out,

@@ -113,6 +113,15 @@ struct MoeArgs {
     int* grp_ppos;      // [T*topk]: padded position of each slot
     uint8_t* grp_img;   // B image: [in/64 chunks][grp_img_rows][128 B]
     int grp_img_rows;   // 2 * padded positions
+    // single-token fused kernel (moe_fused.cu): counters (zeroed by the
+    // kernel itself before a grid barrier), split-K partial sums and the
+    // finished experts' down outputs, all in the workspace
+    unsigned* fz_ctr;   // kFzCtrWords words, zeroed by the router kernel (null: not the fused path)
+    float* fz_gu_part;  // [topk][2*inter/128][gu_csize][128]
+    float* fz_dn_part;  // [hidden/128][topk][dn_ksplit][128]
+    float* fz_dres;     // unused (the finishing CTA keeps the experts' outputs in shared memory)
+    long long fz_wait_ns;   // a wait on another CTA gives up after this long
+    int fz_skip_publish;    // test hook: the gate_up outputs are never published, so every wait on them gives up
 };
 
 // Largest token count of a grouped work item, and the largest batch that
@@ -178,6 +187,35 @@ cudaError_t launch_residual_rmsnorm(float* h, const float* add, int T, int hidde
 // expert's gate_up rows and gate
 cudaError_t launch_moe_router(const MoeArgs& a, bool with_shared, cudaStream_t s);
 cudaError_t launch_moe_gate_up(const MoeArgs& a, int num_sms, cudaStream_t s);
+
+// One token, two kernels: the per-slot router kernel (logits, the shared
+// expert's gate_up rows and gate; it also zeroes the counters below), then
+// one cooperative grid for everything else (top-k, gate_up, down, shared
+// expert down rows, combine) whose CTAs hand work to each other through
+// counters in the workspace (bounded waits). Same splits and summation
+// orders as the three per-slot kernels, so the same bits.
+// fused_fits: the shape is one the kernel covers (hidden <= 2048, shared
+// expert inter <= 512) and its grid fits on the device at once.
+constexpr int kFzCtrWords = 320;
+struct FusedPlan {
+    int n_gate_up, n_extra, n_down, grid, smem;
+    size_t ctr_bytes, gu_part_bytes, dn_part_bytes, dres_bytes;
+};
+bool fused_shape_ok(int hidden, int inter, int E, int topk, int sh_inter);
+FusedPlan fused_plan(int hidden, int inter, int E, int topk, int sh_inter);
+// cudaSuccess and *fits = false when the grid cannot be resident at once
+cudaError_t fused_fits(const FusedPlan& p, int gu_K, int dn_K, int num_sms, bool* fits);
+cudaError_t launch_moe_fused(const MoeArgs& a, const FusedPlan& p, cudaStream_t s);
+
+// Input splits of the per-slot path for T tokens: gate_up CTAs per output
+// block (gu_csize, each over gu_kt_per_cta tile rows) and down splits per
+// expert (dn_ksplit). A fixed function of the shape, so a result does not
+// depend on the device; the single-token fused kernel takes the same splits
+// and so gives the same bits.
+struct SlotPlan {
+    int gu_csize, gu_kt_per_cta, dn_ksplit;
+};
+SlotPlan slot_plan(int T, int hidden, int inter, int topk);
 cudaError_t launch_moe_down(const MoeArgs& a, int num_sms, cudaStream_t s);
 
 }  // namespace escha

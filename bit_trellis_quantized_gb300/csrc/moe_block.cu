@@ -49,26 +49,6 @@ constexpr int kWaveSms = 152;
 // partials are combined by the xor butterfly (offsets 16, 8, 4, 2, 1) and
 // rounded to f16 (RNE).
 // ---------------------------------------------------------------------------
-// acc += x.lo * w.lo, then acc += x.hi * w.hi: fp16 operands, f32 accumulator,
-// one rounding per step (the product of two fp16 values is exact in f32, so
-// this equals an f32 fma of the converted operands).
-__device__ __forceinline__ void fma2_f16(uint32_t x2, uint32_t w2, float& acc) {
-    asm("{\n\t.reg .f16 xl, xh, wl, wh;\n\t"
-        "mov.b32 {xl, xh}, %1;\n\t"
-        "mov.b32 {wl, wh}, %2;\n\t"
-        "fma.rn.f32.f16 %0, xl, wl, %0;\n\t"
-        "fma.rn.f32.f16 %0, xh, wh, %0;\n\t}"
-        : "+f"(acc)
-        : "r"(x2), "r"(w2));
-}
-
-__device__ __forceinline__ void dot8_f16(const uint4& xv, const uint4& wv, float& acc) {
-    fma2_f16(xv.x, wv.x, acc);
-    fma2_f16(xv.y, wv.y, acc);
-    fma2_f16(xv.z, wv.z, acc);
-    fma2_f16(xv.w, wv.w, acc);
-}
-
 // Residual norm of tokens t0 .. t0+nt-1 (nt <= NT) by one CTA of 128 threads,
 // hidden <= 2048: x = f16_rne(v * inv) with v = h + add, into xh (fp16,
 // [nt][hidden], shared memory), in exactly the arithmetic of
@@ -163,7 +143,12 @@ __device__ void router_logits(const MoeArgs& a, int warp, int lane, uint16_t* xh
             // the first weights are in flight; x (and the workspace, which the
             // previous call's kernels may still read) only after the wait
             pdl_wait();
-            if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *a.err = 0;  // the previous call has finished
+            if (blockIdx.x == 0 && blockIdx.y == 0) {  // the previous call has finished
+                if (threadIdx.x == 0) *a.err = 0;
+                // one token on the fused path: the expert kernel's counters start at zero
+                if (a.fz_ctr)
+                    for (int i = threadIdx.x; i < kFzCtrWords; i += kK0Threads) a.fz_ctr[i] = 0u;
+            }
             if constexpr (FUSED) {
                 resid_norm_cta<kFusedNormMaxT>(a, t0, nt, xh);
                 if (blockIdx.x == 0) {
@@ -1019,25 +1004,9 @@ cudaError_t launch_gate_up(MoeArgs a, int num_sms, cudaStream_t s) {
     (void)num_sms;  // splits are sized for kWaveSms
     const int oblks = 2 * a.inter / 128;
     const int slots = a.T * a.topk;
-    const int kblks = a.hidden / 128;
-    // Largest input split (CTAs per cluster, <= 8) for which the routed CTAs
-    // fit in one wave of 4 CTAs per SM; when only an unsplit grid fits, a
-    // split of two is still taken while it needs at most 1.3 waves (measured
-    // on GB300 for the 35B layer with 3 CTAs per SM: 4 tokens 61 -> 56 us per
-    // block; 5 tokens, 1.5 waves, is slower split). Four CTAs per SM instead
-    // of three: 1 token 23.7 -> 21.5 us per block, 2 tokens 35.8 -> 31.1 us,
-    // 4 to 16 tokens unchanged.
-    auto ctas = [&](int cs) { return (long long)cs * oblks * slots; };
-    int csize = 1;
-    for (int c = 1; c <= 8 && c <= kblks; ++c) {
-        const int per = (kblks + c - 1) / c;
-        const int cs = (kblks + per - 1) / per;
-        if (ctas(cs) <= 4LL * kWaveSms) csize = cs;
-    }
-    if (csize == 1 && kblks >= 2 && 10 * ctas(2) <= 13LL * 4 * kWaveSms) csize = 2;
-    const int per = (kblks + csize - 1) / csize;
-    csize = (kblks + per - 1) / per;
-    a.gu_kt_per_cta = per * 8;
+    const SlotPlan sp = slot_plan(a.T, a.hidden, a.inter, a.topk);
+    const int csize = sp.gu_csize;
+    a.gu_kt_per_cta = sp.gu_kt_per_cta;
     const int smem = (kMaxCluster * 128 + a.gu_kt_per_cta * 16 + (kGuWarps + 1) * 128) * 4;
     const void* f = reinterpret_cast<const void*>(moe_gate_up_kernel<K>);
     cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -1048,13 +1017,7 @@ cudaError_t launch_gate_up(MoeArgs a, int num_sms, cudaStream_t s) {
 template <int K>
 cudaError_t launch_down(MoeArgs a, int num_sms, cudaStream_t s) {
     (void)num_sms;  // splits are sized for kWaveSms
-    // Split each expert's input in two when it spans an even number (>= 2)
-    // of Hadamard blocks, the cluster stays within 16 CTAs and the split grid
-    // still fits one wave of 3 CTAs per SM (one token for the 35B layer;
-    // from 2 tokens on the unsplit grid was measured faster on GB300, e.g. 8
-    // tokens 109 -> 92 us per block).
-    const long long split_ctas = 2LL * a.topk * (a.hidden / 128) * a.T;
-    a.dn_ksplit = ((a.inter / 128) % 2 == 0 && 2 * a.topk <= kMaxCluster && split_ctas <= 3LL * kWaveSms) ? 2 : 1;
+    a.dn_ksplit = slot_plan(a.T, a.hidden, a.inter, a.topk).dn_ksplit;
     const int csz = a.topk * a.dn_ksplit;
     a.dn_xt_floats = (a.inter / a.dn_ksplit + 31) / 32 * 32;
     // routed inputs of one rank, then the shared expert's inputs (swizzled
@@ -1078,6 +1041,39 @@ cudaError_t launch_down(MoeArgs a, int num_sms, cudaStream_t s) {
 }
 
 }  // namespace
+
+SlotPlan slot_plan(int T, int hidden, int inter, int topk) {
+    SlotPlan p{};
+    const int oblks = 2 * inter / 128;
+    const int slots = T * topk;
+    const int kblks = hidden / 128;
+    // gate_up: the largest input split (CTAs per cluster, <= 8) for which the
+    // routed CTAs fit in one wave of 4 CTAs per SM; when only an unsplit grid
+    // fits, a split of two is still taken while it needs at most 1.3 waves
+    // (measured on GB300 for the 35B layer with 3 CTAs per SM: 4 tokens 61 ->
+    // 56 us per block; 5 tokens, 1.5 waves, is slower split). Four CTAs per
+    // SM instead of three: 1 token 23.7 -> 21.5 us per block, 2 tokens 35.8
+    // -> 31.1 us, 4 to 16 tokens unchanged.
+    auto ctas = [&](int cs) { return (long long)cs * oblks * slots; };
+    int csize = 1;
+    for (int c = 1; c <= 8 && c <= kblks; ++c) {
+        const int per = (kblks + c - 1) / c;
+        const int cs = (kblks + per - 1) / per;
+        if (ctas(cs) <= 4LL * kWaveSms) csize = cs;
+    }
+    if (csize == 1 && kblks >= 2 && 10 * ctas(2) <= 13LL * 4 * kWaveSms) csize = 2;
+    const int per = (kblks + csize - 1) / csize;
+    p.gu_csize = (kblks + per - 1) / per;
+    p.gu_kt_per_cta = per * 8;
+    // down: each expert's input split in two when it spans an even number
+    // (>= 2) of Hadamard blocks, the cluster stays within 16 CTAs and the
+    // split grid still fits one wave of 3 CTAs per SM (one token for the 35B
+    // layer; from 2 tokens on the unsplit grid was measured faster on GB300,
+    // e.g. 8 tokens 109 -> 92 us per block).
+    const long long split_ctas = 2LL * topk * (hidden / 128) * T;
+    p.dn_ksplit = ((inter / 128) % 2 == 0 && 2 * topk <= kMaxCluster && split_ctas <= 3LL * kWaveSms) ? 2 : 1;
+    return p;
+}
 
 cudaError_t launch_moe_router(const MoeArgs& a, bool with_shared, cudaStream_t s) {
     if (!with_shared && a.T >= kRtTok) {

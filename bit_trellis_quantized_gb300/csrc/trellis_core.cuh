@@ -69,17 +69,37 @@ __device__ __forceinline__ void load_lane_codes(LaneCodes<K>& lc, const uint16_t
     }
 }
 
-// Decode the lane's 64 weights and accumulate acc[t][q] += W[r][q] * xr[t][r]
-// over its 4 input rows. Half-row j (input row j/2, output columns
+// Decode the lane's 64 weights and accumulate into its 16 column sums per
+// token over its 4 input rows. Half-row j (input row j/2, output columns
 // 8*(j%2)..+7) starts at bit 8*K*j of the lane's words and its weight m at
 // bit 8*K*j + K*m; all offsets are compile-time constants.
 // K = 3 decodes weights in pairs (m, m+1); K = 2 takes columns m and m + 8 of
 // one input row from a single 32-bit stream window (cb_decode_window). Both
 // were measured faster on GB300 than one weight at a time (fewer
-// integer-pipe instructions); every accumulator still receives its weights
-// in the same order, so the sums are unchanged.
+// integer-pipe instructions). Each pair of weights meets the same input, so
+// for one token one packed fma.rn.f32x2 (__ffma2_rn: two independent f32
+// fmas, each rounded to nearest even) updates both column sums: acc2[t][i]
+// holds the sums of columns acc2_col<K>(i, 0) and acc2_col<K>(i, 1). Every
+// sum still receives its weights in the same order, with the same roundings.
+template <int K>
+__host__ __device__ constexpr int acc2_col(int i, int half) {
+    return K == 2 ? i + 8 * half : 2 * i + half;
+}
+
+// acc += w * (x, x): one packed fma for one token; for several tokens two
+// scalar fmas (the register pairs the packed form needs spill the 2- and
+// 4-token GEMV builds). Same results either way.
+template <int NB>
+__device__ __forceinline__ float2 fma_pair(float2 w, float x, float2 acc) {
+    if constexpr (NB == 1) {
+        return __ffma2_rn(w, make_float2(x, x), acc);
+    } else {
+        return make_float2(fmaf(w.x, x, acc.x), fmaf(w.y, x, acc.y));
+    }
+}
+
 template <int K, int NB>
-__device__ __forceinline__ void decode_fma(const LaneCodes<K>& lc, const float (&xr)[NB][4], float (&acc)[NB][16]) {
+__device__ __forceinline__ void decode_fma(const LaneCodes<K>& lc, const float (&xr)[NB][4], float2 (&acc2)[NB][8]) {
     if constexpr (K == 2) {  // weights (row r, col m) and (row r, col m + 8) share a window
         uint32_t q[5];
 #pragma unroll
@@ -88,12 +108,9 @@ __device__ __forceinline__ void decode_fma(const LaneCodes<K>& lc, const float (
             constexpr int r = decltype(I)::value / 8, m = decltype(I)::value % 8;
             __half ha, hb;
             cb_decode_window(bits32<2 * m>(q[r], q[r + 1]), ha, hb);
-            const float wa = __half2float(ha), wb = __half2float(hb);
+            const float2 w = make_float2(__half2float(ha), __half2float(hb));
 #pragma unroll
-            for (int t = 0; t < NB; ++t) {
-                acc[t][m] = fmaf(wa, xr[t][r], acc[t][m]);
-                acc[t][m + 8] = fmaf(wb, xr[t][r], acc[t][m + 8]);
-            }
+            for (int t = 0; t < NB; ++t) acc2[t][m] = fma_pair<NB>(w, xr[t][r], acc2[t][m]);
         });
         return;
     }
@@ -104,11 +121,9 @@ __device__ __forceinline__ void decode_fma(const LaneCodes<K>& lc, const float (
         const uint32_t s0 = window_state<(b0 & 15)>(stream_window<(b0 >> 4)>(lc.p));
         const uint32_t s1 = window_state<(b1 & 15)>(stream_window<(b1 >> 4)>(lc.p));
         const float2 w = __half22float2(cb_decode_h2(s0, s1));
+        constexpr int i = (8 * (j & 1) + m) / 2;  // columns 2i, 2i + 1
 #pragma unroll
-        for (int t = 0; t < NB; ++t) {
-            acc[t][8 * (j & 1) + m] = fmaf(w.x, xr[t][j >> 1], acc[t][8 * (j & 1) + m]);
-            acc[t][8 * (j & 1) + m + 1] = fmaf(w.y, xr[t][j >> 1], acc[t][8 * (j & 1) + m + 1]);
-        }
+        for (int t = 0; t < NB; ++t) acc2[t][i] = fma_pair<NB>(w, xr[t][j >> 1], acc2[t][i]);
     });
 }
 
@@ -126,11 +141,11 @@ __device__ __forceinline__ void cta_gemv_partial(const uint16_t* codes, const Ti
     const int lane = threadIdx.x & 31;
     const int c = lane & 3;
     const int nbr = (lane & ~3) | ((lane + 1) & 3);
-    float acc[NB][16];
+    float2 acc2[NB][8];
 #pragma unroll
     for (int t = 0; t < NB; ++t)
 #pragma unroll
-        for (int q = 0; q < 16; ++q) acc[t][q] = 0.f;
+        for (int i = 0; i < 8; ++i) acc2[t][i] = make_float2(0.f, 0.f);
 
     auto step = [&](LaneCodes<K>& lc, int kt) {
         lc.p[2 * K] = __shfl_sync(0xffffffffu, lc.p[0], nbr) & 0xFFFFu;
@@ -143,7 +158,7 @@ __device__ __forceinline__ void cta_gemv_partial(const uint16_t* codes, const Ti
             xr[t][2] = xv.z;
             xr[t][3] = xv.w;
         }
-        decode_fma<K, NB>(lc, xr, acc);
+        decode_fma<K, NB>(lc, xr, acc2);
     };
     // rows kt0 + warp + i*NW, two per iteration: `cur` and `nxt` take turns, so
     // the codes of the next row load while a row is decoded and are never
@@ -158,6 +173,15 @@ __device__ __forceinline__ void cta_gemv_partial(const uint16_t* codes, const Ti
         step(nxt, kt + NW);
     }
 
+    // column sums in column order
+    float acc[NB][16];
+#pragma unroll
+    for (int t = 0; t < NB; ++t)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            acc[t][acc2_col<K>(i, 0)] = acc2[t][i].x;
+            acc[t][acc2_col<K>(i, 1)] = acc2[t][i].y;
+        }
     // Reduce-scatter over the 4 lanes of a tile: lane c keeps output columns
     // 4c..4c+3 of tile lane/4.
 #pragma unroll
@@ -303,13 +327,14 @@ __device__ __forceinline__ void int8_rows_dot(const int8_t* w, long long ld, int
 // order-preserving unsigned 16-bit value (with -0 folded into +0, since the
 // two compare equal), above 0xFFFF - id. k rounds of a warp-wide max
 // (__reduce_max_sync) pick the keys. Lane j < k returns expert j and weight j.
-__device__ __forceinline__ void topk_softmax_warp(const uint16_t* logits, int E, int topk, int lane, int* e_out,
-                                                  float* w_out) {
+// bits[i] holds the f16 logit of expert lane + 32 i (ignored for experts >= E).
+__device__ __forceinline__ void topk_softmax_warp_bits(const uint16_t (&bits)[8], int E, int topk, int lane,
+                                                       int* e_out, float* w_out) {
     uint32_t key[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int e = lane + 32 * i;
-        uint32_t b = e < E ? logits[e] : 0u;
+        uint32_t b = e < E ? bits[i] : 0u;
         if (b == 0x8000u) b = 0u;
         const uint32_t ord = (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
         key[i] = e < E ? ((ord << 16) | (0xFFFFu - static_cast<uint32_t>(e))) : 0u;
@@ -325,8 +350,8 @@ __device__ __forceinline__ void topk_softmax_warp(const uint16_t* logits, int E,
         if (lane == k) mine = g;
     }
     const uint32_t ord = mine >> 16;
-    const uint32_t bits = (ord & 0x8000u) ? (ord & 0x7FFFu) : (~ord & 0xFFFFu);
-    const float lv = h2f_bits(static_cast<uint16_t>(bits));
+    const uint32_t lbits = (ord & 0x8000u) ? (ord & 0x7FFFu) : (~ord & 0xFFFFu);
+    const float lv = h2f_bits(static_cast<uint16_t>(lbits));
     const float top = __shfl_sync(0xffffffffu, lv, 0);
     float ex = lane < topk ? expf(lv - top) : 0.f;
     float den = ex;
@@ -334,6 +359,14 @@ __device__ __forceinline__ void topk_softmax_warp(const uint16_t* logits, int E,
     for (int m = 16; m >= 1; m >>= 1) den += __shfl_xor_sync(0xffffffffu, den, m);
     *e_out = static_cast<int>(0xFFFFu - (mine & 0xFFFFu));
     *w_out = ex / den;
+}
+
+__device__ __forceinline__ void topk_softmax_warp(const uint16_t* logits, int E, int topk, int lane, int* e_out,
+                                                  float* w_out) {
+    uint16_t bits[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) bits[i] = lane + 32 * i < E ? logits[lane + 32 * i] : 0;
+    topk_softmax_warp_bits(bits, E, topk, lane, e_out, w_out);
 }
 
 // ---------------------------------------------------------------------------

@@ -27,6 +27,10 @@ ESCHA_E_DEVICE = -7
 ESCHA_E_CKPT = -8
 ESCHA_E_IO = -9
 
+ESCHA_PATH_FUSED = 1
+ESCHA_PATH_SLOT = 2
+ESCHA_PATH_GROUPED = 3
+
 ESCHA_F16 = 1
 ESCHA_BF16 = 2
 ESCHA_F32 = 3
@@ -52,6 +56,9 @@ EXPORTS = [
     "escha_moe_block_timed",
     "escha_moe_block_resid",
     "escha_moe_block_noalloc",
+    "escha_moe_block_path",
+    "escha_debug_set_moe_route",
+    "escha_debug_set_fused_wait",
     "escha_moe_route_workspace",
     "escha_moe_route",
     "escha_residual_rmsnorm",
@@ -167,6 +174,12 @@ def lib() -> ctypes.CDLL:
         L.escha_moe_block_resid.restype = _i
         L.escha_moe_block_noalloc.argtypes = [ctypes.POINTER(EschaMoeLayer), _vp, _i, _vp, _vp, _vp, _vp]
         L.escha_moe_block_noalloc.restype = _i
+        L.escha_moe_block_path.argtypes = [ctypes.POINTER(EschaMoeLayer), _i]
+        L.escha_moe_block_path.restype = _i
+        L.escha_debug_set_moe_route.argtypes = [_i]
+        L.escha_debug_set_moe_route.restype = _i
+        L.escha_debug_set_fused_wait.argtypes = [ctypes.c_longlong, _i]
+        L.escha_debug_set_fused_wait.restype = _i
         L.escha_moe_route_workspace.argtypes = [ctypes.POINTER(EschaMoeLayer), _i]
         L.escha_moe_route_workspace.restype = _sz
         L.escha_moe_route.argtypes = [ctypes.POINTER(EschaMoeLayer), _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
@@ -182,6 +195,18 @@ def lib() -> ctypes.CDLL:
         L.int8_w8a16_dequant.restype = _i
         _LIB = L
     return _LIB
+
+
+def set_moe_route(mode: int) -> None:
+    """Diagnostic: 0 = one-token blocks run the fused single kernel where it
+    applies, 1 = always the three per-slot kernels, 2 = always the fused one."""
+    check(lib().escha_debug_set_moe_route(int(mode)))
+
+
+def set_fused_wait(wait_ns: int = 2_000_000_000, skip_publish: bool = False) -> None:
+    """Diagnostic: the fused kernel's wait bound, and the test hook that keeps
+    the routing unpublished so that every wait on it runs out."""
+    check(lib().escha_debug_set_fused_wait(int(wait_ns), int(bool(skip_publish))))
 
 
 class EschaError(RuntimeError):
@@ -524,6 +549,14 @@ class MoeBlock:
             L.sh_dn_w8, L.sh_dn_scale = ptr(t["sh_dn_w8"]), ptr(t["sh_dn_scale"])
             L.sh_gate = ptr(t["sh_gate"])
         return L
+
+    def path(self, T: int) -> int:
+        """ESCHA_PATH_FUSED, ESCHA_PATH_SLOT or ESCHA_PATH_GROUPED: the kernels a
+        call with T tokens runs on the current device."""
+        r = lib().escha_moe_block_path(ctypes.byref(self.layer), T)
+        if r < 0:
+            check(r)
+        return r
 
     def workspace(self, T: int) -> torch.Tensor:
         need = lib().escha_moe_block_workspace(ctypes.byref(self.layer), T)

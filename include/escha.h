@@ -268,8 +268,18 @@ typedef struct escha_moe_layer {
 
 /* The first 4 bytes of the workspace hold a status word that the call sets
  * to 0 when its first kernel starts and to a non-zero value if a kernel had
- * to give up waiting on a cluster peer (it then returns instead of hanging;
- * the outputs of that call are invalid). Read it after synchronising.
+ * to give up waiting on a cluster peer or, at one token, on another CTA of
+ * the fused kernel (it then returns instead of hanging; the outputs of that
+ * call are invalid). Read it after synchronising.
+ * One token (T = 1, the batch-1 decode step) runs, where the layer allows it
+ * (hidden <= 2048, shared-expert inter <= 512, and the grid fits on the
+ * device at once), as TWO kernels: the router kernel, then one cooperative
+ * kernel in which top-k, gate_up, down, the shared expert's down rows and the
+ * combine hand work to each other through counters kept in the workspace;
+ * the router kernel zeroes them, so nothing in the workspace has to start at
+ * zero. Its input splits and summation orders are those of the per-slot
+ * kernels, so the results are bit for bit the same. Calls that share a
+ * workspace must not overlap on the GPU (as for every path).
  * Larger batches (the grouped path) run the int8 shared expert on a second
  * stream beside the routed kernels: a non-blocking stream and two events per
  * host thread and device, created by the first such call made outside a
@@ -309,10 +319,37 @@ int escha_moe_block_resid(const escha_moe_layer* L, float* h, const float* add, 
  * before the router kernel (on up to 16 tokens it also computes the shared
  * expert's gate_up rows and gate), [1] after it, [2] after the routed gate_up
  * kernel, [3] after the down/combine kernel. Recording events between the kernels serialises them (no
- * programmatic overlap), so each interval is one kernel's duration. Same
+ * programmatic overlap), so each interval is one kernel's duration. When one
+ * token runs on the fused path, [0] is recorded before the router kernel,
+ * [1] after it, and [2] and [3] after the cooperative expert kernel. Same
  * results and errors as escha_moe_block. */
 int escha_moe_block_timed(const escha_moe_layer* L, const uint16_t* x, int T, float* out, int32_t* ids_out,
                           float* w_out, void* ws, size_t ws_bytes, void* stream, void* const* events);
+
+/* Which kernels escha_moe_block(L, T) runs on the current device (with the
+ * route setting below): ESCHA_PATH_FUSED (the router kernel and one
+ * cooperative expert kernel, T = 1),
+ * ESCHA_PATH_SLOT (router, gate_up and down/combine kernels per (token,
+ * expert), T <= 16) or ESCHA_PATH_GROUPED (tokens grouped by expert on the
+ * tensor cores, T > 16); a negative ESCHA_E_* code for an invalid layer. */
+#define ESCHA_PATH_FUSED 1
+#define ESCHA_PATH_SLOT 2
+#define ESCHA_PATH_GROUPED 3
+int escha_moe_block_path(const escha_moe_layer* L, int T);
+
+/* Diagnostic exports (tests and measurements; not part of the hot path).
+ * escha_debug_set_moe_route: how one-token blocks run in this process:
+ *   0 = the fused single kernel where it applies (default), 1 = always the
+ *   three per-slot kernels, 2 = always the fused kernel (ESCHA_E_SHAPE when
+ *   the layer or the device does not allow it). ESCHA_E_ARG for other modes.
+ * escha_debug_set_fused_wait: the fused kernel's bound on each wait for
+ *   another CTA (wait_ns in [1e3, 6e10], default 2e9) and, for tests, a hook
+ *   (skip_publish = 1) that keeps every expert's gate_up outputs from being
+ *   published, so every down unit's wait for them runs out: the kernel then
+ *   ends with the status word set to 5 instead of hanging. Both settings are
+ *   process-wide and read when a call is enqueued. */
+int escha_debug_set_moe_route(int mode);
+int escha_debug_set_fused_wait(long long wait_ns, int skip_publish);
 
 /* ---- MoE block with built-in scratch (no allocation by the caller) -------
  * The pages have no counterpart to this entry point; it exists for callers
