@@ -76,10 +76,10 @@ int cuda_status(cudaError_t e, const char* what) {
 
 size_t align_up(size_t v) { return (v + 255) & ~size_t(255); }
 
-// Diagnostic settings (escha_debug_*): the route of one-token blocks (0 the
-// fused kernel where it applies, 1 always the three per-slot kernels, 2
-// always the fused kernel or an error) and the fused kernel's wait limit and
-// publish hook.
+// Diagnostic settings (escha_debug_*): the route of one-token blocks (0 and
+// 1 the three per-slot kernels, measured faster for a single block; 2 the
+// router kernel plus the cooperative expert kernel, or an error where that
+// path does not apply) and the cooperative kernel's wait limit and test hook.
 std::atomic<int> g_moe_route_mode{0};
 std::atomic<long long> g_fz_wait_ns{2000000000ll};
 std::atomic<int> g_fz_skip_publish{0};
@@ -458,7 +458,7 @@ std::vector<std::pair<FzFitKey, bool>> g_fz_fits;
 int fused_route(const escha_moe_layer* L, int T, int sms, FusedRoute* out) {
     out->use = false;
     const int mode = g_moe_route_mode.load();
-    if (T != 1 || mode == 1) return ESCHA_OK;
+    if (T != 1 || mode != 2) return ESCHA_OK;
     const bool shape = escha::fused_shape_ok(L->hidden, L->inter, L->n_experts, L->topk, L->sh_inter);
     if (!shape) {
         if (mode == 2) return fail(ESCHA_E_SHAPE, "moe_block: the one-token fused kernel does not cover this layer");

@@ -271,14 +271,17 @@ typedef struct escha_moe_layer {
  * to give up waiting on a cluster peer or, at one token, on another CTA of
  * the fused kernel (it then returns instead of hanging; the outputs of that
  * call are invalid). Read it after synchronising.
- * One token (T = 1, the batch-1 decode step) runs, where the layer allows it
- * (hidden <= 2048, shared-expert inter <= 512, and the grid fits on the
- * device at once), as TWO kernels: the router kernel, then one cooperative
+ * One token can also run (escha_debug_set_moe_route(2); the layer must have
+ * hidden <= 2048 and shared-expert inter <= 512, and the grid must fit on the
+ * device at once) as TWO kernels: the router kernel, then one cooperative
  * kernel in which top-k, gate_up, down, the shared expert's down rows and the
  * combine hand work to each other through counters kept in the workspace;
  * the router kernel zeroes them, so nothing in the workspace has to start at
  * zero. Its input splits and summation orders are those of the per-slot
- * kernels, so the results are bit for bit the same. Calls that share a
+ * kernels, so the results are bit for bit the same. It is not the default:
+ * a cooperative grid is scheduled only when all of it fits, so it cannot
+ * overlap the kernels around it, and on GB300 a single block took 22.05 us
+ * this way against 21.4 us for the per-slot kernels. Calls that share a
  * workspace must not overlap on the GPU (as for every path).
  * Larger batches (the grouped path) run the int8 shared expert on a second
  * stream beside the routed kernels: a non-blocking stream and two events per
@@ -339,9 +342,9 @@ int escha_moe_block_path(const escha_moe_layer* L, int T);
 
 /* Diagnostic exports (tests and measurements; not part of the hot path).
  * escha_debug_set_moe_route: how one-token blocks run in this process:
- *   0 = the fused single kernel where it applies (default), 1 = always the
- *   three per-slot kernels, 2 = always the fused kernel (ESCHA_E_SHAPE when
- *   the layer or the device does not allow it). ESCHA_E_ARG for other modes.
+ *   0 (default) or 1 = the three per-slot kernels, 2 = the router kernel and
+ *   the cooperative expert kernel (ESCHA_E_SHAPE when the layer or the device
+ *   does not allow it). ESCHA_E_ARG for other modes.
  * escha_debug_set_fused_wait: the fused kernel's bound on each wait for
  *   another CTA (wait_ns in [1e3, 6e10], default 2e9) and, for tests, a hook
  *   (skip_publish = 1) that keeps every expert's gate_up outputs from being

@@ -83,13 +83,14 @@ def test_fused_bit_identical_to_per_slot_kernels(native, cfg):
 
 
 def test_fused_repeatable_and_default_route(native):
-    """The default route at one token is the fused kernel (it must agree
-    with the forced one bit for bit), and repeated calls on one workspace
-    give the same bits (the counters are re-zeroed by every call)."""
+    """The default route at one token (the per-slot kernels) agrees with the
+    fused one bit for bit, and repeated fused calls on one workspace give the
+    same bits (the counters are re-zeroed by every call)."""
     d = gen.moe_layer(1002)
     block = native.MoeBlock(d, topk=8)
     xs = dev(gen.fp16_normal(gen.rng(777), (3, 2048)))
     first = [_run(native, block, xs[t:t + 1], 2)[0] for t in range(3)]
+    assert block.path(1) == native.ESCHA_PATH_SLOT
     for t in range(3):
         out, _, _ = block(xs[t:t + 1])
         assert torch.equal(out, first[t])
