@@ -8,7 +8,8 @@ experts change). One step = one MoE block forward of one token: router
 (logits, top-8, softmax), input Hadamard transforms, fused trellis decode
 GEMVs for gate_up and down, output transforms, SwiGLU, the int8 shared expert
 and the combine, all in the library's kernels behind the C ABI, replayed from
-a CUDA graph.
+a CUDA graph of 8 steps, which run as one launch of the sequence kernel
+(escha_moe_blocks; --path per-slot: one escha_moe_block call per step).
 
 L2: inputs larger than L2. The benchmark cycles through 24 distinct layers of
 this shape (about 6.5 GB of weights), one layer per step, so a step's weights
@@ -384,7 +385,12 @@ def run_ours(args, ws, rank, local):
     layer_seed, x_seed = replica_seeds(rank)
     blocks = [native.MoeBlock(moe_layer_device(layer_seed + l, dev), device=dev, topk=TOPK)
               for l in range(n_layers)]
-    path = blocks[0].path(1)
+    # the steps of a graph run as one sequence launch (escha_moe_blocks: one
+    # cooperative kernel for up to 8 independent one-token blocks), or with
+    # --path per-slot as one escha_moe_block call (three kernels) per step
+    sequence = args.path == "sequence"
+    path = "sequence" if sequence else blocks[0].path(1)
+    seq_ws = torch.empty(native.seq_workspace_bytes(blocks[:STEPS_PER_GRAPH]), dtype=torch.uint8, device=dev)
     n_total = args.warmup + args.steps
     xs_host = torch.from_numpy(gen.fp16_normal(gen.rng(x_seed), (n_total, HIDDEN))).pin_memory()
     xs = xs_host.to(dev)
@@ -402,16 +408,27 @@ def run_ours(args, ws, rank, local):
     chunks = [(i0, STEPS_PER_GRAPH) for i0 in range(0, args.warmup, STEPS_PER_GRAPH)]
     chunks += [(i0, min(STEPS_PER_GRAPH, n_total - i0)) for i0 in range(args.warmup, n_total, STEPS_PER_GRAPH)]
     stream = torch.cuda.Stream(device=dev)
+
+    def run_chunk(i0, n):
+        """Steps i0 .. i0+n-1 on the current stream."""
+        if sequence:
+            idx = range(i0, i0 + n)
+            native.moe_blocks([blocks[layer_of[i]] for i in idx], [xs[i] for i in idx], [outs[i] for i in idx],
+                              ids=[ids_all[i] for i in idx], w=[w_all[i] for i in idx], ws=seq_ws)
+        else:
+            for i in range(i0, i0 + n):
+                blocks[layer_of[i]](xs[i:i + 1], out=outs[i:i + 1], ids=ids_all[i:i + 1], w=w_all[i:i + 1])
+
     graphs = []
     with torch.cuda.stream(stream):
         for blk in blocks:  # workspaces sized and kernels loaded before capture
             blk(xs[0:1], out=outs[0:1], ids=ids_all[0:1], w=w_all[0:1])
+        run_chunk(0, min(STEPS_PER_GRAPH, n_total))
         torch.cuda.synchronize()
         for i0, n in (chunks if not args.no_graph else []):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
-                for i in range(i0, i0 + n):
-                    blocks[layer_of[i]](xs[i:i + 1], out=outs[i:i + 1], ids=ids_all[i:i + 1], w=w_all[i:i + 1])
+                run_chunk(i0, n)
             graphs.append(g)
     torch.cuda.synchronize()
     n_warm_graphs = args.warmup // STEPS_PER_GRAPH
@@ -421,12 +438,12 @@ def run_ours(args, ws, rank, local):
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
             if args.no_graph:  # direct launches (for profilers)
-                for i in range(args.warmup):
-                    blocks[layer_of[i]](xs[i:i + 1], out=outs[i:i + 1], ids=ids_all[i:i + 1], w=w_all[i:i + 1])
+                for i0, n in chunks[:n_warm_graphs]:
+                    run_chunk(i0, n)
                 barrier()
                 t0.record(stream)
-                for i in range(args.warmup, n_total):
-                    blocks[layer_of[i]](xs[i:i + 1], out=outs[i:i + 1], ids=ids_all[i:i + 1], w=w_all[i:i + 1])
+                for i0, n in chunks[n_warm_graphs:]:
+                    run_chunk(i0, n)
                 t1.record(stream)
                 barrier()
             else:
@@ -472,8 +489,7 @@ def run_ours(args, ws, rank, local):
                 if gi > 0:
                     d2h(gi - 1)
                 join.record(copy_stream)
-            for i in range(i0, i0 + n):
-                blocks[layer_of[i]](xs[i:i + 1], out=outs[i:i + 1], ids=ids_all[i:i + 1], w=w_all[i:i + 1])
+            run_chunk(i0, n)
             stream.wait_event(join)
 
         e2e_graphs = []
@@ -503,25 +519,40 @@ def run_ours(args, ws, rank, local):
         del e2e_graphs
 
         # per-kernel durations, timed live by events on the launch stream
-        # around each kernel (the events serialise the three kernels)
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_total)]
-        with torch.cuda.stream(stream):
-            for row in evs:  # torch creates the CUDA events lazily, at their first record
-                for e in row:
-                    e.record(stream)
-            torch.cuda.synchronize()
-            handles = [(native.ctypes.c_void_p * 4)(*[e.cuda_event for e in row]) for row in evs]
-            barrier()
-            for i in range(n_total):
-                blk = blocks[layer_of[i]]
-                ws_t = blk.workspace(1)
-                native.check(native.lib().escha_moe_block_timed(
-                    native.ctypes.byref(blk.layer), native.ptr(xs[i:i + 1]), 1, native.ptr(outs[i:i + 1]),
-                    native.ptr(ids_all[i:i + 1]), native.ptr(w_all[i:i + 1]), native.ptr(ws_t), ws_t.numel(),
-                    stream.cuda_stream, handles[i]))
-            barrier()
-        phase = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(3)]
-                          for i in range(args.warmup, n_total)])
+        # around each kernel (the events serialise the kernels): the
+        # sequence kernel per launch of up to 8 steps, or the three per-slot
+        # kernels of each step
+        if sequence:
+            kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in chunks]
+            with torch.cuda.stream(stream):
+                barrier()
+                for (i0, n), (a, b) in zip(chunks, kev):
+                    a.record(stream)
+                    run_chunk(i0, n)
+                    b.record(stream)
+                barrier()
+            seq_launch = [(a.elapsed_time(b), n) for (i0, n), (a, b) in list(zip(chunks, kev))[n_warm_graphs:]]
+            phase = None
+        else:
+            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_total)]
+            with torch.cuda.stream(stream):
+                for row in evs:  # torch creates the CUDA events lazily, at their first record
+                    for e in row:
+                        e.record(stream)
+                torch.cuda.synchronize()
+                handles = [(native.ctypes.c_void_p * 4)(*[e.cuda_event for e in row]) for row in evs]
+                barrier()
+                for i in range(n_total):
+                    blk = blocks[layer_of[i]]
+                    ws_t = blk.workspace(1)
+                    native.check(native.lib().escha_moe_block_timed(
+                        native.ctypes.byref(blk.layer), native.ptr(xs[i:i + 1]), 1, native.ptr(outs[i:i + 1]),
+                        native.ptr(ids_all[i:i + 1]), native.ptr(w_all[i:i + 1]), native.ptr(ws_t), ws_t.numel(),
+                        stream.cuda_stream, handles[i]))
+                barrier()
+            phase = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(3)]
+                              for i in range(args.warmup, n_total)])
+        status = int(seq_ws[:4].view(torch.int32).item()) if sequence else 0
     clocks = clk.summary()
 
     # max over ranks
@@ -532,20 +563,31 @@ def run_ours(args, ws, rank, local):
         return
 
     hbm, tflops, src = peaks()
-    ph = phase.mean(axis=0)  # per kernel (ms); the fused path records all of it in the first interval
     fused = path == native.ESCHA_PATH_FUSED
-    if fused:
+    if sequence:
+        # the dominant kernel: the sequence kernel, per launch of n steps (n = 8
+        # but for a shorter last launch); its work scales with n
+        per_block = [ms / n for ms, n in seq_launch]
+        launch_ms = [ms for ms, n in seq_launch if n == STEPS_PER_GRAPH] or [ms for ms, n in seq_launch]
+        k_ms = float(np.mean(launch_ms))
+        k_bytes, k_weights = STEPS_PER_GRAPH * BLOCK_BYTES, STEPS_PER_GRAPH * BLOCK_WEIGHTS
+        k_name = (f"moe_multi_kernel ({STEPS_PER_GRAPH} independent one-token blocks per launch: router, top-k, "
+                  f"gate_up, down, shared expert, combine of each)")
+        phase_ms = {"sequence_kernel_per_launch": k_ms, "per_block": float(np.mean(per_block))}
+    elif fused:
+        ph = phase.mean(axis=0)
         k_ms, k_bytes, k_weights = float(ph[1]), FUSED_KERNEL_BYTES, BLOCK_WEIGHTS
         k_name = f"moe_fused_kernel<3,2> (top-k, {TOPK} experts' gate_up and down, the shared expert's down rows, " \
                  f"combine; one cooperative grid)"
         phase_ms = {"router+shared_gate_up": float(ph[0]), "fused_experts": float(ph[1])}
     else:
+        ph = phase.mean(axis=0)  # router (+shared gate_up), gate_up, down (+shared down, combine) (ms)
         k_ms, k_bytes, k_weights = float(ph[1]), GATE_UP_KERNEL_BYTES, GU_WEIGHTS
         k_name = "moe_gate_up_kernel<K=3> (8 routed experts)"
         phase_ms = {"router+shared_gate_up": float(ph[0]), "gate_up": float(ph[1]),
                     "down+shared_down+combine": float(ph[2])}
     achieved = k_bytes / (k_ms * 1e-3) / 1e9
-    ipw = measured_instr_per_weight() if fused else None
+    ipw = measured_instr_per_weight() if sequence else None
     ops = ipw if ipw else ALU_OPS_PER_WEIGHT
     routed_code_bytes = TOPK * (GU_CODE_BYTES + DN_CODE_BYTES)
     distinct = len({tuple(r) for r in ids_all[args.warmup:args.warmup + 16].cpu().numpy().tolist()})
@@ -558,8 +600,10 @@ def run_ours(args, ws, rank, local):
         "config": {"workload": WORKLOAD, "batch": 1, "tokens_per_step_per_gpu": 1,
                    "l2": f"inputs larger than L2: {n_layers} distinct MoE layers "
                          f"({n_layers * 272} MB) cycled, one per step, no flush",
-                   "cuda_graph": "none (direct launches)" if args.no_graph else
-                                 f"up to {STEPS_PER_GRAPH} steps per graph (programmatic launches)",
+                   "cuda_graph": ("none (direct launches)" if args.no_graph else
+                                  f"up to {STEPS_PER_GRAPH} steps per graph") +
+                                 (f"; the steps of a graph as one sequence launch (escha_moe_blocks)" if sequence else
+                                  "; one escha_moe_block call per step (programmatic launches)"),
                    "parallelism": f"replicas x{ws} (independent token streams)"},
         # The dominant kernel is bound by instruction issue for the decode,
         # not by HBM: its roofline is the issue peak (152 SMs x 4 schedulers
@@ -573,7 +617,7 @@ def run_ours(args, ws, rank, local):
         "roofline": {"bound": "alu", "achieved": k_weights * ops / 32 / (k_ms * 1e-3) / 1e12,
                      "peak": ALU_PEAK_WARP_INSTR / 1e12, "unit": "T warp-instructions/s",
                      "frac": k_weights * ops / 32 / (k_ms * 1e-3) / ALU_PEAK_WARP_INSTR,
-                     "traffic": measured_traffic() if fused else None, "algorithmic_bytes_per_launch": k_bytes,
+                     "traffic": measured_traffic() if sequence else None, "algorithmic_bytes_per_launch": k_bytes,
                      "kernel": k_name, "decoded_weights_per_launch": k_weights,
                      "instructions_per_weight": ops,
                      "instructions_per_weight_source": "ncu smsp__inst_executed.sum / weights (profiles/traffic.json)"
@@ -581,14 +625,16 @@ def run_ours(args, ws, rank, local):
                      "ms_per_launch": k_ms, "peak_source": "derived: 152 SMs x 4 x 2.07e9 /s"},
         # the same launch against the measured HBM copy bandwidth
         "roofline_hbm": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                         "traffic": measured_traffic() if fused else None, "algorithmic_bytes_per_launch": k_bytes,
+                         "traffic": measured_traffic() if sequence else None, "algorithmic_bytes_per_launch": k_bytes,
                          "ms_per_launch": k_ms, "peak_source": src},
         "packed_expert_gbs": routed_code_bytes / (t_step * 1e-3) / 1e9,
         "packed_expert_frac": routed_code_bytes / (t_step * 1e-3) / 1e9 / hbm,
         "phase_ms": phase_ms,
-        "block_path": {native.ESCHA_PATH_FUSED: "fused (one cooperative kernel)",
-                       native.ESCHA_PATH_SLOT: "per-slot (three kernels)"}.get(path, str(path)),
-        "gpu_launches": (2 if fused else KERNELS_PER_STEP) * args.steps,
+        "block_path": {"sequence": f"escha_moe_blocks: one cooperative launch per {STEPS_PER_GRAPH} steps",
+                       native.ESCHA_PATH_FUSED: "router kernel + cooperative expert kernel per step",
+                       native.ESCHA_PATH_SLOT: "per-slot (three kernels per step)"}.get(path, str(path)),
+        "status_word": status,
+        "gpu_launches": len(chunks[n_warm_graphs:]) if sequence else (2 if fused else KERNELS_PER_STEP) * args.steps,
         "e2e": {"value": aggregate_tokens_per_s(ws, t_e2e), "unit": UNIT, "h2d_bytes_per_step": HIDDEN * 2,
                 "d2h_bytes_per_step": HIDDEN * 4,
                 "note": f"per group of up to {STEPS_PER_GRAPH} steps, one graph: the steps, and on a copy stream "
@@ -695,10 +741,16 @@ def extended(dev, blocks, hbm, tflops):
     del codes
     torch.cuda.empty_cache()
 
-    # MoE block at batch 8 / 16 (per-slot path), 64 / 256 / 2048 (grouped path)
-    # over the headline's layers, fresh x per call
+    # MoE block at batch 1 through one escha_moe_block call per step (the
+    # three per-slot kernels; the headline runs 8 steps per sequence launch)
     nl = len(blocks)
     mb = {}
+    xs1 = torch.randn((nl, 1, HIDDEN), device=dev).to(torch.float16)
+    out1 = torch.empty((1, HIDDEN), dtype=torch.float32, device=dev)
+    t = _time_graph(torch, stream, lambda i: blocks[i % nl](xs1[i % nl], out=out1), reps=nl)
+    mb["b1_per_slot_calls"] = {"tokens_per_s": 1 / (t[0] * 1e-3), "us_per_block": t[0] * 1e3, **_stats(t)}
+    # MoE block at batch 8 / 16 (per-slot path), 64 / 256 / 2048 (grouped path)
+    # over the headline's layers, fresh x per call
     for T in (8, 16, 64, 256, 2048):
         ws = torch.empty(max(native.lib().escha_moe_block_workspace(native.ctypes.byref(blocks[0].layer), T), 256),
                          dtype=torch.uint8, device=dev)
@@ -747,13 +799,21 @@ def extended(dev, blocks, hbm, tflops):
         sblocks.append(native.MoeBlock(moe_layer_device(5000 + l, dev, k_gu=kg, k_dn=kd), device=dev))
     stack = native.MoeStack(sblocks)
     st = {}
-    for T in (1, 8, 128, 2048):
+    for T in ("1_sequence", 1, 8, 128, 2048):
+        seq = T == "1_sequence"
+        T = 1 if seq else T
         x0 = torch.randn((T, HIDDEN), device=dev)
         h = x0.clone()
         xb = torch.empty((T, HIDDEN), dtype=torch.float16, device=dev)
         ob = torch.empty((T, HIDDEN), dtype=torch.float32, device=dev)
         stack.workspace(T)
-        t = _time_graph(torch, stream, lambda i: stack(h, xb, ob), reps=2 if T == 2048 else 4)
+        t = _time_graph(torch, stream, lambda i: stack(h, xb, ob, sequence=seq), reps=2 if T == 2048 else 4)
+        if seq:
+            st["b1_one_launch"] = {"tokens_per_s": 1 / (t[0] * 1e-3), "ms_per_pass": t[0],
+                                   "ms_per_pass_min_max": [t[1], t[2]],
+                                   "note": "the 40 blocks as one escha_moe_stack launch (same bits as block by "
+                                           "block, b1)"}
+            continue
         ms = t[0]
         st[f"b{T}" if T < 2048 else "prefill_2048"] = {"tokens_per_s": T / (ms * 1e-3), "ms_per_pass": ms,
                                                        "ms_per_pass_min_max": [t[1], t[2]]}
@@ -824,6 +884,8 @@ def main():
                                                                "single projection, int8 shapes, 40-block stack)")
     ap.add_argument("--no-graph", action="store_true", help="launch the steps directly (for profilers)")
     ap.add_argument("--layers", type=int, default=N_LAYERS, help="distinct layers cycled through")
+    ap.add_argument("--path", default="sequence", choices=["sequence", "per-slot"],
+                    help="the steps of a graph as one sequence launch, or one block call (three kernels) per step")
     ap.add_argument("--profile-case", help="comma-separated workloads (" + ", ".join(PROFILE_CASES) +
                                            ") run with direct launches (for profilers), then exit")
     ap.add_argument("--reps", type=int, default=3, help="launches of --profile-case")

@@ -625,7 +625,252 @@ int moe_block_impl(const escha_moe_layer* L, const uint16_t* x, int T, float* ou
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// A sequence of one-token blocks in one cooperative launch (moe_multi.cu).
+// ---------------------------------------------------------------------------
+namespace {
+
+struct SeqWs {
+    size_t err, ctr, logits, ygu, shgu, shgate, sh, gu_part, dn_part, ids, w, total;
+};
+
+SeqWs seq_ws_layout(const escha::MbPlan& p) {
+    SeqWs w{};
+    size_t off = 0;
+    w.err = off;
+    off += 256;
+    w.ctr = off;
+    off += align_up(p.ctr_bytes);
+    w.logits = off;
+    off += align_up(p.logits_bytes);
+    w.ygu = off;
+    off += align_up(p.ygu_bytes);
+    w.shgu = off;
+    off += align_up(p.shgu_bytes);
+    w.shgate = off;
+    off += align_up(p.shgate_bytes);
+    w.sh = off;
+    off += align_up(p.sh_bytes);
+    w.gu_part = off;
+    off += align_up(p.gu_part_bytes);
+    w.dn_part = off;
+    off += align_up(p.dn_part_bytes);
+    w.ids = off;
+    off += align_up(p.ids_bytes);
+    w.w = off;
+    off += align_up(p.ids_bytes);
+    w.total = off;
+    return w;
+}
+
+// The layers of a sequence: each valid, all of one shape (K may differ per
+// layer and projection), a shape the sequence kernel covers.
+int seq_check(const escha_moe_layer* const* layers, int n, const char* name, escha::MbPlan* plan) {
+    if (!layers) return fail(ESCHA_E_ARG, "%s: layers is null", name);
+    if (n < 1 || n > escha::kMbMaxBlocks)
+        return fail(ESCHA_E_ARG, "%s: n_blocks=%d not in 1..%d", name, n, escha::kMbMaxBlocks);
+    for (int i = 0; i < n; ++i) {
+        int r = check_layer(layers[i]);
+        if (r) return r;
+        const escha_moe_layer* a = layers[0];
+        const escha_moe_layer* b = layers[i];
+        if (b->hidden != a->hidden || b->inter != a->inter || b->n_experts != a->n_experts || b->topk != a->topk ||
+            b->sh_inter != a->sh_inter)
+            return fail(ESCHA_E_SHAPE, "%s: layer %d differs in shape from layer 0", name, i);
+    }
+    const escha_moe_layer* L = layers[0];
+    if (!escha::multi_shape_ok(L->hidden, L->inter, L->n_experts, L->topk, L->sh_inter))
+        return fail(ESCHA_E_SHAPE,
+                    "%s: the sequence kernel covers hidden <= 2048 (a multiple of 256), 2*inter/128 <= 32 and a "
+                    "shared expert inter <= 512",
+                    name);
+    *plan = escha::multi_plan(n, L->hidden, L->inter, L->n_experts, L->topk, L->sh_inter);
+    return ESCHA_OK;
+}
+
+std::mutex g_seq_mu;
+int g_seq_grid[64][2];  // per device: smem the grid was sized for, CTAs (every SM slot)
+
+int seq_grid(int sms, int smem, int* grid) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(ESCHA_E_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64) return fail(ESCHA_E_DEVICE, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_seq_mu);
+    if (g_seq_grid[dev][1] == 0 || g_seq_grid[dev][0] != smem) {
+        int g = 0;
+        e = escha::multi_grid(sms, smem, &g);
+        if (e != cudaSuccess) return fail(ESCHA_E_CUDA, "sequence kernel occupancy: %s", cudaGetErrorString(e));
+        if (g < 1) return fail(ESCHA_E_DEVICE, "the sequence kernel cannot be resident on this device");
+        g_seq_grid[dev][0] = smem;
+        g_seq_grid[dev][1] = g;
+    }
+    *grid = g_seq_grid[dev][1];
+    return ESCHA_OK;
+}
+
+// The work queue of a sequence (escha::MbSeg): block after block for a
+// stack; a three-stage software pipeline for independent blocks.
+void seq_segments(escha::MbArgs& m, int n, const escha::MbPlan& p, bool stack) {
+    int ns = 0, pos = 0;
+    auto add = [&](int b, int first, int count) {
+        if (b < 0 || b >= n || count <= 0) return;
+        escha::MbSeg& s = m.seg[ns++];
+        s.block = static_cast<short>(b);
+        s.first = static_cast<short>(first);
+        s.count = static_cast<short>(count);
+        s.pos = pos;
+        pos += count;
+    };
+    const int rs = p.nR + p.nS, g0 = rs, d0 = rs + p.nG + p.nX;
+    if (stack) {
+        for (int b = 0; b < n; ++b) add(b, 0, p.U);
+    } else {
+        add(0, 0, rs);
+        add(1, 0, rs);
+        add(0, g0, p.nG + p.nX);
+        for (int b = 0; b < n; ++b) {
+            add(b + 2, 0, rs);
+            add(b + 1, g0, p.nG + p.nX);
+            add(b, d0, p.nD);
+        }
+    }
+    m.n_segs = ns;
+}
+
+escha::MbArgs seq_args(const escha_moe_layer* const* layers, int n, const escha::MbPlan& p, char* base,
+                       const SeqWs& w) {
+    escha::MbArgs m{};
+    escha::MbHead& h = m.h;
+    const escha_moe_layer* L = layers[0];
+    h.n_blocks = n;
+    h.hidden = L->hidden;
+    h.inter = L->inter;
+    h.E = L->n_experts;
+    h.topk = L->topk;
+    h.sh_inter = L->sh_inter;
+    h.ctr = reinterpret_cast<unsigned*>(base + w.ctr);
+    h.logits = reinterpret_cast<uint16_t*>(base + w.logits);
+    h.ygu = reinterpret_cast<float*>(base + w.ygu);
+    h.shgu = reinterpret_cast<float*>(base + w.shgu);
+    h.shgate = reinterpret_cast<float*>(base + w.shgate);
+    h.sh = reinterpret_cast<float*>(base + w.sh);
+    h.gu_part = reinterpret_cast<float*>(base + w.gu_part);
+    h.dn_part = reinterpret_cast<float*>(base + w.dn_part);
+    h.err = reinterpret_cast<int*>(base + w.err);
+    h.wait_ns = g_fz_wait_ns.load();
+    h.skip_publish = g_fz_skip_publish.load();
+    h.gu_csize = p.gu_csize;
+    h.gu_kt = p.gu_kt;
+    h.dn_ks = p.dn_ks;
+    h.nR = p.nR;
+    h.nS = p.nS;
+    h.nG = p.nG;
+    h.nX = p.nX;
+    h.nD = p.nD;
+    h.U = p.U;
+    h.xt_floats = p.xt_floats;
+    h.smem = p.smem;
+    for (int i = 0; i < n; ++i) {
+        const escha_moe_layer* li = layers[i];
+        escha::MbBlock& B = m.blk[i];
+        B.router_w = li->router_w;
+        B.gu_codes = li->gu_codes;
+        B.gu_rin = li->gu_rin;
+        B.gu_rout = li->gu_rout;
+        B.dn_codes = li->dn_codes;
+        B.dn_rin = li->dn_rin;
+        B.dn_rout = li->dn_rout;
+        B.sh_gu_w8 = li->sh_gu_w8;
+        B.sh_gu_scale = li->sh_gu_scale;
+        B.sh_dn_w8 = li->sh_dn_w8;
+        B.sh_dn_scale = li->sh_dn_scale;
+        B.sh_gate = li->sh_gate;
+        B.gu_K = li->gu_K;
+        B.dn_K = li->dn_K;
+        B.ids = reinterpret_cast<int32_t*>(base + w.ids) + (size_t)i * L->topk;
+        B.w = reinterpret_cast<float*>(base + w.w) + (size_t)i * L->topk;
+    }
+    return m;
+}
+
+}  // namespace
+
 extern "C" {
+
+size_t escha_moe_seq_workspace(const escha_moe_layer* const* layers, int n_blocks) {
+    if (!layers || n_blocks < 1 || n_blocks > escha::kMbMaxBlocks || !layers[0]) return 0;
+    const escha_moe_layer* L = layers[0];
+    if (L->topk < 1 || L->n_experts < 1) return 0;
+    return seq_ws_layout(escha::multi_plan(n_blocks, L->hidden, L->inter, L->n_experts, L->topk, L->sh_inter)).total;
+}
+
+int escha_moe_blocks(const escha_moe_layer* const* layers, int n_blocks, const uint16_t* const* x, float* const* out,
+                     int32_t* const* ids_out, float* const* w_out, void* ws, size_t ws_bytes, void* stream) {
+    escha::MbPlan p{};
+    int r = seq_check(layers, n_blocks, "moe_blocks", &p);
+    if (r) return r;
+    if (!x || !out) return fail(ESCHA_E_ARG, "moe_blocks: null x / out array");
+    for (int i = 0; i < n_blocks; ++i) {
+        if (!x[i] || !out[i]) return fail(ESCHA_E_ARG, "moe_blocks: null x / out of block %d", i);
+        if (!aligned16(x[i]) || !aligned16(out[i]) || (ids_out && ids_out[i] && (reinterpret_cast<uintptr_t>(ids_out[i]) & 3)) ||
+            (w_out && w_out[i] && (reinterpret_cast<uintptr_t>(w_out[i]) & 3)))
+            return fail(ESCHA_E_ALIGN, "moe_blocks: block %d: x / out not 16-byte or ids / w not 4-byte aligned", i);
+    }
+    const SeqWs w = seq_ws_layout(p);
+    if (!ws || ws_bytes < w.total) return fail(ESCHA_E_WORKSPACE, "moe_blocks: workspace %zu bytes, need %zu", ws_bytes, w.total);
+    if (!aligned16(ws)) return fail(ESCHA_E_ALIGN, "moe_blocks: workspace not 16-byte aligned");
+    int sms, grid;
+    if ((r = device_check(&sms))) return r;
+    if ((r = seq_grid(sms, p.smem, &grid))) return r;
+    escha::MbArgs m = seq_args(layers, n_blocks, p, static_cast<char*>(ws), w);
+    seq_segments(m, n_blocks, p, false);
+    for (int i = 0; i < n_blocks; ++i) {
+        m.blk[i].x = x[i];
+        m.blk[i].out = out[i];
+        if (ids_out && ids_out[i]) m.blk[i].ids = ids_out[i];
+        if (w_out && w_out[i]) m.blk[i].w = w_out[i];
+    }
+    return cuda_status(escha::launch_moe_multi(m, grid, static_cast<cudaStream_t>(stream)), "moe_blocks launch");
+}
+
+int escha_moe_stack(const escha_moe_layer* const* layers, int n_blocks, float* h, float eps, uint16_t* x_buf,
+                    float* out_buf, int32_t* ids_out, float* w_out, void* ws, size_t ws_bytes, void* stream) {
+    escha::MbPlan p{};
+    int r = seq_check(layers, n_blocks, "moe_stack", &p);
+    if (r) return r;
+    if (!h || !x_buf || !out_buf) return fail(ESCHA_E_ARG, "moe_stack: null h / x_buf / out_buf");
+    if (!(eps >= 0.f)) return fail(ESCHA_E_ARG, "moe_stack: eps must be >= 0");
+    if (!aligned16(h) || !aligned16(x_buf) || !aligned16(out_buf) || (reinterpret_cast<uintptr_t>(ids_out) & 3) ||
+        (reinterpret_cast<uintptr_t>(w_out) & 3))
+        return fail(ESCHA_E_ALIGN, "moe_stack: h / x_buf / out_buf not 16-byte or ids / w not 4-byte aligned");
+    const size_t H = layers[0]->hidden;
+    auto overlap = [](const void* a, size_t na, const void* b, size_t nb) {
+        const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+        return a0 < b0 + nb && b0 < a0 + na;
+    };
+    if (overlap(h, 4 * H, x_buf, 2 * H) || overlap(h, 4 * H, out_buf, 4 * H) || overlap(x_buf, 2 * H, out_buf, 4 * H))
+        return fail(ESCHA_E_ARG, "moe_stack: h, x_buf and out_buf must not overlap");
+    const SeqWs w = seq_ws_layout(p);
+    if (!ws || ws_bytes < w.total) return fail(ESCHA_E_WORKSPACE, "moe_stack: workspace %zu bytes, need %zu", ws_bytes, w.total);
+    if (!aligned16(ws)) return fail(ESCHA_E_ALIGN, "moe_stack: workspace not 16-byte aligned");
+    int sms, grid;
+    if ((r = device_check(&sms))) return r;
+    if ((r = seq_grid(sms, p.smem, &grid))) return r;
+    escha::MbArgs m = seq_args(layers, n_blocks, p, static_cast<char*>(ws), w);
+    seq_segments(m, n_blocks, p, true);
+    m.h.stack = 1;
+    m.h.res = h;
+    m.h.eps = eps;
+    m.h.xbuf = x_buf;
+    m.h.outbuf = out_buf;
+    const int k = layers[0]->topk;
+    for (int i = 0; i < n_blocks; ++i) {
+        if (ids_out) m.blk[i].ids = ids_out + (size_t)i * k;
+        if (w_out) m.blk[i].w = w_out + (size_t)i * k;
+    }
+    return cuda_status(escha::launch_moe_multi(m, grid, static_cast<cudaStream_t>(stream)), "moe_stack launch");
+}
 
 int escha_moe_block(const escha_moe_layer* L, const uint16_t* x, int T, float* out, int32_t* ids_out, float* w_out,
                     void* ws, size_t ws_bytes, void* stream) {

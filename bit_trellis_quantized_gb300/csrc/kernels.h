@@ -207,6 +207,82 @@ FusedPlan fused_plan(int hidden, int inter, int E, int topk, int sh_inter);
 cudaError_t fused_fits(const FusedPlan& p, int gu_K, int dn_K, int num_sms, bool* fits);
 cudaError_t launch_moe_fused(const MoeArgs& a, const FusedPlan& p, cudaStream_t s);
 
+// A sequence of one-token blocks in one cooperative launch (moe_multi.cu):
+// independent blocks (each its own input and output) or a residual stack
+// (h += previous output, x = RMSNorm(h), block; h += the last output).
+constexpr int kMbMaxBlocks = 48;
+constexpr int kMbCtrWords = 320;
+struct MbBlock {
+    const uint16_t* router_w;
+    const uint16_t* gu_codes;
+    const uint16_t* gu_rin;
+    const uint16_t* gu_rout;
+    const uint16_t* dn_codes;
+    const uint16_t* dn_rin;
+    const uint16_t* dn_rout;
+    const int8_t* sh_gu_w8;
+    const float* sh_gu_scale;
+    const int8_t* sh_dn_w8;
+    const float* sh_dn_scale;
+    const uint16_t* sh_gate;
+    int gu_K, dn_K;
+    const uint16_t* x;  // independent blocks: the input token (fp16 [hidden])
+    float* out;         // independent blocks: the output [hidden]
+    int32_t* ids;       // [topk]
+    float* w;           // [topk]
+};
+struct MbPlan {
+    int gu_csize, gu_kt, dn_ks;
+    int nR, nS, nG, nX, nD, U;  // work units per block: router, shared gate_up, gate_up, shared down, down
+    int xt_floats, smem;
+    size_t ctr_bytes, logits_bytes, ygu_bytes, shgu_bytes, shgate_bytes, sh_bytes, gu_part_bytes, dn_part_bytes,
+        ids_bytes;
+};
+struct MbHead {
+    int n_blocks, hidden, inter, E, topk, sh_inter;
+    int stack;       // 1: residual stack on res, xbuf, outbuf
+    float* res;      // [hidden] the residual stream h
+    float eps;
+    uint16_t* xbuf;  // [hidden] the current block's normalised input
+    float* outbuf;   // [hidden] the current block's output
+    unsigned* ctr;   // [n_blocks][kMbCtrWords], then the work queue
+    uint16_t* logits;
+    float* ygu;
+    float* shgu;
+    float* shgate;
+    float* sh;
+    float* gu_part;
+    float* dn_part;
+    int* err;
+    long long wait_ns;
+    int skip_publish;
+    int gu_csize, gu_kt, dn_ks;
+    int nR, nS, nG, nX, nD, U;
+    int xt_floats, smem;
+};
+// The work queue in segments: units [first, first + count) of block `block`,
+// segment after segment; `pos` = the queue position of the segment's first
+// unit.
+constexpr int kMbMaxSegs = 4 * kMbMaxBlocks + 4;
+struct MbSeg {
+    short block;
+    short first;
+    short count;
+    short pad;
+    int pos;
+};
+struct MbArgs {
+    MbHead h;
+    int n_segs;
+    MbSeg seg[kMbMaxSegs];
+    MbBlock blk[kMbMaxBlocks];
+};
+bool multi_shape_ok(int hidden, int inter, int E, int topk, int sh_inter);
+MbPlan multi_plan(int n_blocks, int hidden, int inter, int E, int topk, int sh_inter);
+// CTAs of the cooperative grid: every CTA slot of the device (smem bytes per CTA)
+cudaError_t multi_grid(int num_sms, int smem, int* grid);
+cudaError_t launch_moe_multi(const MbArgs& m, int grid, cudaStream_t s);
+
 // Input splits of the per-slot path for T tokens: gate_up CTAs per output
 // block (gu_csize, each over gu_kt_per_cta tile rows) and down splits per
 // expert (dn_ksplit). A fixed function of the shape, so a result does not

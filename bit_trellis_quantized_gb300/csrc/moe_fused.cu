@@ -40,6 +40,7 @@
 #include <atomic>
 #include <mutex>
 
+#include "coop.cuh"
 #include "kernels.h"
 #include "trellis_core.cuh"
 
@@ -70,49 +71,6 @@ struct FzGeo {
     int gu_csize, gu_kt, dn_ks;
     int xt_floats;
 };
-
-__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-// Arrival counts: the CTA's writes before the barrier that precedes the add
-// are released with it (acq_rel also acquires the other arrivals' writes,
-// for the CTA that turns out to be last); red: release only.
-__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
-    unsigned old;
-    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
-}
-__device__ __forceinline__ void red_add_release(unsigned* p, unsigned v) {
-    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ unsigned long long global_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// One thread: true once *p >= target; after wait_ns without it, sets *err and
-// returns false.
-__device__ bool wait_geq(const unsigned* p, unsigned target, long long wait_ns, int* err, int code) {
-    if (ld_acquire(p) >= target) return true;
-    const unsigned long long t0 = global_ns();
-    for (;;) {
-        if (ld_acquire(p) >= target) return true;
-        if (static_cast<long long>(global_ns() - t0) > wait_ns) {
-            atomicExch(err, code);
-            return false;
-        }
-    }
-}
-
-// The whole CTA: thread 0 waits, the others learn the outcome at the barrier.
-__device__ bool cta_wait_geq(const unsigned* p, unsigned target, const MoeArgs& a, int code) {
-    int ok = 1;
-    if (threadIdx.x == 0) ok = wait_geq(p, target, a.fz_wait_ns, a.err, code);
-    return __syncthreads_and(ok) != 0;
-}
 
 // The token's routing, by warp 0 from the router's f16 logits: experts and
 // weights of the slots into e_s / w_s (shared memory). Ends with the CTA
@@ -235,7 +193,7 @@ __device__ void fz_down(const MoeArgs& a, const FzGeo& g, int d, const int* e_s,
     uint2 rout_pre = make_uint2(0u, 0u);  // warp q: expert q's output scales of the block, in case this unit finishes it
     if (warp < a.topk)
         rout_pre = *reinterpret_cast<const uint2*>(a.dn_rout + (long long)e_s[warp] * a.hidden + ob * 128 + 4 * lane);
-    if (!cta_wait_geq(a.fz_ctr + kCtGuJ + j, static_cast<unsigned>(2 * a.inter / 128), a, kErrGuJ)) return;
+    if (!cta_wait_geq(a.fz_ctr + kCtGuJ + j, static_cast<unsigned>(2 * a.inter / 128), a.fz_wait_ns, a.err, kErrGuJ)) return;
 
     // xt = H128(rin_e * SwiGLU(ygu[j])) over this split's inputs
     const float* yr = a.ygu + (long long)j * 2 * a.inter;

@@ -56,6 +56,9 @@ EXPORTS = [
     "escha_moe_block_timed",
     "escha_moe_block_resid",
     "escha_moe_block_noalloc",
+    "escha_moe_seq_workspace",
+    "escha_moe_blocks",
+    "escha_moe_stack",
     "escha_moe_block_path",
     "escha_debug_set_moe_route",
     "escha_debug_set_fused_wait",
@@ -174,6 +177,14 @@ def lib() -> ctypes.CDLL:
         L.escha_moe_block_resid.restype = _i
         L.escha_moe_block_noalloc.argtypes = [ctypes.POINTER(EschaMoeLayer), _vp, _i, _vp, _vp, _vp, _vp]
         L.escha_moe_block_noalloc.restype = _i
+        _lp = ctypes.POINTER(ctypes.POINTER(EschaMoeLayer))
+        L.escha_moe_seq_workspace.argtypes = [_lp, _i]
+        L.escha_moe_seq_workspace.restype = _sz
+        L.escha_moe_blocks.argtypes = [_lp, _i, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
+                                       ctypes.POINTER(_vp), _vp, _sz, _vp]
+        L.escha_moe_blocks.restype = _i
+        L.escha_moe_stack.argtypes = [_lp, _i, _vp, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+        L.escha_moe_stack.restype = _i
         L.escha_moe_block_path.argtypes = [ctypes.POINTER(EschaMoeLayer), _i]
         L.escha_moe_block_path.restype = _i
         L.escha_debug_set_moe_route.argtypes = [_i]
@@ -626,6 +637,32 @@ class MoeBlock:
         return r
 
 
+def _layer_array(blocks):
+    arr = (ctypes.POINTER(EschaMoeLayer) * len(blocks))(*[ctypes.pointer(b.layer) for b in blocks])
+    return arr
+
+
+def seq_workspace_bytes(blocks) -> int:
+    return lib().escha_moe_seq_workspace(_layer_array(blocks), len(blocks))
+
+
+def moe_blocks(blocks, xs, outs, ids=None, w=None, ws=None, stream=None):
+    """Independent one-token blocks in one launch: block i of ``blocks``
+    (MoeBlock) on xs[i] (fp16 [hidden] or [1][hidden]) into outs[i] (f32).
+    ``ids`` / ``w``: optional lists of per-block [topk] tensors. ``ws``: a
+    workspace of at least seq_workspace_bytes(blocks) bytes."""
+    n = len(blocks)
+    _need_cuda(*xs, *outs)
+    if ws is None:
+        ws = torch.empty(seq_workspace_bytes(blocks), dtype=torch.uint8, device=xs[0].device)
+    px = (_vp * n)(*[ptr(t) for t in xs])
+    po = (_vp * n)(*[ptr(t) for t in outs])
+    pi = (_vp * n)(*[ptr(t) for t in ids]) if ids is not None else None
+    pw = (_vp * n)(*[ptr(t) for t in w]) if w is not None else None
+    check(lib().escha_moe_blocks(_layer_array(blocks), n, px, po, pi, pw, ptr(ws), ws.numel(), stream_handle(stream)))
+    return outs
+
+
 class MoeStack:
     """MoE blocks on an f32 residual stream h: for each block, x =
     fp16(RMSNorm(h)) (weightless), h += block(x); the add and the norm are
@@ -636,6 +673,7 @@ class MoeStack:
         self.blocks = list(blocks)
         self.eps = eps
         self._ws = None
+        self._seq_ws = None
 
     def workspace(self, T: int) -> torch.Tensor:
         need = max(lib().escha_moe_block_workspace(ctypes.byref(b.layer), T) for b in self.blocks)
@@ -643,14 +681,34 @@ class MoeStack:
             self._ws = torch.empty(max(need, 256), dtype=torch.uint8, device=self.blocks[0].t["router_w"].device)
         return self._ws
 
-    def __call__(self, h: torch.Tensor, x_buf=None, out_buf=None, stream=None, trace=None):
-        """Runs the stack on h (f32 [T][hidden], updated in place). With a list
-        ``trace``, appends (h before the block, x, block output) per block as
-        host copies (testing only: it synchronises)."""
+    def sequence_ok(self) -> bool:
+        """Whether one token runs the whole stack in one launch (escha_moe_stack)."""
+        b0 = self.blocks[0]
+        return (len(self.blocks) <= 48 and b0.hidden <= 2048 and b0.hidden % 256 == 0 and 2 * b0.inter // 128 <= 32
+                and b0.sh_inter <= 512
+                and all((b.hidden, b.inter, b.n_experts, b.topk, b.sh_inter)
+                        == (b0.hidden, b0.inter, b0.n_experts, b0.topk, b0.sh_inter) for b in self.blocks))
+
+    def __call__(self, h: torch.Tensor, x_buf=None, out_buf=None, stream=None, trace=None, sequence=False):
+        """Runs the stack on h (f32 [T][hidden], updated in place). With
+        ``sequence`` one token runs the whole stack in one launch
+        (escha_moe_stack; same bits) when the layers allow it; by default the
+        blocks run one call each (escha_moe_block_resid), measured faster for
+        a dependent stack on GB300. With a list ``trace``, appends (h before
+        the block, x, block output) per block as host copies (testing only: it
+        synchronises; block by block)."""
         _need_cuda(h)
         T, H = h.shape
         x = x_buf if x_buf is not None else torch.empty((T, H), dtype=torch.float16, device=h.device)
         out = out_buf if out_buf is not None else torch.empty((T, H), dtype=torch.float32, device=h.device)
+        if T == 1 and trace is None and sequence and self.sequence_ok():
+            need = seq_workspace_bytes(self.blocks)
+            if self._seq_ws is None or self._seq_ws.numel() < need:
+                self._seq_ws = torch.empty(need, dtype=torch.uint8, device=h.device)
+            check(lib().escha_moe_stack(_layer_array(self.blocks), len(self.blocks), ptr(h), float(self.eps), ptr(x),
+                                        ptr(out), None, None, ptr(self._seq_ws), self._seq_ws.numel(),
+                                        stream_handle(stream)))
+            return h
         ws = self.workspace(T)
         for i, b in enumerate(self.blocks):
             b.resid(h, out if i > 0 else None, x, self.eps, out=out, stream=stream, ws=ws)

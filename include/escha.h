@@ -329,6 +329,41 @@ int escha_moe_block_resid(const escha_moe_layer* L, float* h, const float* add, 
 int escha_moe_block_timed(const escha_moe_layer* L, const uint16_t* x, int T, float* out, int32_t* ids_out,
                           float* w_out, void* ws, size_t ws_bytes, void* stream, void* const* events);
 
+/* ---- a sequence of one-token blocks in one launch ---------------------
+ * The decode step of a model runs its MoE blocks one after another for one
+ * token. Launched one block at a time, each block pays its kernels' grid
+ * boundaries, which at one token cost more than the decode itself. These two
+ * calls run up to 48 blocks in ONE cooperative launch (every CTA resident):
+ * the CTAs take work units (router rows, the shared expert's rows, gate_up
+ * and down pieces of each routed expert) from one queue and hand results to
+ * each other through counters in the workspace; every wait is bounded (the
+ * status word reports a wait that ran out; see escha_debug_set_fused_wait).
+ * Every block gives bit for bit the outputs of escha_moe_block (per-slot
+ * kernels) on the same input. The layers must share hidden (a multiple of
+ * 256, <= 2048), inter (2*inter/128 <= 32), n_experts, topk and sh_inter
+ * (<= 512); gu_K / dn_K may differ per layer. ESCHA_E_SHAPE otherwise.
+ *
+ * escha_moe_blocks: independent blocks, block i on its own token:
+ *   x[i] fp16 [hidden] -> out[i] f32 [hidden]; ids_out / w_out: arrays of
+ *   per-block [topk] outputs, or NULL (either the array or an entry).
+ *   A block's router and gate_up work overlaps the previous block's down.
+ * escha_moe_stack: a residual stack, the blocks of one decode step:
+ *   for each block i: h += out_buf (i > 0), x_buf = fp16 RMSNorm(h) (the
+ *   weightless norm of escha_residual_rmsnorm, same arithmetic), out_buf =
+ *   block_i(x_buf); at the end h += out_buf. The same h, x_buf and out_buf
+ *   bits as escha_moe_block_resid per block followed by
+ *   escha_residual_rmsnorm(h, out_buf, x_out = NULL).
+ *   h f32 [hidden] (updated), x_buf fp16 [hidden], out_buf f32 [hidden]
+ *   (written; h, x_buf, out_buf must not overlap); ids_out int32 and w_out
+ *   f32 [n_blocks][topk] or NULL.
+ * Workspace: escha_moe_seq_workspace(layers, n_blocks) bytes (independent of
+ * the call's kind); nothing in it has to start at zero. */
+size_t escha_moe_seq_workspace(const escha_moe_layer* const* layers, int n_blocks);
+int escha_moe_blocks(const escha_moe_layer* const* layers, int n_blocks, const uint16_t* const* x, float* const* out,
+                     int32_t* const* ids_out, float* const* w_out, void* ws, size_t ws_bytes, void* stream);
+int escha_moe_stack(const escha_moe_layer* const* layers, int n_blocks, float* h, float eps, uint16_t* x_buf,
+                    float* out_buf, int32_t* ids_out, float* w_out, void* ws, size_t ws_bytes, void* stream);
+
 /* Which kernels escha_moe_block(L, T) runs on the current device (with the
  * route setting below): ESCHA_PATH_FUSED (the router kernel and one
  * cooperative expert kernel, T = 1),
