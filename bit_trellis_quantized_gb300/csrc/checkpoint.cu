@@ -333,15 +333,23 @@ int parse_shard(escha_ckpt* c, int si) {
         x.name = kv.first;
         x.dtype = dt->str;
         x.shard = si;
+        const int es = escha_ckpt_impl::dtype_size(x.dtype);
+        if (!es) return ck_fail(ESCHA_E_IO, "checkpoint: unknown dtype " + x.dtype + " of tensor " + kv.first);
+        // element count, checked against the shard's data size before every
+        // multiply, so a claimed shape cannot wrap around 64 bits
+        const unsigned long long max_n = dsize / static_cast<unsigned long long>(es);
         unsigned long long n = 1;
+        bool empty = false;
         for (const Json& d : sh->arr) {
             if (d.kind != Json::kNum || !d.is_int || d.inum < 0 || d.inum > (1ll << 40))
                 return ck_fail(ESCHA_E_IO, "checkpoint: bad shape of tensor " + kv.first);
             x.shape.push_back(d.inum);
-            n *= static_cast<unsigned long long>(d.inum);
+            const unsigned long long dim = static_cast<unsigned long long>(d.inum);
+            if (dim == 0) empty = true;
+            if (!empty && dim > 0 && n > max_n / dim)
+                return ck_fail(ESCHA_E_IO, "checkpoint: shape of tensor " + kv.first + " exceeds its shard's data");
+            n = empty ? 0 : n * dim;
         }
-        const int es = escha_ckpt_impl::dtype_size(x.dtype);
-        if (!es) return ck_fail(ESCHA_E_IO, "checkpoint: unknown dtype " + x.dtype + " of tensor " + kv.first);
         for (const Json& o : off->arr)
             if (o.kind != Json::kNum || !o.is_int || o.inum < 0)
                 return ck_fail(ESCHA_E_IO, "checkpoint: bad data_offsets of tensor " + kv.first);
@@ -461,7 +469,7 @@ int validate(escha_ckpt* c) {
         I.config_k = -1;
         if (I.has_config) {
             const Tensor& cf = *L.at("escha_config");
-            if (cf.dtype == "I32" && !cf.shape.empty() && cf.shape.back() == 9) {
+            if (cf.dtype == "I32" && !cf.shape.empty() && cf.shape.back() == 9 && cf.end - cf.begin >= 8) {
                 int32_t v[2] = {0, 0};
                 File f(fopen(c->shards[cf.shard].path.c_str(), "rb"));
                 if (f && fseek(f.get(), static_cast<long>(cf.begin), SEEK_SET) == 0 && fread(v, 4, 2, f.get()) == 2)
@@ -619,20 +627,17 @@ int escha_ckpt_load_projection(const escha_ckpt* c, int i, uint16_t* codes, uint
     int r;
     if (!nt_major) {
         if ((r = copy_to_device(c, *pj.code, codes, s))) return r;
-    } else {  // through a device scratch copy and the whole-tile transpose kernel
-        void* tmp = nullptr;
-        const size_t n = pj.code->end - pj.code->begin;
-        cudaError_t e = cudaMalloc(&tmp, n);
+    } else {  // whole tiles moved to the nt-major grid in host memory, then one copy (no device scratch)
+        const Tensor& t = *pj.code;
+        std::vector<unsigned char> src(t.end - t.begin), dst(t.end - t.begin);
+        if ((r = read_host(c, t, src.data()))) return r;
+        const size_t KT = pj.info.in / 16, NT = pj.info.out / 16, tile = 16 * 2 * static_cast<size_t>(pj.info.K);
+        for (size_t kt = 0; kt < KT; ++kt)
+            for (size_t nt = 0; nt < NT; ++nt)
+                memcpy(dst.data() + (nt * KT + kt) * tile, src.data() + (kt * NT + nt) * tile, tile);
+        cudaError_t e = cudaMemcpyAsync(codes, dst.data(), dst.size(), cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);  // the staging buffer goes out of scope
         if (e != cudaSuccess) return ck_fail(ESCHA_E_CUDA, std::string("ckpt_load_projection: ") + cudaGetErrorString(e));
-        r = copy_to_device(c, *pj.code, tmp, s);
-        if (!r) {
-            e = escha::launch_codes_to_nt_major(static_cast<const uint16_t*>(tmp), pj.info.in, pj.info.out, pj.info.K,
-                                                codes, s);
-            if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-            if (e != cudaSuccess) r = ck_fail(ESCHA_E_CUDA, std::string("ckpt_load_projection: ") + cudaGetErrorString(e));
-        }
-        cudaFree(tmp);
-        if (r) return r;
     }
     if ((r = copy_to_device(c, *pj.rin, rin, s))) return r;
     if ((r = copy_to_device(c, *pj.rout, rout, s))) return r;

@@ -1,6 +1,7 @@
 // C ABI of the trellis MoE library: argument validation, workspace layout and
 // kernel launches. Every check runs before anything is enqueued; errors are
 // returned as ESCHA_E_* codes with a thread-local message.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -1051,21 +1052,54 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[ESCHA_NOALLOC_S
 
 std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[64];
+unsigned long long g_noalloc_ctx[64];  // the context the address was looked up in
 
-// Device address of g_noalloc_scratch on the current device (looked up on the
-// first call for that device).
+// Unique id of the current context (0 if it cannot be read): the driver's
+// cuCtxGetCurrent / cuCtxGetId, reached through the runtime, so the library
+// needs no link against the driver library.
+unsigned long long current_context_id() {
+    typedef CUresult (*GetCurrent)(CUcontext*);
+    typedef CUresult (*GetId)(CUcontext, unsigned long long*);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrent>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetId>(f);
+        cudaGetLastError();
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of g_noalloc_scratch on the current device, looked up on the
+// first call for that device and again whenever the device's context has
+// changed since (after cudaDeviceReset the module is loaded anew and the
+// buffer can move).
 int noalloc_scratch(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail(ESCHA_E_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
     if (dev < 0 || dev >= 64) return fail(ESCHA_E_DEVICE, "device ordinal %d out of range", dev);
+    const unsigned long long ctx = current_context_id();  // 0 before the runtime has made a context current
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
+    if (!g_noalloc_ptr[dev] || ctx == 0 || ctx != g_noalloc_ctx[dev]) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess || !p)
             return fail(ESCHA_E_CUDA, "cudaGetSymbolAddress(built-in scratch): %s", cudaGetErrorString(e));
         g_noalloc_ptr[dev] = p;
+        g_noalloc_ctx[dev] = current_context_id();  // the lookup has made the device's context current
     }
     *out = g_noalloc_ptr[dev];
     return ESCHA_OK;

@@ -404,7 +404,9 @@ int escha_debug_set_fused_wait(long long wait_ns, int skip_publish);
  *     per-slot path, 731 KB at T = 16); the grouped path of T >= 17 needs
  *     several MB (its B image) and is rejected.
  *   - The first call on a device looks the buffer's device address up
- *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *     (cudaGetSymbolAddress), and so does the first call after the device's
+ *     context changed (cudaDeviceReset loads the library's module anew); make
+ *     such a call before any stream capture.
  *   - All calls on a device share the one buffer, which keeps the last call's
  *     contents: calls that can overlap on the GPU (different streams without
  *     ordering between them) race and corrupt each other's results. Nothing

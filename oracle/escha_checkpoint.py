@@ -160,7 +160,8 @@ def validate(paths):
         if "escha_config" in leaves:
             si, entry = leaves["escha_config"]
             if entry[0] == "I32" and len(entry[1]) >= 1 and entry[1][-1] == 9:
-                config_k = int(_array(raws[si], entry).reshape(-1)[1])
+                cfg = _array(raws[si], entry).reshape(-1)
+                config_k = int(cfg[1]) if cfg.size >= 2 else -1  # an empty config has no K to report
         has_bias = False
         if f"{prefix}.bias" in tensors:
             _, (bdt, bshape, _, _) = tensors[f"{prefix}.bias"]

@@ -148,6 +148,13 @@ def _cases(tmp_path):
                                             {"dtype": "F32", "shape": [128], "data_offsets": [0, 100]}})
     variant("unknown_dtype", header_override={"model.layers.0.mlp.down_proj.bias":
                                               {"dtype": "Q4", "shape": [128], "data_offsets": [0, 512]}})
+    # a shape whose element count wraps around 64 bits (2^33 * 2^31 * 4 bytes)
+    # over an empty byte range must not pass as an empty tensor
+    variant("wrapping_shape", header_override={"model.layers.0.mlp.down_proj.bias":
+                                               {"dtype": "F32", "shape": [2 ** 33, 2 ** 31], "data_offsets": [0, 0]}})
+    # an empty escha_config: reported as absent K, nothing read past it
+    variant("empty_config", lambda t: t.update({"model.layers.0.mlp.down_proj.escha_config":
+                                                np.zeros((0, 9), np.int32)}))
     bad = tmp_path / "not_json.safetensors"
     bad.write_bytes(struct.pack("<Q", 8) + b"{not js}")
     out.append(("not_json", [str(bad)]))
@@ -157,7 +164,7 @@ def _cases(tmp_path):
 
 def test_loader_matches_oracle_on_every_case(native, tmp_path):
     expect = {"export_one_shard": "ok", "export_two_shards": "ok", "dense_biased": "ok",
-              "other_layer_unbiased": "ok", "bf16_bias": "ok"}
+              "other_layer_unbiased": "ok", "bf16_bias": "ok", "empty_config": "ok", "wrapping_shape": "io"}
     for tag, paths in _cases(tmp_path):
         if tag == "missing_file":
             ov = ("io", "")

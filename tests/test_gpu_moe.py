@@ -169,6 +169,25 @@ def test_moe_grouped_full_size_batch64_sampled(native):
     _check_block(native, d, x, topk=8, tokens=[0, 17, 38, 63])
 
 
+def test_moe_grouped_full_size_batch256_sampled(native):
+    """The full Qwen3.6-35B-A3B-shaped block at batch 256 (the batched-decode
+    workload): routing checked for every token (the oracle routes 64 tokens
+    at a time), outputs for a sample of tokens."""
+    d = gen.moe_layer(1003)
+    x = gen.fp16_normal(gen.rng(2006), (256, 2048))
+    block = native.MoeBlock(d, topk=8)
+    out, ids, w = block(dev(x))
+    out, ids, w = out.cpu().numpy(), ids.cpu().numpy(), w.cpu().numpy()
+    assert int(block.workspace(256)[:4].view(torch.int32).item()) == 0
+    for c in range(0, 256, 64):
+        ref_ids, ref_w, _ = o.route(x[c:c + 64], d["Wg"], 8)
+        assert np.array_equal(ids[c:c + 64], ref_ids), c
+        assert np.allclose(w[c:c + 64], ref_w, rtol=1e-5, atol=1e-6)
+    sample = [0, 101, 170, 255]
+    ref, _, _, _ = o.moe_block(o.MoeLayer(**d), x[sample], k=8)
+    assert rel_err_rows(out[sample], ref).max() <= TOL
+
+
 @pytest.mark.parametrize("T,E,topk,tokens", [
     (17, 64, 8, None),                    # item capacity 16, runs of 1-4 tokens
     (96, 32, 4, range(0, 96, 5)),         # capacity 32

@@ -62,11 +62,12 @@ def test_stack_small_each_block_against_oracle(native, T):
     assert np.array_equal(h.cpu().numpy().view(np.uint32), final.view(np.uint32))
 
 
-@pytest.mark.parametrize("T", [1, 8])
+@pytest.mark.parametrize("T", [1, 8, 128])
 def test_stack_40_blocks_full_size(native, T):
     """The 40-block stack of full-size blocks (K per projection from seed
-    5000 + layer): finite, no bounded wait gave up, and block 17 (generated on
-    the host) matches the oracle on the x it received."""
+    5000 + layer) at decode batches 1, 8 and 128: finite, no bounded wait gave
+    up, and block 17 (generated on the host) matches the oracle on the x it
+    received (every token's norm; the outputs of sampled tokens)."""
     from escha_synth.gen_torch import moe_layer_device
 
     d17 = None
@@ -90,10 +91,34 @@ def test_stack_40_blocks_full_size(native, T):
     h_before, x, out = trace[17]
     _, ref_x = o.residual_rmsnorm(h_before.numpy(), None, eps=1e-6)
     assert np.array_equal(x.numpy().view(np.uint16), ref_x)
-    ref, _, _, _ = o.moe_block(o.MoeLayer(**d17), x.numpy(), k=8)
-    assert rel_err_rows(out.numpy(), ref).max() <= TOL
+    rows = list(range(T)) if T <= 8 else [0, 37, 64, 127]
+    ref, _, _, _ = o.moe_block(o.MoeLayer(**d17), x.numpy()[rows], k=8)
+    assert rel_err_rows(out.numpy()[rows], ref).max() <= TOL
     del blocks, stack
     torch.cuda.empty_cache()
+
+
+def test_stack_prefill_chunk_2048_one_block(native):
+    """A 2048-token prefill chunk through one full-size residual block (norm
+    kernel, then the grouped tensor-core path): every token's x is the
+    oracle's norm bit for bit, the outputs of sampled tokens match the
+    oracle's block, and h ends as h + output."""
+    kg, kd = gen.stack_k(0)
+    d = gen.moe_layer(5000, k_gu=kg, k_dn=kd)
+    stack = native.MoeStack([native.MoeBlock(d)])
+    x0 = gen.fp16_normal(gen.rng(93), (2048, 2048)).astype(np.float32)
+    h = dev(x0)
+    trace = []
+    stack(h, trace=trace)
+    assert int(stack.workspace(2048)[:4].view(torch.int32).item()) == 0
+    h_before, x, out = trace[0]
+    _, ref_x = o.residual_rmsnorm(h_before.numpy(), None, eps=1e-6)
+    assert np.array_equal(x.numpy().view(np.uint16), ref_x)
+    rows = [0, 777, 1500, 2047]
+    ref, _, _, _ = o.moe_block(o.MoeLayer(**d), x.numpy()[rows], k=8)
+    assert rel_err_rows(out.numpy()[rows], ref).max() <= TOL
+    final = (h_before.numpy() + out.numpy()).astype(np.float32)
+    assert np.array_equal(h.cpu().numpy().view(np.uint32), final.view(np.uint32))
 
 
 @pytest.mark.parametrize("T,H", [(1, 2048), (1, 768), (2, 2048), (2, 768), (1, 256), (3, 2048), (1, 4096), (20, 512)])
