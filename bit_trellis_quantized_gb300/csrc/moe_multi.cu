@@ -28,10 +28,10 @@
 // being run by some CTA: no deadlock while all CTAs are resident, which the
 // cooperative launch guarantees. A residual stack is queued block after
 // block (R S G X D). Independent blocks (each its own input) are queued as a
-// software pipeline: R S of blocks 0 and 1, G and X of block 0, then per
-// step b: R S of block b + 2, G X of block b + 1, D of block b. A unit is
-// taken long after the units it waits for, so few CTAs sit idle waiting, and
-// the blocks' routers, gate_ups and downs overlap.
+// software pipeline of depth 2: R S of blocks 0..2, G X of blocks 0 and 1,
+// then per step b: R S of block b + 3, G X of block b + 2, D of block b. A
+// unit is taken long after the units it waits for, so few CTAs sit idle
+// waiting, and the blocks' routers, gate_ups and downs overlap.
 //
 // Each unit's arithmetic, the input splits and every summation order are
 // those of the per-slot kernels at one token (slot_plan), so every block's
