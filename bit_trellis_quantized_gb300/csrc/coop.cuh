@@ -30,7 +30,9 @@ __device__ __forceinline__ unsigned long long global_ns() {
     return t;
 }
 
-// One thread: true once *p >= target; after wait_ns without it, sets *err and
+// One thread: true once *p >= target; after wait_ns without it, records
+// `code` in *err unless an earlier wait already did (so the status word names
+// the first wait that ran out, not the waits that then starve behind it) and
 // returns false. Between polls the thread sleeps a little, so that waiting
 // CTAs take few issue slots from the warps working beside them on the SM and
 // few L2 accesses from everyone.
@@ -41,7 +43,7 @@ __device__ __forceinline__ bool wait_geq(const unsigned* p, unsigned target, lon
         __nanosleep(200);
         if (ld_acquire(p) >= target) return true;
         if (static_cast<long long>(global_ns() - t0) > wait_ns) {
-            atomicExch(err, code);
+            atomicCAS(err, 0, code);
             return false;
         }
     }

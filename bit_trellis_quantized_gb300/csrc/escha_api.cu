@@ -712,6 +712,8 @@ int seq_grid(int sms, int smem, int* grid) {
 
 // The work queue of a sequence (escha::MbSeg): block after block for a
 // stack; a three-stage software pipeline for independent blocks.
+// at most 6 + 5 n + 1 segments (independent blocks) or n (stack)
+static_assert(escha::kMbMaxSegs >= 5 * escha::kMbMaxBlocks + 7, "segment table");
 void seq_segments(escha::MbArgs& m, int n, const escha::MbPlan& p, bool stack) {
     int ns = 0, pos = 0;
     auto add = [&](int b, int first, int count) {
@@ -723,20 +725,26 @@ void seq_segments(escha::MbArgs& m, int n, const escha::MbPlan& p, bool stack) {
         s.pos = pos;
         pos += count;
     };
-    const int rs = p.nR + p.nS, g0 = rs, d0 = rs + p.nG + p.nX;
+    // a block's units in order: R S, G X, F, D, C
+    const int rs = p.nR + p.nS, g0 = rs, f0 = g0 + p.nG + p.nX, d0 = f0 + p.nF, c0 = d0 + p.nD;
     if (stack) {
         for (int b = 0; b < n; ++b) add(b, 0, p.U);
     } else {
         // stage s of the pipeline: R S of block s + kDepth + 1, G X of block
-        // s + kDepth, D of block s (the first stages fill it)
+        // s + kDepth, F of block s + 1, D of block s, C of block s - 1 (the
+        // first stages fill it, a last C empties it)
         constexpr int kDepth = 2;  // measured on GB300, 8 blocks per launch: depth 1 16.8 us per block, 2 16.3, 3 16.4
         for (int b = 0; b <= kDepth; ++b) add(b, 0, rs);
         for (int b = 0; b < kDepth; ++b) add(b, g0, p.nG + p.nX);
+        add(0, f0, p.nF);
         for (int b = 0; b < n; ++b) {
             add(b + kDepth + 1, 0, rs);
             add(b + kDepth, g0, p.nG + p.nX);
+            add(b + 1, f0, p.nF);
             add(b, d0, p.nD);
+            add(b - 1, c0, p.nC);
         }
+        add(n - 1, c0, p.nC);
     }
     m.n_segs = ns;
 }
@@ -771,6 +779,8 @@ escha::MbArgs seq_args(const escha_moe_layer* const* layers, int n, const escha:
     h.nG = p.nG;
     h.nX = p.nX;
     h.nD = p.nD;
+    h.nF = p.nF;
+    h.nC = p.nC;
     h.U = p.U;
     h.xt_floats = p.xt_floats;
     h.smem = p.smem;

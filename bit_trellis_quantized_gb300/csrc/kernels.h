@@ -233,10 +233,11 @@ struct MbBlock {
 };
 struct MbPlan {
     int gu_csize, gu_kt, dn_ks;
-    int nR, nS, nG, nX, nD, U;  // work units per block: router, shared gate_up, gate_up, shared down, down
+    // work units per block: router, shared gate_up, gate_up, shared down,
+    // gate_up finish, down, combine
+    int nR, nS, nG, nX, nF, nD, nC, U;
     int xt_floats, smem;
-    size_t ctr_bytes, logits_bytes, ygu_bytes, shgu_bytes, shgate_bytes, sh_bytes, gu_part_bytes, dn_part_bytes,
-        ids_bytes;
+    size_t ctr_bytes, logits_bytes, ygu_bytes, shgu_bytes, shgate_bytes, sh_bytes, gu_part_bytes, dn_part_bytes, ids_bytes;
 };
 struct MbHead {
     int n_blocks, hidden, inter, E, topk, sh_inter;
@@ -257,13 +258,13 @@ struct MbHead {
     long long wait_ns;
     int skip_publish;
     int gu_csize, gu_kt, dn_ks;
-    int nR, nS, nG, nX, nD, U;
+    int nR, nS, nG, nX, nF, nD, nC, U;
     int xt_floats, smem;
 };
 // The work queue in segments: units [first, first + count) of block `block`,
 // segment after segment; `pos` = the queue position of the segment's first
 // unit.
-constexpr int kMbMaxSegs = 4 * kMbMaxBlocks + 4;
+constexpr int kMbMaxSegs = 5 * kMbMaxBlocks + 8;
 struct MbSeg {
     short block;
     short first;

@@ -12,26 +12,31 @@
 //   S  the int8 shared expert's gate_up: 2 rows per warp, and its gate
 //   G  gate_up: one (slot, 128-wide output block, input split)
 //   X  the shared expert's down rows (up to 3 per warp)
-//   D  down: one (slot, output block, input split); the last of an output
-//      block's D units finishes every expert of the block and adds them and
-//      the shared expert (hipfire PR #694, commit "Executed the moeblk golden
-//      against real shipped layer-0 weights": the weighted sum of the routed
-//      experts' gate_up -> SwiGLU -> down plus the sigmoid-gated shared
-//      expert).
+//   F  one slot's gate_up outputs: the G units' split partial sums added,
+//      then the output transform
+//   D  down: one (slot, output block, input split)
+//   C  combine: one output block; finishes every expert's down outputs of
+//      the block and adds them and the shared expert (hipfire PR #694,
+//      commit "Executed the moeblk golden against real shipped layer-0
+//      weights": the weighted sum of the routed experts' gate_up -> SwiGLU
+//      -> down plus the sigmoid-gated shared expert).
+// G and D units only publish their partial sums (a release add on a
+// counter, with no answer to wait for); F and C add them.
 //
-// A unit waits (bounded) only for units earlier in the queue: G and D for
-// their block's routing (the block's last R unit computes the top-k and
-// publishes it),
-// D for its expert's gate_up outputs, X for its block's shared gate_up rows,
-// the finishing D for X, and, in a stack, R for the previous block's output.
+// A unit waits (bounded) only for units earlier in the queue: G, F, D and C
+// for their block's routing (the block's last R unit computes the top-k and
+// publishes it), F for its slot's G units, D for its slot's F unit, X for
+// its block's shared gate_up rows, C for its output block's D units and for
+// X, and, in a stack, R for the previous block's output.
 // Work is taken in queue order, so the earliest unfinished unit is always
 // being run by some CTA: no deadlock while all CTAs are resident, which the
 // cooperative launch guarantees. A residual stack is queued block after
-// block (R S G X D). Independent blocks (each its own input) are queued as a
-// software pipeline of depth 2: R S of blocks 0..2, G X of blocks 0 and 1,
-// then per step b: R S of block b + 3, G X of block b + 2, D of block b. A
-// unit is taken long after the units it waits for, so few CTAs sit idle
-// waiting, and the blocks' routers, gate_ups and downs overlap.
+// block (R S G X F D C). Independent blocks (each its own input) are queued
+// as a software pipeline of depth 2: R S of blocks 0..2, G X of blocks 0 and
+// 1, F of block 0, then per step b: R S of block b + 3, G X of block b + 2,
+// F of block b + 1, D of block b, C of block b - 1. A unit is taken long
+// after the units it waits for, so few CTAs sit idle waiting, and the
+// blocks' routers, gate_ups and downs overlap.
 //
 // Each unit's arithmetic, the input splits and every summation order are
 // those of the per-slot kernels at one token (slot_plan), so every block's
@@ -60,14 +65,15 @@ constexpr int kMcLogit = 0;                    // R units done
 constexpr int kMcShGu = 1;                     // S units done
 constexpr int kMcShDn = 2;                     // X units done
 constexpr int kMcDone = 3;                     // output blocks finished
-constexpr int kMcGu = 4;                       // [8][kMbMaxOb] gate_up splits arrived per (slot, block)
-constexpr int kMcGuJ = kMcGu + 8 * kMbMaxOb;   // [8] gate_up blocks finished per slot
-constexpr int kMcCmb = kMcGuJ + 8;             // [kMbMaxOb] down units arrived per output block
+constexpr int kMcGu = 4;                       // [8] gate_up partial sums arrived per slot
+constexpr int kMcGuJ = kMcGu + 8;              // [8] the slot's gate_up outputs finished (F unit)
+constexpr int kMcCmb = kMcGuJ + 8;             // [kMbMaxOb] down partial sums arrived per output block
 constexpr int kMcRouted = kMcCmb + kMbMaxOb;   // the block's routing (ids, w) published
 constexpr int kMcWords = kMcRouted + 1;
 static_assert(kMcWords <= kMbCtrWords, "counter block");
 
-constexpr int kErrLogit = 8, kErrShGu = 9, kErrGuJ = 10, kErrShDn = 11, kErrPrev = 12, kErrNotCoop = 13;
+constexpr int kErrLogit = 8, kErrShGu = 9, kErrGuJ = 10, kErrShDn = 11, kErrPrev = 12, kErrNotCoop = 13,
+              kErrCmb = 14, kErrGu = 15;
 
 // The block's routing (experts and weights of its slots, published by its
 // last R unit) into the CTA's cache.
@@ -239,14 +245,14 @@ __device__ __forceinline__ void mb_shared_gate_up(const MbHead& m, const MbBlock
     if (threadIdx.x == 0) red_add_release(ctr + kMcShGu, 1u);
 }
 
-// G unit u of block b (slot j, output block ob, input split c), expert e.
+// G unit u of block b (slot j, output block ob, input split c), expert e:
+// the split's partial sums, published on the slot for its F unit.
 // In a stack, unit 0 also stores h += (previous output) before its partial
 // sums go out: every reader of h for this block (its R units) has finished,
 // and the next block's R units, and this block's output (written over the
 // previous one), come after every G unit.
 template <int K>
 __device__ __forceinline__ void mb_gate_up(const MbHead& m, const MbBlock& B, int b, int u, int e, float* sm) {
-    __shared__ int last_s;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int oblks = 2 * m.inter / 128, cs = m.gu_csize;
     const int j = u / (oblks * cs), ob = (u / cs) % oblks, c = u % cs;
@@ -259,8 +265,6 @@ __device__ __forceinline__ void mb_gate_up(const MbHead& m, const MbBlock& B, in
     float* red = xt + m.xt_floats;
     LaneCodes<K> cur;
     if (kt0 + warp < kt1) load_lane_codes<K>(cur, codes, grid, kt0 + warp, ob * 8, lane);
-    uint2 rout_pre = make_uint2(0u, 0u);
-    if (warp == 0) rout_pre = *reinterpret_cast<const uint2*>(B.gu_rout + (long long)e * n_out + ob * 128 + 4 * lane);
     const uint16_t* rin = B.gu_rin + (long long)e * m.hidden;
     const uint16_t* x = mb_x(m, B);
     for (int blk = warp; blk < nk / 128; blk += kMbWarps) {
@@ -286,28 +290,45 @@ __device__ __forceinline__ void mb_gate_up(const MbHead& m, const MbBlock& B, in
     float* zp = red + kMbWarps * 128;
     cta_gemv_partial<K, 1, kMbWarps>(codes, grid, ob, kt0, kt1, xt, nk, cur, red, zp);
 
-    const long long pbase = ((long long)b * m.topk * oblks + (long long)j * oblks + ob) * cs * 128;
-    float* part = m.gu_part + pbase;
-    if (warp == 0) __stcg(reinterpret_cast<float4*>(part + c * 128 + 4 * lane), *reinterpret_cast<const float4*>(zp + 4 * lane));
-    __syncthreads();
-    unsigned* ctr = m.ctr + (long long)b * kMbCtrWords;
-    if (threadIdx.x == 0) last_s = atom_add_acq_rel(ctr + kMcGu + j * kMbMaxOb + ob, 1u) == static_cast<unsigned>(cs - 1);
-    __syncthreads();
-    if (!last_s || warp != 0) return;
-    float v[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int r = 0; r < cs; ++r) {
-        const float4 z4 = r == c ? *reinterpret_cast<const float4*>(zp + 4 * lane)
-                                 : __ldcg(reinterpret_cast<const float4*>(part + r * 128 + 4 * lane));
-        v[0] += z4.x;
-        v[1] += z4.y;
-        v[2] += z4.z;
-        v[3] += z4.w;
+    // warp 0 stores the split's partial sums and publishes them on the slot
+    // (its lanes' stores are ordered before lane 0's release by the warp
+    // barrier); the slot's F unit adds the splits
+    if (warp == 0) {
+        float* part = m.gu_part + ((long long)b * m.topk * oblks + (long long)j * oblks + ob) * cs * 128;
+        __stcg(reinterpret_cast<float4*>(part + c * 128 + 4 * lane), *reinterpret_cast<const float4*>(zp + 4 * lane));
+        __syncwarp();
+        if (lane == 0) red_add_release(m.ctr + (long long)b * kMbCtrWords + kMcGu + j, 1u);
     }
-    output_transform_regs(v, rout_pre, lane);
-    __stcg(reinterpret_cast<float4*>(m.ygu + ((long long)b * m.topk + j) * n_out + ob * 128 + 4 * lane),
-           make_float4(v[0], v[1], v[2], v[3]));
-    __syncwarp();
-    if (lane == 0 && !m.skip_publish) red_add_release(ctr + kMcGuJ + j, 1u);
+}
+
+// F unit j of block b: slot j's gate_up outputs, output block ob by warp
+// ob % NW: the G units' split partial sums added in split order, then the
+// output transform (the per-slot gate_up kernel's rank 0).
+__device__ __forceinline__ void mb_gate_up_finish(const MbHead& m, const MbBlock& B, int b, int j, const int* e_s) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int oblks = 2 * m.inter / 128, cs = m.gu_csize, n_out = 2 * m.inter;
+    const int e = e_s[j];
+    uint2 rout_pre = make_uint2(0u, 0u);
+    if (warp < oblks) rout_pre = *reinterpret_cast<const uint2*>(B.gu_rout + (long long)e * n_out + warp * 128 + 4 * lane);
+    unsigned* ctr = m.ctr + (long long)b * kMbCtrWords;
+    if (!cta_wait_geq(ctr + kMcGu + j, static_cast<unsigned>(oblks * cs), m.wait_ns, m.err, kErrGu)) return;
+    for (int ob = warp; ob < oblks; ob += kMbWarps) {
+        const float* part = m.gu_part + ((long long)b * m.topk * oblks + (long long)j * oblks + ob) * cs * 128;
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int r = 0; r < cs; ++r) {
+            const float4 z4 = __ldcg(reinterpret_cast<const float4*>(part + r * 128 + 4 * lane));
+            v[0] += z4.x;
+            v[1] += z4.y;
+            v[2] += z4.z;
+            v[3] += z4.w;
+        }
+        const uint2 rb = ob == warp ? rout_pre : *reinterpret_cast<const uint2*>(B.gu_rout + (long long)e * n_out + ob * 128 + 4 * lane);
+        output_transform_regs(v, rb, lane);
+        __stcg(reinterpret_cast<float4*>(m.ygu + ((long long)b * m.topk + j) * n_out + ob * 128 + 4 * lane),
+               make_float4(v[0], v[1], v[2], v[3]));
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !m.skip_publish) red_add_release(ctr + kMcGuJ + j, 1u);
 }
 
 // X unit x of block b: shared down rows x * 8 + warp + k * 8 * nX (the
@@ -349,16 +370,12 @@ __device__ __forceinline__ void mb_shared_down(const MbHead& m, const MbBlock& B
     if (threadIdx.x == 0) red_add_release(ctr + kMcShDn, 1u);
 }
 
-// D unit d of block b (slot j, output block ob, input split h). The last of
-// the output block's topk * ks units finishes it: warp q adds expert q's
-// split partials in split order and applies its output transform and
-// routing weight; the experts are added in slot order and the shared expert
-// last (the per-slot down kernel's rank 0); in a stack the last block also
-// adds its output to h.
+// D unit d of block b (slot j, output block ob, input split h): SwiGLU of
+// the slot's finished gate_up outputs, rin and the input Hadamard, then the
+// split's partial sums of the 128 outputs, published on ob for the C unit.
 template <int K>
 __device__ __forceinline__ void mb_down(const MbHead& m, const MbBlock& B, int b, int d, const int* e_s, const float* w_s,
                                         float* sm) {
-    __shared__ int last_s;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nob = m.hidden / 128, ks = m.dn_ks;
     const int j = d / (nob * ks), ob = (d / ks) % nob, h = d % ks;
@@ -382,11 +399,8 @@ __device__ __forceinline__ void mb_down(const MbHead& m, const MbBlock& B, int b
     const uint16_t* rin = B.dn_rin + (long long)e * m.inter;
     uint2 rin_pre = make_uint2(0u, 0u);
     if (warp < nk / 128) rin_pre = *reinterpret_cast<const uint2*>(rin + kt0 * 16 + warp * 128 + 4 * lane);
-    uint2 rout_pre = make_uint2(0u, 0u);
-    if (warp < m.topk)
-        rout_pre = *reinterpret_cast<const uint2*>(B.dn_rout + (long long)e_s[warp] * m.hidden + ob * 128 + 4 * lane);
     unsigned* ctr = m.ctr + (long long)b * kMbCtrWords;
-    if (!cta_wait_geq(ctr + kMcGuJ + j, static_cast<unsigned>(2 * m.inter / 128), m.wait_ns, m.err, kErrGuJ)) return;
+    if (!cta_wait_geq(ctr + kMcGuJ + j, 1u, m.wait_ns, m.err, kErrGuJ)) return;
 
     const float* yr = m.ygu + ((long long)b * m.topk + j) * 2 * m.inter;
     for (int blk = warp; blk < nk / 128; blk += kMbWarps) {
@@ -406,19 +420,40 @@ __device__ __forceinline__ void mb_down(const MbHead& m, const MbBlock& B, int b
     float* zp = red + kMbWarps * 128;
     cta_gemv_partial<K, 1, kMbWarps>(codes, grid, ob, kt0, kt1, xt, nk, cur, red, zp);
 
-    float* part = m.dn_part + (((long long)b * nob + ob) * m.topk) * ks * 128;  // [topk][ks][128] of the block
-    if (warp == 0) __stcg(reinterpret_cast<float4*>(part + (j * ks + h) * 128 + 4 * lane), *reinterpret_cast<const float4*>(zp + 4 * lane));
-    __syncthreads();
-    if (threadIdx.x == 0) last_s = atom_add_acq_rel(ctr + kMcCmb + ob, 1u) == static_cast<unsigned>(m.topk * ks - 1);
-    __syncthreads();
-    if (!last_s) return;
-    float* dres = red;  // [topk][128]; zp (own partial) lies beyond it
+    if (warp == 0) {
+        float* part = m.dn_part + (((long long)b * nob + ob) * m.topk) * ks * 128;  // [topk][ks][128] of the block
+        __stcg(reinterpret_cast<float4*>(part + (j * ks + h) * 128 + 4 * lane), *reinterpret_cast<const float4*>(zp + 4 * lane));
+        __syncwarp();
+        if (lane == 0) red_add_release(ctr + kMcCmb + ob, 1u);
+    }
+}
+
+// C unit: output block ob of block b. Warp q adds expert q's down split
+// partials in split order and applies its output transform and routing
+// weight; the experts are added in slot order and the shared expert last
+// (the per-slot down kernel's rank 0); in a stack the last block also adds
+// its output to h.
+__device__ __forceinline__ void mb_combine(const MbHead& m, const MbBlock& B, int b, int ob, const int* e_s,
+                                           const float* w_s, float* sm) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nob = m.hidden / 128, ks = m.dn_ks;
+    uint2 rout_pre = make_uint2(0u, 0u);
+    if (warp < m.topk)
+        rout_pre = *reinterpret_cast<const uint2*>(B.dn_rout + (long long)e_s[warp] * m.hidden + ob * 128 + 4 * lane);
+    unsigned* ctr = m.ctr + (long long)b * kMbCtrWords;
+    int ok = 1;
+    if (threadIdx.x == 0) {
+        ok = wait_geq(ctr + kMcCmb + ob, static_cast<unsigned>(m.topk * ks), m.wait_ns, m.err, kErrCmb);
+        if (ok && m.sh_inter > 0) ok = wait_geq(ctr + kMcShDn, static_cast<unsigned>(m.nX), m.wait_ns, m.err, kErrShDn);
+    }
+    if (!__syncthreads_and(ok)) return;
+    const float* part = m.dn_part + (((long long)b * nob + ob) * m.topk) * ks * 128;
+    float* dres = sm;  // [topk][128]
     if (warp < m.topk) {
         const int q = warp;
         float v[4] = {0.f, 0.f, 0.f, 0.f};
         for (int sp = 0; sp < ks; ++sp) {
-            const float4 z4 = (q == j && sp == h) ? *reinterpret_cast<const float4*>(zp + 4 * lane)
-                                                  : __ldcg(reinterpret_cast<const float4*>(part + (q * ks + sp) * 128 + 4 * lane));
+            const float4 z4 = __ldcg(reinterpret_cast<const float4*>(part + (q * ks + sp) * 128 + 4 * lane));
             v[0] += z4.x;
             v[1] += z4.y;
             v[2] += z4.z;
@@ -428,9 +463,7 @@ __device__ __forceinline__ void mb_down(const MbHead& m, const MbBlock& B, int b
         const float wq = w_s[q];
         *reinterpret_cast<float4*>(dres + q * 128 + 4 * lane) = make_float4(wq * v[0], wq * v[1], wq * v[2], wq * v[3]);
     }
-    int ok = 1;
-    if (m.sh_inter > 0 && threadIdx.x == 0) ok = wait_geq(ctr + kMcShDn, static_cast<unsigned>(m.nX), m.wait_ns, m.err, kErrShDn);
-    if (!__syncthreads_and(ok)) return;
+    __syncthreads();
     if (threadIdx.x < 128) {
         const int i = threadIdx.x;
         float sum = 0.f;
@@ -518,14 +551,19 @@ __global__ void __launch_bounds__(kMbThreads, 4) moe_multi_kernel(const __grid_c
             }
         } else if (l < m.nR + m.nS + m.nG + m.nX) {
             mb_shared_down(m, B, b, l - m.nR - m.nS - m.nG, sm);
-        } else {
-            const int d = l - m.nR - m.nS - m.nG - m.nX;
+        } else if (l < m.nR + m.nS + m.nG + m.nX + m.nF) {
+            if (mb_routing(m, B, b, &tk_block, e_s, w_s)) mb_gate_up_finish(m, B, b, l - m.nR - m.nS - m.nG - m.nX, e_s);
+        } else if (l < m.nR + m.nS + m.nG + m.nX + m.nF + m.nD) {
+            const int d = l - m.nR - m.nS - m.nG - m.nX - m.nF;
             if (mb_routing(m, B, b, &tk_block, e_s, w_s)) {
                 if (B.dn_K == 2)
                     mb_down<2>(m, B, b, d, e_s, w_s, sm);
                 else
                     mb_down<3>(m, B, b, d, e_s, w_s, sm);
             }
+        } else {
+            if (mb_routing(m, B, b, &tk_block, e_s, w_s))
+                mb_combine(m, B, b, l - m.nR - m.nS - m.nG - m.nX - m.nF - m.nD, e_s, w_s, sm);
         }
         __syncthreads();
         if (threadIdx.x == 0) q_s = q_next;
@@ -555,7 +593,9 @@ MbPlan multi_plan(int n_blocks, int hidden, int inter, int E, int topk, int sh_i
     p.nG = topk * (2 * inter / 128) * sp.gu_csize;
     p.nX = sh_inter > 0 ? (hidden + 3 * kMbWarps - 1) / (3 * kMbWarps) : 0;
     p.nD = topk * (hidden / 128) * sp.dn_ksplit;
-    p.U = p.nR + p.nS + p.nG + p.nX + p.nD;
+    p.nF = topk;
+    p.nC = hidden / 128;
+    p.U = p.nR + p.nS + p.nG + p.nX + p.nF + p.nD + p.nC;
     p.xt_floats = (max(sp.gu_kt_per_cta * 16, inter / sp.dn_ksplit) + 31) / 32 * 32;
     const int unit_floats = max(max(p.xt_floats + (kMbWarps + 1) * 128, hidden), max(sh_inter, hidden / 2));
     p.smem = unit_floats * 4;

@@ -127,6 +127,70 @@ __device__ __forceinline__ void decode_fma(const LaneCodes<K>& lc, const float (
     });
 }
 
+// The warp's column sums (acc2 as decode_fma leaves them) reduce-scattered
+// over the 4 lanes of each tile and stored as the warp's row of `red`
+// ([NW][NB][128] floats, smem).
+template <int K, int NB>
+__device__ __forceinline__ void warp_partial_store(const float2 (&acc2)[NB][8], float* red) {
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int c = lane & 3;
+    // column sums in column order
+    float acc[NB][16];
+#pragma unroll
+    for (int t = 0; t < NB; ++t)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            acc[t][acc2_col<K>(i, 0)] = acc2[t][i].x;
+            acc[t][acc2_col<K>(i, 1)] = acc2[t][i].y;
+        }
+    // Reduce-scatter over the 4 lanes of a tile: lane c keeps output columns
+    // 4c..4c+3 of tile lane/4.
+#pragma unroll
+    for (int t = 0; t < NB; ++t) {
+        float h8[8];
+        const bool hi2 = (c & 2) != 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float send = hi2 ? acc[t][i] : acc[t][8 + i];
+            const float keep = hi2 ? acc[t][8 + i] : acc[t][i];
+            h8[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+        }
+        const bool hi1 = (c & 1) != 0;
+        float h4[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float send = hi1 ? h8[i] : h8[4 + i];
+            const float keep = hi1 ? h8[4 + i] : h8[i];
+            h4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+        }
+        *reinterpret_cast<float4*>(red + (warp * NB + t) * 128 + (lane >> 2) * 16 + 4 * c) =
+            make_float4(h4[0], h4[1], h4[2], h4[3]);
+    }
+}
+
+// zp[i] = the warps' rows of red summed in warp order (i < n), by the CTA's
+// NW warps. No barrier.
+template <int NW>
+__device__ __forceinline__ void cta_sum_rows(const float* red, int n, float* zp) {
+    for (int i = threadIdx.x; i < n; i += NW * 32) {
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) s += red[w * n + i];
+        zp[i] = s;
+    }
+}
+
+// In-CTA reduction of the warps' column sums into zp[NB][128] (smem); `red`
+// is smem scratch of NW*NB*128 floats. Ends with __syncthreads().
+template <int K, int NB, int NW>
+__device__ __forceinline__ void cta_partial_reduce(const float2 (&acc2)[NB][8], float* red, float* zp) {
+    warp_partial_store<K, NB>(acc2, red);
+    __syncthreads();
+    cta_sum_rows<NW>(red, NB * 128, zp);
+    __syncthreads();
+}
+
 // Main loop and in-CTA reduction. `codes` is the expert's code tensor, `g`
 // its tile grid, `ob` the output block, rows kt0..kt1-1,
 // `xt` the transformed inputs [NB][nk] of those rows (smem), `first` the
@@ -173,46 +237,7 @@ __device__ __forceinline__ void cta_gemv_partial(const uint16_t* codes, const Ti
         step(nxt, kt + NW);
     }
 
-    // column sums in column order
-    float acc[NB][16];
-#pragma unroll
-    for (int t = 0; t < NB; ++t)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            acc[t][acc2_col<K>(i, 0)] = acc2[t][i].x;
-            acc[t][acc2_col<K>(i, 1)] = acc2[t][i].y;
-        }
-    // Reduce-scatter over the 4 lanes of a tile: lane c keeps output columns
-    // 4c..4c+3 of tile lane/4.
-#pragma unroll
-    for (int t = 0; t < NB; ++t) {
-        float h8[8];
-        const bool hi2 = (c & 2) != 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float send = hi2 ? acc[t][i] : acc[t][8 + i];
-            const float keep = hi2 ? acc[t][8 + i] : acc[t][i];
-            h8[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-        }
-        const bool hi1 = (c & 1) != 0;
-        float h4[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float send = hi1 ? h8[i] : h8[4 + i];
-            const float keep = hi1 ? h8[4 + i] : h8[i];
-            h4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
-        }
-        *reinterpret_cast<float4*>(red + (warp * NB + t) * 128 + (lane >> 2) * 16 + 4 * c) =
-            make_float4(h4[0], h4[1], h4[2], h4[3]);
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < NB * 128; i += NW * 32) {
-        float s = 0.f;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) s += red[w * NB * 128 + i];
-        zp[i] = s;
-    }
-    __syncthreads();
+    cta_partial_reduce<K, NB, NW>(acc2, red, zp);
 }
 
 // Output transform of one 128-block by one warp: v holds 4 consecutive

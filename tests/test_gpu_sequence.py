@@ -185,9 +185,12 @@ def test_stack_40_blocks_full_size_bit_identical(native):
 
 def test_sequence_bounded_wait_runs_out(native):
     """With every expert's gate_up outputs kept unpublished and a 2 ms bound,
-    the down units give up: the launch ends and the status word says so
-    (10 = the wait for an expert's gate_up outputs); the next launch with the
-    default settings is correct again."""
+    the down units give up, and so do the combine units that wait for them:
+    the launch ends and the status word names the first wait that ran out
+    (10 = a down unit's wait for its expert's gate_up outputs, 14 = a combine
+    unit's wait for the down partial sums; which comes first depends on when
+    each unit was taken); the next launch with the default settings is
+    correct again."""
     blocks = [native.MoeBlock(d, topk=4) for d in _stack_layers(2)]
     xs = [dev(gen.fp16_normal(gen.rng(700 + i), (512,))) for i in range(2)]
     ref_out, _, _ = _per_block(blocks, xs)
@@ -198,7 +201,7 @@ def test_sequence_bounded_wait_runs_out(native):
         dt = time.time() - t0
     finally:
         native.set_fused_wait()
-    assert status == 10, status
+    assert status in (10, 14), status
     assert dt < 10.0
     out, _, _, status = _sequence(native, blocks, xs)
     assert status == 0
