@@ -479,30 +479,37 @@ __device__ __forceinline__ void mb_combine(const MbHead& m, const MbBlock& B, in
 
 // Queue position q -> (block, unit index within the block): the segment
 // holding q (the last one whose first position is <= q; binary search).
-__device__ __forceinline__ void mb_unit_at(const MbArgs& a, int q, int* b, int* l) {
-    int lo = 0, hi = a.n_segs - 1;
+__device__ __forceinline__ void mb_unit_at(const MbSeg* seg, int n_segs, int q, int* b, int* l) {
+    int lo = 0, hi = n_segs - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (a.seg[mid].pos <= q) lo = mid;
+        if (seg[mid].pos <= q) lo = mid;
         else hi = mid - 1;
     }
-    *b = a.seg[lo].block;
-    *l = a.seg[lo].first + (q - a.seg[lo].pos);
+    *b = seg[lo].block;
+    *l = seg[lo].first + (q - seg[lo].pos);
 }
 
 __global__ void __launch_bounds__(kMbThreads, 4) moe_multi_kernel(const __grid_constant__ MbArgs args) {
     extern __shared__ __align__(16) float sm[];
-    // the launch's settings and the current block's descriptor live in shared
-    // memory: units reload them after their barriers instead of holding them
-    // in registers across the whole work loop
+    // the launch's settings, the blocks' descriptors and the queue's segments
+    // live in shared memory: units read them there (not through the
+    // parameter space, and not held in registers across the work loop)
     __shared__ __align__(16) MbHead m;
-    __shared__ __align__(16) MbBlock Bs;
-    __shared__ int q_s, tk_block, blk_s;
+    __shared__ __align__(16) MbBlock blk_s[kMbMaxBlocks];
+    __shared__ __align__(16) MbSeg seg_s[kMbMaxSegs];
+    __shared__ int tk_block;
     __shared__ int e_s[8];
     __shared__ float w_s[8];
-    static_assert(sizeof(MbHead) % 8 == 0, "settings copied in 8-byte words");
+    __shared__ int4 qbl_s[2];  // the next unit (queue position, block, unit in block), two slots used in turn
+    static_assert(sizeof(MbHead) % 8 == 0 && sizeof(MbBlock) % 8 == 0 && sizeof(MbSeg) % 4 == 0, "copied in words");
+    const int n_segs = args.n_segs;
     if (threadIdx.x < static_cast<int>(sizeof(MbHead) / 8))
         reinterpret_cast<unsigned long long*>(&m)[threadIdx.x] = reinterpret_cast<const unsigned long long*>(&args.h)[threadIdx.x];
+    for (int i = threadIdx.x; i < args.h.n_blocks * static_cast<int>(sizeof(MbBlock) / 8); i += kMbThreads)
+        reinterpret_cast<unsigned long long*>(blk_s)[i] = reinterpret_cast<const unsigned long long*>(args.blk)[i];
+    for (int i = threadIdx.x; i < n_segs * static_cast<int>(sizeof(MbSeg) / 4); i += kMbThreads)
+        reinterpret_cast<int*>(seg_s)[i] = reinterpret_cast<const int*>(args.seg)[i];
     __syncthreads();
     pdl_wait();
     cg::grid_group grid = cg::this_grid();
@@ -515,27 +522,27 @@ __global__ void __launch_bounds__(kMbThreads, 4) moe_multi_kernel(const __grid_c
     for (long long i = (long long)blockIdx.x * kMbThreads + threadIdx.x; i < words; i += (long long)gridDim.x * kMbThreads)
         m.ctr[i] = 0u;
     if (blockIdx.x == 0 && threadIdx.x == 0) *m.err = 0;
-    if (threadIdx.x == 0) tk_block = blk_s = -1;
+    if (threadIdx.x == 0) tk_block = -1;
     grid.sync();
 
     unsigned* queue = m.ctr + (long long)m.n_blocks * kMbCtrWords;
     const int total = m.n_blocks * m.U;
-    if (threadIdx.x == 0) q_s = static_cast<int>(atomicAdd(queue, 1u));
+    // thread 0 takes the queue positions and looks them up; the next unit
+    // reaches the CTA through qbl_s (one barrier per unit)
+    if (threadIdx.x == 0) {
+        const int q0 = static_cast<int>(atomicAdd(queue, 1u));
+        int b0 = 0, l0 = 0;
+        if (q0 < total) mb_unit_at(seg_s, n_segs, q0, &b0, &l0);
+        qbl_s[0] = make_int4(q0, b0, l0, 0);
+    }
     __syncthreads();
-    int q = q_s;
-    while (q < total) {
+    for (int it = 0;; ++it) {
+        const int4 cur = qbl_s[it & 1];
+        if (cur.x >= total) break;
+        const int b = cur.y, l = cur.z;
         int q_next = 0;
         if (threadIdx.x == 0) q_next = static_cast<int>(atomicAdd(queue, 1u));  // in flight while this unit runs
-        int b, l;
-        mb_unit_at(args, q, &b, &l);
-        if (b != blk_s) {  // the block's descriptor into shared memory (read there, not through the parameter array)
-            if (threadIdx.x < static_cast<int>(sizeof(MbBlock) / 8))
-                reinterpret_cast<unsigned long long*>(&Bs)[threadIdx.x] =
-                    reinterpret_cast<const unsigned long long*>(&args.blk[b])[threadIdx.x];
-            __syncthreads();
-            if (threadIdx.x == 0) blk_s = b;
-        }
-        const MbBlock& B = Bs;
+        const MbBlock& B = blk_s[b];
         if (l < m.nR) {
             mb_router(m, B, b, l, sm);
         } else if (l < m.nR + m.nS) {
@@ -565,10 +572,12 @@ __global__ void __launch_bounds__(kMbThreads, 4) moe_multi_kernel(const __grid_c
             if (mb_routing(m, B, b, &tk_block, e_s, w_s))
                 mb_combine(m, B, b, l - m.nR - m.nS - m.nG - m.nX - m.nF - m.nD, e_s, w_s, sm);
         }
+        if (threadIdx.x == 0) {
+            int bn = 0, ln = 0;
+            if (q_next < total) mb_unit_at(seg_s, n_segs, q_next, &bn, &ln);
+            qbl_s[(it + 1) & 1] = make_int4(q_next, bn, ln, 0);
+        }
         __syncthreads();
-        if (threadIdx.x == 0) q_s = q_next;
-        __syncthreads();
-        q = q_s;
     }
 }
 
