@@ -68,26 +68,44 @@ constexpr int kMcDone = 3;                     // output blocks finished
 constexpr int kMcGu = 4;                       // [8] gate_up partial sums arrived per slot
 constexpr int kMcGuJ = kMcGu + 8;              // [8] the slot's gate_up outputs finished (F unit)
 constexpr int kMcCmb = kMcGuJ + 8;             // [kMbMaxOb] down partial sums arrived per output block
-constexpr int kMcRouted = kMcCmb + kMbMaxOb;   // the block's routing (ids, w) published
-constexpr int kMcWords = kMcRouted + 1;
+// [8] 64-bit words, one per slot: routing weight bits << 32 | (expert + 1),
+// published by the block's last R unit (0 until then)
+constexpr int kMcRoute = kMcCmb + kMbMaxOb;
+constexpr int kMcWords = kMcRoute + 16;
+static_assert(kMcRoute % 2 == 0 && kMbCtrWords % 2 == 0, "64-bit routing words");
 static_assert(kMcWords <= kMbCtrWords, "counter block");
 
 constexpr int kErrLogit = 8, kErrShGu = 9, kErrGuJ = 10, kErrShDn = 11, kErrPrev = 12, kErrNotCoop = 13,
               kErrCmb = 14, kErrGu = 15;
 
 // The block's routing (experts and weights of its slots, published by its
-// last R unit) into the CTA's cache.
-__device__ __forceinline__ bool mb_routing(const MbHead& m, const MbBlock& B, int b, int* tk_block, int* e_s,
-                                           float* w_s) {
+// last R unit) into the CTA's cache: thread j < topk reads slot j's word,
+// which carries the expert, its weight and the publication at once.
+__device__ __forceinline__ bool mb_routing(const MbHead& m, int b, int* tk_block, int* e_s, float* w_s) {
     if (*tk_block == b) return true;
-    const unsigned* ctr = m.ctr + (long long)b * kMbCtrWords;
-    if (!cta_wait_geq(ctr + kMcRouted, 1u, m.wait_ns, m.err, kErrLogit)) return false;
+    int ok = 1;
     if (threadIdx.x < m.topk) {
-        e_s[threadIdx.x] = __ldcg(B.ids + threadIdx.x);
-        w_s[threadIdx.x] = __ldcg(B.w + threadIdx.x);
+        const unsigned long long* rt =
+            reinterpret_cast<const unsigned long long*>(m.ctr + (long long)b * kMbCtrWords + kMcRoute) + threadIdx.x;
+        unsigned long long v = ld_acquire_u64(rt);
+        if (static_cast<unsigned>(v) == 0u) {
+            const unsigned long long t0 = global_ns();
+            for (;;) {
+                __nanosleep(200);
+                v = ld_acquire_u64(rt);
+                if (static_cast<unsigned>(v) != 0u) break;
+                if (static_cast<long long>(global_ns() - t0) > m.wait_ns) {
+                    atomicCAS(m.err, 0, kErrLogit);
+                    ok = 0;
+                    break;
+                }
+            }
+        }
+        e_s[threadIdx.x] = static_cast<int>(static_cast<unsigned>(v)) - 1;
+        w_s[threadIdx.x] = __uint_as_float(static_cast<unsigned>(v >> 32));
     }
+    if (!__syncthreads_and(ok)) return false;
     if (threadIdx.x == 0) *tk_block = b;
-    __syncthreads();
     return true;
 }
 
@@ -189,9 +207,9 @@ __device__ __forceinline__ void mb_router(const MbHead& m, const MbBlock& B, int
     if (lane < m.topk) {
         __stcg(B.ids + lane, e_l);
         __stcg(B.w + lane, w_l);
+        st_release_u64(reinterpret_cast<unsigned long long*>(ctr + kMcRoute) + lane,
+                       (static_cast<unsigned long long>(__float_as_uint(w_l)) << 32) | static_cast<unsigned>(e_l + 1));
     }
-    __syncwarp();
-    if (lane == 0) red_add_release(ctr + kMcRouted, 1u);
 }
 
 // S unit s of block b: shared gate_up rows 16 s .. 16 s + 15 (2 per warp) and,
@@ -549,7 +567,7 @@ __global__ void __launch_bounds__(kMbThreads, 4) moe_multi_kernel(const __grid_c
             mb_shared_gate_up(m, B, b, l - m.nR, sm);
         } else if (l < m.nR + m.nS + m.nG) {
             const int u = l - m.nR - m.nS;
-            if (mb_routing(m, B, b, &tk_block, e_s, w_s)) {
+            if (mb_routing(m, b, &tk_block, e_s, w_s)) {
                 const int e = e_s[u / (2 * m.inter / 128 * m.gu_csize)];
                 if (B.gu_K == 2)
                     mb_gate_up<2>(m, B, b, u, e, sm);
@@ -559,17 +577,17 @@ __global__ void __launch_bounds__(kMbThreads, 4) moe_multi_kernel(const __grid_c
         } else if (l < m.nR + m.nS + m.nG + m.nX) {
             mb_shared_down(m, B, b, l - m.nR - m.nS - m.nG, sm);
         } else if (l < m.nR + m.nS + m.nG + m.nX + m.nF) {
-            if (mb_routing(m, B, b, &tk_block, e_s, w_s)) mb_gate_up_finish(m, B, b, l - m.nR - m.nS - m.nG - m.nX, e_s);
+            if (mb_routing(m, b, &tk_block, e_s, w_s)) mb_gate_up_finish(m, B, b, l - m.nR - m.nS - m.nG - m.nX, e_s);
         } else if (l < m.nR + m.nS + m.nG + m.nX + m.nF + m.nD) {
             const int d = l - m.nR - m.nS - m.nG - m.nX - m.nF;
-            if (mb_routing(m, B, b, &tk_block, e_s, w_s)) {
+            if (mb_routing(m, b, &tk_block, e_s, w_s)) {
                 if (B.dn_K == 2)
                     mb_down<2>(m, B, b, d, e_s, w_s, sm);
                 else
                     mb_down<3>(m, B, b, d, e_s, w_s, sm);
             }
         } else {
-            if (mb_routing(m, B, b, &tk_block, e_s, w_s))
+            if (mb_routing(m, b, &tk_block, e_s, w_s))
                 mb_combine(m, B, b, l - m.nR - m.nS - m.nG - m.nX - m.nF - m.nD, e_s, w_s, sm);
         }
         if (threadIdx.x == 0) {
