@@ -632,7 +632,7 @@ int moe_block_impl(const escha_moe_layer* L, const uint16_t* x, int T, float* ou
 namespace {
 
 struct SeqWs {
-    size_t err, ctr, logits, ygu, shgu, shgate, sh, gu_part, dn_part, ids, w, total;
+    size_t err, ctr, logits, xdg, shgu, shgate, sh, gu_part, dn_part, ids, w, total;
 };
 
 SeqWs seq_ws_layout(const escha::MbPlan& p) {
@@ -644,8 +644,8 @@ SeqWs seq_ws_layout(const escha::MbPlan& p) {
     off += align_up(p.ctr_bytes);
     w.logits = off;
     off += align_up(p.logits_bytes);
-    w.ygu = off;
-    off += align_up(p.ygu_bytes);
+    w.xdg = off;
+    off += align_up(p.xdg_bytes);
     w.shgu = off;
     off += align_up(p.shgu_bytes);
     w.shgate = off;
@@ -762,7 +762,7 @@ escha::MbArgs seq_args(const escha_moe_layer* const* layers, int n, const escha:
     h.sh_inter = L->sh_inter;
     h.ctr = reinterpret_cast<unsigned*>(base + w.ctr);
     h.logits = reinterpret_cast<uint16_t*>(base + w.logits);
-    h.ygu = reinterpret_cast<float*>(base + w.ygu);
+    h.xdg = reinterpret_cast<float*>(base + w.xdg);
     h.shgu = reinterpret_cast<float*>(base + w.shgu);
     h.shgate = reinterpret_cast<float*>(base + w.shgate);
     h.sh = reinterpret_cast<float*>(base + w.sh);

@@ -237,7 +237,7 @@ struct MbPlan {
     // gate_up finish, down, combine
     int nR, nS, nG, nX, nF, nD, nC, U;
     int xt_floats, smem;
-    size_t ctr_bytes, logits_bytes, ygu_bytes, shgu_bytes, shgate_bytes, sh_bytes, gu_part_bytes, dn_part_bytes, ids_bytes;
+    size_t ctr_bytes, logits_bytes, xdg_bytes, shgu_bytes, shgate_bytes, sh_bytes, gu_part_bytes, dn_part_bytes, ids_bytes;
 };
 struct MbHead {
     int n_blocks, hidden, inter, E, topk, sh_inter;
@@ -248,7 +248,7 @@ struct MbHead {
     float* outbuf;   // [hidden] the current block's output
     unsigned* ctr;   // [n_blocks][kMbCtrWords], then the work queue
     uint16_t* logits;
-    float* ygu;
+    float* xdg;      // [n_blocks][topk][inter]: the slots' transformed down inputs
     float* shgu;
     float* shgate;
     float* sh;

@@ -321,13 +321,19 @@ __device__ __forceinline__ void mb_gate_up(const MbHead& m, const MbBlock& B, in
 
 // F unit j of block b: slot j's gate_up outputs, output block ob by warp
 // ob % NW: the G units' split partial sums added in split order, then the
-// output transform (the per-slot gate_up kernel's rank 0).
-__device__ __forceinline__ void mb_gate_up_finish(const MbHead& m, const MbBlock& B, int b, int j, const int* e_s) {
+// output transform (the per-slot gate_up kernel's rank 0); then, from them,
+// the slot's down inputs H128(rin * SwiGLU(gate, up)), 128-block i by warp i
+// % NW (the per-slot down kernel's prologue), into the workspace for the
+// slot's D units.
+__device__ __forceinline__ void mb_gate_up_finish(const MbHead& m, const MbBlock& B, int b, int j, const int* e_s,
+                                                  float* ys) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int oblks = 2 * m.inter / 128, cs = m.gu_csize, n_out = 2 * m.inter;
+    const int oblks = 2 * m.inter / 128, cs = m.gu_csize, n_out = 2 * m.inter, nib = m.inter / 128;
     const int e = e_s[j];
-    uint2 rout_pre = make_uint2(0u, 0u);
+    uint2 rout_pre = make_uint2(0u, 0u), rin_pre = make_uint2(0u, 0u);
     if (warp < oblks) rout_pre = *reinterpret_cast<const uint2*>(B.gu_rout + (long long)e * n_out + warp * 128 + 4 * lane);
+    const uint16_t* rin = B.dn_rin + (long long)e * m.inter;
+    if (warp < nib) rin_pre = *reinterpret_cast<const uint2*>(rin + warp * 128 + 4 * lane);
     unsigned* ctr = m.ctr + (long long)b * kMbCtrWords;
     if (!cta_wait_geq(ctr + kMcGu + j, static_cast<unsigned>(oblks * cs), m.wait_ns, m.err, kErrGu)) return;
     for (int ob = warp; ob < oblks; ob += kMbWarps) {
@@ -342,8 +348,21 @@ __device__ __forceinline__ void mb_gate_up_finish(const MbHead& m, const MbBlock
         }
         const uint2 rb = ob == warp ? rout_pre : *reinterpret_cast<const uint2*>(B.gu_rout + (long long)e * n_out + ob * 128 + 4 * lane);
         output_transform_regs(v, rb, lane);
-        __stcg(reinterpret_cast<float4*>(m.ygu + ((long long)b * m.topk + j) * n_out + ob * 128 + 4 * lane),
-               make_float4(v[0], v[1], v[2], v[3]));
+        *reinterpret_cast<float4*>(ys + ob * 128 + 4 * lane) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+    __syncthreads();
+    float* xd = m.xdg + ((long long)b * m.topk + j) * m.inter;
+    for (int i = warp; i < nib; i += kMbWarps) {
+        const float4 gv = *reinterpret_cast<const float4*>(ys + i * 128 + 4 * lane);
+        const float4 uv = *reinterpret_cast<const float4*>(ys + (nib + i) * 128 + 4 * lane);
+        const uint2 rb = i == warp ? rin_pre : *reinterpret_cast<const uint2*>(rin + i * 128 + 4 * lane);
+        float v[4];
+        v[0] = h2f_bits(static_cast<uint16_t>(rb.x & 0xFFFFu)) * (silu_f(gv.x) * uv.x);
+        v[1] = h2f_bits(static_cast<uint16_t>(rb.x >> 16)) * (silu_f(gv.y) * uv.y);
+        v[2] = h2f_bits(static_cast<uint16_t>(rb.y & 0xFFFFu)) * (silu_f(gv.z) * uv.z);
+        v[3] = h2f_bits(static_cast<uint16_t>(rb.y >> 16)) * (silu_f(gv.w) * uv.w);
+        h128_warp(v, lane);
+        __stcg(reinterpret_cast<float4*>(xd + i * 128 + 4 * lane), make_float4(v[0], v[1], v[2], v[3]));
     }
     __syncthreads();
     if (threadIdx.x == 0 && !m.skip_publish) red_add_release(ctr + kMcGuJ + j, 1u);
@@ -400,11 +419,10 @@ __device__ __forceinline__ void mb_down(const MbHead& m, const MbBlock& B, int b
     const int e = e_s[j];
     const int KT = m.inter >> 4, NT = m.hidden >> 4;
     const int rows_h = KT / ks;
-    const int kt0 = h * rows_h, kt1 = kt0 + rows_h, nk = rows_h * 16;
+    const int kt0 = h * rows_h, kt1 = kt0 + rows_h;
     const uint16_t* codes = B.dn_codes + (long long)e * KT * NT * (16 * K);
     const TileStrides grid{NT, 1};
-    float* xt = sm;
-    float* red = xt + m.xt_floats;
+    float* red = sm;
     LaneCodes<K> cur;
     if (kt0 + warp < kt1) load_lane_codes<K>(cur, codes, grid, kt0 + warp, ob * 8, lane);
     {
@@ -414,29 +432,11 @@ __device__ __forceinline__ void mb_down(const MbHead& m, const MbBlock& B, int b
             asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
         }
     }
-    const uint16_t* rin = B.dn_rin + (long long)e * m.inter;
-    uint2 rin_pre = make_uint2(0u, 0u);
-    if (warp < nk / 128) rin_pre = *reinterpret_cast<const uint2*>(rin + kt0 * 16 + warp * 128 + 4 * lane);
     unsigned* ctr = m.ctr + (long long)b * kMbCtrWords;
     if (!cta_wait_geq(ctr + kMcGuJ + j, 1u, m.wait_ns, m.err, kErrGuJ)) return;
-
-    const float* yr = m.ygu + ((long long)b * m.topk + j) * 2 * m.inter;
-    for (int blk = warp; blk < nk / 128; blk += kMbWarps) {
-        const int ib = kt0 * 16 + blk * 128 + 4 * lane;
-        const float4 gv = __ldcg(reinterpret_cast<const float4*>(yr + ib));
-        const float4 uv = __ldcg(reinterpret_cast<const float4*>(yr + m.inter + ib));
-        const uint2 rb = blk == warp ? rin_pre : *reinterpret_cast<const uint2*>(rin + ib);
-        float v[4];
-        v[0] = h2f_bits(static_cast<uint16_t>(rb.x & 0xFFFFu)) * (silu_f(gv.x) * uv.x);
-        v[1] = h2f_bits(static_cast<uint16_t>(rb.x >> 16)) * (silu_f(gv.y) * uv.y);
-        v[2] = h2f_bits(static_cast<uint16_t>(rb.y & 0xFFFFu)) * (silu_f(gv.z) * uv.z);
-        v[3] = h2f_bits(static_cast<uint16_t>(rb.y >> 16)) * (silu_f(gv.w) * uv.w);
-        h128_warp(v, lane);
-        *reinterpret_cast<float4*>(xt + blk * 128 + 4 * lane) = make_float4(v[0], v[1], v[2], v[3]);
-    }
-    __syncthreads();
     float* zp = red + kMbWarps * 128;
-    cta_gemv_partial<K, 1, kMbWarps>(codes, grid, ob, kt0, kt1, xt, nk, cur, red, zp);
+    cta_gemv_partial_gx<K, kMbWarps>(codes, grid, ob, kt0, kt1,
+                                     m.xdg + ((long long)b * m.topk + j) * m.inter + kt0 * 16, cur, red, zp);
 
     if (warp == 0) {
         float* part = m.dn_part + (((long long)b * nob + ob) * m.topk) * ks * 128;  // [topk][ks][128] of the block
@@ -577,7 +577,7 @@ __global__ void __launch_bounds__(kMbThreads, 4) moe_multi_kernel(const __grid_c
         } else if (l < m.nR + m.nS + m.nG + m.nX) {
             mb_shared_down(m, B, b, l - m.nR - m.nS - m.nG, sm);
         } else if (l < m.nR + m.nS + m.nG + m.nX + m.nF) {
-            if (mb_routing(m, b, &tk_block, e_s, w_s)) mb_gate_up_finish(m, B, b, l - m.nR - m.nS - m.nG - m.nX, e_s);
+            if (mb_routing(m, b, &tk_block, e_s, w_s)) mb_gate_up_finish(m, B, b, l - m.nR - m.nS - m.nG - m.nX, e_s, sm);
         } else if (l < m.nR + m.nS + m.nG + m.nX + m.nF + m.nD) {
             const int d = l - m.nR - m.nS - m.nG - m.nX - m.nF;
             if (mb_routing(m, b, &tk_block, e_s, w_s)) {
@@ -623,13 +623,17 @@ MbPlan multi_plan(int n_blocks, int hidden, int inter, int E, int topk, int sh_i
     p.nF = topk;
     p.nC = hidden / 128;
     p.U = p.nR + p.nS + p.nG + p.nX + p.nF + p.nD + p.nC;
-    p.xt_floats = (max(sp.gu_kt_per_cta * 16, inter / sp.dn_ksplit) + 31) / 32 * 32;
-    const int unit_floats = max(max(p.xt_floats + (kMbWarps + 1) * 128, hidden), max(sh_inter, hidden / 2));
+    p.xt_floats = (sp.gu_kt_per_cta * 16 + 31) / 32 * 32;
+    // G: xt, the reduction scratch, the partial sums; S: x as floats; X: the
+    // shared SwiGLU; R in a stack: the normalised x; F: one slot's gate_up
+    // outputs
+    const int unit_floats =
+        max(max(p.xt_floats + (kMbWarps + 1) * 128, hidden), max(max(sh_inter, hidden / 2), 2 * inter));
     p.smem = unit_floats * 4;
     const size_t n = n_blocks;
     p.ctr_bytes = (n * kMbCtrWords + 32) * 4;
     p.logits_bytes = n * E * 2;
-    p.ygu_bytes = n * topk * 2 * inter * 4;
+    p.xdg_bytes = n * topk * inter * 4;
     p.shgu_bytes = n * 2 * sh_inter * 4;
     p.shgate_bytes = n * 4;
     p.sh_bytes = n * hidden * 4;

@@ -240,6 +240,47 @@ __device__ __forceinline__ void cta_gemv_partial(const uint16_t* codes, const Ti
     cta_partial_reduce<K, NB, NW>(acc2, red, zp);
 }
 
+// cta_gemv_partial<K, 1, NW> for one token whose transformed inputs xg[nk]
+// (rows kt0..kt1-1) lie in global memory, written by another CTA of the
+// running grid (read through L2): each warp loads the 4 inputs of a tile
+// row together with that row's codes, so no CTA barrier precedes the
+// decode. Same arithmetic and order as cta_gemv_partial<K, 1, NW>.
+template <int K, int NW>
+__device__ __forceinline__ void cta_gemv_partial_gx(const uint16_t* codes, const TileStrides& g, int ob, int kt0, int kt1,
+                                                    const float* xg, LaneCodes<K>& cur, float* red, float* zp) {
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int c = lane & 3;
+    const int nbr = (lane & ~3) | ((lane + 1) & 3);
+    float2 acc2[1][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc2[0][i] = make_float2(0.f, 0.f);
+    auto load_x = [&](int kt) { return __ldcg(reinterpret_cast<const float4*>(xg + (kt - kt0) * 16 + 4 * c)); };
+    auto step = [&](LaneCodes<K>& lc, const float4& xv) {
+        lc.p[2 * K] = __shfl_sync(0xffffffffu, lc.p[0], nbr) & 0xFFFFu;
+        const float xr[1][4] = {{xv.x, xv.y, xv.z, xv.w}};
+        decode_fma<K, 1>(lc, xr, acc2);
+    };
+    LaneCodes<K> nxt;
+    float4 xc = make_float4(0.f, 0.f, 0.f, 0.f), xn = xc;
+    if (kt0 + warp < kt1) xc = load_x(kt0 + warp);
+    for (int kt = kt0 + warp; kt < kt1; kt += 2 * NW) {
+        const bool more1 = kt + NW < kt1;
+        if (more1) {
+            load_lane_codes<K>(nxt, codes, g, kt + NW, ob * 8, lane);
+            xn = load_x(kt + NW);
+        }
+        step(cur, xc);
+        if (!more1) break;
+        if (kt + 2 * NW < kt1) {
+            load_lane_codes<K>(cur, codes, g, kt + 2 * NW, ob * 8, lane);
+            xc = load_x(kt + 2 * NW);
+        }
+        step(nxt, xn);
+    }
+    cta_partial_reduce<K, 1, NW>(acc2, red, zp);
+}
+
 // Output transform of one 128-block by one warp: v holds 4 consecutive
 // values per lane (element 4*lane + j); returns rout * (2^-7 * H128(v)) in v.
 // (Both Hadamards run unscaled; their two 1/sqrt(128) factors make the exact
