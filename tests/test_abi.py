@@ -211,3 +211,52 @@ def test_product_path_has_no_oracle_import():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 src = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in src.replace("the oracle", ""), f"{f} mentions the oracle"
+
+
+def test_sequence_validation_before_launch():
+    """escha_moe_blocks / escha_moe_stack reject their arguments on the host:
+    block counts outside 1..48, null arrays, layers of different shapes,
+    shapes the sequence kernel does not cover, a short workspace, aliasing
+    stack buffers; the workspace query returns 0 for what it cannot size."""
+    native, L = _lib()
+    g = 0x10000
+
+    def layer(hidden=2048, inter=512, sh_inter=0):
+        lay = native.EschaMoeLayer()
+        lay.hidden, lay.inter, lay.n_experts, lay.topk = hidden, inter, 256, 8
+        for f in ("router_w", "gu_codes", "gu_rin", "gu_rout", "dn_codes", "dn_rin", "dn_rout"):
+            setattr(lay, f, g)
+        lay.gu_K, lay.dn_K = 3, 2
+        lay.sh_inter = sh_inter
+        return lay
+
+    def arr(layers):
+        return (ctypes.POINTER(native.EschaMoeLayer) * len(layers))(*[ctypes.pointer(x) for x in layers])
+
+    vp = ctypes.c_void_p
+    ptrs = lambda n, base: (vp * n)(*[base + 0x10000 * i for i in range(n)])
+    two = [layer(), layer()]
+    need = L.escha_moe_seq_workspace(arr(two), 2)
+    assert need > 0
+    assert L.escha_moe_seq_workspace(arr(two), 0) == 0
+    assert L.escha_moe_seq_workspace(arr([layer()] * 49), 49) == 0
+    assert L.escha_moe_seq_workspace(None, 2) == 0
+    blocks = lambda layers, n, x, out, ws_bytes: L.escha_moe_blocks(
+        arr(layers) if layers is not None else None, n, x, out, None, None, g, ws_bytes, None)
+    x2, o2 = ptrs(2, 0x1000000), ptrs(2, 0x2000000)
+    assert blocks(two, 0, x2, o2, need) == native.ESCHA_E_ARG
+    assert blocks([layer()] * 49, 49, ptrs(49, 0x1000000), ptrs(49, 0x4000000), 1 << 40) == native.ESCHA_E_ARG
+    assert blocks(None, 2, x2, o2, need) == native.ESCHA_E_ARG
+    assert blocks(two, 2, None, o2, need) == native.ESCHA_E_ARG
+    assert blocks(two, 2, x2, None, need) == native.ESCHA_E_ARG
+    assert blocks([layer(), layer(inter=256)], 2, x2, o2, need) == native.ESCHA_E_SHAPE
+    assert blocks([layer(hidden=4096), layer(hidden=4096)], 2, x2, o2, 1 << 40) == native.ESCHA_E_SHAPE
+    assert blocks(two, 2, x2, o2, need - 1) == native.ESCHA_E_WORKSPACE
+    stack = lambda layers, n, h, xb, ob, ws_bytes: L.escha_moe_stack(arr(layers), n, h, 1e-6, xb, ob, None, None, g,
+                                                                   ws_bytes, None)
+    h, xb, ob = 0x100000, 0x200000, 0x300000
+    assert stack(two, 2, None, xb, ob, need) == native.ESCHA_E_ARG
+    assert stack(two, 2, h, xb, h + 4096, need) == native.ESCHA_E_ARG  # out_buf inside h
+    assert stack(two, 2, h + 4, xb, ob, need) == native.ESCHA_E_ALIGN
+    assert stack(two, 0, h, xb, ob, need) == native.ESCHA_E_ARG
+    assert L.escha_moe_stack(arr(two), 2, h, -1.0, xb, ob, None, None, g, need, None) == native.ESCHA_E_ARG
