@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
@@ -82,6 +83,8 @@ size_t align_up(size_t v) { return (v + 255) & ~size_t(255); }
 // router kernel plus the cooperative expert kernel, or an error where that
 // path does not apply) and the cooperative kernel's wait limit and test hook.
 std::atomic<int> g_moe_route_mode{0};
+// escha_moe_blocks: 0 = by shape, 1 = the per-slot kernels over all blocks, 2 = the sequence kernel
+std::atomic<int> g_blocks_route{0};
 std::atomic<long long> g_fz_wait_ns{2000000000ll};
 std::atomic<int> g_fz_skip_publish{0};
 
@@ -811,11 +814,64 @@ escha::MbArgs seq_args(const escha_moe_layer* const* layers, int n, const escha:
 
 extern "C" {
 
+// Independent one-token blocks on the per-slot kernels (one launch of each
+// over all blocks' slots, token t running layer t): up to kMlMaxT blocks of
+// one shape and one K pair, hidden <= 2048. Workspace: the per-slot path's
+// for T = n, then the layer table.
+bool ml_covers(const escha_moe_layer* const* layers, int n) {
+    if (n < 1 || n > escha::kMlMaxT || layers[0]->hidden > 2048) return false;
+    for (int i = 1; i < n; ++i)
+        if (layers[i]->gu_K != layers[0]->gu_K || layers[i]->dn_K != layers[0]->dn_K) return false;
+    return true;
+}
+size_t ml_table_offset(const escha_moe_layer* L, int n) { return align_up(moe_ws_layout(L, n).total); }
+size_t ml_ws_bytes(const escha_moe_layer* L, int n) {
+    return ml_table_offset(L, n) + align_up((size_t)n * sizeof(escha::MoeLayerPtrs));
+}
+
+int ml_blocks(const escha_moe_layer* const* layers, int n, const uint16_t* const* x, float* const* out,
+              int32_t* const* ids_out, float* const* w_out, void* ws, int sms, cudaStream_t s) {
+    const escha_moe_layer* L = layers[0];
+    char* base = static_cast<char*>(ws);
+    const MoeWs m = moe_ws_layout(L, n);
+    escha::MoeArgs a = moe_args(L, x[0], n, out[0], nullptr, nullptr, base, m);
+    a.fz_ctr = nullptr;
+    a.lay = reinterpret_cast<escha::MoeLayerPtrs*>(base + ml_table_offset(L, n));
+    a.lay_n = n;
+    escha::MlTable tab{};
+    for (int i = 0; i < n; ++i) {
+        const escha_moe_layer* Li = layers[i];
+        escha::MoeLayerPtrs& t = tab.l[i];
+        t.router_w = Li->router_w;
+        t.gu_codes = Li->gu_codes;
+        t.gu_rin = Li->gu_rin;
+        t.gu_rout = Li->gu_rout;
+        t.dn_codes = Li->dn_codes;
+        t.dn_rin = Li->dn_rin;
+        t.dn_rout = Li->dn_rout;
+        t.sh_gu_w8 = Li->sh_gu_w8;
+        t.sh_gu_scale = Li->sh_gu_scale;
+        t.sh_dn_w8 = Li->sh_dn_w8;
+        t.sh_dn_scale = Li->sh_dn_scale;
+        t.sh_gate = Li->sh_gate;
+        t.x = x[i];
+        t.out = out[i];
+        t.ids = ids_out ? ids_out[i] : nullptr;
+        t.w = w_out ? w_out[i] : nullptr;
+    }
+    int r;
+    if ((r = cuda_status(escha::launch_moe_router_ml(a, tab, s), "router launch"))) return r;
+    if ((r = cuda_status(escha::launch_moe_gate_up(a, sms, s), "gate_up launch"))) return r;
+    return cuda_status(escha::launch_moe_down(a, sms, s), "down/combine launch");
+}
+
 size_t escha_moe_seq_workspace(const escha_moe_layer* const* layers, int n_blocks) {
     if (!layers || n_blocks < 1 || n_blocks > escha::kMbMaxBlocks || !layers[0]) return 0;
     const escha_moe_layer* L = layers[0];
     if (L->topk < 1 || L->n_experts < 1) return 0;
-    return seq_ws_layout(escha::multi_plan(n_blocks, L->hidden, L->inter, L->n_experts, L->topk, L->sh_inter)).total;
+    size_t need = seq_ws_layout(escha::multi_plan(n_blocks, L->hidden, L->inter, L->n_experts, L->topk, L->sh_inter)).total;
+    if (n_blocks <= escha::kMlMaxT) need = std::max(need, ml_ws_bytes(L, n_blocks));
+    return need;
 }
 
 int escha_moe_blocks(const escha_moe_layer* const* layers, int n_blocks, const uint16_t* const* x, float* const* out,
@@ -831,10 +887,17 @@ int escha_moe_blocks(const escha_moe_layer* const* layers, int n_blocks, const u
             return fail(ESCHA_E_ALIGN, "moe_blocks: block %d: x / out not 16-byte or ids / w not 4-byte aligned", i);
     }
     const SeqWs w = seq_ws_layout(p);
-    if (!ws || ws_bytes < w.total) return fail(ESCHA_E_WORKSPACE, "moe_blocks: workspace %zu bytes, need %zu", ws_bytes, w.total);
+    const size_t need = escha_moe_seq_workspace(layers, n_blocks);
+    if (!ws || ws_bytes < need) return fail(ESCHA_E_WORKSPACE, "moe_blocks: workspace %zu bytes, need %zu", ws_bytes, need);
     if (!aligned16(ws)) return fail(ESCHA_E_ALIGN, "moe_blocks: workspace not 16-byte aligned");
     int sms, grid;
     if ((r = device_check(&sms))) return r;
+    const int route = g_blocks_route.load();
+    const bool ml = ml_covers(layers, n_blocks);
+    if (route == 1 && !ml)
+        return fail(ESCHA_E_SHAPE, "moe_blocks: the per-slot route takes up to %d blocks with one K pair", escha::kMlMaxT);
+    if (ml && route != 2)
+        return ml_blocks(layers, n_blocks, x, out, ids_out, w_out, ws, sms, static_cast<cudaStream_t>(stream));
     if ((r = seq_grid(sms, p.smem, &grid))) return r;
     escha::MbArgs m = seq_args(layers, n_blocks, p, static_cast<char*>(ws), w);
     seq_segments(m, n_blocks, p, false);
@@ -923,6 +986,22 @@ int escha_moe_block_path(const escha_moe_layer* L, int T) {
     FusedRoute fr{};
     if ((r = fused_route(L, T, sms, &fr))) return r;
     return fr.use ? ESCHA_PATH_FUSED : ESCHA_PATH_SLOT;
+}
+
+int escha_debug_set_blocks_route(int mode) {
+    if (mode < 0 || mode > 2) return fail(ESCHA_E_ARG, "escha_debug_set_blocks_route: mode %d not in 0..2", mode);
+    g_blocks_route.store(mode);
+    return ESCHA_OK;
+}
+
+int escha_moe_blocks_path(const escha_moe_layer* const* layers, int n_blocks) {
+    escha::MbPlan p{};
+    int r = seq_check(layers, n_blocks, "moe_blocks_path", &p);
+    if (r) return r;
+    const int route = g_blocks_route.load();
+    const bool ml = ml_covers(layers, n_blocks);
+    if (route == 1 && !ml) return fail(ESCHA_E_SHAPE, "moe_blocks_path: the per-slot route does not cover these blocks");
+    return ml && route != 2 ? ESCHA_PATH_SLOT : ESCHA_PATH_SEQUENCE;
 }
 
 int escha_debug_set_moe_route(int mode) {

@@ -63,6 +63,32 @@ cudaError_t launch_int8_gemm(const int8_t* W, const float* scales, int N, int Ki
 // kernel waits for its predecessor with griddepcontrol.wait).
 cudaError_t launch_kernel(const void* f, dim3 grid, dim3 block, int smem, bool pdl, cudaStream_t s, void** args);
 
+// One token's layer in a multi-layer per-slot launch: independent one-token
+// blocks of one shape (and one K pair), token t running layer t, each with
+// its own input and outputs.
+struct MoeLayerPtrs {
+    const uint16_t* router_w;
+    const uint16_t* gu_codes;
+    const uint16_t* gu_rin;
+    const uint16_t* gu_rout;
+    const uint16_t* dn_codes;
+    const uint16_t* dn_rin;
+    const uint16_t* dn_rout;
+    const int8_t* sh_gu_w8;
+    const float* sh_gu_scale;
+    const int8_t* sh_dn_w8;
+    const float* sh_dn_scale;
+    const uint16_t* sh_gate;
+    const uint16_t* x;  // fp16 [hidden]
+    float* out;         // [hidden]
+    int32_t* ids;       // [topk]
+    float* w;           // [topk]
+};
+constexpr int kMlMaxT = 16;  // blocks of one multi-layer launch (the per-slot path's token limit)
+struct MlTable {
+    MoeLayerPtrs l[kMlMaxT];
+};
+
 // Everything the three MoE-block kernels read and write.
 struct MoeArgs {
     int T, hidden, inter, E, topk, sh_inter;
@@ -122,6 +148,11 @@ struct MoeArgs {
     float* fz_dres;     // unused (the finishing CTA keeps the experts' outputs in shared memory)
     long long fz_wait_ns;   // a wait on another CTA gives up after this long
     int fz_skip_publish;    // test hook: the gate_up outputs are never published, so every wait on them gives up
+    // multi-layer per-slot launch: token t's layer, input and outputs (in the
+    // workspace, written by the router kernel; null: one layer, x, out, ids
+    // and w as above)
+    MoeLayerPtrs* lay;
+    int lay_n;  // entries of lay (the launch's tokens)
 };
 
 // Largest token count of a grouped work item, and the largest batch that
@@ -186,6 +217,11 @@ cudaError_t launch_residual_rmsnorm(float* h, const float* add, int T, int hidde
 // with_shared (per-slot path): the same grid also computes the shared
 // expert's gate_up rows and gate
 cudaError_t launch_moe_router(const MoeArgs& a, bool with_shared, cudaStream_t s);
+// Multi-layer per-slot launch (a.lay set, a.T = blocks <= kMlMaxT, hidden <=
+// 2048): token t's router logits and shared-expert gate_up rows with layer
+// t's weights; CTA (0, 0) also stores the table at a.lay for the gate_up and
+// down kernels.
+cudaError_t launch_moe_router_ml(const MoeArgs& a, const MlTable& tab, cudaStream_t s);
 cudaError_t launch_moe_gate_up(const MoeArgs& a, int num_sms, cudaStream_t s);
 
 // One token, two kernels: the per-slot router kernel (logits, the shared

@@ -124,10 +124,11 @@ __device__ void resid_norm_cta(const MoeArgs& a, int t0, int nt, uint16_t* xh) {
 // FUSED (residual block, <= kFusedNormMaxT tokens, hidden <= 2048): x is
 // computed by resid_norm_cta into xh (shared memory) after the wait, and CTA
 // x = 0 also stores it as the block's x for the later kernels.
+// t0: the CTA's first token (of a.T); tab (multi-layer launch): the table
+// CTA (0, 0) stores at a.lay once the preceding kernel has finished.
 template <bool FUSED>
-__device__ void router_logits(const MoeArgs& a, int warp, int lane, uint16_t* xh) {
+__device__ void router_logits(const MoeArgs& a, int warp, int lane, uint16_t* xh, int t0, const MlTable* tab) {
     const int e = blockIdx.x * kK0Warps + warp;
-    const int t0 = blockIdx.y * kLgTG;
     const int nt = min(kLgTG, a.T - t0);
     const uint16_t* wrow = a.router_w + (long long)(e < a.E ? e : 0) * a.hidden;
     const int passes = a.hidden >> 8;
@@ -145,6 +146,9 @@ __device__ void router_logits(const MoeArgs& a, int warp, int lane, uint16_t* xh
             pdl_wait();
             if (blockIdx.x == 0 && blockIdx.y == 0) {  // the previous call has finished
                 if (threadIdx.x == 0) *a.err = 0;
+                if (tab)
+                    for (int i = threadIdx.x; i < a.lay_n * static_cast<int>(sizeof(MoeLayerPtrs) / 8); i += kK0Threads)
+                        reinterpret_cast<unsigned long long*>(a.lay)[i] = reinterpret_cast<const unsigned long long*>(tab->l)[i];
                 // one token on the fused path: the expert kernel's counters start at zero
                 if (a.fz_ctr)
                     for (int i = threadIdx.x; i < kFzCtrWords; i += kK0Threads) a.fz_ctr[i] = 0u;
@@ -571,7 +575,8 @@ __global__ void __launch_bounds__(kK0Threads) moe_router_kernel(const MoeArgs a,
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     static_assert(!FUSED || MT <= kFusedNormMaxT, "the residual norm runs in the router grid for few tokens only");
     if (static_cast<int>(blockIdx.x) < n_lg) {
-        router_logits<FUSED>(a, warp, lane, xh);  // waits for the preceding kernel after its first weight loads
+        // waits for the preceding kernel after its first weight loads
+        router_logits<FUSED>(a, warp, lane, xh, static_cast<int>(blockIdx.y) * kLgTG, nullptr);
         return;
     }
     if (blockIdx.y != 0) return;
@@ -585,6 +590,34 @@ __global__ void __launch_bounds__(kK0Threads) moe_router_kernel(const MoeArgs a,
     } else {
         shared_gate_up_staged<kK0Warps, MT>(a, cta, xs_sh, warp, lane);
     }
+}
+
+// Multi-layer per-slot launch: row y of the grid is token y, with its own
+// layer. Its CTAs run the one-token code on a view of the arguments that
+// holds that layer's weights and input and that token's outputs, so every
+// logit, shared-expert row and gate has the one-token (and the one-layer
+// multi-token) summation order.
+__global__ void __launch_bounds__(kK0Threads) moe_router_ml_kernel(const MoeArgs a, int n_lg,
+                                                                   const __grid_constant__ MlTable tab) {
+    pdl_trigger();
+    const int t = static_cast<int>(blockIdx.y);
+    const MoeLayerPtrs& L = tab.l[t];
+    MoeArgs la = a;
+    la.T = 1;
+    la.x = L.x;
+    la.router_w = L.router_w;
+    la.sh_gu_w8 = L.sh_gu_w8;
+    la.sh_gu_scale = L.sh_gu_scale;
+    la.sh_gate = L.sh_gate;
+    la.logits = a.logits + (long long)t * a.E;
+    la.shgu = a.shgu + (long long)t * 2 * a.sh_inter;
+    la.shgate = a.shgate + t;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (static_cast<int>(blockIdx.x) < n_lg) {
+        router_logits<false>(la, warp, lane, nullptr, 0, &tab);
+        return;
+    }
+    shared_gate_up_direct<1, false>(la, static_cast<int>(blockIdx.x) - n_lg, warp, lane, nullptr);
 }
 
 // Router logits for many tokens: a CTA stages 16 tokens of x in shared memory
@@ -678,9 +711,10 @@ __device__ void gate_up_routed(const MoeArgs& a, float* smem) {
     // x may still be written by the kernel before the router (this grid can
     // start while it runs): its loads go out right after the wait, beside
     // the logits' (only rin depends on the routing)
-    const uint16_t* xrow = a.x + (long long)t * a.hidden;
-    pdl_wait();     // router logits
+    pdl_wait();     // router logits (and, in a multi-layer launch, the layer table)
     pdl_trigger();  // logits complete: the down kernel may read them early
+    const MoeLayerPtrs* ly = a.lay ? a.lay + t : nullptr;  // token t's layer (multi-layer launch)
+    const uint16_t* xrow = ly ? ly->x : a.x + (long long)t * a.hidden;
     uint2 x_pre = make_uint2(0u, 0u);
     if (warp < nk / 128) x_pre = *reinterpret_cast<const uint2*>(xrow + kt0 * 16 + warp * 128 + 4 * lane);
     if (warp == 0) {
@@ -691,8 +725,10 @@ __device__ void gate_up_routed(const MoeArgs& a, float* smem) {
             e_s[lane] = e_l;
             w_s[lane] = w_l;
             if (crank == 0 && ob == 0 && j == 0) {  // one CTA per token publishes the routing
-                a.ids[(long long)t * a.topk + lane] = e_l;
-                a.w[(long long)t * a.topk + lane] = w_l;
+                int32_t* ids = ly && ly->ids ? ly->ids : a.ids + (long long)t * a.topk;
+                float* ws = ly && ly->w ? ly->w : a.w + (long long)t * a.topk;
+                ids[lane] = e_l;
+                ws[lane] = w_l;
             }
         }
     } else if (a.rs_h && a.rs_add && crank == 0 && ob == 0 && j == 0) {
@@ -709,13 +745,13 @@ __device__ void gate_up_routed(const MoeArgs& a, float* smem) {
     }
     __syncthreads();
     const int e = e_s[j];
-    const uint16_t* codes = a.gu_codes + (long long)e * KT * NT * (16 * K);
+    const uint16_t* codes = (ly ? ly->gu_codes : a.gu_codes) + (long long)e * KT * NT * (16 * K);
     LaneCodes<K> cur;
     const TileStrides grid{NT, 1};  // experts are stored kt-major
     if (kt0 + warp < kt1) load_lane_codes<K>(cur, codes, grid, kt0 + warp, ob * 8, lane);
 
     // xt = H128(rin_e * x[t]) over this CTA's inputs
-    const uint16_t* rin = a.gu_rin + (long long)e * a.hidden;
+    const uint16_t* rin = (ly ? ly->gu_rin : a.gu_rin) + (long long)e * a.hidden;
     for (int blk = warp; blk < nk / 128; blk += kGuWarps) {
         const int ib = kt0 * 16 + blk * 128 + 4 * lane;
         const uint2 rb = *reinterpret_cast<const uint2*>(rin + ib);
@@ -731,7 +767,8 @@ __device__ void gate_up_routed(const MoeArgs& a, float* smem) {
     __syncthreads();
     uint2 rout_pre = make_uint2(0u, 0u);  // rank 0's output scales, fetched while the loop runs
     if (crank == 0 && warp == 0)
-        rout_pre = *reinterpret_cast<const uint2*>(a.gu_rout + (long long)e * n_out + ob * 128 + 4 * lane);
+        rout_pre = *reinterpret_cast<const uint2*>((ly ? ly->gu_rout : a.gu_rout) + (long long)e * n_out + ob * 128 +
+                                                   4 * lane);
     float* zp = crank == 0 ? slots : red + kGuWarps * 128;  // rank 0 keeps its partial in slot 0
     cta_gemv_partial<K, 1, kGuWarps>(codes, grid, ob, kt0, kt1, xt, nk, cur, red, zp);
 
@@ -781,6 +818,11 @@ __global__ void __launch_bounds__(kDnThreads, MINB) moe_down_kernel(const MoeArg
     const int j = rank / ks, h = rank % ks;
     const int ob = blockIdx.y;
     const int t = blockIdx.z;
+    // token t's layer in a multi-layer launch (the table was stored by the
+    // router kernel, which finished before this grid was scheduled, as the
+    // logits read below)
+    const MoeLayerPtrs* ly = a.lay ? a.lay + t : nullptr;
+    const int8_t* sh_dn_w8 = ly ? ly->sh_dn_w8 : a.sh_dn_w8;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     extern __shared__ __align__(16) float smem[];
     float* slots = smem;                      // [csz][128] partials, on rank 0
@@ -805,7 +847,7 @@ __global__ void __launch_bounds__(kDnThreads, MINB) moe_down_kernel(const MoeArg
     for (int i = 0; i < 2; ++i) {
         const int rr = warp + kDnWarps * i, row = rank * sh_per + rr;
         if (a.sh_inter > 0 && a.sh_inter <= 512 && rr < sh_per && row < 128 && lane * 16 < a.sh_inter)
-            shw[i] = ldg_stream_v4(a.sh_dn_w8 + (long long)(ob * 128 + row) * a.sh_inter + lane * 16);
+            shw[i] = ldg_stream_v4(sh_dn_w8 + (long long)(ob * 128 + row) * a.sh_inter + lane * 16);
     }
 
     const int slot = t * a.topk + j;
@@ -826,11 +868,11 @@ __global__ void __launch_bounds__(kDnThreads, MINB) moe_down_kernel(const MoeArg
     const int rows_h = KT / ks;  // whole Hadamard blocks per input split
     const int kt0 = h * rows_h, kt1 = kt0 + rows_h;
     const int nk = rows_h * 16;
-    const uint16_t* codes = a.dn_codes + (long long)e * KT * NT * (16 * K);
+    const uint16_t* codes = (ly ? ly->dn_codes : a.dn_codes) + (long long)e * KT * NT * (16 * K);
     LaneCodes<K> cur;
     const TileStrides grid{NT, 1};  // experts are stored kt-major
     if (kt0 + warp < kt1) load_lane_codes<K>(cur, codes, grid, kt0 + warp, ob * 8, lane);
-    const uint16_t* rin = a.dn_rin + (long long)e * a.inter;
+    const uint16_t* rin = (ly ? ly->dn_rin : a.dn_rin) + (long long)e * a.inter;
     uint2 rin_pre = make_uint2(0u, 0u);
     if (warp < nk / 128) rin_pre = *reinterpret_cast<const uint2*>(rin + kt0 * 16 + warp * 128 + 4 * lane);
     pdl_wait();  // gate_up outputs and the shared expert's gate_up
@@ -881,7 +923,8 @@ __global__ void __launch_bounds__(kDnThreads, MINB) moe_down_kernel(const MoeArg
     __syncthreads();
     uint2 rout_pre = make_uint2(0u, 0u);  // rank 0: every expert's output scales, fetched while the loop runs
     if (rank == 0 && warp < a.topk)
-        rout_pre = *reinterpret_cast<const uint2*>(a.dn_rout + (long long)e_s[warp] * a.hidden + ob * 128 + 4 * lane);
+        rout_pre = *reinterpret_cast<const uint2*>((ly ? ly->dn_rout : a.dn_rout) + (long long)e_s[warp] * a.hidden +
+                                                   ob * 128 + 4 * lane);
     float* zp = rank == 0 ? slots : red + kDnWarps * 128;
     cta_gemv_partial<K, 1, kDnWarps>(codes, grid, ob, kt0, kt1, xt, nk, cur, red, zp);
 
@@ -916,11 +959,11 @@ __global__ void __launch_bounds__(kDnThreads, MINB) moe_down_kernel(const MoeArg
                 dot = acc;
             } else {
                 float d1[1][1];
-                int8_rows_dot<1, 1, 4>(a.sh_dn_w8 + (long long)(ob * 128 + sh_row) * n_sh, n_sh, 1, n_sh, xsh, n_sh, lane,
+                int8_rows_dot<1, 1, 4>(sh_dn_w8 + (long long)(ob * 128 + sh_row) * n_sh, n_sh, 1, n_sh, xsh, n_sh, lane,
                                        d1);
                 dot = d1[0][0];
             }
-            const float sh_val = gate * (a.sh_dn_scale[ob * 128 + sh_row] * dot);
+            const float sh_val = gate * ((ly ? ly->sh_dn_scale : a.sh_dn_scale)[ob * 128 + sh_row] * dot);
             if (lane == 0) {
                 if (rank == 0) {
                     shres[sh_row] = sh_val;
@@ -968,7 +1011,7 @@ __global__ void __launch_bounds__(kDnThreads, MINB) moe_down_kernel(const MoeArg
         float sum = 0.f;
         for (int q = 0; q < a.topk; ++q) sum += dres[q * 128 + i];
         if (a.sh_inter > 0) sum += shres[i];
-        a.out[(long long)t * a.hidden + ob * 128 + i] = sum;
+        (ly ? ly->out : a.out + (long long)t * a.hidden)[ob * 128 + i] = sum;
     }
 }
 
@@ -1110,6 +1153,24 @@ cudaError_t launch_moe_router(const MoeArgs& a, bool with_shared, cudaStream_t s
     cfg.numAttrs = 1;
     void* args[] = {const_cast<MoeArgs*>(&a), &n_lg};
     return cudaLaunchKernelExC(&cfg, f, args);
+}
+
+cudaError_t launch_moe_router_ml(const MoeArgs& a, const MlTable& tab, cudaStream_t s) {
+    int n_lg = (a.E + kK0Warps - 1) / kK0Warps;
+    const int rows_per_cta = kK0Warps * kShRowsPerWarp;
+    const int n_sh = a.sh_inter > 0 ? (2 * a.sh_inter + rows_per_cta - 1) / rows_per_cta : 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(n_lg + n_sh, a.T);
+    cfg.blockDim = dim3(kK0Threads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void* args[] = {const_cast<MoeArgs*>(&a), &n_lg, const_cast<MlTable*>(&tab)};
+    return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(moe_router_ml_kernel), args);
 }
 
 cudaError_t launch_moe_gate_up(const MoeArgs& a, int num_sms, cudaStream_t s) {

@@ -30,6 +30,7 @@ ESCHA_E_IO = -9
 ESCHA_PATH_FUSED = 1
 ESCHA_PATH_SLOT = 2
 ESCHA_PATH_GROUPED = 3
+ESCHA_PATH_SEQUENCE = 4
 
 ESCHA_F16 = 1
 ESCHA_BF16 = 2
@@ -60,6 +61,8 @@ EXPORTS = [
     "escha_moe_blocks",
     "escha_moe_stack",
     "escha_moe_block_path",
+    "escha_moe_blocks_path",
+    "escha_debug_set_blocks_route",
     "escha_debug_set_moe_route",
     "escha_debug_set_fused_wait",
     "escha_moe_route_workspace",
@@ -187,6 +190,10 @@ def lib() -> ctypes.CDLL:
         L.escha_moe_stack.restype = _i
         L.escha_moe_block_path.argtypes = [ctypes.POINTER(EschaMoeLayer), _i]
         L.escha_moe_block_path.restype = _i
+        L.escha_moe_blocks_path.argtypes = [_lp, _i]
+        L.escha_moe_blocks_path.restype = _i
+        L.escha_debug_set_blocks_route.argtypes = [_i]
+        L.escha_debug_set_blocks_route.restype = _i
         L.escha_debug_set_moe_route.argtypes = [_i]
         L.escha_debug_set_moe_route.restype = _i
         L.escha_debug_set_fused_wait.argtypes = [ctypes.c_longlong, _i]
@@ -212,6 +219,12 @@ def set_moe_route(mode: int) -> None:
     """Diagnostic: 0 = one-token blocks run the fused single kernel where it
     applies, 1 = always the three per-slot kernels, 2 = always the fused one."""
     check(lib().escha_debug_set_moe_route(int(mode)))
+
+
+def set_blocks_route(mode: int = 0) -> None:
+    """Diagnostic: escha_moe_blocks by shape (0), forced onto the per-slot
+    kernels over all blocks (1) or onto the sequence kernel (2)."""
+    check(lib().escha_debug_set_blocks_route(int(mode)))
 
 
 def set_fused_wait(wait_ns: int = 2_000_000_000, skip_publish: bool = False) -> None:
@@ -646,8 +659,17 @@ def seq_workspace_bytes(blocks) -> int:
     return lib().escha_moe_seq_workspace(_layer_array(blocks), len(blocks))
 
 
+def blocks_path(blocks) -> int:
+    """ESCHA_PATH_SLOT or ESCHA_PATH_SEQUENCE: the kernels moe_blocks runs
+    these blocks on (with the route setting)."""
+    r = lib().escha_moe_blocks_path(_layer_array(blocks), len(blocks))
+    if r < 0:
+        check(r)
+    return r
+
+
 def moe_blocks(blocks, xs, outs, ids=None, w=None, ws=None, stream=None):
-    """Independent one-token blocks in one launch: block i of ``blocks``
+    """Independent one-token blocks in few launches: block i of ``blocks``
     (MoeBlock) on xs[i] (fp16 [hidden] or [1][hidden]) into outs[i] (f32).
     ``ids`` / ``w``: optional lists of per-block [topk] tensors. ``ws``: a
     workspace of at least seq_workspace_bytes(blocks) bytes."""

@@ -329,25 +329,41 @@ int escha_moe_block_resid(const escha_moe_layer* L, float* h, const float* add, 
 int escha_moe_block_timed(const escha_moe_layer* L, const uint16_t* x, int T, float* out, int32_t* ids_out,
                           float* w_out, void* ws, size_t ws_bytes, void* stream, void* const* events);
 
-/* ---- a sequence of one-token blocks in one launch ---------------------
+/* ---- many one-token blocks in few launches ----------------------------
  * The decode step of a model runs its MoE blocks one after another for one
  * token. Launched one block at a time, each block pays its kernels' grid
- * boundaries, which at one token cost more than the decode itself. These two
- * calls run up to 48 blocks in ONE cooperative launch (every CTA resident):
- * the CTAs take work units (router rows, the shared expert's rows, gate_up
- * and down pieces of each routed expert) from one queue and hand results to
- * each other through counters in the workspace; every wait is bounded (the
- * status word reports a wait that ran out; see escha_debug_set_fused_wait).
- * Every block gives bit for bit the outputs of escha_moe_block (per-slot
- * kernels) on the same input. The layers must share hidden (a multiple of
- * 256, <= 2048), inter (2*inter/128 <= 32), n_experts, topk and sh_inter
- * (<= 512); gu_K / dn_K may differ per layer. ESCHA_E_SHAPE otherwise.
+ * boundaries, which at one token cost more than the decode itself. The
+ * layers must share hidden (a multiple of 256, <= 2048), inter (2*inter/128
+ * <= 32), n_experts, topk and sh_inter (<= 512); ESCHA_E_SHAPE otherwise.
  *
  * escha_moe_blocks: independent blocks, block i on its own token:
  *   x[i] fp16 [hidden] -> out[i] f32 [hidden]; ids_out / w_out: arrays of
  *   per-block [topk] outputs, or NULL (either the array or an entry).
- *   A block's router and gate_up work overlaps the previous block's down.
- * escha_moe_stack: a residual stack, the blocks of one decode step:
+ *   Up to 16 blocks whose layers share gu_K and dn_K run on the per-slot
+ *   kernels (ESCHA_PATH_SLOT): one launch each of the router, gate_up and
+ *   down/combine kernels over every block's slots, token t with layer t,
+ *   exactly as escha_moe_block runs n tokens of one layer (so n copies of
+ *   one layer give bit for bit escha_moe_block's output for those n
+ *   tokens); the input splits are those of n tokens, so the bits differ
+ *   from n one-token calls (within the block's tolerance). Otherwise
+ *   (more blocks, or K differing between layers) the blocks run in the
+ *   sequence kernel below (ESCHA_PATH_SEQUENCE), where every block gives bit
+ *   for bit escha_moe_block's one-token output; a block's router and
+ *   gate_up work overlaps the previous block's down.
+ *   escha_moe_blocks_path tells which (or a negative error code);
+ *   escha_debug_set_blocks_route(0 by shape, 1 per-slot kernels (ESCHA_E_SHAPE
+ *   when they do not cover the blocks), 2 sequence kernel) forces one, for
+ *   tests (process-wide, read when a call is enqueued).
+ *
+ * The sequence kernel runs up to 48 blocks in ONE cooperative launch (every
+ * CTA resident): the CTAs take work units (router rows, the shared expert's
+ * rows, gate_up and down pieces of each routed expert) from one queue and
+ * hand results to each other through counters in the workspace; every wait
+ * is bounded (the status word reports a wait that ran out; see
+ * escha_debug_set_fused_wait). gu_K / dn_K may differ per layer.
+ *
+ * escha_moe_stack: a residual stack, the blocks of one decode step, in the
+ * sequence kernel:
  *   for each block i: h += out_buf (i > 0), x_buf = fp16 RMSNorm(h) (the
  *   weightless norm of escha_residual_rmsnorm, same arithmetic), out_buf =
  *   block_i(x_buf); at the end h += out_buf. The same h, x_buf and out_buf
@@ -359,6 +375,8 @@ int escha_moe_block_timed(const escha_moe_layer* L, const uint16_t* x, int T, fl
  * Workspace: escha_moe_seq_workspace(layers, n_blocks) bytes (independent of
  * the call's kind); nothing in it has to start at zero. */
 size_t escha_moe_seq_workspace(const escha_moe_layer* const* layers, int n_blocks);
+int escha_moe_blocks_path(const escha_moe_layer* const* layers, int n_blocks);
+int escha_debug_set_blocks_route(int mode);
 int escha_moe_blocks(const escha_moe_layer* const* layers, int n_blocks, const uint16_t* const* x, float* const* out,
                      int32_t* const* ids_out, float* const* w_out, void* ws, size_t ws_bytes, void* stream);
 int escha_moe_stack(const escha_moe_layer* const* layers, int n_blocks, float* h, float eps, uint16_t* x_buf,
@@ -373,6 +391,7 @@ int escha_moe_stack(const escha_moe_layer* const* layers, int n_blocks, float* h
 #define ESCHA_PATH_FUSED 1
 #define ESCHA_PATH_SLOT 2
 #define ESCHA_PATH_GROUPED 3
+#define ESCHA_PATH_SEQUENCE 4
 int escha_moe_block_path(const escha_moe_layer* L, int T);
 
 /* Diagnostic exports (tests and measurements; not part of the hot path).

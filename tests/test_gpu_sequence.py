@@ -18,12 +18,17 @@ pytestmark = pytest.mark.gpu
 
 @pytest.fixture(scope="module")
 def native():
+    """These tests run the sequence kernel: escha_moe_blocks is held on it
+    (independent blocks of up to 16 would otherwise take the per-slot
+    kernels, tested in test_gpu_blocks.py)."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from bit_trellis_quantized_gb300 import native as n
 
     n.lib()
+    n.set_blocks_route(2)
     yield n
+    n.set_blocks_route(0)
     n.set_fused_wait()
 
 
