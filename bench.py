@@ -8,8 +8,10 @@ experts change). One step = one MoE block forward of one token: router
 (logits, top-8, softmax), input Hadamard transforms, fused trellis decode
 GEMVs for gate_up and down, output transforms, SwiGLU, the int8 shared expert
 and the combine, all in the library's kernels behind the C ABI, replayed from
-a CUDA graph of 8 steps, which run as one launch of the sequence kernel
-(escha_moe_blocks; --path per-slot: one escha_moe_block call per step).
+a CUDA graph of 8 steps, which run as one escha_moe_blocks call: one launch
+each of the router, gate_up and down/combine kernels over the 8 blocks'
+slots (--path sequence: the same call held on the one-launch sequence kernel;
+--path per-slot: one escha_moe_block call per step).
 
 L2: inputs larger than L2. The benchmark cycles through 24 distinct layers of
 this shape (about 6.5 GB of weights), one layer per step, so a step's weights
@@ -83,9 +85,10 @@ BLOCK_BYTES = (TOPK * (GU_CODE_BYTES + DN_CODE_BYTES + (HIDDEN + 2 * INTER) * 2 
                + HIDDEN * 2 + HIDDEN * 4)
 
 
-def _profile_record(name: str):
-    """A committed ncu figure (profiles/<name>.json), or None when the kernel
-    sources it depends on changed since the capture."""
+def _profile_record(name: str, mode=None):
+    """A committed ncu figure (profiles/<name>.json) of the bench mode `mode`,
+    or None when it is another mode's or the kernel sources it depends on
+    changed since the capture."""
     import hashlib
 
     p = os.path.join(ROOT, "profiles", name + ".json")
@@ -93,6 +96,8 @@ def _profile_record(name: str):
         return None
     with open(p) as f:
         rec = json.load(f)
+    if rec.get("mode") != mode:
+        return None
     h = hashlib.sha256()
     for src in rec["sources"]:
         with open(os.path.join(ROOT, "bit_trellis_quantized_gb300", "csrc", src), "rb") as f:
@@ -100,18 +105,19 @@ def _profile_record(name: str):
     return rec if h.hexdigest() == rec["sources_sha256"] else None
 
 
-def measured_traffic():
-    """DRAM bytes per launch of the batch-1 block's kernel from the committed
-    ncu capture, or None when the kernel sources changed since the capture."""
-    rec = _profile_record("traffic")
+def measured_traffic(mode=None):
+    """DRAM bytes per launch of the batch-1 block's dominant kernel in bench
+    mode `mode` from the committed ncu capture, or None (another mode's, or
+    the kernel sources changed since the capture)."""
+    rec = _profile_record("traffic", mode)
     return rec["dram_bytes_per_launch"] if rec else None
 
 
-def measured_instr_per_weight():
+def measured_instr_per_weight(mode=None):
     """Executed warp-instructions x 32 per decoded weight of the batch-1
     block's kernel (ncu smsp__inst_executed.sum over the launch, divided by
     the weights it decodes), or None without a current capture."""
-    rec = _profile_record("traffic")
+    rec = _profile_record("traffic", mode)
     return rec.get("instructions_per_weight") if rec else None
 
 
@@ -385,11 +391,14 @@ def run_ours(args, ws, rank, local):
     layer_seed, x_seed = replica_seeds(rank)
     blocks = [native.MoeBlock(moe_layer_device(layer_seed + l, dev), device=dev, topk=TOPK)
               for l in range(n_layers)]
-    # the steps of a graph run as one sequence launch (escha_moe_blocks: one
-    # cooperative kernel for up to 8 independent one-token blocks), or with
-    # --path per-slot as one escha_moe_block call (three kernels) per step
-    sequence = args.path == "sequence"
-    path = "sequence" if sequence else blocks[0].path(1)
+    # the steps of a graph run as one escha_moe_blocks call (by shape: the
+    # per-slot kernels over all 8 blocks; --path sequence holds it on the
+    # one-launch sequence kernel), or with --path per-slot as one
+    # escha_moe_block call (three kernels) per step
+    sequence = args.path in ("blocks", "sequence")  # one escha_moe_blocks call per graph
+    native.lib()
+    native.set_blocks_route(2 if args.path == "sequence" else 0)
+    path = args.path if sequence else blocks[0].path(1)
     seq_ws = torch.empty(native.seq_workspace_bytes(blocks[:STEPS_PER_GRAPH]), dtype=torch.uint8, device=dev)
     n_total = args.warmup + args.steps
     xs_host = torch.from_numpy(gen.fp16_normal(gen.rng(x_seed), (n_total, HIDDEN))).pin_memory()
@@ -409,12 +418,13 @@ def run_ours(args, ws, rank, local):
     chunks += [(i0, min(STEPS_PER_GRAPH, n_total - i0)) for i0 in range(args.warmup, n_total, STEPS_PER_GRAPH)]
     stream = torch.cuda.Stream(device=dev)
 
-    def run_chunk(i0, n):
-        """Steps i0 .. i0+n-1 on the current stream."""
+    def run_chunk(i0, n, events=None):
+        """Steps i0 .. i0+n-1 on the current stream (events: four CUDA events
+        recorded between the call's kernels)."""
         if sequence:
             idx = range(i0, i0 + n)
             native.moe_blocks([blocks[layer_of[i]] for i in idx], [xs[i] for i in idx], [outs[i] for i in idx],
-                              ids=[ids_all[i] for i in idx], w=[w_all[i] for i in idx], ws=seq_ws)
+                              ids=[ids_all[i] for i in idx], w=[w_all[i] for i in idx], ws=seq_ws, events=events)
         else:
             for i in range(i0, i0 + n):
                 blocks[layer_of[i]](xs[i:i + 1], out=outs[i:i + 1], ids=ids_all[i:i + 1], w=w_all[i:i + 1])
@@ -519,19 +529,23 @@ def run_ours(args, ws, rank, local):
         del e2e_graphs
 
         # per-kernel durations, timed live by events on the launch stream
-        # around each kernel (the events serialise the kernels): the
-        # sequence kernel per launch of up to 8 steps, or the three per-slot
-        # kernels of each step
+        # between the kernels (the events serialise them): per call of up to
+        # 8 steps the router, gate_up and down/combine kernels over all its
+        # blocks (or the one sequence launch), or the three per-slot kernels
+        # of each step
         if sequence:
-            kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in chunks]
+            kev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in chunks]
             with torch.cuda.stream(stream):
+                for row in kev:  # torch creates the CUDA events lazily, at their first record
+                    for e in row:
+                        e.record(stream)
                 barrier()
-                for (i0, n), (a, b) in zip(chunks, kev):
-                    a.record(stream)
-                    run_chunk(i0, n)
-                    b.record(stream)
+                for (i0, n), row in zip(chunks, kev):
+                    run_chunk(i0, n, events=row)
                 barrier()
-            seq_launch = [(a.elapsed_time(b), n) for (i0, n), (a, b) in list(zip(chunks, kev))[n_warm_graphs:]]
+            # (ms of each interval, steps) per timed call
+            seq_launch = [([row[j].elapsed_time(row[j + 1]) for j in range(3)], n)
+                          for (i0, n), row in list(zip(chunks, kev))[n_warm_graphs:]]
             phase = None
         else:
             evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_total)]
@@ -564,11 +578,24 @@ def run_ours(args, ws, rank, local):
 
     hbm, tflops, src = peaks()
     fused = path == native.ESCHA_PATH_FUSED
-    if sequence:
+    blocks_mode = args.path == "blocks"
+    if blocks_mode:
+        # the dominant kernel: the gate_up kernel over the 8 blocks' slots of
+        # one escha_moe_blocks call (calls of 8 steps; its work scales with n)
+        full = [iv for iv, n in seq_launch if n == STEPS_PER_GRAPH] or [iv for iv, n in seq_launch]
+        ph = np.array(full).mean(axis=0)  # router (+ shared gate_up), gate_up, down (+ shared down, combine) (ms)
+        k_ms = float(ph[1])
+        k_bytes, k_weights = STEPS_PER_GRAPH * GATE_UP_KERNEL_BYTES, STEPS_PER_GRAPH * GU_WEIGHTS
+        k_name = (f"moe_gate_up_kernel<K=3> over {STEPS_PER_GRAPH} blocks' slots ({STEPS_PER_GRAPH * TOPK} "
+                  f"(token, expert) pairs, each with its own layer's expert)")
+        phase_ms = {"router+shared_gate_up": float(ph[0]), "gate_up": float(ph[1]),
+                    "down+shared_down+combine": float(ph[2]),
+                    "per_block_serialised": float(ph.sum() / STEPS_PER_GRAPH)}
+    elif sequence:
         # the dominant kernel: the sequence kernel, per launch of n steps (n = 8
         # but for a shorter last launch); its work scales with n
-        per_block = [ms / n for ms, n in seq_launch]
-        launch_ms = [ms for ms, n in seq_launch if n == STEPS_PER_GRAPH] or [ms for ms, n in seq_launch]
+        per_block = [iv[0] / n for iv, n in seq_launch]
+        launch_ms = [iv[0] for iv, n in seq_launch if n == STEPS_PER_GRAPH] or [iv[0] for iv, n in seq_launch]
         k_ms = float(np.mean(launch_ms))
         k_bytes, k_weights = STEPS_PER_GRAPH * BLOCK_BYTES, STEPS_PER_GRAPH * BLOCK_WEIGHTS
         k_name = (f"moe_multi_kernel ({STEPS_PER_GRAPH} independent one-token blocks per launch: router, top-k, "
@@ -587,7 +614,8 @@ def run_ours(args, ws, rank, local):
         phase_ms = {"router+shared_gate_up": float(ph[0]), "gate_up": float(ph[1]),
                     "down+shared_down+combine": float(ph[2])}
     achieved = k_bytes / (k_ms * 1e-3) / 1e9
-    ipw = measured_instr_per_weight() if sequence else None
+    prof_mode = args.path if sequence else None  # the committed ncu record covers one mode's dominant kernel
+    ipw = measured_instr_per_weight(prof_mode)
     ops = ipw if ipw else ALU_OPS_PER_WEIGHT
     routed_code_bytes = TOPK * (GU_CODE_BYTES + DN_CODE_BYTES)
     distinct = len({tuple(r) for r in ids_all[args.warmup:args.warmup + 16].cpu().numpy().tolist()})
@@ -602,7 +630,9 @@ def run_ours(args, ws, rank, local):
                          f"({n_layers * 272} MB) cycled, one per step, no flush",
                    "cuda_graph": ("none (direct launches)" if args.no_graph else
                                   f"up to {STEPS_PER_GRAPH} steps per graph") +
-                                 (f"; the steps of a graph as one sequence launch (escha_moe_blocks)" if sequence else
+                                 ("; the steps of a graph as one escha_moe_blocks call: the router, gate_up and "
+                                  "down kernels over all its blocks" if blocks_mode else
+                                  "; the steps of a graph as one sequence launch (escha_moe_blocks)" if sequence else
                                   "; one escha_moe_block call per step (programmatic launches)"),
                    "parallelism": f"replicas x{ws} (independent token streams)"},
         # The dominant kernel is bound by instruction issue for the decode,
@@ -617,7 +647,7 @@ def run_ours(args, ws, rank, local):
         "roofline": {"bound": "alu", "achieved": k_weights * ops / 32 / (k_ms * 1e-3) / 1e12,
                      "peak": ALU_PEAK_WARP_INSTR / 1e12, "unit": "T warp-instructions/s",
                      "frac": k_weights * ops / 32 / (k_ms * 1e-3) / ALU_PEAK_WARP_INSTR,
-                     "traffic": measured_traffic() if sequence else None, "algorithmic_bytes_per_launch": k_bytes,
+                     "traffic": measured_traffic(prof_mode), "algorithmic_bytes_per_launch": k_bytes,
                      "kernel": k_name, "decoded_weights_per_launch": k_weights,
                      "instructions_per_weight": ops,
                      "instructions_per_weight_source": "ncu smsp__inst_executed.sum / weights (profiles/traffic.json)"
@@ -625,16 +655,19 @@ def run_ours(args, ws, rank, local):
                      "ms_per_launch": k_ms, "peak_source": "derived: 152 SMs x 4 x 2.07e9 /s"},
         # the same launch against the measured HBM copy bandwidth
         "roofline_hbm": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                         "traffic": measured_traffic() if sequence else None, "algorithmic_bytes_per_launch": k_bytes,
+                         "traffic": measured_traffic(prof_mode), "algorithmic_bytes_per_launch": k_bytes,
                          "ms_per_launch": k_ms, "peak_source": src},
         "packed_expert_gbs": routed_code_bytes / (t_step * 1e-3) / 1e9,
         "packed_expert_frac": routed_code_bytes / (t_step * 1e-3) / 1e9 / hbm,
         "phase_ms": phase_ms,
-        "block_path": {"sequence": f"escha_moe_blocks: one cooperative launch per {STEPS_PER_GRAPH} steps",
+        "block_path": {"blocks": f"escha_moe_blocks: the per-slot kernels over {STEPS_PER_GRAPH} blocks' slots "
+                                 f"(3 launches per {STEPS_PER_GRAPH} steps)",
+                       "sequence": f"escha_moe_blocks: one cooperative launch per {STEPS_PER_GRAPH} steps",
                        native.ESCHA_PATH_FUSED: "router kernel + cooperative expert kernel per step",
                        native.ESCHA_PATH_SLOT: "per-slot (three kernels per step)"}.get(path, str(path)),
         "status_word": status,
-        "gpu_launches": len(chunks[n_warm_graphs:]) if sequence else (2 if fused else KERNELS_PER_STEP) * args.steps,
+        "gpu_launches": (3 if blocks_mode else 1) * len(chunks[n_warm_graphs:]) if sequence
+        else (2 if fused else KERNELS_PER_STEP) * args.steps,
         "e2e": {"value": aggregate_tokens_per_s(ws, t_e2e), "unit": UNIT, "h2d_bytes_per_step": HIDDEN * 2,
                 "d2h_bytes_per_step": HIDDEN * 4,
                 "note": f"per group of up to {STEPS_PER_GRAPH} steps, one graph: the steps, and on a copy stream "
@@ -884,8 +917,9 @@ def main():
                                                                "single projection, int8 shapes, 40-block stack)")
     ap.add_argument("--no-graph", action="store_true", help="launch the steps directly (for profilers)")
     ap.add_argument("--layers", type=int, default=N_LAYERS, help="distinct layers cycled through")
-    ap.add_argument("--path", default="sequence", choices=["sequence", "per-slot"],
-                    help="the steps of a graph as one sequence launch, or one block call (three kernels) per step")
+    ap.add_argument("--path", default="blocks", choices=["blocks", "sequence", "per-slot"],
+                    help="the steps of a graph as one escha_moe_blocks call (by shape: the per-slot kernels over "
+                         "all its blocks), the same call held on the sequence kernel, or one block call per step")
     ap.add_argument("--profile-case", help="comma-separated workloads (" + ", ".join(PROFILE_CASES) +
                                            ") run with direct launches (for profilers), then exit")
     ap.add_argument("--reps", type=int, default=3, help="launches of --profile-case")

@@ -830,7 +830,7 @@ size_t ml_ws_bytes(const escha_moe_layer* L, int n) {
 }
 
 int ml_blocks(const escha_moe_layer* const* layers, int n, const uint16_t* const* x, float* const* out,
-              int32_t* const* ids_out, float* const* w_out, void* ws, int sms, cudaStream_t s) {
+              int32_t* const* ids_out, float* const* w_out, void* ws, int sms, cudaStream_t s, cudaEvent_t* ev) {
     const escha_moe_layer* L = layers[0];
     char* base = static_cast<char*>(ws);
     const MoeWs m = moe_ws_layout(L, n);
@@ -860,9 +860,13 @@ int ml_blocks(const escha_moe_layer* const* layers, int n, const uint16_t* const
         t.w = w_out ? w_out[i] : nullptr;
     }
     int r;
+    if ((r = record(ev, 0, s))) return r;
     if ((r = cuda_status(escha::launch_moe_router_ml(a, tab, s), "router launch"))) return r;
+    if ((r = record(ev, 1, s))) return r;
     if ((r = cuda_status(escha::launch_moe_gate_up(a, sms, s), "gate_up launch"))) return r;
-    return cuda_status(escha::launch_moe_down(a, sms, s), "down/combine launch");
+    if ((r = record(ev, 2, s))) return r;
+    if ((r = cuda_status(escha::launch_moe_down(a, sms, s), "down/combine launch"))) return r;
+    return record(ev, 3, s);
 }
 
 size_t escha_moe_seq_workspace(const escha_moe_layer* const* layers, int n_blocks) {
@@ -874,8 +878,10 @@ size_t escha_moe_seq_workspace(const escha_moe_layer* const* layers, int n_block
     return need;
 }
 
-int escha_moe_blocks(const escha_moe_layer* const* layers, int n_blocks, const uint16_t* const* x, float* const* out,
-                     int32_t* const* ids_out, float* const* w_out, void* ws, size_t ws_bytes, void* stream) {
+namespace {
+int moe_blocks_impl(const escha_moe_layer* const* layers, int n_blocks, const uint16_t* const* x, float* const* out,
+                    int32_t* const* ids_out, float* const* w_out, void* ws, size_t ws_bytes, void* stream,
+                    cudaEvent_t* ev) {
     escha::MbPlan p{};
     int r = seq_check(layers, n_blocks, "moe_blocks", &p);
     if (r) return r;
@@ -897,7 +903,7 @@ int escha_moe_blocks(const escha_moe_layer* const* layers, int n_blocks, const u
     if (route == 1 && !ml)
         return fail(ESCHA_E_SHAPE, "moe_blocks: the per-slot route takes up to %d blocks with one K pair", escha::kMlMaxT);
     if (ml && route != 2)
-        return ml_blocks(layers, n_blocks, x, out, ids_out, w_out, ws, sms, static_cast<cudaStream_t>(stream));
+        return ml_blocks(layers, n_blocks, x, out, ids_out, w_out, ws, sms, static_cast<cudaStream_t>(stream), ev);
     if ((r = seq_grid(sms, p.smem, &grid))) return r;
     escha::MbArgs m = seq_args(layers, n_blocks, p, static_cast<char*>(ws), w);
     seq_segments(m, n_blocks, p, false);
@@ -907,7 +913,26 @@ int escha_moe_blocks(const escha_moe_layer* const* layers, int n_blocks, const u
         if (ids_out && ids_out[i]) m.blk[i].ids = ids_out[i];
         if (w_out && w_out[i]) m.blk[i].w = w_out[i];
     }
-    return cuda_status(escha::launch_moe_multi(m, grid, static_cast<cudaStream_t>(stream)), "moe_blocks launch");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if ((r = record(ev, 0, st))) return r;
+    if ((r = cuda_status(escha::launch_moe_multi(m, grid, st), "moe_blocks launch"))) return r;
+    for (int i = 1; i < 4; ++i)
+        if ((r = record(ev, i, st))) return r;
+    return ESCHA_OK;
+}
+}  // namespace
+
+int escha_moe_blocks(const escha_moe_layer* const* layers, int n_blocks, const uint16_t* const* x, float* const* out,
+                     int32_t* const* ids_out, float* const* w_out, void* ws, size_t ws_bytes, void* stream) {
+    return moe_blocks_impl(layers, n_blocks, x, out, ids_out, w_out, ws, ws_bytes, stream, nullptr);
+}
+
+int escha_moe_blocks_timed(const escha_moe_layer* const* layers, int n_blocks, const uint16_t* const* x,
+                           float* const* out, int32_t* const* ids_out, float* const* w_out, void* ws, size_t ws_bytes,
+                           void* stream, void* const* events) {
+    cudaEvent_t ev[4];
+    for (int i = 0; i < 4; ++i) ev[i] = events ? static_cast<cudaEvent_t>(events[i]) : nullptr;
+    return moe_blocks_impl(layers, n_blocks, x, out, ids_out, w_out, ws, ws_bytes, stream, ev);
 }
 
 int escha_moe_stack(const escha_moe_layer* const* layers, int n_blocks, float* h, float eps, uint16_t* x_buf,

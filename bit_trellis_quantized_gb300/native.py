@@ -62,6 +62,7 @@ EXPORTS = [
     "escha_moe_stack",
     "escha_moe_block_path",
     "escha_moe_blocks_path",
+    "escha_moe_blocks_timed",
     "escha_debug_set_blocks_route",
     "escha_debug_set_moe_route",
     "escha_debug_set_fused_wait",
@@ -190,6 +191,9 @@ def lib() -> ctypes.CDLL:
         L.escha_moe_stack.restype = _i
         L.escha_moe_block_path.argtypes = [ctypes.POINTER(EschaMoeLayer), _i]
         L.escha_moe_block_path.restype = _i
+        L.escha_moe_blocks_timed.argtypes = [_lp, _i, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
+                                             ctypes.POINTER(_vp), _vp, _sz, _vp, ctypes.POINTER(_vp)]
+        L.escha_moe_blocks_timed.restype = _i
         L.escha_moe_blocks_path.argtypes = [_lp, _i]
         L.escha_moe_blocks_path.restype = _i
         L.escha_debug_set_blocks_route.argtypes = [_i]
@@ -668,11 +672,12 @@ def blocks_path(blocks) -> int:
     return r
 
 
-def moe_blocks(blocks, xs, outs, ids=None, w=None, ws=None, stream=None):
+def moe_blocks(blocks, xs, outs, ids=None, w=None, ws=None, stream=None, events=None):
     """Independent one-token blocks in few launches: block i of ``blocks``
     (MoeBlock) on xs[i] (fp16 [hidden] or [1][hidden]) into outs[i] (f32).
     ``ids`` / ``w``: optional lists of per-block [topk] tensors. ``ws``: a
-    workspace of at least seq_workspace_bytes(blocks) bytes."""
+    workspace of at least seq_workspace_bytes(blocks) bytes. ``events``: four
+    torch.cuda.Event recorded between the kernels (escha_moe_blocks_timed)."""
     n = len(blocks)
     _need_cuda(*xs, *outs)
     if ws is None:
@@ -681,7 +686,13 @@ def moe_blocks(blocks, xs, outs, ids=None, w=None, ws=None, stream=None):
     po = (_vp * n)(*[ptr(t) for t in outs])
     pi = (_vp * n)(*[ptr(t) for t in ids]) if ids is not None else None
     pw = (_vp * n)(*[ptr(t) for t in w]) if w is not None else None
-    check(lib().escha_moe_blocks(_layer_array(blocks), n, px, po, pi, pw, ptr(ws), ws.numel(), stream_handle(stream)))
+    if events is None:
+        check(lib().escha_moe_blocks(_layer_array(blocks), n, px, po, pi, pw, ptr(ws), ws.numel(),
+                                     stream_handle(stream)))
+    else:  # four torch.cuda.Event: the kernels' boundaries (escha_moe_blocks_timed)
+        ev = (_vp * 4)(*[e.cuda_event for e in events])
+        check(lib().escha_moe_blocks_timed(_layer_array(blocks), n, px, po, pi, pw, ptr(ws), ws.numel(),
+                                           stream_handle(stream), ev))
     return outs
 
 

@@ -379,6 +379,16 @@ int escha_moe_blocks_path(const escha_moe_layer* const* layers, int n_blocks);
 int escha_debug_set_blocks_route(int mode);
 int escha_moe_blocks(const escha_moe_layer* const* layers, int n_blocks, const uint16_t* const* x, float* const* out,
                      int32_t* const* ids_out, float* const* w_out, void* ws, size_t ws_bytes, void* stream);
+/* Measurement export: escha_moe_blocks that also records four caller-created
+ * CUDA events (any may be null) on `stream`: on the per-slot route [0]
+ * before the router kernel, [1] after it, [2] after the gate_up kernel, [3]
+ * after the down/combine kernel (recording between the kernels serialises
+ * them, so each interval is one kernel's duration); on the sequence route
+ * [0] before its launch and [1]..[3] after it. Same results and errors as
+ * escha_moe_blocks. */
+int escha_moe_blocks_timed(const escha_moe_layer* const* layers, int n_blocks, const uint16_t* const* x,
+                           float* const* out, int32_t* const* ids_out, float* const* w_out, void* ws, size_t ws_bytes,
+                           void* stream, void* const* events);
 int escha_moe_stack(const escha_moe_layer* const* layers, int n_blocks, float* h, float eps, uint16_t* x_buf,
                     float* out_buf, int32_t* ids_out, float* w_out, void* ws, size_t ws_bytes, void* stream);
 
