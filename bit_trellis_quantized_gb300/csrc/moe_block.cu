@@ -592,6 +592,81 @@ __global__ void __launch_bounds__(kK0Threads) moe_router_kernel(const MoeArgs a,
     }
 }
 
+// One token, hidden <= 2048, few registers: shared_gate_up_direct<1> with
+// the int8 rows kept packed until after the wait and converted as they are
+// used (the same values, the same order of every sum), so that the router
+// grid of a multi-layer launch, one row of CTAs per token, keeps many CTAs
+// per SM.
+__device__ void shared_gate_up_light(const MoeArgs& a, int cta, int warp, int lane) {
+    constexpr int R = kShRowsPerWarp;
+    const int rows = 2 * a.sh_inter;
+    const int r0 = (cta * kK0Warps + warp) * R;
+    const int nrows = min(R, rows - r0);
+    const bool gate = cta == 0 && warp == kK0Warps - 1;
+    uint4 wv[R][4];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            wv[r][c] = (r < nrows && c * 512 + lane * 16 < a.hidden)
+                           ? ldg_stream_v4(a.sh_gu_w8 + (long long)(r0 + r) * a.hidden + c * 512 + lane * 16)
+                           : make_uint4(0u, 0u, 0u, 0u);
+    pdl_wait();  // x, and the workspace the previous call's kernels may still read
+    if (nrows > 0) {
+        float acc[R] = {0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            if (c * 512 + lane * 16 >= a.hidden) break;
+            const uint4 x0 = __ldg(reinterpret_cast<const uint4*>(a.x + c * 512 + lane * 16));
+            const uint4 x1 = __ldg(reinterpret_cast<const uint4*>(a.x + c * 512 + lane * 16 + 8));
+            const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float xq[4] = {h2f_bits(static_cast<uint16_t>(xw[2 * q] & 0xFFFFu)),
+                                     h2f_bits(static_cast<uint16_t>(xw[2 * q] >> 16)),
+                                     h2f_bits(static_cast<uint16_t>(xw[2 * q + 1] & 0xFFFFu)),
+                                     h2f_bits(static_cast<uint16_t>(xw[2 * q + 1] >> 16))};
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const uint32_t word = q == 0 ? wv[r][c].x : q == 1 ? wv[r][c].y : q == 2 ? wv[r][c].z : wv[r][c].w;
+                    float f[4];
+                    i8x4_to_f32(word, f);
+                    acc[r] = fmaf(f[0], xq[0], acc[r]);
+                    acc[r] = fmaf(f[1], xq[1], acc[r]);
+                    acc[r] = fmaf(f[2], xq[2], acc[r]);
+                    acc[r] = fmaf(f[3], xq[3], acc[r]);
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            float v = acc[r];
+#pragma unroll
+            for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+            if (lane == 0 && r < nrows) a.shgu[r0 + r] = a.sh_gu_scale[r0 + r] * v;
+        }
+    }
+    if (gate) {
+        float acc = 0.f;
+#pragma unroll 1
+        for (int k = 0; k < 8; ++k) {
+            const int i0 = lane * 8 + 256 * k;
+            if (i0 >= a.hidden) break;
+            const uint4 g4 = __ldg(reinterpret_cast<const uint4*>(a.sh_gate + i0));
+            const uint4 xg = __ldg(reinterpret_cast<const uint4*>(a.x + i0));
+            const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w}, xw[4] = {xg.x, xg.y, xg.z, xg.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                acc = fmaf(h2f_bits(static_cast<uint16_t>(gw[q] & 0xFFFFu)), h2f_bits(static_cast<uint16_t>(xw[q] & 0xFFFFu)), acc);
+                acc = fmaf(h2f_bits(static_cast<uint16_t>(gw[q] >> 16)), h2f_bits(static_cast<uint16_t>(xw[q] >> 16)), acc);
+            }
+        }
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+        if (lane == 0) *a.shgate = sigmoid_f(acc);
+    }
+}
+
 // Multi-layer per-slot launch: row y of the grid is token y, with its own
 // layer. Its CTAs run the one-token code on a view of the arguments that
 // holds that layer's weights and input and that token's outputs, so every
@@ -617,7 +692,7 @@ __global__ void __launch_bounds__(kK0Threads) moe_router_ml_kernel(const MoeArgs
         router_logits<false>(la, warp, lane, nullptr, 0, &tab);
         return;
     }
-    shared_gate_up_direct<1, false>(la, static_cast<int>(blockIdx.x) - n_lg, warp, lane, nullptr);
+    shared_gate_up_light(la, static_cast<int>(blockIdx.x) - n_lg, warp, lane);
 }
 
 // Router logits for many tokens: a CTA stages 16 tokens of x in shared memory
