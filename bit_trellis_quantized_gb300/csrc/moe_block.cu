@@ -1167,11 +1167,13 @@ SlotPlan slot_plan(int T, int hidden, int inter, int topk) {
     const int kblks = hidden / 128;
     // gate_up: the largest input split (CTAs per cluster, <= 8) for which the
     // routed CTAs fit in one wave of 4 CTAs per SM; when only an unsplit grid
-    // fits, a split of two is still taken while it needs at most 1.3 waves
-    // (measured on GB300 for the 35B layer with 3 CTAs per SM: 4 tokens 61 ->
-    // 56 us per block; 5 tokens, 1.5 waves, is slower split). Four CTAs per
-    // SM instead of three: 1 token 23.7 -> 21.5 us per block, 2 tokens 35.8
-    // -> 31.1 us, 4 to 16 tokens unchanged.
+    // fits, a split of two is still taken while it needs at most 1.8 waves:
+    // an unsplit grid that fills a wave only partly leaves SMs with 3 CTAs
+    // beside SMs with 4 (measured on GB300 for the 35B layer: 8 one-token
+    // blocks of distinct layers in one launch 11.05 -> 10.68 us per block
+    // with the split; 1.3 waves was the limit before, set with 3 CTAs per
+    // SM). Four CTAs per SM instead of three: 1 token 23.7 -> 21.5 us per
+    // block, 2 tokens 35.8 -> 31.1 us, 4 to 16 tokens unchanged.
     auto ctas = [&](int cs) { return (long long)cs * oblks * slots; };
     int csize = 1;
     for (int c = 1; c <= 8 && c <= kblks; ++c) {
@@ -1179,7 +1181,7 @@ SlotPlan slot_plan(int T, int hidden, int inter, int topk) {
         const int cs = (kblks + per - 1) / per;
         if (ctas(cs) <= 4LL * kWaveSms) csize = cs;
     }
-    if (csize == 1 && kblks >= 2 && 10 * ctas(2) <= 13LL * 4 * kWaveSms) csize = 2;
+    if (csize == 1 && kblks >= 2 && 10 * ctas(2) <= 18LL * 4 * kWaveSms) csize = 2;
     const int per = (kblks + csize - 1) / csize;
     p.gu_csize = (kblks + per - 1) / per;
     p.gu_kt_per_cta = per * 8;
