@@ -127,6 +127,64 @@ __device__ __forceinline__ void decode_fma(const LaneCodes<K>& lc, const float (
     });
 }
 
+// Decode ahead of the activations. decode_store writes the lane's 64
+// weights of one tile row as 32 half2 pairs, in the order decode_fma
+// consumes them, to the warp's 4 KB of shared memory `wd` (layout
+// [8][32 lanes][4 words]: a warp's 16-byte accesses are conflict-free).
+// fma_decoded later runs decode_fma's multiply-adds on them for one token:
+// the same weights in the same order, so the same results.
+template <int K>
+__device__ __forceinline__ void decode_store(const LaneCodes<K>& lc, uint32_t* wd, int lane) {
+    uint32_t h[4];
+    auto put = [&](auto I, __half2 w) {
+        constexpr int i = decltype(I)::value;
+        h[i % 4] = *reinterpret_cast<const uint32_t*>(&w);
+        if constexpr (i % 4 == 3)
+            *reinterpret_cast<uint4*>(wd + ((i / 4) * 32 + lane) * 4) = make_uint4(h[0], h[1], h[2], h[3]);
+    };
+    if constexpr (K == 2) {
+        uint32_t q[5];
+#pragma unroll
+        for (int i = 0; i < 5; ++i) q[i] = stream_pair(lc.p[i]);
+        static_for<32>([&](auto I) {
+            constexpr int r = decltype(I)::value / 8, m = decltype(I)::value % 8;
+            __half ha, hb;
+            cb_decode_window(bits32<2 * m>(q[r], q[r + 1]), ha, hb);
+            put(I, __halves2half2(ha, hb));
+        });
+    } else {
+        static_for<32>([&](auto I) {
+            constexpr int j = (2 * decltype(I)::value) / 8;
+            constexpr int m = (2 * decltype(I)::value) % 8;
+            constexpr int b0 = 8 * K * j + K * m, b1 = b0 + K;
+            const uint32_t s0 = window_state<(b0 & 15)>(stream_window<(b0 >> 4)>(lc.p));
+            const uint32_t s1 = window_state<(b1 & 15)>(stream_window<(b1 >> 4)>(lc.p));
+            put(I, cb_decode_h2(s0, s1));
+        });
+    }
+}
+
+template <int K>
+__device__ __forceinline__ void fma_decoded(const uint32_t* wd, int lane, const float (&xr)[4], float2 (&acc2)[8]) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const uint4 v = *reinterpret_cast<const uint4*>(wd + (q * 32 + lane) * 4);
+        const uint32_t h[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int I = 4 * q + u;
+            const float2 w = __half22float2(*reinterpret_cast<const __half2*>(&h[u]));
+            if constexpr (K == 2) {
+                acc2[I % 8] = fma_pair<1>(w, xr[I / 8], acc2[I % 8]);
+            } else {
+                const int j = (2 * I) / 8, m = (2 * I) % 8;
+                const int i = (8 * (j & 1) + m) / 2;
+                acc2[i] = fma_pair<1>(w, xr[j >> 1], acc2[i]);
+            }
+        }
+    }
+}
+
 // The warp's column sums (acc2 as decode_fma leaves them) reduce-scattered
 // over the 4 lanes of each tile and stored as the warp's row of `red`
 // ([NW][NB][128] floats, smem).
