@@ -145,20 +145,27 @@ __global__ void __launch_bounds__(tc::kMlThreads + 32, 1)
         y += (long long)blockIdx.z * M * N;
         y_stride = N;
     }
-    // producer thread t converts output row t of the CTA (M tile t / 128), all
-    // 64 values of every chunk. Three register sets rotate: chunk c + 2 loads
-    // into one while chunk c is converted from another, so a load has two
-    // chunks of MMA time to arrive, and no set is ever copied (a copy would
-    // wait for the load).
-    const int r = tid & 255;
-    const int8_t* wrow = W + (long long)min(n0 + r, N - 1) * Kin + b_first * 128;
+    // producer warp w converts output rows 32w .. 32w + 31 of the CTA (M tile
+    // w / 4): in part j (0..3) lane l takes row 32w + 8j + l/4, values
+    // 16(l%4) .. +15 of the chunk, so four lanes read one row's 64 bytes and
+    // each load instruction reads eight whole 64-byte row segments (one
+    // row per lane left every sector half used for L1 to keep, and L1 is
+    // small beside these shared-memory stages). Three register sets rotate:
+    // chunk c + 2 loads into one while chunk c is converted from another, so
+    // a load has two chunks of MMA time to arrive, and no set is ever copied
+    // (a copy would wait for the load).
+    const int r0 = (tid & 255) & ~31;  // the warp's first row
+    const int8_t* wrow = W + (long long)min(n0 + r0 + (lane >> 2), N - 1) * Kin + b_first * 128 + 16 * (lane & 3);
+    long long jstep[4];  // row j of the lane's four, clamped to the last weight row
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        jstep[j] = (long long)(min(n0 + r0 + 8 * j + (lane >> 2), N - 1) - min(n0 + r0 + (lane >> 2), N - 1)) * Kin;
     const int nch = 2 * nblk;
     uint4 w0[4], w1[4], w2[4];
     auto load = [&](uint4 (&w)[4], int c) {
         if (c < nch) {
-            const uint4* src = reinterpret_cast<const uint4*>(wrow + c * 64);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) w[j] = __ldg(src + j);
+            for (int j = 0; j < 4; ++j) w[j] = __ldg(reinterpret_cast<const uint4*>(wrow + jstep[j] + c * 64));
         }
     };
     if (tid < tc::kMlThreads) {
@@ -166,14 +173,15 @@ __global__ void __launch_bounds__(tc::kMlThreads + 32, 1)
         load(w1, 1);
     }
     auto convert = [&](const uint4 (&w)[4], uint8_t* A) {
-        uint8_t* dst = A + (r >> 7) * tc::kWsAStageBytes;
-        const uint32_t rr = static_cast<uint32_t>(r & 127);
+        uint8_t* dst = A + (r0 >> 7) * tc::kWsAStageBytes;
+        const uint32_t k0 = 16u * static_cast<uint32_t>(lane & 3);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
+            const uint32_t rr = static_cast<uint32_t>((r0 & 127) + 8 * j + (lane >> 2));
             const uint2 x0 = i8x4_to_16<BF16>(w[j].x), x1 = i8x4_to_16<BF16>(w[j].y);
             const uint2 x2 = i8x4_to_16<BF16>(w[j].z), x3 = i8x4_to_16<BF16>(w[j].w);
-            *reinterpret_cast<uint4*>(dst + tc::kmajor_off(rr, 16u * j)) = make_uint4(x0.x, x0.y, x1.x, x1.y);
-            *reinterpret_cast<uint4*>(dst + tc::kmajor_off(rr, 16u * j + 8u)) = make_uint4(x2.x, x2.y, x3.x, x3.y);
+            *reinterpret_cast<uint4*>(dst + tc::kmajor_off(rr, k0)) = make_uint4(x0.x, x0.y, x1.x, x1.y);
+            *reinterpret_cast<uint4*>(dst + tc::kmajor_off(rr, k0 + 8u)) = make_uint4(x2.x, x2.y, x3.x, x3.y);
         }
     };
 
