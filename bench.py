@@ -857,7 +857,7 @@ def extended(dev, blocks, hbm, tflops):
 
 
 PROFILE_CASES = ("block_b1", "block_b8", "block_b64", "block_b256", "prefill_2048", "projection_b1",
-                 "int8_m1", "int8_m2048", "dense_m1", "dense_m2048", "dense_split_m13")
+                 "int8_m1", "int8_m2048", "int8_head_m2048", "dense_m1", "dense_m2048", "dense_split_m13")
 
 
 def profile_case(name: str, reps: int):
@@ -896,11 +896,13 @@ def profile_case(name: str, reps: int):
         for i in range(reps):
             lin(x, y=y)
     else:
+        # int8 w8a16: 4096 x 2048 at 1 or 2048 tokens; the 152064 x 2048 head at 2048 tokens
         M = 1 if name == "int8_m1" else 2048
-        W = torch.randint(-127, 128, (4096, 2048), dtype=torch.int8, device=dev)
-        s = torch.rand(4096, device=dev) * 9e-3 + 1e-3
+        N = 152064 if name == "int8_head_m2048" else 4096
+        W = torch.randint(-127, 128, (N, 2048), dtype=torch.int8, device=dev)
+        s = torch.rand(N, device=dev) * 9e-3 + 1e-3
         x = torch.randn((M, 2048), device=dev).to(torch.bfloat16)
-        y = torch.empty((M, 4096), dtype=torch.float32, device=dev)
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
         for i in range(reps):
             native.int8_w8a16_matvec(W, s, x, y=y)
     torch.cuda.synchronize()
