@@ -67,7 +67,9 @@ def test_dense_linear_matches_oracle(native, M, nt_major):
     assert np.array_equal(y[:, pruned], np.broadcast_to(p["bias"][pruned], (M, pruned.sum())))
 
 
-@pytest.mark.parametrize("M", [2, 40])
+# M = 1: one tile row per warp, weights decoded before the wait on the
+# preceding kernel; M = 2: the two-token GEMV; M = 40: the GEMM route
+@pytest.mark.parametrize("M", [1, 2, 40])
 def test_dense_linear_no_bias_f32_input(native, M):
     p = gen.dense_projection(2000 + M, 640, 384, 2, M)
     x = p["x"].astype(np.float32) * np.float32(1.37)  # not representable in fp16
