@@ -743,6 +743,12 @@ def extended(dev, blocks, hbm, tflops):
     res["single_projection_1024x2048_k2_b1"] = {"us": ms * 1e3, **_stats(t), "packed_gbs": b / (ms * 1e-3) / 1e9,
                                                "frac_of_hbm": b / (ms * 1e-3) / 1e9 / hbm,
                                                "l2": f"{P} distinct projections ({P * b >> 20} MB) cycled"}
+    # the same projection every call: its 512 KB of codes stay in L2
+    t = _time_graph(torch, stream, lambda i: native.trellis_gemv(pj["codes"][0], pj["x"][0:1], pj["rin"][0],
+                                                                 pj["rout"][0], y=y[0:1]), reps=256)
+    res["single_projection_1024x2048_k2_b1_l2_resident"] = {
+        "us": t[0] * 1e3, **_stats(t), "packed_gbs": b / (t[0] * 1e-3) / 1e9,
+        "l2": "L2-resident: one projection, 256 calls per graph"}
     del pj, y
 
     # dense trellis linear 5120 -> 17408, K = 2 (a 27B-class gate_proj) with an
@@ -782,6 +788,23 @@ def extended(dev, blocks, hbm, tflops):
     out1 = torch.empty((1, HIDDEN), dtype=torch.float32, device=dev)
     t = _time_graph(torch, stream, lambda i: blocks[i % nl](xs1[i % nl], out=out1), reps=nl)
     mb["b1_per_slot_calls"] = {"tokens_per_s": 1 / (t[0] * 1e-3), "us_per_block": t[0] * 1e3, **_stats(t)}
+    # one layer and one x every call: the 8 routed experts, the router and the
+    # shared expert (12.6 MB) stay in L2
+    t = _time_graph(torch, stream, lambda i: blocks[0](xs1[0], out=out1), reps=64)
+    mb["b1_per_slot_calls_l2_resident"] = {"tokens_per_s": 1 / (t[0] * 1e-3), "us_per_block": t[0] * 1e3,
+                                           **_stats(t), "l2": "L2-resident: one layer, one x, 64 calls per graph"}
+    sws = torch.empty(native.seq_workspace_bytes([blocks[0]] * STEPS_PER_GRAPH), dtype=torch.uint8, device=dev)
+    outs8 = torch.empty((STEPS_PER_GRAPH, HIDDEN), dtype=torch.float32, device=dev)
+    t = _time_graph(torch, stream, lambda i: native.moe_blocks([blocks[0]] * STEPS_PER_GRAPH,
+                                                               [xs1[0][0]] * STEPS_PER_GRAPH,
+                                                               [outs8[j] for j in range(STEPS_PER_GRAPH)], ws=sws),
+                    reps=16)
+    mb["b1_blocks_l2_resident"] = {"tokens_per_s": STEPS_PER_GRAPH / (t[0] * 1e-3),
+                                   "us_per_block": t[0] * 1e3 / STEPS_PER_GRAPH,
+                                   **{k: v / STEPS_PER_GRAPH for k, v in _stats(t).items()},
+                                   "l2": f"L2-resident: {STEPS_PER_GRAPH} blocks of one layer on one x per "
+                                         "escha_moe_blocks call, 16 calls per graph"}
+    del sws, outs8
     # MoE block at batch 8 / 16 (per-slot path), 64 / 256 / 2048 (grouped path)
     # over the headline's layers, fresh x per call
     for T in (8, 16, 64, 256, 2048):
