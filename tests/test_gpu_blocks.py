@@ -107,6 +107,53 @@ def test_distinct_small_layers_against_the_oracle(native):
         assert rel_err_rows(out[i].cpu().numpy()[None], ref).max() <= TOL
 
 
+# (hidden, inter, experts, topk, shared inter (0: none), K gate_up, K down, blocks)
+SHAPES = [
+    (256, 128, 8, 2, 0, 2, 2, 3),
+    (768, 384, 24, 8, 384, 2, 3, 2),
+    (1024, 128, 64, 1, 16, 3, 3, 4),
+    (512, 256, 16, 4, 256, 3, 2, 16),
+]
+
+
+@pytest.mark.parametrize("cfg", SHAPES, ids=[f"h{c[0]}_i{c[1]}_e{c[2]}_k{c[3]}_sh{c[4]}_K{c[5]}{c[6]}_n{c[7]}"
+                                             for c in SHAPES])
+def test_distinct_layer_shapes(native, cfg):
+    """Distinct layers of other shapes (no shared expert, top-1 / 2 / 8, K = 2
+    or 3 on either projection, 16 blocks): routing bit-exact against the
+    oracle and the sequence kernel, outputs within the tolerance of the
+    oracle and within 1e-5 of the sequence kernel (whose input splits
+    differ)."""
+    hidden, inter, E, topk, sh, kg, kd, n = cfg
+    layers = []
+    for i in range(n):
+        d = gen.moe_layer(3600 + 10 * i + hidden, hidden=hidden, inter=inter, n_experts=E, k_gu=kg, k_dn=kd,
+                          sh_inter=max(sh, 16))
+        if sh == 0:
+            d["sh_inter"] = 0
+        layers.append(d)
+    blocks = [native.MoeBlock(d, topk=topk) for d in layers]
+    assert native.blocks_path(blocks) == native.ESCHA_PATH_SLOT
+    xs_np = [gen.fp16_normal(gen.rng(3700 + i), (hidden,)) for i in range(n)]
+    xs = [dev(x) for x in xs_np]
+    out, ids, w = _run(native, blocks, xs, route=1)
+    s_out, s_ids, s_w = _run(native, blocks, xs, route=2)
+    for i, d in enumerate(layers):
+        assert torch.equal(ids[i], s_ids[i])
+        assert torch.equal(w[i], s_w[i])
+        err = float((out[i] - s_out[i]).abs().max() / s_out[i].abs().max())
+        assert err <= 1e-5, (i, err)
+        layer = o.MoeLayer(**d)
+        x1 = xs_np[i][None]
+        ref, r_ids, r_w, _ = o.moe_block(layer, x1, k=topk)
+        if sh == 0:
+            xv = o.f16_to_f64(x1.view(np.uint16))[0]
+            ref = sum(r_w[0, j] * o.moe_expert(layer, r_ids[0, j], xv) for j in range(topk))[None]
+        assert np.array_equal(ids[i].cpu().numpy(), r_ids[0])
+        assert np.allclose(w[i].cpu().numpy(), r_w[0], rtol=1e-5, atol=1e-6)
+        assert rel_err_rows(out[i].cpu().numpy()[None], ref).max() <= TOL
+
+
 def test_route_choice(native):
     """Mixed K pairs, or more than 16 blocks, take the sequence kernel; forcing
     the per-slot route on them is an error before anything is enqueued."""
