@@ -24,12 +24,17 @@
  *     bytes; each entry point has a *_workspace() query. A larger workspace
  *     is accepted. The library allocates no device memory.
  *   - Kernels are launched with programmatic dependent launch: a kernel may
- *     start while the kernel enqueued before it on the stream is finishing,
- *     and it reads weights (code tensors, rin / rout, int8 matrices, scales,
- *     router weights) before waiting for that kernel. Activations and
- *     outputs are only touched after the wait. So weights must not be
- *     written by the kernel launched just before the call on the same stream
- *     (a copy, an event or any other kernel in between is enough).
+ *     start while the kernel enqueued before it on the stream is still
+ *     running, and it reads weights (code tensors, rin / rout, int8
+ *     matrices, scales, router weights) before waiting for that kernel.
+ *     Activations and outputs are only touched after the wait. Some of the
+ *     library's kernels release the kernel after them before their own wait
+ *     (the routers, and the one-token GEMV that decodes its weights ahead),
+ *     so a chain of library calls does not order weight writes: weights must
+ *     be written by work that is ordered before the call by a stream point
+ *     these launches cannot pass (a memory copy, an event record, a kernel
+ *     launched without programmatic dependent launch, or host
+ *     synchronisation) rather than by another call of this library.
  *   - Every argument is validated before anything is enqueued. On error the
  *     call returns a negative ESCHA_E_* code, enqueues nothing, and
  *     escha_last_error() describes the problem. Asynchronous device faults
