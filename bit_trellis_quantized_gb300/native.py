@@ -328,6 +328,10 @@ class DenseLinear:
         self.n_in, self.n_out, self.K = KT * 16, NT * 16, L // 16
         self.nt_major = bool(nt_major)
         self.codes = codes_to_nt_major(codes, stream) if self.nt_major else codes
+        if self.nt_major:
+            # the transposed codes are weights, which the kernels read before
+            # their programmatic-launch wait: finish the load-time copy first
+            (stream if stream is not None else torch.cuda.current_stream(codes.device)).synchronize()
         self.rin, self.rout = rin, rout
         self.bias = bias.contiguous() if bias is not None else None
         self._ws = None

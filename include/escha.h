@@ -129,6 +129,9 @@ int escha_trellis_gemv(const uint16_t* codes, int in, int out, int K, const void
  *   codes  uint16 source, dst uint16 destination of the same size; the two
  *          must not overlap (ESCHA_E_ARG). Both caller-owned, 16-byte aligned.
  *   in,out multiples of 16;  K in {2, 3}
+ * dst is a weight for the calls that read it: order the transpose before
+ * them by a stream point that programmatic launches cannot pass (see the
+ * conventions above), e.g. an event record or host synchronisation.
  * Errors: ESCHA_E_ARG, ESCHA_E_SHAPE, ESCHA_E_K, ESCHA_E_ALIGN, ESCHA_E_CUDA,
  *         ESCHA_E_DEVICE. */
 int escha_codes_to_nt_major(const uint16_t* codes, int in, int out, int K, uint16_t* dst, void* stream);
