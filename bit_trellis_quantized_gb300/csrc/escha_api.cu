@@ -87,6 +87,8 @@ std::atomic<int> g_moe_route_mode{0};
 std::atomic<int> g_blocks_route{0};
 std::atomic<long long> g_fz_wait_ns{2000000000ll};
 std::atomic<int> g_fz_skip_publish{0};
+std::atomic<int> g_mbar_limit_log2{24};
+std::atomic<int> g_skip_cluster_arrive{0};
 
 int check_trellis(const uint16_t* codes, int in, int out, int K, int mult, const char* name) {
     if (!codes) return fail(ESCHA_E_ARG, "%s: codes is null", name);
@@ -443,6 +445,8 @@ escha::MoeArgs moe_args(const escha_moe_layer* L, const uint16_t* x, int T, floa
     }
     a.fz_wait_ns = g_fz_wait_ns.load();
     a.fz_skip_publish = g_fz_skip_publish.load();
+    a.mbar_limit_log2 = g_mbar_limit_log2.load();
+    a.skip_cluster_arrive = g_skip_cluster_arrive.load();
     return a;
 }
 
@@ -1032,6 +1036,16 @@ int escha_moe_blocks_path(const escha_moe_layer* const* layers, int n_blocks) {
 int escha_debug_set_moe_route(int mode) {
     if (mode < 0 || mode > 2) return fail(ESCHA_E_ARG, "debug_set_moe_route: mode=%d not in 0..2", mode);
     g_moe_route_mode.store(mode);
+    return ESCHA_OK;
+}
+
+int escha_debug_set_cluster_wait(int poll_limit_log2, int skip_arrive) {
+    if (poll_limit_log2 < 8 || poll_limit_log2 > 30)
+        return fail(ESCHA_E_ARG, "debug_set_cluster_wait: poll_limit_log2=%d not in [8, 30]", poll_limit_log2);
+    if (skip_arrive != 0 && skip_arrive != 1)
+        return fail(ESCHA_E_ARG, "debug_set_cluster_wait: skip_arrive=%d must be 0 or 1", skip_arrive);
+    g_mbar_limit_log2.store(poll_limit_log2);
+    g_skip_cluster_arrive.store(skip_arrive);
     return ESCHA_OK;
 }
 

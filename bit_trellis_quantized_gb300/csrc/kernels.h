@@ -148,6 +148,12 @@ struct MoeArgs {
     float* fz_dres;     // unused (the finishing CTA keeps the experts' outputs in shared memory)
     long long fz_wait_ns;   // a wait on another CTA gives up after this long
     int fz_skip_publish;    // test hook: the gate_up outputs are never published, so every wait on them gives up
+    // per-slot cluster reductions (gate_up, down): rank 0's mbarrier wait
+    // gives up after 2^mbar_limit_log2 polls; test hook skip_cluster_arrive:
+    // ranks != 0 write nothing into rank 0's shared memory and never arrive,
+    // so that wait runs out
+    int mbar_limit_log2;
+    int skip_cluster_arrive;
     // multi-layer per-slot launch: token t's layer, input and outputs (in the
     // workspace, written by the router kernel; null: one layer, x, out, ids
     // and w as above)

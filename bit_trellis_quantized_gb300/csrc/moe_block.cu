@@ -849,7 +849,7 @@ __device__ void gate_up_routed(const MoeArgs& a, float* smem) {
 
     cluster_wait();
     if (crank != 0) {
-        if (warp == 0) {
+        if (warp == 0 && !a.skip_cluster_arrive) {
             const uint32_t dst = cluster_map(smem_u32(slots + crank * 128 + 4 * lane), 0);
             st_cluster_v4(dst, *reinterpret_cast<const float4*>(zp + 4 * lane));
             mbar_arrive_cluster(cluster_map(smem_u32(&bar), 0));
@@ -857,7 +857,7 @@ __device__ void gate_up_routed(const MoeArgs& a, float* smem) {
         return;
     }
     if (warp == 0) {
-        if (csize > 1) mbar_wait_bounded(smem_u32(&bar), a.err, 1);
+        if (csize > 1) mbar_wait_bounded(smem_u32(&bar), a.err, 1, 1ll << a.mbar_limit_log2);
         float v[4] = {0.f, 0.f, 0.f, 0.f};
         for (int r = 0; r < csize; ++r) {
             const float4 z4 = *reinterpret_cast<const float4*>(slots + r * 128 + 4 * lane);
@@ -1042,7 +1042,7 @@ __global__ void __launch_bounds__(kDnThreads, MINB) moe_down_kernel(const MoeArg
             if (lane == 0) {
                 if (rank == 0) {
                     shres[sh_row] = sh_val;
-                } else {
+                } else if (!a.skip_cluster_arrive) {
                     const uint32_t dst = cluster_map(smem_u32(shres + sh_row), 0);
                     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst), "f"(sh_val) : "memory");
                 }
@@ -1054,7 +1054,7 @@ __global__ void __launch_bounds__(kDnThreads, MINB) moe_down_kernel(const MoeArg
 
     if (rank != 0) {
         __syncthreads();
-        if (warp == 0) {
+        if (warp == 0 && !a.skip_cluster_arrive) {
             asm volatile("fence.acq_rel.cluster;" ::: "memory");
             const uint32_t dst = cluster_map(smem_u32(slots + rank * 128 + 4 * lane), 0);
             st_cluster_v4(dst, *reinterpret_cast<const float4*>(zp + 4 * lane));
@@ -1063,7 +1063,7 @@ __global__ void __launch_bounds__(kDnThreads, MINB) moe_down_kernel(const MoeArg
         return;
     }
     if (csz > 1) {
-        if (warp == 0) mbar_wait_bounded(smem_u32(&bar), a.err, 2);
+        if (warp == 0) mbar_wait_bounded(smem_u32(&bar), a.err, 2, 1ll << a.mbar_limit_log2);
     }
     __syncthreads();
     if (warp < a.topk) {  // warp q finishes expert q: its splits in order, output transform, routing weight

@@ -534,10 +534,9 @@ __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.w
 
 // Waits for phase 0 of the mbarrier; gives up after `limit` polls (each poll
 // may suspend for a while inside try_wait) and sets *err.
-__device__ __forceinline__ void mbar_wait_bounded(uint32_t bar, int* err, int code) {
-    constexpr long long kLimit = 1ll << 24;
+__device__ __forceinline__ void mbar_wait_bounded(uint32_t bar, int* err, int code, long long limit = 1ll << 24) {
     for (long long it = 0; !mbar_try_wait(bar, 0); ++it) {
-        if (it > kLimit) {
+        if (it > limit) {
             if (err) atomicExch(err, code);
             break;
         }

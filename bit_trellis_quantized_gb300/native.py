@@ -66,6 +66,7 @@ EXPORTS = [
     "escha_debug_set_blocks_route",
     "escha_debug_set_moe_route",
     "escha_debug_set_fused_wait",
+    "escha_debug_set_cluster_wait",
     "escha_moe_route_workspace",
     "escha_moe_route",
     "escha_residual_rmsnorm",
@@ -202,6 +203,8 @@ def lib() -> ctypes.CDLL:
         L.escha_debug_set_moe_route.restype = _i
         L.escha_debug_set_fused_wait.argtypes = [ctypes.c_longlong, _i]
         L.escha_debug_set_fused_wait.restype = _i
+        L.escha_debug_set_cluster_wait.argtypes = [_i, _i]
+        L.escha_debug_set_cluster_wait.restype = _i
         L.escha_moe_route_workspace.argtypes = [ctypes.POINTER(EschaMoeLayer), _i]
         L.escha_moe_route_workspace.restype = _sz
         L.escha_moe_route.argtypes = [ctypes.POINTER(EschaMoeLayer), _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
@@ -235,6 +238,13 @@ def set_fused_wait(wait_ns: int = 2_000_000_000, skip_publish: bool = False) -> 
     """Diagnostic: the fused kernel's wait bound, and the test hook that keeps
     the routing unpublished so that every wait on it runs out."""
     check(lib().escha_debug_set_fused_wait(int(wait_ns), int(bool(skip_publish))))
+
+
+def set_cluster_wait(poll_limit_log2: int = 24, skip_arrive: bool = False) -> None:
+    """Diagnostic: the per-slot cluster reductions' wait bound (2^poll_limit_log2
+    polls), and the test hook that keeps ranks != 0 from storing or arriving
+    so that rank 0's wait runs out."""
+    check(lib().escha_debug_set_cluster_wait(int(poll_limit_log2), int(bool(skip_arrive))))
 
 
 class EschaError(RuntimeError):

@@ -422,7 +422,17 @@ int escha_moe_block_path(const escha_moe_layer* L, int T);
  *   (skip_publish = 1) that keeps every expert's gate_up outputs from being
  *   published, so every down unit's wait for them runs out: the kernel then
  *   ends with the status word set to 5 instead of hanging. Both settings are
- *   process-wide and read when a call is enqueued. */
+ *   process-wide and read when a call is enqueued.
+ * escha_debug_set_cluster_wait: the per-slot kernels' cluster reductions
+ *   (gate_up, down/combine), where ranks != 0 store their partial sums into
+ *   rank 0's shared memory and arrive on its mbarrier: rank 0's wait gives
+ *   up after 2^poll_limit_log2 polls (poll_limit_log2 in [8, 30], default
+ *   24), sets the status word (1: gate_up, 2: down) and goes on. For tests,
+ *   skip_arrive = 1 makes ranks != 0 write nothing into rank 0's shared
+ *   memory and never arrive, so every such wait runs out; the outputs are
+ *   then invalid and the status word says so. Process-wide, read when a call
+ *   is enqueued; ESCHA_E_ARG for values out of range. */
+int escha_debug_set_cluster_wait(int poll_limit_log2, int skip_arrive);
 int escha_debug_set_moe_route(int mode);
 int escha_debug_set_fused_wait(long long wait_ns, int skip_publish);
 

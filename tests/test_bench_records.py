@@ -1,6 +1,7 @@
 """The bench line's committed ncu figures (profiles/traffic.json): used only
 for the bench mode they were captured in, and only while the kernel sources
 they depend on are byte for byte those of the capture (CPU)."""
+import hashlib
 import json
 import os
 import shutil
@@ -13,13 +14,19 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def _copy_tree(tmp_path):
-    """profiles/ and the kernel sources named by the record, in a scratch root."""
+    """The record and the kernel sources it names, in a scratch root, the
+    record's hash taken over those sources (so it is current there whether
+    or not the committed one is)."""
     rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
-    shutil.copytree(os.path.join(ROOT, "profiles"), tmp_path / "profiles")
+    (tmp_path / "profiles").mkdir()
     csrc = tmp_path / "bit_trellis_quantized_gb300" / "csrc"
     csrc.mkdir(parents=True)
+    h = hashlib.sha256()
     for src in rec["sources"]:
         shutil.copy(os.path.join(ROOT, "bit_trellis_quantized_gb300", "csrc", src), csrc / src)
+        h.update((csrc / src).read_bytes())
+    rec["sources_sha256"] = h.hexdigest()
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
     return rec, csrc
 
 

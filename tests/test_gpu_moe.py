@@ -355,3 +355,44 @@ def test_moe_grouped_in_cuda_graph_matches_eager(native):
         g.replay()
         torch.cuda.synchronize()
         assert torch.equal(out, eager)
+
+
+@pytest.mark.parametrize("T", [1, 4])
+def test_cluster_reduction_wait_runs_out(native, T):
+    """Ranks != 0 of the per-slot cluster reductions kept from storing into
+    rank 0 and from arriving (a test hook), with a 2^10-poll bound: rank 0's
+    mbarrier waits run out, the status word reports it (1: gate_up, 2: down),
+    the call returns without hanging, and the next call with the default
+    settings is correct bit for bit."""
+    import time
+
+    block = native.MoeBlock(gen.moe_layer(1002), topk=8)
+    x = dev(gen.fp16_normal(gen.rng(2100 + T), (T, 2048)))
+    ref, ref_ids, _ = block(x)
+    torch.cuda.synchronize()
+    assert int(block.workspace(T)[:4].view(torch.int32).item()) == 0
+    native.set_cluster_wait(10, skip_arrive=True)
+    try:
+        t0 = time.time()
+        block(x)
+        torch.cuda.synchronize()
+        dt = time.time() - t0
+        status = int(block.workspace(T)[:4].view(torch.int32).item())
+    finally:
+        native.set_cluster_wait()
+    assert status in (1, 2), status
+    assert dt < 5.0
+    out, ids, _ = block(x)
+    torch.cuda.synchronize()
+    assert int(block.workspace(T)[:4].view(torch.int32).item()) == 0
+    assert torch.equal(ids, ref_ids)
+    assert torch.equal(out, ref)
+
+
+def test_cluster_wait_setting_rejects_bad_values(native):
+    with pytest.raises(native.EschaError) as ei:
+        native.set_cluster_wait(7)
+    assert ei.value.code == native.ESCHA_E_ARG
+    assert native.lib().escha_debug_set_cluster_wait(31, 0) == native.ESCHA_E_ARG
+    assert native.lib().escha_debug_set_cluster_wait(24, 2) == native.ESCHA_E_ARG
+    native.set_cluster_wait()
